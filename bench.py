@@ -1,0 +1,413 @@
+"""Benchmark: one decode step of paged attention on the 70B-GQA layer workload.
+
+A step is the decode hot path over one batch: KV append of the new token of
+all 256 sequences, then paged decode attention (split-K + log-sum-exp merge)
+over their histories (context lengths uniform in [1024, 8192], 64 query / 8
+KV heads, d_head 128, 16-token blocks, bf16 with 0.1% of K rows x100).
+
+Metric: KV GB/s (logical K+V bytes the decode reads, per second), with decode
+tokens/s and the fraction of the measured HBM peak.  Inputs (~4.8 GB of KV)
+are larger than L2, so no flush is needed between steps.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``
+prints one JSON line.  With N > 1 (torchrun, one rank per GPU) every rank runs
+its own replica of the workload (the path has no cross-GPU exchange) and the
+value is the total over ranks divided by the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import resource
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_52_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attn: KV GB/s & % of GB300 HBM peak; decode tokens/s at 70B-GQA"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa70b", choices=sorted(wl.DECODE_SPECS))
+    ap.add_argument("--partition-blocks", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-time budget of the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(w, spec, plan):
+    lens = w.meta["lens"]
+    return {
+        "workload": spec.name,
+        "num_seqs": w.num_seqs, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
+        "d_head": w.d_head, "block_size": wl.BLOCK_SIZE,
+        "context_len_min": min(lens), "context_len_max": max(lens),
+        "context_len_mean": round(sum(lens) / len(lens), 1),
+        "kv_bytes_per_step": w.kv_bytes(),
+        "partition_blocks": plan[0], "num_parts": plan[1],
+        "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush",
+        "step": "kv_append(1 token/seq) + paged_decode_attention (split-K + LSE merge)",
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (every 200 ms) while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _host_sequence(w, s):
+    """Host copy of what the oracle needs for sequence s of a device workload:
+    its physical blocks renumbered 0..n-1 (pages may sit anywhere), its new
+    token's slot in that numbering, q and the new K/V rows."""
+    nb = wl.blocks_for(int(w.meta["lens"][s]))
+    ids = w.block_tables[s, :nb].to(torch.int64)
+    kc = wl.bf16_bits(w.k_cache.index_select(0, ids))
+    vc = wl.bf16_bits(w.v_cache.index_select(0, ids))
+    slot = int(w.slot_mapping[s])
+    phys = ids.cpu().tolist()
+    local = phys.index(slot // wl.BLOCK_SIZE) * wl.BLOCK_SIZE + slot % wl.BLOCK_SIZE
+    return dict(kc=kc, vc=vc, table=[list(range(nb))], slot=[local], len=[w.meta["lens"][s]],
+                q=wl.bf16_bits(w.q[s:s + 1]), k_new=wl.bf16_bits(w.k_new[s:s + 1]),
+                v_new=wl.bf16_bits(w.v_new[s:s + 1]))
+
+
+def cpu_oracle_sample(w, budget_s: float):
+    """Time the CPU oracle, as it stands, on whole sequences of the workload
+    (append, then decode) until the wall-time budget is spent.  Returns the
+    same metric (KV GB/s) and a description; `cores` is CPU time / wall time
+    of the oracle calls, i.e. the threads it actually kept busy."""
+    import oracle  # CPU baseline only
+
+    row_bytes = 2 * w.kv_heads * w.d_head * 2
+    done_bytes, wall, cpu, nseq = 0, 0.0, 0.0, 0
+    s = 0
+    while wall < budget_s and s < w.num_seqs:
+        h = _host_sequence(w, s)
+        c0, t0 = time.process_time(), time.perf_counter()
+        kc, vc = oracle.kv_append(h["k_new"], h["v_new"], h["slot"], h["kc"], h["vc"])
+        oracle.paged_decode_attention(h["q"], kc, vc, h["table"], h["len"], w.scale)
+        wall += time.perf_counter() - t0
+        cpu += time.process_time() - c0
+        done_bytes += h["len"][0] * row_bytes
+        nseq += 1
+        s += 1
+    value = done_bytes / wall / 1e9 if wall > 0 else None
+    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    info = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "host_cpus": len(os.sched_getaffinity(0)),
+            "sample": f"append+decode of the first {nseq} of {w.num_seqs} sequences "
+                      f"({done_bytes / 1e9:.3f} GB of KV) in {wall:.1f} s, numpy float64"}
+    return value, info
+
+
+def read_traffic(kernel_tag: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken.  The summary holds a
+    line `traffic <tag> source_sha256=<hex> dram_bytes_per_launch=<int>`."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("paged_decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_52_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None, sha
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".txt", ".md")):
+            continue
+        with open(os.path.join(pdir, name)) as fh:
+            for ln in fh:
+                parts = ln.split()
+                if len(parts) >= 4 and parts[0] == "traffic" and parts[1] == kernel_tag:
+                    kv = dict(p.split("=", 1) for p in parts[2:] if "=" in p)
+                    if kv.get("source_sha256") == sha:
+                        return int(kv["dram_bytes_per_launch"]), sha
+    return None, sha
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from paged_kv_cache_52_gb300 import pagedkv
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    spec = wl.DECODE_SPECS[args.workload]
+    w = wl.make_decode_workload(spec, device=dev, gen_device=dev)
+    S, hq, hkv, d = w.num_seqs, w.q_heads, w.kv_heads, w.d_head
+    max_len = max(w.meta["lens"])
+    plan = pagedkv.decode_plan(S, hq, hkv, d, max_len, args.partition_blocks)
+    ws = pagedkv.decode_workspace(S, hq, hkv, d, max_len, dev, args.partition_blocks)
+    out = torch.empty(S, hq, d, dtype=torch.float32, device=dev)
+    kc, vc = w.k_cache, w.v_cache
+    kv_bytes = w.kv_bytes()
+
+    def append(k_new, v_new, slots):
+        pagedkv.kv_append(k_new, v_new, slots, kc, vc)
+
+    def decode(q, tables, lens):
+        pagedkv.paged_decode_attention(q, kc, vc, tables, lens, w.scale, out=out,
+                                       max_context_len=max_len, workspace=ws,
+                                       partition_blocks=args.partition_blocks)
+
+    for _ in range(max(3, args.warmup)):
+        append(w.k_new, w.v_new, w.slot_mapping)
+        decode(w.q, w.block_tables, w.context_lens)
+    torch.cuda.synchronize()
+    err = pagedkv.get_device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x}: {pagedkv.describe_device_error(err)}")
+
+    K = args.steps
+    E = torch.cuda.Event
+    start, end = E(enable_timing=True), E(enable_timing=True)
+    marks = [(E(enable_timing=True), E(enable_timing=True), E(enable_timing=True))
+             for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record()
+        for a, b, c in marks:
+            a.record()
+            append(w.k_new, w.v_new, w.slot_mapping)
+            b.record()
+            decode(w.q, w.block_tables, w.context_lens)
+            c.record()
+        end.record()
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    decode_ms = sum(b.elapsed_time(c) for _, b, c in marks) / K
+    append_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / K
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * kv_bytes * K / (total_ms / 1e3) / 1e9
+
+    # End to end through the public API: this step's inputs from pinned host
+    # memory, the step, and the output read back, every step.
+    host = {n: getattr(w, n).cpu().pin_memory() for n in
+            ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    devb = {n: torch.empty_like(getattr(w, n)) for n in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            devb[n].copy_(t, non_blocking=True)
+        append(devb["k_new"], devb["v_new"], devb["slot_mapping"])
+        decode(devb["q"], devb["block_tables"], devb["context_lens"])
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s2, e2 = E(enable_timing=True), E(enable_timing=True)
+    s2.record()
+    for _ in range(K):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * kv_bytes * K / (e2e_ms / 1e3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    achieved = kv_bytes / (decode_ms / 1e3) / 1e9
+    traffic, _ = read_traffic(args.workload)
+    launches_per_step = 2 + (1 if plan[1] > 1 else 0)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded randn bf16 K/V/q, random block tables (no dataset)",
+        "config": workload_config(w, spec, plan),
+        "decode_tokens_per_s": round(world * S * K / (total_ms / 1e3), 1),
+        "decode_ms": round(decode_ms, 4), "append_ms": round(append_ms, 4),
+        "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"kernel": "paged_decode (split-K kernel + LSE merge, one call)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (copy GB/s)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kv_bytes},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 4)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        _, info = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = info
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle on the host cores, on the same metric: each step is the
+    append + decode of a bounded sample of the workload's sequences."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # the reference arm of this benchmark is the CPU oracle
+
+    spec = wl.DECODE_SPECS[args.workload]
+    if spec.lens is not None:
+        all_lens = list(spec.lens)
+    else:
+        lo, hi = spec.len_range
+        g = torch.Generator().manual_seed(1000 * spec.config_id + 5)
+        all_lens = torch.randint(lo, hi + 1, (spec.num_seqs,), generator=g).tolist()
+    per_step = 4 if max(all_lens) <= 16384 else 1
+    sample = all_lens[:per_step]
+    w = wl.make_decode_workload(spec, lens_override=sample)
+    kc0, vc0 = wl.bf16_bits(w.k_cache), wl.bf16_bits(w.v_cache)
+    kn, vn = wl.bf16_bits(w.k_new), wl.bf16_bits(w.v_new)
+    q = wl.bf16_bits(w.q)
+    slots = w.slot_mapping.numpy()
+    tables = w.block_tables.numpy()
+    kv_bytes = w.kv_bytes()
+
+    def step():
+        kc, vc = oracle.kv_append(kn, vn, slots, kc0, vc0)
+        oracle.paged_decode_attention(q, kc, vc, tables, sample, w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    c0, t0 = time.process_time(), time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    value = kv_bytes * args.steps / wall / 1e9
+    cores = max(1, round(cpu / wall))
+    desc = (f"oracle append+decode of {per_step} of {spec.num_seqs} sequences per step "
+            f"(context lens {sample}), numpy float64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded randn bf16 K/V/q, random block tables (no dataset)",
+        "config": {"workload": spec.name, "sample_seqs": per_step, "sample_context_lens": sample,
+                   "kv_bytes_per_step": kv_bytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "host_cpus": len(os.sched_getaffinity(0)),
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * The library holds no tensors.  Every buffer is owned by the caller and is
+ * a DEVICE pointer unless stated otherwise; every call is asynchronous on
+ * the stream it is given (a cudaStream_t passed as `pkv_stream_t`; NULL is
+ * the legacy default stream).  A return value of PKV_OK means the work was
+ * validated and launched; a fault inside a kernel surfaces at the caller's
+ * next synchronisation, and index checks done on the device are reported
+ * through pkv_get_device_error().  No call allocates device memory except
+ * where stated.
+ *
+ * Data layout (nano-vLLM page "Maitriser les mecanismes cles de l'inference
+ * des grands modeles avec nano-vLLM", section "Implementation du cache":
+ * one layer's pool is torch.empty(2, num_blocks, block_size, kv_heads,
+ * d_head)):
+ *   k_cache, v_cache : [num_blocks][block_size][kv_heads][d_head] bf16,
+ *                      contiguous, 16-byte aligned.  One slot (a token row)
+ *                      is kv_heads * d_head contiguous elements.
+ *   block_tables     : [num_seqs][max_blocks_per_seq] int32, row-major;
+ *                      entry j of row s is the physical block holding logical
+ *                      positions [16 j, 16 j + 16) of sequence s ("Cache KV,
+ *                      attention et optimisation de l'inference", section
+ *                      "PagedAttention KV cache comme memoire virtuelle").
+ *   context_lens     : [num_seqs] int32, the number of tokens of each
+ *                      sequence INCLUDING the ones appended in this step (the
+ *                      cache is updated first and the new token attends to
+ *                      itself: "Optimisation de l'inference", "Etape 1/2").
+ *
+ * Supported shapes: block_size 16; d_head 64 or 128; q_heads a multiple of
+ * kv_heads with a group q_heads / kv_heads of 1, 2, 4, 8 or 16.  Anything
+ * else returns PKV_EUNSUPPORTED without launching.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,        /* null pointer, negative size, misaligned buffer or stride */
+  PKV_EUNSUPPORTED = -2,  /* shape outside the supported set listed above */
+  PKV_ECUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
+  PKV_ENOMEM = -4,        /* the workspace passed is smaller than required */
+  PKV_EDEVICE_CHECK = -5, /* reserved: a device-side index check failed */
+  PKV_ETIMEOUT = -6       /* reserved: a bounded device wait ran out */
+} pkv_status;
+
+/* Shape of one layer's K (and V) pool: [num_blocks][block_size][kv_heads][d_head]. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t kv_heads;
+  int32_t d_head;
+} pkv_cache_desc;
+
+/* A cudaStream_t. */
+typedef void* pkv_stream_t;
+
+/* Bits of the device error word returned by pkv_get_device_error(). */
+#define PKV_DEVERR_BAD_SLOT 0x1u        /* slot outside [-1, num_blocks*16): token skipped */
+#define PKV_DEVERR_BAD_BLOCK_ID 0x2u    /* block id outside the pool: its rows read as 0 */
+#define PKV_DEVERR_BAD_CONTEXT 0x4u     /* context_len < 0 or > 16*max_blocks_per_seq: clamped */
+#define PKV_DEVERR_WAIT_TIMEOUT 0x8u    /* a bounded wait on an mbarrier ran out */
+#define PKV_DEVERR_BAD_QUERY_RANGE 0x10u /* q_start not monotone or chunk longer than context */
+#define PKV_DEVERR_TMEM_ALLOC 0x20u     /* tensor memory could not be allocated */
+
+/*
+ * pkv_kv_append -- scatter new K/V rows into the paged pools.
+ *
+ * Passage: nano-vLLM page, section "Ecriture dans le cache" (the store
+ * kernel): for each new token t, slot = slot_mapping[t]; slot == -1 skips the
+ * token; otherwise the token's kv_heads*d_head K elements are copied to row
+ * `slot` of k_cache (block slot / 16, offset slot % 16) and likewise for V.
+ * The copy is a bit copy.
+ *
+ *   k, v          : [num_tokens][kv_heads][d_head] bf16 rows; row t starts at
+ *                   element t * k_tok_stride (resp. v_tok_stride), so views of
+ *                   a fused QKV projection are accepted.  Base pointers and
+ *                   strides must be 16-byte aligned (strides are in elements).
+ *   slot_mapping  : [num_tokens] int64.  Two tokens with the same slot race
+ *                   (the result is one of them).
+ *   k_cache, v_cache : pools described by `cache`, written in place.
+ * Slots outside [-1, num_blocks*16) are skipped and set
+ * PKV_DEVERR_BAD_SLOT.  num_tokens == 0 launches nothing.
+ */
+PKV_API int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_tok_stride,
+                  const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                  void* v_cache, pkv_cache_desc cache, pkv_stream_t stream);
+
+/*
+ * Decode plan: the partition size (in 16-token blocks) and the number of
+ * partitions the split-K decode uses for these sizes, and the workspace it
+ * needs.  partition_blocks <= 0 lets the library choose from the longest
+ * context and the device's SM count; a positive value (1..1024) forces it.
+ * The plan depends on the current device.  Returns PKV_OK or PKV_EINVAL /
+ * PKV_EUNSUPPORTED.
+ */
+PKV_API int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
+                    int partition_blocks, int* out_partition_blocks, int* out_num_parts,
+                    size_t* out_workspace_bytes);
+
+/* Workspace bytes pkv_paged_decode_attention needs (0 when one partition suffices). */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,
+                                  int max_context_len);
+
+/*
+ * pkv_paged_decode_attention -- one query token per sequence attends over
+ * its paged history (memory-bound decode step).
+ *
+ * Passages: "Optimisation de l'inference", section "Etape 2: Attention avec
+ * KV Cache" (softmax(q K^T * scale) V, single query, no mask); "Cache KV,
+ * attention et optimisation de l'inference", section "Etape 2: softmax en
+ * carreaux" (online softmax: running max and sum, rescaled accumulator);
+ * "第 10 讲：推理（Inference）", "核心概念与定义" (GQA: a group of query heads
+ * shares one KV head; FlashDecoding named as the long-context method).
+ *
+ *   q            : [num_seqs][q_heads][d_head] bf16, contiguous.
+ *   block_tables : [num_seqs][max_blocks_per_seq] int32.
+ *   context_lens : [num_seqs] int32 (include this step's appended token).
+ *   max_context_len : host-side bound on context_lens (>= every entry),
+ *                  used to plan the split and size the workspace.  Tokens of
+ *                  a longer sequence beyond the planned partitions are not
+ *                  attended and PKV_DEVERR_BAD_CONTEXT is set.
+ *   scale        : softmax scale, e.g. 1/sqrt(d_head).
+ *   out          : [num_seqs][q_heads][d_head] float32 (not normalised to bf16).
+ *   workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
+ *                  bytes, or NULL when that is 0; contents need no
+ *                  initialisation and are overwritten.  Calls that share a
+ *                  workspace must be ordered on the GPU.
+ * Query head h uses KV head h / (q_heads / kv_heads).  A sequence with
+ * context_len 0 yields zeros.  Block ids outside the pool read as zero rows
+ * and set PKV_DEVERR_BAD_BLOCK_ID; context_len beyond 16*max_blocks_per_seq
+ * is clamped and sets PKV_DEVERR_BAD_CONTEXT.  Returns PKV_ENOMEM if
+ * ws_bytes is too small.
+ */
+PKV_API int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                               const void* v_cache, pkv_cache_desc cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float scale,
+                               float* out, void* workspace, size_t ws_bytes,
+                               pkv_stream_t stream);
+
+/* Same as pkv_paged_decode_attention with an explicit partition size
+ * (partition_blocks as in pkv_decode_plan; <= 0 = library choice). */
+PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                                  const void* v_cache, pkv_cache_desc cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int max_context_len, float scale,
+                                  float* out, void* workspace, size_t ws_bytes,
+                                  int partition_blocks, pkv_stream_t stream);
+
+/*
+ * Read the device error word of the current device (an OR of the
+ * PKV_DEVERR_* bits raised by kernels since the last clear).  Synchronises
+ * the device.  clear != 0 resets the word to 0.  Returns PKV_OK or PKV_ECUDA.
+ */
+PKV_API int pkv_get_device_error(unsigned int* word, int clear);
+
+/* Human-readable name of a pkv_status value (static string). */
+PKV_API const char* pkv_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+PKV_API int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,86 @@
+// KV append: scatter new K/V token rows into the paged pools through the
+// per-token slot mapping (nano-vLLM page, section "Ecriture dans le cache":
+// slot -1 skips the token, otherwise the row lands in block slot / 16 at
+// offset slot % 16).
+//
+// One warp copies one token row of K and of V with 16-byte vector loads and
+// stores; the grid strides over tokens.  Pure HBM copy: 2 * row bytes read and
+// 2 * row bytes written per token.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static __device__ unsigned g_append_error = 0;
+
+constexpr int kAppendThreads = 256;
+constexpr int kAppendVecPerLane = 4;  // 16-byte vectors kept in flight per lane per row
+
+__global__ void __launch_bounds__(kAppendThreads)
+kv_append_kernel(const uint4* __restrict__ k, int64_t k_stride_vec, const uint4* __restrict__ v,
+                 int64_t v_stride_vec, const int64_t* __restrict__ slot_mapping,
+                 int64_t num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                 int64_t num_slots, int row_vec) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kAppendThreads) >> 5;
+  for (int64_t t = warp; t < num_tokens; t += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot == -1) continue;
+    if (slot < -1 || slot >= num_slots) {
+      if (lane == 0) atomicOr(&g_append_error, kErrBadSlot);
+      continue;
+    }
+    const uint4* ks = k + t * k_stride_vec;
+    const uint4* vs = v + t * v_stride_vec;
+    uint4* kd = k_cache + slot * row_vec;
+    uint4* vd = v_cache + slot * row_vec;
+    for (int base = 0; base < row_vec; base += 32 * kAppendVecPerLane) {
+      uint4 kr[kAppendVecPerLane], vr[kAppendVecPerLane];
+#pragma unroll
+      for (int u = 0; u < kAppendVecPerLane; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < row_vec) {
+          kr[u] = __ldg(ks + i);
+          vr[u] = __ldg(vs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kAppendVecPerLane; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < row_vec) {
+          kd[i] = kr[u];
+          vd[i] = vr[u];
+        }
+      }
+    }
+  }
+}
+
+unsigned read_append_error(bool clear) {
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_append_error, sizeof(word)) != cudaSuccess) return ~0u;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_append_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  }
+  return word;
+}
+
+cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                             const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                             void* v_cache, int64_t num_slots, int row_elems,
+                             cudaStream_t stream, int num_sms) {
+  const int row_vec = row_elems / 8;  // 8 bf16 per 16-byte vector
+  const int64_t warps_needed = num_tokens;
+  const int64_t blocks_needed = (warps_needed * 32 + kAppendThreads - 1) / kAppendThreads;
+  const int64_t max_blocks = int64_t(num_sms) * 8;
+  const int grid = int(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+  kv_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
+      static_cast<const uint4*>(k), k_stride / 8, static_cast<const uint4*>(v), v_stride / 8,
+      slot_mapping, num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      num_slots, row_vec);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

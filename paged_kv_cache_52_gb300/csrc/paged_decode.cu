@@ -1,0 +1,488 @@
+// Paged decode attention with split-K (flash-decoding) and a log-sum-exp
+// merge.
+//
+// What is computed ("Optimisation de l'inference", section "Etape 2:
+// Attention avec KV Cache"; "Cache KV, attention et optimisation de
+// l'inference", section "Etape 2: softmax en carreaux"): for every sequence s
+// and query head h, out = softmax(q[s,h] . K_s^T * scale) V_s over the
+// sequence's context_len tokens, whose K/V rows are gathered through the block
+// table (16-token pages).  Query head h reads KV head h / G (G = group size,
+// the GQA sharing of "第 10 讲：推理（Inference）").
+//
+// Design (GB300):
+//  * one CTA per (sequence x KV head, partition) -- grid (S*Hkv, parts); the partition is a run of
+//    `partition_blocks` 16-token blocks.  All G query heads of the group live
+//    in the CTA, so every K/V byte is read from HBM once.
+//  * each warp owns a ring of STAGES shared-memory stages and streams its own
+//    blocks (round-robin over the partition) with TMA: one 4-D tensor-map load
+//    per 64-column half of a block's K (and V), 128-byte swizzled, completing
+//    on a per-stage mbarrier.  The block ids of the partition are staged in
+//    shared memory once, so no id load sits on the issue path.
+//  * QK^T and PV run on the tensor cores as warp-level m16n8k16 bf16 MMAs with
+//    fp32 accumulators: the G heads are the M rows (padded to 16), 16 tokens
+//    are the N (QK^T) or K (PV) extent.  At G = 8 this contraction is 8 flop
+//    per KV byte, which would keep the fp32 pipe ~70% busy at HBM speed; on
+//    the tensor pipe it costs a few percent of its rate.
+//  * online softmax in the log2 domain (scores pre-multiplied by
+//    scale * log2 e, MUFU ex2); row max/sum are quad shuffles.  P enters the
+//    PV MMA as bf16 hi + bf16 lo (two MMAs), which keeps P's rounding error
+//    at ~2^-16 relative instead of bf16's 2^-9.
+//  * warps merge in shared memory; a single-partition sequence writes the
+//    final output, otherwise the CTA writes its normalised partial output and
+//    its log2-sum-exp, and a small merge kernel combines the partitions.
+//  * every mbarrier wait is bounded; a timeout sets an error bit, drains the
+//    warp's outstanding copies (also bounded) and lets the CTA finish.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static __device__ unsigned g_decode_error = 0;
+
+constexpr int kBlockTokens = 16;
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 3;
+constexpr int kMaxPartitionBlocks = 1024;
+
+int decode_warps_per_cta() { return kDecodeWarps; }
+
+template <int D>
+struct DecodeTile {
+  static constexpr int kHalfBytes = kBlockTokens * 128;       // 16 rows x 64 bf16
+  static constexpr int kTileBytes = kBlockTokens * D * 2;     // one block, one head
+  static constexpr int kStageBytes = 2 * kTileBytes;          // K + V
+  static constexpr int kRingBytes = kDecodeStages * kStageBytes;
+  static constexpr int kRingsBytes = kDecodeWarps * kRingBytes;
+  static constexpr int kBarOffset = kRingsBytes;
+  static constexpr int kIdsOffset = kBarOffset + kDecodeWarps * kDecodeStages * 8;
+  static constexpr int kSmemBytes = kIdsOffset + kMaxPartitionBlocks * 4 + 1024;  // +align slack
+};
+
+// Blocks of a sequence the kernels attend over, after clamping to what the
+// block table and the plan cover.  Both kernels use this so they agree.
+__device__ __forceinline__ int effective_blocks(int len, int max_blocks_per_seq, int num_parts,
+                                                int partition_blocks, bool* bad) {
+  *bad = false;
+  if (len < 0) {
+    len = 0;
+    *bad = true;
+  }
+  int nblk = (len + kBlockTokens - 1) / kBlockTokens;
+  if (nblk > max_blocks_per_seq) {
+    nblk = max_blocks_per_seq;
+    *bad = true;
+  }
+  const int covered = num_parts * partition_blocks;
+  if (nblk > covered) {
+    nblk = covered;
+    *bad = true;
+  }
+  return nblk;
+}
+
+__device__ __forceinline__ int effective_len(int len, int nblk) {
+  len = len < 0 ? 0 : len;
+  return len < nblk * kBlockTokens ? len : nblk * kBlockTokens;
+}
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* out;
+  float* part_o;
+  float* part_lse;
+  int q_heads, kv_heads, num_blocks, max_blocks_per_seq, partition_blocks, num_parts;
+  float scale_log2;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using T = DecodeTile<D>;
+  constexpr bool kTwoRows = (G > 8);  // heads gid+8 are real rows too
+  constexpr int KSTEPS = D / 16;       // k-steps of QK^T
+  constexpr int NT = D / 8;            // n-tiles of the output
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + T::kIdsOffset);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int pair = blockIdx.x;
+  const int part = blockIdx.y;
+  const int seq = pair / p.kv_heads;
+  const int kvh = pair - seq * p.kv_heads;
+
+  bool bad_ctx;
+  const int raw_len = __ldg(p.context_lens + seq);
+  const int nblk = effective_blocks(raw_len, p.max_blocks_per_seq, p.num_parts,
+                                    p.partition_blocks, &bad_ctx);
+  const int len = effective_len(raw_len, nblk);
+  if (bad_ctx && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
+  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
+  if (part >= nparts_s) return;
+  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
+  if (nblk == 0) {  // empty context: zeros
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
+    return;
+  }
+  const int b0 = part * p.partition_blocks;
+  const int nb_local = min(nblk - b0, p.partition_blocks);
+
+  // Stage this partition's block ids; ids outside the pool are flagged (their
+  // TMA boxes are out of bounds and read as zeros).
+  const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq + b0;
+  for (int i = threadIdx.x; i < nb_local; i += blockDim.x) {
+    const int32_t id = __ldg(table + i);
+    if (id < 0 || id >= p.num_blocks) atomicOr(&g_decode_error, kErrBadBlockId);
+    ids[i] = id;
+  }
+  const uint32_t ring = smem_u32(smem + warp * T::kRingBytes);
+  const uint32_t bars = smem_u32(smem + T::kBarOffset) + warp * kDecodeStages * 8;
+  if (lane == 0) {
+    for (int st = 0; st < kDecodeStages; ++st) mbar_init(bars + st * 8, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+
+  // Q fragments (A operand, rows = heads of the group, zero beyond G).
+  uint32_t qa[KSTEPS][2];
+  uint32_t qb[kTwoRows ? KSTEPS : 1][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (row0 + gid) * D);
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      const bool ok = gid < G;
+      qa[kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
+      qa[kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
+      if constexpr (kTwoRows) {
+        const uint32_t* qrow8 = qrow + 8 * D / 2;
+        qb[kk][0] = __ldg(qrow8 + (kk * 16 + tig * 2) / 2);
+        qb[kk][1] = __ldg(qrow8 + (kk * 16 + 8 + tig * 2) / 2);
+      }
+    }
+  }
+  __syncthreads();  // ids staged, barriers initialised
+
+  const int cnt = warp < nb_local ? (nb_local - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  auto issue = [&](int i) {
+    const int st = i % kDecodeStages;
+    const uint32_t bar = bars + st * 8;
+    const uint32_t kdst = ring + st * T::kStageBytes;
+    const uint32_t vdst = kdst + T::kTileBytes;
+    const int bid = ids[warp + i * kDecodeWarps];
+    mbar_arrive_expect_tx(bar, T::kStageBytes);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_4d(kdst + h * T::kHalfBytes, &tmap_k, bar, h * 64, kvh, 0, bid);
+      tma_load_4d(vdst + h * T::kHalfBytes, &tmap_v, bar, h * 64, kvh, 0, bid);
+    }
+  };
+  int issued = 0;
+  if (lane == 0) {
+    for (int i = 0; i < cnt && i < kDecodeStages; ++i) issue(i);
+  }
+  issued = cnt < kDecodeStages ? cnt : kDecodeStages;
+
+  // Per-lane ldmatrix geometry.
+  const int mi = lane >> 3, mr = lane & 7;
+  const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (tok 0-7|8-15) x (chunk even|odd)
+  const int v_tok = (mi & 1) * 8 + mr;   // V (trans): matrices (tok 0-7|8-15) x (chunk even|odd)
+
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  bool failed = false;
+  int i = 0;
+  for (; i < cnt; ++i) {
+    const int st = i % kDecodeStages;
+    const uint32_t par = (i / kDecodeStages) & 1;
+    const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(bars + st * 8, par));
+    if (!ready) {
+      failed = true;
+      break;
+    }
+    const uint32_t kbase = ring + st * T::kStageBytes;
+    const uint32_t vbase = kbase + T::kTileBytes;
+    const int tok0 = (b0 + warp + i * kDecodeWarps) * kBlockTokens;
+
+    // S = Q K^T for 16 tokens (two n-tiles of 8).
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      const int chunk = 2 * kk + (mi & 1);
+      const uint32_t addr = kbase + (chunk >> 3) * T::kHalfBytes + k_tok * 128 +
+                            (((chunk & 7) ^ (k_tok & 7)) << 4);
+      uint32_t b0r, b1r, b2r, b3r;
+      ldsm_x4(addr, b0r, b1r, b2r, b3r);
+      uint32_t a1 = 0u, a3 = 0u;
+      if constexpr (kTwoRows) {
+        a1 = qb[kk][0];
+        a3 = qb[kk][1];
+      }
+      mma_bf16_16816(s[0], qa[kk][0], a1, qa[kk][1], a3, b0r, b1r);
+      mma_bf16_16816(s[1], qa[kk][0], a1, qa[kk][1], a3, b2r, b3r);
+    }
+
+    // Online softmax in the log2 domain; mask tokens at or past the length.
+    float x[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * p.scale_log2;
+    if (tok0 + kBlockTokens > len) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (tok0 + nt * 8 + tig * 2 + (e & 1) >= len) x[nt][e] = -INFINITY;
+    }
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    const float mn0 = fmaxf(m0, mx0);
+    const float alpha0 = ex2(m0 - mn0);
+    m0 = mn0;
+    float pr[2][4];
+    pr[0][0] = ex2(x[0][0] - mn0);
+    pr[0][1] = ex2(x[0][1] - mn0);
+    pr[1][0] = ex2(x[1][0] - mn0);
+    pr[1][1] = ex2(x[1][1] - mn0);
+    l0 = l0 * alpha0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    float alpha1 = 1.f;
+    if constexpr (kTwoRows) {
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn1 = fmaxf(m1, mx1);
+      alpha1 = ex2(m1 - mn1);
+      m1 = mn1;
+      pr[0][2] = ex2(x[0][2] - mn1);
+      pr[0][3] = ex2(x[0][3] - mn1);
+      pr[1][2] = ex2(x[1][2] - mn1);
+      pr[1][3] = ex2(x[1][3] - mn1);
+      l1 = l1 * alpha1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    } else {
+      pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= alpha0;
+      o[n][1] *= alpha0;
+      if constexpr (kTwoRows) {
+        o[n][2] *= alpha1;
+        o[n][3] *= alpha1;
+      }
+    }
+
+    // P as the A operand (rows = heads, k = 16 tokens), split into bf16 hi + lo.
+    uint32_t ph[4], pl[4];
+    ph[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    ph[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    ph[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    ph[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    pl[0] = pack_bf16x2(pr[0][0] - bf16_lo_to_f32(ph[0]), pr[0][1] - bf16_hi_to_f32(ph[0]));
+    pl[1] = pack_bf16x2(pr[0][2] - bf16_lo_to_f32(ph[1]), pr[0][3] - bf16_hi_to_f32(ph[1]));
+    pl[2] = pack_bf16x2(pr[1][0] - bf16_lo_to_f32(ph[2]), pr[1][1] - bf16_hi_to_f32(ph[2]));
+    pl[3] = pack_bf16x2(pr[1][2] - bf16_lo_to_f32(ph[3]), pr[1][3] - bf16_hi_to_f32(ph[3]));
+
+    // O += P V: V tiles through ldmatrix.trans (B operand, k = tokens, n = dims).
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn) {
+      const int chunk = 2 * dn + (mi >> 1);
+      const uint32_t addr = vbase + (chunk >> 3) * T::kHalfBytes + v_tok * 128 +
+                            (((chunk & 7) ^ (v_tok & 7)) << 4);
+      uint32_t b0r, b1r, b2r, b3r;
+      ldsm_x4_trans(addr, b0r, b1r, b2r, b3r);
+      mma_bf16_16816(o[2 * dn], ph[0], ph[1], ph[2], ph[3], b0r, b1r);
+      mma_bf16_16816(o[2 * dn], pl[0], pl[1], pl[2], pl[3], b0r, b1r);
+      mma_bf16_16816(o[2 * dn + 1], ph[0], ph[1], ph[2], ph[3], b2r, b3r);
+      mma_bf16_16816(o[2 * dn + 1], pl[0], pl[1], pl[2], pl[3], b2r, b3r);
+    }
+
+    __syncwarp();  // every lane is done reading this stage
+    if (i + kDecodeStages < cnt) {
+      if (lane == 0) issue(i + kDecodeStages);
+      ++issued;
+    }
+  }
+
+  if (failed) {
+    // Record the timeout and wait (bounded) for this warp's copies still in
+    // flight, so no TMA writes into shared memory after the CTA exits.
+    if (lane == 0) {
+      atomicOr(&g_decode_error, kErrWaitTimeout);
+      for (int k = i; k < issued; ++k)
+        (void)mbar_wait_bounded(bars + (k % kDecodeStages) * 8, (k / kDecodeStages) & 1);
+    }
+    __syncwarp();
+  }
+
+  // Row sums were kept per lane: reduce over the quad.
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  if constexpr (kTwoRows) {
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  }
+
+  // Cross-warp merge through shared memory (each warp reuses its own ring).
+  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);  // [G][D]
+  float* mml = mo + G * D;                                            // m[G], l[G]
+  if (gid < G) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      mo[gid * D + n * 8 + tig * 2] = o[n][0];
+      mo[gid * D + n * 8 + tig * 2 + 1] = o[n][1];
+    }
+    if (tig == 0) {
+      mml[gid] = m0;
+      mml[G + gid] = l0;
+    }
+  }
+  if constexpr (kTwoRows) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      mo[(gid + 8) * D + n * 8 + tig * 2] = o[n][2];
+      mo[(gid + 8) * D + n * 8 + tig * 2 + 1] = o[n][3];
+    }
+    if (tig == 0) {
+      mml[gid + 8] = m1;
+      mml[G + gid + 8] = l1;
+    }
+  }
+  __syncthreads();
+
+  const bool final_out = (nparts_s == 1);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int row = idx / D, col = idx - row * D;
+    float big = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float* wm = reinterpret_cast<const float*>(smem + w * T::kRingBytes) + G * D;
+      big = fmaxf(big, wm[row]);
+    }
+    float tot = 0.f, val = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float* wo = reinterpret_cast<const float*>(smem + w * T::kRingBytes);
+      const float wgt = ex2(wo[G * D + row] - big);
+      tot += wo[G * D + G + row] * wgt;
+      val += wo[row * D + col] * wgt;
+    }
+    const float res = val / tot;
+    if (final_out) {
+      p.out[(row0 + row) * D + col] = res;
+    } else {
+      const size_t prow = (row0 + row) * p.num_parts + part;
+      p.part_o[prow * D + col] = res;
+      if (col == 0) p.part_lse[prow] = big + __log2f(tot);
+    }
+  }
+}
+
+// Log-sum-exp merge of the partitions of one (sequence, query head): with
+// lse_p the log2-sum-exp of partition p and o_p its normalised output,
+// out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p.
+template <int D>
+__global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParams p) {
+  const size_t row = blockIdx.x;  // seq * q_heads + head
+  const int seq = int(row / p.q_heads);
+  bool bad;
+  const int nblk = effective_blocks(__ldg(p.context_lens + seq), p.max_blocks_per_seq,
+                                    p.num_parts, p.partition_blocks, &bad);
+  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
+  if (nparts_s == 1) return;  // written by the split kernel
+  const float* lse = p.part_lse + row * p.num_parts;
+  const float* po = p.part_o + row * p.num_parts * D + threadIdx.x;
+  float big = -INFINITY;
+  for (int q = 0; q < nparts_s; ++q) big = fmaxf(big, __ldg(lse + q));
+  float tot = 0.f, val = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < nparts_s; ++q) {
+    const float w = ex2(__ldg(lse + q) - big);
+    tot += w;
+    val += w * __ldg(po + size_t(q) * D);
+  }
+  p.out[row * D + threadIdx.x] = val / tot;
+}
+
+template <int D, int G>
+static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
+                                   const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                   cudaStream_t stream) {
+  using T = DecodeTile<D>;
+  static bool attr_set = false;  // per instantiation; idempotent if raced
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_split_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
+  paged_decode_split_kernel<D, G><<<grid, kDecodeWarps * 32, T::kSmemBytes, stream>>>(
+      *tmap_k, *tmap_v, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || prm.num_parts == 1) return e;
+  paged_decode_merge_kernel<D><<<num_seqs * prm.q_heads, D, 0, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_decode_d(const DecodeParams& prm, int num_seqs, int group,
+                                   const CUtensorMap* tk, const CUtensorMap* tv,
+                                   cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_decode_t<D, 1>(prm, num_seqs, tk, tv, st);
+    case 2: return launch_decode_t<D, 2>(prm, num_seqs, tk, tv, st);
+    case 4: return launch_decode_t<D, 4>(prm, num_seqs, tk, tv, st);
+    case 8: return launch_decode_t<D, 8>(prm, num_seqs, tk, tv, st);
+    case 16: return launch_decode_t<D, 16>(prm, num_seqs, tk, tv, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                const CUtensorMap* tmap_v, cudaStream_t stream) {
+  DecodeParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.out = a.out;
+  prm.part_o = a.part_o;
+  prm.part_lse = a.part_lse;
+  prm.q_heads = a.q_heads;
+  prm.kv_heads = a.kv_heads;
+  prm.num_blocks = a.num_blocks;
+  prm.max_blocks_per_seq = a.max_blocks_per_seq;
+  prm.partition_blocks = a.partition_blocks;
+  prm.num_parts = a.num_parts;
+  prm.scale_log2 = a.scale_log2;
+  const int group = a.q_heads / a.kv_heads;
+  if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
+  if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
+  return cudaErrorInvalidValue;
+}
+
+int decode_max_partition_blocks() { return kMaxPartitionBlocks; }
+
+unsigned read_decode_error(bool clear) {
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_decode_error, sizeof(word)) != cudaSuccess) return ~0u;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  }
+  return word;
+}
+
+}  // namespace pkv

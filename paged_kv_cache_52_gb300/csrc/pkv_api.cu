@@ -1,0 +1,268 @@
+// C ABI of the paged-KV attention library: argument validation, launch
+// planning (split-K partition choice, workspace layout), TMA descriptor
+// encoding and error reporting.  All compute runs in the kernels of the other
+// translation units; nothing here touches tensor data.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+constexpr int kBlockSize = 16;
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int current_device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D view of a pool [num_blocks][16][kv_heads][d_head] bf16, innermost first:
+// (d_head, kv_heads, 16, num_blocks).  One box is 64 columns x 1 head x 16
+// tokens x 1 block, 128-byte swizzled in shared memory.
+bool encode_pool_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(c.d_head), cuuint64_t(c.kv_heads),
+                              cuuint64_t(c.block_size), cuuint64_t(c.num_blocks)};
+  const cuuint64_t row = cuuint64_t(c.d_head) * 2;
+  const cuuint64_t strides[3] = {row, row * cuuint64_t(c.kv_heads),
+                                 row * cuuint64_t(c.kv_heads) * cuuint64_t(c.block_size)};
+  const cuuint32_t box[4] = {64, 1, cuuint32_t(c.block_size), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache_desc(const pkv_cache_desc& c) {
+  if (c.num_blocks <= 0 || c.kv_heads <= 0 || c.d_head <= 0 || c.block_size <= 0)
+    return PKV_EINVAL;
+  if (c.block_size != kBlockSize) return PKV_EUNSUPPORTED;
+  return PKV_OK;
+}
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+struct Plan {
+  int partition_blocks = 1;
+  int num_parts = 1;
+  size_t ws_bytes = 0;
+  size_t lse_offset = 0;
+};
+
+// Partition choice.  Work items are (sequence x KV head, partition); the
+// target is enough items to fill every SM several times over (so uneven
+// context lengths do not leave a long tail), with partitions of at most
+// kAutoMaxPartBlocks blocks (1024 tokens) and at least kAutoMinPartBlocks.
+constexpr int kAutoMinPartBlocks = 16;
+constexpr int kAutoMaxPartBlocks = 64;
+constexpr int kItemsPerSm = 16;
+
+int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
+              int partition_blocks, Plan* plan) {
+  if (num_seqs < 0 || q_heads <= 0 || kv_heads <= 0 || max_context_len < 0) return PKV_EINVAL;
+  if (q_heads % kv_heads) return PKV_EUNSUPPORTED;
+  if (!supported_group(q_heads / kv_heads)) return PKV_EUNSUPPORTED;
+  if (d_head != 64 && d_head != 128) return PKV_EUNSUPPORTED;
+  const int max_pb = pkv::decode_max_partition_blocks();
+  const int nblk_max = (max_context_len + kBlockSize - 1) / kBlockSize;
+  int pb;
+  if (partition_blocks > 0) {
+    if (partition_blocks > max_pb) return PKV_EINVAL;
+    pb = partition_blocks;
+  } else {
+    const long long pairs = (long long)num_seqs * kv_heads;
+    const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
+    const long long target = (long long)kItemsPerSm * sms;
+    long long per_pair = pairs > 0 ? (target + pairs - 1) / pairs : 1;
+    if (per_pair < 1) per_pair = 1;
+    long long want = (nblk_max + per_pair - 1) / per_pair;
+    const int lo = nblk_max < kAutoMinPartBlocks ? (nblk_max > 0 ? nblk_max : 1)
+                                                 : kAutoMinPartBlocks;
+    if (want < lo) want = lo;
+    if (want > kAutoMaxPartBlocks) want = kAutoMaxPartBlocks;
+    pb = int(want);
+  }
+  const long long parts = nblk_max > 0 ? ((long long)nblk_max + pb - 1) / pb : 1;
+  if (parts > 65535) return PKV_EUNSUPPORTED;
+  plan->partition_blocks = pb;
+  plan->num_parts = int(parts);
+  if (parts > 1) {
+    const size_t rows = size_t(num_seqs) * size_t(q_heads) * size_t(parts);
+    const size_t o_bytes = rows * size_t(d_head) * sizeof(float);
+    plan->lse_offset = (o_bytes + 255) / 256 * 256;
+    plan->ws_bytes = plan->lse_offset + rows * sizeof(float);
+  } else {
+    plan->ws_bytes = 0;
+    plan->lse_offset = 0;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_EINVAL: return "PKV_EINVAL: invalid argument";
+    case PKV_EUNSUPPORTED: return "PKV_EUNSUPPORTED: unsupported shape";
+    case PKV_ECUDA: return "PKV_ECUDA: CUDA call or launch failed";
+    case PKV_ENOMEM: return "PKV_ENOMEM: workspace too small";
+    case PKV_EDEVICE_CHECK: return "PKV_EDEVICE_CHECK: device-side check failed";
+    case PKV_ETIMEOUT: return "PKV_ETIMEOUT: bounded device wait ran out";
+    default: return "unknown pkv status";
+  }
+}
+
+int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_tok_stride,
+                  const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                  void* v_cache, pkv_cache_desc cache, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
+  const int64_t row = int64_t(cache.kv_heads) * cache.d_head;
+  if (row % 8) return PKV_EUNSUPPORTED;  // rows move as 16-byte vectors
+  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+    return PKV_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  const int64_t num_slots = int64_t(cache.num_blocks) * cache.block_size;
+  cudaError_t e = pkv::launch_kv_append(k, k_tok_stride, v, v_tok_stride, slot_mapping,
+                                        num_tokens, k_cache, v_cache, num_slots, int(row),
+                                        static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
+                    int partition_blocks, int* out_partition_blocks, int* out_num_parts,
+                    size_t* out_workspace_bytes) {
+  Plan plan;
+  const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                           partition_blocks, &plan);
+  if (st != PKV_OK) return st;
+  if (out_partition_blocks) *out_partition_blocks = plan.partition_blocks;
+  if (out_num_parts) *out_num_parts = plan.num_parts;
+  if (out_workspace_bytes) *out_workspace_bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,
+                                  int max_context_len) {
+  Plan plan;
+  if (make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &plan) != PKV_OK)
+    return 0;
+  return plan.ws_bytes;
+}
+
+int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                                  const void* v_cache, pkv_cache_desc cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int max_context_len, float scale,
+                                  float* out, void* workspace, size_t ws_bytes,
+                                  int partition_blocks, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  Plan plan;
+  st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
+                 partition_blocks, &plan);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+  if (max_blocks_per_seq <= 0) return PKV_EINVAL;
+  if (!std::isfinite(scale)) return PKV_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+    return PKV_EINVAL;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
+    if (!aligned(workspace, 256)) return PKV_EINVAL;
+  }
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::DecodeArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                        plan.lse_offset)
+                             : nullptr;
+  a.num_seqs = num_seqs;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.partition_blocks = plan.partition_blocks;
+  a.num_parts = plan.num_parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                               const void* v_cache, pkv_cache_desc cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float scale,
+                               float* out, void* workspace, size_t ws_bytes,
+                               pkv_stream_t stream) {
+  return pkv_paged_decode_attention_ex(q, num_seqs, q_heads, k_cache, v_cache, cache,
+                                       block_tables, max_blocks_per_seq, context_lens,
+                                       max_context_len, scale, out, workspace, ws_bytes, 0,
+                                       stream);
+}
+
+int pkv_get_device_error(unsigned int* word, int clear) {
+  if (!word) return PKV_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ECUDA;
+  const unsigned a = pkv::read_append_error(clear != 0);
+  const unsigned d = pkv::read_decode_error(clear != 0);
+  if (a == ~0u || d == ~0u) return PKV_ECUDA;
+  *word = a | d;
+  return PKV_OK;
+}
+
+}  // extern "C"

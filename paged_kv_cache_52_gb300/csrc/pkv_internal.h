@@ -1,0 +1,41 @@
+// Host-side launch entry points of each kernel translation unit, called by
+// the C ABI layer (pkv_api.cu).  Arguments are validated before these run.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// ---- kv_append.cu
+cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                             const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                             void* v_cache, int64_t num_slots, int row_elems,
+                             cudaStream_t stream, int num_sms);
+unsigned read_append_error(bool clear);
+
+// ---- paged_decode.cu
+struct DecodeArgs {
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* out;
+  float* part_o;    // [S][Hq][num_parts][d] (num_parts > 1 only)
+  float* part_lse;  // [S][Hq][num_parts]
+  int num_seqs, q_heads, kv_heads, d_head, num_blocks;
+  int max_blocks_per_seq;
+  int partition_blocks, num_parts;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Number of K/V stages and warps the decode kernel uses (for the plan).
+int decode_warps_per_cta();
+int decode_max_partition_blocks();
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                const CUtensorMap* tmap_v, cudaStream_t stream);
+unsigned read_decode_error(bool clear);
+
+}  // namespace pkv

@@ -1,0 +1,204 @@
+"""Thin ctypes binding over ``libpagedkv.so`` (argument marshalling only).
+
+Every function here checks tensor dtypes/shapes/devices, takes raw device
+pointers and the current CUDA stream from torch, and calls the C entry point
+of the same name; all compute runs in the library's CUDA kernels.  Importing
+this module loads the library and raises if it is missing: there is no
+fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+
+PKV_OK = 0
+BLOCK_SIZE = 16
+
+DEVERR_BITS = {
+    0x1: "bad slot",
+    0x2: "bad block id",
+    0x4: "bad context length",
+    0x8: "wait timeout",
+    0x10: "bad query range",
+    0x20: "tensor memory allocation",
+}
+
+
+class PagedKVError(RuntimeError):
+    """A library call returned a non-zero pkv_status."""
+
+    def __init__(self, func: str, status: int, text: str):
+        super().__init__(f"{func} failed with status {status} ({text})")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("d_head", ctypes.c_int32)]
+
+
+_vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                              ctypes.c_size_t)
+
+SIGNATURES = {
+    "pkv_version": ([], ctypes.c_int),
+    "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "pkv_kv_append": ([_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, CacheDesc, _vp], ctypes.c_int),
+    "pkv_decode_plan": ([ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(_sz)], ctypes.c_int),
+    "pkv_decode_workspace_bytes": ([ctypes.c_int] * 5, _sz),
+    "pkv_paged_decode_attention": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
+                                    ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz, _vp],
+                                   ctypes.c_int),
+    "pkv_paged_decode_attention_ex": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
+                                       ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
+                                       ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -m paged_kv_cache_52_gb300.build`"
+                           " (the CUDA library is required, there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.pkv_status_string(int(status)).decode()
+
+
+def _check(func: str, status: int):
+    if status != PKV_OK:
+        raise PagedKVError(func, status, status_string(status))
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    _need(k_cache.dim() == 4, "cache must be [num_blocks, block_size, kv_heads, d_head]")
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d)
+
+
+def _check_cache(k_cache, v_cache):
+    for c in (k_cache, v_cache):
+        _need(c.is_cuda and c.dtype == torch.bfloat16 and c.is_contiguous(),
+              "caches must be contiguous bf16 CUDA tensors")
+    _need(k_cache.shape == v_cache.shape, "k_cache and v_cache shapes differ")
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+              k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """Scatter ``k, v [T, kv_heads, d]`` into the pools at ``slot_mapping [T]`` (-1 skips)."""
+    _check_cache(k_cache, v_cache)
+    t = slot_mapping.shape[0]
+    for x in (k, v):
+        _need(x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 3,
+              "k, v must be [T, kv_heads, d] bf16 CUDA tensors")
+        _need(x.shape[0] == t and tuple(x.shape[1:]) == tuple(k_cache.shape[2:]),
+              "k, v rows must match the cache rows")
+        _need(x.stride(2) == 1 and x.stride(1) == x.shape[2],
+              "each token row of k, v must be contiguous")
+    _need(slot_mapping.is_cuda and slot_mapping.dtype == torch.int64 and
+          slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64 on the GPU")
+    st = lib.pkv_kv_append(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), t,
+                           _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _stream(k_cache))
+    _check("pkv_kv_append", st)
+
+
+def decode_plan(num_seqs: int, q_heads: int, kv_heads: int, d_head: int, max_context_len: int,
+                partition_blocks: int = 0):
+    """(partition_blocks, num_parts, workspace_bytes) the decode will use."""
+    pb, np_, ws = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    st = lib.pkv_decode_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                             partition_blocks, ctypes.byref(pb), ctypes.byref(np_),
+                             ctypes.byref(ws))
+    _check("pkv_decode_plan", st)
+    return pb.value, np_.value, ws.value
+
+
+def decode_workspace(num_seqs, q_heads, kv_heads, d_head, max_context_len, device,
+                     partition_blocks: int = 0) -> Optional[torch.Tensor]:
+    """A workspace tensor large enough for the plan (None when not needed)."""
+    _, _, ws = decode_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                           partition_blocks)
+    if ws == 0:
+        return None
+    return torch.empty(ws, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None,
+                           max_context_len: Optional[int] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           partition_blocks: int = 0) -> torch.Tensor:
+    """Decode attention: ``q [S, Hq, d]`` over each sequence's paged history.
+
+    Returns ``out [S, Hq, d]`` float32.  ``max_context_len`` (host int) plans
+    the split; when omitted it is read from ``context_lens`` (a device sync).
+    """
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
+    S, hq, d = q.shape
+    _need(d == k_cache.shape[3], "q and cache head dims differ")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous() and
+          context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, hq, d),
+          "out must be contiguous float32 [S, Hq, d]")
+    hkv = k_cache.shape[2]
+    if workspace is None:
+        workspace = decode_workspace(S, hq, hkv, d, max_context_len, q.device, partition_blocks)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_decode_attention_ex(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
+    _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def get_device_error(clear: bool = True) -> int:
+    """OR of the device-side check bits raised since the last clear (syncs)."""
+    word = ctypes.c_uint()
+    _check("pkv_get_device_error", lib.pkv_get_device_error(ctypes.byref(word), int(clear)))
+    return word.value
+
+
+def describe_device_error(word: int) -> list[str]:
+    return [name for bit, name in DEVERR_BITS.items() if word & bit]

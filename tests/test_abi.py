@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every entry point its header declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_52_gb300 import build as b
+    if not os.path.exists(b.LIB_PATH):
+        b.build()
+    from paged_kv_cache_52_gb300 import pagedkv
+    return pagedkv
+
+
+def declared_symbols():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        names += re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for required in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_decode_plan",
+                     "pkv_get_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+    # every declared symbol also has a ctypes signature in the binding
+    assert set(declared_symbols()) <= set(pk.SIGNATURES), set(declared_symbols()) - set(pk.SIGNATURES)
+
+
+def test_version_and_status_strings(pk):
+    assert pk.lib.pkv_version() >= 100
+    assert pk.status_string(0) == "PKV_OK"
+    assert "invalid" in pk.status_string(-1)
+    assert "unsupported" in pk.status_string(-2)
+
+
+def _desc(pk, nb=64, bs=16, hkv=2, d=64):
+    return pk.CacheDesc(nb, bs, hkv, d)
+
+
+def test_append_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    assert lib.pkv_kv_append(null, 128, null, 128, null, 0, null, null, _desc(pk), null) == 0
+    assert lib.pkv_kv_append(null, 128, null, 128, null, -1, null, null, _desc(pk), null) == -1
+    assert lib.pkv_kv_append(dummy, 128, dummy, 128, dummy, 4, null, dummy, _desc(pk), null) == -1
+    assert lib.pkv_kv_append(dummy, 128, dummy, 128, dummy, 4, dummy, dummy,
+                             _desc(pk, bs=8), null) == -2
+    assert lib.pkv_kv_append(dummy, 127, dummy, 128, dummy, 4, dummy, dummy, _desc(pk),
+                             null) == -1               # stride below the row / not 16-byte
+    assert lib.pkv_kv_append(ctypes.c_void_p((1 << 20) + 2), 128, dummy, 128, dummy, 4, dummy,
+                             dummy, _desc(pk), null) == -1  # misaligned base
+    assert lib.pkv_kv_append(dummy, 128, dummy, 128, dummy, 4, dummy, dummy,
+                             _desc(pk, nb=0), null) == -1
+
+
+def test_decode_plan_and_workspace(pk):
+    pb, parts, ws = pk.decode_plan(4, 8, 2, 64, 1000, partition_blocks=16)
+    assert (pb, parts) == (16, 4)                      # ceil(ceil(1000/16) / 16)
+    rows = 4 * 8 * parts
+    assert ws == (rows * 64 * 4 + 255) // 256 * 256 + rows * 4
+    pb, parts, ws = pk.decode_plan(4, 8, 2, 64, 250, partition_blocks=16)
+    assert (parts, ws) == (1, 0)
+    with pytest.raises(pk.PagedKVError):
+        pk.decode_plan(4, 12, 4, 64, 100)              # group 3
+    with pytest.raises(pk.PagedKVError):
+        pk.decode_plan(4, 8, 2, 96, 100)               # d_head 96
+    with pytest.raises(pk.PagedKVError):
+        pk.decode_plan(4, 8, 2, 64, 100, partition_blocks=2048)
+    with pytest.raises(pk.PagedKVError):
+        pk.decode_plan(4, 8, 2, 64, -1)
+    # automatic plan: partitions stay within [16, 64] blocks once contexts are long
+    pb, parts, _ = pk.decode_plan(4, 64, 8, 128, 131072)
+    assert 16 <= pb <= 64 and parts == -(-8192 // pb)
+    assert pk.lib.pkv_decode_workspace_bytes(4, 64, 8, 128, 131072) == \
+        pk.decode_plan(4, 64, 8, 128, 131072)[2]
+
+
+def test_decode_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    args = lambda S, hq, desc, ws=null, wsb=0, pb=16, out=dummy: (  # noqa: E731
+        dummy, S, hq, dummy, dummy, desc, dummy, 16, dummy, 250, 0.125, out, ws, wsb, pb, null)
+    assert lib.pkv_paged_decode_attention_ex(*args(0, 8, _desc(pk))) == 0      # nothing to do
+    assert lib.pkv_paged_decode_attention_ex(*args(4, 8, _desc(pk), out=null)) == -1
+    assert lib.pkv_paged_decode_attention_ex(*args(4, 6, _desc(pk))) == -2     # group 3
+    assert lib.pkv_paged_decode_attention_ex(*args(4, 8, _desc(pk, bs=32))) == -2
+    # split plan (pb=4 -> 4 parts) without a workspace
+    assert lib.pkv_paged_decode_attention_ex(*args(4, 8, _desc(pk), pb=4)) == -4

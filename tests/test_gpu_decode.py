@@ -1,0 +1,121 @@
+"""Paged decode attention on the GPU against the CPU oracle.
+
+Small cases compare every output element; the full-size 7B-MHA, 70B-GQA and
+128K long-context workloads run in the launch configuration the benchmark
+times (automatic split plan) and compare sampled sequences.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_52_gb300 import workloads as wl
+from parity import DecodeStepOracle, assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_52_gb300 import pagedkv
+    pagedkv.get_device_error(clear=True)
+    return pagedkv
+
+
+def run_step(pk, w, partition_blocks=0, max_context_len=None):
+    """One decode step on the GPU: append the new token of every sequence, then attend."""
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    mcl = max(w.meta["lens"]) if max_context_len is None else max_context_len
+    out = pk.paged_decode_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                    max_context_len=mcl, partition_blocks=partition_blocks)
+    torch.cuda.synchronize()
+    return out
+
+
+def _to_dev(w):
+    for name in ("q", "k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "block_tables",
+                 "context_lens"):
+        setattr(w, name, getattr(w, name).to(DEV))
+    return w
+
+
+@pytest.mark.parametrize("pb", [0, 1, 2, 3, 5, 16])
+def test_tiny_config_all_partitions(pk, pb):
+    w = wl.make_decode_workload(wl.TINY)
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    out = run_step(pk, _to_dev(w), partition_blocks=pb)
+    assert_attention_close(out.cpu().numpy(), ref, f"tiny pb={pb}")
+    assert pk.get_device_error() == 0
+
+
+SHAPES = [(8, 8, 128), (8, 4, 64), (16, 4, 128), (64, 8, 128), (32, 2, 64), (16, 16, 64)]
+EDGE_LENS = [1, 15, 16, 17, 33, 200, 0, 161]
+
+
+@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+@pytest.mark.parametrize("pb", [0, 2])
+def test_groups_heads_and_ragged_lengths(pk, hq, hkv, d, pb):
+    spec = wl.DecodeSpec("edge", 11, len(EDGE_LENS), hq, hkv, d, lens=tuple(EDGE_LENS))
+    w = wl.make_decode_workload(spec, lens_override=EDGE_LENS)
+    # the empty sequence appends nothing
+    w.slot_mapping[EDGE_LENS.index(0)] = -1
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    out = run_step(pk, _to_dev(w), partition_blocks=pb)
+    assert_attention_close(out.cpu().numpy(), ref, f"{hq}/{hkv} d{d} pb={pb}")
+    assert np.all(out[EDGE_LENS.index(0)].cpu().numpy() == 0.0)
+    assert pk.get_device_error() == 0
+
+
+def test_massive_activation_outliers_small(pk):
+    # the 70B-GQA recipe (0.1% K rows x100), shrunk to lengths the oracle does whole
+    w = wl.make_decode_workload(wl.GQA_70B, lens_override=[1024, 3000, 777, 4096, 2049, 1500])
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    for pb in (0, 7):
+        out = run_step(pk, _to_dev(w) if not w.q.is_cuda else w, partition_blocks=pb)
+        assert_attention_close(out.cpu().numpy(), ref, f"outliers pb={pb}")
+
+
+def test_repeatable_bitwise(pk):
+    w = _to_dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[900, 2500, 64]))
+    a = run_step(pk, w)
+    b = run_step(pk, w)
+    assert torch.equal(a, b)
+
+
+def test_bad_block_id_and_context_are_flagged(pk):
+    w = _to_dev(wl.make_decode_workload(wl.TINY))
+    pk.get_device_error(clear=True)
+    bt = w.block_tables.clone()
+    bt[1, 0] = 10_000                      # outside the 64-block pool
+    pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.scale,
+                              max_context_len=250)
+    assert pk.get_device_error(clear=True) & 0x2
+    lens = w.context_lens.clone()
+    lens[0] = 16 * bt.shape[1] + 5         # longer than the block table
+    out = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.scale,
+                                    max_context_len=int(lens.max()))
+    assert pk.get_device_error(clear=True) & 0x4
+    assert torch.isfinite(out).all()
+    # a max_context_len below the real lengths: flagged, never out of bounds
+    pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                              w.scale, max_context_len=40, partition_blocks=1)
+    assert pk.get_device_error(clear=True) & 0x4
+
+
+FULL = [("mha7b", [0, 17, 40, 63]), ("gqa70b", [0, 1, 100, 200, 255]), ("long128k", [2])]
+
+
+@pytest.mark.parametrize("name,seqs", FULL)
+def test_full_size_configs_sampled(pk, name, seqs):
+    spec = wl.DECODE_SPECS[name]
+    w = wl.make_decode_workload(spec, device=DEV, gen_device=DEV)
+    ref = DecodeStepOracle(w, seqs).output()
+    out = run_step(pk, w)
+    assert_attention_close(out[seqs].cpu().numpy(), ref, name)
+    assert torch.isfinite(out).all()
+    assert pk.get_device_error() == 0
+    del w
+    torch.cuda.empty_cache()
