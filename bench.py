@@ -44,11 +44,13 @@ NOMINAL_HBM_GBS = 8000.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa70b", choices=sorted(wl.DECODE_SPECS))
     ap.add_argument("--partition-blocks", type=int, default=0)
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="shrink the workload to this many sequences (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -75,7 +77,8 @@ def measured_peak():
 def workload_config(w, spec, plan):
     lens = w.meta["lens"]
     return {
-        "workload": spec.name,
+        "workload": spec.name if w.num_seqs == spec.num_seqs else
+        f"{spec.name}, shrunk to {w.num_seqs} sequences",
         "num_seqs": w.num_seqs, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
         "d_head": w.d_head, "block_size": wl.BLOCK_SIZE,
         "context_len_min": min(lens), "context_len_max": max(lens),
@@ -88,7 +91,8 @@ def workload_config(w, spec, plan):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi clock/throttle samples (every 100 ms) while the GPU runs the
+    step under load: a 0.6 s lead-in of the same steps, then the timed region."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -102,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -225,7 +229,8 @@ def run_ours(args):
             torch.distributed.barrier()
 
     spec = wl.DECODE_SPECS[args.workload]
-    w = wl.make_decode_workload(spec, device=dev, gen_device=dev)
+    w = wl.make_decode_workload(spec, device=dev, gen_device=dev,
+                                num_seqs_override=args.num_seqs or None)
     S, hq, hkv, d = w.num_seqs, w.q_heads, w.kv_heads, w.d_head
     max_len = max(w.meta["lens"])
     plan = pagedkv.decode_plan(S, hq, hkv, d, max_len, args.partition_blocks)
@@ -258,6 +263,14 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # keep the GPU under the same load while nvidia-smi starts sampling,
+        # so the samples bracket the timed region
+        t_load = time.perf_counter()
+        while time.perf_counter() - t_load < 0.6:
+            for _ in range(50):
+                append(w.k_new, w.v_new, w.slot_mapping)
+                decode(w.q, w.block_tables, w.context_lens)
+            torch.cuda.synchronize()
         start.record()
         for a, b, c in marks:
             a.record()
