@@ -54,7 +54,8 @@ typedef enum {
   PKV_ECUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
   PKV_ENOMEM = -4,        /* the workspace passed is smaller than required */
   PKV_EDEVICE_CHECK = -5, /* reserved: a device-side index check failed */
-  PKV_ETIMEOUT = -6       /* reserved: a bounded device wait ran out */
+  PKV_ETIMEOUT = -6,      /* reserved: a bounded device wait ran out */
+  PKV_ESCRATCH_TOO_SMALL = -7 /* the no-allocation decode's fixed scratch cannot hold the plan */
 } pkv_status;
 
 /* Shape of one layer's K (and V) pool: [num_blocks][block_size][kv_heads][d_head]. */
@@ -160,6 +161,35 @@ PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_hea
                                   const int32_t* context_lens, int max_context_len, float scale,
                                   float* out, void* workspace, size_t ws_bytes,
                                   int partition_blocks, pkv_stream_t stream);
+
+/*
+ * Decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that are handed
+ * device buffers but may not call cudaMalloc (a fixed, pre-reserved memory
+ * budget with no allocator, a plug-in inside another runtime, a serving loop
+ * that must never allocate mid-step).
+ *
+ * Same computation and arguments as pkv_paged_decode_attention_ex, but the
+ * split-K scratch is a 32 MiB array compiled into the library
+ * (pkv_noalloc_scratch_bytes()), held by every GPU that loads the library
+ * until the process exits.  No call allocates or frees memory.  The first
+ * call on a device looks up the array's device address (make it before any
+ * stream capture).  All calls share the array: calls whose work overlaps on
+ * the GPU race on it, so order them on one stream.  Nothing in it needs to
+ * start at zero.  Returns PKV_ESCRATCH_TOO_SMALL when the plan for these
+ * sizes (pkv_decode_plan's workspace bytes) exceeds the array; a larger
+ * partition_blocks needs less scratch.
+ */
+PKV_API size_t pkv_noalloc_scratch_bytes(void);
+
+PKV_API int pkv_paged_decode_attention_noalloc(const void* q, int num_seqs, int q_heads,
+                                               const void* k_cache, const void* v_cache,
+                                               pkv_cache_desc cache,
+                                               const int32_t* block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t* context_lens, int max_context_len,
+                                               float scale, float* out, int partition_blocks,
+                                               pkv_stream_t stream);
 
 /*
  * Read the device error word of the current device (an OR of the

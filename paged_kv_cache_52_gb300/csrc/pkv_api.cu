@@ -146,6 +146,8 @@ const char* pkv_status_string(int status) {
     case PKV_ENOMEM: return "PKV_ENOMEM: workspace too small";
     case PKV_EDEVICE_CHECK: return "PKV_EDEVICE_CHECK: device-side check failed";
     case PKV_ETIMEOUT: return "PKV_ETIMEOUT: bounded device wait ran out";
+    case PKV_ESCRATCH_TOO_SMALL:
+      return "PKV_ESCRATCH_TOO_SMALL: plan needs more than the fixed no-allocation scratch";
     default: return "unknown pkv status";
   }
 }

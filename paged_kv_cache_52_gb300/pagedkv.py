@@ -61,6 +61,10 @@ SIGNATURES = {
                                        ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                        ctypes.c_int, _vp], ctypes.c_int),
     "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
+    "pkv_noalloc_scratch_bytes": ([], _sz),
+    "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
+                                            _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
+                                            ctypes.c_int, _vp], ctypes.c_int),
 }
 
 
@@ -190,6 +194,30 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
     _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def paged_decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                                   max_context_len: int, partition_blocks: int = 0) -> torch.Tensor:
+    """Decode attention that allocates nothing: the split-K scratch is the
+    library's fixed array (see ``pkv_paged_decode_attention_noalloc``).  The
+    caller passes the output buffer; nothing here allocates either."""
+    _check_cache(k_cache, v_cache)
+    S, hq, d = q.shape
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous(), "q: contiguous bf16")
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, hq, d),
+          "out must be contiguous float32 [S, Hq, d]")
+    _need(block_tables.dtype == torch.int32 and block_tables.is_contiguous(),
+          "block_tables: contiguous int32")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens: contiguous int32")
+    st = lib.pkv_paged_decode_attention_noalloc(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        int(partition_blocks), _stream(q))
+    _check("pkv_paged_decode_attention_noalloc", st)
     return out
 
 
