@@ -163,6 +163,42 @@ PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_hea
                                   int partition_blocks, pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention -- chunked prefill: each sequence's new query
+ * tokens attend over its paged context (the continuous-batching step in which
+ * new prompt chunks join running decodes).  Runs on the tcgen05 tensor cores.
+ *
+ * Passages: "Optimisation de l'inference", section "Etape 2: Attention avec
+ * KV Cache" (softmax(q K^T * scale + mask) V; for more than one query the
+ * mask is triu(ones(Tq, Tk), k = Tk - Tq + 1), i.e. bottom-right aligned);
+ * "Cache KV, attention et optimisation de l'inference", section "Attention a
+ * la lumiere" (FlashAttention tiling: a query tile stays on chip while K/V
+ * tiles stream by with a running max and sum).
+ *
+ *   q            : [total_q][q_heads][d_head] bf16, contiguous; the rows
+ *                  q_start[s] .. q_start[s+1]-1 are the chunk of sequence s.
+ *   q_start      : [num_seqs + 1] int32, non-decreasing, q_start[num_seqs] <= total_q.
+ *   max_q_len    : host bound on q_start[s+1] - q_start[s] (sizes the grid).
+ *   context_lens : [num_seqs] int32, INCLUDING the chunk (its K/V must have
+ *                  been appended first); the chunk is the last n tokens.
+ *   causal       : nonzero = query i of a chunk of n sees keys
+ *                  0 .. context_len - n + i; zero = every query sees the
+ *                  whole context.
+ *   out          : [total_q][q_heads][d_head] float32, 16-byte aligned; rows
+ *                  outside every chunk are not written.
+ * A chunk longer than its context, a non-monotone q_start or a context beyond
+ * the block table skips that sequence and sets PKV_DEVERR_BAD_QUERY_RANGE; a
+ * chunk longer than max_q_len is computed only up to max_q_len tokens and
+ * sets the same bit.  No workspace is needed.
+ */
+PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_seqs,
+                                        int total_q, int max_q_len, int q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        pkv_cache_desc cache, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* context_lens,
+                                        int causal, float scale, float* out,
+                                        pkv_stream_t stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that are handed
  * device buffers but may not call cudaMalloc (a fixed, pre-reserved memory

@@ -64,6 +64,24 @@ bool encode_pool_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view of packed queries [total_q][q_heads][d_head] bf16: (d_head, q_heads,
+// total_q).  One box is 64 columns x `group` heads x `tokens` tokens -- the
+// 128 (token, head) rows of one prefill tile, 128-byte swizzled.
+bool encode_query_map(CUtensorMap* map, const void* q, int total_q, int q_heads, int d_head,
+                      int group, int tokens) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(d_head), cuuint64_t(q_heads), cuuint64_t(total_q)};
+  const cuuint64_t row = cuuint64_t(d_head) * 2;
+  const cuuint64_t strides[2] = {row, row * cuuint64_t(q_heads)};
+  const cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tokens)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_cache_desc(const pkv_cache_desc& c) {
@@ -257,13 +275,59 @@ int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads, const v
                                        stream);
 }
 
+int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_seqs, int total_q,
+                                int max_q_len, int q_heads, const void* k_cache,
+                                const void* v_cache, pkv_cache_desc cache,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int causal, float scale, float* out,
+                                pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || q_heads <= 0) return PKV_EINVAL;
+  if (q_heads % cache.kv_heads) return PKV_EUNSUPPORTED;
+  const int group = q_heads / cache.kv_heads;
+  if (!supported_group(group)) return PKV_EUNSUPPORTED;
+  if (cache.d_head != 64 && cache.d_head != 128) return PKV_EUNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_EINVAL;
+  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
+  if ((long long)num_seqs * cache.kv_heads > 65535) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_EINVAL;
+  const int rows = pkv::prefill_rows_per_tile();
+  CUtensorMap tq, tk, tv;
+  if (!encode_query_map(&tq, q, total_q, q_heads, cache.d_head, group, rows / group) ||
+      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::PrefillArgs a;
+  a.q_start = q_start;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_q_len = max_q_len;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 int pkv_get_device_error(unsigned int* word, int clear) {
   if (!word) return PKV_EINVAL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ECUDA;
   const unsigned a = pkv::read_append_error(clear != 0);
   const unsigned d = pkv::read_decode_error(clear != 0);
-  if (a == ~0u || d == ~0u) return PKV_ECUDA;
-  *word = a | d;
+  const unsigned f = pkv::read_prefill_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u) return PKV_ECUDA;
+  *word = a | d | f;
   return PKV_OK;
 }
 

@@ -38,4 +38,24 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);
 unsigned read_decode_error(bool clear);
 
+// ---- paged_prefill.cu
+struct PrefillArgs {
+  const int32_t* q_start;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* out;
+  int num_seqs, total_q, max_q_len, q_heads, kv_heads, d_head, num_blocks;
+  int max_blocks_per_seq;
+  int causal;
+  float scale_log2;
+};
+
+// Query rows (tokens x heads of a GQA group) per prefill tile.
+int prefill_rows_per_tile();
+
+cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q,
+                                 const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                 cudaStream_t stream);
+unsigned read_prefill_error(bool clear);
+
 }  // namespace pkv

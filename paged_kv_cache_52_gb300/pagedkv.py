@@ -61,6 +61,9 @@ SIGNATURES = {
                                        ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                        ctypes.c_int, _vp], ctypes.c_int),
     "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
+    "pkv_paged_prefill_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
+                                     ctypes.c_int, _f32, _vp, _vp], ctypes.c_int),
     "pkv_noalloc_scratch_bytes": ([], _sz),
     "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
@@ -194,6 +197,41 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
     _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, causal: bool, scale: float,
+                            out: Optional[torch.Tensor] = None,
+                            max_q_len: Optional[int] = None) -> torch.Tensor:
+    """Chunked prefill: rows ``q_start[s]:q_start[s+1]`` of ``q [total, Hq, d]``
+    are the last tokens of sequence s (already appended).  Returns ``out``
+    float32 ``[total, Hq, d]``.  ``max_q_len`` (host int) sizes the grid; when
+    omitted it is read from ``q_start`` (a device sync)."""
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [total, Hq, d] bf16 CUDA tensor")
+    total, hq, d = q.shape
+    S = context_lens.shape[0]
+    _need(q_start.dtype == torch.int32 and q_start.is_contiguous() and q_start.shape == (S + 1,),
+          "q_start must be contiguous int32 [S + 1]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be contiguous int32 [S]")
+    if max_q_len is None:
+        max_q_len = int((q_start[1:] - q_start[:-1]).max().item()) if S else 0
+    if out is None:
+        out = torch.empty(total, hq, d, dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (total, hq, d),
+          "out must be contiguous float32 [total, Hq, d]")
+    st = lib.pkv_paged_prefill_attention(
+        _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+        cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        int(bool(causal)), float(scale), _ptr(out), _stream(q))
+    _check("pkv_paged_prefill_attention", st)
     return out
 
 

@@ -324,3 +324,44 @@ def make_mixed_workload(spec: MixedSpec = MIXED, device="cpu", gen_device=None,
 def bf16_bits(t: torch.Tensor):
     """Raw 16-bit patterns of a bf16 tensor as a numpy uint16 array (CPU)."""
     return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def make_chunked_workload(q_heads: int, kv_heads: int, d_head: int, priors: Sequence[int],
+                          chunks: Sequence[int], config_id: int = 6, shared_prefix: int = 0,
+                          device="cpu", gen_device=None) -> MixedWorkload:
+    """Prefill-only step with per-sequence chunk lengths: sequence s has
+    ``priors[s]`` tokens already cached (the first ``shared_prefix`` of them in
+    blocks common to every sequence) and appends ``chunks[s]`` new tokens."""
+    base = 1000 * config_id
+    if shared_prefix % BLOCK_SIZE:
+        raise ValueError("the shared prefix must fill whole blocks")
+    if any(p < shared_prefix for p in priors):
+        raise ValueError("every prior must cover the shared prefix")
+    lens = [int(p) + int(c) for p, c in zip(priors, chunks)]
+    pblocks = shared_prefix // BLOCK_SIZE
+    need = pblocks + sum(max(0, blocks_for(L) - pblocks) for L in lens)
+    nb = max(1, math.ceil(1.25 * need))
+    perm = torch.randperm(nb, generator=_cpu_gen(base + 6))
+    tables, _ = build_block_tables(lens, perm, shared_prefix_blocks=pblocks)
+    pool_shape = (nb, BLOCK_SIZE, kv_heads, d_head)
+    k_cache = _randn_bf16(pool_shape, base + 1, device, gen_device)
+    v_cache = _randn_bf16(pool_shape, base + 2, device, gen_device)
+    positions = [list(range(int(p), int(p) + int(c))) for p, c in zip(priors, chunks)]
+    t_new = sum(int(c) for c in chunks)
+    k_new = _randn_bf16((t_new, kv_heads, d_head), base + 3, device, gen_device)
+    v_new = _randn_bf16((t_new, kv_heads, d_head), base + 4, device, gen_device)
+    q = _randn_bf16((t_new, q_heads, d_head), base + 0, device, gen_device)
+    q_start = torch.zeros(len(chunks) + 1, dtype=torch.int32)
+    q_start[1:] = torch.cumsum(torch.tensor([int(c) for c in chunks], dtype=torch.int32), 0)
+    empty_tab = torch.zeros((0, tables.shape[1]), dtype=torch.int32)
+    return MixedWorkload(
+        name="chunked prefill", k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new,
+        slot_mapping=append_slots(tables, positions).to(device), q_prefill=q,
+        q_start=q_start.to(device), prefill_tables=tables.to(device),
+        prefill_lens=torch.tensor(lens, dtype=torch.int32, device=device),
+        q_decode=torch.empty((0, q_heads, d_head), dtype=torch.bfloat16, device=device),
+        decode_tables=empty_tab.to(device),
+        decode_lens=torch.empty(0, dtype=torch.int32, device=device),
+        scale=1.0 / math.sqrt(d_head),
+        meta={"config_id": config_id, "num_blocks": nb, "prefill_lens": lens, "decode_lens": [],
+              "chunks": [int(c) for c in chunks], "shared_prefix": shared_prefix})

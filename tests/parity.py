@@ -91,3 +91,49 @@ class DecodeStepOracle:
     def output(self):
         kc, vc = oracle.kv_append(self.k_new, self.v_new, self.slots, self.kc, self.vc)
         return oracle.paged_decode_attention(self.q, kc, vc, self.tables, self.lens, self.scale)
+
+
+class PrefillStepOracle:
+    """Oracle for a chunked-prefill step (append the chunks, then attend) of
+    the chosen sequences, from a host snapshot taken BEFORE the GPU step."""
+
+    def __init__(self, w, seqs, causal=True):
+        self.seqs = list(seqs)
+        self.causal = causal
+        lens = [int(x) for x in w.prefill_lens.cpu().tolist()]
+        self.lens = [lens[s] for s in self.seqs]
+        self.kc, self.vc, self.tables, remap = compact_pool(w.k_cache, w.v_cache,
+                                                            w.prefill_tables, lens, self.seqs)
+        qs = w.q_start.cpu().numpy()
+        rows = np.concatenate([np.arange(qs[s], qs[s + 1]) for s in self.seqs]).astype(np.int64)
+        self.rows = rows
+        self.q_start = np.concatenate([[0], np.cumsum([qs[s + 1] - qs[s] for s in self.seqs])])
+        slots = w.slot_mapping.cpu().numpy()[rows]
+        self.slots = remap_slots(slots, remap)
+        idx = torch.tensor(rows, dtype=torch.int64, device=w.q_prefill.device)
+        self.k_new = wl.bf16_bits(w.k_new.index_select(0, idx))
+        self.v_new = wl.bf16_bits(w.v_new.index_select(0, idx))
+        self.q = wl.bf16_bits(w.q_prefill.index_select(0, idx))
+        self.scale = w.scale
+
+    def cache(self):
+        return oracle.kv_append(self.k_new, self.v_new, self.slots, self.kc, self.vc)
+
+    def output(self):
+        kc, vc = self.cache()
+        return oracle.paged_prefill_attention(self.q, self.q_start, kc, vc, self.tables, self.lens,
+                                              self.causal, self.scale)
+
+    def rows_output(self, picks):
+        """Oracle rows for (local sequence index, query index in its chunk)
+        pairs: query i of a causal chunk of n equals a decode over the first
+        context_len - n + i + 1 tokens."""
+        kc, vc = self.cache()
+        out = []
+        for si, i in picks:
+            n = int(self.q_start[si + 1] - self.q_start[si])
+            ctx = self.lens[si] - n + i + 1 if self.causal else self.lens[si]
+            qrow = self.q[int(self.q_start[si]) + i][None]
+            out.append(oracle.paged_decode_attention(qrow, kc, vc, self.tables[si:si + 1], [ctx],
+                                                     self.scale)[0])
+        return np.stack(out)

@@ -1,0 +1,141 @@
+"""Chunked-prefill attention (tcgen05 + TMEM kernel) against the CPU oracle,
+and the continuous-batching mixed step (append, prefill chunks, decodes)."""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_52_gb300 import workloads as wl
+from parity import DecodeStepOracle, PrefillStepOracle, assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_52_gb300 import pagedkv
+    pagedkv.get_device_error(clear=True)
+    return pagedkv
+
+
+def _to_dev(w):
+    for n in ("k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "q_prefill", "q_start",
+              "prefill_tables", "prefill_lens", "q_decode", "decode_tables", "decode_lens"):
+        setattr(w, n, getattr(w, n).to(DEV))
+    return w
+
+
+def run_prefill(pk, w, causal=True, max_q_len=None):
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    out = torch.full((w.q_prefill.shape[0], w.q_prefill.shape[1], w.q_prefill.shape[2]),
+                     float("nan"), dtype=torch.float32, device=DEV)
+    mql = max(w.meta.get("chunks", [w.meta.get("chunk", 0)])) if max_q_len is None else max_q_len
+    pk.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables, w.prefill_lens,
+                               causal, w.scale, out=out, max_q_len=mql)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+PRIORS = [0, 40, 17, 300, 1000, 5]
+CHUNKS = [5, 130, 1, 129, 64, 16]
+SHAPES = [(8, 8, 128), (8, 4, 64), (16, 4, 128), (64, 8, 128), (32, 2, 64), (16, 16, 64)]
+
+
+@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunks_groups_and_ragged_lengths(pk, hq, hkv, d, causal):
+    w = wl.make_chunked_workload(hq, hkv, d, PRIORS, CHUNKS)
+    ref = PrefillStepOracle(w, range(len(CHUNKS)), causal=causal).output()
+    out, _, _ = run_prefill(pk, _to_dev(w), causal=causal)
+    assert_attention_close(out.cpu().numpy(), ref, f"{hq}/{hkv} d{d} causal={causal}")
+    assert pk.get_device_error() == 0
+
+
+def test_long_chunk_many_kv_tiles(pk):
+    # 2 chunks spanning several query tiles and ~40 K/V tiles (rescaling path)
+    w = wl.make_chunked_workload(64, 8, 128, [4000, 700], [300, 513], config_id=7)
+    ref = PrefillStepOracle(w, [0, 1]).output()
+    out, _, _ = run_prefill(pk, _to_dev(w))
+    assert_attention_close(out.cpu().numpy(), ref, "long chunk")
+
+
+def test_outlier_keys_in_prefill(pk):
+    # massive-activation K rows (x100) force many lazy-rescale events
+    w = wl.make_chunked_workload(64, 8, 128, [900, 64], [200, 77], config_id=8)
+    g = torch.Generator().manual_seed(5)
+    kc = w.k_cache.float()
+    rows = torch.randperm(kc.shape[0] * 16, generator=g)[:40]
+    kc.view(-1, 8, 128)[rows] *= 100.0
+    w.k_cache = kc.to(torch.bfloat16)
+    ref = PrefillStepOracle(w, [0, 1]).output()
+    out, _, _ = run_prefill(pk, _to_dev(w))
+    assert_attention_close(out.cpu().numpy(), ref, "outliers")
+
+
+def test_shared_prefix_mixed_step_small(pk):
+    w = _to_dev(wl.make_mixed_workload(num_prefill=3, num_decode=5, chunk=200,
+                                       prior_range=(0, 300), shared_prefix=64, decode_cap=700))
+    pre_ref = PrefillStepOracle(w, range(3)).output()
+    # decode oracle: the decodes' appended rows are the last 5 of k_new
+    out, kc, vc = run_prefill(pk, w, max_q_len=200)
+    assert_attention_close(out.cpu().numpy(), pre_ref, "mixed prefill")
+    dec = pk.paged_decode_attention(w.q_decode, kc, vc, w.decode_tables, w.decode_lens, w.scale,
+                                    max_context_len=max(w.meta["decode_lens"]))
+    torch.cuda.synchronize()
+    P = 3 * 200
+    dw = wl.DecodeWorkload("mixed decodes", w.q_decode, w.k_cache, w.v_cache, w.k_new[P:],
+                           w.v_new[P:], w.slot_mapping[P:], w.decode_tables, w.decode_lens,
+                           w.scale, {"lens": w.meta["decode_lens"]})
+    # the prefill chunks' rows are appended too; the decodes never read them
+    dref = DecodeStepOracle(dw, range(5)).output()
+    assert_attention_close(dec.cpu().numpy(), dref, "mixed decode")
+
+
+def test_repeatable_bitwise(pk):
+    w = _to_dev(wl.make_chunked_workload(64, 8, 128, [500, 0], [300, 77], config_id=9))
+    a, _, _ = run_prefill(pk, w)
+    b, _, _ = run_prefill(pk, w)
+    assert torch.equal(a, b)
+
+
+def test_bad_query_range_is_flagged(pk):
+    w = _to_dev(wl.make_chunked_workload(16, 4, 64, [10, 20], [8, 8], config_id=10))
+    pk.get_device_error(clear=True)
+    lens = w.prefill_lens.clone()
+    lens[1] = 4                       # chunk of 8 longer than its context
+    out = torch.zeros(w.q_prefill.shape, dtype=torch.float32, device=DEV)
+    pk.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache, w.prefill_tables,
+                               lens, True, w.scale, out=out, max_q_len=8)
+    assert pk.get_device_error(clear=True) & 0x10
+    assert torch.all(out[8:] == 0)    # the bad sequence is skipped
+    pk.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache, w.prefill_tables,
+                               w.prefill_lens, True, w.scale, out=out, max_q_len=4)
+    assert pk.get_device_error(clear=True) & 0x10
+
+
+def test_full_mixed_step_sampled(pk):
+    """The 70B-GQA continuous-batching step at full size: append 8 x 512 + 248
+    tokens, prefill the 8 chunks, decode the 248 sequences; sampled rows."""
+    w = wl.make_mixed_workload(device=DEV, gen_device=DEV)
+    pre = PrefillStepOracle(w, [0, 7])
+    P = 8 * 512
+    dw = wl.DecodeWorkload("mixed decodes", w.q_decode, w.k_cache, w.v_cache, w.k_new[P:],
+                           w.v_new[P:], w.slot_mapping[P:], w.decode_tables, w.decode_lens,
+                           w.scale, {"lens": w.meta["decode_lens"]})
+    dsamp = [0, 100, 247]
+    dor = DecodeStepOracle(dw, dsamp)
+    out, kc, vc = run_prefill(pk, w, max_q_len=512)
+    dec = pk.paged_decode_attention(w.q_decode, kc, vc, w.decode_tables, w.decode_lens, w.scale,
+                                    max_context_len=max(w.meta["decode_lens"]))
+    torch.cuda.synchronize()
+    picks = [(0, 0), (0, 1), (0, 255), (0, 511), (1, 0), (1, 300), (1, 511)]
+    ref_rows = pre.rows_output(picks)
+    qs = w.q_start.cpu().numpy()
+    got_rows = np.stack([out[int(qs[[0, 7][si]]) + i].cpu().numpy() for si, i in picks])
+    assert_attention_close(got_rows, ref_rows, "mixed prefill rows")
+    assert torch.isfinite(out).all()
+    assert_attention_close(dec[dsamp].cpu().numpy(), dor.output(), "mixed decodes")
+    assert pk.get_device_error() == 0
