@@ -54,6 +54,13 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true",
+                    help="skip the continuous-batching mixed-step measurement")
+    ap.add_argument("--mixed-steps", type=int, default=30)
+    ap.add_argument("--mixed-decodes", type=int, default=None,
+                    help="shrink the mixed step to this many decode sequences (profiling runs)")
+    ap.add_argument("--only-mixed", action="store_true",
+                    help="time only the mixed step (profiling runs)")
     return ap.parse_args()
 
 
@@ -215,6 +222,93 @@ def read_traffic(kernel_tag: str):
     return None, sha
 
 
+def prefill_flops(prefill_lens, chunks) -> int:
+    """Algorithmic FLOPs of causal chunked prefill: QK^T and PV, 2 flops per
+    multiply-add, over the keys each query sees (n * prior + n (n + 1) / 2 per
+    chunk), times heads and head size.  Masked work the kernel skips or
+    wastes is not counted."""
+    total = 0
+    for L, n in zip(prefill_lens, chunks):
+        prior = L - n
+        total += n * prior + n * (n + 1) // 2
+    return total
+
+
+def run_mixed(args, dev, pagedkv, E):
+    """The continuous-batching step at full size: append 8 x 512 + 248 new
+    tokens, prefill the 8 chunks (tcgen05), decode the 248 sequences."""
+    w = wl.make_mixed_workload(device=dev, gen_device=dev, num_decode=args.mixed_decodes)
+    kc, vc = w.k_cache, w.v_cache
+    chunk = w.meta["chunk"]
+    plens, dlens = w.meta["prefill_lens"], w.meta["decode_lens"]
+    hq, d, hkv = w.q_prefill.shape[1], w.q_prefill.shape[2], kc.shape[2]
+    max_d = max(dlens)
+    ws = pagedkv.decode_workspace(len(dlens), hq, hkv, d, max_d, dev)
+    pout = torch.empty(w.q_prefill.shape, dtype=torch.float32, device=dev)
+    dout = torch.empty(w.q_decode.shape, dtype=torch.float32, device=dev)
+
+    def append():
+        pagedkv.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+
+    def prefill():
+        pagedkv.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
+                                        w.prefill_lens, True, w.scale, out=pout,
+                                        max_q_len=chunk)
+
+    def decode():
+        pagedkv.paged_decode_attention(w.q_decode, kc, vc, w.decode_tables, w.decode_lens,
+                                       w.scale, out=dout, max_context_len=max_d, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        append(), prefill(), decode()
+    torch.cuda.synchronize()
+    K = args.mixed_steps
+    marks = [tuple(E(enable_timing=True) for _ in range(4)) for _ in range(K)]
+    for a, b, c, e in marks:
+        a.record()
+        append()
+        b.record()
+        prefill()
+        c.record()
+        decode()
+        e.record()
+    torch.cuda.synchronize()
+    ms = lambda i, j: sum(m[i].elapsed_time(m[j]) for m in marks) / K  # noqa: E731
+    t_step, t_app, t_pre, t_dec = ms(0, 3), ms(0, 1), ms(1, 2), ms(2, 3)
+    flops = prefill_flops(plens, [chunk] * len(plens)) * 4 * hq * d
+    row = 2 * hkv * d * 2
+    dec_logical = sum(dlens) * row
+    prefix_blocks = w.meta["shared_prefix"] // wl.BLOCK_SIZE
+    dec_unique = dec_logical - (len(dlens) - 1) * prefix_blocks * wl.BLOCK_SIZE * row
+    pre_kv = sum(plens) * row
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    tflops_peak = float(peaks.get("bf16_tflops", 1900.0))
+    hbm, _ = measured_peak()
+    t_roof = (dec_unique + pre_kv) / (hbm * 1e9) + flops / (tflops_peak * 1e12)
+    return {
+        "workload": w.name, "steps": K, "ms_per_step": round(t_step, 4),
+        "append_ms": round(t_app, 4), "prefill_ms": round(t_pre, 4),
+        "decode_ms": round(t_dec, 4),
+        "new_tokens": int(w.slot_mapping.shape[0]),
+        "prefill": {"kernel": "paged_prefill_kernel<128,8> (tcgen05)", "bound": "tensor",
+                    "flops_per_launch": flops, "achieved": round(flops / (t_pre / 1e3) / 1e12, 1),
+                    "peak": tflops_peak, "unit": "TFLOP/s",
+                    "frac": round(flops / (t_pre / 1e3) / 1e12 / tflops_peak, 4),
+                    "peak_kind": "measured bf16 burst"},
+        "decode": {"logical_kv_bytes": dec_logical, "unique_kv_bytes": dec_unique,
+                   "logical_GBps": round(dec_logical / (t_dec / 1e3) / 1e9, 1),
+                   "unique_GBps": round(dec_unique / (t_dec / 1e3) / 1e9, 1)},
+        "gpu_launches": K * (3 + (1 if ws is not None else 0)),
+        "roofline_step_ms": round(t_roof * 1e3, 4),
+        "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),
+    }
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
@@ -228,6 +322,9 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
+    if args.only_mixed:
+        print(json.dumps({"mixed_step": run_mixed(args, dev, pagedkv, torch.cuda.Event)}))
+        return
     spec = wl.DECODE_SPECS[args.workload]
     w = wl.make_decode_workload(spec, device=dev, gen_device=dev,
                                 num_seqs_override=args.num_seqs or None)
@@ -347,6 +444,9 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
+    if not args.no_mixed:
+        del host, devb
+        line["mixed_step"] = run_mixed(args, dev, pagedkv, E)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         _, info = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = info
