@@ -12,19 +12,24 @@
 // a running max and sum.
 //
 // Design (GB300):
-//  * one CTA per (128-row query tile, sequence x KV head).  The 128 rows are
-//    128/G query tokens x the G heads of the GQA group (rows token-major), so
-//    one TMA box brings the tile in and every K/V tile serves all G heads.
-//    Tiles are launched longest-first (the last tiles of a chunk see the most
-//    keys).
-//  * warp roles: warps 0-3 softmax / correction / epilogue (thread = row =
-//    TMEM lane), warp 4 TMA producer (32 lanes issue the 32 per-block boxes
-//    of a K+V tile), warp 5 MMA issuer (one thread).
-//  * S = Q K^T (M=128, N=128, K=d) into one of two TMEM S buffers; the MMA
-//    warp issues S for tile j+2 while softmax works on tile j+1, then
-//    O += P V (M=128, N=d, K=128) into a TMEM O accumulator.  Q, K, P are
-//    K-major 128-byte-swizzled operands; V is the MN-major operand straight
-//    from the pool layout, so no transpose pass is needed.
+//  * one CTA per (two 128-row query tiles, sequence x KV head).  The 128 rows
+//    of a tile are 128/G query tokens x the G heads of the GQA group (rows
+//    token-major), so one TMA box brings a tile in and every K/V tile serves
+//    all G heads of both tiles.  CTAs are launched longest-first (the last
+//    tiles of a chunk see the most keys).
+//  * warp roles: warps 0-3 and 4-7 are the softmax / correction / epilogue
+//    warpgroups of Q tiles 0 and 1 (thread = row = TMEM lane), warp 8 the TMA
+//    producer (its lanes issue the 32 per-page boxes of a K+V tile), warp 9
+//    the MMA issuer (one thread).
+//  * per Q tile t, tensor memory holds S_t = Q_t K^T (128 fp32 columns) and
+//    O_t (d columns).  The softmax overwrites S_t with P_t and the PV product
+//    reads P_t straight from tensor memory (A operand in TMEM); V is the
+//    MN-major shared-memory operand straight from the pool layout, so no
+//    transpose pass and no shared-memory P buffer are needed.
+//  * ping-pong: the MMA thread issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+//    the tensor core works on one tile while the other tile's softmax runs.
+//    Consecutive MMAs of the one issuing thread execute in order, which is
+//    what lets S_t(j+1) overwrite the P_t(j) that PV_t(j) reads.
 //  * P enters the PV product as bf16 hi + bf16 lo (two MMAs per k-step), so
 //    its rounding error is ~2^-17 relative instead of bf16's 2^-9 -- needed
 //    for rows that see only a few keys, where one rounded weight moves the
@@ -45,28 +50,27 @@ namespace pkv {
 
 static __device__ unsigned g_prefill_error = 0;
 
-constexpr int kPfRows = 128;          // query rows per CTA (tokens x heads)
+constexpr int kPfRows = 128;          // query rows per Q tile (tokens x heads)
+constexpr int kPfQTiles = 2;          // Q tiles per CTA, one softmax warpgroup each
 constexpr int kPfKvTile = 128;        // keys per K/V tile (8 pages of 16)
 constexpr int kPfStages = 2;          // K/V tile ring
-constexpr int kPfThreads = 192;       // 4 softmax warps + TMA warp + MMA warp
-constexpr int kPfProducerWarp = 4;
-constexpr int kPfMmaWarp = 5;
-constexpr uint32_t kPfTmemCols = 512; // S0 | S1 | O
+constexpr int kPfThreads = 320;       // 2 softmax warpgroups + TMA warp + MMA warp
+constexpr int kPfProducerWarp = 8;
+constexpr int kPfMmaWarp = 9;
+constexpr uint32_t kPfTmemCols = 512; // per Q tile t: S_t / P_t at 256 t, O_t at 256 t + 128
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > x256
 
 template <int D>
 struct PrefillSmem {
   static constexpr int kHalf = kPfRows * 128;                // 128 rows x 64 bf16 (16 KB)
-  static constexpr int kQBytes = (D / 64) * kHalf;
+  static constexpr int kQTileBytes = (D / 64) * kHalf;
   static constexpr int kTileBytes = (D / 64) * kHalf;        // K or V: 128 keys x D
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kPBytes = 2 * kHalf;                  // P: 128 rows x 128 keys bf16
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + kQBytes;
-  static constexpr int kPOff = kStageOff + kPfStages * kStageBytes;  // P hi, then P lo
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], p_full, o_done, drain
-  static constexpr int kNumBars = 10;
+  static constexpr int kStageOff = kQOff + kPfQTiles * kQTileBytes;
+  static constexpr int kBarOff = kStageOff + kPfStages * kStageBytes;
+  // q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 12;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kUsed = kMiscOff + 16 + 1024;          // + alignment slack
   // One CTA per SM: it holds all 512 TMEM columns.
@@ -74,8 +78,8 @@ struct PrefillSmem {
   static_assert(kSmemBytes <= 232448, "prefill tile does not fit in shared memory");
 };
 
-enum PfBar { kQFull = 0, kKvFull0 = 1, kKvEmpty0 = 3, kSFull0 = 5, kPFull = 7, kODone = 8,
-             kDrain = 9 };
+enum PfBar { kQFull = 0, kKvFull0 = 1, kKvEmpty0 = 3, kSFull0 = 5, kPFull0 = 7, kODone0 = 9,
+             kDrain = 11 };
 
 struct PrefillParams {
   const int32_t* q_start;
@@ -107,7 +111,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   using L = PrefillSmem<D>;
-  constexpr int TPT = kPfRows / G;  // query tokens per tile
+  constexpr int TPT = kPfRows / G;          // query tokens per Q tile
+  constexpr int TPC = kPfQTiles * TPT;      // query tokens per CTA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -120,22 +125,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int pair = blockIdx.y;
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
-  const int tile = int(gridDim.x) - 1 - int(blockIdx.x);  // longest-first
+  const int cta_tile = int(gridDim.x) - 1 - int(blockIdx.x);  // longest-first
 
   // ---- per-CTA bounds (uniform over the CTA, so early exits are safe)
   const int qs = __ldg(p.q_start + seq), qe = __ldg(p.q_start + seq + 1);
   const int ctx = __ldg(p.context_lens + seq);
   const int n = qe - qs;
-  if (qs < 0 || n < 0 || qe > p.total_q || n > ctx ||
-      ctx > p.max_blocks_per_seq * 16) {
-    if (tile == 0 && threadIdx.x == 0) atomicOr(&g_prefill_error, kErrBadQueryRange);
+  if (qs < 0 || n < 0 || qe > p.total_q || n > ctx || ctx > p.max_blocks_per_seq * 16) {
+    if (cta_tile == 0 && threadIdx.x == 0) atomicOr(&g_prefill_error, kErrBadQueryRange);
     return;
   }
-  if (n > p.max_q_len && tile == 0 && threadIdx.x == 0)
-    atomicOr(&g_prefill_error, kErrBadQueryRange);  // tiles past the grid are not computed
-  const int t0 = tile * TPT;
+  if (n > p.max_q_len && cta_tile == 0 && threadIdx.x == 0)
+    atomicOr(&g_prefill_error, kErrBadQueryRange);  // tokens past the grid are not computed
+  const int t0 = cta_tile * TPC;
   if (t0 >= n) return;
-  const int tok_valid = min(TPT, n - t0);
+  const int tok_valid = min(TPC, n - t0);
   const int kv_end = p.causal ? (ctx - n + t0 + tok_valid) : ctx;  // keys [0, kv_end)
   const int ntiles = (kv_end + kPfKvTile - 1) / kPfKvTile;
   const int nblk = (ctx + 15) / 16;
@@ -143,13 +147,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // ---- set-up: barriers (producer lane 0), tensor memory (warp 0)
   if (warp == kPfProducerWarp && lane == 0) {
     mbar_init(bars + 8 * kQFull, 1);
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bars + 8 * (kKvFull0 + s), 1);
       mbar_init(bars + 8 * (kKvEmpty0 + s), 1);
       mbar_init(bars + 8 * (kSFull0 + s), 1);
+      mbar_init(bars + 8 * (kPFull0 + s), 4);
+      mbar_init(bars + 8 * (kODone0 + s), 1);
     }
-    mbar_init(bars + 8 * kPFull, 4);
-    mbar_init(bars + 8 * kODone, 1);
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -162,8 +166,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t q_smem = sbase + L::kQOff;
-  const uint32_t p_smem = sbase + L::kPOff;
 
   if (warp == kPfProducerWarp) {
     // ================= TMA producer =================
@@ -172,10 +174,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
-      mbar_arrive_expect_tx(bars + 8 * kQFull, L::kQBytes);
+      mbar_arrive_expect_tx(bars + 8 * kQFull, kPfQTiles * L::kQTileBytes);
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_load_3d(q_smem + h * L::kHalf, &tmap_q, bars + 8 * kQFull, h * 64, kvh * G, qs + t0);
+      for (int t = 0; t < kPfQTiles; ++t)
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sbase + L::kQOff + t * L::kQTileBytes + h * L::kHalf, &tmap_q,
+                      bars + 8 * kQFull, h * 64, kvh * G, qs + t0 + t * TPT);
       issued_q = 1;
     }
     const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
@@ -222,44 +227,68 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, kPfKvTile, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = pf_wait(bars + 8 * kQFull, 0, abort_flag);
-      // S_j = Q K_j^T into TMEM columns [128 (j % 2), +128)
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kPfStages;
-        if (!pf_wait(bars + 8 * (kKvFull0 + st), (j / kPfStages) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t k_smem = sbase + L::kStageOff + st * L::kStageBytes;
+      // S_t(j) = Q_t K_j^T into TMEM columns [256 t, 256 t + 128)
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_smem = sbase + L::kQOff + t * L::kQTileBytes;
+        const uint32_t k_smem = sbase + L::kStageOff + (j % kPfStages) * L::kStageBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * L::kHalf + (k & 3) * 32;
-          umma_bf16(tmem + (j & 1) * 128, smem_desc_sw128(q_smem + off, 16, 1024),
+          umma_bf16(tmem + t * 256, smem_desc_sw128(q_smem + off, 16, 1024),
                     smem_desc_sw128(k_smem + off, 16, 1024), kIdescS, k > 0);
         }
-        umma_commit(bars + 8 * (kSFull0 + (j & 1)));
-        return true;
+        umma_commit(bars + 8 * (kSFull0 + t));
       };
-      for (int j = 0; ok && j < ntiles && j < 2; ++j) ok = issue_s(j);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (!pf_wait(bars + 8 * kPFull, j & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // O += P_j V_j: P K-major (rows x keys), V MN-major (keys x d) from the pool layout
+      // O_t += P_t(j) V_j: P (bf16 hi, lo) read from TMEM over S_t's columns,
+      // V the MN-major operand (keys x d) straight from the pool layout
+      auto issue_pv = [&](int t, int j) {
         const uint32_t v_smem = sbase + L::kStageOff + (j % kPfStages) * L::kStageBytes +
                                 L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kPfKvTile / 16; ++k) {
-          const uint32_t poff = (k >> 2) * L::kHalf + (k & 3) * 32;
           const uint64_t vdesc = smem_desc_sw128(v_smem + k * 2048, L::kHalf, 1024);
-          umma_bf16(tmem + 256, smem_desc_sw128(p_smem + poff, 16, 1024), vdesc, kIdescPV,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          umma_bf16(tmem + 256, smem_desc_sw128(p_smem + L::kPBytes + poff, 16, 1024), vdesc,
-                    kIdescPV, 1u);
+          // keys [16 k, 16 k + 16): hi in column 64 (k / 4) + 8 (k % 4), lo 32 columns on
+          const uint32_t a_hi = tmem + t * 256 + 64 * (k >> 2) + 8 * (k & 3);
+          umma_bf16_ts(tmem + t * 256 + 128, a_hi, vdesc, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + t * 256 + 128, a_hi + 32, vdesc, kIdescPV, 1u);
         }
-        umma_commit(bars + 8 * (kKvEmpty0 + (j % kPfStages)));
-        umma_commit(bars + 8 * kODone);
-        if (j + 2 < ntiles) ok = issue_s(j + 2);
+        umma_commit(bars + 8 * (kODone0 + t));
+      };
+      auto kv_ready = [&](int j) {
+        const bool r = pf_wait(bars + 8 * (kKvFull0 + j % kPfStages), (j / kPfStages) & 1,
+                               abort_flag);
+        if (r) tc_fence_after();
+        return r;
+      };
+      bool ok = pf_wait(bars + 8 * kQFull, 0, abort_flag) && kv_ready(0);
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      // Ping-pong: the tensor core works on one Q tile while the other's softmax runs.
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (!pf_wait(bars + 8 * kPFull0, j & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, j);
+        const bool more = j + 1 < ntiles;
+        if (more) {
+          if (!kv_ready(j + 1)) {
+            ok = false;
+            break;
+          }
+          issue_s(0, j + 1);
+        }
+        if (!pf_wait(bars + 8 * (kPFull0 + 1), j & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(bars + 8 * (kKvEmpty0 + j % kPfStages));
+        if (more) issue_s(1, j + 1);
       }
       if (!ok) pf_abort(abort_flag);
       // every MMA issued has completed before tensor memory is released
@@ -268,103 +297,99 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
     __syncwarp();
   } else {
-    // ================= softmax / correction / epilogue (warps 0-3) =================
-    const int r = warp * 32 + lane;  // row = TMEM lane
+    // ============ softmax / correction / epilogue: warpgroup wg owns Q tile wg ============
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // row of the Q tile = TMEM lane
     const int token = r / G, head = r - (r / G) * G;
-    const int tok = t0 + token;
+    const int tok = t0 + wg * TPT + token;
     const bool valid_row = tok < n;
     // rows past the chunk compute finite garbage over the whole context and are not stored
     const int limit = (p.causal && valid_row) ? (ctx - n + tok) : (ctx - 1);
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+    const uint32_t s_col = wg * 256, o_col = wg * 256 + 128;
+    const uint32_t s_full = bars + 8 * (kSFull0 + wg), p_full = bars + 8 * (kPFull0 + wg);
+    const uint32_t o_done = bars + 8 * (kODone0 + wg);
     float m_used = -INFINITY, lsum = 0.f;
     bool ok = true;
-    int j = 0;
-    for (; j < ntiles; ++j) {
-      ok = __all_sync(0xffffffffu, pf_wait(bars + 8 * (kSFull0 + (j & 1)), (j >> 1) & 1,
-                                           abort_flag));
+    for (int j = 0; j < ntiles; ++j) {
+      ok = __all_sync(0xffffffffu, pf_wait(s_full, j & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + (j & 1) * 128 + c * 32, s[c]);
-      tmem_wait_ld();
+      // pass 1: row max of the scaled, masked scores
       const int key0 = j * kPfKvTile;
       const bool need_mask = key0 + kPfKvTile - 1 > limit;
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(lane_base + s_col + c * 32, v);
+        tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float x = s[c][i] * p.scale_log2;
-          if (need_mask && key0 + c * 32 + i > limit) x = -INFINITY;
-          s[c][i] = x;
+          const float x = (need_mask && key0 + c * 32 + i > limit) ? -INFINITY
+                                                                    : v[i] * p.scale_log2;
           mx = fmaxf(mx, x);
         }
-      if (j > 0) {
-        // PV_{j-1} done: the P buffer is free and O is stable
-        ok = __all_sync(0xffffffffu, pf_wait(bars + 8 * kODone, (j - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
       }
       const bool resc = mx > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, resc)) {
         const float m_new = resc ? mx : m_used;
         const float alpha = ex2(m_used - m_new);  // 0 when m_used is -inf, 1 when unchanged
         if (j > 0) {
+          // PV_{j-1} must be done before O is rescaled
+          ok = __all_sync(0xffffffffu, pf_wait(o_done, (j - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tmem_ld32(lane_base + 256 + c * 32, o);
+            tmem_ld32(lane_base + o_col + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_base + 256 + c * 32, o);
+            tmem_st32(lane_base + o_col + c * 32, o);
           }
-          tmem_wait_st();
         }
         lsum *= alpha;
         m_used = m_new;
       }
-      // P = 2^(x - m_used) as bf16 into the K-major swizzled P tile
+      // pass 2: P = 2^(x - m_used) for 64 keys at a time, written over the
+      // columns those keys' scores just vacated: bf16 hi of keys [64 g, 64 g + 64)
+      // in columns [64 g, 64 g + 32), the bf16 residual lo in [64 g + 32, 64 g + 64),
+      // two keys per column.
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int g = 0; g < 2; ++g) {
+        float va[32], vb[32];
+        tmem_ld32(lane_base + s_col + 64 * g, va);
+        tmem_ld32(lane_base + s_col + 64 * g + 32, vb);
+        tmem_wait_ld();
+        uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            e[u] = ex2(s[c][g8 * 8 + u] - m_used);
-            lsum += e[u];
-          }
-          const int key = c * 32 + g8 * 8;  // first of 8 keys in this 16-byte chunk
-          const int half = key >> 6, chunk = (key & 63) >> 3;
-          const uint32_t addr = p_smem + half * L::kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
-          uint32_t w[4], wl[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            w[u] = pack_bf16x2(e[2 * u], e[2 * u + 1]);
-            wl[u] = pack_bf16x2(e[2 * u] - bf16_lo_to_f32(w[u]),
-                                e[2 * u + 1] - bf16_hi_to_f32(w[u]));
-          }
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr + L::kPBytes),
-                       "r"(wl[0]), "r"(wl[1]), "r"(wl[2]), "r"(wl[3])
-                       : "memory");
+        for (int u = 0; u < 32; ++u) {
+          const int kk = 2 * u;  // key within the group
+          const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+          const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+          const int key = key0 + 64 * g + kk;
+          const float x0 = (need_mask && key > limit) ? -INFINITY : s0 * p.scale_log2;
+          const float x1 = (need_mask && key + 1 > limit) ? -INFINITY : s1 * p.scale_log2;
+          const float e0 = ex2(x0 - m_used), e1 = ex2(x1 - m_used);
+          lsum += e0 + e1;
+          hi[u] = pack_bf16x2(e0, e1);
+          lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
         }
+        tmem_st32u(lane_base + s_col + 64 * g, hi);
+        tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * kPFull);
+      if (lane == 0) mbar_arrive(p_full);
     }
     if (!ok) {
       if (lane == 0) pf_abort(abort_flag);
     } else {
       // epilogue: wait for the last PV, then out = O / l
-      ok = __all_sync(0xffffffffu,
-                      pf_wait(bars + 8 * kODone, (ntiles - 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, pf_wait(o_done, (ntiles - 1) & 1, abort_flag));
       if (!ok) {
         if (lane == 0) pf_abort(abort_flag);
       } else {
@@ -374,7 +399,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tmem_ld32(lane_base + 256 + c * 32, o);
+          tmem_ld32(lane_base + o_col + c * 32, o);
           tmem_wait_ld();
           if (valid_row) {
 #pragma unroll
@@ -409,7 +434,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap*
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((prm.max_q_len + TPT - 1) / TPT, prm.num_seqs * prm.kv_heads);
+  constexpr int TPC = kPfQTiles * TPT;
+  dim3 grid((prm.max_q_len + TPC - 1) / TPC, prm.num_seqs * prm.kv_heads);
   paged_prefill_kernel<D, G><<<grid, kPfThreads, L::kSmemBytes, stream>>>(*tq, *tk, *tv, prm);
   return cudaGetLastError();
 }
