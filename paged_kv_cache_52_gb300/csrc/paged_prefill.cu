@@ -315,21 +315,42 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       ok = __all_sync(0xffffffffu, pf_wait(s_full, j & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // pass 1: row max of the scaled, masked scores
+      // pass 1: row max.  On unmasked tiles the max is taken over the raw
+      // scores and scaled once (scale > 0 keeps the order; scale < 0 flips it).
       const int key0 = j * kPfKvTile;
       const bool need_mask = key0 + kPfKvTile - 1 > limit;
-      float mx = -INFINITY;
+      float mx;
+      {
+        float va[32], vb[32];
+        // the extreme that becomes the max after scaling: max for scale >= 0,
+        // min (taken as the max of the negated scores) for scale < 0
+        const bool neg = p.scale_log2 < 0.f;  // uniform over the CTA
+        float ext = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(lane_base + s_col + c * 32, v);
-        tmem_wait_ld();
+        for (int c = 0; c < 4; c += 2) {
+          tmem_ld32(lane_base + s_col + c * 32, va);
+          tmem_ld32(lane_base + s_col + c * 32 + 32, vb);
+          tmem_wait_ld();
+          if (neg) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = (need_mask && key0 + c * 32 + i > limit) ? -INFINITY
-                                                                    : v[i] * p.scale_log2;
-          mx = fmaxf(mx, x);
+            for (int i = 0; i < 32; ++i) {
+              va[i] = -va[i];
+              vb[i] = -vb[i];
+            }
+          }
+          if (!need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ext = fmaxf(ext, fmaxf(va[i], vb[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (key0 + c * 32 + i <= limit) ext = fmaxf(ext, va[i]);
+              if (key0 + c * 32 + 32 + i <= limit) ext = fmaxf(ext, vb[i]);
+            }
+          }
         }
+        // a tile past the row's limit leaves the max at -inf and its P all zeros
+        mx = ext == -INFINITY ? -INFINITY : ext * fabsf(p.scale_log2);
       }
       const bool resc = mx > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, resc)) {
@@ -364,18 +385,32 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_ld32(lane_base + s_col + 64 * g + 32, vb);
         tmem_wait_ld();
         uint32_t hi[32], lo[32];
+        const float neg_m = -m_used;
+        if (!need_mask) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int kk = 2 * u;  // key within the group
-          const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
-          const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
-          const int key = key0 + 64 * g + kk;
-          const float x0 = (need_mask && key > limit) ? -INFINITY : s0 * p.scale_log2;
-          const float x1 = (need_mask && key + 1 > limit) ? -INFINITY : s1 * p.scale_log2;
-          const float e0 = ex2(x0 - m_used), e1 = ex2(x1 - m_used);
-          lsum += e0 + e1;
-          hi[u] = pack_bf16x2(e0, e1);
-          lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
+          for (int u = 0; u < 32; ++u) {
+            const int kk = 2 * u;  // key within the group
+            const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+            const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+            const float e0 = ex2(fmaf(s0, p.scale_log2, neg_m));
+            const float e1 = ex2(fmaf(s1, p.scale_log2, neg_m));
+            lsum += e0 + e1;
+            hi[u] = pack_bf16x2(e0, e1);
+            lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const int kk = 2 * u;
+            const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+            const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+            const int key = key0 + 64 * g + kk;
+            const float e0 = key <= limit ? ex2(fmaf(s0, p.scale_log2, neg_m)) : 0.f;
+            const float e1 = key + 1 <= limit ? ex2(fmaf(s1, p.scale_log2, neg_m)) : 0.f;
+            lsum += e0 + e1;
+            hi[u] = pack_bf16x2(e0, e1);
+            lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
+          }
         }
         tmem_st32u(lane_base + s_col + 64 * g, hi);
         tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
