@@ -71,6 +71,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (a control all-reduce; the data path has none)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms / 1e3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -378,15 +393,11 @@ def run_ours(args):
         end.record()
         torch.cuda.synchronize()
     barrier()
-    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(start.elapsed_time(end), dev)
     decode_ms = sum(b.elapsed_time(c) for _, b, c in marks) / K
     append_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / K
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / K
-    value = world * kv_bytes * K / (total_ms / 1e3) / 1e9
+    value = whole_job_gbps(kv_bytes, K, world, total_ms)
 
     # End to end through the public API: this step's inputs from pinned host
     # memory, the step, and the output read back, every step.
@@ -414,12 +425,8 @@ def run_ours(args):
         e2e_step()
     e2.record()
     torch.cuda.synchronize()
-    e2e_ms = s2.elapsed_time(e2)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * kv_bytes * K / (e2e_ms / 1e3) / 1e9
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+    e2e_value = whole_job_gbps(kv_bytes, K, world, e2e_ms)
 
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (decode_ms / 1e3) / 1e9
