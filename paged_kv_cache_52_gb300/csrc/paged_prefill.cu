@@ -18,9 +18,12 @@
 //    all G heads of both tiles.  CTAs are launched longest-first (the last
 //    tiles of a chunk see the most keys).
 //  * warp roles: warps 0-3 and 4-7 are the softmax / correction / epilogue
-//    warpgroups of Q tiles 0 and 1 (thread = row = TMEM lane), warp 8 the TMA
-//    producer (its lanes issue the 32 per-page boxes of a K+V tile), warp 9
-//    the MMA issuer (one thread).
+//    warpgroups of Q tiles 0 and 1 (thread = row = TMEM lane), warp 9 the MMA
+//    issuer (one thread), warps 8 and 10 the TMA producers of Q + the K ring
+//    (3 stages) and of the V ring (2 stages); their lanes issue the per-page
+//    boxes of a 128-key tile.  A K tile is released as soon as both S
+//    products have read it, a V tile after both PV products, so each ring
+//    refills as early as the MMA order allows.
 //  * per Q tile t, tensor memory holds S_t = Q_t K^T (128 fp32 columns) and
 //    O_t (d columns).  The softmax overwrites S_t with P_t and the PV product
 //    reads P_t straight from tensor memory (A operand in TMEM); V is the
@@ -53,10 +56,12 @@ static __device__ unsigned g_prefill_error = 0;
 constexpr int kPfRows = 128;          // query rows per Q tile (tokens x heads)
 constexpr int kPfQTiles = 2;          // Q tiles per CTA, one softmax warpgroup each
 constexpr int kPfKvTile = 128;        // keys per K/V tile (8 pages of 16)
-constexpr int kPfStages = 2;          // K/V tile ring
-constexpr int kPfThreads = 320;       // 2 softmax warpgroups + TMA warp + MMA warp
-constexpr int kPfProducerWarp = 8;
+constexpr int kPfKStages = 3;         // K tile ring (freed once both S products are done)
+constexpr int kPfVStages = 2;         // V tile ring (freed once both PV products are done)
+constexpr int kPfThreads = 352;       // 2 softmax warpgroups + K/Q TMA + MMA + V TMA warps
+constexpr int kPfProducerWarp = 8;    // loads Q and K
 constexpr int kPfMmaWarp = 9;
+constexpr int kPfVProducerWarp = 10;  // loads V
 constexpr uint32_t kPfTmemCols = 512; // per Q tile t: S_t / P_t at 256 t, O_t at 256 t + 128
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > x256
 
@@ -65,12 +70,12 @@ struct PrefillSmem {
   static constexpr int kHalf = kPfRows * 128;                // 128 rows x 64 bf16 (16 KB)
   static constexpr int kQTileBytes = (D / 64) * kHalf;
   static constexpr int kTileBytes = (D / 64) * kHalf;        // K or V: 128 keys x D
-  static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + kPfQTiles * kQTileBytes;
-  static constexpr int kBarOff = kStageOff + kPfStages * kStageBytes;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 12;
+  static constexpr int kKOff = kQOff + kPfQTiles * kQTileBytes;
+  static constexpr int kVOff = kKOff + kPfKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kPfVStages * kTileBytes;
+  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 18;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kUsed = kMiscOff + 16 + 1024;          // + alignment slack
   // One CTA per SM: it holds all 512 TMEM columns.
@@ -78,8 +83,8 @@ struct PrefillSmem {
   static_assert(kSmemBytes <= 232448, "prefill tile does not fit in shared memory");
 };
 
-enum PfBar { kQFull = 0, kKvFull0 = 1, kKvEmpty0 = 3, kSFull0 = 5, kPFull0 = 7, kODone0 = 9,
-             kDrain = 11 };
+enum PfBar { kQFull = 0, kKFull0 = 1, kKEmpty0 = 4, kVFull0 = 7, kVEmpty0 = 9, kSFull0 = 11,
+             kPFull0 = 13, kODone0 = 15, kDrain = 17 };
 
 struct PrefillParams {
   const int32_t* q_start;
@@ -147,9 +152,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // ---- set-up: barriers (producer lane 0), tensor memory (warp 0)
   if (warp == kPfProducerWarp && lane == 0) {
     mbar_init(bars + 8 * kQFull, 1);
+    for (int s = 0; s < kPfKStages; ++s) {
+      mbar_init(bars + 8 * (kKFull0 + s), 1);
+      mbar_init(bars + 8 * (kKEmpty0 + s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bars + 8 * (kKvFull0 + s), 1);
-      mbar_init(bars + 8 * (kKvEmpty0 + s), 1);
+      mbar_init(bars + 8 * (kVFull0 + s), 1);
+      mbar_init(bars + 8 * (kVEmpty0 + s), 1);
       mbar_init(bars + 8 * (kSFull0 + s), 1);
       mbar_init(bars + 8 * (kPFull0 + s), 4);
       mbar_init(bars + 8 * (kODone0 + s), 1);
@@ -167,13 +176,18 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kPfProducerWarp) {
-    // ================= TMA producer =================
-    int issued_q = 0, issued[kPfStages] = {0, 0};
-    if (lane == 0) {
+  if (warp == kPfProducerWarp || warp == kPfVProducerWarp) {
+    // ============ TMA producers: warp 8 loads Q and the K ring, warp 10 the V ring ============
+    const bool is_v = warp == kPfVProducerWarp;
+    const int stages = is_v ? kPfVStages : kPfKStages;
+    const uint32_t ring = sbase + (is_v ? L::kVOff : L::kKOff);
+    const uint32_t full0 = bars + 8 * (is_v ? kVFull0 : kKFull0);
+    const uint32_t empty0 = bars + 8 * (is_v ? kVEmpty0 : kKEmpty0);
+    const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+    int issued_q = 0, issued[kPfKStages] = {0, 0, 0};
+    if (!is_v && lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
       mbar_arrive_expect_tx(bars + 8 * kQFull, kPfQTiles * L::kQTileBytes);
 #pragma unroll
       for (int t = 0; t < kPfQTiles; ++t)
@@ -183,24 +197,23 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       bars + 8 * kQFull, h * 64, kvh * G, qs + t0 + t * TPT);
       issued_q = 1;
     }
+    if (is_v && lane == 0) tma_prefetch_desc(&tmap_v);
     const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
-    constexpr int kLoads = 2 * 8 * (D / 64);  // K and V, 8 pages, D/64 column halves
+    constexpr int kLoads = 8 * (D / 64);  // 8 pages x D/64 column halves
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kPfStages;
-      if (j >= kPfStages) {
+      const int st = j % stages;
+      if (j >= stages) {
         const bool ok = __all_sync(0xffffffffu,
-                                   pf_wait(bars + 8 * (kKvEmpty0 + st), ((j / kPfStages) - 1) & 1,
-                                           abort_flag));
+                                   pf_wait(empty0 + 8 * st, ((j / stages) - 1) & 1, abort_flag));
         if (!ok) {
           if (lane == 0) pf_abort(abort_flag);
           break;
         }
       }
-      if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (kKvFull0 + st), L::kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, L::kTileBytes);
       __syncwarp();
       if (lane < kLoads) {
-        const int kv = lane / (8 * (D / 64));
-        const int b = (lane / (D / 64)) & 7;
+        const int b = lane / (D / 64);
         const int h = lane % (D / 64);
         const int blk = j * 8 + b;
         int id = -1;  // pages past the context: the box is out of bounds and reads zeros
@@ -208,18 +221,17 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           id = __ldg(table + blk);
           if (id < 0 || id >= p.num_blocks) atomicOr(&g_prefill_error, kErrBadBlockId);
         }
-        const uint32_t dst = sbase + L::kStageOff + st * L::kStageBytes + kv * L::kTileBytes +
-                             h * L::kHalf + b * 2048;
-        tma_load_4d(dst, kv ? &tmap_v : &tmap_k, bars + 8 * (kKvFull0 + st), h * 64, kvh, 0, id);
+        tma_load_4d(ring + st * L::kTileBytes + h * L::kHalf + b * 2048, map, full0 + 8 * st,
+                    h * 64, kvh, 0, id);
       }
-      if (lane == 0) issued[st] = j / kPfStages + 1;
+      if (lane == 0) issued[st] = j / stages + 1;
     }
     // Drain: wait (bounded, regardless of aborts) for every phase issued, so no
     // copy lands in shared memory after the CTA exits.
     if (lane == 0 && *abort_flag) {
       if (issued_q) (void)mbar_wait_bounded(bars + 8 * kQFull, 0);
-      for (int s = 0; s < kPfStages; ++s)
-        if (issued[s] > 0) (void)mbar_wait_bounded(bars + 8 * (kKvFull0 + s), (issued[s] - 1) & 1);
+      for (int s = 0; s < stages; ++s)
+        if (issued[s] > 0) (void)mbar_wait_bounded(full0 + 8 * s, (issued[s] - 1) & 1);
     }
   }
   else if (warp == kPfMmaWarp) {
@@ -230,7 +242,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // S_t(j) = Q_t K_j^T into TMEM columns [256 t, 256 t + 128)
       auto issue_s = [&](int t, int j) {
         const uint32_t q_smem = sbase + L::kQOff + t * L::kQTileBytes;
-        const uint32_t k_smem = sbase + L::kStageOff + (j % kPfStages) * L::kStageBytes;
+        const uint32_t k_smem = sbase + L::kKOff + (j % kPfKStages) * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * L::kHalf + (k & 3) * 32;
@@ -242,8 +254,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // O_t += P_t(j) V_j: P (bf16 hi, lo) read from TMEM over S_t's columns,
       // V the MN-major operand (keys x d) straight from the pool layout
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_smem = sbase + L::kStageOff + (j % kPfStages) * L::kStageBytes +
-                                L::kTileBytes;
+        const uint32_t v_smem = sbase + L::kVOff + (j % kPfVStages) * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kPfKvTile / 16; ++k) {
           const uint64_t vdesc = smem_desc_sw128(v_smem + k * 2048, L::kHalf, 1024);
@@ -254,20 +265,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         umma_commit(bars + 8 * (kODone0 + t));
       };
-      auto kv_ready = [&](int j) {
-        const bool r = pf_wait(bars + 8 * (kKvFull0 + j % kPfStages), (j / kPfStages) & 1,
-                               abort_flag);
+      auto ready = [&](uint32_t full0, int stages, int j) {
+        const bool r = pf_wait(full0 + 8 * (j % stages), (j / stages) & 1, abort_flag);
         if (r) tc_fence_after();
         return r;
       };
-      bool ok = pf_wait(bars + 8 * kQFull, 0, abort_flag) && kv_ready(0);
+      const uint32_t kfull0 = bars + 8 * kKFull0, vfull0 = bars + 8 * kVFull0;
+      bool ok = pf_wait(bars + 8 * kQFull, 0, abort_flag) && ready(kfull0, kPfKStages, 0);
       if (ok) {
         issue_s(0, 0);
         issue_s(1, 0);
+        umma_commit(bars + 8 * kKEmpty0);  // K_0 free once both S products are done
       }
       // Ping-pong: the tensor core works on one Q tile while the other's softmax runs.
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (!pf_wait(bars + 8 * kPFull0, j & 1, abort_flag)) {
+        if (!pf_wait(bars + 8 * kPFull0, j & 1, abort_flag) || !ready(vfull0, kPfVStages, j)) {
           ok = false;
           break;
         }
@@ -275,7 +287,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         issue_pv(0, j);
         const bool more = j + 1 < ntiles;
         if (more) {
-          if (!kv_ready(j + 1)) {
+          if (!ready(kfull0, kPfKStages, j + 1)) {
             ok = false;
             break;
           }
@@ -287,8 +299,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         tc_fence_after();
         issue_pv(1, j);
-        umma_commit(bars + 8 * (kKvEmpty0 + j % kPfStages));
-        if (more) issue_s(1, j + 1);
+        umma_commit(bars + 8 * (kVEmpty0 + j % kPfVStages));  // V_j free after both PV
+        if (more) {
+          issue_s(1, j + 1);
+          umma_commit(bars + 8 * (kKEmpty0 + (j + 1) % kPfKStages));  // K_{j+1} free
+        }
       }
       if (!ok) pf_abort(abort_flag);
       // every MMA issued has completed before tensor memory is released
@@ -325,7 +340,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // the extreme that becomes the max after scaling: max for scale >= 0,
         // min (taken as the max of the negated scores) for scale < 0
         const bool neg = p.scale_log2 < 0.f;  // uniform over the CTA
-        float ext = -INFINITY;
+        // 8 independent partial maxima keep the reduction off one long chain
+        float ex[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) ex[a] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; c += 2) {
           tmem_ld32(lane_base + s_col + c * 32, va);
@@ -340,15 +358,17 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           if (!need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ext = fmaxf(ext, fmaxf(va[i], vb[i]));
+            for (int i = 0; i < 32; ++i) ex[i & 7] = fmaxf(ex[i & 7], fmaxf(va[i], vb[i]));
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              if (key0 + c * 32 + i <= limit) ext = fmaxf(ext, va[i]);
-              if (key0 + c * 32 + 32 + i <= limit) ext = fmaxf(ext, vb[i]);
+              if (key0 + c * 32 + i <= limit) ex[i & 7] = fmaxf(ex[i & 7], va[i]);
+              if (key0 + c * 32 + 32 + i <= limit) ex[i & 7] = fmaxf(ex[i & 7], vb[i]);
             }
           }
         }
+        const float ext = fmaxf(fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])),
+                                fmaxf(fmaxf(ex[4], ex[5]), fmaxf(ex[6], ex[7])));
         // a tile past the row's limit leaves the max at -inf and its P all zeros
         mx = ext == -INFINITY ? -INFINITY : ext * fabsf(p.scale_log2);
       }
@@ -386,6 +406,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_wait_ld();
         uint32_t hi[32], lo[32];
         const float neg_m = -m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
         if (!need_mask) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
@@ -394,7 +415,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
             const float e0 = ex2(fmaf(s0, p.scale_log2, neg_m));
             const float e1 = ex2(fmaf(s1, p.scale_log2, neg_m));
-            lsum += e0 + e1;
+            ls[u & 3] += e0 + e1;
             hi[u] = pack_bf16x2(e0, e1);
             lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
           }
@@ -407,11 +428,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const int key = key0 + 64 * g + kk;
             const float e0 = key <= limit ? ex2(fmaf(s0, p.scale_log2, neg_m)) : 0.f;
             const float e1 = key + 1 <= limit ? ex2(fmaf(s1, p.scale_log2, neg_m)) : 0.f;
-            lsum += e0 + e1;
+            ls[u & 3] += e0 + e1;
             hi[u] = pack_bf16x2(e0, e1);
             lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
           }
         }
+        lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st32u(lane_base + s_col + 64 * g, hi);
         tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
       }
