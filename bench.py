@@ -324,6 +324,49 @@ def run_mixed(args, dev, pagedkv, E):
     }
 
 
+def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
+    """Launch-bound small-batch decode steps of the 70B-GQA layer shape:
+    per-step time of eager calls vs replay of a CUDA graph captured for the
+    batch's bucket (append + split-K decode)."""
+    from paged_kv_cache_52_gb300.graphs import DecodeGraphRunner
+    res = {}
+    for bsz in batches:
+        w = wl.make_decode_workload(wl.GQA_70B, device=dev, gen_device=dev,
+                                    num_seqs_override=bsz)
+        max_len = max(w.meta["lens"])
+        ws = pagedkv.decode_workspace(bsz, w.q_heads, w.kv_heads, w.d_head, max_len, dev)
+        out = torch.empty(w.q.shape, dtype=torch.float32, device=dev)
+
+        def eager():
+            pagedkv.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+            pagedkv.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                           w.context_lens, w.scale, out=out,
+                                           max_context_len=max_len, workspace=ws)
+
+        runner = DecodeGraphRunner(w.k_cache, w.v_cache, w.q_heads, w.block_tables.shape[1],
+                                   max_len, w.scale, buckets=(bsz,))
+        b = runner.capture(bsz)
+        b.q.copy_(w.q), b.k_new.copy_(w.k_new), b.v_new.copy_(w.v_new)
+        b.slots.copy_(w.slot_mapping), b.tables.copy_(w.block_tables), b.lens.copy_(w.context_lens)
+        times = {}
+        for name, fn in (("eager", eager), ("graph", b.graph.replay)):
+            for _ in range(10):
+                fn()
+            torch.cuda.synchronize()
+            s0, s1 = E(enable_timing=True), E(enable_timing=True)
+            s0.record()
+            for _ in range(steps):
+                fn()
+            s1.record()
+            torch.cuda.synchronize()
+            times[name] = s0.elapsed_time(s1) / steps * 1e3
+        res[str(bsz)] = {"eager_us": round(times["eager"], 2), "graph_us": round(times["graph"], 2),
+                         "kv_bytes": w.kv_bytes(),
+                         "graph_GBps": round(w.kv_bytes() / (times["graph"] / 1e6) / 1e9, 1)}
+        del w, runner, b
+    return res
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
@@ -454,6 +497,7 @@ def run_ours(args):
     if not args.no_mixed:
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)
+        line["small_batch_decode"] = run_small_batch(dev, pagedkv, E)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         _, info = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = info
