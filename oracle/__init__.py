@@ -26,3 +26,12 @@ from .paged_attention import (  # noqa: F401
     kv_bytes_per_token,
     kv_cache_bytes,
 )
+
+from .fp8_cache import (  # noqa: F401,E402
+    e4m3_bits_to_f64,
+    f32_to_e4m3_bits,
+    quantize_rows,
+    kv_append_fp8,
+    dequantize,
+    paged_decode_attention_fp8,
+)

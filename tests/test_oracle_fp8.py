@@ -1,0 +1,71 @@
+"""Pins of the FP8 (e4m3) cache oracle: the format against torch's own
+float8_e4m3fn conversion and closed forms, and FP8 decode against the pinned
+bf16 oracle on the dequantized values."""
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_52_gb300 import workloads as wl
+
+
+def test_e4m3_decode_matches_torch_for_all_256_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_bits_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(20000, generator=g) * torch.exp(torch.randn(20000, generator=g) * 3)
+    x = x[x.abs() < 460]
+    # every code's value, and every midpoint between neighbouring codes (ties)
+    vals = oracle.e4m3_bits_to_f64(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = (vals[1:] + vals[:-1]) / 2
+    extra = torch.tensor(np.concatenate([vals, mids, -vals, -mids]), dtype=torch.float32)
+    x = torch.cat([x, extra])
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = oracle.f32_to_e4m3_bits(x.numpy())
+    assert np.array_equal(mine, ref)
+
+
+def test_e4m3_saturation_closed_forms():
+    enc = oracle.f32_to_e4m3_bits
+    assert enc([448.0])[0] == 0x7E and enc([463.9])[0] == 0x7E      # stays finite
+    assert enc([464.0])[0] == 0x7E and enc([1e30])[0] == 0x7E      # satfinite, not NaN
+    assert enc([np.inf])[0] == 0x7E and enc([-np.inf])[0] == 0xFE
+    assert enc([np.nan])[0] == 0x7F
+    assert enc([2.0 ** -10])[0] == 0x00                           # tie to even (zero)
+    assert enc([3 * 2.0 ** -10])[0] == 0x02                       # tie to even (2 * 2^-9)
+    assert oracle.e4m3_bits_to_f64(np.array([0x08], np.uint8))[0] == 2.0 ** -6
+
+
+def test_fp8_decode_equals_bf16_decode_of_dequantized_cache():
+    # with power-of-two scales every dequantized value is exactly a bf16 value
+    w = wl.make_decode_workload(wl.TINY)
+    k_scale, v_scale = 0.0625, 0.03125
+    kc8 = oracle.quantize_rows(wl.bf16_bits(w.k_cache), k_scale)
+    vc8 = oracle.quantize_rows(wl.bf16_bits(w.v_cache), v_scale)
+    kc8, vc8 = oracle.kv_append_fp8(wl.bf16_bits(w.k_new), wl.bf16_bits(w.v_new),
+                                    w.slot_mapping.numpy(), kc8, vc8, k_scale, v_scale)
+    got = oracle.paged_decode_attention_fp8(wl.bf16_bits(w.q), kc8, vc8, w.block_tables.numpy(),
+                                            w.context_lens.numpy(), w.scale, k_scale, v_scale)
+    kb = oracle.f64_to_bf16_bits(oracle.dequantize(kc8, k_scale))
+    vb = oracle.f64_to_bf16_bits(oracle.dequantize(vc8, v_scale))
+    assert np.array_equal(oracle.bf16_bits_to_f64(kb), oracle.dequantize(kc8, k_scale))
+    ref = oracle.paged_decode_attention(wl.bf16_bits(w.q), kb, vb, w.block_tables.numpy(),
+                                        w.context_lens.numpy(), w.scale)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_quantization_error_is_bounded():
+    # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 for normal values
+    g = torch.Generator().manual_seed(9)
+    x = (torch.randn(5000, generator=g) * 3).numpy().astype(np.float32)
+    scale = np.float32(0.05)
+    deq = oracle.dequantize(oracle.quantize_rows(x, scale), scale)
+    inv = np.float32(1) / scale
+    normal = np.abs(x * inv) >= 2.0 ** -6
+    assert np.all(np.abs(deq - x)[normal] <= np.abs(x)[normal] * 2.0 ** -4 * 1.001)
