@@ -324,6 +324,51 @@ def run_mixed(args, dev, pagedkv, E):
     }
 
 
+def run_fp8(w, dev, pagedkv, E, args, peak):
+    """The same 70B-GQA decode step over an FP8 (e4m3) cache: quantizing
+    append + FP8 decode.  KV bytes are the e4m3 codes read (half of bf16)."""
+    ks, vs = wl.FP8_SCALES[args.workload]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    S, hq, hkv, d = w.num_seqs, w.q_heads, w.kv_heads, w.d_head
+    max_len = max(w.meta["lens"])
+    ws = pagedkv.decode_workspace(S, hq, hkv, d, max_len, dev)
+    out = torch.empty(S, hq, d, dtype=torch.float32, device=dev)
+
+    def step():
+        pagedkv.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, ks, vs)
+        pagedkv.paged_decode_attention_fp8(w.q, kc8, vc8, w.block_tables, w.context_lens,
+                                           w.scale, ks, vs, out=out, max_context_len=max_len,
+                                           workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    marks = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(K)]
+    s0, s1 = E(enable_timing=True), E(enable_timing=True)
+    s0.record()
+    for a, b in marks:
+        pagedkv.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, ks, vs)
+        a.record()
+        pagedkv.paged_decode_attention_fp8(w.q, kc8, vc8, w.block_tables, w.context_lens,
+                                           w.scale, ks, vs, out=out, max_context_len=max_len,
+                                           workspace=ws)
+        b.record()
+    s1.record()
+    torch.cuda.synchronize()
+    t_step = s0.elapsed_time(s1) / K
+    t_dec = sum(a.elapsed_time(b) for a, b in marks) / K
+    fp8_bytes = int(w.context_lens.sum().item()) * 2 * hkv * d  # one byte per element
+    del kc8, vc8
+    return {"k_scale": ks, "v_scale": vs, "ms_per_step": round(t_step, 4),
+            "decode_ms": round(t_dec, 4), "kv_bytes_per_step": fp8_bytes,
+            "KV_GBps": round(fp8_bytes / (t_step / 1e3) / 1e9, 1),
+            "decode_GBps": round(fp8_bytes / (t_dec / 1e3) / 1e9, 1),
+            "decode_frac_of_hbm": round(fp8_bytes / (t_dec / 1e3) / 1e9 / peak, 4),
+            "decode_tokens_per_s": round(S / (t_step / 1e3), 1),
+            "gpu_launches": K * (2 + (1 if ws is not None else 0))}
+
+
 def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
     """Launch-bound small-batch decode steps of the 70B-GQA layer shape:
     per-step time of eager calls vs replay of a CUDA graph captured for the
@@ -494,6 +539,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
+    line["fp8_cache"] = run_fp8(w, dev, pagedkv, E, args, peak)
     if not args.no_mixed:
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)

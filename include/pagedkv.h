@@ -76,6 +76,7 @@ typedef void* pkv_stream_t;
 #define PKV_DEVERR_WAIT_TIMEOUT 0x8u    /* a bounded wait on an mbarrier ran out */
 #define PKV_DEVERR_BAD_QUERY_RANGE 0x10u /* q_start not monotone or chunk longer than context */
 #define PKV_DEVERR_TMEM_ALLOC 0x20u     /* tensor memory could not be allocated */
+#define PKV_DEVERR_FP16_RANGE 0x40u     /* FP8 decode: a query value is outside f16's range */
 
 /*
  * pkv_kv_append -- scatter new K/V rows into the paged pools.
@@ -197,6 +198,42 @@ PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, i
                                         int max_blocks_per_seq, const int32_t* context_lens,
                                         int causal, float scale, float* out,
                                         pkv_stream_t stream);
+
+/*
+ * FP8 KV cache.  The pages name FP8 KV caches as the way to halve decode's
+ * KV bytes ("Cache KV, attention et optimisation de l'inference", section
+ * "Utilisez-le": --kv-cache-dtype fp8; "第 10 讲：推理（Inference）": fewer
+ * bits, fewer bytes) without fixing a format.  Here: pools of e4m3 codes
+ * (one byte each, same [num_blocks][16][kv_heads][d_head] layout) with one
+ * float32 scale per pool; a code c stands for e4m3(c) * scale.
+ *
+ * pkv_kv_append_fp8 -- as pkv_kv_append, but each element is stored as
+ * e4m3(float32(x) * (1 / scale)), rounded to nearest even, finite overflow
+ * saturating to +-448.  k/v are bf16 rows; scales must be positive and
+ * finite; kv_heads * d_head must be a multiple of 16.
+ */
+PKV_API int pkv_kv_append_fp8(const void* k, int64_t k_tok_stride, const void* v,
+                              int64_t v_tok_stride, const int64_t* slot_mapping,
+                              int64_t num_tokens, void* k_cache, void* v_cache,
+                              pkv_cache_desc cache, float k_scale, float v_scale,
+                              pkv_stream_t stream);
+
+/*
+ * pkv_paged_decode_attention_fp8 -- pkv_paged_decode_attention over FP8
+ * pools: the result is the attention of the dequantized cache
+ * (K = k_scale * e4m3(k_cache), V = v_scale * e4m3(v_cache)).  d_head must
+ * be 128.  Same plan and workspace as the bf16 decode (pkv_decode_plan);
+ * partition_blocks <= 0 = library choice.  Query values must fit f16's range
+ * (|q| < 65520), else PKV_DEVERR_FP16_RANGE is set.
+ */
+PKV_API int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
+                                           const void* k_cache, const void* v_cache,
+                                           pkv_cache_desc cache, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int max_context_len, float scale, float k_scale,
+                                           float v_scale, float* out, void* workspace,
+                                           size_t ws_bytes, int partition_blocks,
+                                           pkv_stream_t stream);
 
 /*
  * Decode for callers that cannot allocate device memory.  The pages have no

@@ -84,3 +84,71 @@ cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int
 }
 
 }  // namespace pkv
+
+// ---------------------------------------------------------------------------
+// FP8 (e4m3) append: each element is quantized as float32(x) * inv_scale,
+// rounded to nearest even with finite overflow saturating to +-448, and the
+// code stored as one byte.  One warp per token; a lane converts 16 bf16 (two
+// 16-byte loads) into 16 codes (one 16-byte store).
+// ---------------------------------------------------------------------------
+#include <cuda_fp8.h>
+
+namespace pkv {
+
+__device__ __forceinline__ uint32_t quant4_e4m3(uint2 bf4, float inv) {
+  const float f0 = bf16_lo_to_f32(bf4.x) * inv, f1 = bf16_hi_to_f32(bf4.x) * inv;
+  const float f2 = bf16_lo_to_f32(bf4.y) * inv, f3 = bf16_hi_to_f32(bf4.y) * inv;
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xffffu) | (hi << 16);
+}
+
+__global__ void __launch_bounds__(kAppendThreads)
+kv_append_fp8_kernel(const uint4* __restrict__ k, int64_t k_stride_vec, const uint4* __restrict__ v,
+                     int64_t v_stride_vec, const int64_t* __restrict__ slot_mapping,
+                     int64_t num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                     int64_t num_slots, int row_vec16, float k_inv, float v_inv) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kAppendThreads) >> 5;
+  for (int64_t t = warp; t < num_tokens; t += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot == -1) continue;
+    if (slot < -1 || slot >= num_slots) {
+      if (lane == 0) atomicOr(&g_append_error, kErrBadSlot);
+      continue;
+    }
+    const uint4* ks = k + t * k_stride_vec;  // 8 bf16 per vector
+    const uint4* vs = v + t * v_stride_vec;
+    uint4* kd = k_cache + slot * row_vec16;   // 16 codes per vector
+    uint4* vd = v_cache + slot * row_vec16;
+    for (int i = lane; i < row_vec16; i += 32) {
+      const uint4 ka = __ldg(ks + 2 * i), kb = __ldg(ks + 2 * i + 1);
+      const uint4 va = __ldg(vs + 2 * i), vb = __ldg(vs + 2 * i + 1);
+      kd[i] = make_uint4(quant4_e4m3(make_uint2(ka.x, ka.y), k_inv),
+                         quant4_e4m3(make_uint2(ka.z, ka.w), k_inv),
+                         quant4_e4m3(make_uint2(kb.x, kb.y), k_inv),
+                         quant4_e4m3(make_uint2(kb.z, kb.w), k_inv));
+      vd[i] = make_uint4(quant4_e4m3(make_uint2(va.x, va.y), v_inv),
+                         quant4_e4m3(make_uint2(va.z, va.w), v_inv),
+                         quant4_e4m3(make_uint2(vb.x, vb.y), v_inv),
+                         quant4_e4m3(make_uint2(vb.z, vb.w), v_inv));
+    }
+  }
+}
+
+cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                                 const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                                 void* v_cache, int64_t num_slots, int row_elems, float k_inv,
+                                 float v_inv, cudaStream_t stream, int num_sms) {
+  const int64_t blocks_needed = (num_tokens * 32 + kAppendThreads - 1) / kAppendThreads;
+  const int64_t max_blocks = int64_t(num_sms) * 8;
+  const int grid = int(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+  kv_append_fp8_kernel<<<grid, kAppendThreads, 0, stream>>>(
+      static_cast<const uint4*>(k), k_stride / 8, static_cast<const uint4*>(v), v_stride / 8,
+      slot_mapping, num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      num_slots, row_elems / 16, k_inv, v_inv);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -34,12 +34,12 @@
 //    warp's outstanding copies (also bounded) and lets the CTA finish.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_decode_common.cuh"
 
 namespace pkv {
 
 static __device__ unsigned g_decode_error = 0;
 
-constexpr int kBlockTokens = 16;
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 3;
 constexpr int kMaxPartitionBlocks = 1024;
@@ -56,44 +56,6 @@ struct DecodeTile {
   static constexpr int kBarOffset = kRingsBytes;
   static constexpr int kIdsOffset = kBarOffset + kDecodeWarps * kDecodeStages * 8;
   static constexpr int kSmemBytes = kIdsOffset + kMaxPartitionBlocks * 4 + 1024;  // +align slack
-};
-
-// Blocks of a sequence the kernels attend over, after clamping to what the
-// block table and the plan cover.  Both kernels use this so they agree.
-__device__ __forceinline__ int effective_blocks(int len, int max_blocks_per_seq, int num_parts,
-                                                int partition_blocks, bool* bad) {
-  *bad = false;
-  if (len < 0) {
-    len = 0;
-    *bad = true;
-  }
-  int nblk = (len + kBlockTokens - 1) / kBlockTokens;
-  if (nblk > max_blocks_per_seq) {
-    nblk = max_blocks_per_seq;
-    *bad = true;
-  }
-  const int covered = num_parts * partition_blocks;
-  if (nblk > covered) {
-    nblk = covered;
-    *bad = true;
-  }
-  return nblk;
-}
-
-__device__ __forceinline__ int effective_len(int len, int nblk) {
-  len = len < 0 ? 0 : len;
-  return len < nblk * kBlockTokens ? len : nblk * kBlockTokens;
-}
-
-struct DecodeParams {
-  const __nv_bfloat16* q;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  float* out;
-  float* part_o;
-  float* part_lse;
-  int q_heads, kv_heads, num_blocks, max_blocks_per_seq, partition_blocks, num_parts;
-  float scale_log2;
 };
 
 template <int D, int G>
@@ -437,6 +399,18 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
   return cudaGetLastError();
 }
 
+cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
+                                cudaStream_t stream) {
+  if (prm.num_parts == 1) return cudaSuccess;
+  if (d_head == 128)
+    paged_decode_merge_kernel<128><<<num_seqs * prm.q_heads, 128, 0, stream>>>(prm);
+  else if (d_head == 64)
+    paged_decode_merge_kernel<64><<<num_seqs * prm.q_heads, 64, 0, stream>>>(prm);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 template <int D>
 static cudaError_t launch_decode_d(const DecodeParams& prm, int num_seqs, int group,
                                    const CUtensorMap* tk, const CUtensorMap* tv,
@@ -467,6 +441,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.partition_blocks = a.partition_blocks;
   prm.num_parts = a.num_parts;
   prm.scale_log2 = a.scale_log2;
+  prm.out_scale = 1.f;
   const int group = a.q_heads / a.kv_heads;
   if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);

@@ -1,0 +1,455 @@
+// Paged decode attention over an FP8 (e4m3) KV cache with per-tensor scales.
+//
+// Same computation as the bf16 decode (paged_decode.cu) on the dequantized
+// cache, K = k_scale * e4m3(k_cache), V = v_scale * e4m3(v_cache): the pages
+// name FP8 KV caches ("Cache KV, attention et optimisation de l'inference",
+// "Utilisez-le": --kv-cache-dtype fp8) as the way to halve decode's KV bytes.
+//
+// Design (GB300), differences from the bf16 kernel:
+//  * a 16-token page of one KV head is 2 KB of codes per tensor: one 4-D TMA
+//    box of 128 bytes x 16 rows, 128-byte swizzled; 4 stages per warp, so
+//    three CTAs (12 warps) share an SM to hide the longer per-byte compute.
+//  * the contractions run as f16 warp MMAs (m16n8k16, fp32 accumulation):
+//    e4m3 -> f16 is exact, bf16 q -> f16 is exact in f16's range (an |q| that
+//    would overflow raises PKV_DEVERR_FP16_RANGE), and both scales factor out
+//    (k_scale into the softmax scale, v_scale into the output).
+//  * K fragments come straight from the code bytes: ldmatrix over the tile as
+//    16-bit units hands each thread 4 consecutive dims of a key, which fill the
+//    B fragment under a fixed permutation of the 16 dims of a k-step; the Q
+//    fragments are loaded with the same permutation, so the dot products are
+//    unchanged.
+//  * V fragments: ldmatrix.trans gives a thread two keys x two adjacent dims;
+//    a byte permute splits them into two key-pairs of one dim each, so every
+//    16-dim chunk feeds an "even dims" and an "odd dims" MMA whose outputs are
+//    de-interleaved when the result is written.
+//  * P enters PV as f16 hi + lo (error ~2^-22 relative).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "pkv_decode_common.cuh"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static __device__ unsigned g_decode_fp8_error = 0;
+
+constexpr int kF8Warps = 4;
+constexpr int kF8Stages = 4;
+constexpr int kF8D = 128;
+constexpr int kF8MaxPartitionBlocks = 1024;
+constexpr unsigned kErrFp16Range = 1u << 6;
+
+struct F8Tile {
+  static constexpr int kTileBytes = kBlockTokens * kF8D;      // 16 keys x 128 codes
+  static constexpr int kStageBytes = 2 * kTileBytes;          // K + V
+  static constexpr int kRingBytes = kF8Stages * kStageBytes;  // 16 KB per warp
+  static constexpr int kRingsBytes = kF8Warps * kRingBytes;
+  static constexpr int kBarOff = kRingsBytes;
+  static constexpr int kIdsOffset = kBarOff + kF8Warps * kF8Stages * 8;
+  static constexpr int kSmemBytes = kIdsOffset + kF8MaxPartitionBlocks * 4 + 1024;
+};
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four e4m3 codes (byte i = code i) -> two f16x2: codes 0, 1 in `lo`, codes
+// 2, 3 in `hi` (first code in the low half); the conversion is exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+}
+
+// Two bf16 (one 32-bit word) -> f16x2, flagging values outside f16's range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool* range_ok) {
+  const float a = bf16_lo_to_f32(w), b = bf16_hi_to_f32(w);
+  if (!(fabsf(a) < 65520.f) || !(fabsf(b) < 65520.f)) *range_ok = false;
+  return pack_f16x2(a, b);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kF8Warps * 32)
+paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using T = F8Tile;
+  constexpr int D = kF8D;
+  constexpr bool kTwoRows = (G > 8);
+  constexpr int NT = D / 8;  // virtual n-tiles of the output (16)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + T::kIdsOffset);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int pair = blockIdx.x;
+  const int part = blockIdx.y;
+  const int seq = pair / p.kv_heads;
+  const int kvh = pair - seq * p.kv_heads;
+
+  bool bad_ctx;
+  const int raw_len = __ldg(p.context_lens + seq);
+  const int nblk = effective_blocks(raw_len, p.max_blocks_per_seq, p.num_parts,
+                                    p.partition_blocks, &bad_ctx);
+  const int len = effective_len(raw_len, nblk);
+  if (bad_ctx && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_fp8_error, kErrBadContext);
+  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
+  if (part >= nparts_s) return;
+  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;
+  if (nblk == 0) {
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
+    return;
+  }
+  const int b0 = part * p.partition_blocks;
+  const int nb_local = min(nblk - b0, p.partition_blocks);
+  const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq + b0;
+  for (int i = threadIdx.x; i < nb_local; i += blockDim.x) {
+    const int32_t id = __ldg(table + i);
+    if (id < 0 || id >= p.num_blocks) atomicOr(&g_decode_fp8_error, kErrBadBlockId);
+    ids[i] = id;
+  }
+  const uint32_t ring = smem_u32(smem + warp * T::kRingBytes);
+  const uint32_t bars = smem_u32(smem + T::kBarOff) + warp * kF8Stages * 8;
+  if (lane == 0) {
+    for (int st = 0; st < kF8Stages; ++st) mbar_init(bars + st * 8, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+
+  // Q fragments as f16 under the k-permutation of the K fragments: within the
+  // 16 dims of k-step kk, fragment slots (2 tig, 2 tig + 1) hold dims
+  // (4 tig, 4 tig + 1) and slots (2 tig + 8, 2 tig + 9) hold (4 tig + 2, 4 tig + 3).
+  uint32_t qa[8][2];
+  uint32_t qb[kTwoRows ? 8 : 1][2];
+  bool range_ok = true;
+  {
+    const __nv_bfloat16* qrow = p.q + (row0 + gid) * D;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (gid < G) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * tig));
+        qa[kk][0] = bf16x2_to_f16x2(w.x, &range_ok);
+        qa[kk][1] = bf16x2_to_f16x2(w.y, &range_ok);
+      } else {
+        qa[kk][0] = qa[kk][1] = 0u;
+      }
+      if constexpr (kTwoRows) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qrow + 8 * D + kk * 16 + 4 * tig));
+        qb[kk][0] = bf16x2_to_f16x2(w.x, &range_ok);
+        qb[kk][1] = bf16x2_to_f16x2(w.y, &range_ok);
+      }
+    }
+  }
+  if (!range_ok) atomicOr(&g_decode_fp8_error, kErrFp16Range);
+  __syncthreads();
+
+  const int cnt = warp < nb_local ? (nb_local - warp + kF8Warps - 1) / kF8Warps : 0;
+  auto issue = [&](int i) {
+    const int st = i % kF8Stages;
+    const uint32_t bar = bars + st * 8;
+    const uint32_t kdst = ring + st * T::kStageBytes;
+    const int bid = ids[warp + i * kF8Warps];
+    mbar_arrive_expect_tx(bar, T::kStageBytes);
+    tma_load_4d(kdst, &tmap_k, bar, 0, kvh, 0, bid);
+    tma_load_4d(kdst + T::kTileBytes, &tmap_v, bar, 0, kvh, 0, bid);
+  };
+  int issued = 0;
+  if (lane == 0) {
+    for (int i = 0; i < cnt && i < kF8Stages; ++i) issue(i);
+  }
+  issued = cnt < kF8Stages ? cnt : kF8Stages;
+
+  const int mi = lane >> 3, mr = lane & 7;
+  const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (keys 0-7|8-15) x (chunk even|odd)
+  const int v_tok = (mi & 1) * 8 + mr;   // V: matrices (keys 0-7|8-15) x (chunk even|odd)
+
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  bool failed = false;
+  int i = 0;
+  for (; i < cnt; ++i) {
+    const int st = i % kF8Stages;
+    const uint32_t par = (i / kF8Stages) & 1;
+    const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(bars + st * 8, par));
+    if (!ready) {
+      failed = true;
+      break;
+    }
+    const uint32_t kbase = ring + st * T::kStageBytes;
+    const uint32_t vbase = kbase + T::kTileBytes;
+    const int tok0 = (b0 + warp + i * kF8Warps) * kBlockTokens;
+
+    // S = Q K^T: one ldmatrix.x4 covers two k-steps for both 8-key n-tiles.
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+      const int chunk = 2 * kp + (mi & 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(kbase + k_tok * 128 + (((chunk ^ (k_tok & 7))) << 4), r0, r1, r2, r3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = 2 * kp + h;
+        uint32_t a1 = 0u, a3 = 0u;
+        if constexpr (kTwoRows) {
+          a1 = qb[kk][0];
+          a3 = qb[kk][1];
+        }
+        uint32_t ba0, ba1, bb0, bb1;
+        e4m3x4_to_f16x2x2(h ? r1 : r0, ba0, ba1);
+        e4m3x4_to_f16x2x2(h ? r3 : r2, bb0, bb1);
+        mma_f16_16816(s[0], qa[kk][0], a1, qa[kk][1], a3, ba0, ba1);
+        mma_f16_16816(s[1], qa[kk][0], a1, qa[kk][1], a3, bb0, bb1);
+      }
+    }
+
+    // Online softmax in the log2 domain (k_scale folded into scale_log2).
+    float x[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * p.scale_log2;
+    if (tok0 + kBlockTokens > len) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (tok0 + nt * 8 + tig * 2 + (e & 1) >= len) x[nt][e] = -INFINITY;
+    }
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    const float mn0 = fmaxf(m0, mx0);
+    const float alpha0 = ex2(m0 - mn0);
+    m0 = mn0;
+    float pr[2][4];
+    pr[0][0] = ex2(x[0][0] - mn0);
+    pr[0][1] = ex2(x[0][1] - mn0);
+    pr[1][0] = ex2(x[1][0] - mn0);
+    pr[1][1] = ex2(x[1][1] - mn0);
+    l0 = l0 * alpha0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    float alpha1 = 1.f;
+    if constexpr (kTwoRows) {
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn1 = fmaxf(m1, mx1);
+      alpha1 = ex2(m1 - mn1);
+      m1 = mn1;
+      pr[0][2] = ex2(x[0][2] - mn1);
+      pr[0][3] = ex2(x[0][3] - mn1);
+      pr[1][2] = ex2(x[1][2] - mn1);
+      pr[1][3] = ex2(x[1][3] - mn1);
+      l1 = l1 * alpha1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    } else {
+      pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= alpha0;
+      o[n][1] *= alpha0;
+      if constexpr (kTwoRows) {
+        o[n][2] *= alpha1;
+        o[n][3] *= alpha1;
+      }
+    }
+
+    // P as the f16 A operand (rows = heads, k = the 16 keys in order), hi + lo.
+    uint32_t ph[4], pl[4];
+    ph[0] = pack_f16x2(pr[0][0], pr[0][1]);
+    ph[1] = pack_f16x2(pr[0][2], pr[0][3]);
+    ph[2] = pack_f16x2(pr[1][0], pr[1][1]);
+    ph[3] = pack_f16x2(pr[1][2], pr[1][3]);
+    pl[0] = pack_f16x2(pr[0][0] - f16_lo(ph[0]), pr[0][1] - f16_hi(ph[0]));
+    pl[1] = pack_f16x2(pr[0][2] - f16_lo(ph[1]), pr[0][3] - f16_hi(ph[1]));
+    pl[2] = pack_f16x2(pr[1][0] - f16_lo(ph[2]), pr[1][1] - f16_hi(ph[2]));
+    pl[3] = pack_f16x2(pr[1][2] - f16_lo(ph[3]), pr[1][3] - f16_hi(ph[3]));
+
+    // O += P V.  ldmatrix.trans over the codes as 16-bit units gives a thread
+    // keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim chunk; the
+    // byte permutes split that into the key pair of dim 2 gid (virtual n-tile
+    // 2 chunk) and of dim 2 gid + 1 (virtual n-tile 2 chunk + 1).
+#pragma unroll
+    for (int cp = 0; cp < 4; ++cp) {
+      const int chunk = 2 * cp + (mi >> 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_trans(vbase + v_tok * 128 + (((chunk ^ (v_tok & 7))) << 4), r0, r1, r2, r3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t lo_keys = h ? r2 : r0;   // keys 0-7 of chunk 2 cp + h
+        const uint32_t hi_keys = h ? r3 : r1;   // keys 8-15
+        const int vn = 2 * (2 * cp + h);
+        // bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
+        uint32_t be0, bo0, be1, bo1;
+        e4m3x4_to_f16x2x2(__byte_perm(lo_keys, 0u, 0x3120), be0, bo0);
+        e4m3x4_to_f16x2x2(__byte_perm(hi_keys, 0u, 0x3120), be1, bo1);
+        mma_f16_16816(o[vn], ph[0], ph[1], ph[2], ph[3], be0, be1);
+        mma_f16_16816(o[vn], pl[0], pl[1], pl[2], pl[3], be0, be1);
+        mma_f16_16816(o[vn + 1], ph[0], ph[1], ph[2], ph[3], bo0, bo1);
+        mma_f16_16816(o[vn + 1], pl[0], pl[1], pl[2], pl[3], bo0, bo1);
+      }
+    }
+
+    __syncwarp();
+    if (i + kF8Stages < cnt) {
+      if (lane == 0) issue(i + kF8Stages);
+      ++issued;
+    }
+  }
+
+  if (failed) {
+    if (lane == 0) {
+      atomicOr(&g_decode_fp8_error, kErrWaitTimeout);
+      for (int k = i; k < issued; ++k)
+        (void)mbar_wait_bounded(bars + (k % kF8Stages) * 8, (k / kF8Stages) & 1);
+    }
+    __syncwarp();
+  }
+
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  if constexpr (kTwoRows) {
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  }
+
+  // Cross-warp merge through shared memory.  Virtual n-tile vn = 2 chunk + par
+  // holds dims 16 chunk + 2 n + par; accumulator columns n = 2 tig, 2 tig + 1.
+  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);  // [G][D]
+  float* mml = mo + G * D;
+#pragma unroll
+  for (int vn = 0; vn < NT; ++vn) {
+    const int dim0 = 16 * (vn >> 1) + 4 * tig + (vn & 1);  // n = 2 tig; n = 2 tig + 1 is dim0 + 2
+    if (gid < G) {
+      mo[gid * D + dim0] = o[vn][0];
+      mo[gid * D + dim0 + 2] = o[vn][1];
+    }
+    if constexpr (kTwoRows) {
+      mo[(gid + 8) * D + dim0] = o[vn][2];
+      mo[(gid + 8) * D + dim0 + 2] = o[vn][3];
+    }
+  }
+  if (tig == 0) {
+    if (gid < G) {
+      mml[gid] = m0;
+      mml[G + gid] = l0;
+    }
+    if constexpr (kTwoRows) {
+      mml[gid + 8] = m1;
+      mml[G + gid + 8] = l1;
+    }
+  }
+  __syncthreads();
+
+  const bool final_out = (nparts_s == 1);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int row = idx / D, col = idx - row * D;
+    float big = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kF8Warps; ++w) {
+      const float* wm = reinterpret_cast<const float*>(smem + w * T::kRingBytes) + G * D;
+      big = fmaxf(big, wm[row]);
+    }
+    float tot = 0.f, val = 0.f;
+#pragma unroll
+    for (int w = 0; w < kF8Warps; ++w) {
+      const float* wo = reinterpret_cast<const float*>(smem + w * T::kRingBytes);
+      const float wgt = ex2(wo[G * D + row] - big);
+      tot += wo[G * D + G + row] * wgt;
+      val += wo[row * D + col] * wgt;
+    }
+    const float res = val / tot * p.out_scale;
+    if (final_out) {
+      p.out[(row0 + row) * D + col] = res;
+    } else {
+      const size_t prow = (row0 + row) * p.num_parts + part;
+      p.part_o[prow * D + col] = res;
+      if (col == 0) p.part_lse[prow] = big + __log2f(tot);
+    }
+  }
+}
+
+template <int G>
+static cudaError_t launch_fp8_t(const DecodeParams& prm, int num_seqs, const CUtensorMap* tk,
+                                const CUtensorMap* tv, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         F8Tile::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
+  paged_decode_fp8_kernel<G><<<grid, kF8Warps * 32, F8Tile::kSmemBytes, stream>>>(*tk, *tv, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_decode_merge(prm, num_seqs, kF8D, stream);
+}
+
+cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                    const CUtensorMap* tmap_v, cudaStream_t stream) {
+  if (a.d_head != kF8D || a.partition_blocks > kF8MaxPartitionBlocks) return cudaErrorInvalidValue;
+  DecodeParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.out = a.out;
+  prm.part_o = a.part_o;
+  prm.part_lse = a.part_lse;
+  prm.q_heads = a.q_heads;
+  prm.kv_heads = a.kv_heads;
+  prm.num_blocks = a.num_blocks;
+  prm.max_blocks_per_seq = a.max_blocks_per_seq;
+  prm.partition_blocks = a.partition_blocks;
+  prm.num_parts = a.num_parts;
+  prm.scale_log2 = a.scale_log2;
+  prm.out_scale = a.out_scale;
+  switch (a.q_heads / a.kv_heads) {
+    case 1: return launch_fp8_t<1>(prm, a.num_seqs, tmap_k, tmap_v, stream);
+    case 2: return launch_fp8_t<2>(prm, a.num_seqs, tmap_k, tmap_v, stream);
+    case 4: return launch_fp8_t<4>(prm, a.num_seqs, tmap_k, tmap_v, stream);
+    case 8: return launch_fp8_t<8>(prm, a.num_seqs, tmap_k, tmap_v, stream);
+    case 16: return launch_fp8_t<16>(prm, a.num_seqs, tmap_k, tmap_v, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+unsigned read_decode_fp8_error(bool clear) {
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_decode_fp8_error, sizeof(word)) != cudaSuccess) return ~0u;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_fp8_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  }
+  return word;
+}
+
+}  // namespace pkv

@@ -82,6 +82,24 @@ bool encode_query_map(CUtensorMap* map, const void* q, int total_q, int q_heads,
   return r == CUDA_SUCCESS;
 }
 
+// FP8 pool [num_blocks][16][kv_heads][d_head] of e4m3 codes (1 byte): one box
+// is a whole 128-byte row x 16 tokens of one head, 128-byte swizzled.
+bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(c.d_head), cuuint64_t(c.kv_heads),
+                              cuuint64_t(c.block_size), cuuint64_t(c.num_blocks)};
+  const cuuint64_t row = cuuint64_t(c.d_head);
+  const cuuint64_t strides[3] = {row, row * cuuint64_t(c.kv_heads),
+                                 row * cuuint64_t(c.kv_heads) * cuuint64_t(c.block_size)};
+  const cuuint32_t box[4] = {cuuint32_t(c.d_head), 1, cuuint32_t(c.block_size), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_cache_desc(const pkv_cache_desc& c) {
@@ -194,6 +212,34 @@ int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+int pkv_kv_append_fp8(const void* k, int64_t k_tok_stride, const void* v, int64_t v_tok_stride,
+                      const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                      void* v_cache, pkv_cache_desc cache, float k_scale, float v_scale,
+                      pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_EINVAL;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
+  const int64_t row = int64_t(cache.kv_heads) * cache.d_head;
+  if (row % 16) return PKV_EUNSUPPORTED;  // rows move as 16-code vectors
+  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+    return PKV_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+  cudaError_t e = pkv::launch_kv_append_fp8(
+      k, k_tok_stride, v, v_tok_stride, slot_mapping, num_tokens, k_cache, v_cache,
+      int64_t(cache.num_blocks) * cache.block_size, int(row), k_inv, v_inv,
+      static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
                     int partition_blocks, int* out_partition_blocks, int* out_num_parts,
                     size_t* out_workspace_bytes) {
@@ -259,7 +305,59 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   a.partition_blocks = plan.partition_blocks;
   a.num_parts = plan.num_parts;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.out_scale = 1.f;
   cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
+                                   const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int max_context_len, float scale,
+                                   float k_scale, float v_scale, float* out, void* workspace,
+                                   size_t ws_bytes, int partition_blocks, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (cache.d_head != 128) return PKV_EUNSUPPORTED;
+  Plan plan;
+  st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
+                 partition_blocks, &plan);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+  if (max_blocks_per_seq <= 0) return PKV_EINVAL;
+  if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return PKV_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+    return PKV_EINVAL;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
+    if (!aligned(workspace, 256)) return PKV_EINVAL;
+  }
+  CUtensorMap tk, tv;
+  if (!encode_pool_map_fp8(&tk, k_cache, cache) || !encode_pool_map_fp8(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::DecodeArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                        plan.lse_offset)
+                             : nullptr;
+  a.num_seqs = num_seqs;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.partition_blocks = plan.partition_blocks;
+  a.num_parts = plan.num_parts;
+  a.scale_log2 = scale * k_scale * 1.4426950408889634f;
+  a.out_scale = v_scale;
+  cudaError_t e = pkv::launch_paged_decode_fp8(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -326,8 +424,9 @@ int pkv_get_device_error(unsigned int* word, int clear) {
   const unsigned a = pkv::read_append_error(clear != 0);
   const unsigned d = pkv::read_decode_error(clear != 0);
   const unsigned f = pkv::read_prefill_error(clear != 0);
-  if (a == ~0u || d == ~0u || f == ~0u) return PKV_ECUDA;
-  *word = a | d | f;
+  const unsigned d8 = pkv::read_decode_fp8_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u) return PKV_ECUDA;
+  *word = a | d | f | d8;
   return PKV_OK;
 }
 

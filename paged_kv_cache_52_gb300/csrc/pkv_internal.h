@@ -15,6 +15,11 @@ cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int
                              void* v_cache, int64_t num_slots, int row_elems,
                              cudaStream_t stream, int num_sms);
 unsigned read_append_error(bool clear);
+// FP8 (e4m3) pools: row_elems must be a multiple of 16.
+cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                                 const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                                 void* v_cache, int64_t num_slots, int row_elems, float k_inv,
+                                 float v_inv, cudaStream_t stream, int num_sms);
 
 // ---- paged_decode.cu
 struct DecodeArgs {
@@ -28,6 +33,7 @@ struct DecodeArgs {
   int max_blocks_per_seq;
   int partition_blocks, num_parts;
   float scale_log2;  // scale * log2(e)
+  float out_scale;   // FP8 pools: the V dequantization scale (1 for bf16)
 };
 
 // Number of K/V stages and warps the decode kernel uses (for the plan).
@@ -37,6 +43,11 @@ int decode_max_partition_blocks();
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);
 unsigned read_decode_error(bool clear);
+
+// ---- paged_decode_fp8.cu (e4m3 pools, d_head 128)
+cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                    const CUtensorMap* tmap_v, cudaStream_t stream);
+unsigned read_decode_fp8_error(bool clear);
 
 // ---- paged_prefill.cu
 struct PrefillArgs {

@@ -27,6 +27,7 @@ DEVERR_BITS = {
     0x8: "wait timeout",
     0x10: "bad query range",
     0x20: "tensor memory allocation",
+    0x40: "query outside f16 range (fp8 decode)",
 }
 
 
@@ -64,6 +65,11 @@ SIGNATURES = {
     "pkv_paged_prefill_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
                                      ctypes.c_int, _f32, _vp, _vp], ctypes.c_int),
+    "pkv_kv_append_fp8": ([_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, CacheDesc, _f32, _f32,
+                           _vp], ctypes.c_int),
+    "pkv_paged_decode_attention_fp8": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
+                                        ctypes.c_int, _vp, ctypes.c_int, _f32, _f32, _f32, _vp,
+                                        _vp, _sz, ctypes.c_int, _vp], ctypes.c_int),
     "pkv_noalloc_scratch_bytes": ([], _sz),
     "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
@@ -138,6 +144,70 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     st = lib.pkv_kv_append(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), t,
                            _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _stream(k_cache))
     _check("pkv_kv_append", st)
+
+
+def _check_fp8_cache(k_cache, v_cache):
+    for c in (k_cache, v_cache):
+        _need(c.is_cuda and c.dtype == torch.uint8 and c.is_contiguous() and c.dim() == 4,
+              "FP8 caches must be contiguous uint8 (e4m3 codes) CUDA tensors "
+              "[num_blocks, block_size, kv_heads, d_head]")
+    _need(k_cache.shape == v_cache.shape, "k_cache and v_cache shapes differ")
+
+
+def kv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                  k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: float,
+                  v_scale: float) -> None:
+    """Quantize ``k, v [T, kv_heads, d]`` (bf16) to e4m3 with per-pool scales
+    and scatter them into the FP8 pools at ``slot_mapping`` (-1 skips)."""
+    _check_fp8_cache(k_cache, v_cache)
+    t = slot_mapping.shape[0]
+    for x in (k, v):
+        _need(x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 3,
+              "k, v must be [T, kv_heads, d] bf16 CUDA tensors")
+        _need(x.shape[0] == t and tuple(x.shape[1:]) == tuple(k_cache.shape[2:]),
+              "k, v rows must match the cache rows")
+        _need(x.stride(2) == 1 and x.stride(1) == x.shape[2],
+              "each token row of k, v must be contiguous")
+    _need(slot_mapping.is_cuda and slot_mapping.dtype == torch.int64 and
+          slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64 on the GPU")
+    st = lib.pkv_kv_append_fp8(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), t,
+                               _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), float(k_scale),
+                               float(v_scale), _stream(k_cache))
+    _check("pkv_kv_append_fp8", st)
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               scale: float, k_scale: float, v_scale: float,
+                               out: Optional[torch.Tensor] = None,
+                               max_context_len: Optional[int] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               partition_blocks: int = 0) -> torch.Tensor:
+    """Decode attention over FP8 pools (the dequantized cache's attention)."""
+    _check_fp8_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
+    S, hq, d = q.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous() and
+          context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(S, hq, k_cache.shape[2], d, max_context_len, q.device,
+                                     partition_blocks)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_decode_attention_fp8(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale),
+        float(k_scale), float(v_scale), _ptr(out), _ptr(workspace), ws_bytes,
+        int(partition_blocks), _stream(q))
+    _check("pkv_paged_decode_attention_fp8", st)
+    return out
 
 
 def decode_plan(num_seqs: int, q_heads: int, kv_heads: int, d_head: int, max_context_len: int,

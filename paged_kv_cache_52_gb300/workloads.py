@@ -365,3 +365,24 @@ def make_chunked_workload(q_heads: int, kv_heads: int, d_head: int, priors: Sequ
         scale=1.0 / math.sqrt(d_head),
         meta={"config_id": config_id, "num_blocks": nb, "prefill_lens": lens, "decode_lens": [],
               "chunks": [int(c) for c in chunks], "shared_prefix": shared_prefix})
+
+
+def fp8_pools(w, k_scale: float, v_scale: float):
+    """Synthetic FP8 (e4m3) pools for a decode workload: the workload's bf16
+    pool values over the per-pool scale, cast with torch's own float8_e4m3fn
+    conversion (an independent library routine; the values are kept inside
+    e4m3's range so no saturation is involved).  Returns uint8 code tensors."""
+    out = []
+    for pool, sc in ((w.k_cache, k_scale), (w.v_cache, v_scale)):
+        x = pool.float() / float(sc)
+        if float(x.abs().max()) >= 448.0:
+            raise ValueError("scale too small for an in-range e4m3 pool")
+        out.append(x.to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        del x
+    return out[0], out[1]
+
+
+# (k_scale, v_scale) per workload: powers of two that keep the pools in
+# e4m3's range (the 70B-GQA K pool holds x100 outlier rows).
+FP8_SCALES = {"gqa70b": (2.0, 0.03125), "mha7b": (0.03125, 0.03125),
+              "long128k": (0.03125, 0.03125), "tiny": (0.03125, 0.03125)}

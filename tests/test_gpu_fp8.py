@@ -1,0 +1,125 @@
+"""FP8 (e4m3) KV cache on the GPU: the quantizing append is bit-exact against
+the oracle's encoder, and decode over the FP8 pools matches the oracle's
+attention over the dequantized cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_52_gb300 import workloads as wl
+from parity import assert_attention_close, compact_pool, remap_slots
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_52_gb300 import pagedkv
+    pagedkv.get_device_error(clear=True)
+    return pagedkv
+
+
+def _fp8_oracle(w, kc8, vc8, k_scale, v_scale, seqs):
+    """Oracle step (quantizing append, then decode) for the chosen sequences,
+    from host copies of the FP8 pools taken before the GPU step."""
+    lens = [int(x) for x in w.context_lens.cpu().tolist()]
+    tables = w.block_tables.cpu().numpy()
+    used = sorted({int(b) for s in seqs for b in tables[s, :wl.blocks_for(lens[s])]})
+    remap = {b: i for i, b in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.int64, device=kc8.device)
+    kc = kc8.index_select(0, idx).cpu().numpy()
+    vc = vc8.index_select(0, idx).cpu().numpy()
+    tab = np.full((len(seqs), tables.shape[1]), -1, dtype=np.int64)
+    for r, s in enumerate(seqs):
+        nb = wl.blocks_for(lens[s])
+        tab[r, :nb] = [remap[int(b)] for b in tables[s, :nb]]
+    sl = remap_slots(w.slot_mapping.cpu().numpy()[list(seqs)], remap)
+    sel = torch.tensor(list(seqs), dtype=torch.int64, device=w.q.device)
+    kc, vc = oracle.kv_append_fp8(wl.bf16_bits(w.k_new.index_select(0, sel)),
+                                  wl.bf16_bits(w.v_new.index_select(0, sel)), sl, kc, vc,
+                                  k_scale, v_scale)
+    return oracle.paged_decode_attention_fp8(wl.bf16_bits(w.q.index_select(0, sel)), kc, vc, tab,
+                                             [lens[s] for s in seqs], w.scale, k_scale, v_scale)
+
+
+def _step(pk, w, kc8, vc8, k_scale, v_scale, pb=0):
+    kc, vc = kc8.clone(), vc8.clone()
+    pk.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, kc, vc, k_scale, v_scale)
+    out = pk.paged_decode_attention_fp8(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                        k_scale, v_scale, max_context_len=max(w.meta["lens"]),
+                                        partition_blocks=pb)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def _dev(w):
+    for n in ("q", "k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "block_tables",
+              "context_lens"):
+        setattr(w, n, getattr(w, n).to(DEV))
+    return w
+
+
+def test_fp8_append_bit_exact(pk):
+    w = _dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[70, 1000, 33, 16, 17]))
+    ks, vs = 2.0, 0.03125
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    kref, vref = oracle.kv_append_fp8(wl.bf16_bits(w.k_new), wl.bf16_bits(w.v_new),
+                                      w.slot_mapping.cpu().numpy(), kc8.cpu().numpy(),
+                                      vc8.cpu().numpy(), ks, vs)
+    kc, vc = kc8.clone(), vc8.clone()
+    pk.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(kc.cpu().numpy(), kref)
+    assert np.array_equal(vc.cpu().numpy(), vref)
+    # saturation: rows far beyond the scale's range clamp to +-448 on both sides
+    big = (w.k_new.float() * 1000).to(torch.bfloat16)
+    kc2 = kc8.clone()
+    pk.kv_append_fp8(big, w.v_new, w.slot_mapping, kc2, vc8.clone(), 0.001, vs)
+    kref2, _ = oracle.kv_append_fp8(wl.bf16_bits(big), wl.bf16_bits(w.v_new),
+                                    w.slot_mapping.cpu().numpy(), kc8.cpu().numpy(),
+                                    vc8.cpu().numpy(), 0.001, vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(kc2.cpu().numpy(), kref2)
+    assert pk.get_device_error() == 0
+
+
+SHAPES = [(8, 8), (16, 4), (64, 8), (32, 2), (16, 16)]
+LENS = [1, 15, 16, 17, 33, 200, 0, 1500]
+
+
+@pytest.mark.parametrize("hq,hkv", SHAPES)
+@pytest.mark.parametrize("pb", [0, 3])
+def test_fp8_decode_groups_and_ragged(pk, hq, hkv, pb):
+    spec = wl.DecodeSpec("fp8 edge", 13, len(LENS), hq, hkv, 128, lens=tuple(LENS))
+    w = _dev(wl.make_decode_workload(spec, lens_override=LENS))
+    w.slot_mapping[LENS.index(0)] = -1
+    ks, vs = 0.03125, 0.03125
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    ref = _fp8_oracle(w, kc8, vc8, ks, vs, range(len(LENS)))
+    out, _, _ = _step(pk, w, kc8, vc8, ks, vs, pb)
+    assert_attention_close(out.cpu().numpy(), ref, f"fp8 {hq}/{hkv} pb={pb}")
+    assert pk.get_device_error() == 0
+
+
+def test_fp8_decode_outliers_small(pk):
+    w = _dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[1024, 3000, 777, 4096, 2049]))
+    ks, vs = wl.FP8_SCALES["gqa70b"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    ref = _fp8_oracle(w, kc8, vc8, ks, vs, range(5))
+    out, _, _ = _step(pk, w, kc8, vc8, ks, vs)
+    assert_attention_close(out.cpu().numpy(), ref, "fp8 outliers")
+
+
+def test_fp8_full_size_70b_gqa_sampled(pk):
+    w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV)
+    ks, vs = wl.FP8_SCALES["gqa70b"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    seqs = [0, 77, 255]
+    ref = _fp8_oracle(w, kc8, vc8, ks, vs, seqs)
+    out, _, _ = _step(pk, w, kc8, vc8, ks, vs)
+    assert_attention_close(out[seqs].cpu().numpy(), ref, "fp8 70B full")
+    assert torch.isfinite(out).all()
+    assert pk.get_device_error() == 0
