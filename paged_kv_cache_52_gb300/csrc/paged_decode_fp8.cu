@@ -208,12 +208,19 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok0 = (b0 + warp + i * kF8Warps) * kBlockTokens;
 
     // S = Q K^T: one ldmatrix.x4 covers two k-steps for both 8-key n-tiles.
+    // Even and odd k-steps accumulate separately (four independent chains).
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int kp = 0; kp < 4; ++kp) {
       const int chunk = 2 * kp + (mi & 1);
       uint32_t r0, r1, r2, r3;
       ldsm_x4(kbase + k_tok * 128 + (((chunk ^ (k_tok & 7))) << 4), r0, r1, r2, r3);
+      uint32_t b[2][2][2];  // [h][n-tile][reg]
+      e4m3x4_to_f16x2x2(r0, b[0][0][0], b[0][0][1]);
+      e4m3x4_to_f16x2x2(r2, b[0][1][0], b[0][1][1]);
+      e4m3x4_to_f16x2x2(r1, b[1][0][0], b[1][0][1]);
+      e4m3x4_to_f16x2x2(r3, b[1][1][0], b[1][1][1]);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int kk = 2 * kp + h;
@@ -222,13 +229,16 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
           a1 = qb[kk][0];
           a3 = qb[kk][1];
         }
-        uint32_t ba0, ba1, bb0, bb1;
-        e4m3x4_to_f16x2x2(h ? r1 : r0, ba0, ba1);
-        e4m3x4_to_f16x2x2(h ? r3 : r2, bb0, bb1);
-        mma_f16_16816(s[0], qa[kk][0], a1, qa[kk][1], a3, ba0, ba1);
-        mma_f16_16816(s[1], qa[kk][0], a1, qa[kk][1], a3, bb0, bb1);
+        float(&acc0)[4] = h ? s_odd[0] : s[0];
+        float(&acc1)[4] = h ? s_odd[1] : s[1];
+        mma_f16_16816(acc0, qa[kk][0], a1, qa[kk][1], a3, b[h][0][0], b[h][0][1]);
+        mma_f16_16816(acc1, qa[kk][0], a1, qa[kk][1], a3, b[h][1][0], b[h][1][1]);
       }
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += s_odd[nt][e];
 
     // Online softmax in the log2 domain (k_scale folded into scale_log2).
     float x[2][4];
@@ -301,19 +311,25 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const int chunk = 2 * cp + (mi >> 1);
       uint32_t r0, r1, r2, r3;
       ldsm_x4_trans(vbase + v_tok * 128 + (((chunk ^ (v_tok & 7))) << 4), r0, r1, r2, r3);
+      // per chunk h: bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
+      uint32_t be[2][2], bo[2][2];  // [h][key half]
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t lo_keys = h ? r2 : r0;   // keys 0-7 of chunk 2 cp + h
-        const uint32_t hi_keys = h ? r3 : r1;   // keys 8-15
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r2 : r0, 0u, 0x3120), be[h][0], bo[h][0]);
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r3 : r1, 0u, 0x3120), be[h][1], bo[h][1]);
+      }
+      // all hi products, then all lo: four independent accumulators in flight
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         const int vn = 2 * (2 * cp + h);
-        // bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
-        uint32_t be0, bo0, be1, bo1;
-        e4m3x4_to_f16x2x2(__byte_perm(lo_keys, 0u, 0x3120), be0, bo0);
-        e4m3x4_to_f16x2x2(__byte_perm(hi_keys, 0u, 0x3120), be1, bo1);
-        mma_f16_16816(o[vn], ph[0], ph[1], ph[2], ph[3], be0, be1);
-        mma_f16_16816(o[vn], pl[0], pl[1], pl[2], pl[3], be0, be1);
-        mma_f16_16816(o[vn + 1], ph[0], ph[1], ph[2], ph[3], bo0, bo1);
-        mma_f16_16816(o[vn + 1], pl[0], pl[1], pl[2], pl[3], bo0, bo1);
+        mma_f16_16816(o[vn], ph[0], ph[1], ph[2], ph[3], be[h][0], be[h][1]);
+        mma_f16_16816(o[vn + 1], ph[0], ph[1], ph[2], ph[3], bo[h][0], bo[h][1]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int vn = 2 * (2 * cp + h);
+        mma_f16_16816(o[vn], pl[0], pl[1], pl[2], pl[3], be[h][0], be[h][1]);
+        mma_f16_16816(o[vn + 1], pl[0], pl[1], pl[2], pl[3], bo[h][0], bo[h][1]);
       }
     }
 
