@@ -290,6 +290,26 @@ def run_mixed(args, dev, pagedkv, E):
     torch.cuda.synchronize()
     ms = lambda i, j: sum(m[i].elapsed_time(m[j]) for m in marks) / K  # noqa: E731
     t_step, t_app, t_pre, t_dec = ms(0, 3), ms(0, 1), ms(1, 2), ms(2, 3)
+    # the same decodes through the shared-prefix (cascade) path
+    pblocks = w.meta["shared_prefix"] // wl.BLOCK_SIZE
+    cws = torch.empty(max(1, pagedkv.lib.pkv_decode_shared_prefix_workspace_bytes(
+        len(dlens), hq, hkv, d, max_d, pblocks)), dtype=torch.uint8, device=dev)
+
+    def decode_cascade():
+        pagedkv.paged_decode_attention_shared_prefix(w.q_decode, kc, vc, w.decode_tables,
+                                                     w.decode_lens, w.scale, pblocks, max_d,
+                                                     out=dout, workspace=cws)
+
+    for _ in range(3):
+        decode_cascade()
+    torch.cuda.synchronize()
+    c0, c1 = E(enable_timing=True), E(enable_timing=True)
+    c0.record()
+    for _ in range(K):
+        decode_cascade()
+    c1.record()
+    torch.cuda.synchronize()
+    t_casc = c0.elapsed_time(c1) / K
     flops = prefill_flops(plens, [chunk] * len(plens)) * 4 * hq * d
     row = 2 * hkv * d * 2
     dec_logical = sum(dlens) * row
@@ -318,6 +338,11 @@ def run_mixed(args, dev, pagedkv, E):
         "decode": {"logical_kv_bytes": dec_logical, "unique_kv_bytes": dec_unique,
                    "logical_GBps": round(dec_logical / (t_dec / 1e3) / 1e9, 1),
                    "unique_GBps": round(dec_unique / (t_dec / 1e3) / 1e9, 1)},
+        "decode_shared_prefix": {
+            "ms": round(t_casc, 4),
+            "unique_GBps": round(dec_unique / (t_casc / 1e3) / 1e9, 1),
+            "note": "prefix attended once (tensor cores) + private pages split-K + LSE merge"},
+        "ms_per_step_shared_prefix": round(t_app + t_pre + t_casc, 4),
         "gpu_launches": K * (3 + (1 if ws is not None else 0)),
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),

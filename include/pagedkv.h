@@ -200,6 +200,34 @@ PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, i
                                         pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_attention_shared_prefix -- the same result as
+ * pkv_paged_decode_attention when every sequence's first prefix_blocks pages
+ * are the same physical blocks (a shared system prompt stored once and
+ * referenced by many requests: "Optimisation de l'inference", section
+ * "PageAtention", and the nano-vLLM page, section "Cache KV": shared prefix
+ * blocks through the mapping table).  The prefix is read once for all
+ * sequences instead of once per sequence:
+ *   1. all num_seqs queries attend the prefix keys (non-causal) on the tensor
+ *      cores, giving a normalised output and log-sum-exp per (sequence, head);
+ *   2. each sequence's own pages after the prefix go through the split-K
+ *      decode;
+ *   3. the log-sum-exp merge combines both parts.
+ * The prefix's block ids are taken from row 0 of block_tables; every
+ * context_len must be >= 16 * prefix_blocks (the new token of a decode step
+ * lives in a private page).  workspace must hold
+ * pkv_decode_shared_prefix_workspace_bytes(...) bytes (256-byte aligned).
+ */
+PKV_API size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
+                                                        int d_head, int max_context_len,
+                                                        int prefix_blocks);
+
+PKV_API int pkv_paged_decode_attention_shared_prefix(
+    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, int prefix_blocks, float scale, float* out,
+    void* workspace, size_t ws_bytes, pkv_stream_t stream);
+
+/*
  * FP8 KV cache.  The pages name FP8 KV caches as the way to halve decode's
  * KV bytes ("Cache KV, attention et optimisation de l'inference", section
  * "Utilisez-le": --kv-cache-dtype fp8; "第 10 讲：推理（Inference）": fewer

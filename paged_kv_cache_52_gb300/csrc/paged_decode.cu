@@ -79,21 +79,18 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
 
-  bool bad_ctx;
-  const int raw_len = __ldg(p.context_lens + seq);
-  const int nblk = effective_blocks(raw_len, p.max_blocks_per_seq, p.num_parts,
-                                    p.partition_blocks, &bad_ctx);
-  const int len = effective_len(raw_len, nblk);
-  if (bad_ctx && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
-  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const int len = sp.len;
+  if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
+  const int nparts_s = span_parts(sp, p);
   if (part >= nparts_s) return;
   const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
-  if (nblk == 0) {  // empty context: zeros
+  if (sp.count == 0) {  // empty context: zeros
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
     return;
   }
-  const int b0 = part * p.partition_blocks;
-  const int nb_local = min(nblk - b0, p.partition_blocks);
+  const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
+  const int nb_local = min(sp.first + sp.count - b0, p.partition_blocks);
 
   // Stage this partition's block ids; ids outside the pool are flagged (their
   // TMA boxes are out of bounds and read as zeros).
@@ -323,7 +320,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   __syncthreads();
 
-  const bool final_out = (nparts_s == 1);
+  const bool final_out = (nparts_s == 1) && !p.force_partials;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int row = idx / D, col = idx - row * D;
     float big = -INFINITY;
@@ -358,23 +355,27 @@ template <int D>
 __global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParams p) {
   const size_t row = blockIdx.x;  // seq * q_heads + head
   const int seq = int(row / p.q_heads);
-  bool bad;
-  const int nblk = effective_blocks(__ldg(p.context_lens + seq), p.max_blocks_per_seq,
-                                    p.num_parts, p.partition_blocks, &bad);
-  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
-  if (nparts_s == 1) return;  // written by the split kernel
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const int nparts_s = span_parts(sp, p);
+  const bool extra = p.extra_o != nullptr;
+  if (nparts_s == 1 && !p.force_partials) return;  // written by the split kernel
   const float* lse = p.part_lse + row * p.num_parts;
   const float* po = p.part_o + row * p.num_parts * D + threadIdx.x;
-  float big = -INFINITY;
+  float big = extra ? __ldg(p.extra_lse + row) : -INFINITY;
   for (int q = 0; q < nparts_s; ++q) big = fmaxf(big, __ldg(lse + q));
   float tot = 0.f, val = 0.f;
+  if (extra) {
+    const float w = ex2(__ldg(p.extra_lse + row) - big);
+    tot += w;
+    val += w * __ldg(p.extra_o + row * D + threadIdx.x);
+  }
 #pragma unroll 4
   for (int q = 0; q < nparts_s; ++q) {
     const float w = ex2(__ldg(lse + q) - big);
     tot += w;
     val += w * __ldg(po + size_t(q) * D);
   }
-  p.out[row * D + threadIdx.x] = val / tot;
+  p.out[row * D + threadIdx.x] = tot > 0.f ? val / tot : 0.f;
 }
 
 template <int D, int G>
@@ -394,14 +395,13 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
   paged_decode_split_kernel<D, G><<<grid, kDecodeWarps * 32, T::kSmemBytes, stream>>>(
       *tmap_k, *tmap_v, prm);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || prm.num_parts == 1) return e;
-  paged_decode_merge_kernel<D><<<num_seqs * prm.q_heads, D, 0, stream>>>(prm);
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_decode_merge(prm, num_seqs, D, stream);
 }
 
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream) {
-  if (prm.num_parts == 1) return cudaSuccess;
+  if (prm.num_parts == 1 && !prm.force_partials) return cudaSuccess;
   if (d_head == 128)
     paged_decode_merge_kernel<128><<<num_seqs * prm.q_heads, 128, 0, stream>>>(prm);
   else if (d_head == 64)
@@ -442,6 +442,10 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.num_parts = a.num_parts;
   prm.scale_log2 = a.scale_log2;
   prm.out_scale = 1.f;
+  prm.first_block = a.first_block;
+  prm.force_partials = a.force_partials;
+  prm.extra_o = a.extra_o;
+  prm.extra_lse = a.extra_lse;
   const int group = a.q_heads / a.kv_heads;
   if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);

@@ -110,21 +110,19 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
 
-  bool bad_ctx;
-  const int raw_len = __ldg(p.context_lens + seq);
-  const int nblk = effective_blocks(raw_len, p.max_blocks_per_seq, p.num_parts,
-                                    p.partition_blocks, &bad_ctx);
-  const int len = effective_len(raw_len, nblk);
-  if (bad_ctx && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_fp8_error, kErrBadContext);
-  const int nparts_s = nblk > 0 ? (nblk + p.partition_blocks - 1) / p.partition_blocks : 1;
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const int len = sp.len;
+  if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_fp8_error, kErrBadContext);
+  const int nparts_s = span_parts(sp, p);
   if (part >= nparts_s) return;
-  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;
-  if (nblk == 0) {
+  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
+  if (sp.count == 0) {  // empty context: zeros
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
     return;
   }
-  const int b0 = part * p.partition_blocks;
-  const int nb_local = min(nblk - b0, p.partition_blocks);
+  const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
+  const int nb_local = min(sp.first + sp.count - b0, p.partition_blocks);
+
   const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq + b0;
   for (int i = threadIdx.x; i < nb_local; i += blockDim.x) {
     const int32_t id = __ldg(table + i);
@@ -384,7 +382,7 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   __syncthreads();
 
-  const bool final_out = (nparts_s == 1);
+  const bool final_out = (nparts_s == 1) && !p.force_partials;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int row = idx / D, col = idx - row * D;
     float big = -INFINITY;
@@ -448,6 +446,10 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap
   prm.num_parts = a.num_parts;
   prm.scale_log2 = a.scale_log2;
   prm.out_scale = a.out_scale;
+  prm.first_block = 0;
+  prm.force_partials = 0;
+  prm.extra_o = nullptr;
+  prm.extra_lse = nullptr;
   switch (a.q_heads / a.kv_heads) {
     case 1: return launch_fp8_t<1>(prm, a.num_seqs, tmap_k, tmap_v, stream);
     case 2: return launch_fp8_t<2>(prm, a.num_seqs, tmap_k, tmap_v, stream);

@@ -87,12 +87,14 @@ enum PfBar { kQFull = 0, kKFull0 = 1, kKEmpty0 = 4, kVFull0 = 7, kVEmpty0 = 9, k
              kPFull0 = 13, kODone0 = 15, kDrain = 17 };
 
 struct PrefillParams {
-  const int32_t* q_start;
+  const int32_t* q_start;       // null: one sequence owning all total_q rows
   const int32_t* block_tables;
-  const int32_t* context_lens;
+  const int32_t* context_lens;  // null: the context length is `context_len`
   float* out;
+  float* lse;                   // optional [total_q][q_heads] log2-sum-exp of each row
   int num_seqs, q_heads, kv_heads, num_blocks, max_blocks_per_seq, total_q, max_q_len;
   int causal;
+  int context_len;
   float scale_log2;
 };
 
@@ -133,10 +135,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int cta_tile = int(gridDim.x) - 1 - int(blockIdx.x);  // longest-first
 
   // ---- per-CTA bounds (uniform over the CTA, so early exits are safe)
-  const int qs = __ldg(p.q_start + seq), qe = __ldg(p.q_start + seq + 1);
-  const int ctx = __ldg(p.context_lens + seq);
+  const int qs = p.q_start ? __ldg(p.q_start + seq) : 0;
+  const int qe = p.q_start ? __ldg(p.q_start + seq + 1) : p.total_q;
+  const int ctx = p.context_lens ? __ldg(p.context_lens + seq) : p.context_len;
   const int n = qe - qs;
-  if (qs < 0 || n < 0 || qe > p.total_q || n > ctx || ctx > p.max_blocks_per_seq * 16) {
+  const bool bad_range = qs < 0 || n < 0 || qe > p.total_q;
+  if (!bad_range && n == 0) return;  // nothing to compute for this sequence
+  if (bad_range || (p.causal && n > ctx) || ctx <= 0 || ctx > p.max_blocks_per_seq * 16) {
     if (cta_tile == 0 && threadIdx.x == 0) atomicOr(&g_prefill_error, kErrBadQueryRange);
     return;
   }
@@ -452,7 +457,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       } else {
         tc_fence_after();
         const float inv = 1.f / lsum;
-        float* orow = p.out + (size_t(qs + tok) * p.q_heads + size_t(kvh) * G + head) * D;
+        const size_t orow_idx = size_t(qs + tok) * p.q_heads + size_t(kvh) * G + head;
+        float* orow = p.out + orow_idx * D;
+        if (p.lse && valid_row) p.lse[orow_idx] = m_used + __log2f(lsum);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -521,6 +528,8 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
   prm.out = a.out;
+  prm.lse = a.lse;
+  prm.context_len = a.context_len;
   prm.num_seqs = a.num_seqs;
   prm.q_heads = a.q_heads;
   prm.kv_heads = a.kv_heads;

@@ -167,6 +167,31 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   return PKV_OK;
 }
 
+// Workspace of the shared-prefix decode: suffix partials (always written),
+// then the prefix part's normalised output and log2-sum-exp.
+struct CascadePlan {
+  Plan suffix;
+  size_t part_o_off = 0, part_lse_off = 0, pre_o_off = 0, pre_lse_off = 0, total = 0;
+};
+
+int make_cascade_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
+                      int prefix_blocks, CascadePlan* cp) {
+  if (prefix_blocks <= 0) return PKV_EINVAL;
+  const int suffix_len = max_context_len > prefix_blocks * kBlockSize
+                             ? max_context_len - prefix_blocks * kBlockSize : 0;
+  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, suffix_len, 0, &cp->suffix);
+  if (st != PKV_OK) return st;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = size_t(num_seqs) * size_t(q_heads);
+  const size_t prow = rows * size_t(cp->suffix.num_parts);
+  cp->part_o_off = 0;
+  cp->part_lse_off = up(prow * d_head * sizeof(float));
+  cp->pre_o_off = cp->part_lse_off + up(prow * sizeof(float));
+  cp->pre_lse_off = cp->pre_o_off + up(rows * d_head * sizeof(float));
+  cp->total = cp->pre_lse_off + up(rows * sizeof(float));
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -415,6 +440,97 @@ int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_s
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
+                                                 int d_head, int max_context_len,
+                                                 int prefix_blocks) {
+  CascadePlan cp;
+  if (make_cascade_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, prefix_blocks,
+                        &cp) != PKV_OK)
+    return 0;
+  return cp.total;
+}
+
+int pkv_paged_decode_attention_shared_prefix(
+    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, int prefix_blocks, float scale, float* out,
+    void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  CascadePlan cp;
+  st = make_cascade_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
+                         prefix_blocks, &cp);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+  if (max_blocks_per_seq < prefix_blocks || !std::isfinite(scale)) return PKV_EINVAL;
+  if ((long long)num_seqs > 65535 * 128LL) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+    return PKV_EINVAL;
+  if (!workspace || ws_bytes < cp.total) return PKV_ENOMEM;
+  if (!aligned(workspace, 256)) return PKV_EINVAL;
+  char* ws = static_cast<char*>(workspace);
+  float* pre_o = reinterpret_cast<float*>(ws + cp.pre_o_off);
+  float* pre_lse = reinterpret_cast<float*>(ws + cp.pre_lse_off);
+  const int group = q_heads / cache.kv_heads;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // 1. the shared prefix: every sequence's query against the prefix keys,
+  //    non-causal, on the tensor cores (one pseudo-sequence of num_seqs rows)
+  CUtensorMap tq, tk, tv;
+  const int rows_per_tile = pkv::prefill_rows_per_tile();
+  if (!encode_query_map(&tq, q, num_seqs, q_heads, cache.d_head, group, rows_per_tile / group) ||
+      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::PrefillArgs pa;
+  pa.q_start = nullptr;
+  pa.block_tables = block_tables;  // row 0 holds the shared prefix
+  pa.context_lens = nullptr;
+  pa.context_len = prefix_blocks * kBlockSize;
+  pa.out = pre_o;
+  pa.lse = pre_lse;
+  pa.num_seqs = 1;
+  pa.total_q = num_seqs;
+  pa.max_q_len = num_seqs;
+  pa.q_heads = q_heads;
+  pa.kv_heads = cache.kv_heads;
+  pa.d_head = cache.d_head;
+  pa.num_blocks = cache.num_blocks;
+  pa.max_blocks_per_seq = max_blocks_per_seq;
+  pa.causal = 0;
+  pa.scale_log2 = scale_log2;
+  cudaError_t e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
+  if (e != cudaSuccess) return PKV_ECUDA;
+
+  // 2. each sequence's own blocks after the prefix, split-K, partials only;
+  // 3. the merge folds the prefix part in as one more partial
+  pkv::DecodeArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.part_o = reinterpret_cast<float*>(ws + cp.part_o_off);
+  a.part_lse = reinterpret_cast<float*>(ws + cp.part_lse_off);
+  a.num_seqs = num_seqs;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.partition_blocks = cp.suffix.partition_blocks;
+  a.num_parts = cp.suffix.num_parts;
+  a.scale_log2 = scale_log2;
+  a.out_scale = 1.f;
+  a.first_block = prefix_blocks;
+  a.force_partials = 1;
+  a.extra_o = pre_o;
+  a.extra_lse = pre_lse;
+  e = pkv::launch_paged_decode(a, &tk, &tv, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -11,33 +11,6 @@ namespace pkv {
 
 constexpr int kBlockTokens = 16;  // tokens per KV page
 
-// Blocks of a sequence the kernels attend over, after clamping to what the
-// block table and the plan cover.  Both kernels use this so they agree.
-__device__ __forceinline__ int effective_blocks(int len, int max_blocks_per_seq, int num_parts,
-                                                int partition_blocks, bool* bad) {
-  *bad = false;
-  if (len < 0) {
-    len = 0;
-    *bad = true;
-  }
-  int nblk = (len + kBlockTokens - 1) / kBlockTokens;
-  if (nblk > max_blocks_per_seq) {
-    nblk = max_blocks_per_seq;
-    *bad = true;
-  }
-  const int covered = num_parts * partition_blocks;
-  if (nblk > covered) {
-    nblk = covered;
-    *bad = true;
-  }
-  return nblk;
-}
-
-__device__ __forceinline__ int effective_len(int len, int nblk) {
-  len = len < 0 ? 0 : len;
-  return len < nblk * kBlockTokens ? len : nblk * kBlockTokens;
-}
-
 struct DecodeParams {
   const __nv_bfloat16* q;
   const int32_t* block_tables;
@@ -48,8 +21,57 @@ struct DecodeParams {
   int q_heads, kv_heads, num_blocks, max_blocks_per_seq, partition_blocks, num_parts;
   float scale_log2;  // softmax scale (times the K dequantization scale) * log2(e)
   float out_scale;   // multiplies the normalised output (the V dequantization scale)
+  // Cascade (shared-prefix) mode: attend only blocks [first_block, ...), always
+  // write partials, and let the merge fold in one extra partial per row.
+  int first_block;
+  int force_partials;
+  const float* extra_o;    // [S][q_heads][d] normalised output of the extra part, or null
+  const float* extra_lse;  // [S][q_heads] its log2-sum-exp
 };
 
+// The blocks of a sequence the kernels attend over: [first, first + count),
+// after clamping to what the block table and the split plan cover, and the
+// context length clamped to match.  The split kernels and the merge use this
+// so they agree.
+struct SeqSpan {
+  int len;    // attended positions end here
+  int first;  // first block attended
+  int count;  // blocks attended
+  bool bad;   // the context length had to be clamped
+};
+
+__device__ __forceinline__ SeqSpan seq_span(int raw_len, const DecodeParams& p) {
+  SeqSpan sp;
+  sp.bad = false;
+  int len = raw_len;
+  if (len < 0) {
+    len = 0;
+    sp.bad = true;
+  }
+  int nblk = (len + kBlockTokens - 1) / kBlockTokens;
+  if (nblk > p.max_blocks_per_seq) {
+    nblk = p.max_blocks_per_seq;
+    sp.bad = true;
+  }
+  sp.first = p.first_block;
+  if (sp.first > 0 && len < sp.first * kBlockTokens) sp.bad = true;  // shorter than the prefix
+  sp.count = nblk > sp.first ? nblk - sp.first : 0;
+  const int covered = p.num_parts * p.partition_blocks;
+  if (sp.count > covered) {
+    sp.count = covered;
+    sp.bad = true;
+  }
+  const int end = (sp.first + sp.count) * kBlockTokens;
+  sp.len = len < end ? len : end;
+  return sp;
+}
+
+// Partitions a sequence's span splits into (0 with an empty span in cascade
+// mode, where the extra partial carries the whole result).
+__device__ __forceinline__ int span_parts(const SeqSpan& sp, const DecodeParams& p) {
+  if (sp.count == 0) return p.force_partials ? 0 : 1;
+  return (sp.count + p.partition_blocks - 1) / p.partition_blocks;
+}
 
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream);

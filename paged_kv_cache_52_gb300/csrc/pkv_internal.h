@@ -34,6 +34,12 @@ struct DecodeArgs {
   int partition_blocks, num_parts;
   float scale_log2;  // scale * log2(e)
   float out_scale;   // FP8 pools: the V dequantization scale (1 for bf16)
+  // cascade (shared prefix): skip the first blocks, always write partials,
+  // merge in one extra normalised partial per row
+  int first_block = 0;
+  int force_partials = 0;
+  const float* extra_o = nullptr;
+  const float* extra_lse = nullptr;
 };
 
 // Number of K/V stages and warps the decode kernel uses (for the plan).
@@ -51,10 +57,12 @@ unsigned read_decode_fp8_error(bool clear);
 
 // ---- paged_prefill.cu
 struct PrefillArgs {
-  const int32_t* q_start;
+  const int32_t* q_start;       // null: one sequence owning all total_q rows
   const int32_t* block_tables;
-  const int32_t* context_lens;
+  const int32_t* context_lens;  // null: context_len below
   float* out;
+  float* lse = nullptr;         // optional per-row log2-sum-exp
+  int context_len = 0;
   int num_seqs, total_q, max_q_len, q_heads, kv_heads, d_head, num_blocks;
   int max_blocks_per_seq;
   int causal;

@@ -70,6 +70,11 @@ SIGNATURES = {
     "pkv_paged_decode_attention_fp8": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
                                         ctypes.c_int, _vp, ctypes.c_int, _f32, _f32, _f32, _vp,
                                         _vp, _sz, ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_decode_shared_prefix_workspace_bytes": ([ctypes.c_int] * 6, _sz),
+    "pkv_paged_decode_attention_shared_prefix": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                                  CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                                                  ctypes.c_int, _f32, _vp, _vp, _sz, _vp],
+                                                 ctypes.c_int),
     "pkv_noalloc_scratch_bytes": ([], _sz),
     "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
@@ -326,6 +331,39 @@ def paged_decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         int(partition_blocks), _stream(q))
     _check("pkv_paged_decode_attention_noalloc", st)
+    return out
+
+
+def paged_decode_attention_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
+                                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                         context_lens: torch.Tensor, scale: float,
+                                         prefix_blocks: int, max_context_len: int,
+                                         out: Optional[torch.Tensor] = None,
+                                         workspace: Optional[torch.Tensor] = None
+                                         ) -> torch.Tensor:
+    """Decode for sequences whose first ``prefix_blocks`` pages are shared:
+    the prefix is attended once for all sequences (tensor cores), the private
+    pages by the split-K decode, and the two merged by log-sum-exp."""
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
+    S, hq, d = q.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.is_contiguous() and
+          block_tables.shape[0] == S, "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be contiguous int32 [S]")
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    hkv = k_cache.shape[2]
+    need = lib.pkv_decode_shared_prefix_workspace_bytes(S, hq, hkv, d, int(max_context_len),
+                                                        int(prefix_blocks))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.pkv_paged_decode_attention_shared_prefix(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), int(prefix_blocks),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("pkv_paged_decode_attention_shared_prefix", st)
     return out
 
 
