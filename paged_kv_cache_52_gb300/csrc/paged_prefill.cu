@@ -15,8 +15,8 @@
 //  * one CTA per (two 128-row query tiles, sequence x KV head).  The 128 rows
 //    of a tile are 128/G query tokens x the G heads of the GQA group (rows
 //    token-major), so one TMA box brings a tile in and every K/V tile serves
-//    all G heads of both tiles.  CTAs are launched longest-first (the last
-//    tiles of a chunk see the most keys).
+//    all G heads of both tiles.  CTAs are dispatched longest-first across all
+//    sequences (the last tiles of a chunk see the most keys).
 //  * warp roles: warps 0-3 and 4-7 are the softmax / correction / epilogue
 //    warpgroups of Q tiles 0 and 1 (thread = row = TMEM lane), warp 9 the MMA
 //    issuer (one thread), warps 8 and 10 the TMA producers of Q + the K ring
@@ -129,10 +129,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.y;
+  // grid (pairs, tiles): CTAs are dispatched x-fastest, so every pair's
+  // longest tile goes first, then every pair's next-longest, ... (a
+  // longest-first order the hardware scheduler balances dynamically)
+  const int pair = blockIdx.x;
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
-  const int cta_tile = int(gridDim.x) - 1 - int(blockIdx.x);  // longest-first
+  const int cta_tile = int(gridDim.y) - 1 - int(blockIdx.y);
 
   // ---- per-CTA bounds (uniform over the CTA, so early exits are safe)
   const int qs = p.q_start ? __ldg(p.q_start + seq) : 0;
@@ -499,7 +502,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap*
     attr_set = true;
   }
   constexpr int TPC = kPfQTiles * TPT;
-  dim3 grid((prm.max_q_len + TPC - 1) / TPC, prm.num_seqs * prm.kv_heads);
+  if ((prm.max_q_len + TPC - 1) / TPC > 65535) return cudaErrorInvalidValue;
+  dim3 grid(prm.num_seqs * prm.kv_heads, (prm.max_q_len + TPC - 1) / TPC);
   paged_prefill_kernel<D, G><<<grid, kPfThreads, L::kSmemBytes, stream>>>(*tq, *tk, *tv, prm);
   return cudaGetLastError();
 }

@@ -415,7 +415,7 @@ int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_s
   if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PKV_EINVAL;
   if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
-  if ((long long)num_seqs * cache.kv_heads > 65535) return PKV_EUNSUPPORTED;
+  if ((long long)num_seqs * cache.kv_heads > INT32_MAX) return PKV_EUNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return PKV_EINVAL;
