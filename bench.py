@@ -424,6 +424,55 @@ def run_fp8(w, dev, pagedkv, E, args, peak):
             "gpu_launches": K * (2 + (1 if ws is not None else 0))}
 
 
+def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps=50):
+    """The other full-size decode workloads (7B-MHA, 128K long context): one
+    step = append + split-K decode, KV GB/s and fraction of the HBM peak."""
+    res = {}
+    for name in names:
+        spec = wl.DECODE_SPECS[name]
+        w = wl.make_decode_workload(spec, device=dev, gen_device=dev)
+        S, hq, hkv, d = w.num_seqs, w.q_heads, w.kv_heads, w.d_head
+        max_len = max(w.meta["lens"])
+        plan = pagedkv.decode_plan(S, hq, hkv, d, max_len)
+        ws = pagedkv.decode_workspace(S, hq, hkv, d, max_len, dev)
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=dev)
+        marks = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
+
+        def append():
+            pagedkv.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+
+        def decode():
+            pagedkv.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                           w.context_lens, w.scale, out=out,
+                                           max_context_len=max_len, workspace=ws)
+
+        for _ in range(5):
+            append(), decode()
+        torch.cuda.synchronize()
+        s0, s1 = E(enable_timing=True), E(enable_timing=True)
+        s0.record()
+        for a, b in marks:
+            append()
+            a.record()
+            decode()
+            b.record()
+        s1.record()
+        torch.cuda.synchronize()
+        t_step = s0.elapsed_time(s1) / steps
+        t_dec = sum(a.elapsed_time(b) for a, b in marks) / steps
+        kv = w.kv_bytes()
+        res[name] = {"workload": spec.name, "kv_bytes": kv, "ms_per_step": round(t_step, 4),
+                     "decode_ms": round(t_dec, 4),
+                     "KV_GBps": round(kv / (t_step / 1e3) / 1e9, 1),
+                     "decode_GBps": round(kv / (t_dec / 1e3) / 1e9, 1),
+                     "decode_frac_of_hbm": round(kv / (t_dec / 1e3) / 1e9 / peak, 4),
+                     "decode_tokens_per_s": round(S / (t_step / 1e3), 1),
+                     "partition_blocks": plan[0], "num_parts": plan[1]}
+        del w, ws, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
     """Launch-bound small-batch decode steps of the 70B-GQA layer shape:
     per-step time of eager calls vs replay of a CUDA graph captured for the
@@ -595,6 +644,8 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     line["fp8_cache"] = run_fp8(w, dev, pagedkv, E, args, peak)
+    if not args.no_mixed:
+        line["other_decode_workloads"] = run_decode_configs(dev, pagedkv, E, peak)
     if not args.no_mixed:
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)

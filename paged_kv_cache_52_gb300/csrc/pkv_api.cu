@@ -118,13 +118,16 @@ struct Plan {
   size_t lse_offset = 0;
 };
 
-// Partition choice.  Work items are (sequence x KV head, partition); the
-// target is enough items to fill every SM several times over (so uneven
-// context lengths do not leave a long tail), with partitions of at most
-// kAutoMaxPartBlocks blocks (1024 tokens) and at least kAutoMinPartBlocks.
+// Partition choice.  Work items are (sequence x KV head, partition).  Long
+// partitions amortise each CTA's pipeline start and keep the partial/merge
+// traffic small, so the partition is sized for about two items per SM
+// (estimated from the longest context), clamped to 16..256 pages (256..4096
+// tokens).  A sweep on GB300 over 8..256 sequences, 7B-MHA and 128K contexts
+// put the best partition at 128-256 pages whenever that still leaves work for
+// every SM.
 constexpr int kAutoMinPartBlocks = 16;
-constexpr int kAutoMaxPartBlocks = 64;
-constexpr int kItemsPerSm = 16;
+constexpr int kAutoMaxPartBlocks = 256;
+constexpr int kItemsPerSm = 2;
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
               int partition_blocks, Plan* plan) {
@@ -141,10 +144,8 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   } else {
     const long long pairs = (long long)num_seqs * kv_heads;
     const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
-    const long long target = (long long)kItemsPerSm * sms;
-    long long per_pair = pairs > 0 ? (target + pairs - 1) / pairs : 1;
-    if (per_pair < 1) per_pair = 1;
-    long long want = (nblk_max + per_pair - 1) / per_pair;
+    const long long slots = (long long)kItemsPerSm * sms;
+    long long want = ((long long)nblk_max * pairs + slots - 1) / slots;
     const int lo = nblk_max < kAutoMinPartBlocks ? (nblk_max > 0 ? nblk_max : 1)
                                                  : kAutoMinPartBlocks;
     if (want < lo) want = lo;

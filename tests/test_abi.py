@@ -86,9 +86,11 @@ def test_decode_plan_and_workspace(pk):
         pk.decode_plan(4, 8, 2, 64, 100, partition_blocks=2048)
     with pytest.raises(pk.PagedKVError):
         pk.decode_plan(4, 8, 2, 64, -1)
-    # automatic plan: partitions stay within [16, 64] blocks once contexts are long
+    # automatic plan: about two work items per SM, partitions within [16, 256] pages
     pb, parts, _ = pk.decode_plan(4, 64, 8, 128, 131072)
-    assert 16 <= pb <= 64 and parts == -(-8192 // pb)
+    assert 16 <= pb <= 256 and parts == -(-8192 // pb)
+    pb_small, _, _ = pk.decode_plan(4, 64, 8, 128, 2048)     # few items: short partitions
+    assert pb_small == 16
     assert pk.lib.pkv_decode_workspace_bytes(4, 64, 8, 128, 131072) == \
         pk.decode_plan(4, 64, 8, 128, 131072)[2]
 
