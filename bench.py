@@ -473,6 +473,45 @@ def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps
     return res
 
 
+def run_append_probe(dev, pagedkv, E, peak, tokens=262144, steps=20):
+    """Bulk KV append: 262,144 tokens of the 70B-GQA row shape (8 KV heads x
+    128, 4096 B of K+V per token in bf16) scattered to random slots of a pool
+    1.25x their size.  Bytes = rows read + rows written."""
+    hkv, d = 8, 128
+    g = torch.Generator(device=dev).manual_seed(7001)
+    k = torch.randn(tokens, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(tokens, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    nb = (tokens * 5 // 4 + wl.BLOCK_SIZE - 1) // wl.BLOCK_SIZE
+    slots = torch.randperm(nb * wl.BLOCK_SIZE, generator=torch.Generator().manual_seed(7002))
+    slots = slots[:tokens].to(dev)
+    kc = torch.empty(nb, wl.BLOCK_SIZE, hkv, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+    vc8 = torch.empty_like(kc8)
+    res = {"tokens": tokens}
+    for name, fn, row_bytes in (
+            ("bf16", lambda: pagedkv.kv_append(k, v, slots, kc, vc), 2 * hkv * d * 2),
+            ("fp8", lambda: pagedkv.kv_append_fp8(k, v, slots, kc8, vc8, 0.03125, 0.03125),
+             2 * hkv * d * 2 + 2 * hkv * d)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = E(enable_timing=True), E(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / steps
+        moved = tokens * (row_bytes if name == "fp8" else 2 * row_bytes)
+        res[name] = {"ms": round(t, 4), "bytes_moved": moved,
+                     "GBps": round(moved / (t / 1e3) / 1e9, 1),
+                     "frac_of_hbm": round(moved / (t / 1e3) / 1e9 / peak, 4)}
+    del k, v, kc, vc, kc8, vc8
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
     """Launch-bound small-batch decode steps of the 70B-GQA layer shape:
     per-step time of eager calls vs replay of a CUDA graph captured for the
@@ -646,6 +685,7 @@ def run_ours(args):
     line["fp8_cache"] = run_fp8(w, dev, pagedkv, E, args, peak)
     if not args.no_mixed:
         line["other_decode_workloads"] = run_decode_configs(dev, pagedkv, E, peak)
+        line["append_probe"] = run_append_probe(dev, pagedkv, E, peak)
     if not args.no_mixed:
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)
