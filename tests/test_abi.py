@@ -106,3 +106,26 @@ def test_decode_host_validation(pk):
     assert lib.pkv_paged_decode_attention_ex(*args(4, 8, _desc(pk, bs=32))) == -2
     # split plan (pb=4 -> 4 parts) without a workspace
     assert lib.pkv_paged_decode_attention_ex(*args(4, 8, _desc(pk), pb=4)) == -4
+
+
+def test_fp8_and_shared_prefix_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    d64 = _desc(pk)                                       # d_head 64: FP8 decode needs 128
+    assert lib.pkv_paged_decode_attention_fp8(dummy, 4, 8, dummy, dummy, d64, dummy, 16, dummy,
+                                              250, 0.125, 1.0, 1.0, dummy, null, 0, 0,
+                                              null) == -2
+    # non-positive scales are rejected by the quantizing append
+    assert lib.pkv_kv_append_fp8(dummy, 128, dummy, 128, dummy, 4, dummy, dummy, d64, 0.0, 1.0,
+                                 null) == -1
+    assert lib.pkv_kv_append_fp8(dummy, 128, dummy, 128, dummy, 4, dummy, dummy,
+                                 _desc(pk, d=4), 1.0, 1.0, null) == -2   # rows of 16 codes needed
+    # a shared prefix of zero pages is not a shared prefix
+    assert lib.pkv_decode_shared_prefix_workspace_bytes(4, 8, 2, 64, 250, 0) == 0
+    assert lib.pkv_paged_decode_attention_shared_prefix(dummy, 4, 8, dummy, dummy, d64, dummy,
+                                                        16, dummy, 250, 0, 0.125, dummy, dummy,
+                                                        1 << 20, null) == -1
+    # the prefix must fit the block table
+    assert lib.pkv_paged_decode_attention_shared_prefix(dummy, 4, 8, dummy, dummy, d64, dummy,
+                                                        2, dummy, 250, 4, 0.125, dummy, dummy,
+                                                        1 << 30, null) == -1

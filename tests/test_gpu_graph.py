@@ -61,3 +61,41 @@ def test_bucketed_graph_replay_matches_oracle(pk):
     assert pk.get_device_error() == 0
     with pytest.raises(ValueError):
         runner.bucket_for(17)
+
+
+def test_mixed_step_captured_in_one_graph(pk):
+    """append + chunked prefill + decode captured once and replayed: same
+    results as the eager calls, and the prefill rows match the oracle."""
+    from parity import PrefillStepOracle
+    m = wl.make_mixed_workload(num_prefill=3, num_decode=9, chunk=100, prior_range=(0, 400),
+                               shared_prefix=32, decode_cap=900)
+    pref = PrefillStepOracle(m, range(3)).output()
+    for n in ("k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "q_prefill", "q_start",
+              "prefill_tables", "prefill_lens", "q_decode", "decode_tables", "decode_lens"):
+        setattr(m, n, getattr(m, n).to(DEV))
+    kc, vc = m.k_cache.clone(), m.v_cache.clone()
+    pout = torch.empty(m.q_prefill.shape, dtype=torch.float32, device=DEV)
+    dout = torch.empty(m.q_decode.shape, dtype=torch.float32, device=DEV)
+    mdl = max(m.meta["decode_lens"])
+    ws = pk.decode_workspace(m.q_decode.shape[0], m.q_decode.shape[1], kc.shape[2], kc.shape[3],
+                             mdl, DEV)
+
+    def step():
+        pk.kv_append(m.k_new, m.v_new, m.slot_mapping, kc, vc)
+        pk.paged_prefill_attention(m.q_prefill, m.q_start, kc, vc, m.prefill_tables,
+                                   m.prefill_lens, True, m.scale, out=pout, max_q_len=100)
+        pk.paged_decode_attention(m.q_decode, kc, vc, m.decode_tables, m.decode_lens, m.scale,
+                                  out=dout, max_context_len=mdl, workspace=ws)
+
+    step()                                    # eager (also sets kernel attributes)
+    torch.cuda.synchronize()
+    eager_p, eager_d = pout.clone(), dout.clone()
+    pout.zero_(), dout.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pout, eager_p) and torch.equal(dout, eager_d)
+    assert_attention_close(pout.cpu().numpy(), pref, "graph mixed step prefill")
+    assert pk.get_device_error() == 0

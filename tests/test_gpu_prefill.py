@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_52_gb300 import workloads as wl
 from parity import DecodeStepOracle, PrefillStepOracle, assert_attention_close
 
@@ -138,4 +139,21 @@ def test_full_mixed_step_sampled(pk):
     assert_attention_close(got_rows, ref_rows, "mixed prefill rows")
     assert torch.isfinite(out).all()
     assert_attention_close(dec[dsamp].cpu().numpy(), dor.output(), "mixed decodes")
+    assert pk.get_device_error() == 0
+
+
+def test_non_causal_chunk_longer_than_context(pk):
+    # without the causal mask a chunk may hold more queries than the context has keys
+    w = wl.make_chunked_workload(16, 4, 128, [0, 0], [40, 7], config_id=14)
+    lens = torch.tensor([25, 3], dtype=torch.int32)          # fewer keys than queries
+    w.prefill_lens = lens
+    ref = oracle.paged_prefill_attention(
+        wl.bf16_bits(w.q_prefill), w.q_start.numpy(), wl.bf16_bits(w.k_cache),
+        wl.bf16_bits(w.v_cache), w.prefill_tables.numpy(), lens.numpy(), False, w.scale)
+    w = _to_dev(w)
+    out = torch.full(w.q_prefill.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pk.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache, w.prefill_tables,
+                               w.prefill_lens, False, w.scale, out=out, max_q_len=40)
+    torch.cuda.synchronize()
+    assert_attention_close(out.cpu().numpy(), ref, "non-causal n > context")
     assert pk.get_device_error() == 0
