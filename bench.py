@@ -555,6 +555,68 @@ def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
     return res
 
 
+
+def e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barrier):
+    """K steps through the public API with host buffers: step i's inputs go up
+    on a copy stream while step i-1 computes, and its output comes back while
+    step i+1 computes.  Two sets of device inputs and outputs, ordered by
+    events; every step still moves all of its inputs and its output."""
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    E = torch.cuda.Event
+    devb = [{n: torch.empty_like(getattr(w, n)) for n in host} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    outs_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    uploaded = [E() for _ in range(2)]
+    computed = [E() for _ in range(2)]
+    read_back = [E() for _ in range(2)]
+    kc, vc = w.k_cache, w.v_cache
+
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(computed[b])     # step i-2 is done with this set
+            for n, t in host.items():
+                devb[b][n].copy_(t, non_blocking=True)
+            uploaded[b].record(copy)
+
+    def run(steps):
+        for b in range(2):
+            computed[b].record(comp)
+            read_back[b].record(comp)
+        upload(0)
+        for i in range(steps):
+            b = i % 2
+            if i + 1 < steps:
+                upload(i + 1)
+            comp.wait_event(uploaded[b])
+            comp.wait_event(read_back[b])    # step i-2's output has left this buffer
+            d = devb[b]
+            append(d["k_new"], d["v_new"], d["slot_mapping"])
+            pagedkv.paged_decode_attention(d["q"], kc, vc, d["block_tables"], d["context_lens"],
+                                           w.scale, out=outs[b], max_context_len=max_len,
+                                           workspace=ws, partition_blocks=args.partition_blocks)
+            computed[b].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(computed[b])
+                outs_h[b].copy_(outs[b], non_blocking=True)
+                read_back[b].record(copy)
+        comp.wait_event(read_back[(steps - 1) % 2])
+        if steps > 1:
+            comp.wait_event(read_back[(steps - 2) % 2])
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier()
+    s, e = E(enable_timing=True), E(enable_timing=True)
+    s.record(comp)
+    copy.wait_event(s)
+    run(K)
+    e.record(comp)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(outs_h[(K - 1) % 2], out.cpu(), rtol=0, atol=0)
+    return max_over_ranks(s.elapsed_time(e), dev)
+
 def run_ours(args):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
@@ -656,7 +718,8 @@ def run_ours(args):
         e2e_step()
     e2.record()
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+    e2e_serial_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+    e2e_ms = e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barrier)
     e2e_value = whole_job_gbps(kv_bytes, K, world, e2e_ms)
 
     peak, peak_kind = measured_peak()
@@ -678,7 +741,13 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": kv_bytes},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 4),
+                "mode": "pipelined: each step's inputs uploaded from pinned host memory and "
+                        "its output read back on a copy stream, double-buffered, so the "
+                        "copies of steps i+1 and i-1 overlap the compute of step i",
+                "serial": {"value": round(whole_job_gbps(kv_bytes, K, world, e2e_serial_ms), 1),
+                           "ms_per_step": round(e2e_serial_ms / K, 4),
+                           "mode": "copy in, step, copy out on one stream"}},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }

@@ -35,3 +35,12 @@ from .fp8_cache import (  # noqa: F401,E402
     dequantize,
     paged_decode_attention_fp8,
 )
+
+from .block_manager import (  # noqa: F401,E402
+    BlockManager,
+    NoFreeBlocks,
+    fnv1a64,
+    block_hash,
+    copy_blocks,
+    num_blocks_for_budget,
+)
