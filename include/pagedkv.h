@@ -52,10 +52,12 @@ typedef enum {
   PKV_EINVAL = -1,        /* null pointer, negative size, misaligned buffer or stride */
   PKV_EUNSUPPORTED = -2,  /* shape outside the supported set listed above */
   PKV_ECUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
-  PKV_ENOMEM = -4,        /* the workspace passed is smaller than required */
+  PKV_ENOMEM = -4,        /* the workspace passed is smaller than required; host memory
+                             ran out (block manager) */
   PKV_EDEVICE_CHECK = -5, /* reserved: a device-side index check failed */
   PKV_ETIMEOUT = -6,      /* reserved: a bounded device wait ran out */
-  PKV_ESCRATCH_TOO_SMALL = -7 /* the no-allocation decode's fixed scratch cannot hold the plan */
+  PKV_ESCRATCH_TOO_SMALL = -7, /* the no-allocation decode's fixed scratch cannot hold the plan */
+  PKV_ENOBLOCKS = -8      /* block manager: fewer free blocks than needed; nothing changed */
 } pkv_status;
 
 /* Shape of one layer's K (and V) pool: [num_blocks][block_size][kv_heads][d_head]. */

@@ -1,7 +1,7 @@
 """Build ``libpagedkv.so`` in-tree with nvcc for sm_103a.
 
-Each ``csrc/*.cu`` translation unit is compiled in parallel (one nvcc process
-each), then linked into a shared library with the CUDA runtime linked
+Each ``csrc/*.cu`` translation unit (and the host-only ``csrc/*.cpp``) is
+compiled in parallel (one nvcc process each), then linked into a shared library with the CUDA runtime linked
 statically, so the library loads without a GPU driver present.  Objects go to
 ``_build/`` beside this file.  Usage: ``python -m paged_kv_cache_52_gb300.build``.
 """
@@ -30,12 +30,16 @@ def _nvcc() -> str:
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _compile(nvcc: str, src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
+    obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+    if src.endswith(".cpp"):   # host-only code: the host compiler, through nvcc
+        cmd = [nvcc, "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden,-Wall",
+               "-c", src, "-o", obj]
+    else:
+        cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
     proc = subprocess.run(cmd, capture_output=True, text=True)
     if proc.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{' '.join(cmd)}\n{proc.stdout}{proc.stderr}")

@@ -152,3 +152,59 @@ cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v,
 }
 
 }  // namespace pkv
+
+// ---------------------------------------------------------------------------
+// Block copy for copy-on-write: for each (src, dst) pair, block dst of the K
+// pool and of the V pool becomes a byte copy of block src.  One CTA copies
+// one block of one pool (a contiguous run of block_size * row bytes) with
+// 16-byte vectors, four in flight per thread; the grid strides over the
+// 2 * num_pairs (pair, pool) items.  Pure HBM copy.
+// ---------------------------------------------------------------------------
+namespace pkv {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                   const int32_t* __restrict__ pairs, int num_pairs, int num_blocks,
+                   int64_t block_vec) {
+  for (int item = blockIdx.x; item < 2 * num_pairs; item += gridDim.x) {
+    const int p = item >> 1;
+    const int32_t src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      if (threadIdx.x == 0 && (item & 1) == 0) atomicOr(&g_append_error, kErrBadBlockId);
+      continue;
+    }
+    uint4* pool = (item & 1) ? v_cache : k_cache;
+    const uint4* from = pool + int64_t(src) * block_vec;
+    uint4* to = pool + int64_t(dst) * block_vec;
+    for (int64_t base = 0; base < block_vec; base += int64_t(kCopyThreads) * kCopyUnroll) {
+      uint4 r[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + int64_t(u) * kCopyThreads + threadIdx.x;
+        if (i < block_vec) r[u] = from[i];
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + int64_t(u) * kCopyThreads + threadIdx.x;
+        if (i < block_vec) to[i] = r[u];
+      }
+    }
+  }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int64_t block_bytes, cudaStream_t stream,
+                               int num_sms) {
+  const int64_t items = 2 * int64_t(num_pairs);
+  const int64_t max_blocks = int64_t(num_sms) * 8;
+  const int grid = int(items < max_blocks ? items : max_blocks);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, num_pairs, num_blocks,
+      block_bytes / 16);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/pagedkv.h"
+#include "../../include/pagedkv_blocks.h"
 #include "pkv_internal.h"
 
 namespace {
@@ -205,11 +206,12 @@ const char* pkv_status_string(int status) {
     case PKV_EINVAL: return "PKV_EINVAL: invalid argument";
     case PKV_EUNSUPPORTED: return "PKV_EUNSUPPORTED: unsupported shape";
     case PKV_ECUDA: return "PKV_ECUDA: CUDA call or launch failed";
-    case PKV_ENOMEM: return "PKV_ENOMEM: workspace too small";
+    case PKV_ENOMEM: return "PKV_ENOMEM: workspace too small or host memory exhausted";
     case PKV_EDEVICE_CHECK: return "PKV_EDEVICE_CHECK: device-side check failed";
     case PKV_ETIMEOUT: return "PKV_ETIMEOUT: bounded device wait ran out";
     case PKV_ESCRATCH_TOO_SMALL:
       return "PKV_ESCRATCH_TOO_SMALL: plan needs more than the fixed no-allocation scratch";
+    case PKV_ENOBLOCKS: return "PKV_ENOBLOCKS: not enough free KV blocks";
     default: return "unknown pkv status";
   }
 }
@@ -235,6 +237,25 @@ int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_
   cudaError_t e = pkv::launch_kv_append(k, k_tok_stride, v, v_tok_stride, slot_mapping,
                                         num_tokens, k_cache, v_cache, num_slots, int(row),
                                         static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache, int32_t elem_bytes,
+                    const int32_t* pairs, int32_t num_pairs, pkv_stream_t stream) {
+  if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.kv_heads <= 0 || cache.d_head <= 0)
+    return PKV_EINVAL;
+  if (elem_bytes != 1 && elem_bytes != 2) return PKV_EINVAL;
+  if (num_pairs < 0) return PKV_EINVAL;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !pairs) return PKV_EINVAL;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 4)) return PKV_EINVAL;
+  const int64_t block_bytes =
+      int64_t(cache.block_size) * cache.kv_heads * cache.d_head * elem_bytes;
+  if (block_bytes % 16) return PKV_EUNSUPPORTED;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, cache.num_blocks,
+                                          block_bytes, static_cast<cudaStream_t>(stream), sms);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -20,6 +20,10 @@ cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v,
                                  const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                                  void* v_cache, int64_t num_slots, int row_elems, float k_inv,
                                  float v_inv, cudaStream_t stream, int num_sms);
+// Copy-on-write block copies: block_bytes a multiple of 16.
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int64_t block_bytes, cudaStream_t stream,
+                               int num_sms);
 
 // ---- paged_decode.cu
 struct DecodeArgs {

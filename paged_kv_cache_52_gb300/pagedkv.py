@@ -39,6 +39,14 @@ class PagedKVError(RuntimeError):
         self.status = status
 
 
+class NoFreeBlocks(PagedKVError):
+    """The block pool has fewer free blocks than the operation needs; the
+    manager is unchanged."""
+
+
+PKV_ENOBLOCKS = -8
+
+
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("kv_heads", ctypes.c_int32), ("d_head", ctypes.c_int32)]
@@ -79,6 +87,23 @@ SIGNATURES = {
     "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                             ctypes.c_int, _vp], ctypes.c_int),
+    # host block manager (pagedkv_blocks.h); pointers are host memory
+    "pkv_bm_create": ([_i32, _i32, ctypes.POINTER(_vp)], ctypes.c_int),
+    "pkv_bm_destroy": ([_vp], None),
+    "pkv_bm_add_sequence": ([_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)], ctypes.c_int),
+    "pkv_bm_append_tokens": ([_vp, _i64, _vp, _i32, _vp, _vp, _i32, ctypes.POINTER(_i32)],
+                             ctypes.c_int),
+    "pkv_bm_fork": ([_vp, _i64, _i64], ctypes.c_int),
+    "pkv_bm_free_sequence": ([_vp, _i64], ctypes.c_int),
+    "pkv_bm_slots": ([_vp, _i64, _i32, _i32, _vp], ctypes.c_int),
+    "pkv_bm_seq_len": ([_vp, _i64, ctypes.POINTER(_i32)], ctypes.c_int),
+    "pkv_bm_block_table": ([_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)], ctypes.c_int),
+    "pkv_bm_block_tables": ([_vp, _vp, _i32, _vp, _i32, _vp], ctypes.c_int),
+    "pkv_bm_num_free_blocks": ([_vp], _i32),
+    "pkv_bm_refcount": ([_vp, _i32], _i32),
+    "pkv_bm_free_list": ([_vp, _vp, _i32, ctypes.POINTER(_i32)], ctypes.c_int),
+    "pkv_blocks_for_budget": ([_i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32], _i64),
+    "pkv_copy_blocks": ([_vp, _vp, CacheDesc, _i32, _vp, _i32, _vp], ctypes.c_int),
 }
 
 
@@ -102,6 +127,8 @@ def status_string(status: int) -> str:
 
 
 def _check(func: str, status: int):
+    if status == PKV_ENOBLOCKS:
+        raise NoFreeBlocks(func, status, status_string(status))
     if status != PKV_OK:
         raise PagedKVError(func, status, status_string(status))
 
@@ -376,3 +403,133 @@ def get_device_error(clear: bool = True) -> int:
 
 def describe_device_error(word: int) -> list[str]:
     return [name for bit, name in DEVERR_BITS.items() if word & bit]
+
+
+# --------------------------------------------------------------------------
+# Host block manager (pagedkv_blocks.h) and the copy-on-write block copy.
+# --------------------------------------------------------------------------
+def _i32_host(values) -> "ctypes.Array":
+    vals = list(values)
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+class BlockManager:
+    """Handle on the library's native block manager: a pool of
+    ``num_blocks`` blocks of ``block_size`` tokens, sequences with block
+    tables, prefix sharing by chained hash, forks and copy-on-write.  All
+    bookkeeping runs in the library; this class only marshals arguments."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE):
+        h = ctypes.c_void_p()
+        _check("pkv_bm_create", lib.pkv_bm_create(int(num_blocks), int(block_size),
+                                                  ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if self._h:
+            lib.pkv_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_sequence(self, seq_id: int, token_ids) -> int:
+        """Blocks for a new prompt; returns the count of leading prompt tokens
+        already held by shared blocks."""
+        ids = list(token_ids)
+        cached = ctypes.c_int32()
+        _check("pkv_bm_add_sequence", lib.pkv_bm_add_sequence(
+            self._h, int(seq_id), _i32_host(ids), len(ids), ctypes.byref(cached)))
+        return cached.value
+
+    def append_tokens(self, seq_id: int, token_ids):
+        """Slots for new tokens, and the (src, dst) block copies to make first."""
+        ids = list(token_ids)
+        slots = (ctypes.c_int64 * max(1, len(ids)))()
+        pairs = (ctypes.c_int32 * 2)()
+        n = ctypes.c_int32()
+        _check("pkv_bm_append_tokens", lib.pkv_bm_append_tokens(
+            self._h, int(seq_id), _i32_host(ids), len(ids), slots, pairs, 1, ctypes.byref(n)))
+        return list(slots[:len(ids)]), [(pairs[0], pairs[1])] if n.value else []
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pkv_bm_fork", lib.pkv_bm_fork(self._h, int(parent), int(child)))
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pkv_bm_free_sequence", lib.pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def slots(self, seq_id: int, start: int, count: int):
+        out = (ctypes.c_int64 * max(1, count))()
+        _check("pkv_bm_slots", lib.pkv_bm_slots(self._h, int(seq_id), int(start), int(count), out))
+        return list(out[:count])
+
+    def seq_len(self, seq_id: int) -> int:
+        n = ctypes.c_int32()
+        _check("pkv_bm_seq_len", lib.pkv_bm_seq_len(self._h, int(seq_id), ctypes.byref(n)))
+        return n.value
+
+    def block_table(self, seq_id: int):
+        n = ctypes.c_int32()
+        lib.pkv_bm_block_table(self._h, int(seq_id), None, 0, ctypes.byref(n))
+        out = (ctypes.c_int32 * max(1, n.value))()
+        _check("pkv_bm_block_table", lib.pkv_bm_block_table(self._h, int(seq_id), out, n.value,
+                                                            ctypes.byref(n)))
+        return list(out[:n.value])
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        """``(block_tables [S, max_blocks] int32, context_lens [S] int32)`` as
+        CPU tensors, in the layout the attention calls take (pad with 0)."""
+        ids = list(seq_ids)
+        S = len(ids)
+        tables = torch.zeros(S, int(max_blocks_per_seq), dtype=torch.int32)
+        lens = torch.zeros(S, dtype=torch.int32)
+        id_arr = (ctypes.c_int64 * max(1, S))(*ids)
+        _check("pkv_bm_block_tables", lib.pkv_bm_block_tables(
+            self._h, id_arr, S, _ptr(tables), int(max_blocks_per_seq), _ptr(lens)))
+        return tables, lens
+
+    def num_free_blocks(self) -> int:
+        return lib.pkv_bm_num_free_blocks(self._h)
+
+    def refcount(self, block: int) -> int:
+        return lib.pkv_bm_refcount(self._h, int(block))
+
+    def free_list(self):
+        n = ctypes.c_int32()
+        out = (ctypes.c_int32 * max(1, self.num_blocks))()
+        _check("pkv_bm_free_list", lib.pkv_bm_free_list(self._h, out, self.num_blocks,
+                                                        ctypes.byref(n)))
+        return list(out[:n.value])
+
+
+def blocks_for_budget(usable_bytes: int, model_bytes: int, activation_peak_bytes: int,
+                      num_layers: int, block_size: int, kv_heads: int, d_head: int,
+                      dtype_size: int) -> int:
+    n = lib.pkv_blocks_for_budget(int(usable_bytes), int(model_bytes), int(activation_peak_bytes),
+                                  int(num_layers), int(block_size), int(kv_heads), int(d_head),
+                                  int(dtype_size))
+    _need(n >= 0, "shape arguments must be positive")
+    return n
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor) -> None:
+    """Copy-on-write on the device: block ``pairs[i, 1]`` of both pools
+    becomes a copy of block ``pairs[i, 0]`` (``pairs`` int32 [n, 2] on the
+    pools' device; bf16 or uint8 (FP8) pools)."""
+    for c in (k_cache, v_cache):
+        _need(c.is_cuda and c.is_contiguous() and c.dim() == 4 and
+              c.dtype in (torch.bfloat16, torch.uint8),
+              "pools must be contiguous bf16 or uint8 CUDA tensors [NB, bs, Hkv, d]")
+    _need(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype,
+          "k_cache and v_cache differ")
+    _need(pairs.dtype == torch.int32 and pairs.is_contiguous() and pairs.dim() == 2 and
+          pairs.shape[1] == 2 and (pairs.numel() == 0 or pairs.device == k_cache.device),
+          "pairs must be a contiguous int32 [n, 2] tensor on the pools' device")
+    st = lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
+                             k_cache.element_size(), _ptr(pairs), pairs.shape[0],
+                             _stream(k_cache))
+    _check("pkv_copy_blocks", st)
