@@ -253,6 +253,16 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     pl[2] = pack_bf16x2(pr[1][0] - bf16_lo_to_f32(ph[2]), pr[1][1] - bf16_hi_to_f32(ph[2]));
     pl[3] = pack_bf16x2(pr[1][2] - bf16_lo_to_f32(ph[3]), pr[1][3] - bf16_hi_to_f32(ph[3]));
 
+    // Rows of the last page past the length may hold anything, NaN included;
+    // their P is 0, and zeroing their V keeps each such product exactly 0.  A
+    // B register holds keys (2 tig, 2 tig + 1) -- or 8 more -- in its halves.
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (tok0 + kBlockTokens > len) {
+      const int k0 = tok0 + 2 * tig;
+      vm0 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+      vm1 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+    }
+
     // O += P V: V tiles through ldmatrix.trans (B operand, k = tokens, n = dims).
 #pragma unroll
     for (int dn = 0; dn < D / 16; ++dn) {
@@ -261,6 +271,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             (((chunk & 7) ^ (v_tok & 7)) << 4);
       uint32_t b0r, b1r, b2r, b3r;
       ldsm_x4_trans(addr, b0r, b1r, b2r, b3r);
+      b0r &= vm0;
+      b1r &= vm1;
+      b2r &= vm0;
+      b3r &= vm1;
       mma_bf16_16816(o[2 * dn], ph[0], ph[1], ph[2], ph[3], b0r, b1r);
       mma_bf16_16816(o[2 * dn], pl[0], pl[1], pl[2], pl[3], b0r, b1r);
       mma_bf16_16816(o[2 * dn + 1], ph[0], ph[1], ph[2], ph[3], b2r, b3r);

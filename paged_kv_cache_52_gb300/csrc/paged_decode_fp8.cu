@@ -304,11 +304,24 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim chunk; the
     // byte permutes split that into the key pair of dim 2 gid (virtual n-tile
     // 2 chunk) and of dim 2 gid + 1 (virtual n-tile 2 chunk + 1).
+    // Rows of the last page past the length may hold any code, NaN included:
+    // zero them (their P is 0).  Each 16-bit unit holds one key's two codes,
+    // keys (2 tig, 2 tig + 1) in r0 / r2 and 8 more in r1 / r3.
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (tok0 + kBlockTokens > len) {
+      const int k0 = tok0 + 2 * tig;
+      vm0 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+      vm1 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+    }
 #pragma unroll
     for (int cp = 0; cp < 4; ++cp) {
       const int chunk = 2 * cp + (mi >> 1);
       uint32_t r0, r1, r2, r3;
       ldsm_x4_trans(vbase + v_tok * 128 + (((chunk ^ (v_tok & 7))) << 4), r0, r1, r2, r3);
+      r0 &= vm0;
+      r1 &= vm1;
+      r2 &= vm0;
+      r3 &= vm1;
       // per chunk h: bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
       uint32_t be[2][2], bo[2][2];  // [h][key half]
 #pragma unroll

@@ -273,6 +273,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         umma_commit(bars + 8 * (kODone0 + t));
       };
+      // Rows of the context's last page past its length may hold anything,
+      // NaN included.  Their P is 0; zeroing their V rows in shared memory
+      // (whole 128-byte rows, so the swizzle does not matter) keeps 0 * V
+      // exactly 0.  Generic stores, then a proxy fence for the tensor core.
+      const int tail_rows = ctx & 15;
+      const int j_tail = (nblk - 1) / 8;
+      auto clear_tail = [&](int j) {
+        const uint32_t page = sbase + L::kVOff + (j % kPfVStages) * L::kTileBytes +
+                              ((nblk - 1) % 8) * 2048;
+        for (int h = 0; h < D / 64; ++h)
+          for (int r = tail_rows; r < 16; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) st_shared_zero16(page + h * L::kHalf + r * 128 + c * 16);
+        fence_proxy_async_smem();
+      };
       auto ready = [&](uint32_t full0, int stages, int j) {
         const bool r = pf_wait(full0 + 8 * (j % stages), (j / stages) & 1, abort_flag);
         if (r) tc_fence_after();
@@ -292,6 +307,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           break;
         }
         tc_fence_after();
+        if (tail_rows && j == j_tail) clear_tail(j);
         issue_pv(0, j);
         const bool more = j + 1 < ntiles;
         if (more) {
