@@ -382,7 +382,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           if (!need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ex[i & 7] = fmaxf(ex[i & 7], fmaxf(va[i], vb[i]));
+            for (int i = 0; i < 32; ++i) ex[i & 7] = max3f(ex[i & 7], va[i], vb[i]);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -405,13 +405,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           ok = __all_sync(0xffffffffu, pf_wait(o_done, (j - 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tmem_ld32(lane_base + o_col + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            for (int i = 0; i < 32; i += 2) f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), a2), o[i], o[i + 1]);
             tmem_st32(lane_base + o_col + c * 32, o);
           }
         }
@@ -429,19 +430,26 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_ld32(lane_base + s_col + 64 * g + 32, vb);
         tmem_wait_ld();
         uint32_t hi[32], lo[32];
-        const float neg_m = -m_used;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
+        // pairs of keys in packed f32x2 arithmetic: one FMA, one ADD and one
+        // SUB instruction per two scores
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t nm2 = f2_pack(-m_used, -m_used);
+        uint64_t ls2[2] = {0ull, 0ull};  // independent partial row sums (pairs)
         if (!need_mask) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const int kk = 2 * u;  // key within the group
             const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
             const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
-            const float e0 = ex2(fmaf(s0, p.scale_log2, neg_m));
-            const float e1 = ex2(fmaf(s1, p.scale_log2, neg_m));
-            ls[u & 3] += e0 + e1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+            const float e0 = ex2(x0), e1 = ex2(x1);
+            const uint64_t e = f2_pack(e0, e1);
+            ls2[u & 1] = f2_add(ls2[u & 1], e);
             hi[u] = pack_bf16x2(e0, e1);
-            lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
+            float r0, r1;
+            f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
+            lo[u] = pack_bf16x2(r0, r1);
           }
         } else {
 #pragma unroll
@@ -450,14 +458,24 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
             const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
             const int key = key0 + 64 * g + kk;
-            const float e0 = key <= limit ? ex2(fmaf(s0, p.scale_log2, neg_m)) : 0.f;
-            const float e1 = key + 1 <= limit ? ex2(fmaf(s1, p.scale_log2, neg_m)) : 0.f;
-            ls[u & 3] += e0 + e1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+            const float e0 = key <= limit ? ex2(x0) : 0.f;
+            const float e1 = key + 1 <= limit ? ex2(x1) : 0.f;
+            const uint64_t e = f2_pack(e0, e1);
+            ls2[u & 1] = f2_add(ls2[u & 1], e);
             hi[u] = pack_bf16x2(e0, e1);
-            lo[u] = pack_bf16x2(e0 - bf16_lo_to_f32(hi[u]), e1 - bf16_hi_to_f32(hi[u]));
+            float r0, r1;
+            f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
+            lo[u] = pack_bf16x2(r0, r1);
           }
         }
-        lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(ls2[0], a0, a1);
+          f2_unpack(ls2[1], b0, b1);
+          lsum += (a0 + a1) + (b0 + b1);
+        }
         tmem_st32u(lane_base + s_col + 64 * g, hi);
         tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
       }
