@@ -275,13 +275,17 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else {
       pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
     }
+    // After the first pages the running max rarely moves: skip the rescale
+    // (alpha = 1 exactly) unless some row of the warp needs it.
+    if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f)) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      o[n][0] *= alpha0;
-      o[n][1] *= alpha0;
-      if constexpr (kTwoRows) {
-        o[n][2] *= alpha1;
-        o[n][3] *= alpha1;
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= alpha0;
+        o[n][1] *= alpha0;
+        if constexpr (kTwoRows) {
+          o[n][2] *= alpha1;
+          o[n][3] *= alpha1;
+        }
       }
     }
 
