@@ -34,6 +34,7 @@ from .fp8_cache import (  # noqa: F401,E402
     kv_append_fp8,
     dequantize,
     paged_decode_attention_fp8,
+    paged_prefill_attention_fp8,
 )
 
 from .block_manager import (  # noqa: F401,E402

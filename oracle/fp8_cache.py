@@ -22,7 +22,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .paged_attention import _as_f64, kv_append, paged_decode_attention
+from .paged_attention import _as_f64, kv_append, paged_decode_attention, paged_prefill_attention
 
 E4M3_MAX = 448.0
 E4M3_NAN = 0x7F
@@ -100,3 +100,11 @@ def paged_decode_attention_fp8(q, k_cache_bits, v_cache_bits, block_tables, cont
     return paged_decode_attention(q, dequantize(k_cache_bits, k_scale),
                                   dequantize(v_cache_bits, v_scale), block_tables,
                                   context_lens, scale)
+
+
+def paged_prefill_attention_fp8(q, q_start, k_cache_bits, v_cache_bits, block_tables,
+                                context_lens, causal, scale, k_scale, v_scale):
+    """Chunked prefill attention over the dequantized FP8 pools."""
+    return paged_prefill_attention(q, q_start, dequantize(k_cache_bits, k_scale),
+                                   dequantize(v_cache_bits, v_scale), block_tables,
+                                   context_lens, causal, scale)

@@ -69,3 +69,41 @@ def test_fp8_quantization_error_is_bounded():
     inv = np.float32(1) / scale
     normal = np.abs(x * inv) >= 2.0 ** -6
     assert np.all(np.abs(deq - x)[normal] <= np.abs(x)[normal] * 2.0 ** -4 * 1.001)
+
+
+def _fp8_chunked(k_scale, v_scale):
+    w = wl.make_chunked_workload(8, 2, 64, [0, 40, 17], [5, 30, 1])
+    kc8 = oracle.quantize_rows(wl.bf16_bits(w.k_cache), k_scale)
+    vc8 = oracle.quantize_rows(wl.bf16_bits(w.v_cache), v_scale)
+    kc8, vc8 = oracle.kv_append_fp8(wl.bf16_bits(w.k_new), wl.bf16_bits(w.v_new),
+                                    w.slot_mapping.numpy(), kc8, vc8, k_scale, v_scale)
+    return w, kc8, vc8
+
+
+def test_fp8_prefill_equals_bf16_prefill_of_dequantized_cache():
+    k_scale, v_scale = 0.0625, 0.03125
+    w, kc8, vc8 = _fp8_chunked(k_scale, v_scale)
+    args = (wl.bf16_bits(w.q_prefill), w.q_start.numpy())
+    tail = (w.prefill_tables.numpy(), w.prefill_lens.numpy(), True, w.scale)
+    got = oracle.paged_prefill_attention_fp8(*args, kc8, vc8, *tail, k_scale, v_scale)
+    kb = oracle.f64_to_bf16_bits(oracle.dequantize(kc8, k_scale))
+    vb = oracle.f64_to_bf16_bits(oracle.dequantize(vc8, v_scale))
+    assert np.array_equal(got, oracle.paged_prefill_attention(*args, kb, vb, *tail))
+
+
+def test_fp8_causal_prefill_equals_repeated_fp8_decode():
+    k_scale, v_scale = 2.0, 0.03125
+    w, kc8, vc8 = _fp8_chunked(k_scale, v_scale)
+    q = wl.bf16_bits(w.q_prefill)
+    qs = w.q_start.numpy()
+    tables, lens = w.prefill_tables.numpy(), w.prefill_lens.numpy()
+    got = oracle.paged_prefill_attention_fp8(q, qs, kc8, vc8, tables, lens, True, w.scale,
+                                             k_scale, v_scale)
+    for s in range(len(lens)):
+        n = int(qs[s + 1] - qs[s])
+        for i in range(n):
+            row = int(qs[s]) + i
+            ref = oracle.paged_decode_attention_fp8(q[row][None], kc8, vc8, tables[s:s + 1],
+                                                    [int(lens[s]) - n + i + 1], w.scale,
+                                                    k_scale, v_scale)
+            np.testing.assert_allclose(got[row], ref[0], rtol=0, atol=1e-12)
