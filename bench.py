@@ -338,6 +338,43 @@ def run_mixed(args, dev, pagedkv, E):
         c1.record()
         torch.cuda.synchronize()
         t_conc[cascade] = c0.elapsed_time(c1) / K
+    # the same step over an FP8 (e4m3) cache: quantizing append, prefill
+    # (pages widened to bf16 in a workspace, then the tensor-core prefill),
+    # FP8 decode
+    ks8, vs8 = 0.03125, 0.03125
+    kc8, vc8 = wl.fp8_pools(w, ks8, vs8)
+    pws8 = torch.empty(pagedkv.prefill_fp8_workspace_bytes(
+        len(plens), w.prefill_tables.shape[1], hkv, d), dtype=torch.uint8, device=dev)
+
+    def fp8_parts():
+        yield lambda: pagedkv.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, kc8, vc8, ks8, vs8)
+        yield lambda: pagedkv.paged_prefill_attention_fp8(
+            w.q_prefill, w.q_start, kc8, vc8, w.prefill_tables, w.prefill_lens, True, w.scale,
+            ks8, vs8, out=pout, max_q_len=chunk, workspace=pws8)
+        yield lambda: pagedkv.paged_decode_attention_fp8(
+            w.q_decode, kc8, vc8, w.decode_tables, w.decode_lens, w.scale, ks8, vs8, out=dout,
+            max_context_len=max_d, workspace=ws)
+
+    parts8 = list(fp8_parts())
+    for _ in range(3):
+        for f in parts8:
+            f()
+    torch.cuda.synchronize()
+    marks8 = [tuple(E(enable_timing=True) for _ in range(4)) for _ in range(K)]
+    for m in marks8:
+        for i, f in enumerate(parts8):
+            m[i].record()
+            f()
+        m[3].record()
+    torch.cuda.synchronize()
+    ms8 = lambda i, j: sum(m[i].elapsed_time(m[j]) for m in marks8) / K  # noqa: E731
+    fp8_step = {"ms_per_step": round(ms8(0, 3), 4), "append_ms": round(ms8(0, 1), 4),
+                "prefill_ms": round(ms8(1, 2), 4), "decode_ms": round(ms8(2, 3), 4),
+                "k_scale": ks8, "v_scale": vs8,
+                "prefill_note": "FP8 pages widened to bf16 (exact) in a workspace, then the "
+                                "tcgen05 prefill with k_scale/v_scale folded in",
+                "gpu_launches": K * (4 + (1 if ws is not None else 0))}
+    del kc8, vc8, pws8
     flops = prefill_flops(plens, [chunk] * len(plens)) * 4 * hq * d
     row = 2 * hkv * d * 2
     dec_logical = sum(dlens) * row
@@ -376,6 +413,7 @@ def run_mixed(args, dev, pagedkv, E):
         "gpu_launches": K * (3 + (1 if ws is not None else 0)),
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),
+        "fp8_cache": fp8_step,
     }
 
 

@@ -266,6 +266,32 @@ PKV_API int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_he
                                            pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention_fp8 -- pkv_paged_prefill_attention over FP8
+ * pools: the attention of the dequantized cache, as above.  The pages a
+ * chunk's sequence uses (its first ceil(context_len / 16) block-table
+ * entries) are first widened to bf16 in the workspace -- exact, every e4m3
+ * value is a bf16 value -- and the tensor-core prefill then runs on them with
+ * k_scale folded into the softmax scale and v_scale into the output.  That
+ * costs one FP8 read and one bf16 write per cached element of those pages on
+ * top of the bf16 prefill.  d_head 64 or 128.
+ * workspace: >= pkv_paged_prefill_attention_fp8_workspace_bytes(num_seqs,
+ * max_blocks_per_seq, kv_heads, d_head) device bytes (PKV_ENOMEM otherwise);
+ * its contents on entry do not matter.  Out-of-range block ids read as zeros
+ * and set PKV_DEVERR_BAD_BLOCK_ID.
+ */
+PKV_API size_t pkv_paged_prefill_attention_fp8_workspace_bytes(int num_seqs,
+                                                               int max_blocks_per_seq,
+                                                               int kv_heads, int d_head);
+PKV_API int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int num_seqs,
+                                            int total_q, int max_q_len, int q_heads,
+                                            const void* k_cache, const void* v_cache,
+                                            pkv_cache_desc cache, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* context_lens,
+                                            int causal, float scale, float k_scale, float v_scale,
+                                            float* out, void* workspace, size_t ws_bytes,
+                                            pkv_stream_t stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that are handed
  * device buffers but may not call cudaMalloc (a fixed, pre-reserved memory

@@ -208,3 +208,79 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
 }
 
 }  // namespace pkv
+
+// ---------------------------------------------------------------------------
+// FP8 pages -> bf16 pages for the chunked prefill over an FP8 cache.  Page j
+// of sequence s (j < ceil(context_len / 16)) is widened into block
+// s * max_blocks + j of a bf16 scratch pool, and entry (s, j) of a scratch
+// block table names it.  e4m3 -> f16 -> f32 -> bf16 is exact: every e4m3
+// value (3 mantissa bits, exponents 2^-9 .. 2^8) is a bf16 value.  One CTA
+// widens one page of K and V; each thread moves 16 codes per step (one
+// 16-byte load, two 16-byte stores per pool).
+// ---------------------------------------------------------------------------
+#include <cuda_fp16.h>
+
+namespace pkv {
+
+constexpr int kPageTokens = 16;
+
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "h"(two));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(h);
+  return pack_bf16x2(f.x, f.y);
+}
+
+__device__ __forceinline__ uint4 widen8(uint32_t a, uint32_t b) {
+  return make_uint4(e4m3x2_to_bf16x2(uint16_t(a & 0xffffu)), e4m3x2_to_bf16x2(uint16_t(a >> 16)),
+                    e4m3x2_to_bf16x2(uint16_t(b & 0xffffu)), e4m3x2_to_bf16x2(uint16_t(b >> 16)));
+}
+
+__global__ void __launch_bounds__(kAppendThreads)
+widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v8,
+                       const int32_t* __restrict__ tables, const int32_t* __restrict__ lens,
+                       int num_seqs, int max_blocks, int num_blocks, int page_vec16,
+                       uint4* __restrict__ kdst, uint4* __restrict__ vdst,
+                       int32_t* __restrict__ table_out) {
+  const int64_t items = int64_t(num_seqs) * max_blocks;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int s = int(item / max_blocks), j = int(item - int64_t(s) * max_blocks);
+    if (threadIdx.x == 0) table_out[item] = int32_t(item);
+    const int len = min(max(__ldg(lens + s), 0), max_blocks * kPageTokens);
+    if (j * kPageTokens >= len) continue;
+    const int32_t src = __ldg(tables + item);
+    const bool ok = src >= 0 && src < num_blocks;
+    if (!ok && threadIdx.x == 0) atomicOr(&g_append_error, kErrBadBlockId);
+    const uint4* ks = k8 + int64_t(ok ? src : 0) * page_vec16;
+    const uint4* vs = v8 + int64_t(ok ? src : 0) * page_vec16;
+    uint4* kd = kdst + item * page_vec16 * 2;  // 16 codes -> 32 bytes of bf16
+    uint4* vd = vdst + item * page_vec16 * 2;
+    for (int i = threadIdx.x; i < page_vec16; i += kAppendThreads) {
+      const uint4 kc = ok ? __ldg(ks + i) : make_uint4(0, 0, 0, 0);
+      const uint4 vc = ok ? __ldg(vs + i) : make_uint4(0, 0, 0, 0);
+      kd[2 * i] = widen8(kc.x, kc.y);
+      kd[2 * i + 1] = widen8(kc.z, kc.w);
+      vd[2 * i] = widen8(vc.x, vc.y);
+      vd[2 * i + 1] = widen8(vc.z, vc.w);
+    }
+  }
+}
+
+cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
+                                   const int32_t* lens, int num_seqs, int max_blocks,
+                                   int num_blocks, int64_t page_codes, void* kdst, void* vdst,
+                                   int32_t* table_out, cudaStream_t stream, int num_sms) {
+  const int64_t items = int64_t(num_seqs) * max_blocks;
+  const int64_t max_grid = int64_t(num_sms) * 8;
+  const int grid = int(items < max_grid ? items : max_grid);
+  widen_fp8_pages_kernel<<<grid, kAppendThreads, 0, stream>>>(
+      static_cast<const uint4*>(k8), static_cast<const uint4*>(v8), tables, lens, num_seqs,
+      max_blocks, num_blocks, int(page_codes / 16), static_cast<uint4*>(kdst),
+      static_cast<uint4*>(vdst), table_out);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -96,6 +96,7 @@ struct PrefillParams {
   int causal;
   int context_len;
   float scale_log2;
+  float out_scale;              // multiplies the output (1, or v_scale over FP8 pools)
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -493,7 +494,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (lane == 0) pf_abort(abort_flag);
       } else {
         tc_fence_after();
-        const float inv = 1.f / lsum;
+        const float inv = p.out_scale / lsum;
         const size_t orow_idx = size_t(qs + tok) * p.q_heads + size_t(kvh) * G + head;
         float* orow = p.out + orow_idx * D;
         if (p.lse && valid_row) p.lse[orow_idx] = m_used + __log2f(lsum);
@@ -568,6 +569,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.out = a.out;
   prm.lse = a.lse;
   prm.context_len = a.context_len;
+  prm.out_scale = a.out_scale;
   prm.num_seqs = a.num_seqs;
   prm.q_heads = a.q_heads;
   prm.kv_heads = a.kv_heads;

@@ -194,6 +194,81 @@ int make_cascade_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int m
   return PKV_OK;
 }
 
+// Argument checks shared by the bf16 and FP8 prefill entry points.
+int check_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q, int max_q_len,
+                  int q_heads, const void* k_cache, const void* v_cache,
+                  const pkv_cache_desc& cache, const int32_t* block_tables,
+                  int max_blocks_per_seq, const int32_t* context_lens, float scale,
+                  const float* out) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || q_heads <= 0) return PKV_EINVAL;
+  if (q_heads % cache.kv_heads) return PKV_EUNSUPPORTED;
+  if (!supported_group(q_heads / cache.kv_heads)) return PKV_EUNSUPPORTED;
+  if (cache.d_head != 64 && cache.d_head != 128) return PKV_EUNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_EINVAL;
+  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
+  if ((long long)num_seqs * cache.kv_heads > INT32_MAX) return PKV_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_EINVAL;
+  return PKV_OK;
+}
+
+// Tensor maps and launch of the tensor-core prefill over bf16 pools.
+int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q, int max_q_len,
+                int q_heads, const void* k_cache, const void* v_cache,
+                const pkv_cache_desc& cache, const int32_t* block_tables,
+                int max_blocks_per_seq, const int32_t* context_lens, int causal,
+                float scale_log2, float out_scale, float* out, cudaStream_t stream) {
+  const int group = q_heads / cache.kv_heads;
+  const int rows = pkv::prefill_rows_per_tile();
+  CUtensorMap tq, tk, tv;
+  if (!encode_query_map(&tq, q, total_q, q_heads, cache.d_head, group, rows / group) ||
+      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::PrefillArgs a;
+  a.q_start = q_start;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_q_len = max_q_len;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2;
+  a.out_scale = out_scale;
+  cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+// Workspace of the FP8 prefill: bf16 K and V scratch pools of
+// num_seqs * max_blocks pages, then the scratch block table.
+struct Fp8PrefillLayout {
+  size_t k_off = 0, v_off = 0, table_off = 0, total = 0;
+};
+
+bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
+                        Fp8PrefillLayout* w) {
+  if (num_seqs <= 0 || max_blocks <= 0 || kv_heads <= 0 || d_head <= 0) return false;
+  const long long pages = (long long)num_seqs * max_blocks;
+  if (pages > INT32_MAX || (long long)max_blocks * kBlockSize > INT32_MAX) return false;
+  const size_t pool = size_t(pages) * kBlockSize * size_t(kv_heads) * size_t(d_head) * 2;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  w->k_off = 0;
+  w->v_off = up(pool);
+  w->table_off = w->v_off + up(pool);
+  w->total = w->table_off + up(size_t(pages) * 4);
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -426,43 +501,53 @@ int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_s
                                 const int32_t* block_tables, int max_blocks_per_seq,
                                 const int32_t* context_lens, int causal, float scale, float* out,
                                 pkv_stream_t stream) {
-  int st = check_cache_desc(cache);
+  int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                         cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
+  if (st != PKV_OK || num_seqs == 0 || total_q == 0 || max_q_len == 0) return st;
+  return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache, cache,
+                     block_tables, max_blocks_per_seq, context_lens, causal,
+                     scale * 1.4426950408889634f, 1.f, out, static_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_paged_prefill_attention_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
+                                                       int kv_heads, int d_head) {
+  Fp8PrefillLayout w;
+  return fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w) ? w.total : 0;
+}
+
+int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int num_seqs,
+                                    int total_q, int max_q_len, int q_heads, const void* k_cache,
+                                    const void* v_cache, pkv_cache_desc cache,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int causal, float scale,
+                                    float k_scale, float v_scale, float* out, void* workspace,
+                                    size_t ws_bytes, pkv_stream_t stream) {
+  int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                         cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
   if (st != PKV_OK) return st;
-  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || q_heads <= 0) return PKV_EINVAL;
-  if (q_heads % cache.kv_heads) return PKV_EUNSUPPORTED;
-  const int group = q_heads / cache.kv_heads;
-  if (!supported_group(group)) return PKV_EUNSUPPORTED;
-  if (cache.d_head != 64 && cache.d_head != 128) return PKV_EUNSUPPORTED;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return PKV_EINVAL;
   if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
-  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return PKV_EINVAL;
-  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
-  if ((long long)num_seqs * cache.kv_heads > INT32_MAX) return PKV_EUNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
-    return PKV_EINVAL;
-  const int rows = pkv::prefill_rows_per_tile();
-  CUtensorMap tq, tk, tv;
-  if (!encode_query_map(&tq, q, total_q, q_heads, cache.d_head, group, rows / group) ||
-      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
-    return PKV_ECUDA;
-  pkv::PrefillArgs a;
-  a.q_start = q_start;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.out = out;
-  a.num_seqs = num_seqs;
-  a.total_q = total_q;
-  a.max_q_len = max_q_len;
-  a.q_heads = q_heads;
-  a.kv_heads = cache.kv_heads;
-  a.d_head = cache.d_head;
-  a.num_blocks = cache.num_blocks;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.causal = causal ? 1 : 0;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  Fp8PrefillLayout w;
+  if (!fp8_prefill_layout(num_seqs, max_blocks_per_seq, cache.kv_heads, cache.d_head, &w))
+    return PKV_EUNSUPPORTED;
+  if (!workspace || ws_bytes < w.total) return PKV_ENOMEM;
+  if (!aligned(workspace, 256)) return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_widen_fp8_pages(
+      k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+      cache.num_blocks, int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws + w.k_off,
+      ws + w.v_off, reinterpret_cast<int32_t*>(ws + w.table_off), cs, sms);
+  if (e != cudaSuccess) return PKV_ECUDA;
+  pkv_cache_desc scratch = cache;
+  scratch.num_blocks = num_seqs * max_blocks_per_seq;
+  return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, ws + w.k_off,
+                     ws + w.v_off, scratch, reinterpret_cast<const int32_t*>(ws + w.table_off),
+                     max_blocks_per_seq, context_lens, causal,
+                     scale * k_scale * 1.4426950408889634f, v_scale, out, cs);
 }
 
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,

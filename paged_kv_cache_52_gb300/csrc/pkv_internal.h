@@ -20,6 +20,12 @@ cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v,
                                  const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                                  void* v_cache, int64_t num_slots, int row_elems, float k_inv,
                                  float v_inv, cudaStream_t stream, int num_sms);
+// FP8 pages of each sequence's context -> bf16 scratch pool + scratch table
+// (page_codes = 16 * kv_heads * d_head, a multiple of 16).
+cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
+                                   const int32_t* lens, int num_seqs, int max_blocks,
+                                   int num_blocks, int64_t page_codes, void* kdst, void* vdst,
+                                   int32_t* table_out, cudaStream_t stream, int num_sms);
 // Copy-on-write block copies: block_bytes a multiple of 16.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int64_t block_bytes, cudaStream_t stream,
@@ -66,6 +72,7 @@ struct PrefillArgs {
   const int32_t* context_lens;  // null: context_len below
   float* out;
   float* lse = nullptr;         // optional per-row log2-sum-exp
+  float out_scale = 1.f;        // multiplies the output (FP8 pools: v_scale)
   int context_len = 0;
   int num_seqs, total_q, max_q_len, q_heads, kv_heads, d_head, num_blocks;
   int max_blocks_per_seq;

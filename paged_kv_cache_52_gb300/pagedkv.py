@@ -87,6 +87,11 @@ SIGNATURES = {
     "pkv_paged_decode_attention_noalloc": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                             ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_paged_prefill_attention_fp8_workspace_bytes": ([ctypes.c_int] * 4, _sz),
+    "pkv_paged_prefill_attention_fp8": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int,
+                                         _vp, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _sz, _vp],
+                                        ctypes.c_int),
     # host block manager (pagedkv_blocks.h); pointers are host memory
     "pkv_bm_create": ([_i32, _i32, ctypes.POINTER(_vp)], ctypes.c_int),
     "pkv_bm_destroy": ([_vp], None),
@@ -335,6 +340,52 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
         int(bool(causal)), float(scale), _ptr(out), _stream(q))
     _check("pkv_paged_prefill_attention", st)
     return out
+
+
+def paged_prefill_attention_fp8(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, causal: bool, scale: float,
+                                k_scale: float, v_scale: float,
+                                out: Optional[torch.Tensor] = None,
+                                max_q_len: Optional[int] = None,
+                                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Chunked prefill over FP8 (e4m3) pools with per-pool scales: the
+    attention of the dequantized cache.  ``workspace`` (uint8, at least
+    ``prefill_fp8_workspace_bytes(...)``) holds the widened pages."""
+    _check_fp8_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [total, Hq, d] bf16 CUDA tensor")
+    total, hq, d = q.shape
+    S = context_lens.shape[0]
+    _need(q_start.dtype == torch.int32 and q_start.is_contiguous() and q_start.shape == (S + 1,),
+          "q_start must be contiguous int32 [S + 1]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be contiguous int32 [S]")
+    if max_q_len is None:
+        max_q_len = int((q_start[1:] - q_start[:-1]).max().item()) if S else 0
+    if out is None:
+        out = torch.empty(total, hq, d, dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (total, hq, d),
+          "out must be contiguous float32 [total, Hq, d]")
+    need = prefill_fp8_workspace_bytes(S, block_tables.shape[1], k_cache.shape[2], d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.pkv_paged_prefill_attention_fp8(
+        _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+        cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        int(bool(causal)), float(scale), float(k_scale), float(v_scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(q))
+    _check("pkv_paged_prefill_attention_fp8", st)
+    return out
+
+
+def prefill_fp8_workspace_bytes(num_seqs: int, max_blocks_per_seq: int, kv_heads: int,
+                                d_head: int) -> int:
+    return lib.pkv_paged_prefill_attention_fp8_workspace_bytes(
+        int(num_seqs), int(max_blocks_per_seq), int(kv_heads), int(d_head))
 
 
 def paged_decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,

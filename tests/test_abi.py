@@ -129,3 +129,23 @@ def test_fp8_and_shared_prefix_host_validation(pk):
     assert lib.pkv_paged_decode_attention_shared_prefix(dummy, 4, 8, dummy, dummy, d64, dummy,
                                                         2, dummy, 250, 4, 0.125, dummy, dummy,
                                                         1 << 30, null) == -1
+
+
+def test_fp8_prefill_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
+    need = lib.pkv_paged_prefill_attention_fp8_workspace_bytes(4, 8, 2, 128)
+    pool = 4 * 8 * 16 * 2 * 128 * 2                     # bf16 pages of 4 x 8 blocks
+    assert need == 2 * pool + 256                        # K, V scratch pools + the table
+    assert lib.pkv_paged_prefill_attention_fp8_workspace_bytes(0, 8, 2, 128) == 0
+
+    def call(desc=d128, k_scale=1.0, v_scale=1.0, ws=dummy, wsb=need, S=4):
+        return lib.pkv_paged_prefill_attention_fp8(dummy, dummy, S, 40, 16, 8, dummy, dummy, desc,
+                                                   dummy, 8, dummy, 1, 0.1, k_scale, v_scale,
+                                                   dummy, ws, wsb, null)
+    assert call(S=0) == 0                                 # nothing to do
+    assert call(k_scale=0.0) == -1 and call(v_scale=float("inf")) == -1
+    assert call(desc=_desc(pk, d=96)) == -2
+    assert call(wsb=need - 1) == -4 and call(ws=null) == -4
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -1   # workspace not 256-byte aligned
