@@ -655,6 +655,53 @@ def e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barr
     torch.testing.assert_close(outs_h[(K - 1) % 2], out.cpu(), rtol=0, atol=0)
     return max_over_ranks(s.elapsed_time(e), dev)
 
+def run_verify(dev, pagedkv, E, peak):
+    """Speculative verification at the 70B-GQA decode shape: 256 sequences,
+    K drafted tokens each (already appended), contexts U[1024, 8192].  The
+    multi-query decode kernel against the same attention through the chunked
+    prefill kernel (K-token causal chunks).  KV bytes are those of the decode."""
+    g = torch.Generator().manual_seed(3005)
+    lens = torch.randint(1024, 8193, (256,), generator=g).tolist()
+    res = {}
+    for K in (2, 4):
+        w = wl.make_chunked_workload(64, 8, 128, [L - K for L in lens], [K] * 256, config_id=9,
+                                     device=dev, gen_device=dev)
+        S, hq, d = 256, 64, 128
+        q = w.q_prefill.view(S, K, hq, d)
+        max_len = max(lens)
+        ws = pagedkv.verify_workspace(S, K, hq, 8, d, max_len, dev)
+        out = torch.empty(S, K, hq, d, dtype=torch.float32, device=dev)
+        pout = torch.empty(w.q_prefill.shape, dtype=torch.float32, device=dev)
+        calls = {
+            "verify_kernel": lambda: pagedkv.paged_verify_attention(
+                q, w.k_cache, w.v_cache, w.prefill_tables, w.prefill_lens, w.scale, out=out,
+                max_context_len=max_len, workspace=ws),
+            "prefill_kernel": lambda: pagedkv.paged_prefill_attention(
+                w.q_prefill, w.q_start, w.k_cache, w.v_cache, w.prefill_tables, w.prefill_lens,
+                True, w.scale, out=pout, max_q_len=K),
+        }
+        kv = sum(lens) * 2 * 8 * d * 2
+        row = {"kv_bytes": kv}
+        for name, f in calls.items():
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            a, b = E(enable_timing=True), E(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                f()
+            b.record()
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b) / 20
+            row[name] = {"ms": round(t, 4), "GBps": round(kv / (t / 1e3) / 1e9, 1),
+                         "frac_of_hbm": round(kv / (t / 1e3) / 1e9 / peak, 4)}
+        row["tokens_verified_per_s"] = round(S * K / (row["verify_kernel"]["ms"] / 1e3), 1)
+        res[f"K{K}"] = row
+        del w, q, out, pout, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
@@ -797,6 +844,7 @@ def run_ours(args):
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)
         line["small_batch_decode"] = run_small_batch(dev, pagedkv, E)
+        line["speculative_verify"] = run_verify(dev, pagedkv, E, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         _, info = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = info

@@ -230,6 +230,36 @@ PKV_API int pkv_paged_decode_attention_shared_prefix(
     void* workspace, size_t ws_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_paged_verify_attention -- multi-query decode, the verification step of
+ * speculative decoding ("Cache KV, attention et optimisation de
+ * l'inference", section "Decodage speculatif": guess several next tokens
+ * cheaply, then check them all in one pass).  Each sequence has q_len query
+ * tokens, already appended, as the last q_len positions of its context:
+ * token t (0 <= t < q_len) sits at position context_len - q_len + t and
+ * attends over keys 0 .. context_len - q_len + t (the bottom-right causal
+ * mask of a q_len-token prefill chunk).
+ *   q   : [num_seqs][q_len][q_heads][d_head] bf16, contiguous.
+ *   out : [num_seqs][q_len][q_heads][d_head] fp32.
+ * (q_heads / kv_heads) * q_len must be <= 32 (e.g. 4 drafted tokens with a
+ * GQA group of 8), else PKV_EUNSUPPORTED.  The K/V bytes of a (sequence, KV
+ * head) are read once for all its query tokens and heads; long contexts are
+ * split as in the decode (same plan for the given partition_blocks, 0 =
+ * library choice), with a workspace of
+ * pkv_verify_workspace_bytes(...) device bytes (0: none needed).  A context
+ * shorter than q_len sets PKV_DEVERR_BAD_QUERY_RANGE; tokens placed before
+ * position 0 see no key and return zeros.
+ */
+PKV_API size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_heads,
+                                          int d_head, int max_context_len, int partition_blocks);
+PKV_API int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_heads,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_cache_desc cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float scale, float* out,
+                                       void* workspace, size_t ws_bytes, int partition_blocks,
+                                       pkv_stream_t stream);
+
+/*
  * FP8 KV cache.  The pages name FP8 KV caches as the way to halve decode's
  * KV bytes ("Cache KV, attention et optimisation de l'inference", section
  * "Utilisez-le": --kv-cache-dtype fp8; "第 10 讲：推理（Inference）": fewer

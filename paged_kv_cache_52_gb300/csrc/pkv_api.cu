@@ -269,6 +269,24 @@ bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
   return true;
 }
 
+// Split plan of the multi-query decode: the decode's partitions, with
+// num_seqs * q_len rows per query head in the workspace.
+int make_verify_plan(int num_seqs, int q_len, int q_heads, int kv_heads, int d_head,
+                     int max_context_len, int partition_blocks, Plan* plan) {
+  if (q_len <= 0) return PKV_EINVAL;
+  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, partition_blocks, plan);
+  if (st != PKV_OK) return st;
+  if ((long long)(q_heads / kv_heads) * q_len > pkv::verify_max_rows()) return PKV_EUNSUPPORTED;
+  if ((long long)num_seqs * q_len > INT32_MAX) return PKV_EUNSUPPORTED;
+  if (plan->num_parts > 1) {
+    const size_t rows =
+        size_t(num_seqs) * size_t(q_len) * size_t(q_heads) * size_t(plan->num_parts);
+    plan->lse_offset = (rows * size_t(d_head) * sizeof(float) + 255) / 256 * 256;
+    plan->ws_bytes = plan->lse_offset + rows * sizeof(float);
+  }
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -550,6 +568,63 @@ int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int n
                      scale * k_scale * 1.4426950408889634f, v_scale, out, cs);
 }
 
+size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_heads, int d_head,
+                                  int max_context_len, int partition_blocks) {
+  Plan plan;
+  if (make_verify_plan(num_seqs, q_len, q_heads, kv_heads, d_head, max_context_len,
+                       partition_blocks, &plan) != PKV_OK)
+    return 0;
+  return plan.ws_bytes;
+}
+
+int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_heads,
+                               const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float scale,
+                               float* out, void* workspace, size_t ws_bytes,
+                               int partition_blocks, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  Plan plan;
+  st = make_verify_plan(num_seqs, q_len, q_heads, cache.kv_heads, cache.d_head, max_context_len,
+                        partition_blocks, &plan);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+    return PKV_EINVAL;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
+    if (!aligned(workspace, 256)) return PKV_EINVAL;
+  }
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+    return PKV_ECUDA;
+  pkv::DecodeArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                        plan.lse_offset)
+                             : nullptr;
+  a.num_seqs = num_seqs;
+  a.q_heads = q_heads;
+  a.kv_heads = cache.kv_heads;
+  a.d_head = cache.d_head;
+  a.num_blocks = cache.num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.partition_blocks = plan.partition_blocks;
+  a.num_parts = plan.num_parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out_scale = 1.f;
+  cudaError_t e = pkv::launch_paged_verify(a, q_len, &tk, &tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
                                                  int d_head, int max_context_len,
                                                  int prefix_blocks) {
@@ -648,8 +723,9 @@ int pkv_get_device_error(unsigned int* word, int clear) {
   const unsigned d = pkv::read_decode_error(clear != 0);
   const unsigned f = pkv::read_prefill_error(clear != 0);
   const unsigned d8 = pkv::read_decode_fp8_error(clear != 0);
-  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u) return PKV_ECUDA;
-  *word = a | d | f | d8;
+  const unsigned v = pkv::read_verify_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u) return PKV_ECUDA;
+  *word = a | d | f | d8 | v;
   return PKV_OK;
 }
 

@@ -52,6 +52,15 @@ struct DecodeArgs {
   const float* extra_lse = nullptr;
 };
 
+// Multi-query decode (speculative verification): q_len query tokens per
+// sequence, rows (seq * q_len + t) * q_heads + head of q and out; group *
+// q_len <= verify_max_rows().  Uses the decode plan and workspace layout with
+// num_seqs * q_len rows per head.
+int verify_max_rows();
+cudaError_t launch_paged_verify(const DecodeArgs& a, int q_len, const CUtensorMap* tmap_k,
+                                const CUtensorMap* tmap_v, cudaStream_t stream);
+unsigned read_verify_error(bool clear);
+
 // Number of K/V stages and warps the decode kernel uses (for the plan).
 int decode_warps_per_cta();
 int decode_max_partition_blocks();

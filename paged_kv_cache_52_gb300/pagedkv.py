@@ -92,6 +92,10 @@ SIGNATURES = {
                                          ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int,
                                          _vp, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _sz, _vp],
                                         ctypes.c_int),
+    "pkv_verify_workspace_bytes": ([ctypes.c_int] * 7, _sz),
+    "pkv_paged_verify_attention": ([_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                    CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
+                                    _vp, _sz, ctypes.c_int, _vp], ctypes.c_int),
     # host block manager (pagedkv_blocks.h); pointers are host memory
     "pkv_bm_create": ([_i32, _i32, ctypes.POINTER(_vp)], ctypes.c_int),
     "pkv_bm_destroy": ([_vp], None),
@@ -386,6 +390,51 @@ def prefill_fp8_workspace_bytes(num_seqs: int, max_blocks_per_seq: int, kv_heads
                                 d_head: int) -> int:
     return lib.pkv_paged_prefill_attention_fp8_workspace_bytes(
         int(num_seqs), int(max_blocks_per_seq), int(kv_heads), int(d_head))
+
+
+def verify_workspace(num_seqs: int, q_len: int, q_heads: int, kv_heads: int, d_head: int,
+                     max_context_len: int, device, partition_blocks: int = 0):
+    """Workspace for ``paged_verify_attention`` (None when no split is planned)."""
+    n = lib.pkv_verify_workspace_bytes(int(num_seqs), int(q_len), int(q_heads), int(kv_heads),
+                                       int(d_head), int(max_context_len), int(partition_blocks))
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def paged_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None,
+                           max_context_len: Optional[int] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           partition_blocks: int = 0) -> torch.Tensor:
+    """Speculative verification: ``q [S, K, Hq, d]`` holds the last K tokens of
+    each sequence (already appended); token t attends causally over the first
+    ``context_len - K + t + 1`` positions.  Returns ``out [S, K, Hq, d]`` fp32."""
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 4 and q.is_contiguous(),
+          "q must be a contiguous [S, K, Hq, d] bf16 CUDA tensor")
+    S, K, hq, d = q.shape
+    _need(d == k_cache.shape[3], "q and cache head dims differ")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous() and
+          context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if out is None:
+        out = torch.empty(S, K, hq, d, dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, K, hq, d),
+          "out must be contiguous float32 [S, K, Hq, d]")
+    if workspace is None:
+        workspace = verify_workspace(S, K, hq, k_cache.shape[2], d, max_context_len, q.device,
+                                     partition_blocks)
+    st = lib.pkv_paged_verify_attention(
+        _ptr(q), S, K, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+        int(partition_blocks), _stream(q))
+    _check("pkv_paged_verify_attention", st)
+    return out
 
 
 def paged_decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
