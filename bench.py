@@ -57,6 +57,10 @@ def parse_args():
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the continuous-batching mixed-step measurement")
     ap.add_argument("--mixed-steps", type=int, default=30)
+    ap.add_argument("--only-verify", action="store_true",
+                    help="run only the speculative-verification comparison")
+    ap.add_argument("--verify-seqs", type=int, default=256,
+                    help="sequences of the speculative-verification workload")
     ap.add_argument("--mixed-decodes", type=int, default=None,
                     help="shrink the mixed step to this many decode sequences (profiling runs)")
     ap.add_argument("--only-mixed", action="store_true",
@@ -655,18 +659,18 @@ def e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barr
     torch.testing.assert_close(outs_h[(K - 1) % 2], out.cpu(), rtol=0, atol=0)
     return max_over_ranks(s.elapsed_time(e), dev)
 
-def run_verify(dev, pagedkv, E, peak):
+def run_verify(dev, pagedkv, E, peak, num_seqs=256):
     """Speculative verification at the 70B-GQA decode shape: 256 sequences,
     K drafted tokens each (already appended), contexts U[1024, 8192].  The
     multi-query decode kernel against the same attention through the chunked
     prefill kernel (K-token causal chunks).  KV bytes are those of the decode."""
     g = torch.Generator().manual_seed(3005)
-    lens = torch.randint(1024, 8193, (256,), generator=g).tolist()
-    res = {}
+    lens = torch.randint(1024, 8193, (num_seqs,), generator=g).tolist()
+    res = {"num_seqs": num_seqs}
     for K in (2, 4):
-        w = wl.make_chunked_workload(64, 8, 128, [L - K for L in lens], [K] * 256, config_id=9,
-                                     device=dev, gen_device=dev)
-        S, hq, d = 256, 64, 128
+        w = wl.make_chunked_workload(64, 8, 128, [L - K for L in lens], [K] * num_seqs,
+                                     config_id=9, device=dev, gen_device=dev)
+        S, hq, d = num_seqs, 64, 128
         q = w.q_prefill.view(S, K, hq, d)
         max_len = max(lens)
         ws = pagedkv.verify_workspace(S, K, hq, 8, d, max_len, dev)
@@ -717,6 +721,11 @@ def run_ours(args):
 
     if args.only_mixed:
         print(json.dumps({"mixed_step": run_mixed(args, dev, pagedkv, torch.cuda.Event)}))
+        return
+    if args.only_verify:
+        peak, _ = measured_peak()
+        print(json.dumps({"speculative_verify": run_verify(dev, pagedkv, torch.cuda.Event, peak,
+                                                           args.verify_seqs)}))
         return
     spec = wl.DECODE_SPECS[args.workload]
     w = wl.make_decode_workload(spec, device=dev, gen_device=dev,
