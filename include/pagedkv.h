@@ -202,6 +202,33 @@ PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, i
                                         pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention_ex -- pkv_paged_prefill_attention with a
+ * workspace that buys a faster kernel.  The V pages the chunks' sequences
+ * use are first converted to f16 in the workspace (page j of sequence s to
+ * scratch block s * max_blocks_per_seq + j); the tensor-core prefill then
+ * reads K from the pool and V from the workspace and feeds P to the P V
+ * product as one f16 operand (rounding error <= 2^-11 relative, so the
+ * output moves by at most 2^-11 times the largest |V| a row attends to),
+ * instead of the bf16 hi + lo pair the plain entry point needs -- one third
+ * less tensor-core work for one bf16 read and one f16 write per V element of
+ * those pages.  The conversion is exact for |v| in [2^-14, 65504]; smaller
+ * values become f16 subnormals (absolute error < 2^-25); a value of
+ * magnitude 65520 or more overflows and sets PKV_DEVERR_FP16_RANGE.
+ * workspace: >= pkv_paged_prefill_workspace_bytes(num_seqs,
+ * max_blocks_per_seq, kv_heads, d_head) device bytes, 256-byte aligned
+ * (PKV_ENOMEM if smaller); NULL runs pkv_paged_prefill_attention.
+ */
+PKV_API size_t pkv_paged_prefill_workspace_bytes(int num_seqs, int max_blocks_per_seq,
+                                                 int kv_heads, int d_head);
+PKV_API int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start, int num_seqs,
+                                           int total_q, int max_q_len, int q_heads,
+                                           const void* k_cache, const void* v_cache,
+                                           pkv_cache_desc cache, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int causal, float scale, float* out, void* workspace,
+                                           size_t ws_bytes, pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_attention_shared_prefix -- the same result as
  * pkv_paged_decode_attention when every sequence's first prefix_blocks pages
  * are the same physical blocks (a shared system prompt stored once and
@@ -299,9 +326,11 @@ PKV_API int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_he
  * pkv_paged_prefill_attention_fp8 -- pkv_paged_prefill_attention over FP8
  * pools: the attention of the dequantized cache, as above.  The pages a
  * chunk's sequence uses (its first ceil(context_len / 16) block-table
- * entries) are first widened to bf16 in the workspace -- exact, every e4m3
- * value is a bf16 value -- and the tensor-core prefill then runs on them with
- * k_scale folded into the softmax scale and v_scale into the output.  That
+ * entries) are first widened in the workspace, K to bf16 and V to f16 --
+ * exact, every e4m3 value is a bf16 and an f16 value -- and the tensor-core
+ * prefill then runs on them with k_scale folded into the softmax scale,
+ * v_scale into the output, and P as one f16 operand (see
+ * pkv_paged_prefill_attention_ex).  That
  * costs one FP8 read and one bf16 write per cached element of those pages on
  * top of the bf16 prefill.  d_head 64 or 128.
  * workspace: >= pkv_paged_prefill_attention_fp8_workspace_bytes(num_seqs,

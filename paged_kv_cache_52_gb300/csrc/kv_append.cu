@@ -224,6 +224,13 @@ namespace pkv {
 
 constexpr int kPageTokens = 16;
 
+// Two floats -> packed f16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2_cvt(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   uint32_t h2;
   asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
@@ -232,6 +239,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   const __half2 h = *reinterpret_cast<const __half2*>(&h2);
   const float2 f = __half22float2(h);
   return pack_bf16x2(f.x, f.y);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "h"(two));
+  return h2;
+}
+
+__device__ __forceinline__ uint4 widen8_f16(uint32_t a, uint32_t b) {
+  return make_uint4(e4m3x2_to_f16x2(uint16_t(a & 0xffffu)), e4m3x2_to_f16x2(uint16_t(a >> 16)),
+                    e4m3x2_to_f16x2(uint16_t(b & 0xffffu)), e4m3x2_to_f16x2(uint16_t(b >> 16)));
 }
 
 __device__ __forceinline__ uint4 widen8(uint32_t a, uint32_t b) {
@@ -244,7 +264,7 @@ widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v
                        const int32_t* __restrict__ tables, const int32_t* __restrict__ lens,
                        int num_seqs, int max_blocks, int num_blocks, int page_vec16,
                        uint4* __restrict__ kdst, uint4* __restrict__ vdst,
-                       int32_t* __restrict__ table_out) {
+                       int32_t* __restrict__ table_out, bool v_f16) {
   const int64_t items = int64_t(num_seqs) * max_blocks;
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int s = int(item / max_blocks), j = int(item - int64_t(s) * max_blocks);
@@ -263,8 +283,8 @@ widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v
       const uint4 vc = ok ? __ldg(vs + i) : make_uint4(0, 0, 0, 0);
       kd[2 * i] = widen8(kc.x, kc.y);
       kd[2 * i + 1] = widen8(kc.z, kc.w);
-      vd[2 * i] = widen8(vc.x, vc.y);
-      vd[2 * i + 1] = widen8(vc.z, vc.w);
+      vd[2 * i] = v_f16 ? widen8_f16(vc.x, vc.y) : widen8(vc.x, vc.y);
+      vd[2 * i + 1] = v_f16 ? widen8_f16(vc.z, vc.w) : widen8(vc.z, vc.w);
     }
   }
 }
@@ -272,14 +292,69 @@ widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v
 cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
                                    const int32_t* lens, int num_seqs, int max_blocks,
                                    int num_blocks, int64_t page_codes, void* kdst, void* vdst,
-                                   int32_t* table_out, cudaStream_t stream, int num_sms) {
+                                   int32_t* table_out, bool v_f16, cudaStream_t stream,
+                                   int num_sms) {
   const int64_t items = int64_t(num_seqs) * max_blocks;
   const int64_t max_grid = int64_t(num_sms) * 8;
   const int grid = int(items < max_grid ? items : max_grid);
   widen_fp8_pages_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k8), static_cast<const uint4*>(v8), tables, lens, num_seqs,
       max_blocks, num_blocks, int(page_codes / 16), static_cast<uint4*>(kdst),
-      static_cast<uint4*>(vdst), table_out);
+      static_cast<uint4*>(vdst), table_out, v_f16);
+  return cudaGetLastError();
+}
+
+// bf16 V pages -> f16 pages for the prefill's single-product P V: page j of
+// sequence s (j < ceil(context_len / 16)) into block s * max_blocks + j of an
+// f16 scratch pool, named by entry (s, j) of a scratch table.  Exact for
+// |v| in [2^-14, 65504]; smaller values become f16 subnormals (absolute error
+// below 2^-25); a value of magnitude 65520 or more overflows and sets the f16
+// range bit of the error word.
+constexpr unsigned kErrFp16RangeAppend = 1u << 6;
+
+__global__ void __launch_bounds__(kAppendThreads)
+v_pages_to_f16_kernel(const uint4* __restrict__ v, const int32_t* __restrict__ tables,
+                      const int32_t* __restrict__ lens, int num_seqs, int max_blocks,
+                      int num_blocks, int page_vec, uint4* __restrict__ vdst,
+                      int32_t* __restrict__ table_out) {
+  const int64_t items = int64_t(num_seqs) * max_blocks;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int s = int(item / max_blocks), j = int(item - int64_t(s) * max_blocks);
+    if (threadIdx.x == 0) table_out[item] = int32_t(item);
+    const int len = min(max(__ldg(lens + s), 0), max_blocks * kPageTokens);
+    if (j * kPageTokens >= len) continue;
+    const int32_t src = __ldg(tables + item);
+    const bool ok = src >= 0 && src < num_blocks;
+    if (!ok && threadIdx.x == 0) atomicOr(&g_append_error, kErrBadBlockId);
+    const uint4* vs = v + int64_t(ok ? src : 0) * page_vec;
+    uint4* vd = vdst + item * page_vec;
+    bool in_range = true;
+    for (int i = threadIdx.x; i < page_vec; i += kAppendThreads) {
+      const uint4 x = ok ? __ldg(vs + i) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float a = bf16_lo_to_f32(w[c]), b = bf16_hi_to_f32(w[c]);
+        in_range &= !(fabsf(a) >= 65520.f) && !(fabsf(b) >= 65520.f);
+        o[c] = pack_f16x2_cvt(a, b);
+      }
+      vd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (!in_range) atomicOr(&g_append_error, kErrFp16RangeAppend);
+  }
+}
+
+cudaError_t launch_v_pages_to_f16(const void* v, const int32_t* tables, const int32_t* lens,
+                                  int num_seqs, int max_blocks, int num_blocks, int64_t page_elems,
+                                  void* vdst, int32_t* table_out, cudaStream_t stream,
+                                  int num_sms) {
+  const int64_t items = int64_t(num_seqs) * max_blocks;
+  const int64_t max_grid = int64_t(num_sms) * 8;
+  const int grid = int(items < max_grid ? items : max_grid);
+  v_pages_to_f16_kernel<<<grid, kAppendThreads, 0, stream>>>(
+      static_cast<const uint4*>(v), tables, lens, num_seqs, max_blocks, num_blocks,
+      int(page_elems / 8), static_cast<uint4*>(vdst), table_out);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,8 @@ struct PrefillParams {
   int context_len;
   float scale_log2;
   float out_scale;              // multiplies the output (1, or v_scale over FP8 pools)
+  const int32_t* v_block_tables;  // null: V pages use block_tables
+  int v_num_blocks;             // blocks of the V pool
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -113,7 +115,9 @@ __device__ __forceinline__ void pf_abort(volatile int* abort_flag) {
   atomicOr(&g_prefill_error, kErrWaitTimeout);
 }
 
-template <int D, int G>
+// F16PV: V is an f16 pool and P enters the PV product as one f16 operand;
+// otherwise V is bf16 and P enters as bf16 hi + lo.
+template <int D, int G, bool F16PV>
 __global__ void __launch_bounds__(kPfThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
@@ -207,7 +211,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       issued_q = 1;
     }
     if (is_v && lane == 0) tma_prefetch_desc(&tmap_v);
-    const int32_t* table = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+    const int32_t* table = (is_v && p.v_block_tables ? p.v_block_tables : p.block_tables) +
+                           size_t(seq) * p.max_blocks_per_seq;
+    const int pool_blocks = is_v ? p.v_num_blocks : p.num_blocks;
     constexpr int kLoads = 8 * (D / 64);  // 8 pages x D/64 column halves
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % stages;
@@ -228,7 +234,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         int id = -1;  // pages past the context: the box is out of bounds and reads zeros
         if (blk < nblk) {
           id = __ldg(table + blk);
-          if (id < 0 || id >= p.num_blocks) atomicOr(&g_prefill_error, kErrBadBlockId);
+          if (id < 0 || id >= pool_blocks) atomicOr(&g_prefill_error, kErrBadBlockId);
         }
         tma_load_4d(ring + st * L::kTileBytes + h * L::kHalf + b * 2048, map, full0 + 8 * st,
                     h * 64, kvh, 0, id);
@@ -247,7 +253,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // ================= MMA issuer (one thread) =================
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, kPfKvTile, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t kIdescPV =
+          F16PV ? idesc_f16_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
       // S_t(j) = Q_t K_j^T into TMEM columns [256 t, 256 t + 128)
       auto issue_s = [&](int t, int j) {
         const uint32_t q_smem = sbase + L::kQOff + t * L::kQTileBytes;
@@ -260,8 +267,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         umma_commit(bars + 8 * (kSFull0 + t));
       };
-      // O_t += P_t(j) V_j: P (bf16 hi, lo) read from TMEM over S_t's columns,
-      // V the MN-major operand (keys x d) straight from the pool layout
+      // O_t += P_t(j) V_j: P (bf16 hi, lo -- or one f16) read from TMEM over S_t's
+      // columns, V the MN-major operand (keys x d) straight from the pool layout
       auto issue_pv = [&](int t, int j) {
         const uint32_t v_smem = sbase + L::kVOff + (j % kPfVStages) * L::kTileBytes;
 #pragma unroll
@@ -270,7 +277,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           // keys [16 k, 16 k + 16): hi in column 64 (k / 4) + 8 (k % 4), lo 32 columns on
           const uint32_t a_hi = tmem + t * 256 + 64 * (k >> 2) + 8 * (k & 3);
           umma_bf16_ts(tmem + t * 256 + 128, a_hi, vdesc, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + t * 256 + 128, a_hi + 32, vdesc, kIdescPV, 1u);
+          if constexpr (!F16PV) umma_bf16_ts(tmem + t * 256 + 128, a_hi + 32, vdesc, kIdescPV, 1u);
         }
         umma_commit(bars + 8 * (kODone0 + t));
       };
@@ -397,7 +404,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // a tile past the row's limit leaves the max at -inf and its P all zeros
         mx = ext == -INFINITY ? -INFINITY : ext * fabsf(p.scale_log2);
       }
-      const bool resc = mx > m_used + kRescaleThreshold;
+      // f16 P: track the max exactly, so the largest weight is exactly 1 and
+      // f16 rounds only the others (<= 2^-12 relative); a lazy max would let
+      // the largest weight reach 256, rounded at up to 2^-11 relative
+      const bool resc = mx > m_used + (F16PV ? 0.f : kRescaleThreshold);
       if (__any_sync(0xffffffffu, resc)) {
         const float m_new = resc ? mx : m_used;
         const float alpha = ex2(m_used - m_new);  // 0 when m_used is -inf, 1 when unchanged
@@ -447,10 +457,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const float e0 = ex2(x0), e1 = ex2(x1);
             const uint64_t e = f2_pack(e0, e1);
             ls2[u & 1] = f2_add(ls2[u & 1], e);
-            hi[u] = pack_bf16x2(e0, e1);
-            float r0, r1;
-            f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
-            lo[u] = pack_bf16x2(r0, r1);
+            if constexpr (F16PV) {
+              hi[u] = pack_f16x2_rn(e0, e1);
+            } else {
+              hi[u] = pack_bf16x2(e0, e1);
+              float r0, r1;
+              f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
+              lo[u] = pack_bf16x2(r0, r1);
+            }
           }
         } else {
 #pragma unroll
@@ -465,10 +479,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const float e1 = key + 1 <= limit ? ex2(x1) : 0.f;
             const uint64_t e = f2_pack(e0, e1);
             ls2[u & 1] = f2_add(ls2[u & 1], e);
-            hi[u] = pack_bf16x2(e0, e1);
-            float r0, r1;
-            f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
-            lo[u] = pack_bf16x2(r0, r1);
+            if constexpr (F16PV) {
+              hi[u] = pack_f16x2_rn(e0, e1);
+            } else {
+              hi[u] = pack_bf16x2(e0, e1);
+              float r0, r1;
+              f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
+              lo[u] = pack_bf16x2(r0, r1);
+            }
           }
         }
         {
@@ -478,7 +496,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           lsum += (a0 + a1) + (b0 + b1);
         }
         tmem_st32u(lane_base + s_col + 64 * g, hi);
-        tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
+        if constexpr (!F16PV) tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -522,7 +540,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool F16PV>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap* tq,
                                     const CUtensorMap* tk, const CUtensorMap* tv,
                                     cudaStream_t stream) {
@@ -530,7 +548,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap*
   constexpr int TPT = kPfRows / G;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -539,20 +557,21 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap*
   constexpr int TPC = kPfQTiles * TPT;
   if ((prm.max_q_len + TPC - 1) / TPC > 65535) return cudaErrorInvalidValue;
   dim3 grid(prm.num_seqs * prm.kv_heads, (prm.max_q_len + TPC - 1) / TPC);
-  paged_prefill_kernel<D, G><<<grid, kPfThreads, L::kSmemBytes, stream>>>(*tq, *tk, *tv, prm);
+  paged_prefill_kernel<D, G, F16PV><<<grid, kPfThreads, L::kSmemBytes, stream>>>(*tq, *tk, *tv,
+                                                                                 prm);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F16PV>
 static cudaError_t launch_prefill_d(const PrefillParams& prm, int group, const CUtensorMap* tq,
                                     const CUtensorMap* tk, const CUtensorMap* tv,
                                     cudaStream_t st) {
   switch (group) {
-    case 1: return launch_prefill_t<D, 1>(prm, tq, tk, tv, st);
-    case 2: return launch_prefill_t<D, 2>(prm, tq, tk, tv, st);
-    case 4: return launch_prefill_t<D, 4>(prm, tq, tk, tv, st);
-    case 8: return launch_prefill_t<D, 8>(prm, tq, tk, tv, st);
-    case 16: return launch_prefill_t<D, 16>(prm, tq, tk, tv, st);
+    case 1: return launch_prefill_t<D, 1, F16PV>(prm, tq, tk, tv, st);
+    case 2: return launch_prefill_t<D, 2, F16PV>(prm, tq, tk, tv, st);
+    case 4: return launch_prefill_t<D, 4, F16PV>(prm, tq, tk, tv, st);
+    case 8: return launch_prefill_t<D, 8, F16PV>(prm, tq, tk, tv, st);
+    case 16: return launch_prefill_t<D, 16, F16PV>(prm, tq, tk, tv, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -579,9 +598,16 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.max_q_len = a.max_q_len;
   prm.causal = a.causal;
   prm.scale_log2 = a.scale_log2;
+  prm.v_block_tables = a.v_block_tables;
+  prm.v_num_blocks = a.v_block_tables ? a.v_num_blocks : a.num_blocks;
   const int group = a.q_heads / a.kv_heads;
-  if (a.d_head == 128) return launch_prefill_d<128>(prm, group, tmap_q, tmap_k, tmap_v, stream);
-  if (a.d_head == 64) return launch_prefill_d<64>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+  if (a.f16_pv) {
+    if (a.d_head == 128) return launch_prefill_d<128, true>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, true>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+  } else {
+    if (a.d_head == 128) return launch_prefill_d<128, false>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, false>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

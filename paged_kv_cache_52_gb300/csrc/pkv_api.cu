@@ -217,17 +217,22 @@ int check_prefill(const void* q, const int32_t* q_start, int num_seqs, int total
   return PKV_OK;
 }
 
-// Tensor maps and launch of the tensor-core prefill over bf16 pools.
+// Tensor maps and launch of the tensor-core prefill over bf16 K pages.  V is
+// a bf16 pool through block_tables, or (f16_pv) an f16 pool of v_num_blocks
+// blocks through v_tables (null: block_tables), with P as one f16 operand.
 int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q, int max_q_len,
                 int q_heads, const void* k_cache, const void* v_cache,
                 const pkv_cache_desc& cache, const int32_t* block_tables,
                 int max_blocks_per_seq, const int32_t* context_lens, int causal,
-                float scale_log2, float out_scale, float* out, cudaStream_t stream) {
+                float scale_log2, float out_scale, float* out, cudaStream_t stream,
+                bool f16_pv = false, const int32_t* v_tables = nullptr, int v_num_blocks = 0) {
   const int group = q_heads / cache.kv_heads;
   const int rows = pkv::prefill_rows_per_tile();
+  pkv_cache_desc vdesc = cache;
+  if (v_tables) vdesc.num_blocks = v_num_blocks;
   CUtensorMap tq, tk, tv;
   if (!encode_query_map(&tq, q, total_q, q_heads, cache.d_head, group, rows / group) ||
-      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
+      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, vdesc))
     return PKV_ECUDA;
   pkv::PrefillArgs a;
   a.q_start = q_start;
@@ -245,6 +250,9 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale_log2;
   a.out_scale = out_scale;
+  a.f16_pv = f16_pv;
+  a.v_block_tables = v_tables;
+  a.v_num_blocks = v_num_blocks;
   cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
@@ -558,14 +566,56 @@ int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int n
   cudaError_t e = pkv::launch_widen_fp8_pages(
       k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
       cache.num_blocks, int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws + w.k_off,
-      ws + w.v_off, reinterpret_cast<int32_t*>(ws + w.table_off), cs, sms);
+      ws + w.v_off, reinterpret_cast<int32_t*>(ws + w.table_off), /*v_f16=*/true, cs, sms);
   if (e != cudaSuccess) return PKV_ECUDA;
   pkv_cache_desc scratch = cache;
   scratch.num_blocks = num_seqs * max_blocks_per_seq;
   return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, ws + w.k_off,
                      ws + w.v_off, scratch, reinterpret_cast<const int32_t*>(ws + w.table_off),
                      max_blocks_per_seq, context_lens, causal,
-                     scale * k_scale * 1.4426950408889634f, v_scale, out, cs);
+                     scale * k_scale * 1.4426950408889634f, v_scale, out, cs, /*f16_pv=*/true);
+}
+
+size_t pkv_paged_prefill_workspace_bytes(int num_seqs, int max_blocks_per_seq, int kv_heads,
+                                         int d_head) {
+  Fp8PrefillLayout w;
+  if (!fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w)) return 0;
+  return w.total - w.v_off;  // the f16 V pool and the table, no K copy
+}
+
+int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start, int num_seqs,
+                                   int total_q, int max_q_len, int q_heads, const void* k_cache,
+                                   const void* v_cache, pkv_cache_desc cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int causal, float scale,
+                                   float* out, void* workspace, size_t ws_bytes,
+                                   pkv_stream_t stream) {
+  if (!workspace)
+    return pkv_paged_prefill_attention(q, q_start, num_seqs, total_q, max_q_len, q_heads,
+                                       k_cache, v_cache, cache, block_tables,
+                                       max_blocks_per_seq, context_lens, causal, scale, out,
+                                       stream);
+  int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                         cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
+  if (st != PKV_OK || num_seqs == 0 || total_q == 0 || max_q_len == 0) return st;
+  Fp8PrefillLayout w;
+  if (!fp8_prefill_layout(num_seqs, max_blocks_per_seq, cache.kv_heads, cache.d_head, &w))
+    return PKV_EUNSUPPORTED;
+  if (ws_bytes < w.total - w.v_off) return PKV_ENOMEM;
+  if (!aligned(workspace, 256)) return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* vtab = reinterpret_cast<int32_t*>(ws + (w.table_off - w.v_off));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_v_pages_to_f16(
+      v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq, cache.num_blocks,
+      int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws, vtab, cs, sms);
+  if (e != cudaSuccess) return PKV_ECUDA;
+  return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, ws, cache,
+                     block_tables, max_blocks_per_seq, context_lens, causal,
+                     scale * 1.4426950408889634f, 1.f, out, cs, /*f16_pv=*/true, vtab,
+                     num_seqs * max_blocks_per_seq);
 }
 
 size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_heads, int d_head,

@@ -25,7 +25,14 @@ cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v,
 cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
                                    const int32_t* lens, int num_seqs, int max_blocks,
                                    int num_blocks, int64_t page_codes, void* kdst, void* vdst,
-                                   int32_t* table_out, cudaStream_t stream, int num_sms);
+                                   int32_t* table_out, bool v_f16, cudaStream_t stream,
+                                   int num_sms);
+// bf16 V pages of each sequence's context -> f16 scratch pool + scratch table
+// (page_elems = 16 * kv_heads * d_head, a multiple of 8).
+cudaError_t launch_v_pages_to_f16(const void* v, const int32_t* tables, const int32_t* lens,
+                                  int num_seqs, int max_blocks, int num_blocks, int64_t page_elems,
+                                  void* vdst, int32_t* table_out, cudaStream_t stream,
+                                  int num_sms);
 // Copy-on-write block copies: block_bytes a multiple of 16.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int64_t block_bytes, cudaStream_t stream,
@@ -82,6 +89,10 @@ struct PrefillArgs {
   float* out;
   float* lse = nullptr;         // optional per-row log2-sum-exp
   float out_scale = 1.f;        // multiplies the output (FP8 pools: v_scale)
+  // V from its own (f16) pool through its own table, P as one f16 operand
+  bool f16_pv = false;
+  const int32_t* v_block_tables = nullptr;  // null: block_tables
+  int v_num_blocks = 0;
   int context_len = 0;
   int num_seqs, total_q, max_q_len, q_heads, kv_heads, d_head, num_blocks;
   int max_blocks_per_seq;

@@ -88,6 +88,10 @@ SIGNATURES = {
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                             ctypes.c_int, _vp], ctypes.c_int),
     "pkv_paged_prefill_attention_fp8_workspace_bytes": ([ctypes.c_int] * 4, _sz),
+    "pkv_paged_prefill_workspace_bytes": ([ctypes.c_int] * 4, _sz),
+    "pkv_paged_prefill_attention_ex": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
+                                        ctypes.c_int, _f32, _vp, _vp, _sz, _vp], ctypes.c_int),
     "pkv_paged_prefill_attention_fp8": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int,
                                          _vp, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _sz, _vp],
@@ -311,15 +315,28 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def prefill_workspace(num_seqs: int, max_blocks_per_seq: int, kv_heads: int, d_head: int,
+                      device) -> torch.Tensor:
+    """Workspace for ``paged_prefill_attention(..., workspace=...)``: the
+    chunks' V pages in f16 and their table."""
+    n = lib.pkv_paged_prefill_workspace_bytes(int(num_seqs), int(max_blocks_per_seq),
+                                              int(kv_heads), int(d_head))
+    _need(n > 0, "unsupported prefill workspace shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
 def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
                             v_cache: torch.Tensor, block_tables: torch.Tensor,
                             context_lens: torch.Tensor, causal: bool, scale: float,
                             out: Optional[torch.Tensor] = None,
-                            max_q_len: Optional[int] = None) -> torch.Tensor:
+                            max_q_len: Optional[int] = None,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Chunked prefill: rows ``q_start[s]:q_start[s+1]`` of ``q [total, Hq, d]``
     are the last tokens of sequence s (already appended).  Returns ``out``
     float32 ``[total, Hq, d]``.  ``max_q_len`` (host int) sizes the grid; when
-    omitted it is read from ``q_start`` (a device sync)."""
+    omitted it is read from ``q_start`` (a device sync).  With a ``workspace``
+    (see ``prefill_workspace``) the V pages are converted to f16 first and the
+    faster single-product P V kernel runs."""
     _check_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
           "q must be a contiguous [total, Hq, d] bf16 CUDA tensor")
@@ -338,11 +355,21 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
         out = torch.empty(total, hq, d, dtype=torch.float32, device=q.device)
     _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (total, hq, d),
           "out must be contiguous float32 [total, Hq, d]")
-    st = lib.pkv_paged_prefill_attention(
+    if workspace is None:
+        st = lib.pkv_paged_prefill_attention(
+            _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+            cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(bool(causal)), float(scale), _ptr(out), _stream(q))
+        _check("pkv_paged_prefill_attention", st)
+        return out
+    _need(workspace.dtype == torch.uint8 and workspace.is_cuda and workspace.is_contiguous(),
+          "workspace must be a contiguous uint8 CUDA tensor")
+    st = lib.pkv_paged_prefill_attention_ex(
         _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
         cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-        int(bool(causal)), float(scale), _ptr(out), _stream(q))
-    _check("pkv_paged_prefill_attention", st)
+        int(bool(causal)), float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(q))
+    _check("pkv_paged_prefill_attention_ex", st)
     return out
 
 

@@ -1,0 +1,112 @@
+"""The prefill with a workspace (V pages converted to f16, P as one f16
+operand in the P V product) against the CPU oracle: the same cases as the
+bf16 hi + lo prefill, plus rows past the length holding NaN and a V value
+beyond f16's range."""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_52_gb300 import workloads as wl
+from parity import PrefillStepOracle, assert_attention_close, attention_errors
+from test_gpu_prefill import CHUNKS, PRIORS, SHAPES, _to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_52_gb300 import pagedkv
+    pagedkv.get_device_error(clear=True)
+    return pagedkv
+
+
+def run_f16pv(pk, w, causal=True, max_q_len=None, poison=False):
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    if poison:  # rows past each length in its last page hold NaN
+        tables = w.prefill_tables.cpu().numpy()
+        for s, L in enumerate(w.prefill_lens.cpu().tolist()):
+            if L % 16:
+                b = int(tables[s, (L - 1) // 16])
+                kc[b, L % 16:] = float("nan")
+                vc[b, L % 16:] = float("nan")
+    S = w.prefill_lens.shape[0]
+    ws = pk.prefill_workspace(S, w.prefill_tables.shape[1], kc.shape[2], kc.shape[3], kc.device)
+    mql = max_q_len or int((w.q_start[1:] - w.q_start[:-1]).max())
+    out = torch.full(w.q_prefill.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pk.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables, w.prefill_lens,
+                               causal, w.scale, out=out, max_q_len=mql, workspace=ws)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_f16pv_groups_and_ragged_lengths(pk, hq, hkv, d, causal):
+    w = wl.make_chunked_workload(hq, hkv, d, PRIORS, CHUNKS)
+    ref = PrefillStepOracle(w, range(len(CHUNKS)), causal=causal).output()
+    out, _, _ = run_f16pv(pk, _to_dev(w), causal)
+    assert_attention_close(out.cpu().numpy(), ref, f"f16 PV {hq}/{hkv} d{d} causal={causal}")
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_f16pv_long_chunks_and_outlier_keys(pk):
+    w = wl.make_chunked_workload(64, 8, 128, [4000, 700, 900], [300, 513, 200], config_id=7)
+    g = torch.Generator().manual_seed(5)
+    kc = w.k_cache.float()
+    rows = torch.randperm(kc.shape[0] * 16, generator=g)[:60]
+    kc.view(-1, 8, 128)[rows] *= 100.0
+    w.k_cache = kc.to(torch.bfloat16)
+    ref = PrefillStepOracle(w, [0, 1, 2]).output()
+    out, _, _ = run_f16pv(pk, _to_dev(w))
+    max_abs, _ = assert_attention_close(out.cpu().numpy(), ref, "f16 PV long + outliers")
+    assert max_abs < 1e-3   # 2^-11 relative in P, measured well inside the bound
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_f16pv_nan_rows_past_the_length(pk):
+    w = wl.make_chunked_workload(16, 4, 128, PRIORS, CHUNKS)
+    ref = PrefillStepOracle(w, range(len(CHUNKS))).output()
+    out, _, _ = run_f16pv(pk, _to_dev(w), poison=True)
+    assert_attention_close(out.cpu().numpy(), ref, "f16 PV NaN tails")
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_f16pv_value_beyond_f16_range_is_flagged(pk):
+    w = wl.make_chunked_workload(8, 2, 64, [40], [8], config_id=15)
+    w.v_cache.view(-1)[0:4] = 1e6          # in some page; out of f16's range
+    w = _to_dev(w)
+    pk.get_device_error(clear=True)
+    tables = w.prefill_tables.clone()
+    tables[0, 0] = 0                       # make sure block 0 is read
+    w.prefill_tables = tables
+    run_f16pv(pk, w)
+    assert pk.get_device_error(clear=True) & 0x40
+
+
+def test_f16pv_full_mixed_step_sampled(pk):
+    w = wl.make_mixed_workload(device=DEV, gen_device=DEV)
+    pre = PrefillStepOracle(w, [0, 7])
+    out, _, _ = run_f16pv(pk, w, max_q_len=512)
+    picks = [(0, 0), (0, 1), (0, 255), (0, 511), (1, 0), (1, 300), (1, 511)]
+    ref_rows = pre.rows_output(picks)
+    qs = w.q_start.cpu().numpy()
+    got_rows = np.stack([out[int(qs[[0, 7][si]]) + i].cpu().numpy() for si, i in picks])
+    assert_attention_close(got_rows, ref_rows, "f16 PV mixed prefill rows")
+    assert torch.isfinite(out).all()
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_f16pv_agrees_with_hi_lo_path(pk):
+    # both paths approximate the same float64 result; they differ only in P's
+    # rounding, by far less than the tolerance
+    w = _to_dev(wl.make_chunked_workload(64, 8, 128, [500, 0, 33], [300, 77, 129], config_id=9))
+    a, kc, vc = run_f16pv(pk, w)
+    b = pk.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
+                                   w.prefill_lens, True, w.scale, max_q_len=300)
+    torch.cuda.synchronize()
+    max_abs, _ = attention_errors(a.cpu().numpy(), b.cpu().numpy())
+    assert max_abs < 1e-3
