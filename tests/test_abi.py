@@ -149,3 +149,19 @@ def test_fp8_prefill_host_validation(pk):
     assert call(desc=_desc(pk, d=96)) == -2
     assert call(wsb=need - 1) == -4 and call(ws=null) == -4
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -1   # workspace not 256-byte aligned
+
+
+def test_prefill_workspace_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    need = lib.pkv_paged_prefill_workspace_bytes(4, 8, 2, 128)
+    assert need == 4 * 8 * 16 * 2 * 128 * 2 + 256        # f16 V pages of 4 x 8 blocks + table
+    assert lib.pkv_paged_prefill_workspace_bytes(4, 0, 2, 128) == 0
+    d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
+
+    def call(ws=dummy, wsb=need, desc=d128):
+        return lib.pkv_paged_prefill_attention_ex(dummy, dummy, 4, 40, 16, 8, dummy, dummy, desc,
+                                                  dummy, 8, dummy, 1, 0.1, dummy, ws, wsb, null)
+    assert call(wsb=need - 1) == -4
+    assert call(ws=ctypes.c_void_p((1 << 20) + 64)) == -1  # not 256-byte aligned
+    assert call(desc=_desc(pk, d=96)) == -2
