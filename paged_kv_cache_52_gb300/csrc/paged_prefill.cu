@@ -42,6 +42,16 @@
 //    8 (a factor 256), and only then is that row's O rescaled in TMEM.  The
 //    final division uses the same stale max for O and the row sum, so the
 //    result is exact in real arithmetic.
+//  * with P as one f16 operand (F16PV) the row sum adds the weights exactly
+//    as they were rounded to f16, so the sum and O weigh every V row alike:
+//    the output is a convex combination of V rows whose weights are off by
+//    at most 2^-11 relative, and the error reaching it is a weighted mean of
+//    those relative errors times (v - out), which vanishes for a row that
+//    one key dominates.  The same sum detects a stale max: every weight is
+//    at most the tile's sum, so a sum <= 256 proves no weight exceeds 2^8,
+//    and after the first tile a CTA takes the exponentials in one pass over
+//    the scores with no max pass; only a warp with a larger sum re-reads S
+//    (still intact: P is stored last), takes the max and rescales.
 //  * every mbarrier wait is bounded; a timeout sets an error bit and an abort
 //    flag that the other roles see, copies and MMAs in flight are drained
 //    (bounded) and tensor memory is freed before the CTA exits.
@@ -362,10 +372,116 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       ok = __all_sync(0xffffffffu, pf_wait(s_full, j & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // pass 1: row max.  On unmasked tiles the max is taken over the raw
-      // scores and scaled once (scale > 0 keeps the order; scale < 0 flips it).
       const int key0 = j * kPfKvTile;
       const bool need_mask = key0 + kPfKvTile - 1 > limit;
+      if constexpr (F16PV) {
+        // P of keys [64 g, 64 g + 64) as packed f16 pairs, held in registers
+        // until the tile is settled and then stored over S's columns
+        uint32_t pk[64];
+        float tsum;
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        // no max pass while the running max may stay: not on the first tile,
+        // nor where a row needs the causal mask
+        bool fast = __all_sync(0xffffffffu, j > 0 && !need_mask);
+        for (;;) {
+          if (!fast) {
+            float ex[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) ex[a] = -INFINITY;
+            const bool neg = p.scale_log2 < 0.f;  // uniform over the CTA
+#pragma unroll
+            for (int c = 0; c < 4; c += 2) {
+              float va[32], vb[32];
+              tmem_ld32(lane_base + s_col + c * 32, va);
+              tmem_ld32(lane_base + s_col + c * 32 + 32, vb);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float a = neg ? -va[i] : va[i], b = neg ? -vb[i] : vb[i];
+                if (key0 + c * 32 + i <= limit) ex[i & 7] = fmaxf(ex[i & 7], a);
+                if (key0 + c * 32 + 32 + i <= limit) ex[i & 7] = fmaxf(ex[i & 7], b);
+              }
+            }
+            const float ext = fmaxf(fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])),
+                                    fmaxf(fmaxf(ex[4], ex[5]), fmaxf(ex[6], ex[7])));
+            const float mx = ext == -INFINITY ? -INFINITY : ext * fabsf(p.scale_log2);
+            const bool resc = mx > m_used + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, resc)) {
+              const float m_new = resc ? mx : m_used;
+              const float alpha = ex2(m_used - m_new);  // 0 when m_used is -inf, 1 when unchanged
+              if (j > 0) {
+                // PV_{j-1} must be done before O is rescaled
+                ok = __all_sync(0xffffffffu, pf_wait(o_done, (j - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                  float o[16];
+                  tmem_ld16(lane_base + o_col + c * 16, o);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; i += 2)
+                    f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), a2), o[i], o[i + 1]);
+                  tmem_st16(lane_base + o_col + c * 16, o);
+                }
+              }
+              lsum *= alpha;
+              m_used = m_new;
+            }
+          }
+          // P = 2^(x - m_used) for all keys, and the sum of the rounded weights
+          const uint64_t nm2 = f2_pack(-m_used, -m_used);
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float va[32], vb[32];
+            tmem_ld32(lane_base + s_col + 64 * g, va);
+            tmem_ld32(lane_base + s_col + 64 * g + 32, vb);
+            tmem_wait_ld();
+            if (!need_mask) {
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const int kk = 2 * u;
+                const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+                const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+                pk[32 * g + u] = pack_f16x2_rn(ex2(x0), ex2(x1));
+                ls[u & 3] = add_f16x2_to_f32(pk[32 * g + u], ls[u & 3]);
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const int kk = 2 * u;
+                const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+                const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+                const int key = key0 + 64 * g + kk;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+                pk[32 * g + u] = pack_f16x2_rn(key <= limit ? ex2(x0) : 0.f,
+                                               key + 1 <= limit ? ex2(x1) : 0.f);
+                ls[u & 3] = add_f16x2_to_f32(pk[32 * g + u], ls[u & 3]);
+              }
+            }
+          }
+          tsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          // every weight <= tsum; NaN or inf fail the test and take the max pass
+          if (!fast || __all_sync(0xffffffffu, tsum <= 256.f)) break;
+          fast = false;
+        }
+        if (!ok) break;
+        lsum += tsum;
+        tmem_st32u(lane_base + s_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+        tmem_st32u(lane_base + s_col + 64, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        continue;
+      }
+      // pass 1: row max.  On unmasked tiles the max is taken over the raw
+      // scores and scaled once (scale > 0 keeps the order; scale < 0 flips it).
       float mx;
       {
         float va[32], vb[32];
@@ -404,10 +520,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // a tile past the row's limit leaves the max at -inf and its P all zeros
         mx = ext == -INFINITY ? -INFINITY : ext * fabsf(p.scale_log2);
       }
-      // f16 P: track the max exactly, so the largest weight is exactly 1 and
-      // f16 rounds only the others (<= 2^-12 relative); a lazy max would let
-      // the largest weight reach 256, rounded at up to 2^-11 relative
-      const bool resc = mx > m_used + (F16PV ? 0.f : kRescaleThreshold);
+      const bool resc = mx > m_used + kRescaleThreshold;
       if (__any_sync(0xffffffffu, resc)) {
         const float m_new = resc ? mx : m_used;
         const float alpha = ex2(m_used - m_new);  // 0 when m_used is -inf, 1 when unchanged
