@@ -271,11 +271,12 @@ def run_mixed(args, dev, pagedkv, E):
 
     pws = pagedkv.prefill_workspace(len(plens), w.prefill_tables.shape[1], hkv, d, dev)
 
-    def prefill():
-        # the workspace path: V pages to f16 first, P as one f16 operand
+    def prefill(max_ctas=None):
+        # the workspace path: V pages to f16 first, P as one f16 operand;
+        # max_ctas: a persistent launch on at most that many SMs
         pagedkv.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
                                         w.prefill_lens, True, w.scale, out=pout,
-                                        max_q_len=chunk, workspace=pws)
+                                        max_q_len=chunk, workspace=pws, max_ctas=max_ctas)
 
     def prefill_plain():
         pagedkv.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
@@ -338,29 +339,39 @@ def run_mixed(args, dev, pagedkv, E):
     main = torch.cuda.current_stream()
     s_pre, s_dec = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def concurrent_step(cascade):
+    # With the SMs split, the prefill runs persistent on at most `ctas` SMs
+    # from a high-priority stream and the decode fills the other SMs at the
+    # same time, instead of waiting for prefill CTAs that each hold a whole SM.
+    s_pre_hi = torch.cuda.Stream(device=dev, priority=-1)
+
+    def concurrent_step(cascade, ctas=None):
+        sp = s_pre if ctas is None else s_pre_hi
         append()
-        s_pre.wait_stream(main)
+        sp.wait_stream(main)
         s_dec.wait_stream(main)
-        with torch.cuda.stream(s_pre):
-            prefill()
+        with torch.cuda.stream(sp):
+            prefill(ctas)
         with torch.cuda.stream(s_dec):
             decode_cascade() if cascade else decode()
-        main.wait_stream(s_pre)
+        main.wait_stream(sp)
         main.wait_stream(s_dec)
 
-    t_conc = {}
-    for cascade in (False, True):
+    def time_concurrent(cascade, ctas=None, steps=K):
         for _ in range(3):
-            concurrent_step(cascade)
+            concurrent_step(cascade, ctas)
         torch.cuda.synchronize()
         c0, c1 = E(enable_timing=True), E(enable_timing=True)
         c0.record()
-        for _ in range(K):
-            concurrent_step(cascade)
+        for _ in range(steps):
+            concurrent_step(cascade, ctas)
         c1.record()
         torch.cuda.synchronize()
-        t_conc[cascade] = c0.elapsed_time(c1) / K
+        return c0.elapsed_time(c1) / steps
+
+    t_conc = {cascade: time_concurrent(cascade) for cascade in (False, True)}
+    split_sweep = {c: round(time_concurrent(True, c), 4) for c in (72, 88, 104, 120, 136)}
+    best_ctas = min(split_sweep, key=split_sweep.get)
+    t_split = time_concurrent(True, best_ctas)
     # the same step over an FP8 (e4m3) cache: quantizing append, prefill
     # (pages widened to bf16 in a workspace, then the tensor-core prefill),
     # FP8 decode
@@ -438,6 +449,10 @@ def run_mixed(args, dev, pagedkv, E):
         "ms_per_step_shared_prefix": round(t_app + t_pre + t_casc, 4),
         "ms_per_step_two_streams": round(t_conc[False], 4),
         "ms_per_step_two_streams_shared_prefix": round(t_conc[True], 4),
+        "two_streams_sm_split": {
+            "ms_per_step": round(t_split, 4), "prefill_ctas": best_ctas,
+            "sweep_ms_by_prefill_ctas": split_sweep,
+            "note": "shared-prefix decode on the SMs the persistent prefill leaves free"},
         "gpu_launches": K * (4 + (1 if ws is not None else 0)),
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),

@@ -229,6 +229,33 @@ PKV_API int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start
                                            size_t ws_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention_limited -- pkv_paged_prefill_attention_ex on at
+ * most max_ctas SMs, leaving the others to kernels on other streams.  The
+ * continuous-batching step ("Cache KV, attention et optimisation de
+ * l'inference", section on continuous batching; CS336 notes, lecture 10,
+ * selective batching) runs chunked prefills next to running decodes: the
+ * prefill is bound by the tensor cores and the decode by HBM, so the decode
+ * launched on another stream after this call runs on the remaining SMs at
+ * the same time instead of after it.
+ * Same result as pkv_paged_prefill_attention_ex (bit for bit: the same
+ * tiles in the same arithmetic); max_ctas persistent CTAs take the
+ * (sequence x KV head, query tile) items longest first from a counter in
+ * the workspace.  max_ctas >= 1 (PKV_EINVAL otherwise); a workspace of
+ * pkv_paged_prefill_workspace_bytes(...) bytes is required (PKV_ENOMEM if
+ * NULL or smaller).  Calls that share a workspace must not overlap.
+ */
+PKV_API int pkv_paged_prefill_attention_limited(const void* q, const int32_t* q_start,
+                                                int num_seqs, int total_q, int max_q_len,
+                                                int q_heads, const void* k_cache,
+                                                const void* v_cache, pkv_cache_desc cache,
+                                                const int32_t* block_tables,
+                                                int max_blocks_per_seq,
+                                                const int32_t* context_lens, int causal,
+                                                float scale, float* out, int max_ctas,
+                                                void* workspace, size_t ws_bytes,
+                                                pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_attention_shared_prefix -- the same result as
  * pkv_paged_decode_attention when every sequence's first prefix_blocks pages
  * are the same physical blocks (a shared system prompt stored once and

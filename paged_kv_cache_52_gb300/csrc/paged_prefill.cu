@@ -55,6 +55,9 @@
 //  * every mbarrier wait is bounded; a timeout sets an error bit and an abort
 //    flag that the other roles see, copies and MMAs in flight are drained
 //    (bounded) and tensor memory is freed before the CTA exits.
+#include <algorithm>
+#include <climits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.cuh"
@@ -109,6 +112,12 @@ struct PrefillParams {
   float out_scale;              // multiplies the output (1, or v_scale over FP8 pools)
   const int32_t* v_block_tables;  // null: V pages use block_tables
   int v_num_blocks;             // blocks of the V pool
+  // persistent mode: CTAs take items (pair, query tile) from this counter,
+  // zero on entry, in the grid mode's longest-first order; null: one item
+  // per CTA from the grid
+  int* work_counter;
+  int num_items;                // pairs * tiles_per_pair
+  int tiles_per_pair;           // CTA-sized query tiles of the longest chunk
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -125,34 +134,28 @@ __device__ __forceinline__ void pf_abort(volatile int* abort_flag) {
   atomicOr(&g_prefill_error, kErrWaitTimeout);
 }
 
+// One item: the two query tiles `cta_tile` of pair (sequence x KV head)
+// `pair`, computed by the whole CTA.  Barriers are set up at the start; at
+// the end every copy, MMA and tensor-memory access of the item has completed
+// and the CTA has synchronised, so the next item can reuse everything.
 // F16PV: V is an f16 pool and P enters the PV product as one f16 operand;
 // otherwise V is bf16 and P enters as bf16 hi + lo.
 template <int D, int G, bool F16PV>
-__global__ void __launch_bounds__(kPfThreads, 1)
-paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                     const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+__device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                             const CUtensorMap& tmap_v, const PrefillParams& p,
+                                             uint8_t* smem, uint32_t tmem, int pair,
+                                             int cta_tile) {
   using L = PrefillSmem<D>;
   constexpr int TPT = kPfRows / G;          // query tokens per Q tile
   constexpr int TPC = kPfQTiles * TPT;      // query tokens per CTA
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::kBarOff;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid (pairs, tiles): CTAs are dispatched x-fastest, so every pair's
-  // longest tile goes first, then every pair's next-longest, ... (a
-  // longest-first order the hardware scheduler balances dynamically)
-  const int pair = blockIdx.x;
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
-  const int cta_tile = int(gridDim.y) - 1 - int(blockIdx.y);
 
-  // ---- per-CTA bounds (uniform over the CTA, so early exits are safe)
+  // ---- per-item bounds (uniform over the CTA, so early exits are safe)
   const int qs = p.q_start ? __ldg(p.q_start + seq) : 0;
   const int qe = p.q_start ? __ldg(p.q_start + seq + 1) : p.total_q;
   const int ctx = p.context_lens ? __ldg(p.context_lens + seq) : p.context_len;
@@ -172,7 +175,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int ntiles = (kv_end + kPfKvTile - 1) / kPfKvTile;
   const int nblk = (ctx + 15) / 16;
 
-  // ---- set-up: barriers (producer lane 0), tensor memory (warp 0)
+  // ---- set-up: barriers (producer lane 0)
   if (warp == kPfProducerWarp && lane == 0) {
     mbar_init(bars + 8 * kQFull, 1);
     for (int s = 0; s < kPfKStages; ++s) {
@@ -187,17 +190,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(bars + 8 * (kODone0 + s), 1);
     }
     mbar_init(bars + 8 * kDrain, 1);
-    *abort_flag = 0;
     fence_barrier_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kPfTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == kPfProducerWarp || warp == kPfVProducerWarp) {
     // ============ TMA producers: warp 8 loads Q and the K ring, warp 10 the V ring ============
@@ -351,6 +348,19 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // every MMA issued has completed before tensor memory is released
       umma_commit(bars + 8 * kDrain);
       (void)mbar_wait_bounded(bars + 8 * kDrain, 0);
+      if (ok) {
+        // ... and every commit has arrived before the barriers are set up
+        // again for the next item: the last phase of each ring slot's
+        // empty barrier (tile j was committed to slot j % stages)
+        for (int s = 0; s < kPfKStages && s < ntiles; ++s) {
+          const int last = s + (ntiles - 1 - s) / kPfKStages * kPfKStages;
+          (void)mbar_wait_bounded(bars + 8 * (kKEmpty0 + s), (last / kPfKStages) & 1);
+        }
+        for (int s = 0; s < kPfVStages && s < ntiles; ++s) {
+          const int last = s + (ntiles - 1 - s) / kPfVStages * kPfVStages;
+          (void)mbar_wait_bounded(bars + 8 * (kVEmpty0 + s), (last / kPfVStages) & 1);
+        }
+      }
     }
     __syncwarp();
   } else {
@@ -647,6 +657,58 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+}
+
+template <int D, int G, bool F16PV, bool PERSIST>
+__global__ void __launch_bounds__(kPfThreads, 1)
+paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                     const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+  using L = PrefillSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
+  const int warp = threadIdx.x >> 5;
+  // tensor memory (warp 0) for the CTA's lifetime
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kPfTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if constexpr (!PERSIST) {
+    // grid (pairs, tiles): CTAs are dispatched x-fastest, so every pair's
+    // longest tile goes first, then every pair's next-longest, ... (a
+    // longest-first order the hardware scheduler balances dynamically)
+    prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, int(blockIdx.x),
+                              int(gridDim.y) - 1 - int(blockIdx.y));
+  } else {
+    // persistent: the same order, taken one item at a time from the counter,
+    // so the launch occupies at most gridDim.x SMs
+    const int pairs = p.num_seqs * p.kv_heads;
+    for (;;) {
+      if (threadIdx.x == 0) *item_slot = atomicAdd(p.work_counter, 1);
+      __syncthreads();
+      const int item = *item_slot;
+      const bool stop = item >= p.num_items || *abort_flag;
+      __syncthreads();  // every thread has read the slot before it is written again
+      if (stop) break;
+      const int rank = item / pairs;
+      prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, item - rank * pairs,
+                                p.tiles_per_pair - 1 - rank);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kPfTmemCols);
@@ -654,37 +716,55 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
 }
 
 template <int D, int G, bool F16PV>
-static cudaError_t launch_prefill_t(const PrefillParams& prm, const CUtensorMap* tq,
-                                    const CUtensorMap* tk, const CUtensorMap* tv,
-                                    cudaStream_t stream) {
+static cudaError_t launch_prefill_t(const PrefillParams& prm, int max_ctas,
+                                    const CUtensorMap* tq, const CUtensorMap* tk,
+                                    const CUtensorMap* tv, cudaStream_t stream) {
   using L = PrefillSmem<D>;
   constexpr int TPT = kPfRows / G;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV>,
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
+    if (e == cudaSuccess && F16PV)
+      e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV, F16PV>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   constexpr int TPC = kPfQTiles * TPT;
-  if ((prm.max_q_len + TPC - 1) / TPC > 65535) return cudaErrorInvalidValue;
-  dim3 grid(prm.num_seqs * prm.kv_heads, (prm.max_q_len + TPC - 1) / TPC);
-  paged_prefill_kernel<D, G, F16PV><<<grid, kPfThreads, L::kSmemBytes, stream>>>(*tq, *tk, *tv,
-                                                                                 prm);
+  const int tiles = (prm.max_q_len + TPC - 1) / TPC;
+  if (prm.work_counter) {
+    if (!F16PV) return cudaErrorInvalidValue;  // instantiated for the f16 P V path only
+    PrefillParams q = prm;
+    const long long items = (long long)prm.num_seqs * prm.kv_heads * tiles;
+    if (items > INT32_MAX - 65536) return cudaErrorInvalidValue;
+    q.num_items = int(items);
+    q.tiles_per_pair = tiles;
+    cudaError_t e = cudaMemsetAsync(prm.work_counter, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+    const int ctas = int(std::min<long long>(items, max_ctas));
+    paged_prefill_kernel<D, G, F16PV, F16PV><<<ctas, kPfThreads, L::kSmemBytes, stream>>>(
+        *tq, *tk, *tv, q);
+    return cudaGetLastError();
+  }
+  if (tiles > 65535) return cudaErrorInvalidValue;
+  dim3 grid(prm.num_seqs * prm.kv_heads, tiles);
+  paged_prefill_kernel<D, G, F16PV, false><<<grid, kPfThreads, L::kSmemBytes, stream>>>(
+      *tq, *tk, *tv, prm);
   return cudaGetLastError();
 }
 
 template <int D, bool F16PV>
-static cudaError_t launch_prefill_d(const PrefillParams& prm, int group, const CUtensorMap* tq,
-                                    const CUtensorMap* tk, const CUtensorMap* tv,
-                                    cudaStream_t st) {
+static cudaError_t launch_prefill_d(const PrefillParams& prm, int max_ctas, int group,
+                                    const CUtensorMap* tq, const CUtensorMap* tk,
+                                    const CUtensorMap* tv, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_prefill_t<D, 1, F16PV>(prm, tq, tk, tv, st);
-    case 2: return launch_prefill_t<D, 2, F16PV>(prm, tq, tk, tv, st);
-    case 4: return launch_prefill_t<D, 4, F16PV>(prm, tq, tk, tv, st);
-    case 8: return launch_prefill_t<D, 8, F16PV>(prm, tq, tk, tv, st);
-    case 16: return launch_prefill_t<D, 16, F16PV>(prm, tq, tk, tv, st);
+    case 1: return launch_prefill_t<D, 1, F16PV>(prm, max_ctas, tq, tk, tv, st);
+    case 2: return launch_prefill_t<D, 2, F16PV>(prm, max_ctas, tq, tk, tv, st);
+    case 4: return launch_prefill_t<D, 4, F16PV>(prm, max_ctas, tq, tk, tv, st);
+    case 8: return launch_prefill_t<D, 8, F16PV>(prm, max_ctas, tq, tk, tv, st);
+    case 16: return launch_prefill_t<D, 16, F16PV>(prm, max_ctas, tq, tk, tv, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -713,13 +793,16 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.scale_log2 = a.scale_log2;
   prm.v_block_tables = a.v_block_tables;
   prm.v_num_blocks = a.v_block_tables ? a.v_num_blocks : a.num_blocks;
+  prm.work_counter = a.max_ctas > 0 ? a.work_counter : nullptr;
+  prm.num_items = 0;        // set by the persistent launch
+  prm.tiles_per_pair = 0;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
-    if (a.d_head == 128) return launch_prefill_d<128, true>(prm, group, tmap_q, tmap_k, tmap_v, stream);
-    if (a.d_head == 64) return launch_prefill_d<64, true>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
   } else {
-    if (a.d_head == 128) return launch_prefill_d<128, false>(prm, group, tmap_q, tmap_k, tmap_v, stream);
-    if (a.d_head == 64) return launch_prefill_d<64, false>(prm, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 128) return launch_prefill_d<128, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -225,7 +225,8 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
                 const pkv_cache_desc& cache, const int32_t* block_tables,
                 int max_blocks_per_seq, const int32_t* context_lens, int causal,
                 float scale_log2, float out_scale, float* out, cudaStream_t stream,
-                bool f16_pv = false, const int32_t* v_tables = nullptr, int v_num_blocks = 0) {
+                bool f16_pv = false, const int32_t* v_tables = nullptr, int v_num_blocks = 0,
+                int max_ctas = 0, int* work_counter = nullptr) {
   const int group = q_heads / cache.kv_heads;
   const int rows = pkv::prefill_rows_per_tile();
   pkv_cache_desc vdesc = cache;
@@ -253,14 +254,18 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
   a.f16_pv = f16_pv;
   a.v_block_tables = v_tables;
   a.v_num_blocks = v_num_blocks;
+  a.max_ctas = max_ctas;
+  a.work_counter = work_counter;
   cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 // Workspace of the FP8 prefill: bf16 K and V scratch pools of
-// num_seqs * max_blocks pages, then the scratch block table.
+// num_seqs * max_blocks pages, then the scratch block table (counter_off
+// bytes in all).  The bf16 prefill's workspace is the same from v_off on,
+// plus the work counter of the persistent launch.
 struct Fp8PrefillLayout {
-  size_t k_off = 0, v_off = 0, table_off = 0, total = 0;
+  size_t k_off = 0, v_off = 0, table_off = 0, counter_off = 0, total = 0;
 };
 
 bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
@@ -273,7 +278,8 @@ bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
   w->k_off = 0;
   w->v_off = up(pool);
   w->table_off = w->v_off + up(pool);
-  w->total = w->table_off + up(size_t(pages) * 4);
+  w->counter_off = w->table_off + up(size_t(pages) * 4);
+  w->total = w->counter_off + 256;
   return true;
 }
 
@@ -538,7 +544,8 @@ int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_s
 size_t pkv_paged_prefill_attention_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
                                                        int kv_heads, int d_head) {
   Fp8PrefillLayout w;
-  return fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w) ? w.total : 0;
+  return fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w) ? w.counter_off
+                                                                                 : 0;
 }
 
 int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int num_seqs,
@@ -557,7 +564,7 @@ int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int n
   Fp8PrefillLayout w;
   if (!fp8_prefill_layout(num_seqs, max_blocks_per_seq, cache.kv_heads, cache.d_head, &w))
     return PKV_EUNSUPPORTED;
-  if (!workspace || ws_bytes < w.total) return PKV_ENOMEM;
+  if (!workspace || ws_bytes < w.counter_off) return PKV_ENOMEM;
   if (!aligned(workspace, 256)) return PKV_EINVAL;
   const int sms = current_device_sms();
   if (sms <= 0) return PKV_ECUDA;
@@ -583,18 +590,13 @@ size_t pkv_paged_prefill_workspace_bytes(int num_seqs, int max_blocks_per_seq, i
   return w.total - w.v_off;  // the f16 V pool and the table, no K copy
 }
 
-int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start, int num_seqs,
-                                   int total_q, int max_q_len, int q_heads, const void* k_cache,
-                                   const void* v_cache, pkv_cache_desc cache,
-                                   const int32_t* block_tables, int max_blocks_per_seq,
-                                   const int32_t* context_lens, int causal, float scale,
-                                   float* out, void* workspace, size_t ws_bytes,
-                                   pkv_stream_t stream) {
-  if (!workspace)
-    return pkv_paged_prefill_attention(q, q_start, num_seqs, total_q, max_q_len, q_heads,
-                                       k_cache, v_cache, cache, block_tables,
-                                       max_blocks_per_seq, context_lens, causal, scale, out,
-                                       stream);
+namespace {
+
+int prefill_f16pv(const void* q, const int32_t* q_start, int num_seqs, int total_q,
+                  int max_q_len, int q_heads, const void* k_cache, const void* v_cache,
+                  pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int causal, float scale, float* out,
+                  void* workspace, size_t ws_bytes, int max_ctas, pkv_stream_t stream) {
   int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
                          cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
   if (st != PKV_OK || num_seqs == 0 || total_q == 0 || max_q_len == 0) return st;
@@ -615,7 +617,41 @@ int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start, int nu
   return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, ws, cache,
                      block_tables, max_blocks_per_seq, context_lens, causal,
                      scale * 1.4426950408889634f, 1.f, out, cs, /*f16_pv=*/true, vtab,
-                     num_seqs * max_blocks_per_seq);
+                     num_seqs * max_blocks_per_seq, max_ctas,
+                     reinterpret_cast<int*>(ws + (w.counter_off - w.v_off)));
+}
+
+}  // namespace
+
+int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start, int num_seqs,
+                                   int total_q, int max_q_len, int q_heads, const void* k_cache,
+                                   const void* v_cache, pkv_cache_desc cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int causal, float scale,
+                                   float* out, void* workspace, size_t ws_bytes,
+                                   pkv_stream_t stream) {
+  if (!workspace)
+    return pkv_paged_prefill_attention(q, q_start, num_seqs, total_q, max_q_len, q_heads,
+                                       k_cache, v_cache, cache, block_tables,
+                                       max_blocks_per_seq, context_lens, causal, scale, out,
+                                       stream);
+  return prefill_f16pv(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                       cache, block_tables, max_blocks_per_seq, context_lens, causal, scale, out,
+                       workspace, ws_bytes, 0, stream);
+}
+
+int pkv_paged_prefill_attention_limited(const void* q, const int32_t* q_start, int num_seqs,
+                                        int total_q, int max_q_len, int q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        pkv_cache_desc cache, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* context_lens,
+                                        int causal, float scale, float* out, int max_ctas,
+                                        void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+  if (max_ctas < 1) return PKV_EINVAL;
+  if (!workspace) return PKV_ENOMEM;
+  return prefill_f16pv(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                       cache, block_tables, max_blocks_per_seq, context_lens, causal, scale, out,
+                       workspace, ws_bytes, max_ctas, stream);
 }
 
 size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_heads, int d_head,

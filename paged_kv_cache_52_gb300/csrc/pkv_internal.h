@@ -98,6 +98,10 @@ struct PrefillArgs {
   int max_blocks_per_seq;
   int causal;
   float scale_log2;
+  // > 0: persistent launch of at most max_ctas CTAs taking query tiles from
+  // work_counter (one int of device memory, zeroed by the launch)
+  int max_ctas = 0;
+  int* work_counter = nullptr;
 };
 
 // Query rows (tokens x heads of a GQA group) per prefill tile.

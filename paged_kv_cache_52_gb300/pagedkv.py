@@ -92,6 +92,10 @@ SIGNATURES = {
     "pkv_paged_prefill_attention_ex": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
                                         ctypes.c_int, _f32, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "pkv_paged_prefill_attention_limited": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, _vp, _vp, CacheDesc, _vp,
+                                             ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
+                                             ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
     "pkv_paged_prefill_attention_fp8": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int,
                                          _vp, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _sz, _vp],
@@ -330,13 +334,16 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
                             context_lens: torch.Tensor, causal: bool, scale: float,
                             out: Optional[torch.Tensor] = None,
                             max_q_len: Optional[int] = None,
-                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                            workspace: Optional[torch.Tensor] = None,
+                            max_ctas: Optional[int] = None) -> torch.Tensor:
     """Chunked prefill: rows ``q_start[s]:q_start[s+1]`` of ``q [total, Hq, d]``
     are the last tokens of sequence s (already appended).  Returns ``out``
     float32 ``[total, Hq, d]``.  ``max_q_len`` (host int) sizes the grid; when
     omitted it is read from ``q_start`` (a device sync).  With a ``workspace``
     (see ``prefill_workspace``) the V pages are converted to f16 first and the
-    faster single-product P V kernel runs."""
+    faster single-product P V kernel runs.  ``max_ctas`` (needs the workspace)
+    runs that kernel on at most that many SMs, leaving the rest to work on
+    other streams (``pkv_paged_prefill_attention_limited``)."""
     _check_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
           "q must be a contiguous [total, Hq, d] bf16 CUDA tensor")
@@ -355,6 +362,7 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
         out = torch.empty(total, hq, d, dtype=torch.float32, device=q.device)
     _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (total, hq, d),
           "out must be contiguous float32 [total, Hq, d]")
+    _need(max_ctas is None or workspace is not None, "max_ctas needs a workspace")
     if workspace is None:
         st = lib.pkv_paged_prefill_attention(
             _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
@@ -364,6 +372,14 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
         return out
     _need(workspace.dtype == torch.uint8 and workspace.is_cuda and workspace.is_contiguous(),
           "workspace must be a contiguous uint8 CUDA tensor")
+    if max_ctas is not None:
+        st = lib.pkv_paged_prefill_attention_limited(
+            _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+            cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(bool(causal)), float(scale), _ptr(out), int(max_ctas), _ptr(workspace),
+            workspace.numel(), _stream(q))
+        _check("pkv_paged_prefill_attention_limited", st)
+        return out
     st = lib.pkv_paged_prefill_attention_ex(
         _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
         cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),

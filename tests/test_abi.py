@@ -155,7 +155,8 @@ def test_prefill_workspace_host_validation(pk):
     lib, null = pk.lib, ctypes.c_void_p(0)
     dummy = ctypes.c_void_p(1 << 20)
     need = lib.pkv_paged_prefill_workspace_bytes(4, 8, 2, 128)
-    assert need == 4 * 8 * 16 * 2 * 128 * 2 + 256        # f16 V pages of 4 x 8 blocks + table
+    # f16 V pages of 4 x 8 blocks + table + the persistent launch's work counter
+    assert need == 4 * 8 * 16 * 2 * 128 * 2 + 256 + 256
     assert lib.pkv_paged_prefill_workspace_bytes(4, 0, 2, 128) == 0
     d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
 
@@ -165,3 +166,13 @@ def test_prefill_workspace_host_validation(pk):
     assert call(wsb=need - 1) == -4
     assert call(ws=ctypes.c_void_p((1 << 20) + 64)) == -1  # not 256-byte aligned
     assert call(desc=_desc(pk, d=96)) == -2
+
+    def limited(ctas=8, ws=dummy, wsb=need, desc=d128, S=4):
+        return lib.pkv_paged_prefill_attention_limited(dummy, dummy, S, 40, 16, 8, dummy, dummy,
+                                                       desc, dummy, 8, dummy, 1, 0.1, dummy, ctas,
+                                                       ws, wsb, null)
+    assert limited(ctas=0) == -1 and limited(ctas=-3) == -1
+    assert limited(ws=null) == -4 and limited(wsb=need - 1) == -4
+    assert limited(ws=ctypes.c_void_p((1 << 20) + 64)) == -1
+    assert limited(desc=_desc(pk, d=96)) == -2
+    assert limited(S=0) == 0                              # nothing to do

@@ -110,3 +110,67 @@ def test_f16pv_agrees_with_hi_lo_path(pk):
     torch.cuda.synchronize()
     max_abs, _ = attention_errors(a.cpu().numpy(), b.cpu().numpy())
     assert max_abs < 1e-3
+
+
+def _limited(pk, w, kc, vc, max_ctas, causal=True, stream=None):
+    S = w.prefill_lens.shape[0]
+    ws = pk.prefill_workspace(S, w.prefill_tables.shape[1], kc.shape[2], kc.shape[3], kc.device)
+    mql = int((w.q_start[1:] - w.q_start[:-1]).max())
+    out = torch.full(w.q_prefill.shape, float("nan"), dtype=torch.float32, device=DEV)
+    with torch.cuda.stream(stream or torch.cuda.current_stream()):
+        pk.paged_prefill_attention(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
+                                   w.prefill_lens, causal, w.scale, out=out, max_q_len=mql,
+                                   workspace=ws, max_ctas=max_ctas)
+    return out
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_limited_sms_equals_grid_launch(pk, causal):
+    # the persistent launch computes the same tiles in the same arithmetic,
+    # so its output is bitwise the grid launch's, for any number of CTAs
+    # (1: one CTA walks every item; more CTAs than items: the surplus exits)
+    w = _to_dev(wl.make_chunked_workload(64, 8, 128, [500, 0, 33, 2000], [300, 77, 129, 64],
+                                         config_id=9))
+    ref_out, kc, vc = run_f16pv(pk, w, causal)
+    for ctas in (1, 7, 148, 100000):
+        out = _limited(pk, w, kc, vc, ctas, causal)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out), f"max_ctas={ctas}"
+    ref = PrefillStepOracle(w, range(4), causal=causal).output()
+    assert_attention_close(ref_out.cpu().numpy(), ref, "limited prefill vs oracle")
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_limited_prefill_beside_decode_on_another_stream(pk):
+    # the continuous-batching step with the SMs split: the prefill on at most
+    # 100 SMs, the decode launched right after it on a second stream; both
+    # results equal the ones computed one after the other
+    w = wl.make_mixed_workload(device=DEV, gen_device=DEV, num_decode=64)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    dl = w.meta["decode_lens"]
+    hq, d, hkv = w.q_decode.shape[1], w.q_decode.shape[2], kc.shape[2]
+    dws = pk.decode_workspace(len(dl), hq, hkv, d, max(dl), kc.device)
+
+    def decode(stream):
+        with torch.cuda.stream(stream):
+            return pk.paged_decode_attention(w.q_decode, kc, vc, w.decode_tables, w.decode_lens,
+                                             w.scale, max_context_len=max(dl), workspace=dws)
+    main = torch.cuda.current_stream()
+    p_serial = _limited(pk, w, kc, vc, 148)
+    d_serial = decode(main)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(main)
+    p_conc = _limited(pk, w, kc, vc, 100)
+    d_conc = decode(side)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert torch.equal(p_conc, p_serial)
+    assert torch.equal(d_conc, d_serial)
+    pre = PrefillStepOracle(w, [0, 7])
+    picks = [(0, 0), (0, 511), (1, 255), (1, 511)]
+    qs = w.q_start.cpu().numpy()
+    got = np.stack([p_conc[int(qs[[0, 7][si]]) + i].cpu().numpy() for si, i in picks])
+    assert_attention_close(got, pre.rows_output(picks), "limited prefill beside decode")
+    assert pk.get_device_error(clear=True) == 0
