@@ -13,15 +13,21 @@
 //    e4m3 -> f16 is exact, bf16 q -> f16 is exact in f16's range (an |q| that
 //    would overflow raises PKV_DEVERR_FP16_RANGE), and both scales factor out
 //    (k_scale into the softmax scale, v_scale into the output).
+//  * the MMAs run transposed, so no MMA row is padding: S^T = K Q^T has the
+//    page's 16 keys as M and the group's heads as N (8 per n-tile), O^T = V^T
+//    P^T has 16 dims per m-tile as M and the heads as N -- 8 + 8 MMAs per page
+//    for a group of 8 instead of 16 + 16 with the heads as (half-empty) M.
 //  * K fragments come straight from the code bytes: ldmatrix over the tile as
 //    16-bit units hands each thread 4 consecutive dims of a key, which fill the
-//    B fragment under a fixed permutation of the 16 dims of a k-step; the Q
-//    fragments are loaded with the same permutation, so the dot products are
-//    unchanged.
+//    A fragment under a fixed permutation of the 16 dims of a k-step; the Q
+//    fragments (B) are loaded with the same permutation, so the dot products
+//    are unchanged.
+//  * P^T: the S^T accumulator holds (key, two heads) per lane; movmatrix.trans
+//    turns each 8 x 8 block into the (two keys, head) layout of the B operand.
 //  * V fragments: ldmatrix.trans gives a thread two keys x two adjacent dims;
-//    a byte permute splits them into two key-pairs of one dim each, so every
-//    16-dim chunk feeds an "even dims" and an "odd dims" MMA whose outputs are
-//    de-interleaved when the result is written.
+//    a byte permute splits them into the key pairs of each dim, which are the
+//    A fragment rows of an m-tile whose row r is dim 2 r and row r + 8 dim
+//    2 r + 1.
 //  * P enters PV as one f16 operand: its rounding error is at most 2^-11
 //    relative (8x below bf16's), so the output moves by at most 2^-11 times
 //    the largest |V| a row attends to; the bf16 kernel needs a hi + lo split
@@ -85,14 +91,26 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool* range_ok) 
   return pack_f16x2(a, b);
 }
 
+// An 8x8 matrix of 16-bit values held one row per lane quad (lane l: row
+// l / 4, columns 2 (l % 4), 2 (l % 4) + 1) -> the same fragment of its transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// The MMAs run transposed: S^T = K Q^T has the 16 keys of a page as its M rows
+// and the GQA group's heads as N (8 per n-tile), and O^T = V^T P^T has 16 dims
+// per m-tile as M and the heads as N, so no MMA row is padding (with the heads
+// as M, a group of 8 fills half of an m16 tile).
 template <int G>
 __global__ void __launch_bounds__(kF8Warps * 32)
 paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using T = F8Tile;
   constexpr int D = kF8D;
-  constexpr bool kTwoRows = (G > 8);
-  constexpr int NT = D / 8;  // virtual n-tiles of the output (16)
+  constexpr int NH = (G + 7) / 8;  // n-tiles of heads
+  constexpr int MT = D / 16;       // m-tiles of O^T (16 dims each)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,27 +154,25 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     tma_prefetch_desc(&tmap_v);
   }
 
-  // Q fragments as f16 under the k-permutation of the K fragments: within the
-  // 16 dims of k-step kk, fragment slots (2 tig, 2 tig + 1) hold dims
-  // (4 tig, 4 tig + 1) and slots (2 tig + 8, 2 tig + 9) hold (4 tig + 2, 4 tig + 3).
-  uint32_t qa[8][2];
-  uint32_t qb[kTwoRows ? 8 : 1][2];
+  // Q as the B operand of S^T = K Q^T: column n = head gid of n-tile nh, and
+  // within the 16 dims of k-step kk the k slots (2 tig, 2 tig + 1) hold dims
+  // (4 tig, 4 tig + 1), the slots (2 tig + 8, 2 tig + 9) dims (4 tig + 2,
+  // 4 tig + 3) -- the order in which the K fragments arrive (below), so the
+  // dot products are unchanged.  Heads past the group are zero.
+  uint32_t qf[NH][8][2];
   bool range_ok = true;
-  {
-    const __nv_bfloat16* qrow = p.q + (row0 + gid) * D;
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh) {
+    const int head = 8 * nh + gid;
+    const __nv_bfloat16* qrow = p.q + (row0 + head) * D;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      if (gid < G) {
+      if (head < G) {
         const uint2 w = __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * tig));
-        qa[kk][0] = bf16x2_to_f16x2(w.x, &range_ok);
-        qa[kk][1] = bf16x2_to_f16x2(w.y, &range_ok);
+        qf[nh][kk][0] = bf16x2_to_f16x2(w.x, &range_ok);
+        qf[nh][kk][1] = bf16x2_to_f16x2(w.y, &range_ok);
       } else {
-        qa[kk][0] = qa[kk][1] = 0u;
-      }
-      if constexpr (kTwoRows) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qrow + 8 * D + kk * 16 + 4 * tig));
-        qb[kk][0] = bf16x2_to_f16x2(w.x, &range_ok);
-        qb[kk][1] = bf16x2_to_f16x2(w.y, &range_ok);
+        qf[nh][kk][0] = qf[nh][kk][1] = 0u;
       }
     }
   }
@@ -183,10 +199,17 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (keys 0-7|8-15) x (chunk even|odd)
   const int v_tok = (mi & 1) * 8 + mr;   // V: matrices (keys 0-7|8-15) x (chunk even|odd)
 
-  float o[NT][4];
+  // O^T accumulators: m-tile mt, row gid = dim 16 mt + 2 gid, row gid + 8 =
+  // dim 16 mt + 2 gid + 1; columns 2 tig, 2 tig + 1 = heads of n-tile nh.
+  float o[NH][MT][4];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[nh][mt][0] = o[nh][mt][1] = o[nh][mt][2] = o[nh][mt][3] = 0.f;
+  // running max and (this lane's part of the) sum of heads 8 nh + 2 tig + c
+  float m[NH][2], l[NH][2];
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh) m[nh][0] = m[nh][1] = -INFINITY, l[nh][0] = l[nh][1] = 0.f;
   bool failed = false;
   int i = 0;
   for (; i < cnt; ++i) {
@@ -201,105 +224,80 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t vbase = kbase + T::kTileBytes;
     const int tok0 = (b0 + warp + i * kF8Warps) * kBlockTokens;
 
-    // S = Q K^T: one ldmatrix.x4 covers two k-steps for both 8-key n-tiles.
-    // Even and odd k-steps accumulate separately (four independent chains).
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S^T = K Q^T: one ldmatrix.x4 covers two k-steps of both 8-key halves:
+    // a lane gets 4 consecutive dims of key gid (r0 | r1) and of key gid + 8
+    // (r2 | r3).  Even and odd k-steps accumulate separately.
+    float s[NH][4], s_odd[NH][4];
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nh][e] = s_odd[nh][e] = 0.f;
 #pragma unroll
     for (int kp = 0; kp < 4; ++kp) {
       const int chunk = 2 * kp + (mi & 1);
       uint32_t r0, r1, r2, r3;
       ldsm_x4(kbase + k_tok * 128 + (((chunk ^ (k_tok & 7))) << 4), r0, r1, r2, r3);
-      uint32_t b[2][2][2];  // [h][n-tile][reg]
-      e4m3x4_to_f16x2x2(r0, b[0][0][0], b[0][0][1]);
-      e4m3x4_to_f16x2x2(r2, b[0][1][0], b[0][1][1]);
-      e4m3x4_to_f16x2x2(r1, b[1][0][0], b[1][0][1]);
-      e4m3x4_to_f16x2x2(r3, b[1][1][0], b[1][1][1]);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int kk = 2 * kp + h;
-        uint32_t a1 = 0u, a3 = 0u;
-        if constexpr (kTwoRows) {
-          a1 = qb[kk][0];
-          a3 = qb[kk][1];
-        }
-        float(&acc0)[4] = h ? s_odd[0] : s[0];
-        float(&acc1)[4] = h ? s_odd[1] : s[1];
-        mma_f16_16816(acc0, qa[kk][0], a1, qa[kk][1], a3, b[h][0][0], b[h][0][1]);
-        mma_f16_16816(acc1, qa[kk][0], a1, qa[kk][1], a3, b[h][1][0], b[h][1][1]);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(h ? r1 : r0, a0, a2);  // key gid
+        e4m3x4_to_f16x2x2(h ? r3 : r2, a1, a3);  // key gid + 8
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+          mma_f16_16816(h ? s_odd[nh] : s[nh], a0, a1, a2, a3, qf[nh][2 * kp + h][0],
+                        qf[nh][2 * kp + h][1]);
       }
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] += s_odd[nt][e];
 
-    // Online softmax in the log2 domain (k_scale folded into scale_log2).
-    float x[2][4];
+    // Online softmax in the log2 domain (k_scale folded into scale_log2), per
+    // head column over the page's 16 keys (rows: this lane's gid and gid + 8,
+    // the other keys in the lanes with the same tig).
+    const bool k0_in = tok0 + gid < len, k1_in = tok0 + gid + 8 < len;
+    uint32_t pb[NH][2];
+    bool all_same = true;
+    float alpha[NH][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nh = 0; nh < NH; ++nh) {
+      float pr[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * p.scale_log2;
-    if (tok0 + kBlockTokens > len) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (tok0 + nt * 8 + tig * 2 + (e & 1) >= len) x[nt][e] = -INFINITY;
-    }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    const float mn0 = fmaxf(m0, mx0);
-    const float alpha0 = ex2(m0 - mn0);
-    m0 = mn0;
-    float pr[2][4];
-    pr[0][0] = ex2(x[0][0] - mn0);
-    pr[0][1] = ex2(x[0][1] - mn0);
-    pr[1][0] = ex2(x[1][0] - mn0);
-    pr[1][1] = ex2(x[1][1] - mn0);
-    l0 = l0 * alpha0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    float alpha1 = 1.f;
-    if constexpr (kTwoRows) {
-      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn1 = fmaxf(m1, mx1);
-      alpha1 = ex2(m1 - mn1);
-      m1 = mn1;
-      pr[0][2] = ex2(x[0][2] - mn1);
-      pr[0][3] = ex2(x[0][3] - mn1);
-      pr[1][2] = ex2(x[1][2] - mn1);
-      pr[1][3] = ex2(x[1][3] - mn1);
-      l1 = l1 * alpha1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-    } else {
-      pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
+      for (int c = 0; c < 2; ++c) {
+        const float x0 = k0_in ? (s[nh][c] + s_odd[nh][c]) * p.scale_log2 : -INFINITY;
+        const float x1 = k1_in ? (s[nh][c + 2] + s_odd[nh][c + 2]) * p.scale_log2 : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[nh][c], mx);
+        alpha[nh][c] = ex2(m[nh][c] - mn);
+        all_same = all_same && m[nh][c] == mn;
+        m[nh][c] = mn;
+        pr[c] = ex2(x0 - mn);
+        pr[c + 2] = ex2(x1 - mn);
+        l[nh][c] = l[nh][c] * alpha[nh][c] + (pr[c] + pr[c + 2]);
+      }
+      // P^T as the B operand of the P V product: k = the page's keys, n = the
+      // heads; the lane's (key, two heads) pairs transposed into (two keys, head)
+      pb[nh][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));  // keys 2 tig, 2 tig + 1
+      pb[nh][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));  // keys 8 + 2 tig, 9 + 2 tig
     }
     // After the first pages the running max rarely moves: skip the rescale
-    // (alpha = 1 exactly) unless some row of the warp needs it.
-    if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f)) {
+    // (alpha = 1 exactly) unless some head of the warp needs it.
+    if (!__all_sync(0xffffffffu, all_same)) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        o[n][0] *= alpha0;
-        o[n][1] *= alpha0;
-        if constexpr (kTwoRows) {
-          o[n][2] *= alpha1;
-          o[n][3] *= alpha1;
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[nh][mt][0] *= alpha[nh][0];
+          o[nh][mt][1] *= alpha[nh][1];
+          o[nh][mt][2] *= alpha[nh][0];
+          o[nh][mt][3] *= alpha[nh][1];
         }
-      }
     }
 
-    // P as the f16 A operand (rows = heads, k = the 16 keys in order).
-    uint32_t ph[4];
-    ph[0] = pack_f16x2(pr[0][0], pr[0][1]);
-    ph[1] = pack_f16x2(pr[0][2], pr[0][3]);
-    ph[2] = pack_f16x2(pr[1][0], pr[1][1]);
-    ph[3] = pack_f16x2(pr[1][2], pr[1][3]);
-
-    // O += P V.  ldmatrix.trans over the codes as 16-bit units gives a thread
-    // keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim chunk; the
-    // byte permutes split that into the key pair of dim 2 gid (virtual n-tile
-    // 2 chunk) and of dim 2 gid + 1 (virtual n-tile 2 chunk + 1).
+    // O^T += V^T P^T.  ldmatrix.trans over the codes as 16-bit units gives a
+    // lane keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim
+    // chunk; the byte permute splits that into the key pair of dim 2 gid (row
+    // gid) and of dim 2 gid + 1 (row gid + 8).
     // Rows of the last page past the length may hold any code, NaN included:
     // zero them (their P is 0).  Each 16-bit unit holds one key's two codes,
     // keys (2 tig, 2 tig + 1) in r0 / r2 and 8 more in r1 / r3.
@@ -318,18 +316,15 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
       r1 &= vm1;
       r2 &= vm0;
       r3 &= vm1;
-      // per chunk h: bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
-      uint32_t be[2][2], bo[2][2];  // [h][key half]
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        e4m3x4_to_f16x2x2(__byte_perm(h ? r2 : r0, 0u, 0x3120), be[h][0], bo[h][0]);
-        e4m3x4_to_f16x2x2(__byte_perm(h ? r3 : r1, 0u, 0x3120), be[h][1], bo[h][1]);
-      }
+        // bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r2 : r0, 0u, 0x3120), a0, a1);  // keys 2 tig, +1
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r3 : r1, 0u, 0x3120), a2, a3);  // keys 8 + 2 tig, +1
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int vn = 2 * (2 * cp + h);
-        mma_f16_16816(o[vn], ph[0], ph[1], ph[2], ph[3], be[h][0], be[h][1]);
-        mma_f16_16816(o[vn + 1], ph[0], ph[1], ph[2], ph[3], bo[h][0], bo[h][1]);
+        for (int nh = 0; nh < NH; ++nh)
+          mma_f16_16816(o[nh][2 * cp + h], a0, a1, a2, a3, pb[nh][0], pb[nh][1]);
       }
     }
 
@@ -349,37 +344,40 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncwarp();
   }
 
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  if constexpr (kTwoRows) {
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  }
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 4);
+      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 8);
+      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 16);
+    }
 
-  // Cross-warp merge through shared memory.  Virtual n-tile vn = 2 chunk + par
-  // holds dims 16 chunk + 2 n + par; accumulator columns n = 2 tig, 2 tig + 1.
-  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);  // [G][D]
+  // Cross-warp merge through shared memory ([G][D] partial O, then m, l).
+  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);
   float* mml = mo + G * D;
 #pragma unroll
-  for (int vn = 0; vn < NT; ++vn) {
-    const int dim0 = 16 * (vn >> 1) + 4 * tig + (vn & 1);  // n = 2 tig; n = 2 tig + 1 is dim0 + 2
-    if (gid < G) {
-      mo[gid * D + dim0] = o[vn][0];
-      mo[gid * D + dim0 + 2] = o[vn][1];
+  for (int nh = 0; nh < NH; ++nh) {
+    const int h0 = 8 * nh + 2 * tig;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int dim0 = 16 * mt + 2 * gid;
+      if (h0 < G) {
+        mo[h0 * D + dim0] = o[nh][mt][0];
+        mo[h0 * D + dim0 + 1] = o[nh][mt][2];
+      }
+      if (h0 + 1 < G) {
+        mo[(h0 + 1) * D + dim0] = o[nh][mt][1];
+        mo[(h0 + 1) * D + dim0 + 1] = o[nh][mt][3];
+      }
     }
-    if constexpr (kTwoRows) {
-      mo[(gid + 8) * D + dim0] = o[vn][2];
-      mo[(gid + 8) * D + dim0 + 2] = o[vn][3];
-    }
-  }
-  if (tig == 0) {
-    if (gid < G) {
-      mml[gid] = m0;
-      mml[G + gid] = l0;
-    }
-    if constexpr (kTwoRows) {
-      mml[gid + 8] = m1;
-      mml[G + gid + 8] = l1;
+    if (gid == 0) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        if (h0 + c < G) {
+          mml[h0 + c] = m[nh][c];
+          mml[G + h0 + c] = l[nh][c];
+        }
     }
   }
   __syncthreads();
