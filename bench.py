@@ -65,6 +65,11 @@ def parse_args():
                     help="shrink the mixed step to this many decode sequences (profiling runs)")
     ap.add_argument("--only-mixed", action="store_true",
                     help="time only the mixed step (profiling runs)")
+    ap.add_argument("--only-append", action="store_true",
+                    help="run only the bulk append probe (profiling runs)")
+    ap.add_argument("--append-tokens", type=int, default=262144,
+                    help="tokens of the bulk append probe")
+    ap.add_argument("--append-steps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -555,9 +560,9 @@ def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps
 
 
 def run_append_probe(dev, pagedkv, E, peak, tokens=262144, steps=20):
-    """Bulk KV append: 262,144 tokens of the 70B-GQA row shape (8 KV heads x
-    128, 4096 B of K+V per token in bf16) scattered to random slots of a pool
-    1.25x their size.  Bytes = rows read + rows written."""
+    """Bulk KV append: `tokens` (default 262,144) of the 70B-GQA row shape (8
+    KV heads x 128, 4096 B of K+V per token in bf16) scattered to random slots
+    of a pool 1.25x their size.  Bytes = rows read + rows written."""
     hkv, d = 8, 128
     g = torch.Generator(device=dev).manual_seed(7001)
     k = torch.randn(tokens, hkv, d, generator=g, device=dev).to(torch.bfloat16)
@@ -760,6 +765,12 @@ def run_ours(args):
 
     if args.only_mixed:
         print(json.dumps({"mixed_step": run_mixed(args, dev, pagedkv, torch.cuda.Event)}))
+        return
+    if args.only_append:
+        peak, _ = measured_peak()
+        print(json.dumps({"append_probe": run_append_probe(dev, pagedkv, torch.cuda.Event, peak,
+                                                           args.append_tokens,
+                                                           args.append_steps)}))
         return
     if args.only_verify:
         peak, _ = measured_peak()
