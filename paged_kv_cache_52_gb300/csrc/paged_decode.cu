@@ -32,6 +32,8 @@
 //    its log2-sum-exp, and a small merge kernel combines the partitions.
 //  * every mbarrier wait is bounded; a timeout sets an error bit, drains the
 //    warp's outstanding copies (also bounded) and lets the CTA finish.
+#include <climits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "pkv_decode_common.cuh"
@@ -392,6 +394,50 @@ __global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParam
   p.out[row * D + threadIdx.x] = tot > 0.f ? val / tot : 0.f;
 }
 
+// The same merge with one warp-sized group of threads per row, each thread
+// four consecutive dims as float4 (out 16-byte aligned): a quarter of the
+// CTAs of the scalar form and four partial values in flight per load.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodeParams p,
+                                                                  long long total_rows) {
+  constexpr int TPR = D / 4;  // threads per row
+  const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = gtid / TPR;
+  const int c4 = int(gtid - row * TPR);
+  if (row >= total_rows) return;
+  const int seq = int(row / p.q_heads);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const int nparts_s = span_parts(sp, p);
+  const bool extra = p.extra_o != nullptr;
+  if (nparts_s == 1 && !p.force_partials) return;  // written by the split kernel
+  const float* lse = p.part_lse + row * p.num_parts;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + row * p.num_parts * D) + c4;
+  float big = extra ? __ldg(p.extra_lse + row) : -INFINITY;
+  for (int q = 0; q < nparts_s; ++q) big = fmaxf(big, __ldg(lse + q));
+  float tot = 0.f;
+  float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (extra) {
+    const float w = ex2(__ldg(p.extra_lse + row) - big);
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p.extra_o + row * D) + c4);
+    tot += w;
+    val = make_float4(w * x.x, w * x.y, w * x.z, w * x.w);
+  }
+#pragma unroll 4
+  for (int q = 0; q < nparts_s; ++q) {
+    const float w = ex2(__ldg(lse + q) - big);
+    const float4 x = __ldg(po + size_t(q) * TPR);
+    tot += w;
+    val.x += w * x.x;
+    val.y += w * x.y;
+    val.z += w * x.z;
+    val.w += w * x.w;
+  }
+  // the same division as the scalar form, so both give the same bits
+  reinterpret_cast<float4*>(p.out + row * D)[c4] =
+      tot > 0.f ? make_float4(val.x / tot, val.y / tot, val.z / tot, val.w / tot)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 template <int D, int G>
 static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
                                    const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
@@ -416,12 +462,22 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream) {
   if (prm.num_parts == 1 && !prm.force_partials) return cudaSuccess;
-  if (d_head == 128)
+  const long long rows = (long long)num_seqs * prm.q_heads;
+  const bool vec = (reinterpret_cast<uintptr_t>(prm.out) & 15) == 0;
+  if (vec && (d_head == 128 || d_head == 64)) {
+    const long long blocks = (rows * (d_head / 4) + 255) / 256;
+    if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+    if (d_head == 128)
+      paged_decode_merge4_kernel<128><<<unsigned(blocks), 256, 0, stream>>>(prm, rows);
+    else
+      paged_decode_merge4_kernel<64><<<unsigned(blocks), 256, 0, stream>>>(prm, rows);
+  } else if (d_head == 128) {
     paged_decode_merge_kernel<128><<<num_seqs * prm.q_heads, 128, 0, stream>>>(prm);
-  else if (d_head == 64)
+  } else if (d_head == 64) {
     paged_decode_merge_kernel<64><<<num_seqs * prm.q_heads, 64, 0, stream>>>(prm);
-  else
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

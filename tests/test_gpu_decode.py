@@ -119,3 +119,25 @@ def test_full_size_configs_sampled(pk, name, seqs):
     assert pk.get_device_error() == 0
     del w
     torch.cuda.empty_cache()
+
+
+def test_merge_output_alignment_forms_agree(pk):
+    # the split-K merge writes float4 rows when out is 16-byte aligned and
+    # one float per thread otherwise (the ABI asks only for 4-byte alignment);
+    # both forms compute the same sums and divisions, so the same bits
+    w = _to_dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[1024, 3000, 777, 64]))
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    S, hq, d = w.q.shape
+    kw = dict(max_context_len=3000, partition_blocks=16)   # several partitions per sequence
+    aligned = pk.paged_decode_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, **kw)
+    buf = torch.full((S * hq * d + 1,), float("nan"), dtype=torch.float32, device=DEV)
+    shifted = buf[1:].view(S, hq, d)                        # 4 bytes past a 16-byte boundary
+    assert shifted.data_ptr() % 16 == 4
+    pk.paged_decode_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, out=shifted,
+                              **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(aligned, shifted)
+    ref = DecodeStepOracle(w, range(S)).output()
+    assert_attention_close(shifted.cpu().numpy(), ref, "merge, 4-byte aligned out")
+    assert pk.get_device_error(clear=True) == 0
