@@ -231,12 +231,12 @@ PKV_API int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start
 /*
  * pkv_paged_prefill_attention_limited -- pkv_paged_prefill_attention_ex on at
  * most max_ctas SMs, leaving the others to kernels on other streams.  The
- * continuous-batching step ("Cache KV, attention et optimisation de
- * l'inference", section on continuous batching; CS336 notes, lecture 10,
- * selective batching) runs chunked prefills next to running decodes: the
- * prefill is bound by the tensor cores and the decode by HBM, so the decode
- * launched on another stream after this call runs on the remaining SMs at
- * the same time instead of after it.
+ * continuous-batching step (nano-vLLM page, section "Traitement par lots
+ * continu"; "第 10 讲：推理（Inference）", "关键要点": iteration-level
+ * scheduling and selective batching) runs chunked prefills next to running
+ * decodes.  The prefill is bound by the tensor cores and the decode by HBM,
+ * so a decode launched on another stream after this call runs on the
+ * remaining SMs at the same time instead of after it.
  * Same result as pkv_paged_prefill_attention_ex (bit for bit: the same
  * tiles in the same arithmetic); max_ctas persistent CTAs take the
  * (sequence x KV head, query tile) items longest first from a counter in
