@@ -87,10 +87,15 @@ def test_decode_plan_and_workspace(pk):
     with pytest.raises(pk.PagedKVError):
         pk.decode_plan(4, 8, 2, 64, -1)
     # automatic plan: about two work items per SM, partitions within [16, 256] pages
-    pb, parts, _ = pk.decode_plan(4, 64, 8, 128, 131072)
-    assert 16 <= pb <= 256 and parts == -(-8192 // pb)
+    pb, parts, _ = pk.decode_plan(256, 64, 8, 128, 8192)
+    assert 16 <= pb <= 256 and parts == -(-512 // pb)
     pb_small, _, _ = pk.decode_plan(4, 64, 8, 128, 2048)     # few items: short partitions
     assert pb_small == 16
+    # few (sequence, KV head) pairs with long contexts: equal partitions that
+    # all fit in one wave of two CTAs per SM (at most 1024 pages each)
+    pb, parts, _ = pk.decode_plan(4, 64, 8, 128, 131072)
+    assert 256 < pb <= 1024 and parts == -(-8192 // pb)
+    assert 4 * 8 * parts <= 2 * 152
     assert pk.lib.pkv_decode_workspace_bytes(4, 64, 8, 128, 131072) == \
         pk.decode_plan(4, 64, 8, 128, 131072)[2]
 
