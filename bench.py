@@ -407,13 +407,46 @@ def run_mixed(args, dev, pagedkv, E):
         m[3].record()
     torch.cuda.synchronize()
     ms8 = lambda i, j: sum(m[i].elapsed_time(m[j]) for m in marks8) / K  # noqa: E731
+    # the FP8 step with the SMs split: the FP8 prefill persistent on at most
+    # `ctas` SMs (high-priority stream), the FP8 decode on the others
+    def fp8_concurrent(ctas):
+        parts8[0]()
+        s_pre_hi.wait_stream(main)
+        s_dec.wait_stream(main)
+        with torch.cuda.stream(s_pre_hi):
+            pagedkv.paged_prefill_attention_fp8(
+                w.q_prefill, w.q_start, kc8, vc8, w.prefill_tables, w.prefill_lens, True,
+                w.scale, ks8, vs8, out=pout, max_q_len=chunk, workspace=pws8, max_ctas=ctas)
+        with torch.cuda.stream(s_dec):
+            parts8[2]()
+        main.wait_stream(s_pre_hi)
+        main.wait_stream(s_dec)
+
+    def time_fp8_concurrent(ctas, steps=K):
+        for _ in range(3):
+            fp8_concurrent(ctas)
+        torch.cuda.synchronize()
+        c0, c1 = E(enable_timing=True), E(enable_timing=True)
+        c0.record()
+        for _ in range(steps):
+            fp8_concurrent(ctas)
+        c1.record()
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / steps
+
+    fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (72, 88, 104, 120)}
+    fp8_best = min(fp8_sweep, key=fp8_sweep.get)
     fp8_step = {"ms_per_step": round(ms8(0, 3), 4), "append_ms": round(ms8(0, 1), 4),
                 "prefill_ms": round(ms8(1, 2), 4), "decode_ms": round(ms8(2, 3), 4),
                 "k_scale": ks8, "v_scale": vs8,
                 "prefill_note": "FP8 pages widened in a workspace (K to bf16, V to f16, exact), "
                                 "then the tcgen05 prefill with P as one f16 operand and "
                                 "k_scale/v_scale folded in",
-                "gpu_launches": K * (4 + (1 if ws is not None else 0))}
+                "gpu_launches": K * (4 + (1 if ws is not None else 0)),
+                "two_streams_sm_split": {
+                    "ms_per_step": round(time_fp8_concurrent(fp8_best), 4),
+                    "prefill_ctas": fp8_best, "sweep_ms_by_prefill_ctas": fp8_sweep,
+                    "note": "FP8 decode on the SMs the persistent FP8 prefill leaves free"}}
     del kc8, vc8, pws8
     flops = prefill_flops(plens, [chunk] * len(plens)) * 4 * hq * d
     row = 2 * hkv * d * 2

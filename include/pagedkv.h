@@ -378,6 +378,26 @@ PKV_API int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_star
                                             pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention_fp8_limited -- pkv_paged_prefill_attention_fp8
+ * on at most max_ctas SMs (persistent CTAs taking query tiles from a counter
+ * in the workspace), leaving the other SMs to a decode launched on another
+ * stream, as pkv_paged_prefill_attention_limited does for bf16 pools.  Same
+ * result bit for bit.  max_ctas >= 1 (PKV_EINVAL otherwise); the workspace
+ * as for pkv_paged_prefill_attention_fp8.  Calls that share a workspace must
+ * not overlap.
+ */
+PKV_API int pkv_paged_prefill_attention_fp8_limited(const void* q, const int32_t* q_start,
+                                                    int num_seqs, int total_q, int max_q_len,
+                                                    int q_heads, const void* k_cache,
+                                                    const void* v_cache, pkv_cache_desc cache,
+                                                    const int32_t* block_tables,
+                                                    int max_blocks_per_seq,
+                                                    const int32_t* context_lens, int causal,
+                                                    float scale, float k_scale, float v_scale,
+                                                    float* out, int max_ctas, void* workspace,
+                                                    size_t ws_bytes, pkv_stream_t stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that are handed
  * device buffers but may not call cudaMalloc (a fixed, pre-reserved memory

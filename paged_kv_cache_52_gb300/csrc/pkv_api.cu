@@ -561,17 +561,16 @@ int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_s
 size_t pkv_paged_prefill_attention_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
                                                        int kv_heads, int d_head) {
   Fp8PrefillLayout w;
-  return fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w) ? w.counter_off
-                                                                                 : 0;
+  return fp8_prefill_layout(num_seqs, max_blocks_per_seq, kv_heads, d_head, &w) ? w.total : 0;
 }
 
-int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int num_seqs,
-                                    int total_q, int max_q_len, int q_heads, const void* k_cache,
-                                    const void* v_cache, pkv_cache_desc cache,
-                                    const int32_t* block_tables, int max_blocks_per_seq,
-                                    const int32_t* context_lens, int causal, float scale,
-                                    float k_scale, float v_scale, float* out, void* workspace,
-                                    size_t ws_bytes, pkv_stream_t stream) {
+namespace {
+
+int prefill_fp8(const void* q, const int32_t* q_start, int num_seqs, int total_q, int max_q_len,
+                int q_heads, const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                int causal, float scale, float k_scale, float v_scale, float* out,
+                void* workspace, size_t ws_bytes, int max_ctas, pkv_stream_t stream) {
   int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
                          cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
   if (st != PKV_OK) return st;
@@ -581,7 +580,7 @@ int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int n
   Fp8PrefillLayout w;
   if (!fp8_prefill_layout(num_seqs, max_blocks_per_seq, cache.kv_heads, cache.d_head, &w))
     return PKV_EUNSUPPORTED;
-  if (!workspace || ws_bytes < w.counter_off) return PKV_ENOMEM;
+  if (!workspace || ws_bytes < w.total) return PKV_ENOMEM;
   if (!aligned(workspace, 256)) return PKV_EINVAL;
   const int sms = current_device_sms();
   if (sms <= 0) return PKV_ECUDA;
@@ -597,7 +596,36 @@ int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int n
   return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, ws + w.k_off,
                      ws + w.v_off, scratch, reinterpret_cast<const int32_t*>(ws + w.table_off),
                      max_blocks_per_seq, context_lens, causal,
-                     scale * k_scale * 1.4426950408889634f, v_scale, out, cs, /*f16_pv=*/true);
+                     scale * k_scale * 1.4426950408889634f, v_scale, out, cs, /*f16_pv=*/true,
+                     nullptr, 0, max_ctas, reinterpret_cast<int*>(ws + w.counter_off));
+}
+
+}  // namespace
+
+int pkv_paged_prefill_attention_fp8(const void* q, const int32_t* q_start, int num_seqs,
+                                    int total_q, int max_q_len, int q_heads, const void* k_cache,
+                                    const void* v_cache, pkv_cache_desc cache,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int causal, float scale,
+                                    float k_scale, float v_scale, float* out, void* workspace,
+                                    size_t ws_bytes, pkv_stream_t stream) {
+  return prefill_fp8(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache, cache,
+                     block_tables, max_blocks_per_seq, context_lens, causal, scale, k_scale,
+                     v_scale, out, workspace, ws_bytes, 0, stream);
+}
+
+int pkv_paged_prefill_attention_fp8_limited(const void* q, const int32_t* q_start, int num_seqs,
+                                            int total_q, int max_q_len, int q_heads,
+                                            const void* k_cache, const void* v_cache,
+                                            pkv_cache_desc cache, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* context_lens,
+                                            int causal, float scale, float k_scale, float v_scale,
+                                            float* out, int max_ctas, void* workspace,
+                                            size_t ws_bytes, pkv_stream_t stream) {
+  if (max_ctas < 1) return PKV_EINVAL;
+  return prefill_fp8(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache, cache,
+                     block_tables, max_blocks_per_seq, context_lens, causal, scale, k_scale,
+                     v_scale, out, workspace, ws_bytes, max_ctas, stream);
 }
 
 size_t pkv_paged_prefill_workspace_bytes(int num_seqs, int max_blocks_per_seq, int kv_heads,

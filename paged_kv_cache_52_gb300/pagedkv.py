@@ -92,6 +92,11 @@ SIGNATURES = {
     "pkv_paged_prefill_attention_ex": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
                                         ctypes.c_int, _f32, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "pkv_paged_prefill_attention_fp8_limited": ([_vp, _vp, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
+                                                 _vp, ctypes.c_int, _vp, ctypes.c_int, _f32,
+                                                 _f32, _f32, _vp, ctypes.c_int, _vp, _sz, _vp],
+                                                ctypes.c_int),
     "pkv_paged_prefill_attention_limited": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, _vp, _vp, CacheDesc, _vp,
                                              ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
@@ -395,10 +400,13 @@ def paged_prefill_attention_fp8(q: torch.Tensor, q_start: torch.Tensor, k_cache:
                                 k_scale: float, v_scale: float,
                                 out: Optional[torch.Tensor] = None,
                                 max_q_len: Optional[int] = None,
-                                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                workspace: Optional[torch.Tensor] = None,
+                                max_ctas: Optional[int] = None) -> torch.Tensor:
     """Chunked prefill over FP8 (e4m3) pools with per-pool scales: the
     attention of the dequantized cache.  ``workspace`` (uint8, at least
-    ``prefill_fp8_workspace_bytes(...)``) holds the widened pages."""
+    ``prefill_fp8_workspace_bytes(...)``) holds the widened pages.
+    ``max_ctas`` runs the tensor-core prefill on at most that many SMs
+    (``pkv_paged_prefill_attention_fp8_limited``)."""
     _check_fp8_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
           "q must be a contiguous [total, Hq, d] bf16 CUDA tensor")
@@ -420,6 +428,14 @@ def paged_prefill_attention_fp8(q: torch.Tensor, q_start: torch.Tensor, k_cache:
     need = prefill_fp8_workspace_bytes(S, block_tables.shape[1], k_cache.shape[2], d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if max_ctas is not None:
+        st = lib.pkv_paged_prefill_attention_fp8_limited(
+            _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+            cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(bool(causal)), float(scale), float(k_scale), float(v_scale), _ptr(out),
+            int(max_ctas), _ptr(workspace), workspace.numel(), _stream(q))
+        _check("pkv_paged_prefill_attention_fp8_limited", st)
+        return out
     st = lib.pkv_paged_prefill_attention_fp8(
         _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
         cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),

@@ -142,7 +142,8 @@ def test_fp8_prefill_host_validation(pk):
     d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
     need = lib.pkv_paged_prefill_attention_fp8_workspace_bytes(4, 8, 2, 128)
     pool = 4 * 8 * 16 * 2 * 128 * 2                     # bf16 pages of 4 x 8 blocks
-    assert need == 2 * pool + 256                        # K, V scratch pools + the table
+    # K, V scratch pools + the table + the persistent launch's work counter
+    assert need == 2 * pool + 256 + 256
     assert lib.pkv_paged_prefill_attention_fp8_workspace_bytes(0, 8, 2, 128) == 0
 
     def call(desc=d128, k_scale=1.0, v_scale=1.0, ws=dummy, wsb=need, S=4):
@@ -154,6 +155,14 @@ def test_fp8_prefill_host_validation(pk):
     assert call(desc=_desc(pk, d=96)) == -2
     assert call(wsb=need - 1) == -4 and call(ws=null) == -4
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -1   # workspace not 256-byte aligned
+
+    def limited(ctas=8, ws=dummy, wsb=need, S=4):
+        return lib.pkv_paged_prefill_attention_fp8_limited(dummy, dummy, S, 40, 16, 8, dummy,
+                                                           dummy, d128, dummy, 8, dummy, 1, 0.1,
+                                                           1.0, 1.0, dummy, ctas, ws, wsb, null)
+    assert limited(ctas=0) == -1
+    assert limited(ws=null) == -4 and limited(wsb=need - 1) == -4
+    assert limited(S=0) == 0
 
 
 def test_prefill_workspace_host_validation(pk):

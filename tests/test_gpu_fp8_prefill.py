@@ -165,3 +165,22 @@ def test_fp8_mixed_step_prefill_sampled(pk):
             got.append(out[int(rows[row])].cpu().numpy())
     assert_attention_close(np.stack(got), np.stack(ref), "fp8 mixed-step prefill")
     assert pk.get_device_error(clear=True) == 0
+
+
+def test_fp8_prefill_limited_sms_equals_grid(pk):
+    # the persistent launch on at most N SMs computes the same tiles in the
+    # same arithmetic: bitwise the grid launch's output, for any N
+    w = _dev(wl.make_chunked_workload(64, 8, 128, [500, 0, 33, 2000], [300, 77, 129, 64],
+                                      config_id=9))
+    ks, vs = wl.FP8_SCALES["gqa70b"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    grid, kc, vc = _step(pk, w, kc8, vc8, ks, vs, True, 300)
+    for ctas in (1, 9, 100000):
+        out = pk.paged_prefill_attention_fp8(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
+                                             w.prefill_lens, True, w.scale, ks, vs,
+                                             max_q_len=300, max_ctas=ctas)
+        torch.cuda.synchronize()
+        assert torch.equal(out, grid), f"max_ctas={ctas}"
+    ref, _ = _fp8_oracle(w, kc8, vc8, ks, vs, True, range(4))
+    assert_attention_close(grid.cpu().numpy(), ref, "fp8 prefill (grid and limited)")
+    assert pk.get_device_error(clear=True) == 0
