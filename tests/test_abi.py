@@ -86,9 +86,13 @@ def test_decode_plan_and_workspace(pk):
         pk.decode_plan(4, 8, 2, 64, 100, partition_blocks=2048)
     with pytest.raises(pk.PagedKVError):
         pk.decode_plan(4, 8, 2, 64, -1)
-    # automatic plan: about two work items per SM, partitions within [16, 256] pages
+    # automatic plan, more (sequence, KV head) pairs than CTA slots: partitions
+    # of about 150 sqrt(pairs / slots) pages (about 390 for 2048 pairs on 148
+    # to 152 SMs), at most what two work items per SM would give
     pb, parts, _ = pk.decode_plan(256, 64, 8, 128, 8192)
-    assert 16 <= pb <= 256 and parts == -(-512 // pb)
+    assert 360 <= pb <= 420 and parts == -(-512 // pb)
+    pb, _, _ = pk.decode_plan(64, 64, 8, 128, 8192)           # 512 pairs
+    assert 180 <= pb <= 210
     pb_small, _, _ = pk.decode_plan(4, 64, 8, 128, 2048)     # few items: short partitions
     assert pb_small == 16
     # few (sequence, KV head) pairs with long contexts: equal partitions that
