@@ -490,6 +490,120 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
         if (lane == 0) mbar_arrive(p_full);
         continue;
       }
+      // hi + lo P keeps fp32's exponent range, so a stale running max only
+      // has to keep the exponentials finite.  After the first tile, where no
+      // row needs the mask, the max pass is skipped: the exponentials are
+      // taken against m_used, 64 keys at a time, and a group is kept while
+      // every row's sum over it stays <= 2^64 (every weight is at most that
+      // sum).  A first group that fails leaves S intact for the two-pass path
+      // below; a second group that fails after the first was stored raises
+      // the max from its own scores and rescales O, the row sum and the
+      // stored first group (hi + lo is exact in fp32) before recomputing.
+      if (__all_sync(0xffffffffu, j > 0 && !need_mask && p.scale_log2 > 0.f)) {
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        bool two_pass = false;
+        for (int g = 0; g < 2; ++g) {
+          float va[32], vb[32];
+          tmem_ld32(lane_base + s_col + 64 * g, va);
+          tmem_ld32(lane_base + s_col + 64 * g + 32, vb);
+          tmem_wait_ld();
+          for (int attempt = 0;; ++attempt) {
+            uint32_t hi[32], lo[32];
+            const uint64_t nm2 = f2_pack(-m_used, -m_used);
+            uint64_t ls2[2] = {0ull, 0ull};
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              const int kk = 2 * u;
+              const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+              const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+              const float e0 = ex2(x0), e1 = ex2(x1);
+              const uint64_t e = f2_pack(e0, e1);
+              ls2[u & 1] = f2_add(ls2[u & 1], e);
+              hi[u] = pack_bf16x2(e0, e1);
+              float r0, r1;
+              f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
+              lo[u] = pack_bf16x2(r0, r1);
+            }
+            float a0, a1, b0, b1;
+            f2_unpack(ls2[0], a0, a1);
+            f2_unpack(ls2[1], b0, b1);
+            const float gsum = (a0 + a1) + (b0 + b1);
+            // NaN or inf fail the test
+            if (attempt > 0 || __all_sync(0xffffffffu, gsum <= 18446744073709551616.f)) {
+              lsum += gsum;
+              tmem_st32u(lane_base + s_col + 64 * g, hi);
+              tmem_st32u(lane_base + s_col + 64 * g + 32, lo);
+              break;
+            }
+            if (g == 0) {  // nothing stored yet
+              two_pass = true;
+              break;
+            }
+            // the max rose within the second group: take it from its scores
+            float ex[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) ex[a] = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ex[i & 7] = max3f(ex[i & 7], va[i], vb[i]);
+            const float ext = fmaxf(fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])),
+                                    fmaxf(fmaxf(ex[4], ex[5]), fmaxf(ex[6], ex[7])));
+            const float m_new = fmaxf(m_used, ext * p.scale_log2);
+            const float alpha = ex2(m_used - m_new);
+            const uint64_t a2 = f2_pack(alpha, alpha);
+            // PV_{j-1} must be done before O is rescaled
+            ok = __all_sync(0xffffffffu, pf_wait(o_done, (j - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(lane_base + o_col + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; i += 2)
+                f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), a2), o[i], o[i + 1]);
+              tmem_st32(lane_base + o_col + c * 32, o);
+            }
+            // the first group's stored P: hi + lo (exact in fp32) times alpha,
+            // split again, 16 columns (32 keys) at a time
+            tmem_wait_st();
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              float ph[16], pl[16];
+              tmem_ld16(lane_base + s_col + 16 * c, ph);
+              tmem_ld16(lane_base + s_col + 32 + 16 * c, pl);
+              tmem_wait_ld();
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const uint32_t hw = __float_as_uint(ph[u]), lw = __float_as_uint(pl[u]);
+                float e0, e1;
+                f2_unpack(f2_mul(f2_add(f2_pack(bf16_lo_to_f32(hw), bf16_hi_to_f32(hw)),
+                                        f2_pack(bf16_lo_to_f32(lw), bf16_hi_to_f32(lw))),
+                                 a2),
+                          e0, e1);
+                const uint32_t h = pack_bf16x2(e0, e1);
+                ph[u] = __uint_as_float(h);
+                pl[u] = __uint_as_float(pack_bf16x2(e0 - bf16_lo_to_f32(h), e1 - bf16_hi_to_f32(h)));
+              }
+              tmem_st16(lane_base + s_col + 16 * c, ph);
+              tmem_st16(lane_base + s_col + 32 + 16 * c, pl);
+            }
+            lsum *= alpha;
+            m_used = m_new;
+          }
+          if (!ok || two_pass) break;
+        }
+        if (!ok) break;
+        if (!two_pass) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
+          continue;
+        }
+      }
       // pass 1: row max.  On unmasked tiles the max is taken over the raw
       // scores and scaled once (scale > 0 keeps the order; scale < 0 flips it).
       float mx;

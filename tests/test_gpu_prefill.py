@@ -157,3 +157,22 @@ def test_non_causal_chunk_longer_than_context(pk):
     torch.cuda.synchronize()
     assert_attention_close(out.cpu().numpy(), ref, "non-causal n > context")
     assert pk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("key", [140, 197])
+def test_running_max_jump_inside_a_tile(pk, key):
+    # after the first 128-key tile the kernel takes the exponentials against
+    # the running max with no max pass and checks each 64-key group's sum; a
+    # key whose score jumps far above the max fails that check.  Key 140 sits
+    # in the first group of the second tile (recomputed with the max pass),
+    # key 197 in the second group, after the first group was stored (its P,
+    # O and the row sum are rescaled in place).  Both must match the oracle.
+    w = wl.make_chunked_workload(64, 8, 128, [300], [64], config_id=21)
+    rows = w.k_cache.view(-1, 8, 128)
+    tables = w.prefill_tables.numpy()
+    slot = int(tables[0, key // 16]) * 16 + key % 16
+    rows[slot] = (rows[slot].float() * 100.0).to(torch.bfloat16)
+    ref = PrefillStepOracle(w, [0]).output()
+    out, _, _ = run_prefill(pk, _to_dev(w), max_q_len=64)
+    assert_attention_close(out.cpu().numpy(), ref, f"max jump at key {key}")
+    assert pk.get_device_error(clear=True) == 0
