@@ -166,6 +166,29 @@ PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_hea
                                   int partition_blocks, pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_attention_bf16out -- pkv_paged_decode_attention_ex with a
+ * bf16 output.  bf16 is inference's default type ("第 10 讲：推理（Inference）",
+ * "核心概念与定义": bf16 as the inference default, 2 bytes per value in the
+ * attention step's byte count), so the layer after attention reads bf16.
+ * The arithmetic is the float32 path's; only the final store rounds each
+ * value to the nearest bf16 (ties to even), so out equals the float32
+ * output of pkv_paged_decode_attention_ex rounded to bf16, bit for bit.
+ *   out : [num_seqs][q_heads][d_head] bf16, 2-byte aligned (8-byte
+ *         alignment lets the split-K merge store four values at once).
+ * Other arguments, the workspace and the errors are those of
+ * pkv_paged_decode_attention_ex.
+ */
+PKV_API int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,
+                                               const void* k_cache, const void* v_cache,
+                                               pkv_cache_desc cache,
+                                               const int32_t* block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t* context_lens, int max_context_len,
+                                               float scale, void* out, void* workspace,
+                                               size_t ws_bytes, int partition_blocks,
+                                               pkv_stream_t stream);
+
+/*
  * pkv_paged_prefill_attention -- chunked prefill: each sequence's new query
  * tokens attend over its paged context (the continuous-batching step in which
  * new prompt chunks join running decodes).  Runs on the tcgen05 tensor cores.
@@ -254,6 +277,28 @@ PKV_API int pkv_paged_prefill_attention_limited(const void* q, const int32_t* q_
                                                 float scale, float* out, int max_ctas,
                                                 void* workspace, size_t ws_bytes,
                                                 pkv_stream_t stream);
+
+/*
+ * pkv_paged_prefill_attention_bf16out -- the chunked prefill with a bf16
+ * output (bf16 as the inference default: "第 10 讲：推理（Inference）",
+ * "核心概念与定义").  With a workspace it is pkv_paged_prefill_attention_ex,
+ * with workspace NULL pkv_paged_prefill_attention; the epilogue rounds each
+ * value of O / l (ties to even) instead of storing float32, so out equals
+ * that entry point's float32 output rounded to bf16, bit for bit.
+ *   out : [total_q][q_heads][d_head] bf16, 16-byte aligned; rows outside
+ *         every chunk are not written.
+ * Other arguments, the workspace and the errors are those of
+ * pkv_paged_prefill_attention_ex.
+ */
+PKV_API int pkv_paged_prefill_attention_bf16out(const void* q, const int32_t* q_start,
+                                                int num_seqs, int total_q, int max_q_len,
+                                                int q_heads, const void* k_cache,
+                                                const void* v_cache, pkv_cache_desc cache,
+                                                const int32_t* block_tables,
+                                                int max_blocks_per_seq,
+                                                const int32_t* context_lens, int causal,
+                                                float scale, void* out, void* workspace,
+                                                size_t ws_bytes, pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention_shared_prefix -- the same result as

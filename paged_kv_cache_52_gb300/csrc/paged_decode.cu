@@ -88,7 +88,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (part >= nparts_s) return;
   const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
   if (sp.count == 0) {  // empty context: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p, row0 * D + i, 0.f);
     return;
   }
   const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
@@ -355,7 +355,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const float res = val / tot;
     if (final_out) {
-      p.out[(row0 + row) * D + col] = res;
+      store_out(p, (row0 + row) * D + col, res);
     } else {
       const size_t prow = (row0 + row) * p.num_parts + part;
       p.part_o[prow * D + col] = res;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParam
     tot += w;
     val += w * __ldg(po + size_t(q) * D);
   }
-  p.out[row * D + threadIdx.x] = tot > 0.f ? val / tot : 0.f;
+  store_out(p, row * D + threadIdx.x, tot > 0.f ? val / tot : 0.f);
 }
 
 // The same merge with one warp-sized group of threads per row, each thread
@@ -433,9 +433,18 @@ __global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodePa
     val.w += w * x.w;
   }
   // the same division as the scalar form, so both give the same bits
-  reinterpret_cast<float4*>(p.out + row * D)[c4] =
-      tot > 0.f ? make_float4(val.x / tot, val.y / tot, val.z / tot, val.w / tot)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 res = tot > 0.f ? make_float4(val.x / tot, val.y / tot, val.z / tot, val.w / tot)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (p.out_bf16) {  // four bf16 (8 bytes; out 8-byte aligned)
+    __nv_bfloat162 lo = __floats2bfloat162_rn(res.x, res.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(res.z, res.w);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * D)[c4] = v;
+  } else {
+    reinterpret_cast<float4*>(p.out + row * D)[c4] = res;
+  }
 }
 
 template <int D, int G>
@@ -463,7 +472,8 @@ cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_hea
                                 cudaStream_t stream) {
   if (prm.num_parts == 1 && !prm.force_partials) return cudaSuccess;
   const long long rows = (long long)num_seqs * prm.q_heads;
-  const bool vec = (reinterpret_cast<uintptr_t>(prm.out) & 15) == 0;
+  const uintptr_t vec_align = prm.out_bf16 ? 7 : 15;  // four outputs per thread
+  const bool vec = (reinterpret_cast<uintptr_t>(prm.out) & vec_align) == 0;
   if (vec && (d_head == 128 || d_head == 64)) {
     const long long blocks = (rows * (d_head / 4) + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
@@ -516,6 +526,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.force_partials = a.force_partials;
   prm.extra_o = a.extra_o;
   prm.extra_lse = a.extra_lse;
+  prm.out_bf16 = a.out_bf16 ? 1 : 0;
   const int group = a.q_heads / a.kv_heads;
   if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);

@@ -131,7 +131,7 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (part >= nparts_s) return;
   const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
   if (sp.count == 0) {  // empty context: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p, row0 * D + i, 0.f);
     return;
   }
   const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
@@ -401,7 +401,7 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const float res = val / tot * p.out_scale;
     if (final_out) {
-      p.out[(row0 + row) * D + col] = res;
+      store_out(p, (row0 + row) * D + col, res);
     } else {
       const size_t prow = (row0 + row) * p.num_parts + part;
       p.part_o[prow * D + col] = res;
@@ -450,6 +450,7 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap
   prm.force_partials = 0;
   prm.extra_o = nullptr;
   prm.extra_lse = nullptr;
+  prm.out_bf16 = a.out_bf16 ? 1 : 0;
   switch (a.q_heads / a.kv_heads) {
     case 1: return launch_fp8_t<1>(prm, a.num_seqs, tmap_k, tmap_v, stream);
     case 2: return launch_fp8_t<2>(prm, a.num_seqs, tmap_k, tmap_v, stream);

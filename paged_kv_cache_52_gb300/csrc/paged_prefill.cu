@@ -118,6 +118,7 @@ struct PrefillParams {
   int* work_counter;
   int num_items;                // pairs * tiles_per_pair
   int tiles_per_pair;           // CTA-sized query tiles of the longest chunk
+  int out_bf16;                 // nonzero: out holds bf16, rounded to nearest even
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -752,13 +753,21 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
         const float inv = p.out_scale / lsum;
         const size_t orow_idx = size_t(qs + tok) * p.q_heads + size_t(kvh) * G + head;
         float* orow = p.out + orow_idx * D;
+        uint4* orow_bf16 = reinterpret_cast<uint4*>(
+            reinterpret_cast<__nv_bfloat16*>(p.out) + orow_idx * D);
         if (p.lse && valid_row) p.lse[orow_idx] = m_used + __log2f(lsum);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tmem_ld32(lane_base + o_col + c * 32, o);
           tmem_wait_ld();
-          if (valid_row) {
+          if (valid_row && p.out_bf16) {  // the same products, rounded to bf16
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
+              orow_bf16[(c * 32 + i) / 8] = make_uint4(
+                  pack_bf16x2(o[i] * inv, o[i + 1] * inv), pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
+                  pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv), pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
+          } else if (valid_row) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               *reinterpret_cast<float4*>(orow + c * 32 + i) =
@@ -910,6 +919,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.work_counter = a.max_ctas > 0 ? a.work_counter : nullptr;
   prm.num_items = 0;        // set by the persistent launch
   prm.tiles_per_pair = 0;
+  prm.out_bf16 = a.out_bf16 ? 1 : 0;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
     if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);

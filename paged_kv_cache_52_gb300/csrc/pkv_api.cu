@@ -229,7 +229,7 @@ int check_prefill(const void* q, const int32_t* q_start, int num_seqs, int total
                   int q_heads, const void* k_cache, const void* v_cache,
                   const pkv_cache_desc& cache, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, float scale,
-                  const float* out) {
+                  const void* out) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || q_heads <= 0) return PKV_EINVAL;
@@ -254,9 +254,9 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
                 int q_heads, const void* k_cache, const void* v_cache,
                 const pkv_cache_desc& cache, const int32_t* block_tables,
                 int max_blocks_per_seq, const int32_t* context_lens, int causal,
-                float scale_log2, float out_scale, float* out, cudaStream_t stream,
+                float scale_log2, float out_scale, void* out, cudaStream_t stream,
                 bool f16_pv = false, const int32_t* v_tables = nullptr, int v_num_blocks = 0,
-                int max_ctas = 0, int* work_counter = nullptr) {
+                int max_ctas = 0, int* work_counter = nullptr, bool out_bf16 = false) {
   const int group = q_heads / cache.kv_heads;
   const int rows = pkv::prefill_rows_per_tile();
   pkv_cache_desc vdesc = cache;
@@ -269,7 +269,8 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
   a.q_start = q_start;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.out = out;
+  a.out = static_cast<float*>(out);
+  a.out_bf16 = out_bf16;
   a.num_seqs = num_seqs;
   a.total_q = total_q;
   a.max_q_len = max_q_len;
@@ -445,12 +446,14 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d
   return plan.ws_bytes;
 }
 
-int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
-                                  const void* v_cache, pkv_cache_desc cache,
-                                  const int32_t* block_tables, int max_blocks_per_seq,
-                                  const int32_t* context_lens, int max_context_len, float scale,
-                                  float* out, void* workspace, size_t ws_bytes,
-                                  int partition_blocks, pkv_stream_t stream) {
+namespace {
+
+// The bf16-pool decode with a float32 (or, out_bf16, a bf16) output.
+int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                     const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                     float scale, void* out, bool out_bf16, void* workspace, size_t ws_bytes,
+                     int partition_blocks, pkv_stream_t stream) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   Plan plan;
@@ -462,7 +465,8 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   if (max_blocks_per_seq <= 0) return PKV_EINVAL;
   if (!std::isfinite(scale)) return PKV_EINVAL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      !aligned(out, out_bf16 ? 2 : 4))
     return PKV_EINVAL;
   if (plan.ws_bytes > 0) {
     if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
@@ -475,7 +479,8 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.out = out;
+  a.out = static_cast<float*>(out);
+  a.out_bf16 = out_bf16;
   a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
   a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                         plan.lse_offset)
@@ -492,6 +497,31 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   a.out_scale = 1.f;
   cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                                  const void* v_cache, pkv_cache_desc cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int max_context_len, float scale,
+                                  float* out, void* workspace, size_t ws_bytes,
+                                  int partition_blocks, pkv_stream_t stream) {
+  return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
+                          workspace, ws_bytes, partition_blocks, stream);
+}
+
+int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_cache_desc cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float scale, void* out,
+                                       void* workspace, size_t ws_bytes, int partition_blocks,
+                                       pkv_stream_t stream) {
+  return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, true,
+                          workspace, ws_bytes, partition_blocks, stream);
 }
 
 int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
@@ -653,8 +683,9 @@ namespace {
 int prefill_f16pv(const void* q, const int32_t* q_start, int num_seqs, int total_q,
                   int max_q_len, int q_heads, const void* k_cache, const void* v_cache,
                   pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
-                  const int32_t* context_lens, int causal, float scale, float* out,
-                  void* workspace, size_t ws_bytes, int max_ctas, pkv_stream_t stream) {
+                  const int32_t* context_lens, int causal, float scale, void* out,
+                  void* workspace, size_t ws_bytes, int max_ctas, pkv_stream_t stream,
+                  bool out_bf16 = false) {
   int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
                          cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
   if (st != PKV_OK || num_seqs == 0 || total_q == 0 || max_q_len == 0) return st;
@@ -676,7 +707,7 @@ int prefill_f16pv(const void* q, const int32_t* q_start, int num_seqs, int total
                      block_tables, max_blocks_per_seq, context_lens, causal,
                      scale * 1.4426950408889634f, 1.f, out, cs, /*f16_pv=*/true, vtab,
                      num_seqs * max_blocks_per_seq, max_ctas,
-                     reinterpret_cast<int*>(ws + (w.counter_off - w.v_off)));
+                     reinterpret_cast<int*>(ws + (w.counter_off - w.v_off)), out_bf16);
 }
 
 }  // namespace
@@ -710,6 +741,26 @@ int pkv_paged_prefill_attention_limited(const void* q, const int32_t* q_start, i
   return prefill_f16pv(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
                        cache, block_tables, max_blocks_per_seq, context_lens, causal, scale, out,
                        workspace, ws_bytes, max_ctas, stream);
+}
+
+int pkv_paged_prefill_attention_bf16out(const void* q, const int32_t* q_start, int num_seqs,
+                                       int total_q, int max_q_len, int q_heads,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_cache_desc cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int causal, float scale, void* out, void* workspace,
+                                       size_t ws_bytes, pkv_stream_t stream) {
+  if (workspace)
+    return prefill_f16pv(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                         cache, block_tables, max_blocks_per_seq, context_lens, causal, scale,
+                         out, workspace, ws_bytes, 0, stream, /*out_bf16=*/true);
+  int st = check_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache,
+                         cache, block_tables, max_blocks_per_seq, context_lens, scale, out);
+  if (st != PKV_OK || num_seqs == 0 || total_q == 0 || max_q_len == 0) return st;
+  return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, v_cache, cache,
+                     block_tables, max_blocks_per_seq, context_lens, causal,
+                     scale * 1.4426950408889634f, 1.f, out, static_cast<cudaStream_t>(stream),
+                     false, nullptr, 0, 0, nullptr, /*out_bf16=*/true);
 }
 
 size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_heads, int d_head,

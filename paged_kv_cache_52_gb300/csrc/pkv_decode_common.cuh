@@ -27,7 +27,17 @@ struct DecodeParams {
   int force_partials;
   const float* extra_o;    // [S][q_heads][d] normalised output of the extra part, or null
   const float* extra_lse;  // [S][q_heads] its log2-sum-exp
+  // nonzero: out holds bf16 (the fp32 result rounded to nearest even)
+  int out_bf16 = 0;
 };
+
+// Store element i of the final output in the caller's precision.
+__device__ __forceinline__ void store_out(const DecodeParams& p, size_t i, float v) {
+  if (p.out_bf16)
+    reinterpret_cast<__nv_bfloat16*>(p.out)[i] = __float2bfloat16_rn(v);
+  else
+    p.out[i] = v;
+}
 
 // The blocks of a sequence the kernels attend over: [first, first + count),
 // after clamping to what the block table and the split plan cover, and the

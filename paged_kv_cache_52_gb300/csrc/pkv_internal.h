@@ -57,6 +57,7 @@ struct DecodeArgs {
   int force_partials = 0;
   const float* extra_o = nullptr;
   const float* extra_lse = nullptr;
+  bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
@@ -102,6 +103,7 @@ struct PrefillArgs {
   // work_counter (one int of device memory, zeroed by the launch)
   int max_ctas = 0;
   int* work_counter = nullptr;
+  bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
 };
 
 // Query rows (tokens x heads of a GQA group) per prefill tile.

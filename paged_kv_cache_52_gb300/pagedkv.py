@@ -69,6 +69,13 @@ SIGNATURES = {
     "pkv_paged_decode_attention_ex": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
                                        ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                        ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_paged_decode_attention_bf16out": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
+                                            _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp,
+                                            _sz, ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_paged_prefill_attention_bf16out": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, _vp, _vp, CacheDesc, _vp,
+                                             ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
+                                             _vp], ctypes.c_int),
     "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
     "pkv_paged_prefill_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
@@ -264,6 +271,13 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     return out
 
 
+def _out_dtype(out: Optional[torch.Tensor], out_dtype: Optional[torch.dtype]) -> torch.dtype:
+    odt = out_dtype if out_dtype is not None else (out.dtype if out is not None
+                                                    else torch.float32)
+    _need(odt in (torch.float32, torch.bfloat16), "out_dtype must be float32 or bfloat16")
+    return odt
+
+
 def decode_plan(num_seqs: int, q_heads: int, kv_heads: int, d_head: int, max_context_len: int,
                 partition_blocks: int = 0):
     """(partition_blocks, num_parts, workspace_bytes) the decode will use."""
@@ -290,11 +304,15 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            out: Optional[torch.Tensor] = None,
                            max_context_len: Optional[int] = None,
                            workspace: Optional[torch.Tensor] = None,
-                           partition_blocks: int = 0) -> torch.Tensor:
+                           partition_blocks: int = 0,
+                           out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
     """Decode attention: ``q [S, Hq, d]`` over each sequence's paged history.
 
-    Returns ``out [S, Hq, d]`` float32.  ``max_context_len`` (host int) plans
-    the split; when omitted it is read from ``context_lens`` (a device sync).
+    Returns ``out [S, Hq, d]``, float32 unless ``out_dtype`` (or a given
+    ``out``) is bfloat16: then the float32 result rounded to bf16 in the
+    kernel's store (``pkv_paged_decode_attention_bf16out``).
+    ``max_context_len`` (host int) plans the split; when omitted it is read
+    from ``context_lens`` (a device sync).
     """
     _check_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
@@ -308,14 +326,22 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
           context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if S else 0
+    odt = _out_dtype(out, out_dtype)
     if out is None:
-        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
-    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, hq, d),
-          "out must be contiguous float32 [S, Hq, d]")
+        out = torch.empty(S, hq, d, dtype=odt, device=q.device)
+    _need(out.dtype == odt and out.is_contiguous() and out.shape == (S, hq, d),
+          "out must be contiguous float32 or bfloat16 [S, Hq, d]")
     hkv = k_cache.shape[2]
     if workspace is None:
         workspace = decode_workspace(S, hq, hkv, d, max_context_len, q.device, partition_blocks)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if odt == torch.bfloat16:
+        st = lib.pkv_paged_decode_attention_bf16out(
+            _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+            float(scale), _ptr(out), _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
+        _check("pkv_paged_decode_attention_bf16out", st)
+        return out
     st = lib.pkv_paged_decode_attention_ex(
         _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
@@ -340,10 +366,13 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
                             out: Optional[torch.Tensor] = None,
                             max_q_len: Optional[int] = None,
                             workspace: Optional[torch.Tensor] = None,
-                            max_ctas: Optional[int] = None) -> torch.Tensor:
+                            max_ctas: Optional[int] = None,
+                            out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
     """Chunked prefill: rows ``q_start[s]:q_start[s+1]`` of ``q [total, Hq, d]``
     are the last tokens of sequence s (already appended).  Returns ``out``
-    float32 ``[total, Hq, d]``.  ``max_q_len`` (host int) sizes the grid; when
+    ``[total, Hq, d]``, float32 unless ``out_dtype`` (or a given ``out``) is
+    bfloat16: then the float32 result rounded to bf16 in the kernel's store
+    (``pkv_paged_prefill_attention_bf16out``; not with ``max_ctas``).  ``max_q_len`` (host int) sizes the grid; when
     omitted it is read from ``q_start`` (a device sync).  With a ``workspace``
     (see ``prefill_workspace``) the V pages are converted to f16 first and the
     faster single-product P V kernel runs.  ``max_ctas`` (needs the workspace)
@@ -363,11 +392,24 @@ def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: tor
           "context_lens must be contiguous int32 [S]")
     if max_q_len is None:
         max_q_len = int((q_start[1:] - q_start[:-1]).max().item()) if S else 0
+    odt = _out_dtype(out, out_dtype)
     if out is None:
-        out = torch.empty(total, hq, d, dtype=torch.float32, device=q.device)
-    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (total, hq, d),
-          "out must be contiguous float32 [total, Hq, d]")
+        out = torch.empty(total, hq, d, dtype=odt, device=q.device)
+    _need(out.dtype == odt and out.is_contiguous() and out.shape == (total, hq, d),
+          "out must be contiguous float32 or bfloat16 [total, Hq, d]")
     _need(max_ctas is None or workspace is not None, "max_ctas needs a workspace")
+    _need(max_ctas is None or odt == torch.float32, "max_ctas writes float32 only")
+    if workspace is not None:
+        _need(workspace.dtype == torch.uint8 and workspace.is_cuda and workspace.is_contiguous(),
+              "workspace must be a contiguous uint8 CUDA tensor")
+    if odt == torch.bfloat16:
+        st = lib.pkv_paged_prefill_attention_bf16out(
+            _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),
+            cache_desc(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(bool(causal)), float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() if workspace is not None else 0, _stream(q))
+        _check("pkv_paged_prefill_attention_bf16out", st)
+        return out
     if workspace is None:
         st = lib.pkv_paged_prefill_attention(
             _ptr(q), _ptr(q_start), S, total, int(max_q_len), hq, _ptr(k_cache), _ptr(v_cache),

@@ -194,3 +194,32 @@ def test_prefill_workspace_host_validation(pk):
     assert limited(ws=ctypes.c_void_p((1 << 20) + 64)) == -1
     assert limited(desc=_desc(pk, d=96)) == -2
     assert limited(S=0) == 0                              # nothing to do
+
+
+def test_bf16_out_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    half_aligned = ctypes.c_void_p((1 << 20) + 2)      # 2-byte aligned, not 4
+    dec = lambda fn, S=4, out=dummy, pb=4: fn(  # noqa: E731
+        dummy, S, 8, dummy, dummy, _desc(pk), dummy, 16, dummy, 250, 0.125, out, null, 0, pb, null)
+    bf = lib.pkv_paged_decode_attention_bf16out
+    assert dec(bf, S=0) == 0                                # nothing to do
+    assert dec(bf, out=null) == -1
+    assert dec(bf, out=ctypes.c_void_p((1 << 20) + 1)) == -1  # a bf16 output needs 2 bytes
+    # 2-byte alignment passes for bf16 (the split plan then wants a workspace),
+    # while the float32 entry point rejects the same pointer
+    assert dec(bf, out=half_aligned) == -4
+    assert dec(lib.pkv_paged_decode_attention_ex, out=half_aligned) == -1
+
+    d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
+    need = lib.pkv_paged_prefill_workspace_bytes(4, 8, 2, 128)
+
+    def pre(ws=dummy, wsb=need, desc=d128, out=dummy, S=4):
+        return lib.pkv_paged_prefill_attention_bf16out(dummy, dummy, S, 40, 16, 8, dummy, dummy,
+                                                       desc, dummy, 8, dummy, 1, 0.1, out, ws,
+                                                       wsb, null)
+    assert pre(S=0) == 0 and pre(ws=null, S=0) == 0
+    assert pre(out=ctypes.c_void_p((1 << 20) + 8)) == -1   # rows are stored 16 bytes at a time
+    assert pre(out=ctypes.c_void_p((1 << 20) + 8), ws=null) == -1
+    assert pre(wsb=need - 1) == -4
+    assert pre(desc=_desc(pk, d=96)) == -2 and pre(desc=_desc(pk, d=96), ws=null) == -2
