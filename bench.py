@@ -226,7 +226,7 @@ def read_traffic(kernel_tag: str):
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("paged_decode.cu", "pkv_device.cuh"):
+    for f in ("paged_decode.cu", "pkv_device.cuh", "pkv_decode_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_52_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     sha = h.hexdigest()
