@@ -236,7 +236,10 @@ PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, i
  * less tensor-core work for one bf16 read and one f16 write per V element of
  * those pages.  The conversion is exact for |v| in [2^-14, 65504]; smaller
  * values become f16 subnormals (absolute error < 2^-25); a value of
- * magnitude 65520 or more overflows and sets PKV_DEVERR_FP16_RANGE.
+ * magnitude 65520 or more overflows and sets PKV_DEVERR_FP16_RANGE.  The
+ * same pass ranks the sequences by context length, and the prefill runs
+ * each sequence's tiles together, longest context first (a dispatch order
+ * only: the result does not depend on it).
  * workspace: >= pkv_paged_prefill_workspace_bytes(num_seqs,
  * max_blocks_per_seq, kv_heads, d_head) device bytes, 256-byte aligned
  * (PKV_ENOMEM if smaller); NULL runs pkv_paged_prefill_attention.
@@ -262,8 +265,8 @@ PKV_API int pkv_paged_prefill_attention_ex(const void* q, const int32_t* q_start
  * remaining SMs at the same time instead of after it.
  * Same result as pkv_paged_prefill_attention_ex (bit for bit: the same
  * tiles in the same arithmetic); max_ctas persistent CTAs take the
- * (sequence x KV head, query tile) items longest first from a counter in
- * the workspace.  max_ctas >= 1 (PKV_EINVAL otherwise); a workspace of
+ * (sequence x KV head, query tile) items from a counter in the workspace,
+ * in the dispatch order of pkv_paged_prefill_attention_ex.  max_ctas >= 1 (PKV_EINVAL otherwise); a workspace of
  * pkv_paged_prefill_workspace_bytes(...) bytes is required (PKV_ENOMEM if
  * NULL or smaller).  Calls that share a workspace must not overlap.
  */

@@ -259,12 +259,33 @@ __device__ __forceinline__ uint4 widen8(uint32_t a, uint32_t b) {
                     e4m3x2_to_bf16x2(uint16_t(b & 0xffffu)), e4m3x2_to_bf16x2(uint16_t(b >> 16)));
 }
 
+// order[r] = the sequence of rank r when sequences are sorted by context
+// length, longest first, ties by index.  Every sequence's rank is the number
+// of sequences before it in that order, so the ranks are a permutation of
+// 0 .. num_seqs-1 whatever the lengths; the grid shares the num_seqs^2
+// comparisons.
+__device__ __forceinline__ void rank_by_length(const int32_t* __restrict__ lens, int num_seqs,
+                                               int32_t* __restrict__ order) {
+  const int stride = int(gridDim.x) * int(blockDim.x);
+  for (int s = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x); s < num_seqs; s += stride) {
+    const int key = __ldg(lens + s);
+    int rank = 0;
+    for (int t = 0; t < num_seqs; ++t) {
+      const int other = __ldg(lens + t);
+      rank += (other > key) || (other == key && t < s);
+    }
+    order[rank] = s;
+  }
+}
+
 __global__ void __launch_bounds__(kAppendThreads)
 widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v8,
                        const int32_t* __restrict__ tables, const int32_t* __restrict__ lens,
                        int num_seqs, int max_blocks, int num_blocks, int page_vec16,
                        uint4* __restrict__ kdst, uint4* __restrict__ vdst,
-                       int32_t* __restrict__ table_out, bool v_f16) {
+                       int32_t* __restrict__ table_out, bool v_f16,
+                       int32_t* __restrict__ seq_order) {
+  if (seq_order) rank_by_length(lens, num_seqs, seq_order);
   const int64_t items = int64_t(num_seqs) * max_blocks;
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int s = int(item / max_blocks), j = int(item - int64_t(s) * max_blocks);
@@ -292,15 +313,15 @@ widen_fp8_pages_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v
 cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
                                    const int32_t* lens, int num_seqs, int max_blocks,
                                    int num_blocks, int64_t page_codes, void* kdst, void* vdst,
-                                   int32_t* table_out, bool v_f16, cudaStream_t stream,
-                                   int num_sms) {
+                                   int32_t* table_out, bool v_f16, int32_t* seq_order,
+                                   cudaStream_t stream, int num_sms) {
   const int64_t items = int64_t(num_seqs) * max_blocks;
   const int64_t max_grid = int64_t(num_sms) * 8;
   const int grid = int(items < max_grid ? items : max_grid);
   widen_fp8_pages_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k8), static_cast<const uint4*>(v8), tables, lens, num_seqs,
       max_blocks, num_blocks, int(page_codes / 16), static_cast<uint4*>(kdst),
-      static_cast<uint4*>(vdst), table_out, v_f16);
+      static_cast<uint4*>(vdst), table_out, v_f16, seq_order);
   return cudaGetLastError();
 }
 
@@ -316,7 +337,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 v_pages_to_f16_kernel(const uint4* __restrict__ v, const int32_t* __restrict__ tables,
                       const int32_t* __restrict__ lens, int num_seqs, int max_blocks,
                       int num_blocks, int page_vec, uint4* __restrict__ vdst,
-                      int32_t* __restrict__ table_out) {
+                      int32_t* __restrict__ table_out, int32_t* __restrict__ seq_order) {
+  if (seq_order) rank_by_length(lens, num_seqs, seq_order);
   const int64_t items = int64_t(num_seqs) * max_blocks;
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int s = int(item / max_blocks), j = int(item - int64_t(s) * max_blocks);
@@ -347,14 +369,14 @@ v_pages_to_f16_kernel(const uint4* __restrict__ v, const int32_t* __restrict__ t
 
 cudaError_t launch_v_pages_to_f16(const void* v, const int32_t* tables, const int32_t* lens,
                                   int num_seqs, int max_blocks, int num_blocks, int64_t page_elems,
-                                  void* vdst, int32_t* table_out, cudaStream_t stream,
-                                  int num_sms) {
+                                  void* vdst, int32_t* table_out, int32_t* seq_order,
+                                  cudaStream_t stream, int num_sms) {
   const int64_t items = int64_t(num_seqs) * max_blocks;
   const int64_t max_grid = int64_t(num_sms) * 8;
   const int grid = int(items < max_grid ? items : max_grid);
   v_pages_to_f16_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(v), tables, lens, num_seqs, max_blocks, num_blocks,
-      int(page_elems / 8), static_cast<uint4*>(vdst), table_out);
+      int(page_elems / 8), static_cast<uint4*>(vdst), table_out, seq_order);
   return cudaGetLastError();
 }
 

@@ -15,8 +15,10 @@
 //  * one CTA per (two 128-row query tiles, sequence x KV head).  The 128 rows
 //    of a tile are 128/G query tokens x the G heads of the GQA group (rows
 //    token-major), so one TMA box brings a tile in and every K/V tile serves
-//    all G heads of both tiles.  CTAs are dispatched longest-first across all
-//    sequences (the last tiles of a chunk see the most keys).
+//    all G heads of both tiles.  CTAs are dispatched pair-major: a pair's
+//    tiles back to back, longest first (the last tiles of a chunk see the
+//    most keys), pairs by context length when an order is given, so the
+//    CTAs running together share few pairs' K/V in L2.
 //  * warp roles: warps 0-3 and 4-7 are the softmax / correction / epilogue
 //    warpgroups of Q tiles 0 and 1 (thread = row = TMEM lane), warp 9 the MMA
 //    issuer (one thread), warps 8 and 10 the TMA producers of Q + the K ring
@@ -119,6 +121,7 @@ struct PrefillParams {
   int num_items;                // pairs * tiles_per_pair
   int tiles_per_pair;           // CTA-sized query tiles of the longest chunk
   int out_bf16;                 // nonzero: out holds bf16, rounded to nearest even
+  const int32_t* seq_order;     // [num_seqs] dispatch order of the sequences, or null
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -783,6 +786,26 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
   tc_fence_after();
 }
 
+// Item `idx` of a launch (pairs x tiles items) -> its pair and query tile.
+// Pair-major: a pair's tiles run back to back, longest first, so the CTAs
+// resident at any time share the K/V of few pairs in L2 instead of touching
+// every pair's pages at once; pairs go in seq_order (longest context first,
+// which keeps the grid close to longest-first overall) when it is given.
+// Returns false for an order entry outside the batch (the item is skipped).
+__device__ __forceinline__ bool item_pair_tile(const PrefillParams& p, long long idx, int tiles,
+                                               int& pair, int& tile) {
+  const int pr = int(idx / tiles);
+  tile = tiles - 1 - int(idx - (long long)pr * tiles);
+  if (!p.seq_order) {
+    pair = pr;
+    return true;
+  }
+  const int rank = pr / p.kv_heads;
+  const int seq = __ldg(p.seq_order + rank);
+  pair = seq * p.kv_heads + (pr - rank * p.kv_heads);
+  return seq >= 0 && seq < p.num_seqs;
+}
+
 template <int D, int G, bool F16PV, bool PERSIST>
 __global__ void __launch_bounds__(kPfThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -808,15 +831,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const uint32_t tmem = *tmem_slot;
 
   if constexpr (!PERSIST) {
-    // grid (pairs, tiles): CTAs are dispatched x-fastest, so every pair's
-    // longest tile goes first, then every pair's next-longest, ... (a
-    // longest-first order the hardware scheduler balances dynamically)
-    prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, int(blockIdx.x),
-                              int(gridDim.y) - 1 - int(blockIdx.y));
+    // grid (pairs, tiles), dispatched in linear block order
+    int pair, tile;
+    const long long idx = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+    if (item_pair_tile(p, idx, int(gridDim.y), pair, tile))
+      prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, pair, tile);
+    else if (threadIdx.x == 0)
+      atomicOr(&g_prefill_error, kErrBadQueryRange);
   } else {
     // persistent: the same order, taken one item at a time from the counter,
     // so the launch occupies at most gridDim.x SMs
-    const int pairs = p.num_seqs * p.kv_heads;
     for (;;) {
       if (threadIdx.x == 0) *item_slot = atomicAdd(p.work_counter, 1);
       __syncthreads();
@@ -824,9 +848,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const bool stop = item >= p.num_items || *abort_flag;
       __syncthreads();  // every thread has read the slot before it is written again
       if (stop) break;
-      const int rank = item / pairs;
-      prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, item - rank * pairs,
-                                p.tiles_per_pair - 1 - rank);
+      int pair, tile;
+      if (item_pair_tile(p, item, p.tiles_per_pair, pair, tile))
+        prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, pair, tile);
+      else if (threadIdx.x == 0)
+        atomicOr(&g_prefill_error, kErrBadQueryRange);
     }
   }
 
@@ -920,6 +946,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.num_items = 0;        // set by the persistent launch
   prm.tiles_per_pair = 0;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
+  prm.seq_order = a.seq_order;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
     if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);

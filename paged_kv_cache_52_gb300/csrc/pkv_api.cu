@@ -256,7 +256,8 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
                 int max_blocks_per_seq, const int32_t* context_lens, int causal,
                 float scale_log2, float out_scale, void* out, cudaStream_t stream,
                 bool f16_pv = false, const int32_t* v_tables = nullptr, int v_num_blocks = 0,
-                int max_ctas = 0, int* work_counter = nullptr, bool out_bf16 = false) {
+                int max_ctas = 0, int* work_counter = nullptr, bool out_bf16 = false,
+                const int32_t* seq_order = nullptr) {
   const int group = q_heads / cache.kv_heads;
   const int rows = pkv::prefill_rows_per_tile();
   pkv_cache_desc vdesc = cache;
@@ -287,16 +288,17 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
   a.v_num_blocks = v_num_blocks;
   a.max_ctas = max_ctas;
   a.work_counter = work_counter;
+  a.seq_order = seq_order;
   cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 // Workspace of the FP8 prefill: bf16 K and V scratch pools of
-// num_seqs * max_blocks pages, then the scratch block table (counter_off
-// bytes in all).  The bf16 prefill's workspace is the same from v_off on,
-// plus the work counter of the persistent launch.
+// num_seqs * max_blocks pages, the scratch block table, the work counter of
+// the persistent launch and the sequences' dispatch order (written by the
+// page pass).  The bf16 prefill's workspace is the same from v_off on.
 struct Fp8PrefillLayout {
-  size_t k_off = 0, v_off = 0, table_off = 0, counter_off = 0, total = 0;
+  size_t k_off = 0, v_off = 0, table_off = 0, counter_off = 0, order_off = 0, total = 0;
 };
 
 bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
@@ -310,7 +312,8 @@ bool fp8_prefill_layout(int num_seqs, int max_blocks, int kv_heads, int d_head,
   w->v_off = up(pool);
   w->table_off = w->v_off + up(pool);
   w->counter_off = w->table_off + up(size_t(pages) * 4);
-  w->total = w->counter_off + 256;
+  w->order_off = w->counter_off + 256;
+  w->total = w->order_off + up(size_t(num_seqs) * 4);
   return true;
 }
 
@@ -632,7 +635,8 @@ int prefill_fp8(const void* q, const int32_t* q_start, int num_seqs, int total_q
   cudaError_t e = pkv::launch_widen_fp8_pages(
       k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
       cache.num_blocks, int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws + w.k_off,
-      ws + w.v_off, reinterpret_cast<int32_t*>(ws + w.table_off), /*v_f16=*/true, cs, sms);
+      ws + w.v_off, reinterpret_cast<int32_t*>(ws + w.table_off), /*v_f16=*/true,
+      reinterpret_cast<int32_t*>(ws + w.order_off), cs, sms);
   if (e != cudaSuccess) return PKV_ECUDA;
   pkv_cache_desc scratch = cache;
   scratch.num_blocks = num_seqs * max_blocks_per_seq;
@@ -640,7 +644,8 @@ int prefill_fp8(const void* q, const int32_t* q_start, int num_seqs, int total_q
                      ws + w.v_off, scratch, reinterpret_cast<const int32_t*>(ws + w.table_off),
                      max_blocks_per_seq, context_lens, causal,
                      scale * k_scale * 1.4426950408889634f, v_scale, out, cs, /*f16_pv=*/true,
-                     nullptr, 0, max_ctas, reinterpret_cast<int*>(ws + w.counter_off));
+                     nullptr, 0, max_ctas, reinterpret_cast<int*>(ws + w.counter_off), false,
+                     reinterpret_cast<const int32_t*>(ws + w.order_off));
 }
 
 }  // namespace
@@ -698,16 +703,17 @@ int prefill_f16pv(const void* q, const int32_t* q_start, int num_seqs, int total
   if (sms <= 0) return PKV_ECUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* vtab = reinterpret_cast<int32_t*>(ws + (w.table_off - w.v_off));
+  int32_t* order = reinterpret_cast<int32_t*>(ws + (w.order_off - w.v_off));
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = pkv::launch_v_pages_to_f16(
       v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq, cache.num_blocks,
-      int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws, vtab, cs, sms);
+      int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws, vtab, order, cs, sms);
   if (e != cudaSuccess) return PKV_ECUDA;
   return run_prefill(q, q_start, num_seqs, total_q, max_q_len, q_heads, k_cache, ws, cache,
                      block_tables, max_blocks_per_seq, context_lens, causal,
                      scale * 1.4426950408889634f, 1.f, out, cs, /*f16_pv=*/true, vtab,
                      num_seqs * max_blocks_per_seq, max_ctas,
-                     reinterpret_cast<int*>(ws + (w.counter_off - w.v_off)), out_bf16);
+                     reinterpret_cast<int*>(ws + (w.counter_off - w.v_off)), out_bf16, order);
 }
 
 }  // namespace

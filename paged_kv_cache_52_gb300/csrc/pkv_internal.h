@@ -21,18 +21,20 @@ cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v,
                                  void* v_cache, int64_t num_slots, int row_elems, float k_inv,
                                  float v_inv, cudaStream_t stream, int num_sms);
 // FP8 pages of each sequence's context -> bf16 scratch pool + scratch table
-// (page_codes = 16 * kv_heads * d_head, a multiple of 16).
+// (page_codes = 16 * kv_heads * d_head, a multiple of 16).  seq_order
+// (optional, [num_seqs]): the sequences by context length, longest first,
+// ties by index -- the prefill's dispatch order.
 cudaError_t launch_widen_fp8_pages(const void* k8, const void* v8, const int32_t* tables,
                                    const int32_t* lens, int num_seqs, int max_blocks,
                                    int num_blocks, int64_t page_codes, void* kdst, void* vdst,
-                                   int32_t* table_out, bool v_f16, cudaStream_t stream,
-                                   int num_sms);
+                                   int32_t* table_out, bool v_f16, int32_t* seq_order,
+                                   cudaStream_t stream, int num_sms);
 // bf16 V pages of each sequence's context -> f16 scratch pool + scratch table
-// (page_elems = 16 * kv_heads * d_head, a multiple of 8).
+// (page_elems = 16 * kv_heads * d_head, a multiple of 8); seq_order as above.
 cudaError_t launch_v_pages_to_f16(const void* v, const int32_t* tables, const int32_t* lens,
                                   int num_seqs, int max_blocks, int num_blocks, int64_t page_elems,
-                                  void* vdst, int32_t* table_out, cudaStream_t stream,
-                                  int num_sms);
+                                  void* vdst, int32_t* table_out, int32_t* seq_order,
+                                  cudaStream_t stream, int num_sms);
 // Copy-on-write block copies: block_bytes a multiple of 16.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int64_t block_bytes, cudaStream_t stream,
@@ -104,6 +106,9 @@ struct PrefillArgs {
   int max_ctas = 0;
   int* work_counter = nullptr;
   bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
+  // optional [num_seqs]: sequences in dispatch order (longest context first);
+  // null: index order
+  const int32_t* seq_order = nullptr;
 };
 
 // Query rows (tokens x heads of a GQA group) per prefill tile.

@@ -147,7 +147,10 @@ def test_fp8_prefill_host_validation(pk):
     need = lib.pkv_paged_prefill_attention_fp8_workspace_bytes(4, 8, 2, 128)
     pool = 4 * 8 * 16 * 2 * 128 * 2                     # bf16 pages of 4 x 8 blocks
     # K, V scratch pools + the table + the persistent launch's work counter
-    assert need == 2 * pool + 256 + 256
+    # + the sequences' dispatch order (4 int32, rounded up to 256 bytes)
+    assert need == 2 * pool + 256 + 256 + 256
+    assert lib.pkv_paged_prefill_attention_fp8_workspace_bytes(100, 8, 2, 128) == \
+        2 * 25 * pool + 3328 + 256 + 512   # table of 800 int32 and order of 100, 256-aligned
     assert lib.pkv_paged_prefill_attention_fp8_workspace_bytes(0, 8, 2, 128) == 0
 
     def call(desc=d128, k_scale=1.0, v_scale=1.0, ws=dummy, wsb=need, S=4):
@@ -174,7 +177,8 @@ def test_prefill_workspace_host_validation(pk):
     dummy = ctypes.c_void_p(1 << 20)
     need = lib.pkv_paged_prefill_workspace_bytes(4, 8, 2, 128)
     # f16 V pages of 4 x 8 blocks + table + the persistent launch's work counter
-    assert need == 4 * 8 * 16 * 2 * 128 * 2 + 256 + 256
+    # + the dispatch order
+    assert need == 4 * 8 * 16 * 2 * 128 * 2 + 256 + 256 + 256
     assert lib.pkv_paged_prefill_workspace_bytes(4, 0, 2, 128) == 0
     d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
 

@@ -184,3 +184,28 @@ def test_fp8_prefill_limited_sms_equals_grid(pk):
     ref, _ = _fp8_oracle(w, kc8, vc8, ks, vs, True, range(4))
     assert_attention_close(grid.cpu().numpy(), ref, "fp8 prefill (grid and limited)")
     assert pk.get_device_error(clear=True) == 0
+
+
+def test_fp8_prefill_dispatch_order_many_sequences(pk):
+    # the widening pass ranks the sequences (more than a warp of them, with
+    # ties and empty chunks) and the prefill runs them in that order; every
+    # row is computed, grid and persistent launches agree bitwise
+    g = np.random.default_rng(14)
+    priors = [int(x) for x in g.integers(1, 300, 70)]
+    chunks = [int(x) for x in g.integers(1, 40, 70)]
+    for s in (3, 4):
+        priors[s], chunks[s] = 64, 16
+    chunks[20] = 0
+    w = _dev(wl.make_chunked_workload(16, 4, 128, priors, chunks, config_id=15))
+    ks, vs = wl.FP8_SCALES["tiny"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    grid, kc, vc = _step(pk, w, kc8, vc8, ks, vs, True, 39)
+    assert bool(torch.isfinite(grid).all())
+    lim = pk.paged_prefill_attention_fp8(w.q_prefill, w.q_start, kc, vc, w.prefill_tables,
+                                         w.prefill_lens, True, w.scale, ks, vs, max_q_len=39,
+                                         max_ctas=23)
+    torch.cuda.synchronize()
+    assert torch.equal(lim, grid)
+    ref, _ = _fp8_oracle(w, kc8, vc8, ks, vs, True, range(70))
+    assert_attention_close(grid.cpu().numpy(), ref, "fp8 prefill, 70 sequences")
+    assert pk.get_device_error(clear=True) == 0

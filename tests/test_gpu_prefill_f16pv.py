@@ -174,3 +174,32 @@ def test_limited_prefill_beside_decode_on_another_stream(pk):
     got = np.stack([p_conc[int(qs[[0, 7][si]]) + i].cpu().numpy() for si, i in picks])
     assert_attention_close(got, pre.rows_output(picks), "limited prefill beside decode")
     assert pk.get_device_error(clear=True) == 0
+
+
+def _many_sequences(seed, n=70):
+    # more sequences than a warp, with tied context lengths and empty chunks
+    g = np.random.default_rng(seed)
+    priors = [int(x) for x in g.integers(1, 300, n)]
+    chunks = [int(x) for x in g.integers(1, 40, n)]
+    for s in (5, 6, 7):                     # three sequences of equal length
+        priors[s], chunks[s] = 100, 20
+    chunks[10] = chunks[11] = 0             # nothing to compute for these
+    return priors, chunks
+
+
+def test_dispatch_order_covers_every_sequence_once(pk):
+    # the page pass ranks the sequences by context length and the prefill
+    # runs them in that order: every sequence is still computed (no output
+    # row left NaN), the result matches the oracle, and the persistent
+    # launch, which takes the same order from its counter, agrees bitwise
+    priors, chunks = _many_sequences(12)
+    w = _to_dev(wl.make_chunked_workload(16, 4, 64, priors, chunks, config_id=13))
+    out, kc, vc = run_f16pv(pk, w)
+    assert bool(torch.isfinite(out).all())
+    for ctas in (1, 37):
+        lim = _limited(pk, w, kc, vc, ctas)
+        torch.cuda.synchronize()
+        assert torch.equal(lim, out), f"max_ctas={ctas}"
+    ref = PrefillStepOracle(w, range(len(chunks))).output()
+    assert_attention_close(out.cpu().numpy(), ref, "70 sequences, dispatch order")
+    assert pk.get_device_error(clear=True) == 0
