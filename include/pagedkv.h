@@ -79,6 +79,7 @@ typedef void* pkv_stream_t;
 #define PKV_DEVERR_BAD_QUERY_RANGE 0x10u /* q_start not monotone or chunk longer than context */
 #define PKV_DEVERR_TMEM_ALLOC 0x20u     /* tensor memory could not be allocated */
 #define PKV_DEVERR_FP16_RANGE 0x40u     /* FP8 decode: a query value is outside f16's range */
+#define PKV_DEVERR_DUPLICATE_SLOT 0x80u /* checked append: a slot named twice; nothing written */
 
 /*
  * pkv_kv_append -- scatter new K/V rows into the paged pools.
@@ -94,7 +95,8 @@ typedef void* pkv_stream_t;
  *                   a fused QKV projection are accepted.  Base pointers and
  *                   strides must be 16-byte aligned (strides are in elements).
  *   slot_mapping  : [num_tokens] int64.  Two tokens with the same slot race
- *                   (the result is one of them).
+ *                   (the result is one of them; pkv_kv_append_checked
+ *                   rejects such a mapping instead).
  *   k_cache, v_cache : pools described by `cache`, written in place.
  * Slots outside [-1, num_blocks*16) are skipped and set
  * PKV_DEVERR_BAD_SLOT.  num_tokens == 0 launches nothing.
@@ -102,6 +104,29 @@ typedef void* pkv_stream_t;
 PKV_API int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_tok_stride,
                   const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                   void* v_cache, pkv_cache_desc cache, pkv_stream_t stream);
+
+/*
+ * pkv_kv_append_checked -- pkv_kv_append that rejects a slot mapping in
+ * which two tokens name the same slot.  The pages' slot mapping gives each
+ * new token its own cache row (nano-vLLM page, section "Ecriture dans le
+ * cache"); two writers of one row would leave it undefined.  A device pass
+ * marks every slot in [0, num_blocks*16) in a bitmap.  If any slot is
+ * marked twice, PKV_DEVERR_DUPLICATE_SLOT is set and the append writes
+ * nothing: the caches are left as they were.  Slots -1 (skip) and slots
+ * outside the pool (skipped, PKV_DEVERR_BAD_SLOT) do not count as repeats.
+ * No host synchronisation: the rejection happens on the stream.
+ *   workspace : >= pkv_kv_append_checked_workspace_bytes(cache) device
+ *               bytes, 256-byte aligned (PKV_ENOMEM if NULL or smaller);
+ *               overwritten by every call, so calls that share it must be
+ *               ordered on the GPU.
+ * Other arguments and errors are those of pkv_kv_append.
+ */
+PKV_API size_t pkv_kv_append_checked_workspace_bytes(pkv_cache_desc cache);
+PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const void* v,
+                                  int64_t v_tok_stride, const int64_t* slot_mapping,
+                                  int64_t num_tokens, void* k_cache, void* v_cache,
+                                  pkv_cache_desc cache, void* workspace, size_t ws_bytes,
+                                  pkv_stream_t stream);
 
 /*
  * Decode plan: the partition size (in 16-token blocks) and the number of

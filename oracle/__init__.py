@@ -15,6 +15,7 @@ from .paged_attention import (  # noqa: F401
     bf16_bits_to_f64,
     f64_to_bf16_bits,
     kv_append,
+    kv_append_checked,
     gather_sequence_kv,
     attention,
     paged_decode_attention,

@@ -135,6 +135,27 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
     return kc, vc
 
 
+def kv_append_checked(k_new, v_new, slot_mapping, k_cache, v_cache):
+    """The append with repeated slots rejected.
+
+    The nano-vLLM page's slot mapping ("Ecriture dans le cache") gives every
+    new token its own cache row; two tokens naming one row would leave that
+    row undefined.  Reading: such a mapping is rejected as a whole.  Returns
+    ``(k_cache, v_cache, rejected)``: unchanged copies and True when a slot
+    other than -1 appears twice, else ``kv_append``'s result and False.
+    """
+    slots = np.asarray(slot_mapping).astype(np.int64)
+    seen = set()
+    for slot in slots.tolist():
+        if slot == -1:
+            continue
+        if slot in seen:
+            return np.array(k_cache, copy=True), np.array(v_cache, copy=True), True
+        seen.add(slot)
+    kc, vc = kv_append(k_new, v_new, slots, k_cache, v_cache)
+    return kc, vc, False
+
+
 # ---------------------------------------------------------------------------
 # Paging: logical position j of a sequence lives in block_table[j // bs], row
 # j % bs (page table of the PagedAttention sections).

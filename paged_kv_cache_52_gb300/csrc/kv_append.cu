@@ -16,11 +16,33 @@ static __device__ unsigned g_append_error = 0;
 constexpr int kAppendThreads = 256;
 constexpr int kAppendVecPerLane = 4;  // 16-byte vectors kept in flight per lane per row
 
+// Checked append, first pass: one bit per slot of the pool (zeroed before).
+// A token whose slot bit was already set shares its slot with an earlier
+// token of the call: the mapping is rejected (*reject = 1), the error word
+// records it, and the append that follows on the stream writes nothing.
+// Slots -1 and outside the pool are left to the append (skipped there).
+__global__ void __launch_bounds__(kAppendThreads)
+slot_duplicates_kernel(const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
+                       int64_t num_slots, unsigned* __restrict__ bitmap, int* __restrict__ reject) {
+  const int64_t stride = int64_t(gridDim.x) * kAppendThreads;
+  for (int64_t t = int64_t(blockIdx.x) * kAppendThreads + threadIdx.x; t < num_tokens;
+       t += stride) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0 || slot >= num_slots) continue;
+    const unsigned bit = 1u << unsigned(slot & 31);
+    if (atomicOr(bitmap + (slot >> 5), bit) & bit) {
+      atomicOr(&g_append_error, kErrDuplicateSlot);
+      atomicExch(reject, 1);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kAppendThreads)
 kv_append_kernel(const uint4* __restrict__ k, int64_t k_stride_vec, const uint4* __restrict__ v,
                  int64_t v_stride_vec, const int64_t* __restrict__ slot_mapping,
                  int64_t num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                 int64_t num_slots, int row_vec) {
+                 int64_t num_slots, int row_vec, const int* __restrict__ reject) {
+  if (reject && *reject) return;  // checked append of a mapping with a repeated slot
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kAppendThreads) >> 5;
@@ -67,10 +89,21 @@ unsigned read_append_error(bool clear) {
   return word;
 }
 
+cudaError_t launch_slot_duplicates(const int64_t* slot_mapping, int64_t num_tokens,
+                                   int64_t num_slots, unsigned* bitmap, int* reject,
+                                   cudaStream_t stream, int num_sms) {
+  const int64_t blocks_needed = (num_tokens + kAppendThreads - 1) / kAppendThreads;
+  const int64_t max_blocks = int64_t(num_sms) * 8;
+  const int grid = int(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+  slot_duplicates_kernel<<<grid, kAppendThreads, 0, stream>>>(slot_mapping, num_tokens,
+                                                              num_slots, bitmap, reject);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
                              const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                              void* v_cache, int64_t num_slots, int row_elems,
-                             cudaStream_t stream, int num_sms) {
+                             cudaStream_t stream, int num_sms, const int* reject) {
   const int row_vec = row_elems / 8;  // 8 bf16 per 16-byte vector
   const int64_t warps_needed = num_tokens;
   const int64_t blocks_needed = (warps_needed * 32 + kAppendThreads - 1) / kAppendThreads;
@@ -79,7 +112,7 @@ cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int
   kv_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k), k_stride / 8, static_cast<const uint4*>(v), v_stride / 8,
       slot_mapping, num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      num_slots, row_vec);
+      num_slots, row_vec, reject);
   return cudaGetLastError();
 }
 

@@ -381,6 +381,48 @@ int pkv_kv_append(const void* k, int64_t k_tok_stride, const void* v, int64_t v_
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+size_t pkv_kv_append_checked_workspace_bytes(pkv_cache_desc cache) {
+  if (check_cache_desc(cache) != PKV_OK) return 0;
+  const int64_t num_slots = int64_t(cache.num_blocks) * cache.block_size;
+  const size_t words = size_t((num_slots + 31) / 32);
+  return 256 + (words * 4 + 255) / 256 * 256;  // reject flag, then the slot bitmap
+}
+
+int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const void* v,
+                          int64_t v_tok_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                          void* k_cache, void* v_cache, pkv_cache_desc cache, void* workspace,
+                          size_t ws_bytes, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
+  const int64_t row = int64_t(cache.kv_heads) * cache.d_head;
+  if (row % 8) return PKV_EUNSUPPORTED;
+  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+    return PKV_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_EINVAL;
+  const size_t need = pkv_kv_append_checked_workspace_bytes(cache);
+  if (!workspace || ws_bytes < need) return PKV_ENOMEM;
+  if (!aligned(workspace, 256)) return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int64_t num_slots = int64_t(cache.num_blocks) * cache.block_size;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* reject = reinterpret_cast<int*>(ws);
+  unsigned* bitmap = reinterpret_cast<unsigned*>(ws + 256);
+  if (cudaMemsetAsync(workspace, 0, need, cs) != cudaSuccess) return PKV_ECUDA;
+  cudaError_t e = pkv::launch_slot_duplicates(slot_mapping, num_tokens, num_slots, bitmap, reject,
+                                              cs, sms);
+  if (e != cudaSuccess) return PKV_ECUDA;
+  e = pkv::launch_kv_append(k, k_tok_stride, v, v_tok_stride, slot_mapping, num_tokens, k_cache,
+                            v_cache, num_slots, int(row), cs, sms, reject);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache, int32_t elem_bytes,
                     const int32_t* pairs, int32_t num_pairs, pkv_stream_t stream) {
   if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.kv_heads <= 0 || cache.d_head <= 0)

@@ -20,6 +20,7 @@ enum : unsigned {
   kErrWaitTimeout = 1u << 3,    // a bounded wait on an mbarrier ran out
   kErrBadQueryRange = 1u << 4,  // q_start not monotone / chunk longer than its context
   kErrTmemAlloc = 1u << 5,      // tensor-memory allocation failed
+  kErrDuplicateSlot = 1u << 7,  // checked append: two tokens name one slot (nothing written)
 };
 
 // A bounded wait gives up after this many polls (each poll of try_wait may

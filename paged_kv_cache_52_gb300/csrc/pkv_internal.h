@@ -10,10 +10,17 @@
 namespace pkv {
 
 // ---- kv_append.cu
+// reject (optional): a device flag set by launch_slot_duplicates; when it is
+// nonzero the append writes nothing.
 cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
                              const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                              void* v_cache, int64_t num_slots, int row_elems,
-                             cudaStream_t stream, int num_sms);
+                             cudaStream_t stream, int num_sms, const int* reject = nullptr);
+// Marks every in-pool slot in `bitmap` (num_slots bits, zeroed by the
+// caller) and sets *reject when a slot repeats.
+cudaError_t launch_slot_duplicates(const int64_t* slot_mapping, int64_t num_tokens,
+                                   int64_t num_slots, unsigned* bitmap, int* reject,
+                                   cudaStream_t stream, int num_sms);
 unsigned read_append_error(bool clear);
 // FP8 (e4m3) pools: row_elems must be a multiple of 16.
 cudaError_t launch_kv_append_fp8(const void* k, int64_t k_stride, const void* v, int64_t v_stride,

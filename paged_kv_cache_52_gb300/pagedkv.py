@@ -28,6 +28,7 @@ DEVERR_BITS = {
     0x10: "bad query range",
     0x20: "tensor memory allocation",
     0x40: "query outside f16 range (fp8 decode)",
+    0x80: "duplicate slot (checked append wrote nothing)",
 }
 
 
@@ -59,6 +60,9 @@ SIGNATURES = {
     "pkv_version": ([], ctypes.c_int),
     "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "pkv_kv_append": ([_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, CacheDesc, _vp], ctypes.c_int),
+    "pkv_kv_append_checked_workspace_bytes": ([CacheDesc], _sz),
+    "pkv_kv_append_checked": ([_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, CacheDesc, _vp, _sz,
+                               _vp], ctypes.c_int),
     "pkv_decode_plan": ([ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(_sz)], ctypes.c_int),
@@ -189,8 +193,13 @@ def _check_cache(k_cache, v_cache):
 
 
 def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
-              k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
-    """Scatter ``k, v [T, kv_heads, d]`` into the pools at ``slot_mapping [T]`` (-1 skips)."""
+              k_cache: torch.Tensor, v_cache: torch.Tensor,
+              checked_workspace: Optional[torch.Tensor] = None) -> None:
+    """Scatter ``k, v [T, kv_heads, d]`` into the pools at ``slot_mapping [T]`` (-1 skips).
+
+    With ``checked_workspace`` (see ``kv_append_checked_workspace``) the call
+    is ``pkv_kv_append_checked``: a mapping that names one slot twice writes
+    nothing and sets the duplicate-slot bit of the device error word."""
     _check_cache(k_cache, v_cache)
     t = slot_mapping.shape[0]
     for x in (k, v):
@@ -202,9 +211,26 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
               "each token row of k, v must be contiguous")
     _need(slot_mapping.is_cuda and slot_mapping.dtype == torch.int64 and
           slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64 on the GPU")
+    if checked_workspace is not None:
+        ws = checked_workspace
+        _need(ws.is_cuda and ws.dtype == torch.uint8 and ws.is_contiguous(),
+              "checked_workspace must be a contiguous uint8 CUDA tensor")
+        st = lib.pkv_kv_append_checked(_ptr(k), k.stride(0), _ptr(v), v.stride(0),
+                                       _ptr(slot_mapping), t, _ptr(k_cache), _ptr(v_cache),
+                                       cache_desc(k_cache), _ptr(ws), ws.numel(),
+                                       _stream(k_cache))
+        _check("pkv_kv_append_checked", st)
+        return
     st = lib.pkv_kv_append(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), t,
                            _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _stream(k_cache))
     _check("pkv_kv_append", st)
+
+
+def kv_append_checked_workspace(k_cache: torch.Tensor) -> torch.Tensor:
+    """Workspace of the checked append for this pool: a flag and one bit per slot."""
+    n = lib.pkv_kv_append_checked_workspace_bytes(cache_desc(k_cache))
+    _need(n > 0, "unsupported cache shape")
+    return torch.empty(n, dtype=torch.uint8, device=k_cache.device)
 
 
 def _check_fp8_cache(k_cache, v_cache):

@@ -227,3 +227,22 @@ def test_bf16_out_host_validation(pk):
     assert pre(out=ctypes.c_void_p((1 << 20) + 8), ws=null) == -1
     assert pre(wsb=need - 1) == -4
     assert pre(desc=_desc(pk, d=96)) == -2 and pre(desc=_desc(pk, d=96), ws=null) == -2
+
+
+def test_checked_append_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    d = _desc(pk, nb=64, bs=16, hkv=2, d=64)             # 1024 slots
+    need = lib.pkv_kv_append_checked_workspace_bytes(d)
+    assert need == 256 + 256                              # flag, then 32 words of bitmap
+    assert lib.pkv_kv_append_checked_workspace_bytes(_desc(pk, nb=1000, bs=16, hkv=2, d=64)) == \
+        256 + 2048                                        # 16,000 slots: 500 words, 256-aligned
+    assert lib.pkv_kv_append_checked_workspace_bytes(_desc(pk, bs=32)) == 0
+
+    def call(ws=dummy, wsb=need, T=4):
+        return lib.pkv_kv_append_checked(dummy, 128, dummy, 128, dummy, T, dummy, dummy, d, ws,
+                                         wsb, null)
+    assert call(T=0) == 0                                 # nothing to do
+    assert call(T=-1) == -1
+    assert call(ws=null) == -4 and call(wsb=need - 1) == -4
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -1  # workspace not 256-byte aligned

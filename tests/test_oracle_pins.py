@@ -95,6 +95,36 @@ def test_append_matches_flat_row_brute_force():
         oracle.kv_append(kn[:1], vn[:1], np.array([nb * bs]), kc, vc)
 
 
+def test_checked_append_rejects_a_repeated_slot():
+    # every token owns its row: a mapping that names one row twice is
+    # rejected whole (caches unchanged); -1 may repeat freely
+    w = wl.make_decode_workload(wl.TINY)
+    kc, vc = wl.bf16_bits(w.k_cache), wl.bf16_bits(w.v_cache)
+    kn, vn = wl.bf16_bits(w.k_new), wl.bf16_bits(w.v_new)
+    slots = w.slot_mapping.numpy().copy()
+    nb, bs, hkv, d = kc.shape
+    k1, v1, rej = oracle.kv_append_checked(kn, vn, slots, kc, vc)
+    assert not rej
+    exp_k = kc.reshape(nb * bs, hkv, d).copy()
+    exp_v = vc.reshape(nb * bs, hkv, d).copy()
+    for t, s_ in enumerate(slots):
+        exp_k[s_] = kn[t]
+        exp_v[s_] = vn[t]
+    assert np.array_equal(k1.reshape(nb * bs, hkv, d), exp_k)
+    assert np.array_equal(v1.reshape(nb * bs, hkv, d), exp_v)
+    dup = slots.copy()
+    dup[3] = dup[0]                                   # two tokens, one row
+    k2, v2, rej = oracle.kv_append_checked(kn, vn, dup, kc, vc)
+    assert rej and np.array_equal(k2, kc) and np.array_equal(v2, vc)
+    skips = slots.copy()
+    skips[1] = skips[2] = -1                          # repeated skips are fine
+    k3, _, rej = oracle.kv_append_checked(kn, vn, skips, kc, vc)
+    assert not rej
+    assert np.array_equal(k3.reshape(nb * bs, hkv, d)[slots[0]], kn[0])
+    assert np.array_equal(k3.reshape(nb * bs, hkv, d)[slots[1]],
+                          kc.reshape(nb * bs, hkv, d)[slots[1]])
+
+
 # ---------------------------------------------------------------------------
 # Paging is address translation: paged == contiguous, and pages may sit
 # anywhere (permutation invariance, bitwise)
