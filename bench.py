@@ -374,7 +374,7 @@ def run_mixed(args, dev, pagedkv, E):
         return c0.elapsed_time(c1) / steps
 
     t_conc = {cascade: time_concurrent(cascade) for cascade in (False, True)}
-    split_sweep = {c: round(time_concurrent(True, c), 4) for c in (72, 88, 104, 120, 136)}
+    split_sweep = {c: round(time_concurrent(True, c), 4) for c in (72, 80, 88, 96, 104, 120, 136)}
     best_ctas = min(split_sweep, key=split_sweep.get)
     t_split = time_concurrent(True, best_ctas)
     # the same step over an FP8 (e4m3) cache: quantizing append, prefill
@@ -434,7 +434,7 @@ def run_mixed(args, dev, pagedkv, E):
         torch.cuda.synchronize()
         return c0.elapsed_time(c1) / steps
 
-    fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (72, 88, 104, 120)}
+    fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (88, 96, 104, 112, 120)}
     fp8_best = min(fp8_sweep, key=fp8_sweep.get)
     fp8_step = {"ms_per_step": round(ms8(0, 3), 4), "append_ms": round(ms8(0, 1), 4),
                 "prefill_ms": round(ms8(1, 2), 4), "decode_ms": round(ms8(2, 3), 4),
