@@ -115,8 +115,8 @@ struct PrefillParams {
   const int32_t* v_block_tables;  // null: V pages use block_tables
   int v_num_blocks;             // blocks of the V pool
   // persistent mode: CTAs take items (pair, query tile) from this counter,
-  // zero on entry, in the grid mode's longest-first order; null: one item
-  // per CTA from the grid
+  // zero on entry, in the grid mode's order (item_pair_tile); null: one
+  // item per CTA from the grid
   int* work_counter;
   int num_items;                // pairs * tiles_per_pair
   int tiles_per_pair;           // CTA-sized query tiles of the longest chunk
