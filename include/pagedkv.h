@@ -386,6 +386,20 @@ PKV_API int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, i
                                        void* workspace, size_t ws_bytes, int partition_blocks,
                                        pkv_stream_t stream);
 
+/* pkv_paged_verify_attention with a bf16 output: the float32 result rounded
+ * to the nearest bf16 (ties to even) in the final store, bit for bit (see
+ * pkv_paged_decode_attention_bf16out).  out: [num_seqs][q_len][q_heads]
+ * [d_head] bf16, 2-byte aligned. */
+PKV_API int pkv_paged_verify_attention_bf16out(const void* q, int num_seqs, int q_len,
+                                               int q_heads, const void* k_cache,
+                                               const void* v_cache, pkv_cache_desc cache,
+                                               const int32_t* block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t* context_lens, int max_context_len,
+                                               float scale, void* out, void* workspace,
+                                               size_t ws_bytes, int partition_blocks,
+                                               pkv_stream_t stream);
+
 /*
  * FP8 KV cache.  The pages name FP8 KV caches as the way to halve decode's
  * KV bytes ("Cache KV, attention et optimisation de l'inference", section
@@ -421,6 +435,21 @@ PKV_API int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_he
                                            float v_scale, float* out, void* workspace,
                                            size_t ws_bytes, int partition_blocks,
                                            pkv_stream_t stream);
+
+/* pkv_paged_decode_attention_fp8 with a bf16 output: the float32 result
+ * rounded to the nearest bf16 (ties to even) in the final store, bit for bit
+ * (see pkv_paged_decode_attention_bf16out).  out: [num_seqs][q_heads][128]
+ * bf16, 2-byte aligned. */
+PKV_API int pkv_paged_decode_attention_fp8_bf16out(const void* q, int num_seqs, int q_heads,
+                                                   const void* k_cache, const void* v_cache,
+                                                   pkv_cache_desc cache,
+                                                   const int32_t* block_tables,
+                                                   int max_blocks_per_seq,
+                                                   const int32_t* context_lens,
+                                                   int max_context_len, float scale,
+                                                   float k_scale, float v_scale, void* out,
+                                                   void* workspace, size_t ws_bytes,
+                                                   int partition_blocks, pkv_stream_t stream);
 
 /*
  * pkv_paged_prefill_attention_fp8 -- pkv_paged_prefill_attention over FP8

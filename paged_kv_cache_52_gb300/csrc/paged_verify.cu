@@ -97,7 +97,7 @@ paged_verify_kernel(const __grid_constant__ CUtensorMap tmap_k,
   };
   if (sp.count == 0) {  // empty context: zeros
     for (int i = threadIdx.x; i < rows_used * D; i += blockDim.x)
-      p.out[out_row(i / D) * D + (i - (i / D) * D)] = 0.f;
+      store_out(p, out_row(i / D) * D + (i - (i / D) * D), 0.f);
     return;
   }
   const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
@@ -375,7 +375,7 @@ paged_verify_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const float res = tot > 0.f ? val / tot : 0.f;
     const size_t orow = out_row(row);
     if (final_out) {
-      p.out[orow * D + col] = res;
+      store_out(p, orow * D + col, res);
     } else {
       const size_t prow = orow * p.num_parts + part;
       p.part_o[prow * D + col] = res;
@@ -450,6 +450,7 @@ cudaError_t launch_paged_verify(const DecodeArgs& a, int q_len, const CUtensorMa
   prm.num_parts = a.num_parts;
   prm.scale_log2 = a.scale_log2;
   prm.out_scale = 1.f;
+  prm.out_bf16 = a.out_bf16 ? 1 : 0;
   prm.first_block = 0;
   prm.force_partials = 0;
   prm.extra_o = nullptr;

@@ -569,12 +569,14 @@ int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,
                           workspace, ws_bytes, partition_blocks, stream);
 }
 
-int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
-                                   const void* k_cache, const void* v_cache, pkv_cache_desc cache,
-                                   const int32_t* block_tables, int max_blocks_per_seq,
-                                   const int32_t* context_lens, int max_context_len, float scale,
-                                   float k_scale, float v_scale, float* out, void* workspace,
-                                   size_t ws_bytes, int partition_blocks, pkv_stream_t stream) {
+namespace {
+
+// The FP8-pool decode with a float32 (or, out_bf16, a bf16) output.
+int decode_fp8_pool(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                    const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                    float scale, float k_scale, float v_scale, void* out, bool out_bf16,
+                    void* workspace, size_t ws_bytes, int partition_blocks, pkv_stream_t stream) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   if (cache.d_head != 128) return PKV_EUNSUPPORTED;
@@ -588,7 +590,8 @@ int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return PKV_EINVAL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      !aligned(out, out_bf16 ? 2 : 4))
     return PKV_EINVAL;
   if (plan.ws_bytes > 0) {
     if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
@@ -601,7 +604,8 @@ int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.out = out;
+  a.out = static_cast<float*>(out);
+  a.out_bf16 = out_bf16;
   a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
   a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                         plan.lse_offset)
@@ -618,6 +622,32 @@ int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
   a.out_scale = v_scale;
   cudaError_t e = pkv::launch_paged_decode_fp8(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
+                                   const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int max_context_len, float scale,
+                                   float k_scale, float v_scale, float* out, void* workspace,
+                                   size_t ws_bytes, int partition_blocks, pkv_stream_t stream) {
+  return decode_fp8_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                         max_blocks_per_seq, context_lens, max_context_len, scale, k_scale,
+                         v_scale, out, false, workspace, ws_bytes, partition_blocks, stream);
+}
+
+int pkv_paged_decode_attention_fp8_bf16out(const void* q, int num_seqs, int q_heads,
+                                           const void* k_cache, const void* v_cache,
+                                           pkv_cache_desc cache, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int max_context_len, float scale, float k_scale,
+                                           float v_scale, void* out, void* workspace,
+                                           size_t ws_bytes, int partition_blocks,
+                                           pkv_stream_t stream) {
+  return decode_fp8_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                         max_blocks_per_seq, context_lens, max_context_len, scale, k_scale,
+                         v_scale, out, true, workspace, ws_bytes, partition_blocks, stream);
 }
 
 int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads, const void* k_cache,
@@ -820,12 +850,14 @@ size_t pkv_verify_workspace_bytes(int num_seqs, int q_len, int q_heads, int kv_h
   return plan.ws_bytes;
 }
 
-int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_heads,
-                               const void* k_cache, const void* v_cache, pkv_cache_desc cache,
-                               const int32_t* block_tables, int max_blocks_per_seq,
-                               const int32_t* context_lens, int max_context_len, float scale,
-                               float* out, void* workspace, size_t ws_bytes,
-                               int partition_blocks, pkv_stream_t stream) {
+namespace {
+
+// The multi-query decode with a float32 (or, out_bf16, a bf16) output.
+int verify_bf16_pool(const void* q, int num_seqs, int q_len, int q_heads, const void* k_cache,
+                     const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                     float scale, void* out, bool out_bf16, void* workspace, size_t ws_bytes,
+                     int partition_blocks, pkv_stream_t stream) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   Plan plan;
@@ -836,7 +868,8 @@ int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_hea
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
   if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PKV_EINVAL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      !aligned(out, out_bf16 ? 2 : 4))
     return PKV_EINVAL;
   if (plan.ws_bytes > 0) {
     if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;
@@ -849,7 +882,8 @@ int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_hea
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.out = out;
+  a.out = static_cast<float*>(out);
+  a.out_bf16 = out_bf16;
   a.part_o = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
   a.part_lse = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                         plan.lse_offset)
@@ -866,6 +900,31 @@ int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_hea
   a.out_scale = 1.f;
   cudaError_t e = pkv::launch_paged_verify(a, q_len, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+int pkv_paged_verify_attention(const void* q, int num_seqs, int q_len, int q_heads,
+                               const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float scale,
+                               float* out, void* workspace, size_t ws_bytes,
+                               int partition_blocks, pkv_stream_t stream) {
+  return verify_bf16_pool(q, num_seqs, q_len, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
+                          workspace, ws_bytes, partition_blocks, stream);
+}
+
+int pkv_paged_verify_attention_bf16out(const void* q, int num_seqs, int q_len, int q_heads,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_cache_desc cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float scale, void* out,
+                                       void* workspace, size_t ws_bytes, int partition_blocks,
+                                       pkv_stream_t stream) {
+  return verify_bf16_pool(q, num_seqs, q_len, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, true,
+                          workspace, ws_bytes, partition_blocks, stream);
 }
 
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,

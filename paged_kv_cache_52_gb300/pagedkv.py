@@ -73,6 +73,14 @@ SIGNATURES = {
     "pkv_paged_decode_attention_ex": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
                                        ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                        ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_paged_decode_attention_fp8_bf16out": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                                CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                                                _f32, _f32, _f32, _vp, _vp, _sz, ctypes.c_int,
+                                                _vp], ctypes.c_int),
+    "pkv_paged_verify_attention_bf16out": ([_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                            _vp, CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                                            _f32, _vp, _vp, _sz, ctypes.c_int, _vp],
+                                           ctypes.c_int),
     "pkv_paged_decode_attention_bf16out": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp,
                                             _sz, ctypes.c_int, _vp], ctypes.c_int),
@@ -269,8 +277,10 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                out: Optional[torch.Tensor] = None,
                                max_context_len: Optional[int] = None,
                                workspace: Optional[torch.Tensor] = None,
-                               partition_blocks: int = 0) -> torch.Tensor:
-    """Decode attention over FP8 pools (the dequantized cache's attention)."""
+                               partition_blocks: int = 0,
+                               out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
+    """Decode attention over FP8 pools (the dequantized cache's attention).
+    ``out`` is float32 unless ``out_dtype`` (or a given ``out``) is bfloat16."""
     _check_fp8_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
           "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
@@ -282,18 +292,23 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
           context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if S else 0
+    odt = _out_dtype(out, out_dtype)
     if out is None:
-        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+        out = torch.empty(S, hq, d, dtype=odt, device=q.device)
+    _need(out.dtype == odt and out.is_contiguous() and out.shape == (S, hq, d),
+          "out must be contiguous float32 or bfloat16 [S, Hq, d]")
     if workspace is None:
         workspace = decode_workspace(S, hq, k_cache.shape[2], d, max_context_len, q.device,
                                      partition_blocks)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib.pkv_paged_decode_attention_fp8(
+    fn = (lib.pkv_paged_decode_attention_fp8_bf16out if odt == torch.bfloat16
+          else lib.pkv_paged_decode_attention_fp8)
+    st = fn(
         _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale),
         float(k_scale), float(v_scale), _ptr(out), _ptr(workspace), ws_bytes,
         int(partition_blocks), _stream(q))
-    _check("pkv_paged_decode_attention_fp8", st)
+    _check(fn.__name__, st)
     return out
 
 
@@ -532,10 +547,12 @@ def paged_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            out: Optional[torch.Tensor] = None,
                            max_context_len: Optional[int] = None,
                            workspace: Optional[torch.Tensor] = None,
-                           partition_blocks: int = 0) -> torch.Tensor:
+                           partition_blocks: int = 0,
+                           out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
     """Speculative verification: ``q [S, K, Hq, d]`` holds the last K tokens of
     each sequence (already appended); token t attends causally over the first
-    ``context_len - K + t + 1`` positions.  Returns ``out [S, K, Hq, d]`` fp32."""
+    ``context_len - K + t + 1`` positions.  Returns ``out [S, K, Hq, d]``,
+    float32 unless ``out_dtype`` (or a given ``out``) is bfloat16."""
     _check_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 4 and q.is_contiguous(),
           "q must be a contiguous [S, K, Hq, d] bf16 CUDA tensor")
@@ -548,19 +565,22 @@ def paged_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
           context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if S else 0
+    odt = _out_dtype(out, out_dtype)
     if out is None:
-        out = torch.empty(S, K, hq, d, dtype=torch.float32, device=q.device)
-    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, K, hq, d),
-          "out must be contiguous float32 [S, K, Hq, d]")
+        out = torch.empty(S, K, hq, d, dtype=odt, device=q.device)
+    _need(out.dtype == odt and out.is_contiguous() and out.shape == (S, K, hq, d),
+          "out must be contiguous float32 or bfloat16 [S, K, Hq, d]")
     if workspace is None:
         workspace = verify_workspace(S, K, hq, k_cache.shape[2], d, max_context_len, q.device,
                                      partition_blocks)
-    st = lib.pkv_paged_verify_attention(
+    fn = (lib.pkv_paged_verify_attention_bf16out if odt == torch.bfloat16
+          else lib.pkv_paged_verify_attention)
+    st = fn(
         _ptr(q), S, K, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len),
         float(scale), _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
         int(partition_blocks), _stream(q))
-    _check("pkv_paged_verify_attention", st)
+    _check(fn.__name__, st)
     return out
 
 

@@ -246,3 +246,22 @@ def test_checked_append_host_validation(pk):
     assert call(T=-1) == -1
     assert call(ws=null) == -4 and call(wsb=need - 1) == -4
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -1  # workspace not 256-byte aligned
+
+
+def test_fp8_decode_and_verify_bf16_out_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    dummy = ctypes.c_void_p(1 << 20)
+    half = ctypes.c_void_p((1 << 20) + 2)                 # 2-byte aligned only
+    d128 = _desc(pk, nb=64, bs=16, hkv=2, d=128)
+    fp8 = lambda fn, out: fn(dummy, 4, 8, dummy, dummy, d128, dummy, 16, dummy, 250,  # noqa: E731
+                             0.125, 1.0, 1.0, out, null, 0, 4, null)
+    # 2-byte alignment passes for bf16 (then the split plan wants a workspace)
+    assert fp8(lib.pkv_paged_decode_attention_fp8_bf16out, half) == -4
+    assert fp8(lib.pkv_paged_decode_attention_fp8, half) == -1
+    assert fp8(lib.pkv_paged_decode_attention_fp8_bf16out, ctypes.c_void_p((1 << 20) + 1)) == -1
+    ver = lambda fn, out, S=4: fn(dummy, S, 2, 8, dummy, dummy, d128, dummy, 16, dummy,  # noqa: E731
+                                  250, 0.125, out, null, 0, 4, null)
+    assert ver(lib.pkv_paged_verify_attention_bf16out, half) == -4
+    assert ver(lib.pkv_paged_verify_attention, half) == -1
+    assert ver(lib.pkv_paged_verify_attention_bf16out, null) == -1
+    assert ver(lib.pkv_paged_verify_attention_bf16out, half, S=0) == 0

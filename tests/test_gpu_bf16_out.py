@@ -148,3 +148,47 @@ def test_prefill_bf16_out_rejects_sm_limit(pk):
         pk.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache,
                                    w.prefill_tables, w.prefill_lens, True, w.scale,
                                    workspace=ws, max_ctas=16, out_dtype=torch.bfloat16)
+
+
+def test_fp8_decode_bf16_out(pk):
+    # FP8 pools: the same kernel arithmetic, rounded in the final store, on
+    # the unsplit path and through the merge (both merge forms)
+    lens = [1, 16, 17, 200, 0, 900, 33]
+    spec = wl.DecodeSpec("fp8edge", 12, len(lens), 64, 8, 128, lens=tuple(lens))
+    w = _decode_dev(wl.make_decode_workload(spec, lens_override=lens))
+    ks, vs = wl.FP8_SCALES["tiny"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    for pb in (0, 2):
+        kw = dict(max_context_len=max(lens), partition_blocks=pb)
+        f32 = pk.paged_decode_attention_fp8(w.q, kc8, vc8, w.block_tables, w.context_lens,
+                                            w.scale, ks, vs, **kw)
+        bf = pk.paged_decode_attention_fp8(w.q, kc8, vc8, w.block_tables, w.context_lens,
+                                           w.scale, ks, vs, out_dtype=torch.bfloat16, **kw)
+        S, hq, d = w.q.shape
+        buf = torch.zeros(S * hq * d + 1, dtype=torch.bfloat16, device=DEV)
+        shifted = buf[1:].view(S, hq, d)
+        pk.paged_decode_attention_fp8(w.q, kc8, vc8, w.block_tables, w.context_lens, w.scale,
+                                      ks, vs, out=shifted, **kw)
+        torch.cuda.synchronize()
+        assert_bf16_rounding_of(bf, f32, f"fp8 decode pb={pb}")
+        assert_bf16_rounding_of(shifted, f32, f"fp8 decode pb={pb}, 2-byte aligned out")
+    assert pk.get_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("K,pb", [(2, 0), (4, 2), (3, 0)])
+def test_verify_bf16_out(pk, K, pb):
+    lens = [4, 17, 33, 300, 1000, 16, 250, 129]
+    w = wl.make_chunked_workload(64, 8, 128, [L - K for L in lens], [K] * len(lens),
+                                 config_id=8)
+    w = _prefill_to_dev(w)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    S = len(lens)
+    q = w.q_prefill.view(S, K, 64, 128)
+    kw = dict(max_context_len=max(lens), partition_blocks=pb)
+    f32 = pk.paged_verify_attention(q, kc, vc, w.prefill_tables, w.prefill_lens, w.scale, **kw)
+    bf = pk.paged_verify_attention(q, kc, vc, w.prefill_tables, w.prefill_lens, w.scale,
+                                   out_dtype=torch.bfloat16, **kw)
+    torch.cuda.synchronize()
+    assert_bf16_rounding_of(bf, f32, f"verify K={K} pb={pb}")
+    assert pk.get_device_error(clear=True) == 0
