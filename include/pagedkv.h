@@ -535,6 +535,23 @@ PKV_API int pkv_paged_decode_attention_noalloc(const void* q, int num_seqs, int 
  */
 PKV_API int pkv_get_device_error(unsigned int* word, int clear);
 
+/*
+ * Failure detection without a fault.  Every kernel waits on its mbarriers
+ * (copies landed, MMAs done) through one bounded wait: after
+ * pkv_wait_poll_limit() polls it gives up, sets PKV_DEVERR_WAIT_TIMEOUT,
+ * waits (again bounded) for its own copies in flight and returns, so a
+ * stuck copy or MMA ends in an error the host reads instead of a hang.
+ * pkv_wait_timeout_probe runs that same wait in a one-thread kernel on a
+ * barrier phase that never completes, with `polls` (1 ..
+ * pkv_wait_poll_limit()) as the limit: the wait runs out, the timeout bit
+ * is set and the kernel returns.  cycles (device pointer, 8-byte aligned,
+ * or NULL) receives the clock64 cycles the wait took.  PKV_EINVAL for polls
+ * out of range.
+ */
+PKV_API uint32_t pkv_wait_poll_limit(void);
+PKV_API int pkv_wait_timeout_probe(uint32_t polls, unsigned long long* cycles,
+                                   pkv_stream_t stream);
+
 /* Human-readable name of a pkv_status value (static string). */
 PKV_API const char* pkv_status_string(int status);
 

@@ -1026,9 +1026,20 @@ int pkv_get_device_error(unsigned int* word, int clear) {
   const unsigned f = pkv::read_prefill_error(clear != 0);
   const unsigned d8 = pkv::read_decode_fp8_error(clear != 0);
   const unsigned v = pkv::read_verify_error(clear != 0);
-  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u) return PKV_ECUDA;
-  *word = a | d | f | d8 | v;
+  const unsigned w = pkv::read_probe_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u || w == ~0u) return PKV_ECUDA;
+  *word = a | d | f | d8 | v | w;
   return PKV_OK;
+}
+
+uint32_t pkv_wait_poll_limit(void) { return pkv::wait_poll_limit(); }
+
+int pkv_wait_timeout_probe(uint32_t polls, unsigned long long* cycles, pkv_stream_t stream) {
+  if (polls == 0 || polls > pkv::wait_poll_limit()) return PKV_EINVAL;
+  if (cycles && !aligned(cycles, 8)) return PKV_EINVAL;
+  const cudaError_t e =
+      pkv::launch_wait_timeout_probe(polls, cycles, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 }  // extern "C"

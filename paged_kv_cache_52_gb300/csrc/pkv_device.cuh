@@ -23,10 +23,13 @@ enum : unsigned {
   kErrDuplicateSlot = 1u << 7,  // checked append: two tokens name one slot (nothing written)
 };
 
-// A bounded wait gives up after this many polls (each poll of try_wait may
-// itself suspend the thread for a short, hardware-defined time), so a wait
-// that can never finish ends in well under a minute instead of hanging.
-constexpr uint32_t kWaitPollLimit = 1u << 24;
+// A bounded wait gives up after this many polls.  A poll of try_wait on a
+// phase that has not completed suspends the thread for a hardware-defined
+// time, measured on GB300 at ~7,770 cycles (3.75 us at 2.07 GHz), so a wait
+// that can never finish ends after about one second instead of hanging.
+// Every wait of these kernels (a copy landing, an MMA group completing)
+// normally takes microseconds.
+constexpr uint32_t kWaitPollLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -64,8 +67,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Returns false if the phase did not complete within the poll limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPollLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint32_t limit = kWaitPollLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;

@@ -42,6 +42,16 @@ cudaError_t launch_v_pages_to_f16(const void* v, const int32_t* tables, const in
                                   int num_seqs, int max_blocks, int num_blocks, int64_t page_elems,
                                   void* vdst, int32_t* table_out, int32_t* seq_order,
                                   cudaStream_t stream, int num_sms);
+// ---- wait_probe.cu
+// Bounded-wait probe: one thread waits on an mbarrier phase that never
+// completes, with `polls` (1 .. kWaitPollLimit) as the poll limit; the wait
+// gives up and the timeout bit is recorded.  cycles (optional, device): the
+// clock64 cycles the wait took.
+cudaError_t launch_wait_timeout_probe(uint32_t polls, unsigned long long* cycles,
+                                      cudaStream_t stream);
+unsigned read_probe_error(bool clear);
+uint32_t wait_poll_limit();
+
 // Copy-on-write block copies: block_bytes a multiple of 16.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int64_t block_bytes, cudaStream_t stream,

@@ -89,6 +89,8 @@ SIGNATURES = {
                                              ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                              _vp], ctypes.c_int),
     "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
+    "pkv_wait_poll_limit": ([], ctypes.c_uint32),
+    "pkv_wait_timeout_probe": ([ctypes.c_uint32, _vp, _vp], ctypes.c_int),
     "pkv_paged_prefill_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, _vp, CacheDesc, _vp, ctypes.c_int, _vp,
                                      ctypes.c_int, _f32, _vp, _vp], ctypes.c_int),
@@ -646,6 +648,18 @@ def get_device_error(clear: bool = True) -> int:
     word = ctypes.c_uint()
     _check("pkv_get_device_error", lib.pkv_get_device_error(ctypes.byref(word), int(clear)))
     return word.value
+
+
+def wait_timeout_probe(polls: int, device=None) -> int:
+    """Run the library's bounded mbarrier wait on a phase that never
+    completes, with ``polls`` as the limit (``pkv_wait_timeout_probe``).
+    Returns the clock64 cycles the wait took; the timeout bit is left in the
+    device error word for the caller to read."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    cycles = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = lib.pkv_wait_timeout_probe(int(polls), _ptr(cycles), _stream(cycles))
+    _check("pkv_wait_timeout_probe", st)
+    return int(cycles.item())
 
 
 def describe_device_error(word: int) -> list[str]:

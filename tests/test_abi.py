@@ -265,3 +265,12 @@ def test_fp8_decode_and_verify_bf16_out_host_validation(pk):
     assert ver(lib.pkv_paged_verify_attention, half) == -1
     assert ver(lib.pkv_paged_verify_attention_bf16out, null) == -1
     assert ver(lib.pkv_paged_verify_attention_bf16out, half, S=0) == 0
+
+
+def test_wait_probe_host_validation(pk):
+    lib, null = pk.lib, ctypes.c_void_p(0)
+    limit = lib.pkv_wait_poll_limit()
+    assert limit == 1 << 18
+    assert lib.pkv_wait_timeout_probe(0, null, null) == -1
+    assert lib.pkv_wait_timeout_probe(limit + 1, null, null) == -1   # never longer than a real wait
+    assert lib.pkv_wait_timeout_probe(16, ctypes.c_void_p((1 << 20) + 4), null) == -1
