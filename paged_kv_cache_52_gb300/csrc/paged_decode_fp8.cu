@@ -9,6 +9,9 @@
 //  * a 16-token page of one KV head is 2 KB of codes per tensor: one 4-D TMA
 //    box of 128 bytes x 16 rows, 128-byte swizzled; 4 stages per warp, so
 //    three CTAs (12 warps) share an SM to hide the longer per-byte compute.
+//  * a warp takes its pages two at a time: the two pages' MMA and
+//    exponential chains are independent and overlap, and one max reduction,
+//    one rescale test and one sum update serve 32 keys.
 //  * the contractions run as f16 warp MMAs (m16n8k16, fp32 accumulation):
 //    e4m3 -> f16 is exact, bf16 q -> f16 is exact in f16's range (an |q| that
 //    would overflow raises PKV_DEVERR_FP16_RANGE), and both scales factor out
@@ -99,18 +102,187 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+// Running state of one warp: O^T accumulators (m-tile mt, row gid = dim
+// 16 mt + 2 gid, row gid + 8 = dim 16 mt + 2 gid + 1; columns 2 tig, 2 tig + 1
+// = heads of n-tile nh), and the running max and this lane's part of the sum
+// of heads 8 nh + 2 tig + c.
+template <int G>
+struct F8Acc {
+  static constexpr int NH = (G + 7) / 8;
+  static constexpr int MT = kF8D / 16;
+  float o[NH][MT][4];
+  float m[NH][2], l[NH][2];
+};
+
+// NP consecutive pages of this warp (ring slots i, i + 1, ...), all landed.
+// Two pages per call keep two independent MMA and exponential chains in
+// flight and share one max reduction and one rescale among 32 keys.
+template <int G, int NP>
+__device__ __forceinline__ void fp8_pages(F8Acc<G>& A, const uint32_t (&qf)[(G + 7) / 8][8][2],
+                                          uint32_t ring, int i, int tok_first, int len,
+                                          float scale_log2, int lane) {
+  using T = F8Tile;
+  constexpr int NH = F8Acc<G>::NH;
+  constexpr int MT = F8Acc<G>::MT;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int mi = lane >> 3, mr = lane & 7;
+  const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (keys 0-7|8-15) x (chunk even|odd)
+  const int v_tok = (mi & 1) * 8 + mr;   // V: matrices (keys 0-7|8-15) x (chunk even|odd)
+  uint32_t kbase[NP];
+  int tok0[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    kbase[pg] = ring + ((i + pg) % kF8Stages) * T::kStageBytes;
+    tok0[pg] = tok_first + pg * kF8Warps * kBlockTokens;
+  }
+
+  // S^T = K Q^T: one ldmatrix.x4 covers two k-steps of both 8-key halves:
+  // a lane gets 4 consecutive dims of key gid (r0 | r1) and of key gid + 8
+  // (r2 | r3).  Even and odd k-steps accumulate separately.
+  float s[NP][NH][4], s_odd[NP][NH][4];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg)
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[pg][nh][e] = s_odd[pg][nh][e] = 0.f;
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) {
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int chunk = 2 * kp + (mi & 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(kbase[pg] + k_tok * 128 + (((chunk ^ (k_tok & 7))) << 4), r0, r1, r2, r3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(h ? r1 : r0, a0, a2);  // key gid
+        e4m3x4_to_f16x2x2(h ? r3 : r2, a1, a3);  // key gid + 8
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+          mma_f16_16816(h ? s_odd[pg][nh] : s[pg][nh], a0, a1, a2, a3, qf[nh][2 * kp + h][0],
+                        qf[nh][2 * kp + h][1]);
+      }
+    }
+  }
+
+  // Online softmax in the log2 domain (k_scale folded into scale_log2), per
+  // head column over the pages' keys (rows: this lane's gid and gid + 8 of
+  // each page, the other keys in the lanes with the same tig).
+  bool k0_in[NP], k1_in[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    k0_in[pg] = tok0[pg] + gid < len;
+    k1_in[pg] = tok0[pg] + gid + 8 < len;
+  }
+  uint32_t pb[NP][NH][2];
+  bool all_same = true;
+  float alpha[NH][2];
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh) {
+    float pr[NP][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float x0[NP], x1[NP];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        x0[pg] = k0_in[pg] ? (s[pg][nh][c] + s_odd[pg][nh][c]) * scale_log2 : -INFINITY;
+        x1[pg] = k1_in[pg] ? (s[pg][nh][c + 2] + s_odd[pg][nh][c + 2]) * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, fmaxf(x0[pg], x1[pg]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(A.m[nh][c], mx);
+      alpha[nh][c] = ex2(A.m[nh][c] - mn);
+      all_same = all_same && A.m[nh][c] == mn;
+      A.m[nh][c] = mn;
+      float add = 0.f;
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        pr[pg][c] = ex2(x0[pg] - mn);
+        pr[pg][c + 2] = ex2(x1[pg] - mn);
+        add += pr[pg][c] + pr[pg][c + 2];
+      }
+      A.l[nh][c] = A.l[nh][c] * alpha[nh][c] + add;
+    }
+    // P^T as the B operand of the P V product: k = a page's keys, n = the
+    // heads; the lane's (key, two heads) pairs transposed into (two keys, head)
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      pb[pg][nh][0] = movmatrix_trans(pack_f16x2(pr[pg][0], pr[pg][1]));  // keys 2 tig, +1
+      pb[pg][nh][1] = movmatrix_trans(pack_f16x2(pr[pg][2], pr[pg][3]));  // keys 8 + 2 tig, +1
+    }
+  }
+  // After the first pages the running max rarely moves: skip the rescale
+  // (alpha = 1 exactly) unless some head of the warp needs it.
+  if (!__all_sync(0xffffffffu, all_same)) {
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        A.o[nh][mt][0] *= alpha[nh][0];
+        A.o[nh][mt][1] *= alpha[nh][1];
+        A.o[nh][mt][2] *= alpha[nh][0];
+        A.o[nh][mt][3] *= alpha[nh][1];
+      }
+  }
+
+  // O^T += V^T P^T.  ldmatrix.trans over the codes as 16-bit units gives a
+  // lane keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim
+  // chunk; the byte permute splits that into the key pair of dim 2 gid (row
+  // gid) and of dim 2 gid + 1 (row gid + 8).
+  // Rows of the last page past the length may hold any code, NaN included:
+  // zero them (their P is 0).  Each 16-bit unit holds one key's two codes,
+  // keys (2 tig, 2 tig + 1) in r0 / r2 and 8 more in r1 / r3.
+  uint32_t vm0[NP], vm1[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    vm0[pg] = vm1[pg] = 0xffffffffu;
+    if (tok0[pg] + kBlockTokens > len) {
+      const int k0 = tok0[pg] + 2 * tig;
+      vm0[pg] = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+      vm1[pg] = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+    }
+  }
+#pragma unroll
+  for (int cp = 0; cp < 4; ++cp) {
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int chunk = 2 * cp + (mi >> 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_trans(kbase[pg] + T::kTileBytes + v_tok * 128 + (((chunk ^ (v_tok & 7))) << 4), r0,
+                    r1, r2, r3);
+      r0 &= vm0[pg];
+      r1 &= vm1[pg];
+      r2 &= vm0[pg];
+      r3 &= vm1[pg];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r2 : r0, 0u, 0x3120), a0, a1);  // keys 2 tig, +1
+        e4m3x4_to_f16x2x2(__byte_perm(h ? r3 : r1, 0u, 0x3120), a2, a3);  // keys 8 + 2 tig, +1
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+          mma_f16_16816(A.o[nh][2 * cp + h], a0, a1, a2, a3, pb[pg][nh][0], pb[pg][nh][1]);
+      }
+    }
+  }
+}
+
 // The MMAs run transposed: S^T = K Q^T has the 16 keys of a page as its M rows
 // and the GQA group's heads as N (8 per n-tile), and O^T = V^T P^T has 16 dims
 // per m-tile as M and the heads as N, so no MMA row is padding (with the heads
 // as M, a group of 8 fills half of an m16 tile).
 template <int G>
-__global__ void __launch_bounds__(kF8Warps * 32)
+__global__ void __launch_bounds__(kF8Warps * 32, 3)
 paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using T = F8Tile;
   constexpr int D = kF8D;
   constexpr int NH = (G + 7) / 8;  // n-tiles of heads
-  constexpr int MT = D / 16;       // m-tiles of O^T (16 dims each)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,143 +367,39 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   issued = cnt < kF8Stages ? cnt : kF8Stages;
 
-  const int mi = lane >> 3, mr = lane & 7;
-  const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (keys 0-7|8-15) x (chunk even|odd)
-  const int v_tok = (mi & 1) * 8 + mr;   // V: matrices (keys 0-7|8-15) x (chunk even|odd)
-
-  // O^T accumulators: m-tile mt, row gid = dim 16 mt + 2 gid, row gid + 8 =
-  // dim 16 mt + 2 gid + 1; columns 2 tig, 2 tig + 1 = heads of n-tile nh.
-  float o[NH][MT][4];
+  F8Acc<G> acc;
 #pragma unroll
-  for (int nh = 0; nh < NH; ++nh)
+  for (int nh = 0; nh < F8Acc<G>::NH; ++nh) {
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[nh][mt][0] = o[nh][mt][1] = o[nh][mt][2] = o[nh][mt][3] = 0.f;
-  // running max and (this lane's part of the) sum of heads 8 nh + 2 tig + c
-  float m[NH][2], l[NH][2];
-#pragma unroll
-  for (int nh = 0; nh < NH; ++nh) m[nh][0] = m[nh][1] = -INFINITY, l[nh][0] = l[nh][1] = 0.f;
+    for (int mt = 0; mt < F8Acc<G>::MT; ++mt)
+      acc.o[nh][mt][0] = acc.o[nh][mt][1] = acc.o[nh][mt][2] = acc.o[nh][mt][3] = 0.f;
+    acc.m[nh][0] = acc.m[nh][1] = -INFINITY;
+    acc.l[nh][0] = acc.l[nh][1] = 0.f;
+  }
   bool failed = false;
   int i = 0;
-  for (; i < cnt; ++i) {
-    const int st = i % kF8Stages;
-    const uint32_t par = (i / kF8Stages) & 1;
-    const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(bars + st * 8, par));
-    if (!ready) {
+  // pages two at a time; an odd last page alone
+  for (; i < cnt; i += 2) {
+    const bool two = i + 1 < cnt;
+    bool landed = mbar_wait_bounded(bars + (i % kF8Stages) * 8, (i / kF8Stages) & 1);
+    if (two && landed)
+      landed = mbar_wait_bounded(bars + ((i + 1) % kF8Stages) * 8, ((i + 1) / kF8Stages) & 1);
+    if (!__all_sync(0xffffffffu, landed)) {
       failed = true;
       break;
     }
-    const uint32_t kbase = ring + st * T::kStageBytes;
-    const uint32_t vbase = kbase + T::kTileBytes;
-    const int tok0 = (b0 + warp + i * kF8Warps) * kBlockTokens;
-
-    // S^T = K Q^T: one ldmatrix.x4 covers two k-steps of both 8-key halves:
-    // a lane gets 4 consecutive dims of key gid (r0 | r1) and of key gid + 8
-    // (r2 | r3).  Even and odd k-steps accumulate separately.
-    float s[NH][4], s_odd[NH][4];
-#pragma unroll
-    for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nh][e] = s_odd[nh][e] = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < 4; ++kp) {
-      const int chunk = 2 * kp + (mi & 1);
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(kbase + k_tok * 128 + (((chunk ^ (k_tok & 7))) << 4), r0, r1, r2, r3);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(h ? r1 : r0, a0, a2);  // key gid
-        e4m3x4_to_f16x2x2(h ? r3 : r2, a1, a3);  // key gid + 8
-#pragma unroll
-        for (int nh = 0; nh < NH; ++nh)
-          mma_f16_16816(h ? s_odd[nh] : s[nh], a0, a1, a2, a3, qf[nh][2 * kp + h][0],
-                        qf[nh][2 * kp + h][1]);
-      }
-    }
-
-    // Online softmax in the log2 domain (k_scale folded into scale_log2), per
-    // head column over the page's 16 keys (rows: this lane's gid and gid + 8,
-    // the other keys in the lanes with the same tig).
-    const bool k0_in = tok0 + gid < len, k1_in = tok0 + gid + 8 < len;
-    uint32_t pb[NH][2];
-    bool all_same = true;
-    float alpha[NH][2];
-#pragma unroll
-    for (int nh = 0; nh < NH; ++nh) {
-      float pr[4];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float x0 = k0_in ? (s[nh][c] + s_odd[nh][c]) * p.scale_log2 : -INFINITY;
-        const float x1 = k1_in ? (s[nh][c + 2] + s_odd[nh][c + 2]) * p.scale_log2 : -INFINITY;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mn = fmaxf(m[nh][c], mx);
-        alpha[nh][c] = ex2(m[nh][c] - mn);
-        all_same = all_same && m[nh][c] == mn;
-        m[nh][c] = mn;
-        pr[c] = ex2(x0 - mn);
-        pr[c + 2] = ex2(x1 - mn);
-        l[nh][c] = l[nh][c] * alpha[nh][c] + (pr[c] + pr[c + 2]);
-      }
-      // P^T as the B operand of the P V product: k = the page's keys, n = the
-      // heads; the lane's (key, two heads) pairs transposed into (two keys, head)
-      pb[nh][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));  // keys 2 tig, 2 tig + 1
-      pb[nh][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));  // keys 8 + 2 tig, 9 + 2 tig
-    }
-    // After the first pages the running max rarely moves: skip the rescale
-    // (alpha = 1 exactly) unless some head of the warp needs it.
-    if (!__all_sync(0xffffffffu, all_same)) {
-#pragma unroll
-      for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          o[nh][mt][0] *= alpha[nh][0];
-          o[nh][mt][1] *= alpha[nh][1];
-          o[nh][mt][2] *= alpha[nh][0];
-          o[nh][mt][3] *= alpha[nh][1];
-        }
-    }
-
-    // O^T += V^T P^T.  ldmatrix.trans over the codes as 16-bit units gives a
-    // lane keys (2 tig, 2 tig + 1) x dims (2 gid, 2 gid + 1) of a 16-dim
-    // chunk; the byte permute splits that into the key pair of dim 2 gid (row
-    // gid) and of dim 2 gid + 1 (row gid + 8).
-    // Rows of the last page past the length may hold any code, NaN included:
-    // zero them (their P is 0).  Each 16-bit unit holds one key's two codes,
-    // keys (2 tig, 2 tig + 1) in r0 / r2 and 8 more in r1 / r3.
-    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-    if (tok0 + kBlockTokens > len) {
-      const int k0 = tok0 + 2 * tig;
-      vm0 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
-      vm1 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int cp = 0; cp < 4; ++cp) {
-      const int chunk = 2 * cp + (mi >> 1);
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_trans(vbase + v_tok * 128 + (((chunk ^ (v_tok & 7))) << 4), r0, r1, r2, r3);
-      r0 &= vm0;
-      r1 &= vm1;
-      r2 &= vm0;
-      r3 &= vm1;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // bytes (k0 d0, k0 d1, k1 d0, k1 d1) -> (k0 d0, k1 d0, k0 d1, k1 d1)
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(__byte_perm(h ? r2 : r0, 0u, 0x3120), a0, a1);  // keys 2 tig, +1
-        e4m3x4_to_f16x2x2(__byte_perm(h ? r3 : r1, 0u, 0x3120), a2, a3);  // keys 8 + 2 tig, +1
-#pragma unroll
-        for (int nh = 0; nh < NH; ++nh)
-          mma_f16_16816(o[nh][2 * cp + h], a0, a1, a2, a3, pb[nh][0], pb[nh][1]);
-      }
-    }
+    const int tok_first = (b0 + warp + i * kF8Warps) * kBlockTokens;
+    if (two)
+      fp8_pages<G, 2>(acc, qf, ring, i, tok_first, len, p.scale_log2, lane);
+    else
+      fp8_pages<G, 1>(acc, qf, ring, i, tok_first, len, p.scale_log2, lane);
 
     __syncwarp();
-    if (i + kF8Stages < cnt) {
-      if (lane == 0) issue(i + kF8Stages);
-      ++issued;
+    for (int j = i; j < i + (two ? 2 : 1); ++j) {
+      if (j + kF8Stages < cnt) {
+        if (lane == 0) issue(j + kF8Stages);
+        ++issued;
+      }
     }
   }
 
@@ -345,38 +413,38 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
 
 #pragma unroll
-  for (int nh = 0; nh < NH; ++nh)
+  for (int nh = 0; nh < F8Acc<G>::NH; ++nh)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 4);
-      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 8);
-      l[nh][c] += __shfl_xor_sync(0xffffffffu, l[nh][c], 16);
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 4);
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 8);
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 16);
     }
 
   // Cross-warp merge through shared memory ([G][D] partial O, then m, l).
   float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);
   float* mml = mo + G * D;
 #pragma unroll
-  for (int nh = 0; nh < NH; ++nh) {
+  for (int nh = 0; nh < F8Acc<G>::NH; ++nh) {
     const int h0 = 8 * nh + 2 * tig;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int mt = 0; mt < F8Acc<G>::MT; ++mt) {
       const int dim0 = 16 * mt + 2 * gid;
       if (h0 < G) {
-        mo[h0 * D + dim0] = o[nh][mt][0];
-        mo[h0 * D + dim0 + 1] = o[nh][mt][2];
+        mo[h0 * D + dim0] = acc.o[nh][mt][0];
+        mo[h0 * D + dim0 + 1] = acc.o[nh][mt][2];
       }
       if (h0 + 1 < G) {
-        mo[(h0 + 1) * D + dim0] = o[nh][mt][1];
-        mo[(h0 + 1) * D + dim0 + 1] = o[nh][mt][3];
+        mo[(h0 + 1) * D + dim0] = acc.o[nh][mt][1];
+        mo[(h0 + 1) * D + dim0 + 1] = acc.o[nh][mt][3];
       }
     }
     if (gid == 0) {
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         if (h0 + c < G) {
-          mml[h0 + c] = m[nh][c];
-          mml[G + h0 + c] = l[nh][c];
+          mml[h0 + c] = acc.m[nh][c];
+          mml[G + h0 + c] = acc.l[nh][c];
         }
     }
   }
