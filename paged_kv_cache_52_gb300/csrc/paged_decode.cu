@@ -33,6 +33,7 @@
 //  * every mbarrier wait is bounded; a timeout sets an error bit, drains the
 //    warp's outstanding copies (also bounded) and lets the CTA finish.
 #include <climits>
+#include <utility>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -234,13 +235,18 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else {
       pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
     }
+    // After the first pages the running max rarely moves: skip the rescale
+    // (alpha = 1 exactly, so the result is unchanged) unless some row of the
+    // warp needs it.
+    if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f)) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      o[n][0] *= alpha0;
-      o[n][1] *= alpha0;
-      if constexpr (kTwoRows) {
-        o[n][2] *= alpha1;
-        o[n][3] *= alpha1;
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= alpha0;
+        o[n][1] *= alpha0;
+        if constexpr (kTwoRows) {
+          o[n][2] *= alpha1;
+          o[n][3] *= alpha1;
+        }
       }
     }
 
@@ -369,6 +375,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p.
 template <int D>
 __global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParams p) {
+  griddep_wait();
   const size_t row = blockIdx.x;  // seq * q_heads + head
   const int seq = int(row / p.q_heads);
   const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
@@ -401,6 +408,7 @@ template <int D>
 __global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodeParams p,
                                                                   long long total_rows) {
   constexpr int TPR = D / 4;  // threads per row
+  griddep_wait();
   const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
   const long long row = gtid / TPR;
   const int c4 = int(gtid - row * TPR);
@@ -468,6 +476,28 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
   return launch_decode_merge(prm, num_seqs, D, stream);
 }
 
+// Launches `kernel` as a programmatic dependent of the stream's previous
+// kernel: its CTAs may be scheduled while that kernel drains, and the
+// kernel's griddep_wait() returns once the previous kernel has completed and
+// its writes are visible.  The launch gap between the two kernels is hidden.
+template <typename... Params, typename... Args>
+static cudaError_t launch_after_previous(void (*kernel)(Params...), unsigned grid, unsigned block,
+                                         cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream) {
   if (prm.num_parts == 1 && !prm.force_partials) return cudaSuccess;
@@ -478,17 +508,18 @@ cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_hea
     const long long blocks = (rows * (d_head / 4) + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     if (d_head == 128)
-      paged_decode_merge4_kernel<128><<<unsigned(blocks), 256, 0, stream>>>(prm, rows);
-    else
-      paged_decode_merge4_kernel<64><<<unsigned(blocks), 256, 0, stream>>>(prm, rows);
+      return launch_after_previous(paged_decode_merge4_kernel<128>, unsigned(blocks), 256, stream,
+                                   prm, rows);
+    return launch_after_previous(paged_decode_merge4_kernel<64>, unsigned(blocks), 256, stream,
+                                 prm, rows);
   } else if (d_head == 128) {
-    paged_decode_merge_kernel<128><<<num_seqs * prm.q_heads, 128, 0, stream>>>(prm);
+    return launch_after_previous(paged_decode_merge_kernel<128>, unsigned(num_seqs * prm.q_heads),
+                                 128, stream, prm);
   } else if (d_head == 64) {
-    paged_decode_merge_kernel<64><<<num_seqs * prm.q_heads, 64, 0, stream>>>(prm);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_after_previous(paged_decode_merge_kernel<64>, unsigned(num_seqs * prm.q_heads),
+                                 64, stream, prm);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 template <int D>

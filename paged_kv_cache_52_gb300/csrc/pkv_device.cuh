@@ -75,6 +75,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Programmatic dependent launch: wait until the grid this one was launched
+// after has completed and its memory operations are visible (returns at once
+// for a kernel launched without that dependency).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // -------------------------------------------------------------------- TMA
 // 4-D tiled load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -86,7 +86,7 @@ def test_fp8_append_bit_exact(pk):
     assert pk.get_device_error() == 0
 
 
-SHAPES = [(8, 8), (16, 4), (64, 8), (32, 2), (16, 16)]
+SHAPES = [(8, 8), (16, 8), (16, 4), (64, 8), (32, 2), (16, 16)]
 LENS = [1, 15, 16, 17, 33, 200, 0, 1500]
 
 
