@@ -65,6 +65,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
   using T = DecodeTile<D>;
   constexpr bool kTwoRows = (G > 8);  // heads gid+8 are real rows too
   constexpr int KSTEPS = D / 16;       // k-steps of QK^T
@@ -469,33 +470,11 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
     attr_set = true;
   }
   dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
-  paged_decode_split_kernel<D, G><<<grid, kDecodeWarps * 32, T::kSmemBytes, stream>>>(
-      *tmap_k, *tmap_v, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after_previous(paged_decode_split_kernel<D, G>, grid,
+                                        dim3(kDecodeWarps * 32), T::kSmemBytes, stream, *tmap_k,
+                                        *tmap_v, prm);
   if (e != cudaSuccess) return e;
   return launch_decode_merge(prm, num_seqs, D, stream);
-}
-
-// Launches `kernel` as a programmatic dependent of the stream's previous
-// kernel: its CTAs may be scheduled while that kernel drains, and the
-// kernel's griddep_wait() returns once the previous kernel has completed and
-// its writes are visible.  The launch gap between the two kernels is hidden.
-template <typename... Params, typename... Args>
-static cudaError_t launch_after_previous(void (*kernel)(Params...), unsigned grid, unsigned block,
-                                         cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
@@ -508,16 +487,16 @@ cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_hea
     const long long blocks = (rows * (d_head / 4) + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     if (d_head == 128)
-      return launch_after_previous(paged_decode_merge4_kernel<128>, unsigned(blocks), 256, stream,
-                                   prm, rows);
-    return launch_after_previous(paged_decode_merge4_kernel<64>, unsigned(blocks), 256, stream,
-                                 prm, rows);
+      return launch_after_previous(paged_decode_merge4_kernel<128>, dim3(unsigned(blocks)),
+                                   dim3(256), 0, stream, prm, rows);
+    return launch_after_previous(paged_decode_merge4_kernel<64>, dim3(unsigned(blocks)), dim3(256),
+                                 0, stream, prm, rows);
   } else if (d_head == 128) {
-    return launch_after_previous(paged_decode_merge_kernel<128>, unsigned(num_seqs * prm.q_heads),
-                                 128, stream, prm);
+    return launch_after_previous(paged_decode_merge_kernel<128>,
+                                 dim3(unsigned(num_seqs * prm.q_heads)), dim3(128), 0, stream, prm);
   } else if (d_head == 64) {
-    return launch_after_previous(paged_decode_merge_kernel<64>, unsigned(num_seqs * prm.q_heads),
-                                 64, stream, prm);
+    return launch_after_previous(paged_decode_merge_kernel<64>,
+                                 dim3(unsigned(num_seqs * prm.q_heads)), dim3(64), 0, stream, prm);
   }
   return cudaErrorInvalidValue;
 }

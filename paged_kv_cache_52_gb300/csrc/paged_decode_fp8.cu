@@ -280,6 +280,7 @@ template <int G>
 __global__ void __launch_bounds__(kF8Warps * 32, 3)
 paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
   using T = F8Tile;
   constexpr int D = kF8D;
   constexpr int NH = (G + 7) / 8;  // n-tiles of heads
@@ -490,8 +491,8 @@ static cudaError_t launch_fp8_t(const DecodeParams& prm, int num_seqs, const CUt
     attr_set = true;
   }
   dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
-  paged_decode_fp8_kernel<G><<<grid, kF8Warps * 32, F8Tile::kSmemBytes, stream>>>(*tk, *tv, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after_previous(paged_decode_fp8_kernel<G>, grid, dim3(kF8Warps * 32),
+                                        F8Tile::kSmemBytes, stream, *tk, *tv, prm);
   if (e != cudaSuccess) return e;
   return launch_decode_merge(prm, num_seqs, kF8D, stream);
 }

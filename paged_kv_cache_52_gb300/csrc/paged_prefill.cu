@@ -811,6 +811,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
   using L = PrefillSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -899,9 +900,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, int max_ctas,
   }
   if (tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(prm.num_seqs * prm.kv_heads, tiles);
-  paged_prefill_kernel<D, G, F16PV, false><<<grid, kPfThreads, L::kSmemBytes, stream>>>(
-      *tq, *tk, *tv, prm);
-  return cudaGetLastError();
+  return launch_after_previous(paged_prefill_kernel<D, G, F16PV, false>, grid, dim3(kPfThreads),
+                               L::kSmemBytes, stream, *tq, *tk, *tv, prm);
 }
 
 template <int D, bool F16PV>

@@ -61,6 +61,7 @@ template <int D, int G, int MT>
 __global__ void __launch_bounds__(kVerifyWarps * 32, 2)
 paged_verify_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const VerifyParams vp) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
   using T = VerifyTile<D, MT>;
   const DecodeParams& p = vp.d;
   constexpr int R = T::kRows;
@@ -407,8 +408,9 @@ static cudaError_t launch_verify_t(const VerifyParams& vp, int num_seqs, const C
     attr_set = true;
   }
   dim3 grid(num_seqs * vp.d.kv_heads, vp.d.num_parts);
-  paged_verify_kernel<D, G, MT><<<grid, kVerifyWarps * 32, T::kSmemBytes, stream>>>(*tk, *tv, vp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after_previous(paged_verify_kernel<D, G, MT>, grid,
+                                        dim3(kVerifyWarps * 32), T::kSmemBytes, stream, *tk, *tv,
+                                        vp);
   if (e != cudaSuccess) return e;
   // The merge sees the K tokens of a sequence as K x q_heads rows of it.
   DecodeParams mp = vp.d;

@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace pkv {
 
 // Bits of the per-library device error word (see pkv_get_device_error).
@@ -80,6 +82,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // for a kernel launched without that dependency).
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches `kernel` as a programmatic dependent of the stream's previous
+// kernel: its CTAs may be scheduled while that kernel drains, and the
+// kernel's griddep_wait() -- its first statement, before any input is read,
+// since the previous kernel may have written them -- returns once the
+// previous kernel has completed and its writes are visible.  This hides the
+// launch gap between the two.
+template <typename... Params, typename... Args>
+static cudaError_t launch_after_previous(void (*kernel)(Params...), dim3 grid, dim3 block,
+                                         size_t smem_bytes, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 // -------------------------------------------------------------------- TMA
