@@ -54,8 +54,8 @@ typedef enum {
   PKV_ECUDA = -3,         /* a CUDA runtime call or a kernel launch failed */
   PKV_ENOMEM = -4,        /* the workspace passed is smaller than required; host memory
                              ran out (block manager) */
-  PKV_EDEVICE_CHECK = -5, /* reserved: a device-side index check failed */
-  PKV_ETIMEOUT = -6,      /* reserved: a bounded device wait ran out */
+  PKV_EDEVICE_CHECK = -5, /* pkv_get_last_device_error: a device-side check raised a bit */
+  PKV_ETIMEOUT = -6,      /* pkv_get_last_device_error: a bounded device wait ran out */
   PKV_ESCRATCH_TOO_SMALL = -7, /* the no-allocation decode's fixed scratch cannot hold the plan */
   PKV_ENOBLOCKS = -8      /* block manager: fewer free blocks than needed; nothing changed */
 } pkv_status;
@@ -236,10 +236,11 @@ PKV_API int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int 
  *                  whole context.
  *   out          : [total_q][q_heads][d_head] float32, 16-byte aligned; rows
  *                  outside every chunk are not written.
- * A chunk longer than its context, a non-monotone q_start or a context beyond
- * the block table skips that sequence and sets PKV_DEVERR_BAD_QUERY_RANGE; a
- * chunk longer than max_q_len is computed only up to max_q_len tokens and
- * sets the same bit.  No workspace is needed.
+ * A chunk longer than its context, a chunk longer than max_q_len, a
+ * non-monotone q_start or a context beyond the block table rejects that
+ * sequence: none of its rows is written and PKV_DEVERR_BAD_QUERY_RANGE is set
+ * (pkv_get_last_device_error returns PKV_EDEVICE_CHECK).  No workspace is
+ * needed.
  */
 PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, int num_seqs,
                                         int total_q, int max_q_len, int q_heads,
@@ -527,6 +528,25 @@ PKV_API int pkv_paged_decode_attention_noalloc(const void* q, int num_seqs, int 
                                                const int32_t* context_lens, int max_context_len,
                                                float scale, float* out, int partition_blocks,
                                                pkv_stream_t stream);
+
+/*
+ * pkv_get_last_device_error -- the checked-mode status of the work queued on
+ * `stream` so far.  The kernels never trap: a bad index is skipped and a
+ * stuck wait gives up, each raising a PKV_DEVERR_* bit in the current
+ * device's error words.  This call queues a one-thread kernel on `stream`
+ * that takes those words and resets them to 0 in one atomic exchange per
+ * word, copies the OR back and synchronises `stream` only (not the device).
+ * Returns PKV_OK when no bit was raised, PKV_ETIMEOUT when a bounded wait ran
+ * out (PKV_DEVERR_WAIT_TIMEOUT), PKV_EDEVICE_CHECK for any other bit, and
+ * PKV_ECUDA when the launch, the copy or the synchronisation failed (e.g. a
+ * stream being captured into a graph).  The words belong to the device, not
+ * to the stream: bits raised by kernels of other streams that finished
+ * before the exchange are reported (and cleared) too; a bit raised after it
+ * stays for the next query.  pkv_get_last_device_error_bits also stores the
+ * bits in *word (NULL allowed).  Host threads' calls are serialised.
+ */
+PKV_API int pkv_get_last_device_error(pkv_stream_t stream);
+PKV_API int pkv_get_last_device_error_bits(pkv_stream_t stream, unsigned int* word);
 
 /*
  * Read the device error word of the current device (an OR of the

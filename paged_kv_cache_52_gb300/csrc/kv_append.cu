@@ -79,6 +79,11 @@ kv_append_kernel(const uint4* __restrict__ k, int64_t k_stride_vec, const uint4*
   }
 }
 
+// Device address of this unit's error word on the current device.
+cudaError_t append_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_append_error);
+}
+
 unsigned read_append_error(bool clear) {
   unsigned word = 0;
   if (cudaMemcpyFromSymbol(&word, g_append_error, sizeof(word)) != cudaSuccess) return ~0u;

@@ -461,13 +461,11 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
                                    const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                    cudaStream_t stream) {
   using T = DecodeTile<D>;
-  static bool attr_set = false;  // per instantiation; idempotent if raced
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_split_kernel<D, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::kSmemBytes);
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  {
+    const cudaError_t e =
+        set_smem_limit_once(paged_decode_split_kernel<D, G>, T::kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
   cudaError_t e = launch_after_previous(paged_decode_split_kernel<D, G>, grid,
@@ -544,6 +542,11 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
 }
 
 int decode_max_partition_blocks() { return kMaxPartitionBlocks; }
+
+// Device address of this unit's error word on the current device.
+cudaError_t decode_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_decode_error);
+}
 
 unsigned read_decode_error(bool clear) {
   unsigned word = 0;

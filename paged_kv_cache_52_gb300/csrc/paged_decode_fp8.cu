@@ -482,13 +482,11 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
 template <int G>
 static cudaError_t launch_fp8_t(const DecodeParams& prm, int num_seqs, const CUtensorMap* tk,
                                 const CUtensorMap* tv, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         F8Tile::kSmemBytes);
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  {
+    const cudaError_t e =
+        set_smem_limit_once(paged_decode_fp8_kernel<G>, F8Tile::kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
   cudaError_t e = launch_after_previous(paged_decode_fp8_kernel<G>, grid, dim3(kF8Warps * 32),
@@ -528,6 +526,11 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap
     case 16: return launch_fp8_t<16>(prm, a.num_seqs, tmap_k, tmap_v, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Device address of this unit's error word on the current device.
+cudaError_t decode_fp8_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_decode_fp8_error);
 }
 
 unsigned read_decode_fp8_error(bool clear) {

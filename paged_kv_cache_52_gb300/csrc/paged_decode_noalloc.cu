@@ -29,22 +29,26 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_scratch_status[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (set-up runs on
 // the first call per device).  Host code must not use the array's name as a
-// device pointer: on the host it only stands in for the symbol.
+// device pointer: on the host it only stands in for the symbol.  Only a
+// successful lookup is kept: a failed one (e.g. a first call made during a
+// stream capture) returns PKV_ECUDA and the next call tries again.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_status[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // leave no sticky launch error behind for the caller
+      return PKV_ECUDA;
+    }
     g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_status[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return PKV_ECUDA;
+  }
   *out = g_scratch_ptr[dev];
   return PKV_OK;
 }

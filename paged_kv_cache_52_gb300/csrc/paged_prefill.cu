@@ -166,12 +166,13 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
   const int n = qe - qs;
   const bool bad_range = qs < 0 || n < 0 || qe > p.total_q;
   if (!bad_range && n == 0) return;  // nothing to compute for this sequence
-  if (bad_range || (p.causal && n > ctx) || ctx <= 0 || ctx > p.max_blocks_per_seq * 16) {
+  // A chunk longer than max_q_len would have tiles the launch does not cover:
+  // the whole sequence is rejected rather than computed in part.
+  if (bad_range || (p.causal && n > ctx) || ctx <= 0 || ctx > p.max_blocks_per_seq * 16 ||
+      n > p.max_q_len) {
     if (cta_tile == 0 && threadIdx.x == 0) atomicOr(&g_prefill_error, kErrBadQueryRange);
     return;
   }
-  if (n > p.max_q_len && cta_tile == 0 && threadIdx.x == 0)
-    atomicOr(&g_prefill_error, kErrBadQueryRange);  // tokens past the grid are not computed
   const int t0 = cta_tile * TPC;
   if (t0 >= n) return;
   const int tok_valid = min(TPC, n - t0);
@@ -871,16 +872,14 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, int max_ctas,
                                     const CUtensorMap* tv, cudaStream_t stream) {
   using L = PrefillSmem<D>;
   constexpr int TPT = kPfRows / G;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
+  static std::atomic<int> attr_grid[kAttrMaxDevices], attr_persist[kAttrMaxDevices];
+  {
+    cudaError_t e =
+        set_smem_limit_once(paged_prefill_kernel<D, G, F16PV, false>, L::kSmemBytes, attr_grid);
     if (e == cudaSuccess && F16PV)
-      e = cudaFuncSetAttribute(paged_prefill_kernel<D, G, F16PV, F16PV>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+      e = set_smem_limit_once(paged_prefill_kernel<D, G, F16PV, F16PV>, L::kSmemBytes,
+                              attr_persist);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   constexpr int TPC = kPfQTiles * TPT;
   const int tiles = (prm.max_q_len + TPC - 1) / TPC;
@@ -956,6 +955,11 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
     if (a.d_head == 64) return launch_prefill_d<64, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+// Device address of this unit's error word on the current device.
+cudaError_t prefill_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_prefill_error);
 }
 
 unsigned read_prefill_error(bool clear) {

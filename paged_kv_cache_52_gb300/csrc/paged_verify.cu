@@ -385,6 +385,11 @@ paged_verify_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
 }
 
+// Device address of this unit's error word on the current device.
+cudaError_t verify_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_verify_error);
+}
+
 unsigned read_verify_error(bool clear) {
   unsigned word = 0;
   if (cudaMemcpyFromSymbol(&word, g_verify_error, sizeof(word)) != cudaSuccess) return ~0u;
@@ -399,13 +404,11 @@ template <int D, int G, int MT>
 static cudaError_t launch_verify_t(const VerifyParams& vp, int num_seqs, const CUtensorMap* tk,
                                    const CUtensorMap* tv, cudaStream_t stream) {
   using T = VerifyTile<D, MT>;
-  static bool attr_set = false;  // per instantiation; idempotent if raced
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_verify_kernel<D, G, MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::kSmemBytes);
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  {
+    const cudaError_t e =
+        set_smem_limit_once(paged_verify_kernel<D, G, MT>, T::kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   dim3 grid(num_seqs * vp.d.kv_heads, vp.d.num_parts);
   cudaError_t e = launch_after_previous(paged_verify_kernel<D, G, MT>, grid,

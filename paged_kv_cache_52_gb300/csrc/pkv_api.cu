@@ -1018,6 +1018,69 @@ int pkv_paged_decode_attention_shared_prefix(
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The error words of every kernel unit, gathered on a stream: one thread
+// reads each word -- and, with `clear`, exchanges it for 0 in the same
+// atomic step, so a bit raised meanwhile by a kernel on another stream stays
+// for the next query instead of being lost -- and stores the OR.
+struct ErrorWordSet {
+  unsigned* word[6];
+  int count;
+  int clear;
+};
+
+__device__ unsigned g_collected_error = 0;
+
+__global__ void collect_error_words_kernel(const ErrorWordSet s) {
+  unsigned acc = 0;
+  for (int i = 0; i < s.count; ++i)
+    acc |= s.clear ? atomicExch(s.word[i], 0u) : atomicOr(s.word[i], 0u);
+  g_collected_error = acc;
+}
+
+std::mutex g_collect_mutex;  // one collection in flight per process
+
+int collect_error_words(cudaStream_t stream, bool clear, unsigned* word) {
+  ErrorWordSet s = {};
+  cudaError_t (*const getters[6])(unsigned**) = {
+      pkv::append_error_word, pkv::decode_error_word, pkv::decode_fp8_error_word,
+      pkv::prefill_error_word, pkv::verify_error_word, pkv::probe_error_word};
+  for (int i = 0; i < 6; ++i)
+    if (getters[i](&s.word[i]) != cudaSuccess) return PKV_ECUDA;
+  s.count = 6;
+  s.clear = clear ? 1 : 0;
+  std::lock_guard<std::mutex> lock(g_collect_mutex);
+  collect_error_words_kernel<<<1, 1, 0, stream>>>(s);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+  unsigned w = 0;
+  if (cudaMemcpyFromSymbolAsync(&w, g_collected_error, sizeof(w), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PKV_ECUDA;
+  *word = w;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_get_last_device_error_bits(pkv_stream_t stream, unsigned int* word) {
+  unsigned w = 0;
+  const int st = collect_error_words(static_cast<cudaStream_t>(stream), true, &w);
+  if (st != PKV_OK) return st;
+  if (word) *word = w;
+  if (w & PKV_DEVERR_WAIT_TIMEOUT) return PKV_ETIMEOUT;
+  return w ? PKV_EDEVICE_CHECK : PKV_OK;
+}
+
+int pkv_get_last_device_error(pkv_stream_t stream) {
+  return pkv_get_last_device_error_bits(stream, nullptr);
+}
+
 int pkv_get_device_error(unsigned int* word, int clear) {
   if (!word) return PKV_EINVAL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ECUDA;

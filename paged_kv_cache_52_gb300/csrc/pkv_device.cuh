@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 namespace pkv {
@@ -106,6 +107,24 @@ static cudaError_t launch_after_previous(void (*kernel)(Params...), dim3 grid, d
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// cudaFuncSetAttribute applies to the current device only, so a kernel's
+// dynamic shared-memory limit is raised once per device: `done` is the
+// calling site's per-device flag array (zero-initialised static storage).
+constexpr int kAttrMaxDevices = 64;
+
+template <typename... Params>
+static cudaError_t set_smem_limit_once(void (*kernel)(Params...), int bytes,
+                                       std::atomic<int>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kAttrMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
+  return e;
 }
 
 // -------------------------------------------------------------------- TMA

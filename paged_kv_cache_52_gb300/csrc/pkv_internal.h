@@ -9,6 +9,16 @@
 
 namespace pkv {
 
+// Every kernel unit keeps its own device error word (an OR of the
+// PKV_DEVERR_* bits its kernels raised); <unit>_error_word gives its device
+// address on the current device.
+cudaError_t append_error_word(unsigned** word);
+cudaError_t decode_error_word(unsigned** word);
+cudaError_t decode_fp8_error_word(unsigned** word);
+cudaError_t prefill_error_word(unsigned** word);
+cudaError_t verify_error_word(unsigned** word);
+cudaError_t probe_error_word(unsigned** word);
+
 // ---- kv_append.cu
 // reject (optional): a device flag set by launch_slot_duplicates; when it is
 // nonzero the append writes nothing.

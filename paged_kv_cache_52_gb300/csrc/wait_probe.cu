@@ -34,6 +34,11 @@ cudaError_t launch_wait_timeout_probe(uint32_t polls, unsigned long long* cycles
 
 uint32_t wait_poll_limit() { return kWaitPollLimit; }
 
+// Device address of this unit's error word on the current device.
+cudaError_t probe_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_probe_error);
+}
+
 unsigned read_probe_error(bool clear) {
   unsigned word = 0;
   if (cudaMemcpyFromSymbol(&word, g_probe_error, sizeof(word)) != cudaSuccess) return ~0u;

@@ -89,6 +89,8 @@ SIGNATURES = {
                                              ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz,
                                              _vp], ctypes.c_int),
     "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_uint), ctypes.c_int], ctypes.c_int),
+    "pkv_get_last_device_error": ([_vp], ctypes.c_int),
+    "pkv_get_last_device_error_bits": ([_vp, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
     "pkv_wait_poll_limit": ([], ctypes.c_uint32),
     "pkv_wait_timeout_probe": ([ctypes.c_uint32, _vp, _vp], ctypes.c_int),
     "pkv_paged_prefill_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -648,6 +650,24 @@ def get_device_error(clear: bool = True) -> int:
     word = ctypes.c_uint()
     _check("pkv_get_device_error", lib.pkv_get_device_error(ctypes.byref(word), int(clear)))
     return word.value
+
+
+PKV_EDEVICE_CHECK = -5
+PKV_ETIMEOUT = -6
+
+
+def get_last_device_error(stream: Optional[torch.cuda.Stream] = None) -> tuple[int, int]:
+    """Stream-ordered checked-mode status (``pkv_get_last_device_error_bits``):
+    waits for the work queued on ``stream`` (torch's current stream by
+    default), takes and clears the device error words, and returns
+    ``(status, bits)`` with status PKV_OK, PKV_ETIMEOUT or PKV_EDEVICE_CHECK.
+    Raises PagedKVError only when the query itself fails."""
+    st_ptr = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    word = ctypes.c_uint()
+    status = lib.pkv_get_last_device_error_bits(ctypes.c_void_p(st_ptr), ctypes.byref(word))
+    if status not in (PKV_OK, PKV_ETIMEOUT, PKV_EDEVICE_CHECK):
+        _check("pkv_get_last_device_error_bits", status)
+    return status, word.value
 
 
 def wait_timeout_probe(polls: int, device=None) -> int:

@@ -112,9 +112,16 @@ def test_bad_query_range_is_flagged(pk):
                                lens, True, w.scale, out=out, max_q_len=8)
     assert pk.get_device_error(clear=True) & 0x10
     assert torch.all(out[8:] == 0)    # the bad sequence is skipped
+    assert torch.any(out[:8] != 0)    # the good one is computed
+    # chunks of 8 with max_q_len 4: both sequences are rejected whole (no row
+    # is written), and the stream-ordered query reports a failed check
+    out.zero_()
     pk.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache, w.prefill_tables,
                                w.prefill_lens, True, w.scale, out=out, max_q_len=4)
-    assert pk.get_device_error(clear=True) & 0x10
+    status, bits = pk.get_last_device_error()
+    assert status == pk.PKV_EDEVICE_CHECK and bits & 0x10
+    assert torch.all(out == 0)
+    assert pk.get_last_device_error() == (0, 0)
 
 
 def test_full_mixed_step_sampled(pk):

@@ -29,6 +29,11 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(pk):
     long_ = pk.wait_timeout_probe(1 << 14)
     assert pk.get_device_error(clear=True) == WAIT_TIMEOUT
     assert 0 < short < long_
+    # the same timeout through the stream-ordered query: PKV_ETIMEOUT
+    pk.wait_timeout_probe(1 << 10)
+    status, bits = pk.get_last_device_error()
+    assert status == pk.PKV_ETIMEOUT and bits == WAIT_TIMEOUT
+    assert pk.get_last_device_error() == (0, 0)
     # the context is intact after the timeouts
     w = wl.make_decode_workload(wl.TINY)
     ref = DecodeStepOracle(w, range(w.num_seqs)).output()

@@ -60,12 +60,17 @@ def test_noalloc_matches_regular_entry_point_twice(pk, spec, lens, pb):
     assert parts > 1 and 0 < need <= pk.lib.pkv_noalloc_scratch_bytes()
     ref = pk.paged_decode_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,
                                     max_context_len=max_len, partition_blocks=pb)
-    outs = []
-    for _ in range(2):                                        # two calls in a row
-        out = torch.full_like(ref, float("nan"))
-        assert _noalloc_call(pk, w, kc, vc, out, max_len, pb) == 0
-        outs.append(out)
+    outs = [torch.full_like(ref, float("nan")) for _ in range(4)]
+    assert _noalloc_call(pk, w, kc, vc, outs[0], max_len, pb) == 0
     torch.cuda.synchronize()
+    # after the first call (which loads the kernels and looks up the scratch
+    # address), further calls take no device memory at all
+    free_before, _ = torch.cuda.mem_get_info()
+    for out in outs[1:]:                                      # more calls in a row
+        assert _noalloc_call(pk, w, kc, vc, out, max_len, pb) == 0
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
     for out in outs:
         assert_attention_close(out.cpu().numpy(), ref.cpu().numpy(), "no-alloc vs regular")
     assert pk.get_device_error() == 0
