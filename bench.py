@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the continuous-batching mixed-step measurement")
     ap.add_argument("--mixed-steps", type=int, default=30)
+    ap.add_argument("--config-cpu-seconds", type=float, default=8.0,
+                    help="wall-time budget of the CPU oracle sample of each other config "
+                         "(7B-MHA, 128K) and of the mixed step; 0 skips them")
     ap.add_argument("--only-verify", action="store_true",
                     help="run only the speculative-verification comparison")
     ap.add_argument("--verify-seqs", type=int, default=256,
@@ -190,17 +193,20 @@ def _host_sequence(w, s):
                 v_new=wl.bf16_bits(w.v_new[s:s + 1]))
 
 
-def cpu_oracle_sample(w, budget_s: float):
+def cpu_oracle_sample(w, budget_s: float, seqs=None):
     """Time the CPU oracle, as it stands, on whole sequences of the workload
     (append, then decode) until the wall-time budget is spent.  Returns the
     same metric (KV GB/s) and a description; `cores` is CPU time / wall time
-    of the oracle calls, i.e. the threads it actually kept busy."""
+    of the oracle calls, i.e. the threads it actually kept busy.  `seqs`:
+    the sequences to take, in order (default: all, from the first)."""
     import oracle  # CPU baseline only
 
     row_bytes = 2 * w.kv_heads * w.d_head * 2
     done_bytes, wall, cpu, nseq = 0, 0.0, 0.0, 0
-    s = 0
-    while wall < budget_s and s < w.num_seqs:
+    order = list(range(w.num_seqs)) if seqs is None else list(seqs)
+    for s in order:
+        if wall >= budget_s:
+            break
         h = _host_sequence(w, s)
         c0, t0 = time.process_time(), time.perf_counter()
         kc, vc = oracle.kv_append(h["k_new"], h["v_new"], h["slot"], h["kc"], h["vc"])
@@ -209,14 +215,54 @@ def cpu_oracle_sample(w, budget_s: float):
         cpu += time.process_time() - c0
         done_bytes += h["len"][0] * row_bytes
         nseq += 1
-        s += 1
     value = done_bytes / wall / 1e9 if wall > 0 else None
     cores = max(1, round(cpu / wall)) if wall > 0 else 1
     info = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
             "host_cpus": len(os.sched_getaffinity(0)),
-            "sample": f"append+decode of the first {nseq} of {w.num_seqs} sequences "
+            "sample": f"append+decode of {nseq} of {w.num_seqs} sequences "
                       f"({done_bytes / 1e9:.3f} GB of KV) in {wall:.1f} s, numpy float64"}
     return value, info
+
+
+def cpu_prefill_sample(w, seqs, tiles, budget_s: float):
+    """Time the CPU oracle on query tiles of prefill chunks of a mixed
+    workload: the sequence's pages and its chunk's new rows to the host, the
+    oracle's append, then the oracle's causal attention of query tokens
+    [a, b) over the first context_len - n + b keys (those tokens are the last
+    b - a positions there).  Returns (GFLOP/s, wall s, flops) with the same
+    flop count as the GPU figure (4 d Hq per visible key per query row)."""
+    import oracle  # CPU baseline only
+
+    chunk = w.meta["chunk"]
+    qs = w.q_start.cpu().tolist()
+    hq, d = w.q_prefill.shape[1], w.q_prefill.shape[2]
+    flops, wall = 0, 0.0
+    for s in seqs:
+        L = int(w.meta["prefill_lens"][s])
+        nb = wl.blocks_for(L)
+        ids = w.prefill_tables[s, :nb].to(torch.int64)
+        kc = wl.bf16_bits(w.k_cache.index_select(0, ids))
+        vc = wl.bf16_bits(w.v_cache.index_select(0, ids))
+        rows = torch.arange(qs[s], qs[s + 1], device=w.q_prefill.device)
+        phys = ids.cpu().tolist()
+        slots = [phys.index(int(x) // wl.BLOCK_SIZE) * wl.BLOCK_SIZE + int(x) % wl.BLOCK_SIZE
+                 for x in w.slot_mapping[qs[s]:qs[s + 1]].cpu().tolist()]
+        kn = wl.bf16_bits(w.k_new.index_select(0, rows))
+        vn = wl.bf16_bits(w.v_new.index_select(0, rows))
+        q = wl.bf16_bits(w.q_prefill.index_select(0, rows))
+        t0 = time.perf_counter()
+        kc2, vc2 = oracle.kv_append(kn, vn, slots, kc, vc)
+        table = list(range(nb))
+        for a, b in tiles:
+            ctx = L - chunk + b
+            kk = oracle.gather_sequence_kv(kc2, table, ctx)
+            vv = oracle.gather_sequence_kv(vc2, table, ctx)
+            oracle.attention(q[a:b], kk, vv, w.scale, causal=True)
+            flops += 4 * d * hq * sum(L - chunk + i + 1 for i in range(a, b))
+        wall += time.perf_counter() - t0
+        if wall >= budget_s:
+            break
+    return flops / wall / 1e9, wall, flops
 
 
 def read_traffic(kernel_tag: str):
@@ -463,6 +509,29 @@ def run_mixed(args, dev, pagedkv, E):
     tflops_peak = float(peaks.get("bf16_tflops", 1900.0))
     hbm, _ = measured_peak()
     t_roof = (dec_unique + pre_kv) / (hbm * 1e9) + flops / (tflops_peak * 1e12)
+    cpu = None
+    if getattr(args, "mixed_cpu_seconds", 0) > 0:
+        # the oracle on a sample of the same step: whole decode sequences
+        # (append + decode), and the first, a middle and the last 128-row
+        # query tile of prefill chunks; the full step's CPU time is
+        # extrapolated from the two rates (KV bytes and FLOPs)
+        P = len(plens)
+        dview = wl.DecodeWorkload("mixed decodes", w.q_decode, kc, vc, w.k_new[P * chunk:],
+                                  w.v_new[P * chunk:], w.slot_mapping[P * chunk:],
+                                  w.decode_tables, w.decode_lens, w.scale,
+                                  {"lens": dlens})
+        dorder = sorted(range(len(dlens)), key=lambda i: (i % 8, i))
+        dec_gbps, dinfo = cpu_oracle_sample(dview, args.mixed_cpu_seconds / 2, dorder)
+        tiles = [(0, 16), (chunk // 2 - 16, chunk // 2), (chunk - 16, chunk)]
+        pre_gflops, pwall, pflops = cpu_prefill_sample(w, range(P), tiles,
+                                                       args.mixed_cpu_seconds / 2)
+        cpu_ms = (dec_logical / (dec_gbps * 1e9) + flops / (pre_gflops * 1e9)) * 1e3
+        cpu = {"value": round(cpu_ms, 1), "unit": "ms per step (extrapolated)",
+               "cores": dinfo["cores"], "kind": "oracle",
+               "decode_GBps": round(dec_gbps, 4), "prefill_GFLOPs": round(pre_gflops, 3),
+               "sample": f"{dinfo['sample']}; prefill: 3 query tiles (16 tokens x 64 heads) "
+                         f"of chunks until {args.mixed_cpu_seconds / 2:.0f} s "
+                         f"({pflops / 1e9:.1f} GFLOP in {pwall:.1f} s), numpy float64"}
     return {
         "workload": w.name, "steps": K, "ms_per_step": round(t_step, 4),
         "append_ms": round(t_app, 4), "prefill_ms": round(t_pre, 4),
@@ -495,6 +564,7 @@ def run_mixed(args, dev, pagedkv, E):
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),
         "fp8_cache": fp8_step,
+        "cpu_baseline": cpu,
     }
 
 
@@ -543,9 +613,11 @@ def run_fp8(w, dev, pagedkv, E, args, peak):
             "gpu_launches": K * (2 + (1 if ws is not None else 0))}
 
 
-def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps=50):
+def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps=50,
+                       cpu_seconds=0.0):
     """The other full-size decode workloads (7B-MHA, 128K long context): one
-    step = append + split-K decode, KV GB/s and fraction of the HBM peak."""
+    step = append + split-K decode, KV GB/s and fraction of the HBM peak, and
+    (cpu_seconds > 0) the CPU oracle on whole sequences of the same workload."""
     res = {}
     for name in names:
         spec = wl.DECODE_SPECS[name]
@@ -587,6 +659,11 @@ def run_decode_configs(dev, pagedkv, E, peak, names=("mha7b", "long128k"), steps
                      "decode_frac_of_hbm": round(kv / (t_dec / 1e3) / 1e9 / peak, 4),
                      "decode_tokens_per_s": round(S / (t_step / 1e3), 1),
                      "partition_blocks": plan[0], "num_parts": plan[1]}
+        if cpu_seconds > 0:
+            # spread over the batch: first, middle and last sequences first
+            order = sorted(range(S), key=lambda i: (i % max(1, S // 4), i))
+            _, info = cpu_oracle_sample(w, cpu_seconds, order)
+            res[name]["cpu_baseline"] = info
         del w, ws, out
         torch.cuda.empty_cache()
     return res
@@ -631,15 +708,18 @@ def run_append_probe(dev, pagedkv, E, peak, tokens=262144, steps=20):
     return res
 
 
-def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
-    """Launch-bound small-batch decode steps of the 70B-GQA layer shape:
-    per-step time of eager calls vs replay of a CUDA graph captured for the
-    batch's bucket (append + split-K decode)."""
+def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_len=512):
+    """Small-batch decode steps of the 70B-GQA layer shape: per-step time of
+    eager calls vs replay of a CUDA graph captured for the batch's bucket
+    (append + split-K decode).  Batches of 1-4 sequences have short contexts
+    (`short_len` tokens each), where launch latency dominates; 8 and 64 draw
+    their contexts from the 70B-GQA recipe."""
     from paged_kv_cache_52_gb300.graphs import DecodeGraphRunner
     res = {}
     for bsz in batches:
+        lens = [short_len] * bsz if bsz <= 4 else None
         w = wl.make_decode_workload(wl.GQA_70B, device=dev, gen_device=dev,
-                                    num_seqs_override=bsz)
+                                    num_seqs_override=bsz, lens_override=lens)
         max_len = max(w.meta["lens"])
         ws = pagedkv.decode_workspace(bsz, w.q_heads, w.kv_heads, w.d_head, max_len, dev)
         out = torch.empty(w.q.shape, dtype=torch.float32, device=dev)
@@ -668,6 +748,7 @@ def run_small_batch(dev, pagedkv, E, batches=(8, 64), steps=200):
             torch.cuda.synchronize()
             times[name] = s0.elapsed_time(s1) / steps * 1e3
         res[str(bsz)] = {"eager_us": round(times["eager"], 2), "graph_us": round(times["graph"], 2),
+                         "context_lens": "512 each" if lens else "U[1024, 8192]",
                          "kv_bytes": w.kv_bytes(),
                          "graph_GBps": round(w.kv_bytes() / (times["graph"] / 1e6) / 1e9, 1)}
         del w, runner, b
@@ -910,6 +991,10 @@ def run_ours(args):
         "data": "synthetic: seeded randn bf16 K/V/q, random block tables (no dataset)",
         "config": workload_config(w, spec, plan),
         "decode_tokens_per_s": round(world * S * K / (total_ms / 1e3), 1),
+        # one token per sequence through 80 such attention layers; excludes
+        # the weights' matmuls and every other part of a real model step
+        "decode_tokens_per_s_80_layers_attention_only": round(
+            world * S * K / (80 * total_ms / 1e3), 1),
         "decode_ms": round(decode_ms, 4), "append_ms": round(append_ms, 4),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"kernel": "paged_decode (split-K kernel + LSE merge, one call)",
@@ -929,21 +1014,65 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     line["fp8_cache"] = run_fp8(w, dev, pagedkv, E, args, peak)
+    cpu_here = rank == 0 and world == 1 and not args.no_cpu_baseline
+    args.mixed_cpu_seconds = args.config_cpu_seconds if cpu_here else 0.0
     if not args.no_mixed:
-        line["other_decode_workloads"] = run_decode_configs(dev, pagedkv, E, peak)
+        line["other_decode_workloads"] = run_decode_configs(
+            dev, pagedkv, E, peak, cpu_seconds=args.mixed_cpu_seconds)
         line["append_probe"] = run_append_probe(dev, pagedkv, E, peak)
     if not args.no_mixed:
         del host, devb
         line["mixed_step"] = run_mixed(args, dev, pagedkv, E)
         line["small_batch_decode"] = run_small_batch(dev, pagedkv, E)
         line["speculative_verify"] = run_verify(dev, pagedkv, E, peak)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if cpu_here:
         _, info = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = info
+    line["per_config"] = per_config_summary(line, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def per_config_summary(line, peak):
+    """A compact per-config digest, printed last so that a reader keeping only
+    the end of the JSON line still sees every workload's headline numbers and
+    its CPU oracle baseline."""
+    def r(x, n=1):
+        return None if x is None else round(x, n)
+
+    def cpu_of(d):
+        c = d.get("cpu_baseline") if d else None
+        return None if not c else r(c.get("value"), 4)
+
+    out = {"peak_GBps": peak,
+           "gqa70b": {"step_GBps": line.get("value"), "decode_frac": line["roofline"]["frac"],
+                      "tok_s": line.get("decode_tokens_per_s"),
+                      "tok_s_80_layers_attn_only":
+                          line.get("decode_tokens_per_s_80_layers_attention_only"),
+                      "cpu_GBps": cpu_of(line)}}
+    for name, d in (line.get("other_decode_workloads") or {}).items():
+        out[name] = {"decode_GBps": d.get("decode_GBps"), "decode_frac": d.get("decode_frac_of_hbm"),
+                     "tok_s": d.get("decode_tokens_per_s"), "cpu_GBps": cpu_of(d)}
+    fp8 = line.get("fp8_cache")
+    if fp8:
+        out["gqa70b_fp8"] = {"decode_GBps": fp8.get("decode_GBps"),
+                             "decode_frac": fp8.get("decode_frac_of_hbm")}
+    m = line.get("mixed_step")
+    if m:
+        out["mixed"] = {"ms": m["ms_per_step"], "roofline_ms": m["roofline_step_ms"],
+                        "prefill_frac": m["prefill"]["frac"],
+                        "plain_prefill_frac": m["prefill"]["plain_entry_point_frac"],
+                        "decode_unique_GBps": m["decode"]["unique_GBps"],
+                        "sm_split_ms": m["two_streams_sm_split"]["ms_per_step"],
+                        "cpu_ms": cpu_of(m)}
+        if "unified" in m:
+            out["mixed"]["unified_ms"] = m["unified"]["ms_per_step"]
+    sb = line.get("small_batch_decode")
+    if sb:
+        out["small_batch_us"] = {k: [v["eager_us"], v["graph_us"]] for k, v in sb.items()}
+    return out
 
 
 def run_reference(args):

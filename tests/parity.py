@@ -124,6 +124,23 @@ class PrefillStepOracle:
         return oracle.paged_prefill_attention(self.q, self.q_start, kc, vc, self.tables, self.lens,
                                               self.causal, self.scale)
 
+    def token_range_output(self, si, a, b):
+        """Oracle rows of queries [a, b) of local sequence si's chunk.  Those
+        queries are the last b - a positions of the first context_len - n + b
+        keys, so they are a causal chunk of that shorter context."""
+        kc, vc = self._cache_once()
+        n = int(self.q_start[si + 1] - self.q_start[si])
+        ctx = self.lens[si] - n + b if self.causal else self.lens[si]
+        kk = oracle.gather_sequence_kv(kc, self.tables[si], ctx)
+        vv = oracle.gather_sequence_kv(vc, self.tables[si], ctx)
+        q0 = int(self.q_start[si])
+        return oracle.attention(self.q[q0 + a:q0 + b], kk, vv, self.scale, causal=self.causal)
+
+    def _cache_once(self):
+        if not hasattr(self, "_cached"):
+            self._cached = self.cache()
+        return self._cached
+
     def rows_output(self, picks):
         """Oracle rows for (local sequence index, query index in its chunk)
         pairs: query i of a causal chunk of n equals a decode over the first

@@ -113,13 +113,13 @@ def test_fp8_decode_outliers_small(pk):
     assert_attention_close(out.cpu().numpy(), ref, "fp8 outliers")
 
 
-def test_fp8_full_size_70b_gqa_sampled(pk):
+def test_fp8_full_size_70b_gqa_whole_batch(pk):
     w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV)
     ks, vs = wl.FP8_SCALES["gqa70b"]
     kc8, vc8 = wl.fp8_pools(w, ks, vs)
-    seqs = [0, 77, 255]
+    seqs = list(range(w.num_seqs))
     ref = _fp8_oracle(w, kc8, vc8, ks, vs, seqs)
     out, _, _ = _step(pk, w, kc8, vc8, ks, vs)
-    assert_attention_close(out[seqs].cpu().numpy(), ref, "fp8 70B full")
+    assert_attention_close(out.cpu().numpy(), ref, "fp8 70B full")
     assert torch.isfinite(out).all()
     assert pk.get_device_error() == 0

@@ -124,28 +124,40 @@ def test_bad_query_range_is_flagged(pk):
     assert pk.get_last_device_error() == (0, 0)
 
 
-def test_full_mixed_step_sampled(pk):
+# query-token ranges of the first, a middle and the last 128-row tile (16
+# tokens x the 8 heads of the group) of a 512-token chunk
+MIXED_TILES = [(0, 16), (240, 256), (496, 512)]
+
+
+def mixed_prefill_tiles_close(out, w, what):
+    """The first, a middle and the last query tile of every chunk of the
+    mixed step against the oracle."""
+    orc = PrefillStepOracle(w, range(len(w.meta["prefill_lens"])))
+    qs = w.q_start.cpu().numpy()
+    for si in range(len(orc.seqs)):
+        for a, b in MIXED_TILES:
+            ref = orc.token_range_output(si, a, b)
+            got = out[int(qs[si]) + a:int(qs[si]) + b].cpu().numpy()
+            assert_attention_close(got, ref, f"{what}: chunk {si} tokens [{a}, {b})")
+
+
+def test_full_mixed_step(pk):
     """The 70B-GQA continuous-batching step at full size: append 8 x 512 + 248
-    tokens, prefill the 8 chunks, decode the 248 sequences; sampled rows."""
+    tokens, prefill the 8 chunks, decode the 248 sequences.  Every decode and
+    three query tiles of every chunk are compared with the oracle."""
     w = wl.make_mixed_workload(device=DEV, gen_device=DEV)
-    pre = PrefillStepOracle(w, [0, 7])
     P = 8 * 512
     dw = wl.DecodeWorkload("mixed decodes", w.q_decode, w.k_cache, w.v_cache, w.k_new[P:],
                            w.v_new[P:], w.slot_mapping[P:], w.decode_tables, w.decode_lens,
                            w.scale, {"lens": w.meta["decode_lens"]})
-    dsamp = [0, 100, 247]
-    dor = DecodeStepOracle(dw, dsamp)
+    dor = DecodeStepOracle(dw, range(dw.q.shape[0]))
     out, kc, vc = run_prefill(pk, w, max_q_len=512)
     dec = pk.paged_decode_attention(w.q_decode, kc, vc, w.decode_tables, w.decode_lens, w.scale,
                                     max_context_len=max(w.meta["decode_lens"]))
     torch.cuda.synchronize()
-    picks = [(0, 0), (0, 1), (0, 255), (0, 511), (1, 0), (1, 300), (1, 511)]
-    ref_rows = pre.rows_output(picks)
-    qs = w.q_start.cpu().numpy()
-    got_rows = np.stack([out[int(qs[[0, 7][si]]) + i].cpu().numpy() for si, i in picks])
-    assert_attention_close(got_rows, ref_rows, "mixed prefill rows")
     assert torch.isfinite(out).all()
-    assert_attention_close(dec[dsamp].cpu().numpy(), dor.output(), "mixed decodes")
+    mixed_prefill_tiles_close(out, w, "mixed prefill (bf16 hi + lo P)")  # w's pools are unchanged
+    assert_attention_close(dec.cpu().numpy(), dor.output(), "mixed decodes")
     assert pk.get_device_error() == 0
 
 
