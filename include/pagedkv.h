@@ -129,18 +129,47 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
                                   pkv_stream_t stream);
 
 /*
+ * How the split-K decode divides each sequence's pages (partition_blocks):
+ *   > 0 (1..1024)        uniform partitions of that many 16-token blocks;
+ *   PKV_SPLIT_UNIFORM    uniform partitions sized by the library from the
+ *                        longest context and the device's SM count;
+ *   PKV_SPLIT_BALANCED   a length-balanced work list (bf16 decode, at most
+ *                        512 sequences): the kernel reads the actual
+ *                        context lengths and cuts every (sequence, KV head)
+ *                        pair's pages into runs of near-equal size, about
+ *                        one wave of CTAs in all ("第 10 讲：推理（Inference）",
+ *                        "核心概念与定义": FlashDecoding's split of long
+ *                        contexts, here balanced on the real lengths);
+ *   0                    the library's choice: the balanced list when the
+ *                        batch has at most 2 x SMs (sequence, KV head)
+ *                        pairs and the workspace holds it, else the
+ *                        library's uniform partitions.
+ * The FP8 decode, the verification decode and the shared-prefix decode
+ * treat every value <= 0 as PKV_SPLIT_UNIFORM.
+ */
+#define PKV_SPLIT_BALANCED (-1)
+#define PKV_SPLIT_UNIFORM (-2)
+
+/*
  * Decode plan: the partition size (in 16-token blocks) and the number of
- * partitions the split-K decode uses for these sizes, and the workspace it
- * needs.  partition_blocks <= 0 lets the library choose from the longest
- * context and the device's SM count; a positive value (1..1024) forces it.
- * The plan depends on the current device.  Returns PKV_OK or PKV_EINVAL /
+ * partitions of the uniform split for these sizes, and the workspace the
+ * bf16 decode needs with this partition_blocks (for the balanced list too,
+ * when it is taken; this also covers the FP8 decode's uniform split).  The
+ * plan depends on the current device.  Returns PKV_OK or PKV_EINVAL /
  * PKV_EUNSUPPORTED.
  */
 PKV_API int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
                     int partition_blocks, int* out_partition_blocks, int* out_num_parts,
                     size_t* out_workspace_bytes);
 
-/* Workspace bytes pkv_paged_decode_attention needs (0 when one partition suffices). */
+/* 1 when the bf16 decode with this partition_blocks takes the length-balanced
+ * list (given a workspace of pkv_decode_plan's size), 0 when it takes the
+ * uniform split, or a negative pkv_status. */
+PKV_API int pkv_decode_plan_uses_list(int num_seqs, int q_heads, int kv_heads, int d_head,
+                                      int max_context_len, int partition_blocks);
+
+/* Workspace bytes pkv_paged_decode_attention needs with the library's choice
+ * (0 when neither a list nor more than one partition is needed). */
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,
                                   int max_context_len);
 
@@ -167,7 +196,10 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_head
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
  *                  bytes, or NULL when that is 0; contents need no
  *                  initialisation and are overwritten.  Calls that share a
- *                  workspace must be ordered on the GPU.
+ *                  workspace must be ordered on the GPU.  With a smaller
+ *                  workspace (or NULL) the library's choice falls back from
+ *                  the balanced list to the uniform split when the latter's
+ *                  own workspace fits.
  * Query head h uses KV head h / (q_heads / kv_heads).  A sequence with
  * context_len 0 yields zeros.  Block ids outside the pool read as zero rows
  * and set PKV_DEVERR_BAD_BLOCK_ID; context_len beyond 16*max_blocks_per_seq
@@ -181,14 +213,38 @@ PKV_API int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads,
                                float* out, void* workspace, size_t ws_bytes,
                                pkv_stream_t stream);
 
-/* Same as pkv_paged_decode_attention with an explicit partition size
- * (partition_blocks as in pkv_decode_plan; <= 0 = library choice). */
+/* Same as pkv_paged_decode_attention with an explicit split choice
+ * (partition_blocks: a size in blocks, PKV_SPLIT_UNIFORM, PKV_SPLIT_BALANCED
+ * or 0 = library choice; see above). */
 PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
                                   const void* v_cache, pkv_cache_desc cache,
                                   const int32_t* block_tables, int max_blocks_per_seq,
                                   const int32_t* context_lens, int max_context_len, float scale,
                                   float* out, void* workspace, size_t ws_bytes,
                                   int partition_blocks, pkv_stream_t stream);
+
+/*
+ * pkv_paged_decode_attention_limited -- the decode on at most max_ctas CTAs,
+ * leaving the other SMs to kernels on other streams (the continuous-batching
+ * step runs a chunked prefill beside the decodes: nano-vLLM page, section
+ * "Traitement par lots continu").  The length-balanced list of
+ * PKV_SPLIT_BALANCED with about four runs per CTA; each CTA takes every
+ * max_ctas-th run.  At most 512 sequences (PKV_EUNSUPPORTED beyond).
+ * workspace: >= pkv_decode_limited_workspace_bytes(..., max_ctas) bytes,
+ * 256-byte aligned (PKV_ENOMEM if smaller).  max_ctas >= 1 (PKV_EINVAL
+ * otherwise).  Other arguments and errors are those of
+ * pkv_paged_decode_attention.
+ */
+PKV_API size_t pkv_decode_limited_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
+                                                  int d_head, int max_context_len, int max_ctas);
+PKV_API int pkv_paged_decode_attention_limited(const void* q, int num_seqs, int q_heads,
+                                               const void* k_cache, const void* v_cache,
+                                               pkv_cache_desc cache, const int32_t* block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t* context_lens, int max_context_len,
+                                               float scale, float* out, int max_ctas,
+                                               void* workspace, size_t ws_bytes,
+                                               pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention_bf16out -- pkv_paged_decode_attention_ex with a

@@ -90,8 +90,17 @@ def kv_append_fp8(k_new, v_new, slot_mapping, k_cache_bits, v_cache_bits, k_scal
                      slot_mapping, k_cache_bits, v_cache_bits)
 
 
+# e4m3_bits_to_f64 evaluated once for each of the 256 codes: dequantizing a
+# pool then indexes this table, which gives the same values as applying the
+# function element by element, at a fraction of the cost on large pools.
+_E4M3_VALUES = e4m3_bits_to_f64(np.arange(256, dtype=np.uint8))
+
+
 def dequantize(cache_bits, scale) -> np.ndarray:
-    return e4m3_bits_to_f64(cache_bits) * float(np.float32(scale))
+    bits = np.asarray(cache_bits)
+    if bits.dtype != np.uint8:
+        raise TypeError(f"expected uint8 e4m3 codes, got {bits.dtype}")
+    return _E4M3_VALUES[bits] * float(np.float32(scale))
 
 
 def paged_decode_attention_fp8(q, k_cache_bits, v_cache_bits, block_tables, context_lens,

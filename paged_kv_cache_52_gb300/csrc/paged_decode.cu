@@ -61,40 +61,25 @@ struct DecodeTile {
   static constexpr int kSmemBytes = kIdsOffset + kMaxPartitionBlocks * 4 + 1024;  // +align slack
 };
 
+// One run of `nb_local` pages of sequence `seq`, KV head `kvh`, starting at
+// block b0, for the G query heads of the group: softmax(q K^T * scale) V over
+// the run's keys below `len`.  final_out: the run is the sequence's whole
+// context and writes the output; otherwise it writes its normalised partial
+// output and log2-sum-exp at partial row pbase + head * pstride.
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  griddep_wait();  // inputs may have been written by the previous kernel in the stream
+__device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                           const DecodeParams& p, uint8_t* smem, int seq, int kvh,
+                                           int b0, int nb_local, int len, bool final_out,
+                                           size_t pbase, int pstride) {
   using T = DecodeTile<D>;
   constexpr bool kTwoRows = (G > 8);  // heads gid+8 are real rows too
   constexpr int KSTEPS = D / 16;       // k-steps of QK^T
   constexpr int NT = D / 8;            // n-tiles of the output
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int32_t* ids = reinterpret_cast<int32_t*>(smem + T::kIdsOffset);
-
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  const int pair = blockIdx.x;
-  const int part = blockIdx.y;
-  const int seq = pair / p.kv_heads;
-  const int kvh = pair - seq * p.kv_heads;
-
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
-  const int len = sp.len;
-  if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
-  const int nparts_s = span_parts(sp, p);
-  if (part >= nparts_s) return;
   const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
-  if (sp.count == 0) {  // empty context: zeros
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p, row0 * D + i, 0.f);
-    return;
-  }
-  const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
-  const int nb_local = min(sp.first + sp.count - b0, p.partition_blocks);
 
   // Stage this partition's block ids; ids outside the pool are flagged (their
   // TMA boxes are out of bounds and read as zeros).
@@ -343,7 +328,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   __syncthreads();
 
-  const bool final_out = (nparts_s == 1) && !p.force_partials;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int row = idx / D, col = idx - row * D;
     float big = -INFINITY;
@@ -364,11 +348,250 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (final_out) {
       store_out(p, (row0 + row) * D + col, res);
     } else {
-      const size_t prow = (row0 + row) * p.num_parts + part;
+      const size_t prow = pbase + size_t(row) * pstride;
       p.part_o[prow * D + col] = res;
       if (col == 0) p.part_lse[prow] = big + __log2f(tot);
     }
   }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int pair = blockIdx.x;
+  const int part = blockIdx.y;
+  const int seq = pair / p.kv_heads;
+  const int kvh = pair - seq * p.kv_heads;
+
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
+  const int nparts_s = span_parts(sp, p);
+  if (part >= nparts_s) return;
+  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;  // first output row
+  if (sp.count == 0) {  // empty context: zeros
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p, row0 * D + i, 0.f);
+    return;
+  }
+  const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
+  const int nb_local = min(sp.first + sp.count - b0, p.partition_blocks);
+  const bool final_out = (nparts_s == 1) && !p.force_partials;
+  decode_run<D, G>(tmap_k, tmap_v, p, smem, seq, kvh, b0, nb_local, sp.len, final_out,
+                   row0 * p.num_parts + part, p.num_parts);
+}
+
+// ---------------------------------------------------------------------------
+// Length-balanced work list.  With fewer (sequence, KV head) pairs than CTA
+// slots, uniform partitions sized from the longest context leave the waves
+// unbalanced: how the real lengths fall into partitions decides the tail.
+// Here every CTA derives the same plan from the context lengths on the device:
+//   n_s  pages of sequence s (clamped to the block table and the host bound),
+//   T    = sum_s n_s,
+//   c    = clamp(ceil(Hkv T / target), min_run, kMaxPartitionBlocks) pages,
+//   k_s  = max(1, ceil(n_s / c)) runs per (s, KV head), of near-equal size
+//          (run r covers blocks [r n_s / k_s, (r + 1) n_s / k_s)),
+// items numbered sequence-major, then KV head, then run; CTA i takes item i.
+// Every run is at most c pages, so a grid of `target` CTA slots finishes in
+// one even wave.  A pair with one run writes the output; otherwise its runs
+// write partials at rows item * G + head and the list merge combines them.
+// Block 0 stores the per-sequence first items (seq_item_base) for the merge.
+// ---------------------------------------------------------------------------
+constexpr int kListMaxSeqs = 512;
+constexpr int kListPerThread = kListMaxSeqs / (kDecodeWarps * 32);
+
+template <int D>
+struct DecodeListTile {
+  static constexpr int kPlanOffset = DecodeTile<D>::kIdsOffset + kMaxPartitionBlocks * 4;
+  static constexpr int kSmemBytes = kPlanOffset + (kListMaxSeqs + 1) * 4 + 1024;  // +align slack
+};
+
+struct DecodeListParams {
+  int32_t* seq_item_base;  // [num_seqs + 1]: first item of each sequence, then the item count
+  int num_seqs;            // <= kListMaxSeqs
+  int target_items;        // runs aimed at: CTA slots of one wave
+  int min_run;             // pages
+  int max_blocks;          // page bound per sequence (block table and host max_context_len)
+};
+
+// Pages of a sequence in the list plan: its context clamped to max_blocks.
+__device__ __forceinline__ int list_pages(int len, int max_blocks) {
+  int n = len <= 0 ? 0 : (len + kBlockTokens - 1) / kBlockTokens;
+  return n < max_blocks ? n : max_blocks;
+}
+
+// Run `item` of the list plan in `base` (every CTA holds the same plan).
+template <int D, int G>
+__device__ __forceinline__ void list_item(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                          const DecodeParams& p, const DecodeListParams& lp,
+                                          uint8_t* smem, const int32_t* base, int item) {
+  constexpr int kThreads = kDecodeWarps * 32;
+  const int S = lp.num_seqs;
+  int lo = 0, hi = S - 1;  // the last sequence whose first item is <= item
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  const int seq = lo;
+  const int runs = (base[seq + 1] - base[seq]) / p.kv_heads;
+  const int local = item - base[seq];
+  const int kvh = local / runs;
+  const int run = local - kvh * runs;
+  const int raw_len = __ldg(p.context_lens + seq);
+  const int ns = list_pages(raw_len, lp.max_blocks);
+  int len = raw_len < 0 ? 0 : raw_len;
+  if (len > ns * kBlockTokens) len = ns * kBlockTokens;
+  if (len != raw_len && kvh == 0 && run == 0 && threadIdx.x == 0)
+    atomicOr(&g_decode_error, kErrBadContext);
+  const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;
+  if (ns == 0) {  // empty context: zeros (one run)
+    for (int i = threadIdx.x; i < G * D; i += kThreads) store_out(p, row0 * D + i, 0.f);
+    return;
+  }
+  const int b0 = int((long long)run * ns / runs);
+  const int b1 = int((long long)(run + 1) * ns / runs);
+  decode_run<D, G>(tmap_k, tmap_v, p, smem, seq, kvh, b0, b1 - b0, len, runs == 1,
+                   size_t(item) * G, 1);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+paged_decode_list_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p,
+                         const DecodeListParams lp) {
+  griddep_wait();  // inputs may have been written by the previous kernel in the stream
+  constexpr int kThreads = kDecodeWarps * 32;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int32_t* base = reinterpret_cast<int32_t*>(smem + DecodeListTile<D>::kPlanOffset);
+  __shared__ long long red_total[kDecodeWarps];
+  __shared__ int red_scan[kDecodeWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int S = lp.num_seqs;
+
+  // 1. pages per sequence and their total (thread t owns sequences
+  //    t * kListPerThread ..., so the scan below is in sequence order)
+  int n[kListPerThread];
+  long long mine = 0;
+#pragma unroll
+  for (int j = 0; j < kListPerThread; ++j) {
+    const int s = threadIdx.x * kListPerThread + j;
+    n[j] = s < S ? list_pages(__ldg(p.context_lens + s), lp.max_blocks) : 0;
+    mine += n[j];
+  }
+  long long tot = mine;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane == 0) red_total[warp] = tot;
+  __syncthreads();
+  long long pages = 0;
+#pragma unroll
+  for (int w = 0; w < kDecodeWarps; ++w) pages += red_total[w];
+
+  // 2. run size and runs per pair
+  long long c = (pages * p.kv_heads + lp.target_items - 1) / lp.target_items;
+  if (c < lp.min_run) c = lp.min_run;
+  if (c > kMaxPartitionBlocks) c = kMaxPartitionBlocks;
+  int k[kListPerThread];
+  int kmine = 0;
+#pragma unroll
+  for (int j = 0; j < kListPerThread; ++j) {
+    const int s = threadIdx.x * kListPerThread + j;
+    k[j] = s < S ? (n[j] > 0 ? int((n[j] + c - 1) / c) : 1) : 0;
+    kmine += k[j];
+  }
+
+  // 3. exclusive scan of the runs per sequence over the CTA
+  int incl = kmine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) red_scan[warp] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kDecodeWarps; ++w) {
+    before += w < warp ? red_scan[w] : 0;
+    all += red_scan[w];
+  }
+  int run_base = before + incl - kmine;
+#pragma unroll
+  for (int j = 0; j < kListPerThread; ++j) {
+    const int s = threadIdx.x * kListPerThread + j;
+    if (s < S) base[s] = run_base * p.kv_heads;
+    run_base += k[j];
+  }
+  if (threadIdx.x == 0) base[S] = all * p.kv_heads;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += kThreads) lp.seq_item_base[i] = base[i];
+
+  // 4. this CTA's items: blockIdx.x, then every gridDim.x-th (a grid smaller
+  //    than the item count keeps the decode on at most that many CTAs)
+  for (int item = blockIdx.x; item < base[S]; item += gridDim.x) {
+    if (item != int(blockIdx.x)) {
+      // the previous run is complete: its copies landed and every thread has
+      // left its merge; its barriers are retired before they are set up again
+      if (lane == 0)
+        for (int st = 0; st < kDecodeStages; ++st)
+          mbar_inval(smem_u32(smem + DecodeTile<D>::kBarOffset) + (warp * kDecodeStages + st) * 8);
+      __syncthreads();
+    }
+    list_item<D, G>(tmap_k, tmap_v, p, lp, smem, base, item);
+  }
+}
+
+// The merge of the list's runs: for the row (sequence s, head h), runs
+// r < k_s of pair (s, h / G) hold their normalised output and log2-sum-exp
+// at partial row (seq_item_base[s] + (h / G) k_s + r) G + h % G; the same
+// log-sum-exp merge as paged_decode_merge4_kernel, four dims per thread.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_merge_list_kernel(const DecodeParams p,
+                                                                      const DecodeListParams lp,
+                                                                      long long total_rows) {
+  constexpr int TPR = D / 4;  // threads per row
+  griddep_wait();
+  const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = gtid / TPR;
+  const int c4 = int(gtid - row * TPR);
+  if (row >= total_rows) return;
+  const int seq = int(row / p.q_heads);
+  const int h = int(row - (long long)seq * p.q_heads);
+  const int G = p.q_heads / p.kv_heads;
+  const int kvh = h / G;
+  const int b = __ldg(lp.seq_item_base + seq);
+  const int runs = (__ldg(lp.seq_item_base + seq + 1) - b) / p.kv_heads;
+  if (runs <= 1) return;  // written by the decode kernel
+  const size_t r0 = size_t(b + kvh * runs) * G + (h - kvh * G);
+  float big = -INFINITY;
+  for (int r = 0; r < runs; ++r) big = fmaxf(big, __ldg(p.part_lse + r0 + size_t(r) * G));
+  float tot = 0.f;
+  float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int r = 0; r < runs; ++r) {
+    const size_t pr = r0 + size_t(r) * G;
+    const float w = ex2(__ldg(p.part_lse + pr) - big);
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p.part_o + pr * D) + c4);
+    tot += w;
+    val.x += w * x.x;
+    val.y += w * x.y;
+    val.z += w * x.z;
+    val.w += w * x.w;
+  }
+  const float4 res = tot > 0.f ? make_float4(val.x / tot, val.y / tot, val.z / tot, val.w / tot)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  const size_t o = size_t(row) * D + size_t(c4) * 4;
+  store_out(p, o, res.x);
+  store_out(p, o + 1, res.y);
+  store_out(p, o + 2, res.z);
+  store_out(p, o + 3, res.w);
 }
 
 // Log-sum-exp merge of the partitions of one (sequence, query head): with
@@ -475,6 +698,40 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
   return launch_decode_merge(prm, num_seqs, D, stream);
 }
 
+template <int D, int G>
+static cudaError_t launch_decode_list_t(const DecodeParams& prm, const DecodeListParams& lp,
+                                        int items, int max_ctas, const CUtensorMap* tmap_k,
+                                        const CUtensorMap* tmap_v, cudaStream_t stream) {
+  using L = DecodeListTile<D>;
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  cudaError_t e = set_smem_limit_once(paged_decode_list_kernel<D, G>, L::kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
+  const int ctas = max_ctas > 0 && max_ctas < items ? max_ctas : items;
+  e = launch_after_previous(paged_decode_list_kernel<D, G>, dim3(unsigned(ctas)),
+                            dim3(kDecodeWarps * 32), L::kSmemBytes, stream, *tmap_k, *tmap_v, prm,
+                            lp);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)lp.num_seqs * prm.q_heads;
+  const long long blocks = (rows * (D / 4) + 255) / 256;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  return launch_after_previous(paged_decode_merge_list_kernel<D>, dim3(unsigned(blocks)),
+                               dim3(256), 0, stream, prm, lp, rows);
+}
+
+template <int D>
+static cudaError_t launch_decode_list_d(const DecodeParams& prm, const DecodeListParams& lp,
+                                        int items, int max_ctas, int group, const CUtensorMap* tk,
+                                        const CUtensorMap* tv, cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_decode_list_t<D, 1>(prm, lp, items, max_ctas, tk, tv, st);
+    case 2: return launch_decode_list_t<D, 2>(prm, lp, items, max_ctas, tk, tv, st);
+    case 4: return launch_decode_list_t<D, 4>(prm, lp, items, max_ctas, tk, tv, st);
+    case 8: return launch_decode_list_t<D, 8>(prm, lp, items, max_ctas, tk, tv, st);
+    case 16: return launch_decode_list_t<D, 16>(prm, lp, items, max_ctas, tk, tv, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream) {
   if (prm.num_parts == 1 && !prm.force_partials) return cudaSuccess;
@@ -536,12 +793,29 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.extra_lse = a.extra_lse;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
   const int group = a.q_heads / a.kv_heads;
+  if (a.list) {
+    if (a.num_seqs > kListMaxSeqs || a.list_items <= 0) return cudaErrorInvalidValue;
+    DecodeListParams lp;
+    lp.seq_item_base = a.list_base;
+    lp.num_seqs = a.num_seqs;
+    lp.target_items = a.list_target;
+    lp.min_run = a.list_min_run;
+    lp.max_blocks = a.list_max_blocks;
+    if (a.d_head == 128)
+      return launch_decode_list_d<128>(prm, lp, a.list_items, a.list_max_ctas, group, tmap_k,
+                                       tmap_v, stream);
+    if (a.d_head == 64)
+      return launch_decode_list_d<64>(prm, lp, a.list_items, a.list_max_ctas, group, tmap_k,
+                                      tmap_v, stream);
+    return cudaErrorInvalidValue;
+  }
   if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
 }
 
 int decode_max_partition_blocks() { return kMaxPartitionBlocks; }
+int decode_list_max_seqs() { return kListMaxSeqs; }
 
 // Device address of this unit's error word on the current device.
 cudaError_t decode_error_word(unsigned** word) {

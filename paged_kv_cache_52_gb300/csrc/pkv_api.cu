@@ -4,6 +4,7 @@
 // translation units; nothing here touches tensor data.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -115,37 +116,49 @@ bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g =
 struct Plan {
   int partition_blocks = 1;
   int num_parts = 1;
-  size_t ws_bytes = 0;
+  size_t ws_bytes = 0;  // covers the uniform plan and, when chosen, the list
   size_t lse_offset = 0;
+  // length-balanced work list (bf16 decode only)
+  bool list = false;
+  int list_target = 0, list_items = 0, list_max_blocks = 0;
+  size_t list_lse_offset = 0, list_base_offset = 0;
 };
 
 // Partition choice.  Work items are (sequence x KV head, partition).  Long
 // partitions amortise each CTA's pipeline start and keep the partial/merge
 // traffic small, so the partition is sized for about two items per SM
-// (estimated from the longest context), clamped to 16..256 pages (256..4096
-// tokens).  A sweep on GB300 over 8..256 sequences, 7B-MHA and 128K contexts
-// put the best partition at 128-256 pages whenever that still leaves work for
-// every SM.
+// (estimated from the longest context).  With more pairs than CTA slots the
+// partition is capped at about 150 sqrt(pairs / slots) pages; with fewer,
+// it stays within 16..256 pages unless few long contexts fill one wave
+// (up to 1024 pages).  The sweeps behind each rule are quoted below.
 constexpr int kAutoMinPartBlocks = 16;
 constexpr int kAutoMaxPartBlocks = 256;
 constexpr int kItemsPerSm = 2;
+// The length-balanced list: runs of at least this many pages, and the CTA
+// slots of one wave as the run count aimed at.
+constexpr int kListMinRun = 8;
+
+// Whether the library's own choice (partition_blocks == 0) takes the
+// length-balanced list for a batch of `pairs` (sequence, KV head) pairs.
+bool list_wins(long long pairs, long long slots) { return pairs <= slots; }
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
-              int partition_blocks, Plan* plan) {
+              int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0) {
   if (num_seqs < 0 || q_heads <= 0 || kv_heads <= 0 || max_context_len < 0) return PKV_EINVAL;
   if (q_heads % kv_heads) return PKV_EUNSUPPORTED;
   if (!supported_group(q_heads / kv_heads)) return PKV_EUNSUPPORTED;
   if (d_head != 64 && d_head != 128) return PKV_EUNSUPPORTED;
+  if (partition_blocks < PKV_SPLIT_UNIFORM) return PKV_EINVAL;
   const int max_pb = pkv::decode_max_partition_blocks();
   const int nblk_max = (max_context_len + kBlockSize - 1) / kBlockSize;
+  const long long pairs = (long long)num_seqs * kv_heads;
+  const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
+  const long long slots = (long long)kItemsPerSm * sms;
   int pb;
   if (partition_blocks > 0) {
     if (partition_blocks > max_pb) return PKV_EINVAL;
     pb = partition_blocks;
   } else {
-    const long long pairs = (long long)num_seqs * kv_heads;
-    const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
-    const long long slots = (long long)kItemsPerSm * sms;
     if (pairs * 4 <= slots && nblk_max >= 4 * kAutoMaxPartBlocks) {
       // Few (sequence, KV head) pairs with long contexts: equal partitions,
       // all in one wave of CTAs (no partly empty last wave), as long as the
@@ -195,6 +208,31 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   } else {
     plan->ws_bytes = 0;
     plan->lse_offset = 0;
+  }
+  const bool want_list = partition_blocks == PKV_SPLIT_BALANCED || list_ctas > 0 ||
+                         (partition_blocks == 0 && list_wins(pairs, slots));
+  if (allow_list && want_list && num_seqs > 0 && num_seqs <= pkv::decode_list_max_seqs()) {
+    // the run count aimed at: one wave of CTA slots, or, on at most
+    // list_ctas CTAs, four runs per CTA (the CTAs take every list_ctas-th
+    // run, so short single-run pairs even out)
+    const long long target = list_ctas > 0 ? 4LL * list_ctas : slots;
+    // runs: at most the target, plus one per pair for the rounding up, plus
+    // what the 1024-page cap on a run adds
+    const long long cap_runs =
+        (pairs * nblk_max + pkv::decode_max_partition_blocks() - 1) /
+        pkv::decode_max_partition_blocks();
+    const long long items = target + pairs + cap_runs;
+    if (items > INT32_MAX / 16) return PKV_EUNSUPPORTED;
+    const size_t rows = size_t(items) * size_t(q_heads / kv_heads);
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    plan->list = true;
+    plan->list_target = int(target);
+    plan->list_items = int(items);
+    plan->list_max_blocks = nblk_max;
+    plan->list_lse_offset = up(rows * size_t(d_head) * sizeof(float));
+    plan->list_base_offset = plan->list_lse_offset + up(rows * sizeof(float));
+    const size_t list_bytes = plan->list_base_offset + size_t(num_seqs + 1) * sizeof(int32_t);
+    if (list_bytes > plan->ws_bytes) plan->ws_bytes = list_bytes;
   }
   return PKV_OK;
 }
@@ -475,7 +513,7 @@ int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max
                     size_t* out_workspace_bytes) {
   Plan plan;
   const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
-                           partition_blocks, &plan);
+                           partition_blocks, &plan, /*allow_list=*/true);
   if (st != PKV_OK) return st;
   if (out_partition_blocks) *out_partition_blocks = plan.partition_blocks;
   if (out_num_parts) *out_num_parts = plan.num_parts;
@@ -486,9 +524,19 @@ int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max
 size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,
                                   int max_context_len) {
   Plan plan;
-  if (make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &plan) != PKV_OK)
+  if (make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &plan,
+                /*allow_list=*/true) != PKV_OK)
     return 0;
   return plan.ws_bytes;
+}
+
+int pkv_decode_plan_uses_list(int num_seqs, int q_heads, int kv_heads, int d_head,
+                              int max_context_len, int partition_blocks) {
+  Plan plan;
+  const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                           partition_blocks, &plan, /*allow_list=*/true);
+  if (st != PKV_OK) return st;
+  return plan.list ? 1 : 0;
 }
 
 namespace {
@@ -498,13 +546,21 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
                      const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
                      int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                      float scale, void* out, bool out_bf16, void* workspace, size_t ws_bytes,
-                     int partition_blocks, pkv_stream_t stream) {
+                     int partition_blocks, pkv_stream_t stream, int list_ctas = 0) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   Plan plan;
   st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
-                 partition_blocks, &plan);
+                 partition_blocks, &plan, /*allow_list=*/true, list_ctas);
   if (st != PKV_OK) return st;
+  if (list_ctas > 0 && !plan.list) return PKV_EUNSUPPORTED;  // more than 512 sequences
+  if (plan.list && partition_blocks == 0 && list_ctas == 0 &&
+      (!workspace || ws_bytes < plan.ws_bytes)) {
+    // the library's choice with less workspace than the list needs: the
+    // uniform split, which may need none
+    st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, 0, &plan);
+    if (st != PKV_OK) return st;
+  }
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
   if (max_blocks_per_seq <= 0) return PKV_EINVAL;
@@ -540,6 +596,18 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
   a.num_parts = plan.num_parts;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_scale = 1.f;
+  if (plan.list) {
+    char* ws = static_cast<char*>(workspace);
+    a.list = true;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(ws + plan.list_lse_offset);
+    a.list_base = reinterpret_cast<int32_t*>(ws + plan.list_base_offset);
+    a.list_target = plan.list_target;
+    a.list_min_run = kListMinRun;
+    a.list_max_blocks = std::min(plan.list_max_blocks, max_blocks_per_seq);
+    a.list_items = plan.list_items;
+    a.list_max_ctas = list_ctas;
+  }
   cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
@@ -555,6 +623,29 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
                           max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
                           workspace, ws_bytes, partition_blocks, stream);
+}
+
+size_t pkv_decode_limited_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,
+                                          int max_context_len, int max_ctas) {
+  if (max_ctas < 1) return 0;
+  Plan plan;
+  if (make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, PKV_SPLIT_BALANCED, &plan,
+                /*allow_list=*/true, max_ctas) != PKV_OK ||
+      !plan.list)
+    return 0;
+  return plan.ws_bytes;
+}
+
+int pkv_paged_decode_attention_limited(const void* q, int num_seqs, int q_heads,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_cache_desc cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float scale, float* out, int max_ctas,
+                                       void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+  if (max_ctas < 1) return PKV_EINVAL;
+  return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
+                          workspace, ws_bytes, PKV_SPLIT_BALANCED, stream, max_ctas);
 }
 
 int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,

@@ -87,6 +87,13 @@ struct DecodeArgs {
   const float* extra_o = nullptr;
   const float* extra_lse = nullptr;
   bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
+  // length-balanced work list (bf16 decode): list_items CTAs (an upper bound
+  // on the runs), partials at part_o / part_lse indexed by run * G + head,
+  // and the per-sequence first runs at list_base ([num_seqs + 1] int32)
+  bool list = false;
+  int32_t* list_base = nullptr;
+  int list_target = 0, list_min_run = 0, list_max_blocks = 0, list_items = 0;
+  int list_max_ctas = 0;  // > 0: at most this many CTAs, each looping over runs
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
@@ -101,6 +108,7 @@ unsigned read_verify_error(bool clear);
 // Number of K/V stages and warps the decode kernel uses (for the plan).
 int decode_warps_per_cta();
 int decode_max_partition_blocks();
+int decode_list_max_seqs();
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);

@@ -19,6 +19,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.
 
 PKV_OK = 0
 BLOCK_SIZE = 16
+# partition_blocks values that name a split rule rather than a size
+SPLIT_BALANCED = -1   # length-balanced work list (bf16 decode)
+SPLIT_UNIFORM = -2    # uniform partitions sized by the library
 
 DEVERR_BITS = {
     0x1: "bad slot",
@@ -67,6 +70,11 @@ SIGNATURES = {
                                               ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(_sz)], ctypes.c_int),
     "pkv_decode_workspace_bytes": ([ctypes.c_int] * 5, _sz),
+    "pkv_decode_plan_uses_list": ([ctypes.c_int] * 6, ctypes.c_int),
+    "pkv_decode_limited_workspace_bytes": ([ctypes.c_int] * 6, _sz),
+    "pkv_paged_decode_attention_limited": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
+                                            _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
+                                            ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
     "pkv_paged_decode_attention": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc, _vp,
                                     ctypes.c_int, _vp, ctypes.c_int, _f32, _vp, _vp, _sz, _vp],
                                    ctypes.c_int),
@@ -334,6 +342,16 @@ def decode_plan(num_seqs: int, q_heads: int, kv_heads: int, d_head: int, max_con
     return pb.value, np_.value, ws.value
 
 
+def decode_plan_uses_list(num_seqs: int, q_heads: int, kv_heads: int, d_head: int,
+                          max_context_len: int, partition_blocks: int = 0) -> bool:
+    """Whether the bf16 decode takes the length-balanced work list."""
+    st = lib.pkv_decode_plan_uses_list(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                                       partition_blocks)
+    if st < 0:
+        _check("pkv_decode_plan_uses_list", st)
+    return st == 1
+
+
 def decode_workspace(num_seqs, q_heads, kv_heads, d_head, max_context_len, device,
                      partition_blocks: int = 0) -> Optional[torch.Tensor]:
     """A workspace tensor large enough for the plan (None when not needed)."""
@@ -392,6 +410,48 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
     _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def decode_limited_workspace(num_seqs, q_heads, kv_heads, d_head, max_context_len, max_ctas,
+                             device) -> torch.Tensor:
+    n = lib.pkv_decode_limited_workspace_bytes(int(num_seqs), int(q_heads), int(kv_heads),
+                                               int(d_head), int(max_context_len), int(max_ctas))
+    _need(n > 0, "unsupported limited-decode shape (more than 512 sequences?)")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention_limited(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: float, max_ctas: int,
+                                   out: Optional[torch.Tensor] = None,
+                                   max_context_len: Optional[int] = None,
+                                   workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The bf16 decode on at most ``max_ctas`` CTAs (length-balanced list;
+    ``pkv_paged_decode_attention_limited``).  float32 ``out [S, Hq, d]``."""
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
+    S, hq, d = q.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous() and
+          context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (S, hq, d),
+          "out must be contiguous float32 [S, Hq, d]")
+    if workspace is None:
+        workspace = decode_limited_workspace(S, hq, k_cache.shape[2], d, max_context_len,
+                                             max_ctas, q.device)
+    st = lib.pkv_paged_decode_attention_limited(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        int(max_ctas), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("pkv_paged_decode_attention_limited", st)
     return out
 
 

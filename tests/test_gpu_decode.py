@@ -141,3 +141,83 @@ def test_merge_output_alignment_forms_agree(pk):
     ref = DecodeStepOracle(w, range(S)).output()
     assert_attention_close(shifted.cpu().numpy(), ref, "merge, 4-byte aligned out")
     assert pk.get_device_error(clear=True) == 0
+
+
+# ---- the length-balanced work list (partition_blocks = SPLIT_BALANCED, and
+# the library's choice for batches with at most 2 x SMs (sequence, KV head)
+# pairs): runs of near-equal size cut from the actual lengths on the device
+LIST_LENS = [0, 1, 15, 16, 17, 16 * 1000 + 1, 4096, 33, 200, 16 * 64 + 1]
+
+
+@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+def test_balanced_list_ragged_lengths(pk, hq, hkv, d):
+    spec = wl.DecodeSpec("list", 13, len(LIST_LENS), hq, hkv, d, lens=tuple(LIST_LENS))
+    w = wl.make_decode_workload(spec, lens_override=LIST_LENS)
+    w.slot_mapping[LIST_LENS.index(0)] = -1          # the empty sequence appends nothing
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    w = _to_dev(w)
+    assert pk.decode_plan_uses_list(w.num_seqs, hq, hkv, d, max(LIST_LENS), pk.SPLIT_BALANCED)
+    out = run_step(pk, w, partition_blocks=pk.SPLIT_BALANCED)
+    assert_attention_close(out.cpu().numpy(), ref, f"list {hq}/{hkv} d{d}")
+    assert np.all(out[LIST_LENS.index(0)].cpu().numpy() == 0.0)
+    uni = run_step(pk, w, partition_blocks=pk.SPLIT_UNIFORM)
+    assert_attention_close(uni.cpu().numpy(), ref, f"uniform {hq}/{hkv} d{d}")
+    assert pk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("num_seqs", [1, 8, 16, 32])
+def test_balanced_list_is_the_small_batch_choice(pk, num_seqs):
+    # 70B-GQA recipe at small batch sizes (outlier rows included): the
+    # library's own choice is the list, compared whole with the oracle
+    w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV,
+                                num_seqs_override=num_seqs)
+    max_len = max(w.meta["lens"])
+    assert pk.decode_plan_uses_list(num_seqs, 64, 8, 128, max_len, 0)
+    ref = DecodeStepOracle(w, range(num_seqs)).output()
+    out = run_step(pk, w)
+    assert_attention_close(out.cpu().numpy(), ref, f"list, {num_seqs} sequences")
+    assert pk.get_device_error() == 0
+
+
+def test_balanced_list_bad_context_and_workspace_fallback(pk):
+    w = _to_dev(wl.make_decode_workload(wl.TINY))
+    pk.get_device_error(clear=True)
+    lens = w.context_lens.clone()
+    lens[0] = 16 * w.block_tables.shape[1] + 5           # longer than the block table
+    out = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.scale,
+                                    max_context_len=int(lens.max()),
+                                    partition_blocks=pk.SPLIT_BALANCED)
+    assert pk.get_device_error(clear=True) & 0x4
+    assert torch.isfinite(out).all()
+    # the library's choice without a workspace: the uniform split (none needed here)
+    S, hq, d = w.q.shape
+    ref = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                    w.scale, max_context_len=250,
+                                    partition_blocks=pk.SPLIT_UNIFORM)
+    out2 = torch.empty_like(ref)
+    st = pk.lib.pkv_paged_decode_attention_ex(
+        pk._ptr(w.q), S, hq, pk._ptr(w.k_cache), pk._ptr(w.v_cache), pk.cache_desc(w.k_cache),
+        pk._ptr(w.block_tables), w.block_tables.shape[1], pk._ptr(w.context_lens), 250,
+        w.scale, pk._ptr(out2), pk._ptr(None), 0, 0, pk._stream(w.q))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out2, ref)
+    assert pk.get_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("max_ctas", [1, 7, 64, 300])
+def test_limited_decode_matches_oracle(pk, max_ctas):
+    # the balanced list on at most max_ctas CTAs, each looping over its runs
+    lens = [5000, 17, 0, 1, 2600, 16 * 300 + 1, 900, 4096]
+    w = wl.make_decode_workload(wl.GQA_70B, lens_override=lens)
+    w.slot_mapping[lens.index(0)] = -1
+    ref = DecodeStepOracle(w, range(len(lens))).output()
+    w = _to_dev(w)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    out = pk.paged_decode_attention_limited(w.q, kc, vc, w.block_tables, w.context_lens,
+                                            w.scale, max_ctas, max_context_len=max(lens))
+    torch.cuda.synchronize()
+    assert_attention_close(out.cpu().numpy(), ref, f"limited decode, {max_ctas} CTAs")
+    assert np.all(out[lens.index(0)].cpu().numpy() == 0.0)
+    assert pk.get_device_error() == 0

@@ -107,3 +107,13 @@ def test_fp8_causal_prefill_equals_repeated_fp8_decode():
                                                     [int(lens[s]) - n + i + 1], w.scale,
                                                     k_scale, v_scale)
             np.testing.assert_allclose(got[row], ref[0], rtol=0, atol=1e-12)
+
+
+def test_dequantize_table_equals_the_decoder():
+    # the pool dequantizer indexes a table of the decoder's value for each
+    # of the 256 codes: the same values, NaN for NaN, bit for bit
+    codes = np.arange(256, dtype=np.uint8).reshape(16, 16)
+    for scale in (1.0, 0.03125, 3.0):
+        a = oracle.fp8_cache.e4m3_bits_to_f64(codes) * float(np.float32(scale))
+        b = oracle.fp8_cache.dequantize(codes, scale)
+        assert np.array_equal(a, b, equal_nan=True)
