@@ -144,6 +144,7 @@ bool list_wins(long long pairs, long long slots) { return pairs <= slots; }
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
               int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0) {
+  *plan = Plan();  // every field is this call's: a plan object may be reused
   if (num_seqs < 0 || q_heads <= 0 || kv_heads <= 0 || max_context_len < 0) return PKV_EINVAL;
   if (q_heads % kv_heads) return PKV_EUNSUPPORTED;
   if (!supported_group(q_heads / kv_heads)) return PKV_EUNSUPPORTED;
@@ -597,6 +598,7 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_scale = 1.f;
   if (plan.list) {
+    if (!workspace || ws_bytes < plan.ws_bytes) return PKV_ENOMEM;  // the list's partials
     char* ws = static_cast<char*>(workspace);
     a.list = true;
     a.part_o = reinterpret_cast<float*>(ws);
