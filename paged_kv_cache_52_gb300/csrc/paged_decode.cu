@@ -19,14 +19,17 @@
 //    on a per-stage mbarrier.  The block ids of the partition are staged in
 //    shared memory once, so no id load sits on the issue path.
 //  * QK^T and PV run on the tensor cores as warp-level m16n8k16 bf16 MMAs with
-//    fp32 accumulators: the G heads are the M rows (padded to 16), 16 tokens
-//    are the N (QK^T) or K (PV) extent.  At G = 8 this contraction is 8 flop
-//    per KV byte, which would keep the fp32 pipe ~70% busy at HBM speed; on
-//    the tensor pipe it costs a few percent of its rate.
+//    fp32 accumulators, transposed so that no MMA row is padding: S^T = K Q^T
+//    has a page's 16 keys as M and the G heads as N (8 per n-tile), O^T =
+//    V^T P^T has 16 dims per m-tile as M and the heads as N.  At G = 8 this
+//    contraction is 8 flop per KV byte, which would keep the fp32 pipe ~70%
+//    busy at HBM speed; on the tensor pipe it costs a few percent of its rate.
+//    A warp takes its pages two at a time (two independent chains).
 //  * online softmax in the log2 domain (scores pre-multiplied by
-//    scale * log2 e, MUFU ex2); row max/sum are quad shuffles.  P enters the
-//    PV MMA as bf16 hi + bf16 lo (two MMAs), which keeps P's rounding error
-//    at ~2^-16 relative instead of bf16's 2^-9.
+//    scale * log2 e, MUFU ex2); a head's max and sum reduce over the 8 lanes
+//    of its column.  P^T enters the PV MMA as bf16 hi + bf16 lo (two MMAs,
+//    each 8 x 8 block moved into the B layout by movmatrix.trans), which keeps
+//    P's rounding error at ~2^-16 relative instead of bf16's 2^-9.
 //  * warps merge in shared memory; a single-partition sequence writes the
 //    final output, otherwise the CTA writes its normalised partial output and
 //    its log2-sum-exp, and a small merge kernel combines the partitions.
@@ -61,6 +64,196 @@ struct DecodeTile {
   static constexpr int kSmemBytes = kIdsOffset + kMaxPartitionBlocks * 4 + 1024;  // +align slack
 };
 
+// An 8x8 matrix of 16-bit values held one row per lane quad (lane l: row
+// l / 4, columns 2 (l % 4), 2 (l % 4) + 1) -> the same fragment of its transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans_b16(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Running state of one warp, transposed layout: O^T accumulators (m-tile mt:
+// row gid = dim 16 mt + gid, row gid + 8 = dim 16 mt + gid + 8; columns 2 tig,
+// 2 tig + 1 = heads 8 nh + 2 tig + c), the running max and this lane's part
+// of the row sum of those heads.
+template <int D, int G>
+struct DecAcc {
+  static constexpr int NH = (G + 7) / 8;  // n-tiles of heads
+  static constexpr int MT = D / 16;       // m-tiles of dims
+  float o[NH][MT][4];
+  float m[NH][2], l[NH][2];
+};
+
+// NP consecutive landed pages of this warp (ring slots i, i + 1, ...).  The
+// MMAs run transposed, so no MMA row is padding: S^T = K Q^T has a page's 16
+// keys as M and the group's heads as N (8 per n-tile); O^T = V^T P^T has 16
+// dims per m-tile as M and the heads as N -- 8 + 16 MMAs per page for a
+// group of 8 (P as hi + lo), where the heads as M (half an m16 tile) took
+// 16 + 32.  Two pages per call keep two independent chains in flight and
+// share one max reduction and one rescale test among 32 keys.
+template <int D, int G, int NP>
+__device__ __forceinline__ void bf16_pages(DecAcc<D, G>& A,
+                                           const uint32_t (&qf)[(G + 7) / 8][D / 16][2],
+                                           uint32_t ring, int i, int tok_first, int len,
+                                           float scale_log2, int lane) {
+  using T = DecodeTile<D>;
+  constexpr int NH = DecAcc<D, G>::NH;
+  constexpr int MT = DecAcc<D, G>::MT;
+  constexpr int KSTEPS = D / 16;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int mi = lane >> 3, mr = lane & 7;
+  // K as the A operand (keys x dims): matrices (keys 0-7 | 8-15) x (dims 0-7 | 8-15)
+  const int k_key = (mi & 1) * 8 + mr, k_sub = mi >> 1;
+  // V^T as the A operand through ldmatrix.trans: matrices (dims 0-7 | 8-15) x (keys 0-7 | 8-15)
+  const int v_key = (mi >> 1) * 8 + mr, v_sub = mi & 1;
+  uint32_t kbase[NP];
+  int tok0[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    kbase[pg] = ring + ((i + pg) % kDecodeStages) * T::kStageBytes;
+    tok0[pg] = tok_first + pg * kDecodeWarps * kBlockTokens;
+  }
+
+  // S^T = K Q^T; even and odd k-steps accumulate separately (shorter chains).
+  float s[NP][NH][4], s_odd[NP][NH][4];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg)
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[pg][nh][e] = s_odd[pg][nh][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int chunk = 2 * kk + k_sub;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kbase[pg] + (chunk >> 3) * T::kHalfBytes + k_key * 128 +
+                  (((chunk & 7) ^ (k_key & 7)) << 4),
+              a0, a1, a2, a3);
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh)
+        mma_bf16_16816((kk & 1) ? s_odd[pg][nh] : s[pg][nh], a0, a1, a2, a3, qf[nh][kk][0],
+                       qf[nh][kk][1]);
+    }
+  }
+
+  // Online softmax in the log2 domain per head column over the pages' keys
+  // (rows gid and gid + 8 of each page here; the other keys in the lanes with
+  // the same tig).  Keys at or past the length are excluded.
+  bool k0_in[NP], k1_in[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    k0_in[pg] = tok0[pg] + gid < len;
+    k1_in[pg] = tok0[pg] + gid + 8 < len;
+  }
+  uint32_t ph[NP][NH][2], pl[NP][NH][2];  // P^T (B operand) hi and lo: keys 2 tig.., 8 + 2 tig..
+  bool all_same = true;
+  float alpha[NH][2];
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh) {
+    float pr[NP][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float x0[NP], x1[NP];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        x0[pg] = k0_in[pg] ? (s[pg][nh][c] + s_odd[pg][nh][c]) * scale_log2 : -INFINITY;
+        x1[pg] = k1_in[pg] ? (s[pg][nh][c + 2] + s_odd[pg][nh][c + 2]) * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, fmaxf(x0[pg], x1[pg]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(A.m[nh][c], mx);
+      alpha[nh][c] = ex2(A.m[nh][c] - mn);
+      all_same = all_same && A.m[nh][c] == mn;
+      A.m[nh][c] = mn;
+      float add = 0.f;
+#pragma unroll
+      for (int pg = 0; pg < NP; ++pg) {
+        pr[pg][c] = ex2(x0[pg] - mn);
+        pr[pg][c + 2] = ex2(x1[pg] - mn);
+        add += pr[pg][c] + pr[pg][c + 2];
+      }
+      A.l[nh][c] = A.l[nh][c] * alpha[nh][c] + add;
+    }
+    // P^T: the lane's (key, two heads) pairs as bf16 hi and the bf16
+    // residual lo, each 8 x 8 block transposed into (two keys, head)
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {  // keys gid (r = 0) / gid + 8 (r = 1)
+        const uint32_t h = pack_bf16x2(pr[pg][2 * r], pr[pg][2 * r + 1]);
+        const uint32_t l = pack_bf16x2(pr[pg][2 * r] - bf16_lo_to_f32(h),
+                                       pr[pg][2 * r + 1] - bf16_hi_to_f32(h));
+        ph[pg][nh][r] = movmatrix_trans_b16(h);
+        pl[pg][nh][r] = movmatrix_trans_b16(l);
+      }
+  }
+  // After the first pages the running max rarely moves: skip the rescale
+  // (alpha = 1 exactly, so the result is unchanged) unless some head needs it.
+  if (!__all_sync(0xffffffffu, all_same)) {
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        A.o[nh][mt][0] *= alpha[nh][0];
+        A.o[nh][mt][1] *= alpha[nh][1];
+        A.o[nh][mt][2] *= alpha[nh][0];
+        A.o[nh][mt][3] *= alpha[nh][1];
+      }
+  }
+
+  // Rows of the last page past the length may hold anything, NaN included;
+  // their P is 0, and zeroing their V keeps each such product exactly 0.  A
+  // V^T register holds keys (2 tig, 2 tig + 1) -- or 8 more -- in its halves.
+  uint32_t vm0[NP], vm1[NP];
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    vm0[pg] = vm1[pg] = 0xffffffffu;
+    if (tok0[pg] + kBlockTokens > len) {
+      const int k0 = tok0[pg] + 2 * tig;
+      vm0[pg] = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+      vm1[pg] = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+    }
+  }
+  // O^T += V^T P^T: one ldmatrix.trans per 16-dim m-tile and page; the hi
+  // products of all m-tiles first, then the lo ones, so no two consecutive
+  // MMAs share an accumulator.
+  uint32_t va[NP][MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const int chunk = 2 * mt + v_sub;
+      ldsm_x4_trans(kbase[pg] + T::kTileBytes + (chunk >> 3) * T::kHalfBytes + v_key * 128 +
+                        (((chunk & 7) ^ (v_key & 7)) << 4),
+                    va[pg][mt][0], va[pg][mt][1], va[pg][mt][2], va[pg][mt][3]);
+      va[pg][mt][0] &= vm0[pg];
+      va[pg][mt][1] &= vm0[pg];
+      va[pg][mt][2] &= vm1[pg];
+      va[pg][mt][3] &= vm1[pg];
+    }
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg)
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        mma_bf16_16816(A.o[nh][mt], va[pg][mt][0], va[pg][mt][1], va[pg][mt][2], va[pg][mt][3],
+                       ph[pg][nh][0], ph[pg][nh][1]);
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg)
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        mma_bf16_16816(A.o[nh][mt], va[pg][mt][0], va[pg][mt][1], va[pg][mt][2], va[pg][mt][3],
+                       pl[pg][nh][0], pl[pg][nh][1]);
+}
+
 // One run of `nb_local` pages of sequence `seq`, KV head `kvh`, starting at
 // block b0, for the G query heads of the group: softmax(q K^T * scale) V over
 // the run's keys below `len`.  final_out: the run is the sequence's whole
@@ -72,9 +265,10 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
                                            int b0, int nb_local, int len, bool final_out,
                                            size_t pbase, int pstride) {
   using T = DecodeTile<D>;
-  constexpr bool kTwoRows = (G > 8);  // heads gid+8 are real rows too
-  constexpr int KSTEPS = D / 16;       // k-steps of QK^T
-  constexpr int NT = D / 8;            // n-tiles of the output
+  using Acc = DecAcc<D, G>;
+  constexpr int NH = Acc::NH;
+  constexpr int MT = Acc::MT;
+  constexpr int KSTEPS = D / 16;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + T::kIdsOffset);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -100,21 +294,19 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
     tma_prefetch_desc(&tmap_v);
   }
 
-  // Q fragments (A operand, rows = heads of the group, zero beyond G).
-  uint32_t qa[KSTEPS][2];
-  uint32_t qb[kTwoRows ? KSTEPS : 1][2];
-  {
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (row0 + gid) * D);
+  // Q as the B operand of S^T = K Q^T: column gid of n-tile nh = head
+  // 8 nh + gid (zero past the group), k slots (2 tig, 2 tig + 1) and
+  // (2 tig + 8, 2 tig + 9) = those dims of the 16-dim k-step.
+  uint32_t qf[NH][KSTEPS][2];
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh) {
+    const int head = 8 * nh + gid;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (row0 + head) * D);
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-      const bool ok = gid < G;
-      qa[kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
-      qa[kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
-      if constexpr (kTwoRows) {
-        const uint32_t* qrow8 = qrow + 8 * D / 2;
-        qb[kk][0] = __ldg(qrow8 + (kk * 16 + tig * 2) / 2);
-        qb[kk][1] = __ldg(qrow8 + (kk * 16 + 8 + tig * 2) / 2);
-      }
+      const bool ok = head < G;
+      qf[nh][kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
+      qf[nh][kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
     }
   }
   __syncthreads();  // ids staged, barriers initialised
@@ -139,146 +331,40 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
   }
   issued = cnt < kDecodeStages ? cnt : kDecodeStages;
 
-  // Per-lane ldmatrix geometry.
-  const int mi = lane >> 3, mr = lane & 7;
-  const int k_tok = (mi >> 1) * 8 + mr;  // K: matrices (tok 0-7|8-15) x (chunk even|odd)
-  const int v_tok = (mi & 1) * 8 + mr;   // V (trans): matrices (tok 0-7|8-15) x (chunk even|odd)
-
-  float o[NT][4];
+  Acc acc;
 #pragma unroll
-  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  for (int nh = 0; nh < NH; ++nh) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      acc.o[nh][mt][0] = acc.o[nh][mt][1] = acc.o[nh][mt][2] = acc.o[nh][mt][3] = 0.f;
+    acc.m[nh][0] = acc.m[nh][1] = -INFINITY;
+    acc.l[nh][0] = acc.l[nh][1] = 0.f;
+  }
   bool failed = false;
   int i = 0;
-  for (; i < cnt; ++i) {
-    const int st = i % kDecodeStages;
-    const uint32_t par = (i / kDecodeStages) & 1;
-    const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(bars + st * 8, par));
-    if (!ready) {
+  // pages two at a time; an odd last page alone
+  for (; i < cnt; i += 2) {
+    const bool two = i + 1 < cnt;
+    bool landed = mbar_wait_bounded(bars + (i % kDecodeStages) * 8, (i / kDecodeStages) & 1);
+    if (two && landed)
+      landed = mbar_wait_bounded(bars + ((i + 1) % kDecodeStages) * 8,
+                                 ((i + 1) / kDecodeStages) & 1);
+    if (!__all_sync(0xffffffffu, landed)) {
       failed = true;
       break;
     }
-    const uint32_t kbase = ring + st * T::kStageBytes;
-    const uint32_t vbase = kbase + T::kTileBytes;
-    const int tok0 = (b0 + warp + i * kDecodeWarps) * kBlockTokens;
+    const int tok_first = (b0 + warp + i * kDecodeWarps) * kBlockTokens;
+    if (two)
+      bf16_pages<D, G, 2>(acc, qf, ring, i, tok_first, len, p.scale_log2, lane);
+    else
+      bf16_pages<D, G, 1>(acc, qf, ring, i, tok_first, len, p.scale_log2, lane);
 
-    // S = Q K^T for 16 tokens (two n-tiles of 8).
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      const int chunk = 2 * kk + (mi & 1);
-      const uint32_t addr = kbase + (chunk >> 3) * T::kHalfBytes + k_tok * 128 +
-                            (((chunk & 7) ^ (k_tok & 7)) << 4);
-      uint32_t b0r, b1r, b2r, b3r;
-      ldsm_x4(addr, b0r, b1r, b2r, b3r);
-      uint32_t a1 = 0u, a3 = 0u;
-      if constexpr (kTwoRows) {
-        a1 = qb[kk][0];
-        a3 = qb[kk][1];
+    __syncwarp();  // every lane is done reading these stages
+    for (int j = i; j < i + (two ? 2 : 1); ++j) {
+      if (j + kDecodeStages < cnt) {
+        if (lane == 0) issue(j + kDecodeStages);
+        ++issued;
       }
-      mma_bf16_16816(s[0], qa[kk][0], a1, qa[kk][1], a3, b0r, b1r);
-      mma_bf16_16816(s[1], qa[kk][0], a1, qa[kk][1], a3, b2r, b3r);
-    }
-
-    // Online softmax in the log2 domain; mask tokens at or past the length.
-    float x[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * p.scale_log2;
-    if (tok0 + kBlockTokens > len) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (tok0 + nt * 8 + tig * 2 + (e & 1) >= len) x[nt][e] = -INFINITY;
-    }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    const float mn0 = fmaxf(m0, mx0);
-    const float alpha0 = ex2(m0 - mn0);
-    m0 = mn0;
-    float pr[2][4];
-    pr[0][0] = ex2(x[0][0] - mn0);
-    pr[0][1] = ex2(x[0][1] - mn0);
-    pr[1][0] = ex2(x[1][0] - mn0);
-    pr[1][1] = ex2(x[1][1] - mn0);
-    l0 = l0 * alpha0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    float alpha1 = 1.f;
-    if constexpr (kTwoRows) {
-      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn1 = fmaxf(m1, mx1);
-      alpha1 = ex2(m1 - mn1);
-      m1 = mn1;
-      pr[0][2] = ex2(x[0][2] - mn1);
-      pr[0][3] = ex2(x[0][3] - mn1);
-      pr[1][2] = ex2(x[1][2] - mn1);
-      pr[1][3] = ex2(x[1][3] - mn1);
-      l1 = l1 * alpha1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-    } else {
-      pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
-    }
-    // After the first pages the running max rarely moves: skip the rescale
-    // (alpha = 1 exactly, so the result is unchanged) unless some row of the
-    // warp needs it.
-    if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f)) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        o[n][0] *= alpha0;
-        o[n][1] *= alpha0;
-        if constexpr (kTwoRows) {
-          o[n][2] *= alpha1;
-          o[n][3] *= alpha1;
-        }
-      }
-    }
-
-    // P as the A operand (rows = heads, k = 16 tokens), split into bf16 hi + lo.
-    uint32_t ph[4], pl[4];
-    ph[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-    ph[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-    ph[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-    ph[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-    pl[0] = pack_bf16x2(pr[0][0] - bf16_lo_to_f32(ph[0]), pr[0][1] - bf16_hi_to_f32(ph[0]));
-    pl[1] = pack_bf16x2(pr[0][2] - bf16_lo_to_f32(ph[1]), pr[0][3] - bf16_hi_to_f32(ph[1]));
-    pl[2] = pack_bf16x2(pr[1][0] - bf16_lo_to_f32(ph[2]), pr[1][1] - bf16_hi_to_f32(ph[2]));
-    pl[3] = pack_bf16x2(pr[1][2] - bf16_lo_to_f32(ph[3]), pr[1][3] - bf16_hi_to_f32(ph[3]));
-
-    // Rows of the last page past the length may hold anything, NaN included;
-    // their P is 0, and zeroing their V keeps each such product exactly 0.  A
-    // B register holds keys (2 tig, 2 tig + 1) -- or 8 more -- in its halves.
-    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-    if (tok0 + kBlockTokens > len) {
-      const int k0 = tok0 + 2 * tig;
-      vm0 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
-      vm1 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
-    }
-
-    // O += P V: V tiles through ldmatrix.trans (B operand, k = tokens, n = dims).
-#pragma unroll
-    for (int dn = 0; dn < D / 16; ++dn) {
-      const int chunk = 2 * dn + (mi >> 1);
-      const uint32_t addr = vbase + (chunk >> 3) * T::kHalfBytes + v_tok * 128 +
-                            (((chunk & 7) ^ (v_tok & 7)) << 4);
-      uint32_t b0r, b1r, b2r, b3r;
-      ldsm_x4_trans(addr, b0r, b1r, b2r, b3r);
-      b0r &= vm0;
-      b1r &= vm1;
-      b2r &= vm0;
-      b3r &= vm1;
-      mma_bf16_16816(o[2 * dn], ph[0], ph[1], ph[2], ph[3], b0r, b1r);
-      mma_bf16_16816(o[2 * dn], pl[0], pl[1], pl[2], pl[3], b0r, b1r);
-      mma_bf16_16816(o[2 * dn + 1], ph[0], ph[1], ph[2], ph[3], b2r, b3r);
-      mma_bf16_16816(o[2 * dn + 1], pl[0], pl[1], pl[2], pl[3], b2r, b3r);
-    }
-
-    __syncwarp();  // every lane is done reading this stage
-    if (i + kDecodeStages < cnt) {
-      if (lane == 0) issue(i + kDecodeStages);
-      ++issued;
     }
   }
 
@@ -293,37 +379,42 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
     __syncwarp();
   }
 
-  // Row sums were kept per lane: reduce over the quad.
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  if constexpr (kTwoRows) {
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  }
+  // Row sums were kept per lane: reduce over the lanes of one head column.
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 4);
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 8);
+      acc.l[nh][c] += __shfl_xor_sync(0xffffffffu, acc.l[nh][c], 16);
+    }
 
-  // Cross-warp merge through shared memory (each warp reuses its own ring).
-  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);  // [G][D]
-  float* mml = mo + G * D;                                            // m[G], l[G]
-  if (gid < G) {
+  // Cross-warp merge through shared memory (each warp reuses its own ring):
+  // [G][D] partial O, then m[G], l[G].
+  float* mo = reinterpret_cast<float*>(smem + warp * T::kRingBytes);
+  float* mml = mo + G * D;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      mo[gid * D + n * 8 + tig * 2] = o[n][0];
-      mo[gid * D + n * 8 + tig * 2 + 1] = o[n][1];
-    }
-    if (tig == 0) {
-      mml[gid] = m0;
-      mml[G + gid] = l0;
-    }
-  }
-  if constexpr (kTwoRows) {
+  for (int nh = 0; nh < NH; ++nh) {
+    const int h0 = 8 * nh + 2 * tig;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      mo[(gid + 8) * D + n * 8 + tig * 2] = o[n][2];
-      mo[(gid + 8) * D + n * 8 + tig * 2 + 1] = o[n][3];
+    for (int mt = 0; mt < MT; ++mt) {
+      const int dim = 16 * mt + gid;
+      if (h0 < G) {
+        mo[h0 * D + dim] = acc.o[nh][mt][0];
+        mo[h0 * D + dim + 8] = acc.o[nh][mt][2];
+      }
+      if (h0 + 1 < G) {
+        mo[(h0 + 1) * D + dim] = acc.o[nh][mt][1];
+        mo[(h0 + 1) * D + dim + 8] = acc.o[nh][mt][3];
+      }
     }
-    if (tig == 0) {
-      mml[gid + 8] = m1;
-      mml[G + gid + 8] = l1;
+    if (gid == 0) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        if (h0 + c < G) {
+          mml[h0 + c] = acc.m[nh][c];
+          mml[G + h0 + c] = acc.l[nh][c];
+        }
     }
   }
   __syncthreads();
@@ -391,13 +482,16 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // Here every CTA derives the same plan from the context lengths on the device:
 //   n_s  pages of sequence s (clamped to the block table and the host bound),
 //   T    = sum_s n_s,
-//   c    = clamp(ceil(Hkv T / target), min_run, kMaxPartitionBlocks) pages,
+//   c    = clamp(ceil(Hkv T / (target - pairs)), min_run, kMaxPartitionBlocks)
+//          pages (target alone when it is not above the pair count),
 //   k_s  = max(1, ceil(n_s / c)) runs per (s, KV head), of near-equal size
 //          (run r covers blocks [r n_s / k_s, (r + 1) n_s / k_s)),
-// items numbered sequence-major, then KV head, then run; CTA i takes item i.
-// Every run is at most c pages, so a grid of `target` CTA slots finishes in
-// one even wave.  A pair with one run writes the output; otherwise its runs
-// write partials at rows item * G + head and the list merge combines them.
+// items numbered sequence-major, then KV head, then run; CTA i takes item i
+// (and every gridDim.x-th after it on a smaller grid).  Every run is at most
+// c pages and, when the target exceeds the pair count, there are at most
+// `target` of them, so a grid of `target` CTA slots finishes in one even
+// wave.  A pair with one run writes the output; otherwise its runs write
+// partials at rows item * G + head and the list merge combines them.
 // Block 0 stores the per-sequence first items (seq_item_base) for the merge.
 // ---------------------------------------------------------------------------
 constexpr int kListMaxSeqs = 512;
@@ -493,8 +587,13 @@ paged_decode_list_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
   for (int w = 0; w < kDecodeWarps; ++w) pages += red_total[w];
 
-  // 2. run size and runs per pair
-  long long c = (pages * p.kv_heads + lp.target_items - 1) / lp.target_items;
+  // 2. run size and runs per pair.  Rounding k_s up adds at most one run per
+  //    pair, so runs of Hkv T / (target - pairs) pages keep the count within
+  //    the target (one wave); with fewer slots than pairs every pair has at
+  //    least one run anyway.
+  const long long pairs = (long long)S * p.kv_heads;
+  const long long room = lp.target_items > pairs ? lp.target_items - pairs : lp.target_items;
+  long long c = (pages * p.kv_heads + room - 1) / room;
   if (c < lp.min_run) c = lp.min_run;
   if (c > kMaxPartitionBlocks) c = kMaxPartitionBlocks;
   int k[kListPerThread];
