@@ -480,6 +480,29 @@ def run_mixed(args, dev, pagedkv, E):
         torch.cuda.synchronize()
         return c0.elapsed_time(c1) / steps
 
+    # the whole step's attention as one persistent launch (prefill tiles and
+    # decode runs from one work list), after the append
+    mws = pagedkv.mixed_step_workspace(len(plens), w.prefill_tables.shape[1], len(dlens), hq,
+                                       hkv, d, max_d, dev)
+
+    def unified_step():
+        append()
+        pagedkv.mixed_step_attention(w.q_prefill, w.q_start, w.prefill_tables, w.prefill_lens,
+                                     True, w.q_decode, w.decode_tables, w.decode_lens, kc, vc,
+                                     w.scale, chunk, max_d, out_prefill=pout, out_decode=dout,
+                                     workspace=mws)
+
+    for _ in range(3):
+        unified_step()
+    torch.cuda.synchronize()
+    c0, c1 = E(enable_timing=True), E(enable_timing=True)
+    c0.record()
+    for _ in range(K):
+        unified_step()
+    c1.record()
+    torch.cuda.synchronize()
+    t_unified = c0.elapsed_time(c1) / K
+    del mws
     fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (88, 96, 104, 112, 120)}
     fp8_best = min(fp8_sweep, key=fp8_sweep.get)
     fp8_step = {"ms_per_step": round(ms8(0, 3), 4), "append_ms": round(ms8(0, 1), 4),
@@ -560,6 +583,12 @@ def run_mixed(args, dev, pagedkv, E):
             "ms_per_step": round(t_split, 4), "prefill_ctas": best_ctas,
             "sweep_ms_by_prefill_ctas": split_sweep,
             "note": "shared-prefix decode on the SMs the persistent prefill leaves free"},
+        "unified": {
+            "ms_per_step": round(t_unified, 4),
+            "frac_of_roofline": round(t_roof * 1e3 / t_unified, 4),
+            "note": "append, then pkv_mixed_step_attention: V pages to f16, the decode plan, "
+                    "one persistent launch of prefill tiles and decode runs from one work "
+                    "list, the decode merge"},
         "gpu_launches": K * (4 + (1 if ws is not None else 0)),
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),

@@ -140,10 +140,10 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
  *                        one wave of CTAs in all ("第 10 讲：推理（Inference）",
  *                        "核心概念与定义": FlashDecoding's split of long
  *                        contexts, here balanced on the real lengths);
- *   0                    the library's choice: the balanced list when the
- *                        batch has at most 2 x SMs (sequence, KV head)
- *                        pairs and the workspace holds it, else the
- *                        library's uniform partitions.
+ *   0                    the library's choice: today the uniform partitions
+ *                        (on GB300 the balanced list did not beat them at any
+ *                        batch size: a small batch's time is the decode's
+ *                        fixed cost more than the balance of its waves).
  * The FP8 decode, the verification decode and the shared-prefix decode
  * treat every value <= 0 as PKV_SPLIT_UNIFORM.
  */
@@ -163,8 +163,7 @@ PKV_API int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head,
                     size_t* out_workspace_bytes);
 
 /* 1 when the bf16 decode with this partition_blocks takes the length-balanced
- * list (given a workspace of pkv_decode_plan's size), 0 when it takes the
- * uniform split, or a negative pkv_status. */
+ * list, 0 when it takes the uniform split, or a negative pkv_status. */
 PKV_API int pkv_decode_plan_uses_list(int num_seqs, int q_heads, int kv_heads, int d_head,
                                       int max_context_len, int partition_blocks);
 
@@ -196,10 +195,7 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_head
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
  *                  bytes, or NULL when that is 0; contents need no
  *                  initialisation and are overwritten.  Calls that share a
- *                  workspace must be ordered on the GPU.  With a smaller
- *                  workspace (or NULL) the library's choice falls back from
- *                  the balanced list to the uniform split when the latter's
- *                  own workspace fits.
+ *                  workspace must be ordered on the GPU.
  * Query head h uses KV head h / (q_heads / kv_heads).  A sequence with
  * context_len 0 yields zeros.  Block ids outside the pool read as zero rows
  * and set PKV_DEVERR_BAD_BLOCK_ID; context_len beyond 16*max_blocks_per_seq
@@ -362,6 +358,55 @@ PKV_API int pkv_paged_prefill_attention_limited(const void* q, const int32_t* q_
                                                 float scale, float* out, int max_ctas,
                                                 void* workspace, size_t ws_bytes,
                                                 pkv_stream_t stream);
+
+/*
+ * pkv_mixed_step_attention -- the attention of one continuous-batching step
+ * in a single persistent launch: the chunked prefill of num_prefill new
+ * prompt chunks and the decode of num_decode running sequences, over the
+ * same K/V pools ("第 10 讲：推理（Inference）", "核心概念与定义": continuous
+ * batching and selective batching -- attention per sequence, every request of
+ * the step in one batch; nano-vLLM page, section "Priorité au
+ * pré-remplissage").  Every SM takes items from one work list: query tiles of
+ * the chunks (tensor cores) and length-balanced runs of the decodes (HBM),
+ * interleaved so that SMs free of one kind of work take the other; the
+ * library sizes the split from the actual lengths, not from a caller's
+ * choice.  Results: out_prefill as pkv_paged_prefill_attention_ex (bit for
+ * bit: the same tile arithmetic, P as one f16 operand -- see there for the
+ * accuracy and V's range), out_decode as pkv_paged_decode_attention with
+ * PKV_SPLIT_BALANCED (within the decode's tolerance: the runs differ).
+ * Before the call, the K/V of every new token (chunks and decode tokens)
+ * must be appended.
+ *   prefill part : q_prefill [total_q][q_heads][d_head] bf16, q_start [num_prefill + 1],
+ *                  prefill_block_tables [num_prefill][prefill_max_blocks],
+ *                  prefill_context_lens [num_prefill], causal -- as in
+ *                  pkv_paged_prefill_attention; out_prefill [total_q][q_heads][d_head] fp32.
+ *   decode part  : q_decode [num_decode][q_heads][d_head] bf16 (num_decode <= 512),
+ *                  decode_block_tables [num_decode][decode_max_blocks],
+ *                  decode_context_lens [num_decode], max_decode_context_len
+ *                  (host bound) -- as in pkv_paged_decode_attention;
+ *                  out_decode [num_decode][q_heads][d_head] fp32, 16-byte aligned.
+ *   workspace    : >= pkv_mixed_step_workspace_bytes(...) device bytes,
+ *                  256-byte aligned (PKV_ENOMEM if smaller); overwritten by
+ *                  every call, so calls that share it must not overlap.
+ * Both parts must be non-empty (PKV_EINVAL otherwise; each separate entry
+ * point serves one part alone).  Errors and device checks are those of the
+ * two separate calls.
+ */
+PKV_API size_t pkv_mixed_step_workspace_bytes(int num_prefill, int prefill_max_blocks,
+                                              int num_decode, int q_heads, int kv_heads,
+                                              int d_head, int max_decode_context_len);
+PKV_API int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start,
+                                     int num_prefill, int total_q, int max_q_len,
+                                     const int32_t* prefill_block_tables, int prefill_max_blocks,
+                                     const int32_t* prefill_context_lens, int causal,
+                                     const void* q_decode, int num_decode,
+                                     const int32_t* decode_block_tables, int decode_max_blocks,
+                                     const int32_t* decode_context_lens,
+                                     int max_decode_context_len, int q_heads,
+                                     const void* k_cache, const void* v_cache,
+                                     pkv_cache_desc cache, float scale, float* out_prefill,
+                                     float* out_decode, void* workspace, size_t ws_bytes,
+                                     pkv_stream_t stream);
 
 /*
  * pkv_paged_prefill_attention_bf16out -- the chunked prefill with a bf16

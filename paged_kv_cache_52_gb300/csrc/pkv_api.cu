@@ -137,10 +137,17 @@ constexpr int kItemsPerSm = 2;
 // The length-balanced list: runs of at least this many pages, and the CTA
 // slots of one wave as the run count aimed at.
 constexpr int kListMinRun = 8;
+// The fused mixed step spreads its prefill items over this share (per mille)
+// of its work list; the rest holds decode runs only.
+constexpr int kMixedPrefillSpanPermille = 900;
 
 // Whether the library's own choice (partition_blocks == 0) takes the
-// length-balanced list for a batch of `pairs` (sequence, KV head) pairs.
-bool list_wins(long long pairs, long long slots) { return pairs <= slots; }
+// length-balanced list.  Measured on GB300 (70B-GQA recipe, 1 to 64
+// sequences) the list never beat the uniform plan: a small batch's time is
+// the decode's fixed cost (launch, pipeline ramp, merge) more than the
+// balance of its waves.  So the library's choice stays uniform, and the list
+// serves PKV_SPLIT_BALANCED, the CTA-capped decode and the fused mixed step.
+bool list_wins(long long /*pairs*/, long long /*slots*/) { return false; }
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
               int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0) {
@@ -555,13 +562,6 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
                  partition_blocks, &plan, /*allow_list=*/true, list_ctas);
   if (st != PKV_OK) return st;
   if (list_ctas > 0 && !plan.list) return PKV_EUNSUPPORTED;  // more than 512 sequences
-  if (plan.list && partition_blocks == 0 && list_ctas == 0 &&
-      (!workspace || ws_bytes < plan.ws_bytes)) {
-    // the library's choice with less workspace than the list needs: the
-    // uniform split, which may need none
-    st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, 0, &plan);
-    if (st != PKV_OK) return st;
-  }
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
   if (max_blocks_per_seq <= 0) return PKV_EINVAL;
@@ -648,6 +648,142 @@ int pkv_paged_decode_attention_limited(const void* q, int num_seqs, int q_heads,
   return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
                           max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
                           workspace, ws_bytes, PKV_SPLIT_BALANCED, stream, max_ctas);
+}
+
+namespace {
+
+// Workspace of the fused mixed step: the f16 prefill's part (V pages in f16,
+// their table, its counter and dispatch order), then the decode list's
+// partials and plan, then the fused launch's counter.
+struct MixedLayout {
+  Fp8PrefillLayout pre;  // offsets from its v_off
+  Plan dec;
+  size_t pre_bytes = 0, dec_off = 0, counter_off = 0, total = 0;
+};
+
+int mixed_layout(int num_prefill, int prefill_max_blocks, int num_decode, int q_heads,
+                 int kv_heads, int d_head, int max_decode_context_len, MixedLayout* m) {
+  if (!fp8_prefill_layout(num_prefill, prefill_max_blocks, kv_heads, d_head, &m->pre))
+    return PKV_EUNSUPPORTED;
+  const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
+  const int st = make_plan(num_decode, q_heads, kv_heads, d_head, max_decode_context_len,
+                           PKV_SPLIT_BALANCED, &m->dec, /*allow_list=*/true, 2 * sms);
+  if (st != PKV_OK) return st;
+  if (!m->dec.list) return PKV_EUNSUPPORTED;  // more than 512 decode sequences
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  m->pre_bytes = m->pre.total - m->pre.v_off;
+  m->dec_off = up(m->pre_bytes);
+  m->counter_off = m->dec_off + up(m->dec.ws_bytes);
+  m->total = m->counter_off + 256;
+  return PKV_OK;
+}
+
+}  // namespace
+
+size_t pkv_mixed_step_workspace_bytes(int num_prefill, int prefill_max_blocks, int num_decode,
+                                      int q_heads, int kv_heads, int d_head,
+                                      int max_decode_context_len) {
+  MixedLayout m;
+  if (mixed_layout(num_prefill, prefill_max_blocks, num_decode, q_heads, kv_heads, d_head,
+                   max_decode_context_len, &m) != PKV_OK)
+    return 0;
+  return m.total;
+}
+
+int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start, int num_prefill,
+                             int total_q, int max_q_len, const int32_t* prefill_block_tables,
+                             int prefill_max_blocks, const int32_t* prefill_context_lens,
+                             int causal, const void* q_decode, int num_decode,
+                             const int32_t* decode_block_tables, int decode_max_blocks,
+                             const int32_t* decode_context_lens, int max_decode_context_len,
+                             int q_heads, const void* k_cache, const void* v_cache,
+                             pkv_cache_desc cache, float scale, float* out_prefill,
+                             float* out_decode, void* workspace, size_t ws_bytes,
+                             pkv_stream_t stream) {
+  int st = check_prefill(q_prefill, q_start, num_prefill, total_q, max_q_len, q_heads, k_cache,
+                         v_cache, cache, prefill_block_tables, prefill_max_blocks,
+                         prefill_context_lens, scale, out_prefill);
+  if (st != PKV_OK) return st;
+  if (num_prefill <= 0 || total_q <= 0 || max_q_len <= 0 || num_decode <= 0)
+    return PKV_EINVAL;  // both parts are needed; the separate calls serve one alone
+  if (!q_decode || !decode_block_tables || !decode_context_lens || !out_decode ||
+      decode_max_blocks <= 0 || max_decode_context_len < 0)
+    return PKV_EINVAL;
+  if (!aligned(q_decode, 16) || !aligned(decode_block_tables, 4) ||
+      !aligned(decode_context_lens, 4) || !aligned(out_decode, 16))
+    return PKV_EINVAL;
+  MixedLayout m;
+  st = mixed_layout(num_prefill, prefill_max_blocks, num_decode, q_heads, cache.kv_heads,
+                    cache.d_head, max_decode_context_len, &m);
+  if (st != PKV_OK) return st;
+  if (!workspace || ws_bytes < m.total) return PKV_ENOMEM;
+  if (!aligned(workspace, 256)) return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // 1. the chunks' V pages to f16 (and the sequences ranked by length)
+  int32_t* vtab = reinterpret_cast<int32_t*>(ws + (m.pre.table_off - m.pre.v_off));
+  int32_t* order = reinterpret_cast<int32_t*>(ws + (m.pre.order_off - m.pre.v_off));
+  cudaError_t e = pkv::launch_v_pages_to_f16(
+      v_cache, prefill_block_tables, prefill_context_lens, num_prefill, prefill_max_blocks,
+      cache.num_blocks, int64_t(kBlockSize) * cache.kv_heads * cache.d_head, ws, vtab, order, cs,
+      sms);
+  if (e != cudaSuccess) return PKV_ECUDA;
+  // 2. tensor maps: prefill queries, the K and V pools, the f16 V scratch
+  const int group = q_heads / cache.kv_heads;
+  pkv_cache_desc vdesc = cache;
+  vdesc.num_blocks = num_prefill * prefill_max_blocks;
+  CUtensorMap tq, tk, tv, tv16;
+  if (!encode_query_map(&tq, q_prefill, total_q, q_heads, cache.d_head, group,
+                        pkv::prefill_rows_per_tile() / group) ||
+      !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache) ||
+      !encode_pool_map(&tv16, ws, vdesc))
+    return PKV_ECUDA;
+  pkv::PrefillArgs pa;
+  pa.q_start = q_start;
+  pa.block_tables = prefill_block_tables;
+  pa.context_lens = prefill_context_lens;
+  pa.out = out_prefill;
+  pa.num_seqs = num_prefill;
+  pa.total_q = total_q;
+  pa.max_q_len = max_q_len;
+  pa.q_heads = q_heads;
+  pa.kv_heads = cache.kv_heads;
+  pa.d_head = cache.d_head;
+  pa.num_blocks = cache.num_blocks;
+  pa.max_blocks_per_seq = prefill_max_blocks;
+  pa.causal = causal ? 1 : 0;
+  pa.scale_log2 = scale * 1.4426950408889634f;
+  pa.f16_pv = true;
+  pa.v_block_tables = vtab;
+  pa.v_num_blocks = vdesc.num_blocks;
+  pa.seq_order = order;
+  pkv::DecodeArgs da;
+  uint8_t* dws = ws + m.dec_off;
+  da.q = q_decode;
+  da.block_tables = decode_block_tables;
+  da.context_lens = decode_context_lens;
+  da.out = out_decode;
+  da.part_o = reinterpret_cast<float*>(dws);
+  da.part_lse = reinterpret_cast<float*>(dws + m.dec.list_lse_offset);
+  da.num_seqs = num_decode;
+  da.q_heads = q_heads;
+  da.kv_heads = cache.kv_heads;
+  da.d_head = cache.d_head;
+  da.num_blocks = cache.num_blocks;
+  da.max_blocks_per_seq = decode_max_blocks;
+  da.scale_log2 = scale * 1.4426950408889634f;
+  da.out_scale = 1.f;
+  da.list = true;
+  da.list_base = reinterpret_cast<int32_t*>(dws + m.dec.list_base_offset);
+  da.list_target = m.dec.list_target;
+  da.list_min_run = kListMinRun;
+  da.list_max_blocks = std::min(m.dec.list_max_blocks, decode_max_blocks);
+  da.list_items = m.dec.list_items;
+  e = pkv::launch_mixed_step(pa, da, reinterpret_cast<int*>(ws + m.counter_off), sms,
+                             kMixedPrefillSpanPermille, &tq, &tk, &tv16, &tv, cs);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,
@@ -1120,7 +1256,7 @@ namespace {
 // atomic step, so a bit raised meanwhile by a kernel on another stream stays
 // for the next query instead of being lost -- and stores the OR.
 struct ErrorWordSet {
-  unsigned* word[6];
+  unsigned* word[8];
   int count;
   int clear;
 };
@@ -1138,12 +1274,13 @@ std::mutex g_collect_mutex;  // one collection in flight per process
 
 int collect_error_words(cudaStream_t stream, bool clear, unsigned* word) {
   ErrorWordSet s = {};
-  cudaError_t (*const getters[6])(unsigned**) = {
+  cudaError_t (*const getters[8])(unsigned**) = {
       pkv::append_error_word, pkv::decode_error_word, pkv::decode_fp8_error_word,
-      pkv::prefill_error_word, pkv::verify_error_word, pkv::probe_error_word};
-  for (int i = 0; i < 6; ++i)
+      pkv::prefill_error_word, pkv::verify_error_word, pkv::probe_error_word,
+      pkv::mixed_decode_error_word, pkv::mixed_prefill_error_word};
+  for (int i = 0; i < 8; ++i)
     if (getters[i](&s.word[i]) != cudaSuccess) return PKV_ECUDA;
-  s.count = 6;
+  s.count = 8;
   s.clear = clear ? 1 : 0;
   std::lock_guard<std::mutex> lock(g_collect_mutex);
   collect_error_words_kernel<<<1, 1, 0, stream>>>(s);
@@ -1183,8 +1320,10 @@ int pkv_get_device_error(unsigned int* word, int clear) {
   const unsigned d8 = pkv::read_decode_fp8_error(clear != 0);
   const unsigned v = pkv::read_verify_error(clear != 0);
   const unsigned w = pkv::read_probe_error(clear != 0);
-  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u || w == ~0u) return PKV_ECUDA;
-  *word = a | d | f | d8 | v | w;
+  const unsigned m = pkv::read_mixed_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u || w == ~0u || m == ~0u)
+    return PKV_ECUDA;
+  *word = a | d | f | d8 | v | w | m;
   return PKV_OK;
 }
 

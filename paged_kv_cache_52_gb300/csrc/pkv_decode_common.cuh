@@ -86,4 +86,17 @@ __device__ __forceinline__ int span_parts(const SeqSpan& sp, const DecodeParams&
 cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_head,
                                 cudaStream_t stream);
 
+// The length-balanced list of runs (see list_plan).
+struct DecodeListParams {
+  int32_t* seq_item_base;  // [num_seqs + 1]: first run of each sequence, then the run count
+  int num_seqs;            // <= kListMaxSeqs
+  int target_items;        // runs aimed at
+  int min_run;             // pages
+  int max_blocks;          // page bound per sequence (block table and host max_context_len)
+};
+
+// The merge of a list decode's runs (after the kernel that wrote them).
+cudaError_t launch_decode_list_merge(const DecodeParams& prm, const DecodeListParams& lp,
+                                     int d_head, cudaStream_t stream);
+
 }  // namespace pkv

@@ -18,6 +18,8 @@ cudaError_t decode_fp8_error_word(unsigned** word);
 cudaError_t prefill_error_word(unsigned** word);
 cudaError_t verify_error_word(unsigned** word);
 cudaError_t probe_error_word(unsigned** word);
+cudaError_t mixed_decode_error_word(unsigned** word);
+cudaError_t mixed_prefill_error_word(unsigned** word);
 
 // ---- kv_append.cu
 // reject (optional): a device flag set by launch_slot_duplicates; when it is
@@ -153,5 +155,18 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
                                  const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                  cudaStream_t stream);
 unsigned read_prefill_error(bool clear);
+
+// ---- mixed_step.cu
+// The continuous-batching step's attention in one persistent launch of
+// `ctas` CTAs: pa describes the chunked prefill (f16 P V path: V through
+// pa.v_block_tables into the f16 scratch pool, which tmap_v16 maps), da the
+// bf16 decode as a length-balanced list (da.list_* set, partials in
+// da.part_o / part_lse).  Launches the decode plan, the fused kernel and the
+// list merge.  counter: one int of device memory.
+cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* counter,
+                              int ctas, int prefill_span_permille, const CUtensorMap* tmap_q,
+                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v16,
+                              const CUtensorMap* tmap_v, cudaStream_t stream);
+unsigned read_mixed_error(bool clear);
 
 }  // namespace pkv

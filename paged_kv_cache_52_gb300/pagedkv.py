@@ -72,6 +72,11 @@ SIGNATURES = {
     "pkv_decode_workspace_bytes": ([ctypes.c_int] * 5, _sz),
     "pkv_decode_plan_uses_list": ([ctypes.c_int] * 6, ctypes.c_int),
     "pkv_decode_limited_workspace_bytes": ([ctypes.c_int] * 6, _sz),
+    "pkv_mixed_step_workspace_bytes": ([ctypes.c_int] * 7, _sz),
+    "pkv_mixed_step_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                  ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                                  ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                  CacheDesc, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "pkv_paged_decode_attention_limited": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                             ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
@@ -453,6 +458,62 @@ def paged_decode_attention_limited(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         int(max_ctas), _ptr(workspace), workspace.numel(), _stream(q))
     _check("pkv_paged_decode_attention_limited", st)
     return out
+
+
+def mixed_step_workspace(num_prefill: int, prefill_max_blocks: int, num_decode: int,
+                         q_heads: int, kv_heads: int, d_head: int, max_decode_context_len: int,
+                         device) -> torch.Tensor:
+    n = lib.pkv_mixed_step_workspace_bytes(int(num_prefill), int(prefill_max_blocks),
+                                           int(num_decode), int(q_heads), int(kv_heads),
+                                           int(d_head), int(max_decode_context_len))
+    _need(n > 0, "unsupported mixed-step shape (more than 512 decode sequences?)")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mixed_step_attention(q_prefill: torch.Tensor, q_start: torch.Tensor,
+                         prefill_block_tables: torch.Tensor, prefill_context_lens: torch.Tensor,
+                         causal: bool, q_decode: torch.Tensor, decode_block_tables: torch.Tensor,
+                         decode_context_lens: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, scale: float, max_q_len: int,
+                         max_decode_context_len: int,
+                         out_prefill: Optional[torch.Tensor] = None,
+                         out_decode: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None):
+    """One continuous-batching step's attention in one persistent launch
+    (``pkv_mixed_step_attention``): the chunked prefill and the decodes over
+    the same pools.  Returns ``(out_prefill, out_decode)``, float32."""
+    _check_cache(k_cache, v_cache)
+    for t, n in ((q_prefill, "q_prefill"), (q_decode, "q_decode")):
+        _need(t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 3 and t.is_contiguous(),
+              f"{n} must be a contiguous [rows, Hq, d] bf16 CUDA tensor")
+    T, hq, d = q_prefill.shape
+    S = q_decode.shape[0]
+    P = q_start.shape[0] - 1
+    for t, n, rows in ((prefill_block_tables, "prefill_block_tables", P),
+                       (decode_block_tables, "decode_block_tables", S)):
+        _need(t.dtype == torch.int32 and t.dim() == 2 and t.is_contiguous() and t.shape[0] == rows,
+              f"{n} must be contiguous int32 [{rows}, max_blocks]")
+    for t, n, rows in ((q_start, "q_start", P + 1), (prefill_context_lens, "prefill_context_lens", P),
+                       (decode_context_lens, "decode_context_lens", S)):
+        _need(t.dtype == torch.int32 and t.is_contiguous() and t.shape == (rows,),
+              f"{n} must be contiguous int32 [{rows}]")
+    if out_prefill is None:
+        out_prefill = torch.empty(T, hq, d, dtype=torch.float32, device=q_prefill.device)
+    if out_decode is None:
+        out_decode = torch.empty(S, hq, d, dtype=torch.float32, device=q_prefill.device)
+    if workspace is None:
+        workspace = mixed_step_workspace(P, prefill_block_tables.shape[1], S, hq,
+                                         k_cache.shape[2], d, max_decode_context_len,
+                                         q_prefill.device)
+    st = lib.pkv_mixed_step_attention(
+        _ptr(q_prefill), _ptr(q_start), P, T, int(max_q_len), _ptr(prefill_block_tables),
+        prefill_block_tables.shape[1], _ptr(prefill_context_lens), int(bool(causal)),
+        _ptr(q_decode), S, _ptr(decode_block_tables), decode_block_tables.shape[1],
+        _ptr(decode_context_lens), int(max_decode_context_len), hq, _ptr(k_cache), _ptr(v_cache),
+        cache_desc(k_cache), float(scale), _ptr(out_prefill), _ptr(out_decode), _ptr(workspace),
+        workspace.numel(), _stream(q_prefill))
+    _check("pkv_mixed_step_attention", st)
+    return out_prefill, out_decode
 
 
 def prefill_workspace(num_seqs: int, max_blocks_per_seq: int, kv_heads: int, d_head: int,

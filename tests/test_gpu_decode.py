@@ -166,15 +166,16 @@ def test_balanced_list_ragged_lengths(pk, hq, hkv, d):
 
 
 @pytest.mark.parametrize("num_seqs", [1, 8, 16, 32])
-def test_balanced_list_is_the_small_batch_choice(pk, num_seqs):
-    # 70B-GQA recipe at small batch sizes (outlier rows included): the
-    # library's own choice is the list, compared whole with the oracle
+def test_balanced_list_small_batches(pk, num_seqs):
+    # 70B-GQA recipe at small batch sizes (outlier rows included), the list
+    # compared whole with the oracle; the library's own choice is uniform
     w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV,
                                 num_seqs_override=num_seqs)
     max_len = max(w.meta["lens"])
-    assert pk.decode_plan_uses_list(num_seqs, 64, 8, 128, max_len, 0)
+    assert pk.decode_plan_uses_list(num_seqs, 64, 8, 128, max_len, pk.SPLIT_BALANCED)
+    assert not pk.decode_plan_uses_list(num_seqs, 64, 8, 128, max_len, 0)
     ref = DecodeStepOracle(w, range(num_seqs)).output()
-    out = run_step(pk, w)
+    out = run_step(pk, w, partition_blocks=pk.SPLIT_BALANCED)
     assert_attention_close(out.cpu().numpy(), ref, f"list, {num_seqs} sequences")
     assert pk.get_device_error() == 0
 
@@ -189,7 +190,7 @@ def test_balanced_list_bad_context_and_workspace_fallback(pk):
                                     partition_blocks=pk.SPLIT_BALANCED)
     assert pk.get_device_error(clear=True) & 0x4
     assert torch.isfinite(out).all()
-    # the library's choice without a workspace: the uniform split (none needed here)
+    # the library's choice (uniform) without a workspace: none needed here
     S, hq, d = w.q.shape
     ref = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
                                     w.scale, max_context_len=250,
