@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the continuous-batching mixed-step measurement")
     ap.add_argument("--mixed-steps", type=int, default=30)
+    ap.add_argument("--mixed-span-sweep", action="store_true",
+                    help="also time the fused mixed step over a range of work-list interleaves")
     ap.add_argument("--config-cpu-seconds", type=float, default=8.0,
                     help="wall-time budget of the CPU oracle sample of each other config "
                          "(7B-MHA, 128K) and of the mixed step; 0 skips them")
@@ -485,23 +487,29 @@ def run_mixed(args, dev, pagedkv, E):
     mws = pagedkv.mixed_step_workspace(len(plens), w.prefill_tables.shape[1], len(dlens), hq,
                                        hkv, d, max_d, dev)
 
-    def unified_step():
+    def unified_step(span=0):
         append()
         pagedkv.mixed_step_attention(w.q_prefill, w.q_start, w.prefill_tables, w.prefill_lens,
                                      True, w.q_decode, w.decode_tables, w.decode_lens, kc, vc,
                                      w.scale, chunk, max_d, out_prefill=pout, out_decode=dout,
-                                     workspace=mws)
+                                     workspace=mws, prefill_span_permille=span)
 
-    for _ in range(3):
-        unified_step()
-    torch.cuda.synchronize()
-    c0, c1 = E(enable_timing=True), E(enable_timing=True)
-    c0.record()
-    for _ in range(K):
-        unified_step()
-    c1.record()
-    torch.cuda.synchronize()
-    t_unified = c0.elapsed_time(c1) / K
+    def time_unified(span=0, steps=K):
+        for _ in range(3):
+            unified_step(span)
+        torch.cuda.synchronize()
+        c0, c1 = E(enable_timing=True), E(enable_timing=True)
+        c0.record()
+        for _ in range(steps):
+            unified_step(span)
+        c1.record()
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / steps
+
+    t_unified = time_unified()
+    span_sweep = ({sp: round(time_unified(sp, max(5, K // 3)), 4)
+                   for sp in (500, 600, 700, 750, 800, 850, 900, 950, 1000)}
+                  if args.mixed_span_sweep else None)
     del mws
     fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (88, 96, 104, 112, 120)}
     fp8_best = min(fp8_sweep, key=fp8_sweep.get)
@@ -585,6 +593,7 @@ def run_mixed(args, dev, pagedkv, E):
             "note": "shared-prefix decode on the SMs the persistent prefill leaves free"},
         "unified": {
             "ms_per_step": round(t_unified, 4),
+            "sweep_ms_by_prefill_span_permille": span_sweep,
             "frac_of_roofline": round(t_roof * 1e3 / t_unified, 4),
             "note": "append, then pkv_mixed_step_attention: V pages to f16, the decode plan, "
                     "one persistent launch of prefill tiles and decode runs from one work "

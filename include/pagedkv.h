@@ -408,6 +408,26 @@ PKV_API int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_sta
                                      float* out_decode, void* workspace, size_t ws_bytes,
                                      pkv_stream_t stream);
 
+/* pkv_mixed_step_attention with the work list's interleave as a parameter:
+ * the prefill items are spread evenly over the first prefill_span_permille
+ * per mille of the list (1..1000), and the rest of the list holds decode runs
+ * only; a smaller share gives the prefill more SMs early and leaves more
+ * decode runs for a tail on every SM.  0 = the library's value.  The results
+ * do not depend on it (the same items, another order). */
+PKV_API int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start,
+                                        int num_prefill, int total_q, int max_q_len,
+                                        const int32_t* prefill_block_tables,
+                                        int prefill_max_blocks,
+                                        const int32_t* prefill_context_lens, int causal,
+                                        const void* q_decode, int num_decode,
+                                        const int32_t* decode_block_tables, int decode_max_blocks,
+                                        const int32_t* decode_context_lens,
+                                        int max_decode_context_len, int q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        pkv_cache_desc cache, float scale, float* out_prefill,
+                                        float* out_decode, void* workspace, size_t ws_bytes,
+                                        int prefill_span_permille, pkv_stream_t stream);
+
 /*
  * pkv_paged_prefill_attention_bf16out -- the chunked prefill with a bf16
  * output (bf16 as the inference default: "第 10 讲：推理（Inference）",

@@ -690,16 +690,18 @@ size_t pkv_mixed_step_workspace_bytes(int num_prefill, int prefill_max_blocks, i
   return m.total;
 }
 
-int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start, int num_prefill,
-                             int total_q, int max_q_len, const int32_t* prefill_block_tables,
-                             int prefill_max_blocks, const int32_t* prefill_context_lens,
-                             int causal, const void* q_decode, int num_decode,
-                             const int32_t* decode_block_tables, int decode_max_blocks,
-                             const int32_t* decode_context_lens, int max_decode_context_len,
-                             int q_heads, const void* k_cache, const void* v_cache,
-                             pkv_cache_desc cache, float scale, float* out_prefill,
-                             float* out_decode, void* workspace, size_t ws_bytes,
-                             pkv_stream_t stream) {
+int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, int num_prefill,
+                                int total_q, int max_q_len, const int32_t* prefill_block_tables,
+                                int prefill_max_blocks, const int32_t* prefill_context_lens,
+                                int causal, const void* q_decode, int num_decode,
+                                const int32_t* decode_block_tables, int decode_max_blocks,
+                                const int32_t* decode_context_lens, int max_decode_context_len,
+                                int q_heads, const void* k_cache, const void* v_cache,
+                                pkv_cache_desc cache, float scale, float* out_prefill,
+                                float* out_decode, void* workspace, size_t ws_bytes,
+                                int prefill_span_permille, pkv_stream_t stream) {
+  if (prefill_span_permille < 0 || prefill_span_permille > 1000) return PKV_EINVAL;
+  if (prefill_span_permille == 0) prefill_span_permille = kMixedPrefillSpanPermille;
   int st = check_prefill(q_prefill, q_start, num_prefill, total_q, max_q_len, q_heads, k_cache,
                          v_cache, cache, prefill_block_tables, prefill_max_blocks,
                          prefill_context_lens, scale, out_prefill);
@@ -782,8 +784,25 @@ int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start, int 
   da.list_max_blocks = std::min(m.dec.list_max_blocks, decode_max_blocks);
   da.list_items = m.dec.list_items;
   e = pkv::launch_mixed_step(pa, da, reinterpret_cast<int*>(ws + m.counter_off), sms,
-                             kMixedPrefillSpanPermille, &tq, &tk, &tv16, &tv, cs);
+                             prefill_span_permille, &tq, &tk, &tv16, &tv, cs);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start, int num_prefill,
+                             int total_q, int max_q_len, const int32_t* prefill_block_tables,
+                             int prefill_max_blocks, const int32_t* prefill_context_lens,
+                             int causal, const void* q_decode, int num_decode,
+                             const int32_t* decode_block_tables, int decode_max_blocks,
+                             const int32_t* decode_context_lens, int max_decode_context_len,
+                             int q_heads, const void* k_cache, const void* v_cache,
+                             pkv_cache_desc cache, float scale, float* out_prefill,
+                             float* out_decode, void* workspace, size_t ws_bytes,
+                             pkv_stream_t stream) {
+  return pkv_mixed_step_attention_ex(
+      q_prefill, q_start, num_prefill, total_q, max_q_len, prefill_block_tables,
+      prefill_max_blocks, prefill_context_lens, causal, q_decode, num_decode, decode_block_tables,
+      decode_max_blocks, decode_context_lens, max_decode_context_len, q_heads, k_cache, v_cache,
+      cache, scale, out_prefill, out_decode, workspace, ws_bytes, 0, stream);
 }
 
 int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,

@@ -77,6 +77,11 @@ SIGNATURES = {
                                   ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                   ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                   CacheDesc, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "pkv_mixed_step_attention_ex": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                     ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                                     ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                     CacheDesc, _f32, _vp, _vp, _vp, _sz, ctypes.c_int, _vp],
+                                    ctypes.c_int),
     "pkv_paged_decode_attention_limited": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                             ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
@@ -478,10 +483,12 @@ def mixed_step_attention(q_prefill: torch.Tensor, q_start: torch.Tensor,
                          max_decode_context_len: int,
                          out_prefill: Optional[torch.Tensor] = None,
                          out_decode: Optional[torch.Tensor] = None,
-                         workspace: Optional[torch.Tensor] = None):
+                         workspace: Optional[torch.Tensor] = None,
+                         prefill_span_permille: int = 0):
     """One continuous-batching step's attention in one persistent launch
-    (``pkv_mixed_step_attention``): the chunked prefill and the decodes over
-    the same pools.  Returns ``(out_prefill, out_decode)``, float32."""
+    (``pkv_mixed_step_attention_ex``): the chunked prefill and the decodes
+    over the same pools.  Returns ``(out_prefill, out_decode)``, float32.
+    ``prefill_span_permille``: the work list's interleave (0 = the library's)."""
     _check_cache(k_cache, v_cache)
     for t, n in ((q_prefill, "q_prefill"), (q_decode, "q_decode")):
         _need(t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 3 and t.is_contiguous(),
@@ -505,14 +512,14 @@ def mixed_step_attention(q_prefill: torch.Tensor, q_start: torch.Tensor,
         workspace = mixed_step_workspace(P, prefill_block_tables.shape[1], S, hq,
                                          k_cache.shape[2], d, max_decode_context_len,
                                          q_prefill.device)
-    st = lib.pkv_mixed_step_attention(
+    st = lib.pkv_mixed_step_attention_ex(
         _ptr(q_prefill), _ptr(q_start), P, T, int(max_q_len), _ptr(prefill_block_tables),
         prefill_block_tables.shape[1], _ptr(prefill_context_lens), int(bool(causal)),
         _ptr(q_decode), S, _ptr(decode_block_tables), decode_block_tables.shape[1],
         _ptr(decode_context_lens), int(max_decode_context_len), hq, _ptr(k_cache), _ptr(v_cache),
         cache_desc(k_cache), float(scale), _ptr(out_prefill), _ptr(out_decode), _ptr(workspace),
-        workspace.numel(), _stream(q_prefill))
-    _check("pkv_mixed_step_attention", st)
+        workspace.numel(), int(prefill_span_permille), _stream(q_prefill))
+    _check("pkv_mixed_step_attention_ex", st)
     return out_prefill, out_decode
 
 
