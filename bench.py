@@ -487,30 +487,41 @@ def run_mixed(args, dev, pagedkv, E):
     mws = pagedkv.mixed_step_workspace(len(plens), w.prefill_tables.shape[1], len(dlens), hq,
                                        hkv, d, max_d, dev)
 
-    def unified_step(span=0):
+    # the decodes' shared 1024-token prefix as one prefix group: attended once
+    # on the tensor cores inside the same launch
+    gws = pagedkv.mixed_step_workspace(len(plens), w.prefill_tables.shape[1], len(dlens), hq,
+                                       hkv, d, max_d, dev, num_groups=1)
+    groups = (torch.tensor([0, len(dlens)], dtype=torch.int32, device=dev),
+              torch.tensor([w.meta["shared_prefix"] // wl.BLOCK_SIZE], dtype=torch.int32,
+                           device=dev), len(dlens), w.meta["shared_prefix"] // wl.BLOCK_SIZE)
+
+    def unified_step(span=0, grouped=False):
         append()
         pagedkv.mixed_step_attention(w.q_prefill, w.q_start, w.prefill_tables, w.prefill_lens,
                                      True, w.q_decode, w.decode_tables, w.decode_lens, kc, vc,
                                      w.scale, chunk, max_d, out_prefill=pout, out_decode=dout,
-                                     workspace=mws, prefill_span_permille=span)
+                                     workspace=gws if grouped else mws,
+                                     prefill_span_permille=span,
+                                     decode_groups=groups if grouped else None)
 
-    def time_unified(span=0, steps=K):
+    def time_unified(span=0, grouped=False, steps=K):
         for _ in range(3):
-            unified_step(span)
+            unified_step(span, grouped)
         torch.cuda.synchronize()
         c0, c1 = E(enable_timing=True), E(enable_timing=True)
         c0.record()
         for _ in range(steps):
-            unified_step(span)
+            unified_step(span, grouped)
         c1.record()
         torch.cuda.synchronize()
         return c0.elapsed_time(c1) / steps
 
     t_unified = time_unified()
-    span_sweep = ({sp: round(time_unified(sp, max(5, K // 3)), 4)
-                   for sp in (500, 600, 700, 750, 800, 850, 900, 950, 1000)}
+    t_unified_grouped = time_unified(grouped=True)
+    span_sweep = ({sp: [round(time_unified(sp, g, max(5, K // 3)), 4) for g in (False, True)]
+                   for sp in (500, 700, 800, 900, 950, 1000)}
                   if args.mixed_span_sweep else None)
-    del mws
+    del mws, gws
     fp8_sweep = {c: round(time_fp8_concurrent(c), 4) for c in (88, 96, 104, 112, 120)}
     fp8_best = min(fp8_sweep, key=fp8_sweep.get)
     fp8_step = {"ms_per_step": round(ms8(0, 3), 4), "append_ms": round(ms8(0, 1), 4),
@@ -592,12 +603,14 @@ def run_mixed(args, dev, pagedkv, E):
             "sweep_ms_by_prefill_ctas": split_sweep,
             "note": "shared-prefix decode on the SMs the persistent prefill leaves free"},
         "unified": {
-            "ms_per_step": round(t_unified, 4),
+            "ms_per_step": round(t_unified_grouped, 4),
+            "frac_of_roofline": round(t_roof * 1e3 / t_unified_grouped, 4),
+            "ms_per_step_without_prefix_group": round(t_unified, 4),
             "sweep_ms_by_prefill_span_permille": span_sweep,
-            "frac_of_roofline": round(t_roof * 1e3 / t_unified, 4),
-            "note": "append, then pkv_mixed_step_attention: V pages to f16, the decode plan, "
-                    "one persistent launch of prefill tiles and decode runs from one work "
-                    "list, the decode merge"},
+            "note": "append, then pkv_mixed_step_attention_ex with the decodes' shared prefix "
+                    "as one prefix group: V pages to f16, the prefix check, the decode plan, "
+                    "one persistent launch of prefix tiles, prefill tiles and decode runs "
+                    "from one work list, the decode merge"},
         "gpu_launches": K * (4 + (1 if ws is not None else 0)),
         "roofline_step_ms": round(t_roof * 1e3, 4),
         "step_frac_of_roofline": round(t_roof * 1e3 / t_step, 4),
@@ -1106,7 +1119,7 @@ def per_config_summary(line, peak):
                         "sm_split_ms": m["two_streams_sm_split"]["ms_per_step"],
                         "cpu_ms": cpu_of(m)}
         if "unified" in m:
-            out["mixed"]["unified_ms"] = m["unified"]["ms_per_step"]
+            out["mixed"]["fused_ms"] = m["unified"]["ms_per_step"]
     sb = line.get("small_batch_decode")
     if sb:
         out["small_batch_us"] = {k: [v["eager_us"], v["graph_us"]] for k, v in sb.items()}

@@ -80,6 +80,8 @@ typedef void* pkv_stream_t;
 #define PKV_DEVERR_TMEM_ALLOC 0x20u     /* tensor memory could not be allocated */
 #define PKV_DEVERR_FP16_RANGE 0x40u     /* FP8 decode: a query value is outside f16's range */
 #define PKV_DEVERR_DUPLICATE_SLOT 0x80u /* checked append: a slot named twice; nothing written */
+#define PKV_DEVERR_PREFIX_MISMATCH 0x100u /* shared-prefix decode: a member's prefix is not its
+                                             group's (or is out of range); decoded without it */
 
 /*
  * pkv_kv_append -- scatter new K/V rows into the paged pools.
@@ -408,12 +410,24 @@ PKV_API int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_sta
                                      float* out_decode, void* workspace, size_t ws_bytes,
                                      pkv_stream_t stream);
 
-/* pkv_mixed_step_attention with the work list's interleave as a parameter:
- * the prefill items are spread evenly over the first prefill_span_permille
- * per mille of the list (1..1000), and the rest of the list holds decode runs
- * only; a smaller share gives the prefill more SMs early and leaves more
- * decode runs for a tail on every SM.  0 = the library's value.  The results
- * do not depend on it (the same items, another order). */
+/* pkv_mixed_step_attention with decode prefix groups and the work list's
+ * interleave as parameters.
+ *   decode_group_start, decode_group_prefix_blocks, num_groups,
+ *   max_group_size, max_prefix_blocks: prefix groups of the decodes exactly
+ *     as in pkv_paged_decode_attention_prefix_groups (device arrays; members
+ *     checked against their leader; num_groups 0 = none).  The list then
+ *     starts with each group's prefix items -- its members' queries against
+ *     its prefix on the tensor cores -- and the decode runs cover only the
+ *     members' own pages; the merge folds the prefix part in.
+ *   prefill_span_permille: the prefill items are spread evenly over the first
+ *     prefill_span_permille per mille of the rest of the list (1..1000), the
+ *     remainder holding decode runs only; 0 = the library's value.  The
+ *     results do not depend on it (the same items, another order).
+ * workspace: >= pkv_mixed_step_groups_workspace_bytes(..., num_groups). */
+PKV_API size_t pkv_mixed_step_groups_workspace_bytes(int num_prefill, int prefill_max_blocks,
+                                                     int num_decode, int q_heads, int kv_heads,
+                                                     int d_head, int max_decode_context_len,
+                                                     int num_groups);
 PKV_API int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start,
                                         int num_prefill, int total_q, int max_q_len,
                                         const int32_t* prefill_block_tables,
@@ -425,7 +439,10 @@ PKV_API int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_
                                         int max_decode_context_len, int q_heads,
                                         const void* k_cache, const void* v_cache,
                                         pkv_cache_desc cache, float scale, float* out_prefill,
-                                        float* out_decode, void* workspace, size_t ws_bytes,
+                                        float* out_decode, const int32_t* decode_group_start,
+                                        const int32_t* decode_group_prefix_blocks,
+                                        int num_groups, int max_group_size,
+                                        int max_prefix_blocks, void* workspace, size_t ws_bytes,
                                         int prefill_span_permille, pkv_stream_t stream);
 
 /*
@@ -451,23 +468,52 @@ PKV_API int pkv_paged_prefill_attention_bf16out(const void* q, const int32_t* q_
                                                 size_t ws_bytes, pkv_stream_t stream);
 
 /*
- * pkv_paged_decode_attention_shared_prefix -- the same result as
- * pkv_paged_decode_attention when every sequence's first prefix_blocks pages
- * are the same physical blocks (a shared system prompt stored once and
- * referenced by many requests: "Optimisation de l'inference", section
- * "PageAtention", and the nano-vLLM page, section "Cache KV": shared prefix
- * blocks through the mapping table).  The prefix is read once for all
- * sequences instead of once per sequence:
- *   1. all num_seqs queries attend the prefix keys (non-causal) on the tensor
- *      cores, giving a normalised output and log-sum-exp per (sequence, head);
- *   2. each sequence's own pages after the prefix go through the split-K
+ * pkv_paged_decode_attention_prefix_groups -- the same result as
+ * pkv_paged_decode_attention when groups of sequences share their first
+ * pages: the same physical blocks for a system prompt stored once, or for
+ * the forks of one prompt ("Optimisation de l'inference", section
+ * "PageAtention": many requests on one system prompt's pages; nano-vLLM
+ * page, section "Implementation du cache": prefix blocks shared through the
+ * chained hash).  Each group's prefix is read once for all its members
+ * instead of once per member:
+ *   0. a device pass checks every member: its first prefix blocks must be
+ *      the group leader's ids (the leader is the group's first sequence) and
+ *      its context must hold the prefix; a member that fails -- or whose
+ *      group's prefix length is out of range -- is decoded over its whole
+ *      context instead, and PKV_DEVERR_PREFIX_MISMATCH is set;
+ *   1. each group's member queries attend the group's prefix keys
+ *      (non-causal) on the tensor cores, giving a normalised output and
+ *      log-sum-exp per (sequence, head);
+ *   2. each sequence's own pages after its prefix go through the split-K
  *      decode;
  *   3. the log-sum-exp merge combines both parts.
- * The prefix's block ids are taken from row 0 of block_tables; every
- * context_len must be >= 16 * prefix_blocks (the new token of a decode step
- * lives in a private page).  workspace must hold
- * pkv_decode_shared_prefix_workspace_bytes(...) bytes (256-byte aligned).
+ *   group_start        : [num_groups + 1] int32 device, non-decreasing: group g is
+ *                        sequences group_start[g] .. group_start[g+1] - 1 (the batch
+ *                        is ordered by group); sequences outside every group
+ *                        have no shared prefix.
+ *   group_prefix_blocks: [num_groups] int32 device: group g's prefix in 16-token
+ *                        blocks, 1 .. max_prefix_blocks.
+ *   max_group_size     : host bound on group_start[g+1] - group_start[g].
+ *   max_prefix_blocks  : host bound on group_prefix_blocks.
+ * workspace: >= pkv_decode_prefix_groups_workspace_bytes(...) bytes, 256-byte
+ * aligned.  Other arguments and errors are those of
+ * pkv_paged_decode_attention.
+ *
+ * pkv_paged_decode_attention_shared_prefix -- the case of one group of
+ * every sequence, whose prefix is the first prefix_blocks ids of row 0;
+ * workspace: pkv_decode_shared_prefix_workspace_bytes(...) bytes.
  */
+PKV_API size_t pkv_decode_prefix_groups_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
+                                                       int d_head, int max_context_len,
+                                                       int num_groups);
+PKV_API int pkv_paged_decode_attention_prefix_groups(
+    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int max_group_size,
+    int max_prefix_blocks, float scale, float* out, void* workspace, size_t ws_bytes,
+    pkv_stream_t stream);
+
 PKV_API size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
                                                         int d_head, int max_context_len,
                                                         int prefix_blocks);

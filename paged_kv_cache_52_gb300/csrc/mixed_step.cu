@@ -23,6 +23,11 @@
 //    are short and fill the tail.
 //  * the decode runs come from the list plan (a one-CTA plan kernel before
 //    this launch); runs of one pair are merged afterwards by the list merge.
+//  * with prefix groups (decodes whose first pages are the same physical
+//    blocks), the list starts with the groups' prefix items: each group's
+//    member queries attend its prefix once on the tensor cores, and the
+//    decode runs cover only each member's own pages; the merge folds the
+//    prefix part in.
 //  * every mbarrier wait is bounded; a prefill item that times out raises the
 //    abort flag, and the CTA stops taking items.
 #include "pkv_decode_body.cuh"
@@ -39,6 +44,10 @@ struct MixedParams {
   int num_prefill_items;         // prefill pairs x tiles_per_pair
   int tiles_per_pair;
   int prefill_span_permille;     // the prefill items are spread over this share of the list
+  // decode prefix groups: the first num_prefix_items positions attend each
+  // group's shared prefix for its members' queries (0: no groups)
+  int num_prefix_items;          // groups x KV heads x prefix_tiles
+  int prefix_tiles;
 };
 
 template <int D>
@@ -66,8 +75,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v16,
-                        const __grid_constant__ CUtensorMap tmap_v, const PrefillParams pp,
-                        const DecodeParams dp, const DecodeListParams lp, const MixedParams mp) {
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ CUtensorMap tmap_qd, const PrefillParams pp,
+                        const PrefillParams pq, const DecodeParams dp, const DecodeListParams lp,
+                        const MixedParams mp) {
   griddep_wait();  // the plan, the f16 V pages and the appended rows are in place
   using L = PrefillSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -87,18 +98,34 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  const long long Q = mp.num_prefix_items;
   const long long P = mp.num_prefill_items;
-  const long long total = P + mp.seq_item_base[lp.num_seqs];
-  long long span = total * mp.prefill_span_permille / 1000;
+  const long long rest = P + mp.seq_item_base[lp.num_seqs];
+  long long span = rest * mp.prefill_span_permille / 1000;
   if (span < P) span = P;
   if (span < 1) span = 1;
   for (;;) {
     if (threadIdx.x == 0) *item_slot = atomicAdd(mp.counter, 1);
     __syncthreads();
-    const long long pos = *item_slot;
-    const bool stop = pos >= total || *abort_flag;
+    const long long at = *item_slot;
+    const bool stop = at >= Q + rest || *abort_flag;
     __syncthreads();  // every thread has read the slot before it is written again
     if (stop) break;
+    if (at < Q) {
+      // a prefix-group item: the members' queries against the group's prefix
+      // (bf16 V from the pool, P as hi + lo), writing the extra partial
+      const int per_group = pq.kv_heads * mp.prefix_tiles;
+      const int grp = int(at / per_group);
+      const int r = int(at - (long long)grp * per_group);
+      const int kvh = r / mp.prefix_tiles;
+      const int tile = mp.prefix_tiles - 1 - (r - kvh * mp.prefix_tiles);
+      prefill_item<D, G, false>(tmap_qd, tmap_k, tmap_v, pq, smem, tmem, grp * pq.kv_heads + kvh,
+                                tile);
+      fence_proxy_async_smem();
+      __syncthreads();
+      continue;
+    }
+    const long long pos = at - Q;
     // prefill items before position pos: floor(pos P / span) inside the span
     const long long before = pos < span ? pos * P / span : P;
     const bool is_prefill = pos < span && (pos + 1) * P / span > before;
@@ -133,8 +160,9 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
 }
 
 struct MixedLaunch {
-  const CUtensorMap *tmap_q, *tmap_k, *tmap_v16, *tmap_v;
+  const CUtensorMap *tmap_q, *tmap_k, *tmap_v16, *tmap_v, *tmap_qd;
   const PrefillParams* pp;
+  const PrefillParams* pq;
   const DecodeParams* dp;
   const DecodeListParams* lp;
   const MixedParams* mp;
@@ -149,7 +177,8 @@ static cudaError_t launch_mixed_t(const MixedLaunch& m, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   return launch_after_previous(paged_mixed_step_kernel<D, G>, dim3(unsigned(m.ctas)),
                                dim3(kPfThreads), S::kSmemBytes, stream, *m.tmap_q, *m.tmap_k,
-                               *m.tmap_v16, *m.tmap_v, *m.pp, *m.dp, *m.lp, *m.mp);
+                               *m.tmap_v16, *m.tmap_v, *m.tmap_qd, *m.pp, *m.pq, *m.dp, *m.lp,
+                               *m.mp);
 }
 
 template <int D>
@@ -164,33 +193,43 @@ static cudaError_t launch_mixed_d(const MixedLaunch& m, int group, cudaStream_t 
   }
 }
 
+static PrefillParams prefill_params(const PrefillArgs& a) {
+  PrefillParams pp;
+  pp.q_start = a.q_start;
+  pp.block_tables = a.block_tables;
+  pp.context_lens = a.context_lens;
+  pp.out = a.out;
+  pp.lse = a.lse;
+  pp.context_len = 0;
+  pp.out_scale = 1.f;
+  pp.num_seqs = a.num_seqs;
+  pp.q_heads = a.q_heads;
+  pp.kv_heads = a.kv_heads;
+  pp.num_blocks = a.num_blocks;
+  pp.max_blocks_per_seq = a.max_blocks_per_seq;
+  pp.total_q = a.total_q;
+  pp.max_q_len = a.max_q_len;
+  pp.causal = a.causal;
+  pp.scale_log2 = a.scale_log2;
+  pp.v_block_tables = a.v_block_tables;
+  pp.v_num_blocks = a.v_block_tables ? a.v_num_blocks : a.num_blocks;
+  pp.work_counter = nullptr;
+  pp.num_items = 0;
+  pp.tiles_per_pair = 0;
+  pp.out_bf16 = 0;
+  pp.seq_order = a.seq_order;
+  pp.table_rows = a.table_rows;
+  pp.allow_empty = a.allow_empty ? 1 : 0;
+  return pp;
+}
+
 cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* counter,
                               int ctas, int prefill_span_permille, const CUtensorMap* tmap_q,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v16,
-                              const CUtensorMap* tmap_v, cudaStream_t stream) {
+                              const CUtensorMap* tmap_v, cudaStream_t stream,
+                              const PrefillArgs* prefix, const CUtensorMap* tmap_qd) {
   // prefill part: the f16 P V path over the f16 V scratch pages
-  PrefillParams pp;
-  pp.q_start = pa.q_start;
-  pp.block_tables = pa.block_tables;
-  pp.context_lens = pa.context_lens;
-  pp.out = pa.out;
-  pp.lse = nullptr;
-  pp.context_len = 0;
-  pp.out_scale = 1.f;
-  pp.num_seqs = pa.num_seqs;
-  pp.q_heads = pa.q_heads;
-  pp.kv_heads = pa.kv_heads;
-  pp.num_blocks = pa.num_blocks;
-  pp.max_blocks_per_seq = pa.max_blocks_per_seq;
-  pp.total_q = pa.total_q;
-  pp.max_q_len = pa.max_q_len;
-  pp.causal = pa.causal;
-  pp.scale_log2 = pa.scale_log2;
-  pp.v_block_tables = pa.v_block_tables;
-  pp.v_num_blocks = pa.v_num_blocks;
-  pp.work_counter = nullptr;
-  pp.out_bf16 = 0;
-  pp.seq_order = pa.seq_order;
+  PrefillParams pp = prefill_params(pa);
   constexpr int TPC = kPfQTiles * kPfRows;  // query rows per item
   const int group = pa.q_heads / pa.kv_heads;
   const int tokens_per_item = TPC / group;
@@ -220,6 +259,19 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
   dp.extra_o = nullptr;
   dp.extra_lse = nullptr;
   dp.out_bf16 = 0;
+  dp.seq_first_block = da.seq_first_block;
+  dp.force_partials = da.force_partials;
+  dp.extra_o = da.extra_o;
+  dp.extra_lse = da.extra_lse;
+  // prefix-group items (none without groups)
+  PrefillParams pq = prefix ? prefill_params(*prefix) : pp;
+  long long qitems = 0;
+  int qtiles = 0;
+  if (prefix) {
+    qtiles = (prefix->max_q_len + tokens_per_item - 1) / tokens_per_item;
+    qitems = (long long)prefix->num_seqs * prefix->kv_heads * qtiles;
+    if (qitems > INT32_MAX / 2) return cudaErrorInvalidValue;
+  }
   DecodeListParams lp;
   lp.seq_item_base = da.list_base;
   lp.num_seqs = da.num_seqs;
@@ -232,12 +284,15 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
   mp.num_prefill_items = int(items);
   mp.tiles_per_pair = tiles;
   mp.prefill_span_permille = prefill_span_permille;
+  mp.num_prefix_items = int(qitems);
+  mp.prefix_tiles = qtiles;
   // 1. the decode plan (and the zeroed counter)
   cudaError_t e = launch_after_previous(mixed_plan_kernel, dim3(1), dim3(512), 0, stream, dp, lp,
                                         counter);
   if (e != cudaSuccess) return e;
   // 2. the fused launch
-  MixedLaunch m{tmap_q, tmap_k, tmap_v16, tmap_v, &pp, &dp, &lp, &mp, ctas};
+  MixedLaunch m{tmap_q, tmap_k, tmap_v16, tmap_v, prefix ? tmap_qd : tmap_q, &pp, &pq, &dp, &lp,
+                &mp, ctas};
   if (pa.d_head == 128) e = launch_mixed_d<128>(m, group, stream);
   else if (pa.d_head == 64) e = launch_mixed_d<64>(m, group, stream);
   else e = cudaErrorInvalidValue;

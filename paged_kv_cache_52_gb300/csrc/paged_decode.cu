@@ -35,6 +35,7 @@
 //    its log2-sum-exp, and a small merge kernel combines the partitions.
 //  * every mbarrier wait is bounded; a timeout sets an error bit, drains the
 //    warp's outstanding copies (also bounded) and lets the CTA finish.
+#include <algorithm>
 #include <climits>
 #include <utility>
 
@@ -58,7 +59,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
 
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p, seq);
   if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
   const int nparts_s = span_parts(sp, p);
   if (part >= nparts_s) return;
@@ -127,12 +128,19 @@ __global__ void __launch_bounds__(256) paged_decode_merge_list_kernel(const Deco
   const int kvh = h / G;
   const int b = __ldg(lp.seq_item_base + seq);
   const int runs = (__ldg(lp.seq_item_base + seq + 1) - b) / p.kv_heads;
-  if (runs <= 1) return;  // written by the decode kernel
+  const bool extra = has_extra(p, seq);
+  if (runs <= 1 && !extra) return;  // written by the decode kernel
   const size_t r0 = size_t(b + kvh * runs) * G + (h - kvh * G);
-  float big = -INFINITY;
+  float big = extra ? __ldg(p.extra_lse + row) : -INFINITY;
   for (int r = 0; r < runs; ++r) big = fmaxf(big, __ldg(p.part_lse + r0 + size_t(r) * G));
   float tot = 0.f;
   float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (extra) {
+    const float w = ex2(__ldg(p.extra_lse + row) - big);
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p.extra_o + row * D) + c4);
+    tot += w;
+    val = make_float4(w * x.x, w * x.y, w * x.z, w * x.w);
+  }
 #pragma unroll 4
   for (int r = 0; r < runs; ++r) {
     const size_t pr = r0 + size_t(r) * G;
@@ -161,9 +169,9 @@ __global__ void __launch_bounds__(D) paged_decode_merge_kernel(const DecodeParam
   griddep_wait();
   const size_t row = blockIdx.x;  // seq * q_heads + head
   const int seq = int(row / p.q_heads);
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p, seq);
   const int nparts_s = span_parts(sp, p);
-  const bool extra = p.extra_o != nullptr;
+  const bool extra = has_extra(p, seq);
   if (nparts_s == 1 && !p.force_partials) return;  // written by the split kernel
   const float* lse = p.part_lse + row * p.num_parts;
   const float* po = p.part_o + row * p.num_parts * D + threadIdx.x;
@@ -197,9 +205,9 @@ __global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodePa
   const int c4 = int(gtid - row * TPR);
   if (row >= total_rows) return;
   const int seq = int(row / p.q_heads);
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p, seq);
   const int nparts_s = span_parts(sp, p);
-  const bool extra = p.extra_o != nullptr;
+  const bool extra = has_extra(p, seq);
   if (nparts_s == 1 && !p.force_partials) return;  // written by the split kernel
   const float* lse = p.part_lse + row * p.num_parts;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + row * p.num_parts * D) + c4;
@@ -361,6 +369,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.extra_o = a.extra_o;
   prm.extra_lse = a.extra_lse;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
+  prm.seq_first_block = a.seq_first_block;
   const int group = a.q_heads / a.kv_heads;
   if (a.list) {
     if (a.num_seqs > kListMaxSeqs || a.list_items <= 0) return cudaErrorInvalidValue;
@@ -381,6 +390,80 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
+}
+
+// Prefix groups (see launch_prefix_groups_setup): one thread per sequence,
+// then one per group.
+__global__ void prefix_groups_setup_kernel(const int32_t* group_start,
+                                           const int32_t* group_prefix_blocks, int num_groups,
+                                           int uniform_prefix_blocks, int num_seqs,
+                                           const int32_t* block_tables, int max_blocks,
+                                           const int32_t* context_lens, int max_prefix_blocks,
+                                           int32_t* seq_first_block, int32_t* group_ctx) {
+  griddep_wait();
+  const bool uniform = group_start == nullptr;
+  const int groups = uniform ? 1 : num_groups;
+  auto prefix_of = [&](int g) {
+    const int pb = uniform ? uniform_prefix_blocks : __ldg(group_prefix_blocks + g);
+    return (pb >= 1 && pb <= max_prefix_blocks && pb <= max_blocks) ? pb : 0;
+  };
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < num_seqs + groups;
+       t += stride) {
+    if (t >= num_seqs) {  // a group's prefix length in tokens
+      const int g = int(t - num_seqs);
+      group_ctx[g] = prefix_of(g) * kBlockTokens;
+      continue;
+    }
+    const int s = int(t);
+    int g = 0, lead = 0;
+    bool in_group = true;
+    if (!uniform) {  // the last group starting at or before s
+      int lo = 0, hi = num_groups - 1;
+      in_group = num_groups > 0 && __ldg(group_start) <= s;
+      while (in_group && lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(group_start + mid) <= s) lo = mid;
+        else hi = mid - 1;
+      }
+      g = lo;
+      lead = in_group ? __ldg(group_start + g) : 0;
+      in_group = in_group && s < __ldg(group_start + g + 1) && lead >= 0;
+    }
+    int pb = in_group ? prefix_of(g) : 0;
+    bool bad = in_group && pb == 0;  // a group whose prefix length is out of range
+    if (pb > 0 && __ldg(context_lens + s) < pb * kBlockTokens) {
+      pb = 0;  // the prefix is longer than the context
+      bad = true;
+    }
+    if (pb > 0 && s != lead) {
+      const int32_t* mine = block_tables + size_t(s) * max_blocks;
+      const int32_t* theirs = block_tables + size_t(lead) * max_blocks;
+      for (int j = 0; j < pb; ++j)
+        if (__ldg(mine + j) != __ldg(theirs + j)) {
+          pb = 0;
+          bad = true;
+          break;
+        }
+    }
+    if (bad) atomicOr(&g_decode_error, kErrPrefixMismatch);
+    seq_first_block[s] = pb;
+  }
+}
+
+cudaError_t launch_prefix_groups_setup(const int32_t* group_start,
+                                       const int32_t* group_prefix_blocks, int num_groups,
+                                       int uniform_prefix_blocks, int num_seqs,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int max_prefix_blocks,
+                                       int32_t* seq_first_block, int32_t* group_ctx,
+                                       cudaStream_t stream) {
+  const long long work = (long long)num_seqs + (group_start ? num_groups : 1);
+  const int blocks = int(std::min<long long>((work + 255) / 256, 1024));
+  return launch_after_previous(prefix_groups_setup_kernel, dim3(blocks), dim3(256), 0, stream,
+                               group_start, group_prefix_blocks, num_groups,
+                               uniform_prefix_blocks, num_seqs, block_tables, max_blocks_per_seq,
+                               context_lens, max_prefix_blocks, seq_first_block, group_ctx);
 }
 
 int decode_max_partition_blocks() { return kMaxPartitionBlocks; }

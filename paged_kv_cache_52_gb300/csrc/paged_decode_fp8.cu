@@ -297,7 +297,7 @@ paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int seq = pair / p.kv_heads;
   const int kvh = pair - seq * p.kv_heads;
 
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p, seq);
   const int len = sp.len;
   if (sp.bad && part == 0 && threadIdx.x == 0) atomicOr(&g_decode_fp8_error, kErrBadContext);
   const int nparts_s = span_parts(sp, p);

@@ -204,6 +204,8 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.tiles_per_pair = 0;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
   prm.seq_order = a.seq_order;
+  prm.table_rows = a.table_rows;
+  prm.allow_empty = a.allow_empty ? 1 : 0;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
     if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);

@@ -83,7 +83,7 @@ paged_verify_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int K = vp.q_len;
   const int rows_used = G * K;  // <= R (checked on the host)
 
-  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p);
+  const SeqSpan sp = seq_span(__ldg(p.context_lens + seq), p, seq);
   const int len = sp.len;
   if (part == 0 && threadIdx.x == 0) {
     if (sp.bad) atomicOr(&g_verify_error, kErrBadContext);

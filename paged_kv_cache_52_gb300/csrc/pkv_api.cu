@@ -245,19 +245,21 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   return PKV_OK;
 }
 
-// Workspace of the shared-prefix decode: suffix partials (always written),
-// then the prefix part's normalised output and log2-sum-exp.
+// Workspace of the shared-prefix decode: the own pages' partials (always
+// written), the prefix part's normalised output and log2-sum-exp, then each
+// sequence's first own block and each group's prefix length.  The own pages
+// are planned over the whole max_context_len, so a member whose prefix check
+// fails (and falls back to its whole context) is still covered.
 struct CascadePlan {
   Plan suffix;
-  size_t part_o_off = 0, part_lse_off = 0, pre_o_off = 0, pre_lse_off = 0, total = 0;
+  size_t part_o_off = 0, part_lse_off = 0, pre_o_off = 0, pre_lse_off = 0;
+  size_t first_off = 0, ctx_off = 0, total = 0;
 };
 
 int make_cascade_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
-                      int prefix_blocks, CascadePlan* cp) {
-  if (prefix_blocks <= 0) return PKV_EINVAL;
-  const int suffix_len = max_context_len > prefix_blocks * kBlockSize
-                             ? max_context_len - prefix_blocks * kBlockSize : 0;
-  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, suffix_len, 0, &cp->suffix);
+                      int num_groups, CascadePlan* cp) {
+  if (num_groups < 1) return PKV_EINVAL;
+  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &cp->suffix);
   if (st != PKV_OK) return st;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = size_t(num_seqs) * size_t(q_heads);
@@ -266,7 +268,9 @@ int make_cascade_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int m
   cp->part_lse_off = up(prow * d_head * sizeof(float));
   cp->pre_o_off = cp->part_lse_off + up(prow * sizeof(float));
   cp->pre_lse_off = cp->pre_o_off + up(rows * d_head * sizeof(float));
-  cp->total = cp->pre_lse_off + up(rows * sizeof(float));
+  cp->first_off = cp->pre_lse_off + up(rows * sizeof(float));
+  cp->ctx_off = cp->first_off + up(size_t(num_seqs) * sizeof(int32_t));
+  cp->total = cp->ctx_off + up(size_t(num_groups) * sizeof(int32_t));
   return PKV_OK;
 }
 
@@ -659,10 +663,14 @@ struct MixedLayout {
   Fp8PrefillLayout pre;  // offsets from its v_off
   Plan dec;
   size_t pre_bytes = 0, dec_off = 0, counter_off = 0, total = 0;
+  // decode prefix groups: the prefix part's output and log2-sum-exp, each
+  // decode's first own block, each group's prefix length
+  size_t pre_o_off = 0, pre_lse_off = 0, first_off = 0, ctx_off = 0;
 };
 
 int mixed_layout(int num_prefill, int prefill_max_blocks, int num_decode, int q_heads,
-                 int kv_heads, int d_head, int max_decode_context_len, MixedLayout* m) {
+                 int kv_heads, int d_head, int max_decode_context_len, int num_groups,
+                 MixedLayout* m) {
   if (!fp8_prefill_layout(num_prefill, prefill_max_blocks, kv_heads, d_head, &m->pre))
     return PKV_EUNSUPPORTED;
   const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
@@ -675,6 +683,14 @@ int mixed_layout(int num_prefill, int prefill_max_blocks, int num_decode, int q_
   m->dec_off = up(m->pre_bytes);
   m->counter_off = m->dec_off + up(m->dec.ws_bytes);
   m->total = m->counter_off + 256;
+  if (num_groups > 0) {
+    const size_t rows = size_t(num_decode) * size_t(q_heads);
+    m->pre_o_off = m->total;
+    m->pre_lse_off = m->pre_o_off + up(rows * size_t(d_head) * sizeof(float));
+    m->first_off = m->pre_lse_off + up(rows * sizeof(float));
+    m->ctx_off = m->first_off + up(size_t(num_decode) * sizeof(int32_t));
+    m->total = m->ctx_off + up(size_t(num_groups) * sizeof(int32_t));
+  }
   return PKV_OK;
 }
 
@@ -683,9 +699,19 @@ int mixed_layout(int num_prefill, int prefill_max_blocks, int num_decode, int q_
 size_t pkv_mixed_step_workspace_bytes(int num_prefill, int prefill_max_blocks, int num_decode,
                                       int q_heads, int kv_heads, int d_head,
                                       int max_decode_context_len) {
+  return pkv_mixed_step_groups_workspace_bytes(num_prefill, prefill_max_blocks, num_decode,
+                                               q_heads, kv_heads, d_head, max_decode_context_len,
+                                               0);
+}
+
+size_t pkv_mixed_step_groups_workspace_bytes(int num_prefill, int prefill_max_blocks,
+                                             int num_decode, int q_heads, int kv_heads,
+                                             int d_head, int max_decode_context_len,
+                                             int num_groups) {
   MixedLayout m;
-  if (mixed_layout(num_prefill, prefill_max_blocks, num_decode, q_heads, kv_heads, d_head,
-                   max_decode_context_len, &m) != PKV_OK)
+  if (num_groups < 0 ||
+      mixed_layout(num_prefill, prefill_max_blocks, num_decode, q_heads, kv_heads, d_head,
+                   max_decode_context_len, num_groups, &m) != PKV_OK)
     return 0;
   return m.total;
 }
@@ -698,9 +724,17 @@ int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, i
                                 const int32_t* decode_context_lens, int max_decode_context_len,
                                 int q_heads, const void* k_cache, const void* v_cache,
                                 pkv_cache_desc cache, float scale, float* out_prefill,
-                                float* out_decode, void* workspace, size_t ws_bytes,
-                                int prefill_span_permille, pkv_stream_t stream) {
+                                float* out_decode, const int32_t* decode_group_start,
+                                const int32_t* decode_group_prefix_blocks, int num_groups,
+                                int max_group_size, int max_prefix_blocks, void* workspace,
+                                size_t ws_bytes, int prefill_span_permille, pkv_stream_t stream) {
   if (prefill_span_permille < 0 || prefill_span_permille > 1000) return PKV_EINVAL;
+  if (num_groups < 0) return PKV_EINVAL;
+  if (num_groups > 0 && (!decode_group_start || !decode_group_prefix_blocks ||
+                         !aligned(decode_group_start, 4) ||
+                         !aligned(decode_group_prefix_blocks, 4) || max_group_size < 1 ||
+                         max_prefix_blocks < 1))
+    return PKV_EINVAL;
   if (prefill_span_permille == 0) prefill_span_permille = kMixedPrefillSpanPermille;
   int st = check_prefill(q_prefill, q_start, num_prefill, total_q, max_q_len, q_heads, k_cache,
                          v_cache, cache, prefill_block_tables, prefill_max_blocks,
@@ -716,7 +750,7 @@ int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, i
     return PKV_EINVAL;
   MixedLayout m;
   st = mixed_layout(num_prefill, prefill_max_blocks, num_decode, q_heads, cache.kv_heads,
-                    cache.d_head, max_decode_context_len, &m);
+                    cache.d_head, max_decode_context_len, num_groups, &m);
   if (st != PKV_OK) return st;
   if (!workspace || ws_bytes < m.total) return PKV_ENOMEM;
   if (!aligned(workspace, 256)) return PKV_EINVAL;
@@ -783,8 +817,47 @@ int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, i
   da.list_min_run = kListMinRun;
   da.list_max_blocks = std::min(m.dec.list_max_blocks, decode_max_blocks);
   da.list_items = m.dec.list_items;
+  pkv::PrefillArgs qa;  // the prefix groups' pass over the decode queries
+  CUtensorMap tqd;
+  if (num_groups > 0) {
+    float* pre_o = reinterpret_cast<float*>(ws + m.pre_o_off);
+    float* pre_lse = reinterpret_cast<float*>(ws + m.pre_lse_off);
+    int32_t* seq_first = reinterpret_cast<int32_t*>(ws + m.first_off);
+    int32_t* group_ctx = reinterpret_cast<int32_t*>(ws + m.ctx_off);
+    e = pkv::launch_prefix_groups_setup(decode_group_start, decode_group_prefix_blocks,
+                                        num_groups, 0, num_decode, decode_block_tables,
+                                        decode_max_blocks, decode_context_lens,
+                                        std::min(max_prefix_blocks, decode_max_blocks), seq_first,
+                                        group_ctx, cs);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (!encode_query_map(&tqd, q_decode, num_decode, q_heads, cache.d_head, group,
+                          pkv::prefill_rows_per_tile() / group))
+      return PKV_ECUDA;
+    qa.q_start = decode_group_start;
+    qa.block_tables = decode_block_tables;
+    qa.table_rows = decode_group_start;
+    qa.context_lens = group_ctx;
+    qa.out = pre_o;
+    qa.lse = pre_lse;
+    qa.num_seqs = num_groups;
+    qa.total_q = num_decode;
+    qa.max_q_len = max_group_size;
+    qa.q_heads = q_heads;
+    qa.kv_heads = cache.kv_heads;
+    qa.d_head = cache.d_head;
+    qa.num_blocks = cache.num_blocks;
+    qa.max_blocks_per_seq = decode_max_blocks;
+    qa.causal = 0;
+    qa.scale_log2 = scale * 1.4426950408889634f;
+    qa.allow_empty = true;
+    da.seq_first_block = seq_first;
+    da.force_partials = 1;
+    da.extra_o = pre_o;
+    da.extra_lse = pre_lse;
+  }
   e = pkv::launch_mixed_step(pa, da, reinterpret_cast<int*>(ws + m.counter_off), sms,
-                             prefill_span_permille, &tq, &tk, &tv16, &tv, cs);
+                             prefill_span_permille, &tq, &tk, &tv16, &tv, cs,
+                             num_groups > 0 ? &qa : nullptr, num_groups > 0 ? &tqd : nullptr);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -802,7 +875,8 @@ int pkv_mixed_step_attention(const void* q_prefill, const int32_t* q_start, int 
       q_prefill, q_start, num_prefill, total_q, max_q_len, prefill_block_tables,
       prefill_max_blocks, prefill_context_lens, causal, q_decode, num_decode, decode_block_tables,
       decode_max_blocks, decode_context_lens, max_decode_context_len, q_heads, k_cache, v_cache,
-      cache, scale, out_prefill, out_decode, workspace, ws_bytes, 0, stream);
+      cache, scale, out_prefill, out_decode, nullptr, nullptr, 0, 0, 0, workspace, ws_bytes, 0,
+      stream);
 }
 
 int pkv_paged_decode_attention_bf16out(const void* q, int num_seqs, int q_heads,
@@ -1178,57 +1252,90 @@ int pkv_paged_verify_attention_bf16out(const void* q, int num_seqs, int q_len, i
 size_t pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
                                                  int d_head, int max_context_len,
                                                  int prefix_blocks) {
+  if (prefix_blocks <= 0) return 0;
   CascadePlan cp;
-  if (make_cascade_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, prefix_blocks,
-                        &cp) != PKV_OK)
+  if (make_cascade_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 1, &cp) != PKV_OK)
     return 0;
   return cp.total;
 }
 
-int pkv_paged_decode_attention_shared_prefix(
-    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
-    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
-    const int32_t* context_lens, int max_context_len, int prefix_blocks, float scale, float* out,
-    void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+size_t pkv_decode_prefix_groups_workspace_bytes(int num_seqs, int q_heads, int kv_heads,
+                                                int d_head, int max_context_len,
+                                                int num_groups) {
+  CascadePlan cp;
+  if (make_cascade_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, num_groups, &cp) !=
+      PKV_OK)
+    return 0;
+  return cp.total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The shared-prefix (cascade) decode over prefix groups.  group_start null:
+// one group of all sequences with uniform_prefix_blocks.
+int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache,
+                   const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                   const int32_t* group_start, const int32_t* group_prefix_blocks,
+                   int num_groups, int max_group_size, int max_prefix_blocks,
+                   int uniform_prefix_blocks, float scale, float* out, void* workspace,
+                   size_t ws_bytes, pkv_stream_t stream) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
+  const bool uniform = group_start == nullptr;
+  const int groups = uniform ? 1 : num_groups;
+  if (groups < 1 || max_prefix_blocks < 1 || max_group_size < 1) return PKV_EINVAL;
   CascadePlan cp;
-  st = make_cascade_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
-                         prefix_blocks, &cp);
+  st = make_cascade_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, groups,
+                         &cp);
   if (st != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
-  if (max_blocks_per_seq < prefix_blocks || !std::isfinite(scale)) return PKV_EINVAL;
+  if (!uniform && !group_prefix_blocks) return PKV_EINVAL;
+  if (max_blocks_per_seq < 1 || !std::isfinite(scale)) return PKV_EINVAL;
   if ((long long)num_seqs > 65535 * 128LL) return PKV_EUNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4) ||
+      (!uniform && (!aligned(group_start, 4) || !aligned(group_prefix_blocks, 4))))
     return PKV_EINVAL;
   if (!workspace || ws_bytes < cp.total) return PKV_ENOMEM;
   if (!aligned(workspace, 256)) return PKV_EINVAL;
   char* ws = static_cast<char*>(workspace);
   float* pre_o = reinterpret_cast<float*>(ws + cp.pre_o_off);
   float* pre_lse = reinterpret_cast<float*>(ws + cp.pre_lse_off);
+  int32_t* seq_first = reinterpret_cast<int32_t*>(ws + cp.first_off);
+  int32_t* group_ctx = reinterpret_cast<int32_t*>(ws + cp.ctx_off);
   const int group = q_heads / cache.kv_heads;
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // 1. the shared prefix: every sequence's query against the prefix keys,
-  //    non-causal, on the tensor cores (one pseudo-sequence of num_seqs rows)
+  // 0. each sequence's first own block (its members checked against the
+  //    group leader's ids) and each group's prefix length
+  cudaError_t e = pkv::launch_prefix_groups_setup(
+      group_start, group_prefix_blocks, num_groups, uniform_prefix_blocks, num_seqs, block_tables,
+      max_blocks_per_seq, context_lens, std::min(max_prefix_blocks, max_blocks_per_seq), seq_first,
+      group_ctx, s);
+  if (e != cudaSuccess) return PKV_ECUDA;
+
+  // 1. every group's queries against its prefix keys, non-causal, on the
+  //    tensor cores (a group is one pseudo-sequence of its members' rows)
   CUtensorMap tq, tk, tv;
   const int rows_per_tile = pkv::prefill_rows_per_tile();
   if (!encode_query_map(&tq, q, num_seqs, q_heads, cache.d_head, group, rows_per_tile / group) ||
       !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
     return PKV_ECUDA;
   pkv::PrefillArgs pa;
-  pa.q_start = nullptr;
-  pa.block_tables = block_tables;  // row 0 holds the shared prefix
-  pa.context_lens = nullptr;
-  pa.context_len = prefix_blocks * kBlockSize;
+  pa.q_start = group_start;       // null: one group of all rows
+  pa.block_tables = block_tables;
+  pa.table_rows = group_start;    // a group reads its leader's row (null: row 0)
+  pa.context_lens = group_ctx;
   pa.out = pre_o;
   pa.lse = pre_lse;
-  pa.num_seqs = 1;
+  pa.num_seqs = groups;
   pa.total_q = num_seqs;
-  pa.max_q_len = num_seqs;
+  pa.max_q_len = uniform ? num_seqs : max_group_size;
   pa.q_heads = q_heads;
   pa.kv_heads = cache.kv_heads;
   pa.d_head = cache.d_head;
@@ -1236,10 +1343,11 @@ int pkv_paged_decode_attention_shared_prefix(
   pa.max_blocks_per_seq = max_blocks_per_seq;
   pa.causal = 0;
   pa.scale_log2 = scale_log2;
-  cudaError_t e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
+  pa.allow_empty = true;          // a group with an invalid prefix has none
+  e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
   if (e != cudaSuccess) return PKV_ECUDA;
 
-  // 2. each sequence's own blocks after the prefix, split-K, partials only;
+  // 2. each sequence's own blocks after its prefix, split-K, partials only;
   // 3. the merge folds the prefix part in as one more partial
   pkv::DecodeArgs a;
   a.q = q;
@@ -1258,12 +1366,42 @@ int pkv_paged_decode_attention_shared_prefix(
   a.num_parts = cp.suffix.num_parts;
   a.scale_log2 = scale_log2;
   a.out_scale = 1.f;
-  a.first_block = prefix_blocks;
+  a.seq_first_block = seq_first;
   a.force_partials = 1;
   a.extra_o = pre_o;
   a.extra_lse = pre_lse;
   e = pkv::launch_paged_decode(a, &tk, &tv, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_decode_attention_shared_prefix(
+    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, int prefix_blocks, float scale, float* out,
+    void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+  if (prefix_blocks <= 0 || prefix_blocks > max_blocks_per_seq) return PKV_EINVAL;
+  return cascade_decode(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                        max_blocks_per_seq, context_lens, max_context_len, nullptr, nullptr, 1,
+                        num_seqs > 0 ? num_seqs : 1, prefix_blocks, prefix_blocks, scale, out,
+                        workspace, ws_bytes, stream);
+}
+
+int pkv_paged_decode_attention_prefix_groups(
+    const void* q, int num_seqs, int q_heads, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int max_group_size,
+    int max_prefix_blocks, float scale, float* out, void* workspace, size_t ws_bytes,
+    pkv_stream_t stream) {
+  if (!group_start) return PKV_EINVAL;
+  return cascade_decode(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                        max_blocks_per_seq, context_lens, max_context_len, group_start,
+                        group_prefix_blocks, num_groups, max_group_size, max_prefix_blocks, 0,
+                        scale, out, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -446,12 +446,6 @@ struct DecodeListTile {
   static constexpr int kSmemBytes = kPlanOffset + (kListMaxSeqs + 1) * 4 + 1024;  // +align slack
 };
 
-// Pages of a sequence in the list plan: its context clamped to max_blocks.
-__device__ __forceinline__ int list_pages(int len, int max_blocks) {
-  int n = len <= 0 ? 0 : (len + kBlockTokens - 1) / kBlockTokens;
-  return n < max_blocks ? n : max_blocks;
-}
-
 // The list plan of S <= kListMaxSeqs sequences, computed by all NT threads of
 // a block: base[s] = the first run of sequence s (its KV heads' runs are
 // consecutive), base[S] = the run count.  The run size c is the smallest in
@@ -481,10 +475,13 @@ __device__ void list_plan(const DecodeParams& p, const DecodeListParams& lp, int
   // pages of this thread's sequences (thread t owns t * PER ..., in order)
   int n[PER];
   long long mine = 0, top = 0;
+  bool pre[PER];  // the sequence merges a shared-prefix partial
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int s = threadIdx.x * PER + j;
-    n[j] = s < S ? list_pages(p.context_lens[s], lp.max_blocks) : 0;
+    int f = 0;
+    n[j] = s < S ? list_own_pages(p, lp, s, &f) : 0;
+    pre[j] = f > 0 && p.extra_o != nullptr;
     mine += n[j];
     top = n[j] > top ? n[j] : top;
   }
@@ -502,11 +499,14 @@ __device__ void list_plan(const DecodeParams& p, const DecodeListParams& lp, int
 #pragma unroll
   for (int w = 0; w < NWARPS; ++w) longest = red_ll[w] > longest ? red_ll[w] : longest;
   // runs at run size c, over the block
+  // runs of a sequence: its own pages cut at c; an empty one still takes a
+  // run (it writes zeros) unless a prefix partial carries its whole result
+  auto runs_of = [&](int j, int c) { return n[j] > 0 ? (n[j] + c - 1) / c : (pre[j] ? 0 : 1); };
   auto runs_at = [&](int c) {
     long long r = 0;
 #pragma unroll
     for (int j = 0; j < PER; ++j)
-      if (threadIdx.x * PER + j < S) r += n[j] > 0 ? (n[j] + c - 1) / c : 1;
+      if (threadIdx.x * PER + j < S) r += runs_of(j, c);
     return block_sum(r) * p.kv_heads;
   };
   long long lo = (pages * p.kv_heads + lp.target_items - 1) / lp.target_items;
@@ -529,7 +529,7 @@ __device__ void list_plan(const DecodeParams& p, const DecodeListParams& lp, int
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int s = threadIdx.x * PER + j;
-    k[j] = s < S ? (n[j] > 0 ? (n[j] + c - 1) / c : 1) : 0;
+    k[j] = s < S ? runs_of(j, c) : 0;
     kmine += k[j];
   }
   int incl = kmine;
@@ -576,20 +576,24 @@ __device__ __forceinline__ void list_item(const CUtensorMap& tmap_k, const CUten
   const int kvh = local / runs;
   const int run = local - kvh * runs;
   const int raw_len = p.context_lens[seq];
-  const int ns = list_pages(raw_len, lp.max_blocks);
+  int first = 0;
+  const int ns = list_own_pages(p, lp, seq, &first);  // pages after the shared prefix
+  const int end = (first + ns) * kBlockTokens;
   int len = raw_len < 0 ? 0 : raw_len;
-  if (len > ns * kBlockTokens) len = ns * kBlockTokens;
+  if (len > end) len = end;
   if (len != raw_len && kvh == 0 && run == 0 && threadIdx.x == 0)
     atomicOr(&g_decode_error, kErrBadContext);
   const size_t row0 = size_t(seq) * p.q_heads + size_t(kvh) * G;
-  if (ns == 0) {  // empty context: zeros (one run)
+  if (ns == 0) {  // empty context: zeros (one run; a prefix partial takes no run)
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p, row0 * D + i, 0.f);
     return;
   }
-  const int b0 = int((long long)run * ns / runs);
-  const int b1 = int((long long)(run + 1) * ns / runs);
-  decode_run<D, G, NW>(tmap_k, tmap_v, p, smem, seq, kvh, b0, b1 - b0, len, runs == 1,
-                   size_t(item) * G, 1);
+  const int b0 = first + int((long long)run * ns / runs);
+  const int b1 = first + int((long long)(run + 1) * ns / runs);
+  // a sequence with a prefix partial always leaves its runs to the merge
+  const bool final_out = runs == 1 && !has_extra(p, seq);
+  decode_run<D, G, NW>(tmap_k, tmap_v, p, smem, seq, kvh, b0, b1 - b0, len, final_out,
+                       size_t(item) * G, 1);
 }
 
 }  // namespace pkv

@@ -29,7 +29,20 @@ struct DecodeParams {
   const float* extra_lse;  // [S][q_heads] its log2-sum-exp
   // nonzero: out holds bf16 (the fp32 result rounded to nearest even)
   int out_bf16 = 0;
+  // prefix groups: sequence s attends blocks [seq_first_block[s], ...) and
+  // merges the extra partial only when that is nonzero (null: first_block)
+  const int32_t* seq_first_block = nullptr;
 };
+
+// First block a sequence's own pages start at (0: no shared prefix).
+__device__ __forceinline__ int first_block_of(const DecodeParams& p, int seq) {
+  return p.seq_first_block ? p.seq_first_block[seq] : p.first_block;
+}
+
+// Whether the row's sequence merges the extra (shared-prefix) partial.
+__device__ __forceinline__ bool has_extra(const DecodeParams& p, int seq) {
+  return p.extra_o != nullptr && first_block_of(p, seq) > 0;
+}
 
 // Store element i of the final output in the caller's precision.
 __device__ __forceinline__ void store_out(const DecodeParams& p, size_t i, float v) {
@@ -50,7 +63,7 @@ struct SeqSpan {
   bool bad;   // the context length had to be clamped
 };
 
-__device__ __forceinline__ SeqSpan seq_span(int raw_len, const DecodeParams& p) {
+__device__ __forceinline__ SeqSpan seq_span(int raw_len, const DecodeParams& p, int seq) {
   SeqSpan sp;
   sp.bad = false;
   int len = raw_len;
@@ -63,7 +76,7 @@ __device__ __forceinline__ SeqSpan seq_span(int raw_len, const DecodeParams& p) 
     nblk = p.max_blocks_per_seq;
     sp.bad = true;
   }
-  sp.first = p.first_block;
+  sp.first = first_block_of(p, seq);
   if (sp.first > 0 && len < sp.first * kBlockTokens) sp.bad = true;  // shorter than the prefix
   sp.count = nblk > sp.first ? nblk - sp.first : 0;
   const int covered = p.num_parts * p.partition_blocks;
@@ -94,6 +107,22 @@ struct DecodeListParams {
   int min_run;             // pages
   int max_blocks;          // page bound per sequence (block table and host max_context_len)
 };
+
+// Pages of a sequence in the list plan: its context clamped to max_blocks.
+__device__ __forceinline__ int list_pages(int len, int max_blocks) {
+  int n = len <= 0 ? 0 : (len + kBlockTokens - 1) / kBlockTokens;
+  return n < max_blocks ? n : max_blocks;
+}
+
+// The sequence's own pages in the list plan (after its shared prefix), and
+// the first of them.
+__device__ __forceinline__ int list_own_pages(const DecodeParams& p, const DecodeListParams& lp,
+                                              int seq, int* first) {
+  const int f = first_block_of(p, seq);
+  const int n = list_pages(p.context_lens[seq], lp.max_blocks) - f;
+  *first = f;
+  return n > 0 ? n : 0;
+}
 
 // The merge of a list decode's runs (after the kernel that wrote them).
 cudaError_t launch_decode_list_merge(const DecodeParams& prm, const DecodeListParams& lp,

@@ -24,6 +24,7 @@ enum : unsigned {
   kErrBadQueryRange = 1u << 4,  // q_start not monotone / chunk longer than its context
   kErrTmemAlloc = 1u << 5,      // tensor-memory allocation failed
   kErrDuplicateSlot = 1u << 7,  // checked append: two tokens name one slot (nothing written)
+  kErrPrefixMismatch = 1u << 8, // a prefix-group member's prefix is not its group's (not shared)
 };
 
 // A bounded wait gives up after this many polls.  A poll of try_wait on a

@@ -88,6 +88,8 @@ struct DecodeArgs {
   int force_partials = 0;
   const float* extra_o = nullptr;
   const float* extra_lse = nullptr;
+  // prefix groups: per-sequence first block (null: first_block for all)
+  const int32_t* seq_first_block = nullptr;
   bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
   // length-balanced work list (bf16 decode): list_items CTAs (an upper bound
   // on the runs), partials at part_o / part_lse indexed by run * G + head,
@@ -106,6 +108,20 @@ int verify_max_rows();
 cudaError_t launch_paged_verify(const DecodeArgs& a, int q_len, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);
 unsigned read_verify_error(bool clear);
+
+// Prefix groups: for each sequence, the first block of its own pages (the
+// group's prefix length in blocks, or 0 when it has no group, its group's
+// prefix is out of range, longer than its context, or its first ids differ
+// from the group leader's -- those set PKV_DEVERR_PREFIX_MISMATCH), and for
+// each group the prefix length in tokens (0 for an invalid one).
+// group_start null: one group of every sequence with uniform_prefix_blocks.
+cudaError_t launch_prefix_groups_setup(const int32_t* group_start,
+                                       const int32_t* group_prefix_blocks, int num_groups,
+                                       int uniform_prefix_blocks, int num_seqs,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int max_prefix_blocks,
+                                       int32_t* seq_first_block, int32_t* group_ctx,
+                                       cudaStream_t stream);
 
 // Number of K/V stages and warps the decode kernel uses (for the plan).
 int decode_warps_per_cta();
@@ -146,6 +162,10 @@ struct PrefillArgs {
   // optional [num_seqs]: sequences in dispatch order (longest context first);
   // null: index order
   const int32_t* seq_order = nullptr;
+  // optional [num_seqs]: the block_tables row of each sequence (prefix
+  // groups: the leader's row); null: its own row
+  const int32_t* table_rows = nullptr;
+  bool allow_empty = false;  // a context of 0 is skipped without a flag
 };
 
 // Query rows (tokens x heads of a GQA group) per prefill tile.
@@ -163,10 +183,15 @@ unsigned read_prefill_error(bool clear);
 // bf16 decode as a length-balanced list (da.list_* set, partials in
 // da.part_o / part_lse).  Launches the decode plan, the fused kernel and the
 // list merge.  counter: one int of device memory.
+// prefix (optional): the decode prefix groups' pass (bf16 V from the pool,
+// queries through tmap_qd); da then carries seq_first_block and the extra
+// partial's buffers.
 cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* counter,
                               int ctas, int prefill_span_permille, const CUtensorMap* tmap_q,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v16,
-                              const CUtensorMap* tmap_v, cudaStream_t stream);
+                              const CUtensorMap* tmap_v, cudaStream_t stream,
+                              const PrefillArgs* prefix = nullptr,
+                              const CUtensorMap* tmap_qd = nullptr);
 unsigned read_mixed_error(bool clear);
 
 }  // namespace pkv

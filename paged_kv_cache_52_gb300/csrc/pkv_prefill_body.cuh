@@ -69,6 +69,10 @@ struct PrefillParams {
   int tiles_per_pair;           // CTA-sized query tiles of the longest chunk
   int out_bf16;                 // nonzero: out holds bf16, rounded to nearest even
   const int32_t* seq_order;     // [num_seqs] dispatch order of the sequences, or null
+  // [num_seqs] row of block_tables each sequence's pages are in (null: its
+  // own row): a prefix group's queries read the group leader's row
+  const int32_t* table_rows = nullptr;
+  int allow_empty = 0;          // nonzero: a context of 0 is skipped without a flag
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -113,6 +117,7 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
   const int n = qe - qs;
   const bool bad_range = qs < 0 || n < 0 || qe > p.total_q;
   if (!bad_range && n == 0) return;  // nothing to compute for this sequence
+  if (!bad_range && ctx == 0 && p.allow_empty) return;  // an empty prefix group
   // A chunk longer than max_q_len would have tiles the launch does not cover:
   // the whole sequence is rejected rather than computed in part.
   if (bad_range || (p.causal && n > ctx) || ctx <= 0 || ctx > p.max_blocks_per_seq * 16 ||
@@ -170,8 +175,10 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
       issued_q = 1;
     }
     if (is_v && lane == 0) tma_prefetch_desc(&tmap_v);
-    const int32_t* table = (is_v && p.v_block_tables ? p.v_block_tables : p.block_tables) +
-                           size_t(seq) * p.max_blocks_per_seq;
+    const bool own_table = is_v && p.v_block_tables;  // a scratch pool's table: one row per sequence
+    const int row = (!own_table && p.table_rows) ? __ldg(p.table_rows + seq) : seq;
+    const int32_t* table = (own_table ? p.v_block_tables : p.block_tables) +
+                           size_t(row) * p.max_blocks_per_seq;
     const int pool_blocks = is_v ? p.v_num_blocks : p.num_blocks;
     constexpr int kLoads = 8 * (D / 64);  // 8 pages x D/64 column halves
     for (int j = 0; j < ntiles; ++j) {

@@ -32,6 +32,7 @@ DEVERR_BITS = {
     0x20: "tensor memory allocation",
     0x40: "query outside f16 range (fp8 decode)",
     0x80: "duplicate slot (checked append wrote nothing)",
+    0x100: "prefix-group member without its group's prefix (decoded without it)",
 }
 
 
@@ -77,10 +78,12 @@ SIGNATURES = {
                                   ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                   ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                   CacheDesc, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "pkv_mixed_step_groups_workspace_bytes": ([ctypes.c_int] * 8, _sz),
     "pkv_mixed_step_attention_ex": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
                                      ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                      ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
-                                     CacheDesc, _f32, _vp, _vp, _vp, _sz, ctypes.c_int, _vp],
+                                     CacheDesc, _f32, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, _vp, _sz, ctypes.c_int, _vp],
                                     ctypes.c_int),
     "pkv_paged_decode_attention_limited": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp, CacheDesc,
                                             _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
@@ -120,6 +123,12 @@ SIGNATURES = {
                                         ctypes.c_int, _vp, ctypes.c_int, _f32, _f32, _f32, _vp,
                                         _vp, _sz, ctypes.c_int, _vp], ctypes.c_int),
     "pkv_decode_shared_prefix_workspace_bytes": ([ctypes.c_int] * 6, _sz),
+    "pkv_decode_prefix_groups_workspace_bytes": ([ctypes.c_int] * 6, _sz),
+    "pkv_paged_decode_attention_prefix_groups": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                                  CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                                                  _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, _f32, _vp, _vp, _sz, _vp],
+                                                 ctypes.c_int),
     "pkv_paged_decode_attention_shared_prefix": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                                   CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int,
                                                   ctypes.c_int, _f32, _vp, _vp, _sz, _vp],
@@ -467,10 +476,11 @@ def paged_decode_attention_limited(q: torch.Tensor, k_cache: torch.Tensor, v_cac
 
 def mixed_step_workspace(num_prefill: int, prefill_max_blocks: int, num_decode: int,
                          q_heads: int, kv_heads: int, d_head: int, max_decode_context_len: int,
-                         device) -> torch.Tensor:
-    n = lib.pkv_mixed_step_workspace_bytes(int(num_prefill), int(prefill_max_blocks),
-                                           int(num_decode), int(q_heads), int(kv_heads),
-                                           int(d_head), int(max_decode_context_len))
+                         device, num_groups: int = 0) -> torch.Tensor:
+    n = lib.pkv_mixed_step_groups_workspace_bytes(int(num_prefill), int(prefill_max_blocks),
+                                                  int(num_decode), int(q_heads), int(kv_heads),
+                                                  int(d_head), int(max_decode_context_len),
+                                                  int(num_groups))
     _need(n > 0, "unsupported mixed-step shape (more than 512 decode sequences?)")
     return torch.empty(n, dtype=torch.uint8, device=device)
 
@@ -484,11 +494,15 @@ def mixed_step_attention(q_prefill: torch.Tensor, q_start: torch.Tensor,
                          out_prefill: Optional[torch.Tensor] = None,
                          out_decode: Optional[torch.Tensor] = None,
                          workspace: Optional[torch.Tensor] = None,
-                         prefill_span_permille: int = 0):
+                         prefill_span_permille: int = 0,
+                         decode_groups: Optional[tuple] = None):
     """One continuous-batching step's attention in one persistent launch
     (``pkv_mixed_step_attention_ex``): the chunked prefill and the decodes
     over the same pools.  Returns ``(out_prefill, out_decode)``, float32.
-    ``prefill_span_permille``: the work list's interleave (0 = the library's)."""
+    ``prefill_span_permille``: the work list's interleave (0 = the library's).
+    ``decode_groups``: optional ``(group_start, group_prefix_blocks,
+    max_group_size, max_prefix_blocks)`` -- decode prefix groups as in
+    ``paged_decode_attention_prefix_groups`` (int32 device tensors)."""
     _check_cache(k_cache, v_cache)
     for t, n in ((q_prefill, "q_prefill"), (q_decode, "q_decode")):
         _need(t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 3 and t.is_contiguous(),
@@ -508,17 +522,26 @@ def mixed_step_attention(q_prefill: torch.Tensor, q_start: torch.Tensor,
         out_prefill = torch.empty(T, hq, d, dtype=torch.float32, device=q_prefill.device)
     if out_decode is None:
         out_decode = torch.empty(S, hq, d, dtype=torch.float32, device=q_prefill.device)
+    gs = gp = None
+    G = mg = mp = 0
+    if decode_groups is not None:
+        gs, gp, mg, mp = decode_groups
+        G = gs.shape[0] - 1
+        for t, n, rows in ((gs, "group_start", G + 1), (gp, "group_prefix_blocks", G)):
+            _need(t.dtype == torch.int32 and t.is_contiguous() and t.shape == (rows,),
+                  f"{n} must be contiguous int32 [{rows}]")
     if workspace is None:
         workspace = mixed_step_workspace(P, prefill_block_tables.shape[1], S, hq,
                                          k_cache.shape[2], d, max_decode_context_len,
-                                         q_prefill.device)
+                                         q_prefill.device, G)
     st = lib.pkv_mixed_step_attention_ex(
         _ptr(q_prefill), _ptr(q_start), P, T, int(max_q_len), _ptr(prefill_block_tables),
         prefill_block_tables.shape[1], _ptr(prefill_context_lens), int(bool(causal)),
         _ptr(q_decode), S, _ptr(decode_block_tables), decode_block_tables.shape[1],
         _ptr(decode_context_lens), int(max_decode_context_len), hq, _ptr(k_cache), _ptr(v_cache),
-        cache_desc(k_cache), float(scale), _ptr(out_prefill), _ptr(out_decode), _ptr(workspace),
-        workspace.numel(), int(prefill_span_permille), _stream(q_prefill))
+        cache_desc(k_cache), float(scale), _ptr(out_prefill), _ptr(out_decode), _ptr(gs),
+        _ptr(gp), G, int(mg), int(mp), _ptr(workspace), workspace.numel(),
+        int(prefill_span_permille), _stream(q_prefill))
     _check("pkv_mixed_step_attention_ex", st)
     return out_prefill, out_decode
 
@@ -770,6 +793,42 @@ def paged_decode_attention_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), int(prefix_blocks),
         float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(q))
     _check("pkv_paged_decode_attention_shared_prefix", st)
+    return out
+
+
+def paged_decode_attention_prefix_groups(q: torch.Tensor, k_cache: torch.Tensor,
+                                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                         context_lens: torch.Tensor, scale: float,
+                                         group_start: torch.Tensor,
+                                         group_prefix_blocks: torch.Tensor, max_group_size: int,
+                                         max_prefix_blocks: int, max_context_len: int,
+                                         out: Optional[torch.Tensor] = None,
+                                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode with groups of sequences sharing their first pages
+    (``pkv_paged_decode_attention_prefix_groups``): group g is sequences
+    ``group_start[g] .. group_start[g+1]-1`` sharing ``group_prefix_blocks[g]``
+    pages.  float32 ``out [S, Hq, d]``."""
+    _check_cache(k_cache, v_cache)
+    S, hq, d = q.shape
+    G = group_start.shape[0] - 1
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous(), "q: contiguous bf16")
+    for t, n, rows in ((group_start, "group_start", G + 1),
+                       (group_prefix_blocks, "group_prefix_blocks", G)):
+        _need(t.dtype == torch.int32 and t.is_contiguous() and t.shape == (rows,),
+              f"{n} must be contiguous int32 [{rows}]")
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = lib.pkv_decode_prefix_groups_workspace_bytes(S, hq, k_cache.shape[2], d,
+                                                         int(max_context_len), G)
+        _need(n > 0, "unsupported prefix-group shape")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    st = lib.pkv_paged_decode_attention_prefix_groups(
+        _ptr(q), S, hq, _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), _ptr(group_start),
+        _ptr(group_prefix_blocks), G, int(max_group_size), int(max_prefix_blocks), float(scale),
+        _ptr(out), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("pkv_paged_decode_attention_prefix_groups", st)
     return out
 
 

@@ -90,3 +90,58 @@ def test_mixed_step_repeatable(pk):
     a = _run(pk, w)
     b = _run(pk, w)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _run_groups(pk, w, gs, gp, span=0):
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    chunk = w.meta["chunk"]
+    mdl = max(w.meta["decode_lens"])
+    sizes = (gs[1:] - gs[:-1]).tolist()
+    pout, dout = pk.mixed_step_attention(
+        w.q_prefill, w.q_start, w.prefill_tables, w.prefill_lens, True, w.q_decode,
+        w.decode_tables, w.decode_lens, kc, vc, w.scale, chunk, mdl, prefill_span_permille=span,
+        decode_groups=(gs.to(DEV), gp.to(DEV), max(sizes), int(gp.max())))
+    torch.cuda.synchronize()
+    return pout, dout
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(64, 8, 128), (16, 4, 64)])
+def test_mixed_step_prefix_groups_small(pk, hq, hkv, d):
+    # four decode groups over the shared 4-block prefix (one of them claims
+    # only its first 2 blocks), one decode outside every group, and one member
+    # whose third prefix page is a private copy: flagged, decoded whole
+    spec = dataclasses.replace(SMALL, q_heads=hq, kv_heads=hkv, d_head=d)
+    w = wl.make_mixed_workload(spec)
+    spare = w.meta["num_blocks"] - 1
+    used = set(w.prefill_tables.flatten().tolist()) | set(w.decode_tables.flatten().tolist())
+    assert spare not in used
+    w.decode_tables[12, 2] = spare                       # member of group 1
+    gs = torch.tensor([0, 10, 25, 30, 36], dtype=torch.int32)   # decode 36 has no group
+    gp = torch.tensor([4, 4, 2, 4], dtype=torch.int32)
+    pre = PrefillStepOracle(w, range(spec.num_prefill)).output()
+    dec = DecodeStepOracle(_decode_view(w), range(spec.num_decode)).output()
+    for n in ("k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "q_prefill", "q_start",
+              "prefill_tables", "prefill_lens", "q_decode", "decode_tables", "decode_lens"):
+        setattr(w, n, getattr(w, n).to(DEV))
+    pk.get_device_error(clear=True)
+    pout, dout = _run_groups(pk, w, gs, gp)
+    assert pk.get_device_error(clear=True) == 0x100      # the mismatched member
+    assert_attention_close(pout.cpu().numpy(), pre, f"grouped mixed prefill {hq}/{hkv} d{d}")
+    assert_attention_close(dout.cpu().numpy(), dec, f"grouped mixed decode {hq}/{hkv} d{d}")
+
+
+def test_mixed_step_prefix_group_full_size(pk):
+    # the 70B-GQA mixed step with its 248 decodes as one group sharing the
+    # 1024-token prefix: every decode against the oracle, the prefill bit for
+    # bit against the workspace prefill
+    w = wl.make_mixed_workload(device=DEV, gen_device=DEV)
+    S = w.q_decode.shape[0]
+    dor = DecodeStepOracle(_decode_view(w), range(S))
+    gs = torch.tensor([0, S], dtype=torch.int32)
+    gp = torch.tensor([w.meta["shared_prefix"] // 16], dtype=torch.int32)
+    pout, dout = _run_groups(pk, w, gs, gp)
+    _, _, sep = _run(pk, w)
+    assert torch.equal(pout, sep)
+    assert_attention_close(dout.cpu().numpy(), dor.output(), "fused mixed step with prefix group")
+    assert pk.get_device_error(clear=True) == 0
