@@ -113,9 +113,8 @@ def test_mixed_step_prefix_groups_small(pk, hq, hkv, d):
     # whose third prefix page is a private copy: flagged, decoded whole
     spec = dataclasses.replace(SMALL, q_heads=hq, kv_heads=hkv, d_head=d)
     w = wl.make_mixed_workload(spec)
-    spare = w.meta["num_blocks"] - 1
     used = set(w.prefill_tables.flatten().tolist()) | set(w.decode_tables.flatten().tolist())
-    assert spare not in used
+    spare = next(b for b in range(w.meta["num_blocks"]) if b not in used)
     w.decode_tables[12, 2] = spare                       # member of group 1
     gs = torch.tensor([0, 10, 25, 30, 36], dtype=torch.int32)   # decode 36 has no group
     gp = torch.tensor([4, 4, 2, 4], dtype=torch.int32)

@@ -163,9 +163,8 @@ def test_prefix_group_mismatch_is_flagged_and_decoded_whole(pk):
     # member 2 of group 0 keeps a private copy of its third prefix page: its
     # ids differ from the leader's, so it is not shared (the content is not
     # the same either, so only decoding its own pages gives the oracle's result)
-    nb = w.k_cache.shape[0]
-    spare = int(nb - 1)
-    assert spare not in w.block_tables.flatten().tolist()
+    used = set(w.block_tables.flatten().tolist())
+    spare = next(b for b in range(w.k_cache.shape[0]) if b not in used)
     w.block_tables[2, 2] = spare
     ref = DecodeStepOracle(w, range(w.num_seqs)).output()
     pk.get_device_error(clear=True)
