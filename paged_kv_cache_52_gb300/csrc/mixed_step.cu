@@ -16,11 +16,10 @@
 //    one sequence x KV head, computed with the prefill kernel's warp roles) or
 //    a decode run (pages of one sequence x KV head, computed by warps 0-7,
 //    each with its own 3-stage TMA ring, as in the decode kernel).
-//  * the prefill items are spread evenly over the first 9/10 of the list, so
-//    at any moment the CTAs share out between tensor-bound prefill items and
-//    HBM-bound decode runs in proportion to the work left of each kind, and
-//    both kinds finish together; the last tenth holds only decode runs, which
-//    are short and fill the tail.
+//  * the prefill items are spread evenly over the list (or over its first
+//    part, a parameter), so at any moment the CTAs share out between
+//    tensor-bound prefill items and HBM-bound decode runs in proportion to
+//    the work left of each kind, and both kinds finish together.
 //  * the decode runs come from the list plan (a one-CTA plan kernel before
 //    this launch); runs of one pair are merged afterwards by the list merge.
 //  * with prefix groups (decodes whose first pages are the same physical
@@ -220,6 +219,7 @@ static PrefillParams prefill_params(const PrefillArgs& a) {
   pp.seq_order = a.seq_order;
   pp.table_rows = a.table_rows;
   pp.allow_empty = a.allow_empty ? 1 : 0;
+  pp.defer_wait = 0;
   return pp;
 }
 

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   griddep_wait();  // inputs may have been written by the previous kernel in the stream
+  if (p.early_trigger) griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodePa
 template <int D, int G>
 static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
                                    const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool with_merge) {
   using T = DecodeTile<D, kDecodeWarps>;
   static std::atomic<int> attr_done[kAttrMaxDevices];
   {
@@ -261,7 +262,7 @@ static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
   cudaError_t e = launch_after_previous(paged_decode_split_kernel<D, G>, grid,
                                         dim3(kDecodeWarps * 32), T::kSmemBytes, stream, *tmap_k,
                                         *tmap_v, prm);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !with_merge) return e;
   return launch_decode_merge(prm, num_seqs, D, stream);
 }
 
@@ -336,19 +337,18 @@ cudaError_t launch_decode_merge(const DecodeParams& prm, int num_seqs, int d_hea
 template <int D>
 static cudaError_t launch_decode_d(const DecodeParams& prm, int num_seqs, int group,
                                    const CUtensorMap* tk, const CUtensorMap* tv,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool with_merge) {
   switch (group) {
-    case 1: return launch_decode_t<D, 1>(prm, num_seqs, tk, tv, st);
-    case 2: return launch_decode_t<D, 2>(prm, num_seqs, tk, tv, st);
-    case 4: return launch_decode_t<D, 4>(prm, num_seqs, tk, tv, st);
-    case 8: return launch_decode_t<D, 8>(prm, num_seqs, tk, tv, st);
-    case 16: return launch_decode_t<D, 16>(prm, num_seqs, tk, tv, st);
+    case 1: return launch_decode_t<D, 1>(prm, num_seqs, tk, tv, st, with_merge);
+    case 2: return launch_decode_t<D, 2>(prm, num_seqs, tk, tv, st, with_merge);
+    case 4: return launch_decode_t<D, 4>(prm, num_seqs, tk, tv, st, with_merge);
+    case 8: return launch_decode_t<D, 8>(prm, num_seqs, tk, tv, st, with_merge);
+    case 16: return launch_decode_t<D, 16>(prm, num_seqs, tk, tv, st, with_merge);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
-                                const CUtensorMap* tmap_v, cudaStream_t stream) {
+static DecodeParams decode_params(const DecodeArgs& a) {
   DecodeParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.block_tables = a.block_tables;
@@ -370,6 +370,18 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   prm.extra_lse = a.extra_lse;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
   prm.seq_first_block = a.seq_first_block;
+  prm.early_trigger = a.early_trigger ? 1 : 0;
+  return prm;
+}
+
+cudaError_t launch_paged_decode_merge_only(const DecodeArgs& a, cudaStream_t stream) {
+  return launch_decode_merge(decode_params(a), a.num_seqs, a.d_head, stream);
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                const CUtensorMap* tmap_v, cudaStream_t stream) {
+  const DecodeParams prm = decode_params(a);
+  const bool with_merge = !a.skip_merge;
   const int group = a.q_heads / a.kv_heads;
   if (a.list) {
     if (a.num_seqs > kListMaxSeqs || a.list_items <= 0) return cudaErrorInvalidValue;
@@ -387,8 +399,10 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                       tmap_v, stream);
     return cudaErrorInvalidValue;
   }
-  if (a.d_head == 128) return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
-  if (a.d_head == 64) return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream);
+  if (a.d_head == 128)
+    return launch_decode_d<128>(prm, a.num_seqs, group, tmap_k, tmap_v, stream, with_merge);
+  if (a.d_head == 64)
+    return launch_decode_d<64>(prm, a.num_seqs, group, tmap_k, tmap_v, stream, with_merge);
   return cudaErrorInvalidValue;
 }
 

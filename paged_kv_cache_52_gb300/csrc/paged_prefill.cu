@@ -70,7 +70,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
-  griddep_wait();  // inputs may have been written by the previous kernel in the stream
+  // inputs may have been written by the previous kernel in the stream; with
+  // defer_wait the previous kernel wrote nothing this one reads and let it
+  // start early, and the wait moves to the end
+  if (!p.defer_wait) griddep_wait();
   using L = PrefillSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -122,6 +125,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tc_fence_after();
     tmem_dealloc(tmem, kPfTmemCols);
   }
+  if (p.defer_wait) griddep_wait();  // complete only after the previous grid
 }
 
 template <int D, int G, bool F16PV>
@@ -206,6 +210,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.seq_order = a.seq_order;
   prm.table_rows = a.table_rows;
   prm.allow_empty = a.allow_empty ? 1 : 0;
+  prm.defer_wait = a.defer_wait ? 1 : 0;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
     if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);

@@ -138,8 +138,11 @@ constexpr int kItemsPerSm = 2;
 // slots of one wave as the run count aimed at.
 constexpr int kListMinRun = 8;
 // The fused mixed step spreads its prefill items over this share (per mille)
-// of its work list; the rest holds decode runs only.
-constexpr int kMixedPrefillSpanPermille = 900;
+// of its work list; the rest holds decode runs only.  On GB300 the mixed
+// step (8 x 512-token chunks + 248 decodes) was fastest with the prefill
+// items spread over the whole list: 0.9005 ms at 1000, 0.9104 at 950,
+// 0.9134 at 900, 0.926 at 800, 0.971 at 500 (with its prefix group).
+constexpr int kMixedPrefillSpanPermille = 1000;
 
 // Whether the library's own choice (partition_blocks == 0) takes the
 // length-balanced list.  Measured on GB300 (70B-GQA recipe, 1 to 64
@@ -1319,36 +1322,14 @@ int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache
       group_ctx, s);
   if (e != cudaSuccess) return PKV_ECUDA;
 
-  // 1. every group's queries against its prefix keys, non-causal, on the
-  //    tensor cores (a group is one pseudo-sequence of its members' rows)
   CUtensorMap tq, tk, tv;
   const int rows_per_tile = pkv::prefill_rows_per_tile();
   if (!encode_query_map(&tq, q, num_seqs, q_heads, cache.d_head, group, rows_per_tile / group) ||
       !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
     return PKV_ECUDA;
-  pkv::PrefillArgs pa;
-  pa.q_start = group_start;       // null: one group of all rows
-  pa.block_tables = block_tables;
-  pa.table_rows = group_start;    // a group reads its leader's row (null: row 0)
-  pa.context_lens = group_ctx;
-  pa.out = pre_o;
-  pa.lse = pre_lse;
-  pa.num_seqs = groups;
-  pa.total_q = num_seqs;
-  pa.max_q_len = uniform ? num_seqs : max_group_size;
-  pa.q_heads = q_heads;
-  pa.kv_heads = cache.kv_heads;
-  pa.d_head = cache.d_head;
-  pa.num_blocks = cache.num_blocks;
-  pa.max_blocks_per_seq = max_blocks_per_seq;
-  pa.causal = 0;
-  pa.scale_log2 = scale_log2;
-  pa.allow_empty = true;          // a group with an invalid prefix has none
-  e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
-  if (e != cudaSuccess) return PKV_ECUDA;
 
-  // 2. each sequence's own blocks after its prefix, split-K, partials only;
-  // 3. the merge folds the prefix part in as one more partial
+  // 1. each sequence's own blocks after its prefix, split-K, partials only.
+  //    Its CTAs let the next launch start while they run ...
   pkv::DecodeArgs a;
   a.q = q;
   a.block_tables = block_tables;
@@ -1370,7 +1351,39 @@ int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache
   a.force_partials = 1;
   a.extra_o = pre_o;
   a.extra_lse = pre_lse;
+  a.early_trigger = true;
+  a.skip_merge = true;
   e = pkv::launch_paged_decode(a, &tk, &tv, s);
+  if (e != cudaSuccess) return PKV_ECUDA;
+
+  // 2. ... which is every group's queries against its prefix keys,
+  //    non-causal, on the tensor cores (a group is one pseudo-sequence of its
+  //    members' rows): it fills the SMs the decode's last CTAs leave, and
+  //    waits for the decode only before it finishes
+  pkv::PrefillArgs pa;
+  pa.q_start = group_start;       // null: one group of all rows
+  pa.block_tables = block_tables;
+  pa.table_rows = group_start;    // a group reads its leader's row (null: row 0)
+  pa.context_lens = group_ctx;
+  pa.out = pre_o;
+  pa.lse = pre_lse;
+  pa.num_seqs = groups;
+  pa.total_q = num_seqs;
+  pa.max_q_len = uniform ? num_seqs : max_group_size;
+  pa.q_heads = q_heads;
+  pa.kv_heads = cache.kv_heads;
+  pa.d_head = cache.d_head;
+  pa.num_blocks = cache.num_blocks;
+  pa.max_blocks_per_seq = max_blocks_per_seq;
+  pa.causal = 0;
+  pa.scale_log2 = scale_log2;
+  pa.allow_empty = true;          // a group with an invalid prefix has none
+  pa.defer_wait = true;
+  e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
+  if (e != cudaSuccess) return PKV_ECUDA;
+
+  // 3. the merge folds the prefix part in as one more partial
+  e = pkv::launch_paged_decode_merge_only(a, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -32,6 +32,9 @@ struct DecodeParams {
   // prefix groups: sequence s attends blocks [seq_first_block[s], ...) and
   // merges the extra partial only when that is nonzero (null: first_block)
   const int32_t* seq_first_block = nullptr;
+  // nonzero: the split kernel lets the next grid (a prefix pass that waits
+  // for this grid only at its end) start while it runs
+  int early_trigger = 0;
 };
 
 // First block a sequence's own pages start at (0: no shared prefix).

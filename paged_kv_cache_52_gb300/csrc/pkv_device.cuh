@@ -92,6 +92,13 @@ __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Programmatic dependent launch: let the grid launched after this one (as a
+// programmatic dependent) start before this grid completes.  It starts once
+// every CTA of this grid has called this or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launches `kernel` as a programmatic dependent of the stream's previous
 // kernel: its CTAs may be scheduled while that kernel drains, and the
 // kernel's griddep_wait() -- its first statement, before any input is read,

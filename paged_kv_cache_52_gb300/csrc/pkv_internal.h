@@ -90,6 +90,11 @@ struct DecodeArgs {
   const float* extra_lse = nullptr;
   // prefix groups: per-sequence first block (null: first_block for all)
   const int32_t* seq_first_block = nullptr;
+  // the split kernel lets the next grid start while it runs (that grid must
+  // wait for it before finishing); skip_merge: launch the split kernel only
+  // (launch_paged_decode_merge_only launches the merge)
+  bool early_trigger = false;
+  bool skip_merge = false;
   bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
   // length-balanced work list (bf16 decode): list_items CTAs (an upper bound
   // on the runs), partials at part_o / part_lse indexed by run * G + head,
@@ -130,6 +135,7 @@ int decode_list_max_seqs();
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);
+cudaError_t launch_paged_decode_merge_only(const DecodeArgs& a, cudaStream_t stream);
 unsigned read_decode_error(bool clear);
 
 // ---- paged_decode_fp8.cu (e4m3 pools, d_head 128)
@@ -166,6 +172,10 @@ struct PrefillArgs {
   // groups: the leader's row); null: its own row
   const int32_t* table_rows = nullptr;
   bool allow_empty = false;  // a context of 0 is skipped without a flag
+  // the grid starts without waiting for the kernel before it (which let it
+  // start early and wrote nothing it reads) and waits for that kernel only
+  // before it finishes, so the next kernel sees both complete
+  bool defer_wait = false;
 };
 
 // Query rows (tokens x heads of a GQA group) per prefill tile.

@@ -73,6 +73,7 @@ struct PrefillParams {
   // own row): a prefix group's queries read the group leader's row
   const int32_t* table_rows = nullptr;
   int allow_empty = 0;          // nonzero: a context of 0 is skipped without a flag
+  int defer_wait = 0;           // nonzero: wait for the previous grid at the end, not the start
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
