@@ -70,6 +70,9 @@ def parse_args():
                     help="shrink the mixed step to this many decode sequences (profiling runs)")
     ap.add_argument("--only-mixed", action="store_true",
                     help="time only the mixed step (profiling runs)")
+    ap.add_argument("--only-fused", action="store_true",
+                    help="time only the fused mixed step (append + one persistent launch), "
+                         "with the decodes' shared prefix as a prefix group (profiling runs)")
     ap.add_argument("--only-append", action="store_true",
                     help="run only the bulk append probe (profiling runs)")
     ap.add_argument("--append-tokens", type=int, default=262144,
@@ -274,7 +277,7 @@ def read_traffic(kernel_tag: str):
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("paged_decode.cu", "pkv_device.cuh", "pkv_decode_common.cuh"):
+    for f in ("paged_decode.cu", "pkv_decode_body.cuh", "pkv_device.cuh", "pkv_decode_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_52_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     sha = h.hexdigest()
@@ -619,6 +622,46 @@ def run_mixed(args, dev, pagedkv, E):
     }
 
 
+def run_fused(args, dev, pagedkv, E):
+    """Only the fused continuous-batching step: append every new token, then
+    pkv_mixed_step_attention_ex with the decodes' shared prefix as one
+    prefix group (profiling runs: few launches besides the fused ones)."""
+    w = wl.make_mixed_workload(device=dev, gen_device=dev, num_decode=args.mixed_decodes)
+    kc, vc = w.k_cache, w.v_cache
+    chunk = w.meta["chunk"]
+    plens, dlens = w.meta["prefill_lens"], w.meta["decode_lens"]
+    hq, d, hkv = w.q_prefill.shape[1], w.q_prefill.shape[2], kc.shape[2]
+    max_d = max(dlens)
+    pout = torch.empty(w.q_prefill.shape, dtype=torch.float32, device=dev)
+    dout = torch.empty(w.q_decode.shape, dtype=torch.float32, device=dev)
+    pb = w.meta["shared_prefix"] // wl.BLOCK_SIZE
+    groups = (torch.tensor([0, len(dlens)], dtype=torch.int32, device=dev),
+              torch.tensor([pb], dtype=torch.int32, device=dev), len(dlens), pb)
+    ws = pagedkv.mixed_step_workspace(len(plens), w.prefill_tables.shape[1], len(dlens), hq, hkv,
+                                      d, max_d, dev, num_groups=1)
+
+    def step():
+        pagedkv.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+        pagedkv.mixed_step_attention(w.q_prefill, w.q_start, w.prefill_tables, w.prefill_lens,
+                                     True, w.q_decode, w.decode_tables, w.decode_lens, kc, vc,
+                                     w.scale, chunk, max_d, out_prefill=pout, out_decode=dout,
+                                     workspace=ws, decode_groups=groups)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.mixed_steps
+    a, b = E(enable_timing=True), E(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    return {"workload": w.name if args.mixed_decodes is None else
+            f"{w.name}, shrunk to {len(dlens)} decodes", "steps": K,
+            "ms_per_step": round(a.elapsed_time(b) / K, 4)}
+
+
 def run_fp8(w, dev, pagedkv, E, args, peak):
     """The same 70B-GQA decode step over an FP8 (e4m3) cache: quantizing
     append + FP8 decode.  KV bytes are the e4m3 codes read (half of bf16)."""
@@ -930,6 +973,9 @@ def run_ours(args):
 
     if args.only_mixed:
         print(json.dumps({"mixed_step": run_mixed(args, dev, pagedkv, torch.cuda.Event)}))
+        return
+    if args.only_fused:
+        print(json.dumps({"fused_mixed_step": run_fused(args, dev, pagedkv, torch.cuda.Event)}))
         return
     if args.only_append:
         peak, _ = measured_peak()
