@@ -317,6 +317,10 @@ PKV_API int pkv_paged_prefill_attention(const void* q, const int32_t* q_start, i
  * those pages.  The conversion is exact for |v| in [2^-14, 65504]; smaller
  * values become f16 subnormals (absolute error < 2^-25); a value of
  * magnitude 65520 or more overflows and sets PKV_DEVERR_FP16_RANGE.  The
+ * error bound scales with V: an output element is off by at most
+ * 2^-10 * max|V| (measured 8.7e-5 * max|V|), so the absolute 2e-3 of the
+ * tests holds while |V| stays below about 20; for larger V use
+ * pkv_paged_prefill_attention (P as bf16 hi + lo, ~2^-17).  The
  * same pass ranks the sequences by context length, and the prefill runs
  * each sequence's tiles together, longest context first (a dispatch order
  * only: the result does not depend on it).
@@ -593,7 +597,9 @@ PKV_API int pkv_kv_append_fp8(const void* k, int64_t k_tok_stride, const void* v
  * (K = k_scale * e4m3(k_cache), V = v_scale * e4m3(v_cache)).  d_head must
  * be 128.  Same plan and workspace as the bf16 decode (pkv_decode_plan);
  * partition_blocks <= 0 = library choice.  Query values must fit f16's range
- * (|q| < 65520), else PKV_DEVERR_FP16_RANGE is set.
+ * (|q| < 65520), else PKV_DEVERR_FP16_RANGE is set.  P enters the P V
+ * product as one f16 operand: an output element is off by at most
+ * 2^-10 * max|V| of the dequantized V (measured 5.3e-5 * max|V|).
  */
 PKV_API int pkv_paged_decode_attention_fp8(const void* q, int num_seqs, int q_heads,
                                            const void* k_cache, const void* v_cache,
