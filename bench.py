@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa70b", choices=sorted(wl.DECODE_SPECS))
     ap.add_argument("--partition-blocks", type=int, default=0)
+    ap.add_argument("--separate-step", action="store_true",
+                    help="time the step as two calls (kv_append, then the decode) instead of "
+                         "pkv_paged_decode_step")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="shrink the workload to this many sequences (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -125,7 +128,9 @@ def workload_config(w, spec, plan):
         "kv_bytes_per_step": w.kv_bytes(),
         "partition_blocks": plan[0], "num_parts": plan[1],
         "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush",
-        "step": "kv_append(1 token/seq) + paged_decode_attention (split-K + LSE merge)",
+        "step": "kv_append(1 token/seq) + paged_decode_attention (split-K + LSE merge), "
+                "through pkv_paged_decode_step (the append's kernel runs beside the split "
+                "kernel; only each sequence's last page waits for it)",
     }
 
 
@@ -850,7 +855,7 @@ def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_
 
 
 
-def e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barrier):
+def e2e_pipelined(host, w, K, step, out, ws, max_len, args, dev, pagedkv, barrier):
     """K steps through the public API with host buffers: step i's inputs go up
     on a copy stream while step i-1 computes, and its output comes back while
     step i+1 computes.  Two sets of device inputs and outputs, ordered by
@@ -886,10 +891,8 @@ def e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barr
             comp.wait_event(uploaded[b])
             comp.wait_event(read_back[b])    # step i-2's output has left this buffer
             d = devb[b]
-            append(d["k_new"], d["v_new"], d["slot_mapping"])
-            pagedkv.paged_decode_attention(d["q"], kc, vc, d["block_tables"], d["context_lens"],
-                                           w.scale, out=outs[b], max_context_len=max_len,
-                                           workspace=ws, partition_blocks=args.partition_blocks)
+            step(d["k_new"], d["v_new"], d["slot_mapping"], d["q"], d["block_tables"],
+                 d["context_lens"], outs[b])
             computed[b].record(comp)
             with torch.cuda.stream(copy):
                 copy.wait_event(computed[b])
@@ -1007,9 +1010,23 @@ def run_ours(args):
                                        max_context_len=max_len, workspace=ws,
                                        partition_blocks=args.partition_blocks)
 
+    def step(k_new, v_new, slots, q, tables, lens, dst=None):
+        """One decode step through the public API: the new token of every
+        sequence appended, then attended (pkv_paged_decode_step, which hides
+        the append under the attention; --separate-step: the two calls)."""
+        dst = out if dst is None else dst
+        if args.separate_step or args.partition_blocks:
+            append(k_new, v_new, slots)
+            pagedkv.paged_decode_attention(q, kc, vc, tables, lens, w.scale, out=dst,
+                                           max_context_len=max_len, workspace=ws,
+                                           partition_blocks=args.partition_blocks)
+        else:
+            pagedkv.paged_decode_step(q, k_new, v_new, slots, kc, vc, tables, lens, w.scale,
+                                      out=dst, max_context_len=max_len, workspace=ws)
+
+    inputs = (w.k_new, w.v_new, w.slot_mapping, w.q, w.block_tables, w.context_lens)
     for _ in range(max(3, args.warmup)):
-        append(w.k_new, w.v_new, w.slot_mapping)
-        decode(w.q, w.block_tables, w.context_lens)
+        step(*inputs)
     torch.cuda.synchronize()
     err = pagedkv.get_device_error(clear=True)
     if err:
@@ -1018,8 +1035,6 @@ def run_ours(args):
     K = args.steps
     E = torch.cuda.Event
     start, end = E(enable_timing=True), E(enable_timing=True)
-    marks = [(E(enable_timing=True), E(enable_timing=True), E(enable_timing=True))
-             for _ in range(K)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -1028,24 +1043,34 @@ def run_ours(args):
         t_load = time.perf_counter()
         while time.perf_counter() - t_load < 0.6:
             for _ in range(50):
-                append(w.k_new, w.v_new, w.slot_mapping)
-                decode(w.q, w.block_tables, w.context_lens)
+                step(*inputs)
             torch.cuda.synchronize()
         start.record()
-        for a, b, c in marks:
-            a.record()
-            append(w.k_new, w.v_new, w.slot_mapping)
-            b.record()
-            decode(w.q, w.block_tables, w.context_lens)
-            c.record()
+        for _ in range(K):
+            step(*inputs)
         end.record()
         torch.cuda.synchronize()
     barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
-    decode_ms = sum(b.elapsed_time(c) for _, b, c in marks) / K
-    append_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / K
     ms_per_step = total_ms / K
     value = whole_job_gbps(kv_bytes, K, world, total_ms)
+    # the step's parts, each call timed alone: the append, and the decode
+    # call whose bytes the roofline counts
+    marks = [(E(enable_timing=True), E(enable_timing=True), E(enable_timing=True))
+             for _ in range(K)]
+    s0, s1 = E(enable_timing=True), E(enable_timing=True)
+    s0.record()
+    for a, b, c in marks:
+        a.record()
+        append(w.k_new, w.v_new, w.slot_mapping)
+        b.record()
+        decode(w.q, w.block_tables, w.context_lens)
+        c.record()
+    s1.record()
+    torch.cuda.synchronize()
+    decode_ms = sum(b.elapsed_time(c) for _, b, c in marks) / K
+    append_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / K
+    separate_ms = s0.elapsed_time(s1) / K
 
     # End to end through the public API: this step's inputs from pinned host
     # memory, the step, and the output read back, every step.
@@ -1059,8 +1084,8 @@ def run_ours(args):
     def e2e_step():
         for n, t in host.items():
             devb[n].copy_(t, non_blocking=True)
-        append(devb["k_new"], devb["v_new"], devb["slot_mapping"])
-        decode(devb["q"], devb["block_tables"], devb["context_lens"])
+        step(devb["k_new"], devb["v_new"], devb["slot_mapping"], devb["q"],
+             devb["block_tables"], devb["context_lens"])
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -1074,7 +1099,7 @@ def run_ours(args):
     e2.record()
     torch.cuda.synchronize()
     e2e_serial_ms = max_over_ranks(s2.elapsed_time(e2), dev)
-    e2e_ms = e2e_pipelined(host, w, K, append, out, ws, max_len, args, dev, pagedkv, barrier)
+    e2e_ms = e2e_pipelined(host, w, K, step, out, ws, max_len, args, dev, pagedkv, barrier)
     e2e_value = whole_job_gbps(kv_bytes, K, world, e2e_ms)
 
     peak, peak_kind = measured_peak()
@@ -1093,6 +1118,7 @@ def run_ours(args):
         "decode_tokens_per_s_80_layers_attention_only": round(
             world * S * K / (80 * total_ms / 1e3), 1),
         "decode_ms": round(decode_ms, 4), "append_ms": round(append_ms, 4),
+        "ms_per_step_separate_calls": round(separate_ms, 4),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"kernel": "paged_decode (split-K kernel + LSE merge, one call)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

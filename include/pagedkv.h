@@ -222,6 +222,29 @@ PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_hea
                                   int partition_blocks, pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_step -- one decode step: pkv_kv_append of each
+ * sequence's new token, then pkv_paged_decode_attention, with the same
+ * results (cache rows bit for bit, outputs bit for bit) and the append's time
+ * hidden: the decode's CTAs start beside the append and only the loads of a
+ * sequence's last page -- the one holding the appended token -- wait for it.
+ * One new token per sequence: row s of k_new / v_new and slot_mapping[s]
+ * belong to sequence s, and slot_mapping[s] must be -1 or the slot of its
+ * position context_lens[s] - 1 (the usual decode step: the cache is updated,
+ * then attended, "Optimisation de l'inference", "Etape 1/2").  A slot
+ * elsewhere is still written but may be missed by the attention; it sets
+ * PKV_DEVERR_BAD_SLOT.  Arguments as in pkv_kv_append and
+ * pkv_paged_decode_attention (library's split choice; the workspace of
+ * pkv_decode_workspace_bytes).
+ */
+PKV_API int pkv_paged_decode_step(const void* q, int num_seqs, int q_heads, const void* k_new,
+                                  int64_t k_tok_stride, const void* v_new, int64_t v_tok_stride,
+                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                  pkv_cache_desc cache, const int32_t* block_tables,
+                                  int max_blocks_per_seq, const int32_t* context_lens,
+                                  int max_context_len, float scale, float* out, void* workspace,
+                                  size_t ws_bytes, pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_attention_limited -- the decode on at most max_ctas CTAs,
  * leaving the other SMs to kernels on other streams (the continuous-batching
  * step runs a chunked prefill beside the decodes: nano-vLLM page, section

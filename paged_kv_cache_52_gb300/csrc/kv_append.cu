@@ -41,7 +41,11 @@ __global__ void __launch_bounds__(kAppendThreads)
 kv_append_kernel(const uint4* __restrict__ k, int64_t k_stride_vec, const uint4* __restrict__ v,
                  int64_t v_stride_vec, const int64_t* __restrict__ slot_mapping,
                  int64_t num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                 int64_t num_slots, int row_vec, const int* __restrict__ reject) {
+                 int64_t num_slots, int row_vec, const int* __restrict__ reject,
+                 int trigger_dependents) {
+  // a decode step's attention may start beside this append: it waits for it
+  // only where it reads the appended rows
+  if (trigger_dependents) griddep_launch_dependents();
   if (reject && *reject) return;  // checked append of a mapping with a repeated slot
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
@@ -108,7 +112,8 @@ cudaError_t launch_slot_duplicates(const int64_t* slot_mapping, int64_t num_toke
 cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
                              const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                              void* v_cache, int64_t num_slots, int row_elems,
-                             cudaStream_t stream, int num_sms, const int* reject) {
+                             cudaStream_t stream, int num_sms, const int* reject,
+                             bool trigger_dependents) {
   const int row_vec = row_elems / 8;  // 8 bf16 per 16-byte vector
   const int64_t warps_needed = num_tokens;
   const int64_t blocks_needed = (warps_needed * 32 + kAppendThreads - 1) / kAppendThreads;
@@ -117,7 +122,7 @@ cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int
   kv_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k), k_stride / 8, static_cast<const uint4*>(v), v_stride / 8,
       slot_mapping, num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      num_slots, row_vec, reject);
+      num_slots, row_vec, reject, trigger_dependents ? 1 : 0);
   return cudaGetLastError();
 }
 

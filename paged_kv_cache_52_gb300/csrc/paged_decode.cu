@@ -50,7 +50,9 @@ template <int D, int G>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  griddep_wait();  // inputs may have been written by the previous kernel in the stream
+  // inputs may have been written by the previous kernel in the stream (with
+  // wait_late: the step's append, waited for only before the last pages)
+  if (!p.wait_late) griddep_wait();
   if (p.early_trigger) griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -371,6 +373,8 @@ static DecodeParams decode_params(const DecodeArgs& a) {
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
   prm.seq_first_block = a.seq_first_block;
   prm.early_trigger = a.early_trigger ? 1 : 0;
+  prm.wait_late = a.wait_late ? 1 : 0;
+  prm.step_slots = a.step_slots;
   return prm;
 }
 

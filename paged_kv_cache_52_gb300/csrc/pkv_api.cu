@@ -561,7 +561,8 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
                      const void* v_cache, pkv_cache_desc cache, const int32_t* block_tables,
                      int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                      float scale, void* out, bool out_bf16, void* workspace, size_t ws_bytes,
-                     int partition_blocks, pkv_stream_t stream, int list_ctas = 0) {
+                     int partition_blocks, pkv_stream_t stream, int list_ctas = 0,
+                     const int64_t* step_slots = nullptr) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   Plan plan;
@@ -617,6 +618,11 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
     a.list_items = plan.list_items;
     a.list_max_ctas = list_ctas;
   }
+  if (step_slots) {  // the decode step: the append just launched runs beside the split kernel
+    if (plan.list) return PKV_EUNSUPPORTED;
+    a.wait_late = true;
+    a.step_slots = step_slots;
+  }
   cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
@@ -632,6 +638,49 @@ int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, cons
   return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
                           max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
                           workspace, ws_bytes, partition_blocks, stream);
+}
+
+int pkv_paged_decode_step(const void* q, int num_seqs, int q_heads, const void* k_new,
+                          int64_t k_tok_stride, const void* v_new, int64_t v_tok_stride,
+                          const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          pkv_cache_desc cache, const int32_t* block_tables,
+                          int max_blocks_per_seq, const int32_t* context_lens,
+                          int max_context_len, float scale, float* out, void* workspace,
+                          size_t ws_bytes, pkv_stream_t stream) {
+  int st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0) return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  // the append's checks (pkv_kv_append) ...
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
+  const int64_t row = int64_t(cache.kv_heads) * cache.d_head;
+  if (row % 8) return PKV_EUNSUPPORTED;
+  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+    return PKV_EINVAL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return PKV_EINVAL;
+  // ... and the decode's, before anything is launched
+  Plan plan;
+  st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, 0, &plan);
+  if (st != PKV_OK) return st;
+  if (!q || !block_tables || !context_lens || !out || max_blocks_per_seq <= 0 ||
+      !std::isfinite(scale))
+    return PKV_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+    return PKV_EINVAL;
+  if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes)) return PKV_ENOMEM;
+  if (plan.ws_bytes > 0 && !aligned(workspace, 256)) return PKV_EINVAL;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PKV_ECUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_kv_append(k_new, k_tok_stride, v_new, v_tok_stride, slot_mapping,
+                                        num_seqs, k_cache, v_cache,
+                                        int64_t(cache.num_blocks) * cache.block_size, int(row),
+                                        cs, sms, nullptr, /*trigger_dependents=*/true);
+  if (e != cudaSuccess) return PKV_ECUDA;
+  return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
+                          workspace, ws_bytes, 0, stream, 0, slot_mapping);
 }
 
 size_t pkv_decode_limited_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,

@@ -284,12 +284,24 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
   __syncthreads();  // ids staged, barriers initialised
 
   const int cnt = (pager && warp < nb_local) ? (nb_local - warp + NW - 1) / NW : 0;
+  // the page holding the sequence's last position (the step's appended
+  // token when the append runs beside this grid: its loads wait for it)
+  const int last_page = len > 0 ? (len - 1) / kBlockTokens : -1;
   auto issue = [&](int i) {
     const int st = i % kDecodeStages;
     const uint32_t bar = bars + st * 8;
     const uint32_t kdst = ring + st * T::kStageBytes;
     const uint32_t vdst = kdst + T::kTileBytes;
     const int bid = ids[warp + i * NW];
+    if (p.wait_late && b0 + warp + i * NW == last_page) {
+      griddep_wait();  // the append is complete and its rows are visible
+      if (p.step_slots && kvh == 0) {
+        // the append must have written exactly this position (or skipped it)
+        const long long slot = p.step_slots[seq];
+        const long long want = (long long)bid * kBlockTokens + (len - 1) % kBlockTokens;
+        if (slot != -1 && slot != want) atomicOr(&g_decode_error, kErrBadSlot);
+      }
+    }
     mbar_arrive_expect_tx(bar, T::kStageBytes);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {

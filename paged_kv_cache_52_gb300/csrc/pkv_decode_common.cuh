@@ -35,6 +35,12 @@ struct DecodeParams {
   // nonzero: the split kernel lets the next grid (a prefix pass that waits
   // for this grid only at its end) start while it runs
   int early_trigger = 0;
+  // nonzero: the grid before this one is the step's append, which let this
+  // grid start early; only the loads of a sequence's last page wait for it
+  // (that page holds the appended token; the append writes nothing else the
+  // decode reads when every slot is its sequence's position context_len - 1)
+  int wait_late = 0;
+  const int64_t* step_slots = nullptr;  // the append's slot mapping (wait_late), for a check
 };
 
 // First block a sequence's own pages start at (0: no shared prefix).

@@ -27,7 +27,8 @@ cudaError_t mixed_prefill_error_word(unsigned** word);
 cudaError_t launch_kv_append(const void* k, int64_t k_stride, const void* v, int64_t v_stride,
                              const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                              void* v_cache, int64_t num_slots, int row_elems,
-                             cudaStream_t stream, int num_sms, const int* reject = nullptr);
+                             cudaStream_t stream, int num_sms, const int* reject = nullptr,
+                             bool trigger_dependents = false);
 // Marks every in-pool slot in `bitmap` (num_slots bits, zeroed by the
 // caller) and sets *reject when a slot repeats.
 cudaError_t launch_slot_duplicates(const int64_t* slot_mapping, int64_t num_tokens,
@@ -95,6 +96,11 @@ struct DecodeArgs {
   // (launch_paged_decode_merge_only launches the merge)
   bool early_trigger = false;
   bool skip_merge = false;
+  // the split kernel starts beside the append launched just before it and
+  // waits for that append only before loading a sequence's last page (the
+  // one holding its appended token); the decode-step entry point sets it
+  bool wait_late = false;
+  const int64_t* step_slots = nullptr;  // with wait_late: the append's slot mapping
   bool out_bf16 = false;  // out is bf16 (rounded to nearest even), not float32
   // length-balanced work list (bf16 decode): list_items CTAs (an upper bound
   // on the runs), partials at part_o / part_lse indexed by run * G + head,

@@ -72,6 +72,9 @@ SIGNATURES = {
                                               ctypes.POINTER(_sz)], ctypes.c_int),
     "pkv_decode_workspace_bytes": ([ctypes.c_int] * 5, _sz),
     "pkv_decode_plan_uses_list": ([ctypes.c_int] * 6, ctypes.c_int),
+    "pkv_paged_decode_step": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _i64, _vp, _vp,
+                               _vp, CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
+                               _vp, _sz, _vp], ctypes.c_int),
     "pkv_decode_limited_workspace_bytes": ([ctypes.c_int] * 6, _sz),
     "pkv_mixed_step_workspace_bytes": ([ctypes.c_int] * 7, _sz),
     "pkv_mixed_step_attention": ([_vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
@@ -429,6 +432,46 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _ptr(workspace), ws_bytes, int(partition_blocks), _stream(q))
     _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None,
+                      max_context_len: Optional[int] = None,
+                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step (``pkv_paged_decode_step``): append each sequence's new
+    token (row s of k_new / v_new at slot_mapping[s]) and attend, the append
+    hidden under the attention.  float32 ``out [S, Hq, d]``."""
+    _check_cache(k_cache, v_cache)
+    _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
+          "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
+    S, hq, d = q.shape
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t.dtype == torch.bfloat16 and t.dim() == 3 and t.shape[0] == S and
+              t.shape[1:] == k_cache.shape[2:] and t.stride(2) == 1 and t.stride(1) == d,
+              f"{n} must be [S, Hkv, d] bf16 with contiguous rows")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == (S,) and
+          slot_mapping.is_contiguous(), "slot_mapping must be contiguous int64 [S]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+          block_tables.is_contiguous() and block_tables.shape[0] == S,
+          "block_tables must be contiguous int32 [S, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous() and
+          context_lens.shape == (S,), "context_lens must be contiguous int32 [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if out is None:
+        out = torch.empty(S, hq, d, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(S, hq, k_cache.shape[2], d, max_context_len, q.device)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.pkv_paged_decode_step(
+        _ptr(q), S, hq, _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0),
+        _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        _ptr(workspace), ws_bytes, _stream(q))
+    _check("pkv_paged_decode_step", st)
     return out
 
 

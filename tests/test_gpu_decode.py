@@ -222,3 +222,53 @@ def test_limited_decode_matches_oracle(pk, max_ctas):
     assert_attention_close(out.cpu().numpy(), ref, f"limited decode, {max_ctas} CTAs")
     assert np.all(out[lens.index(0)].cpu().numpy() == 0.0)
     assert pk.get_device_error() == 0
+
+
+# ---- the decode step (pkv_paged_decode_step): append and attend, the append
+# hidden under the attention; the same cache rows and outputs bit for bit
+
+
+@pytest.mark.parametrize("name,lens", [("tiny", None), ("gqa70b", [1024, 3000, 777, 17, 16, 2049])])
+def test_decode_step_equals_append_then_decode(pk, name, lens):
+    spec = wl.DECODE_SPECS[name]
+    w = _to_dev(wl.make_decode_workload(spec, lens_override=lens))
+    mcl = max(w.meta["lens"])
+    kc1, vc1 = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc1, vc1)
+    sep = pk.paged_decode_attention(w.q, kc1, vc1, w.block_tables, w.context_lens, w.scale,
+                                    max_context_len=mcl)
+    kc2, vc2 = w.k_cache.clone(), w.v_cache.clone()
+    fused = pk.paged_decode_step(w.q, w.k_new, w.v_new, w.slot_mapping, kc2, vc2,
+                                 w.block_tables, w.context_lens, w.scale, max_context_len=mcl)
+    torch.cuda.synchronize()
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    assert torch.equal(sep, fused)
+    ref = DecodeStepOracle(_to_dev(wl.make_decode_workload(spec, lens_override=lens)),
+                           range(w.num_seqs)).output()
+    assert_attention_close(fused.cpu().numpy(), ref, f"decode step {name}")
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_decode_step_full_size_70b_gqa(pk):
+    w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV)
+    mcl = max(w.meta["lens"])
+    sep = run_step(pk, w)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    fused = pk.paged_decode_step(w.q, w.k_new, w.v_new, w.slot_mapping, kc, vc, w.block_tables,
+                                 w.context_lens, w.scale, max_context_len=mcl)
+    torch.cuda.synchronize()
+    assert torch.equal(sep, fused)
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_decode_step_slot_elsewhere_is_flagged(pk):
+    w = _to_dev(wl.make_decode_workload(wl.TINY))
+    slots = w.slot_mapping.clone()
+    slots[1] = -1                                  # no token appended: attends the cache as is
+    slots[2] = int(w.block_tables[2, 0]) * 16 + 3  # an earlier position of sequence 2
+    pk.get_device_error(clear=True)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    pk.paged_decode_step(w.q, w.k_new, w.v_new, slots, kc, vc, w.block_tables, w.context_lens,
+                         w.scale, max_context_len=250)
+    torch.cuda.synchronize()
+    assert pk.get_device_error(clear=True) == 0x1
