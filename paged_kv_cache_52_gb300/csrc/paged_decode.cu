@@ -410,8 +410,8 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
   return cudaErrorInvalidValue;
 }
 
-// Prefix groups (see launch_prefix_groups_setup): one thread per sequence,
-// then one per group.
+// Prefix groups (see launch_prefix_groups_setup): one warp per sequence (its
+// lanes compare the prefix ids 32 at a time), then one thread per group.
 __global__ void prefix_groups_setup_kernel(const int32_t* group_start,
                                            const int32_t* group_prefix_blocks, int num_groups,
                                            int uniform_prefix_blocks, int num_seqs,
@@ -421,19 +421,18 @@ __global__ void prefix_groups_setup_kernel(const int32_t* group_start,
   griddep_wait();
   const bool uniform = group_start == nullptr;
   const int groups = uniform ? 1 : num_groups;
+  const int lane = threadIdx.x & 31;
   auto prefix_of = [&](int g) {
     const int pb = uniform ? uniform_prefix_blocks : __ldg(group_prefix_blocks + g);
     return (pb >= 1 && pb <= max_prefix_blocks && pb <= max_blocks) ? pb : 0;
   };
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < num_seqs + groups;
-       t += stride) {
-    if (t >= num_seqs) {  // a group's prefix length in tokens
-      const int g = int(t - num_seqs);
-      group_ctx[g] = prefix_of(g) * kBlockTokens;
-      continue;
-    }
-    const int s = int(t);
+  const long long threads = (long long)gridDim.x * blockDim.x;
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  // a group's prefix length in tokens
+  for (long long g = gtid; g < groups; g += threads) group_ctx[g] = prefix_of(int(g)) * kBlockTokens;
+  const long long warps = threads / 32;
+  for (long long w = gtid / 32; w < num_seqs; w += warps) {
+    const int s = int(w);
     int g = 0, lead = 0;
     bool in_group = true;
     if (!uniform) {  // the last group starting at or before s
@@ -457,15 +456,17 @@ __global__ void prefix_groups_setup_kernel(const int32_t* group_start,
     if (pb > 0 && s != lead) {
       const int32_t* mine = block_tables + size_t(s) * max_blocks;
       const int32_t* theirs = block_tables + size_t(lead) * max_blocks;
-      for (int j = 0; j < pb; ++j)
-        if (__ldg(mine + j) != __ldg(theirs + j)) {
-          pb = 0;
-          bad = true;
-          break;
-        }
+      bool same = true;
+      for (int j = lane; j < pb; j += 32) same = same && __ldg(mine + j) == __ldg(theirs + j);
+      if (!__all_sync(0xffffffffu, same)) {
+        pb = 0;
+        bad = true;
+      }
     }
-    if (bad) atomicOr(&g_decode_error, kErrPrefixMismatch);
-    seq_first_block[s] = pb;
+    if (lane == 0) {
+      if (bad) atomicOr(&g_decode_error, kErrPrefixMismatch);
+      seq_first_block[s] = pb;
+    }
   }
 }
 
@@ -476,8 +477,9 @@ cudaError_t launch_prefix_groups_setup(const int32_t* group_start,
                                        const int32_t* context_lens, int max_prefix_blocks,
                                        int32_t* seq_first_block, int32_t* group_ctx,
                                        cudaStream_t stream) {
-  const long long work = (long long)num_seqs + (group_start ? num_groups : 1);
-  const int blocks = int(std::min<long long>((work + 255) / 256, 1024));
+  const long long warps = (long long)num_seqs > (group_start ? num_groups : 1)
+                              ? num_seqs : (group_start ? num_groups : 1);
+  const int blocks = int(std::min<long long>((warps * 32 + 255) / 256, 1024));
   return launch_after_previous(prefix_groups_setup_kernel, dim3(blocks), dim3(256), 0, stream,
                                group_start, group_prefix_blocks, num_groups,
                                uniform_prefix_blocks, num_seqs, block_tables, max_blocks_per_seq,
