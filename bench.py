@@ -810,7 +810,7 @@ def run_append_probe(dev, pagedkv, E, peak, tokens=262144, steps=20):
 def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_len=512):
     """Small-batch decode steps of the 70B-GQA layer shape: per-step time of
     eager calls vs replay of a CUDA graph captured for the batch's bucket
-    (append + split-K decode).  Batches of 1-4 sequences have short contexts
+    (the decode step: append + split-K decode).  Batches of 1-4 sequences have short contexts
     (`short_len` tokens each), where launch latency dominates; 8 and 64 draw
     their contexts from the 70B-GQA recipe."""
     from paged_kv_cache_52_gb300.graphs import DecodeGraphRunner
@@ -824,10 +824,9 @@ def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_
         out = torch.empty(w.q.shape, dtype=torch.float32, device=dev)
 
         def eager():
-            pagedkv.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
-            pagedkv.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
-                                           w.context_lens, w.scale, out=out,
-                                           max_context_len=max_len, workspace=ws)
+            pagedkv.paged_decode_step(w.q, w.k_new, w.v_new, w.slot_mapping, w.k_cache,
+                                      w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
+                                      max_context_len=max_len, workspace=ws)
 
         runner = DecodeGraphRunner(w.k_cache, w.v_cache, w.q_heads, w.block_tables.shape[1],
                                    max_len, w.scale, buckets=(bsz,))

@@ -5,9 +5,9 @@ modeles avec nano-vLLM", section "CUDA Graph") captures the decode step once
 per batch-size bucket and pads each live batch to the smallest bucket that
 holds it, so a step costs one graph launch instead of one launch per kernel.
 
-Here a step is the library's own two calls -- ``kv_append`` of each
-sequence's new token, then ``paged_decode_attention`` -- captured on static
-buffers.  Padding needs no special case in the kernels: a padded sequence has
+Here a step is the library's decode step -- ``paged_decode_step``: each
+sequence's new token appended, then attended, the append's kernel running
+beside the attention -- captured on static buffers.  Padding needs no special case in the kernels: a padded sequence has
 ``context_len == 0`` (its output is zero) and slot ``-1`` (nothing is
 appended).  The split-K workspace is allocated once per bucket before
 capture, so the captured calls allocate nothing.  This module only stages
@@ -59,11 +59,9 @@ class DecodeGraphRunner:
         self.buckets: Dict[int, _Bucket] = {}
 
     def _step(self, b: _Bucket):
-        pagedkv.kv_append(b.k_new, b.v_new, b.slots, self.k_cache, self.v_cache)
-        pagedkv.paged_decode_attention(b.q, self.k_cache, self.v_cache, b.tables, b.lens,
-                                       self.scale, out=b.out,
-                                       max_context_len=self.max_context_len,
-                                       workspace=b.workspace)
+        pagedkv.paged_decode_step(b.q, b.k_new, b.v_new, b.slots, self.k_cache, self.v_cache,
+                                  b.tables, b.lens, self.scale, out=b.out,
+                                  max_context_len=self.max_context_len, workspace=b.workspace)
 
     def capture(self, size: int) -> _Bucket:
         b = _Bucket(size, self.q_heads, self.kv_heads, self.d_head, self.max_blocks,
