@@ -14,8 +14,9 @@
 //    512 tensor-memory columns), 11 warps.  A CTA takes list positions from a
 //    counter; a position is either a prefill item (two 128-row query tiles of
 //    one sequence x KV head, computed with the prefill kernel's warp roles) or
-//    a decode run (pages of one sequence x KV head, computed by warps 0-7,
-//    each with its own 3-stage TMA ring, as in the decode kernel).
+//    a decode run (pages of one sequence x KV head, computed by the warps
+//    whose 3-stage TMA rings fit below the prefill's bookkeeping -- 9 at
+//    d_head 128 (216 KB in flight), 8 at 64 -- each as in the decode kernel).
 //  * the prefill items are spread evenly over the list (or over its first
 //    part, a parameter), so at any moment the CTAs share out between
 //    tensor-bound prefill items and HBM-bound decode runs in proportion to
@@ -35,7 +36,12 @@
 
 namespace pkv {
 
-constexpr int kMixedDecodeWarps = 8;  // warps that own decode rings in a mixed CTA
+// Warps that own decode rings in a mixed CTA: as many 3-stage rings as fit
+// below the prefill's bookkeeping (9 at d_head 128, 8 at 64).
+template <int D>
+struct MixedDecodeWarps {
+  static constexpr int value = DecodeTile<D, 9>::kEnd <= PrefillSmem<D>::kMiscOff ? 9 : 8;
+};
 
 struct MixedParams {
   int* counter;                  // list positions taken, zeroed by the plan kernel
@@ -52,12 +58,12 @@ struct MixedParams {
 template <int D>
 struct MixedSmem {
   static constexpr int kPrefill = PrefillSmem<D>::kSmemBytes;
-  static constexpr int kDecode = DecodeTile<D, kMixedDecodeWarps>::kSmemBytes;
+  static constexpr int kDecode = DecodeTile<D, MixedDecodeWarps<D>::value>::kSmemBytes;
   static constexpr int kSmemBytes = kPrefill > kDecode ? kPrefill : kDecode;
   static_assert(kSmemBytes <= 232448, "mixed-step CTA does not fit in shared memory");
   // the prefill's own bookkeeping (tensor-memory address, abort flag, item
   // slot) lies past every decode buffer
-  static_assert(PrefillSmem<D>::kMiscOff >= DecodeTile<D, kMixedDecodeWarps>::kEnd,
+  static_assert(PrefillSmem<D>::kMiscOff >= DecodeTile<D, MixedDecodeWarps<D>::value>::kEnd,
                 "decode buffers overlap the prefill's bookkeeping");
 };
 
@@ -135,13 +141,13 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
       else if (threadIdx.x == 0)
         atomicOr(&g_prefill_error, kErrBadQueryRange);
     } else {
-      list_item<D, G, kMixedDecodeWarps>(tmap_k, tmap_v, dp, lp, smem, mp.seq_item_base,
+      list_item<D, G, MixedDecodeWarps<D>::value>(tmap_k, tmap_v, dp, lp, smem, mp.seq_item_base,
                                          int(pos - before));
       __syncthreads();  // every warp has left the run's merge
       // the run's barriers are retired: this memory holds prefill tiles next
-      if (warp < kMixedDecodeWarps && lane == 0)
+      if (warp < MixedDecodeWarps<D>::value && lane == 0)
         for (int st = 0; st < kDecodeStages; ++st)
-          mbar_inval(smem_u32(smem + DecodeTile<D, kMixedDecodeWarps>::kBarOffset) +
+          mbar_inval(smem_u32(smem + DecodeTile<D, MixedDecodeWarps<D>::value>::kBarOffset) +
                      (warp * kDecodeStages + st) * 8);
     }
     // the item's generic shared-memory accesses come before the next item's
