@@ -142,15 +142,25 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
  *                        one wave of CTAs in all ("第 10 讲：推理（Inference）",
  *                        "核心概念与定义": FlashDecoding's split of long
  *                        contexts, here balanced on the real lengths);
- *   0                    the library's choice: today the uniform partitions
- *                        (on GB300 the balanced list did not beat them at any
- *                        batch size: a small batch's time is the decode's
- *                        fixed cost more than the balance of its waves).
+ *   PKV_SPLIT_FLAT       the flat split (bf16 decode, at most 1024
+ *                        sequences): a persistent grid of one CTA per SM
+ *                        whose warps each stream one contiguous range of
+ *                        the pages of all (sequence, KV head) pairs laid end
+ *                        to end; the ranges differ by at most one page, and
+ *                        a warp's page copies run on across the pairs of its
+ *                        range, so the copy pipeline fills once per warp;
+ *   0                    the library's choice between the uniform
+ *                        partitions and the flat split (the balanced list
+ *                        did not beat the uniform partitions at any batch
+ *                        size on GB300: a small batch's time is the
+ *                        decode's fixed cost more than the balance of its
+ *                        waves).
  * The FP8 decode, the verification decode and the shared-prefix decode
  * treat every value <= 0 as PKV_SPLIT_UNIFORM.
  */
 #define PKV_SPLIT_BALANCED (-1)
 #define PKV_SPLIT_UNIFORM (-2)
+#define PKV_SPLIT_FLAT (-3)
 
 /*
  * Decode plan: the partition size (in 16-token blocks) and the number of
@@ -167,6 +177,11 @@ PKV_API int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head,
 /* 1 when the bf16 decode with this partition_blocks takes the length-balanced
  * list, 0 when it takes the uniform split, or a negative pkv_status. */
 PKV_API int pkv_decode_plan_uses_list(int num_seqs, int q_heads, int kv_heads, int d_head,
+                                      int max_context_len, int partition_blocks);
+
+/* 1 when the bf16 decode with this partition_blocks takes the flat split, 0
+ * when it does not, or a negative pkv_status. */
+PKV_API int pkv_decode_plan_uses_flat(int num_seqs, int q_heads, int kv_heads, int d_head,
                                       int max_context_len, int partition_blocks);
 
 /* Workspace bytes pkv_paged_decode_attention needs with the library's choice
@@ -212,8 +227,8 @@ PKV_API int pkv_paged_decode_attention(const void* q, int num_seqs, int q_heads,
                                pkv_stream_t stream);
 
 /* Same as pkv_paged_decode_attention with an explicit split choice
- * (partition_blocks: a size in blocks, PKV_SPLIT_UNIFORM, PKV_SPLIT_BALANCED
- * or 0 = library choice; see above). */
+ * (partition_blocks: a size in blocks, PKV_SPLIT_UNIFORM, PKV_SPLIT_BALANCED,
+ * PKV_SPLIT_FLAT or 0 = library choice; see above). */
 PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_heads, const void* k_cache,
                                   const void* v_cache, pkv_cache_desc cache,
                                   const int32_t* block_tables, int max_blocks_per_seq,

@@ -1,0 +1,497 @@
+// Flat split of the bf16 paged decode: every warp of a persistent grid (one
+// CTA per SM) streams one contiguous range of the pages of all (sequence, KV
+// head) pairs, laid end to end.  The ranges differ by at most one page, so
+// every warp finishes at about the same time whatever the lengths, and a
+// warp's ring of page copies runs on across the pair boundaries inside its
+// range, so the pipeline fills once per warp instead of once per partition.
+// A warp holding a whole pair writes its output; the pieces of a pair split
+// between warps are written as normalised partials with their log2-sum-exp
+// and combined by the flat merge (the same log-sum-exp merge as the uniform
+// split's).  The per-page arithmetic is the decode body's (bf16_pages).
+
+#include <atomic>
+#include <climits>
+
+#include "pkv_decode_body.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int kFlatMaxSeqs = 1024;
+
+// Ring-owning warps of a flat CTA: 3 stages of one page each per warp, as
+// many warps as one SM's shared memory holds.
+template <int D>
+struct FlatWarps {
+  static constexpr int value = D == 128 ? 9 : 16;
+};
+
+template <int D>
+struct FlatTile {
+  static constexpr int NW = FlatWarps<D>::value;
+  using T = DecodeTile<D, NW>;  // rings and barriers (its ids area is not used)
+  static constexpr int kPreOffset = T::kIdsOffset;  // [kFlatMaxSeqs + 1] page prefix sums
+  static constexpr int kScanOffset = kPreOffset + (kFlatMaxSeqs + 1) * 4;  // per-warp totals
+  static constexpr int kEnd = kScanOffset + 32 * 4;
+  static constexpr int kSmemBytes = kEnd + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "flat decode CTA does not fit in shared memory");
+};
+
+struct DecodeFlatParams {
+  int32_t* pre_out;  // [num_seqs + 1] the page prefix sums, for the merge
+  int num_seqs;      // <= kFlatMaxSeqs
+  int max_blocks;    // pages attended per sequence at most
+  int total_warps;   // warps of the launch
+};
+
+// Pages of a context of `len` tokens, clamped to `max_blocks` (bad: the
+// length was negative or had to be clamped).
+__device__ __forceinline__ int flat_pages(int len, int max_blocks, bool& bad) {
+  bad = len < 0;
+  int n = len <= 0 ? 0 : len / kBlockTokens + (len % kBlockTokens != 0);
+  if (n > max_blocks) {
+    n = max_blocks;
+    bad = true;
+  }
+  return n;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(FlatWarps<D>::value * 32, 1)
+paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p,
+                         const DecodeFlatParams fp) {
+  constexpr int NW = FlatWarps<D>::value;
+  constexpr int kThreads = NW * 32;
+  using F = FlatTile<D>;
+  using T = DecodeTile<D, NW>;
+  using Acc = DecAcc<D, G>;
+  constexpr int NH = Acc::NH;
+  constexpr int MT = Acc::MT;
+  constexpr int KSTEPS = D / 16;
+  constexpr unsigned kFull = 0xffffffffu;
+  // with wait_late only the loads of a sequence's last page wait for the
+  // grid before (the step's append); otherwise every input may be its output
+  if (!p.wait_late) griddep_wait();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int32_t* pre = reinterpret_cast<int32_t*>(smem + F::kPreOffset);
+  int32_t* scan = reinterpret_cast<int32_t*>(smem + F::kScanOffset);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int S = fp.num_seqs;
+  const int Hkv = p.kv_heads;
+
+  // ---- the plan, computed alike by every CTA: pages per sequence and their
+  // exclusive prefix sum pre[], pre[S] the pages of one KV head
+  const int per = (S + kThreads - 1) / kThreads;
+  const int s_begin = threadIdx.x * per;
+  int local = 0;
+  for (int k = 0; k < per; ++k) {
+    const int s = s_begin + k;
+    if (s < S) {
+      bool bad;
+      const int n = flat_pages(__ldg(p.context_lens + s), fp.max_blocks, bad);
+      if (bad && blockIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
+      pre[s] = n;
+      local += n;
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan[warp] = incl;
+  const uint32_t ring = smem_u32(smem + warp * T::kRingBytes);
+  const uint32_t bars = smem_u32(smem + T::kBarOffset) + warp * kDecodeStages * 8;
+  if (lane == 0) {
+    for (int st = 0; st < kDecodeStages; ++st) mbar_init(bars + st * 8, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < NW ? scan[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane < NW) scan[lane] = v;  // inclusive over the warps
+  }
+  __syncthreads();
+  {
+    int base = (warp > 0 ? scan[warp - 1] : 0) + incl - local;
+    for (int k = 0; k < per; ++k) {
+      const int s = s_begin + k;
+      if (s < S) {
+        const int n = pre[s];
+        pre[s] = base;
+        base += n;
+      }
+    }
+    if (threadIdx.x == 0) pre[S] = scan[NW - 1];
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int s = threadIdx.x; s <= S; s += kThreads) fp.pre_out[s] = pre[s];
+
+  // ---- this warp's range [f0, f1) of the pages laid end to end: pair
+  // (s, h) = s Hkv + h holds offsets Hkv pre[s] + h n_s + b, b < n_s
+  const long long total = (long long)Hkv * pre[S];
+  const long long W = (long long)gridDim.x * NW;
+  const long long c = total > 0 ? (total + W - 1) / W : 1;
+  const long long gw = (long long)blockIdx.x * NW + warp;
+  const long long f0 = gw * c;
+  const long long f1 = f0 + c < total ? f0 + c : total;
+  const int cnt = f0 < f1 ? int(f1 - f0) : 0;
+  if (cnt == 0) return;  // no CTA-wide barrier follows
+
+  // offset f -> (sequence, KV head, block): the last sequence starting at or
+  // before f (empty sequences start where the next one does, so the search
+  // passes over them)
+  auto locate = [&](long long f, int& s, int& h, int& b) {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)Hkv * pre[mid] <= f) lo = mid;
+      else hi = mid - 1;
+    }
+    s = lo;
+    const int n = pre[s + 1] - pre[s];
+    const long long r = f - (long long)Hkv * pre[s];
+    h = int(r / n);
+    b = int(r - (long long)h * n);
+  };
+  // Two windows of 32 consecutive pages of the range, lane k holding page
+  // 32 w + k: its block id, pair and block.  The copies run at most
+  // kDecodeStages pages ahead of the pages being computed, so they stay
+  // within the current window and the next.
+  int c_id = 0, c_pair = -1, c_blk = 0, n_id = 0, n_pair = -1, n_blk = 0;
+  auto load_window = [&](int win, int& id, int& pair, int& blk) {
+    const long long f = f0 + (long long)win * 32 + lane;
+    id = 0;
+    pair = -1;
+    blk = 0;
+    if (f < f1) {
+      int s, h, b;
+      locate(f, s, h, b);
+      id = __ldg(p.block_tables + size_t(s) * p.max_blocks_per_seq + b);
+      if (id < 0 || id >= p.num_blocks) atomicOr(&g_decode_error, kErrBadBlockId);
+      pair = s * Hkv + h;
+      blk = b;
+    }
+  };
+  int wcur = 0;
+  load_window(0, c_id, c_pair, c_blk);
+  load_window(1, n_id, n_pair, n_blk);
+  // warp-wide: page j of the range (in the current window or the next)
+  auto info = [&](int j, int& id, int& pair, int& blk) {
+    const bool in_cur = (j >> 5) == wcur;
+    id = __shfl_sync(kFull, in_cur ? c_id : n_id, j & 31);
+    pair = __shfl_sync(kFull, in_cur ? c_pair : n_pair, j & 31);
+    blk = __shfl_sync(kFull, in_cur ? c_blk : n_blk, j & 31);
+  };
+  // warp-wide: copy page j into ring stage j % kDecodeStages (lane 0 issues)
+  auto issue = [&](int j) {
+    int id, pair, blk;
+    info(j, id, pair, blk);
+    if (lane == 0) {
+      const int s = pair / Hkv, h = pair - s * Hkv;
+      if (p.wait_late && blk == pre[s + 1] - pre[s] - 1) {
+        griddep_wait();  // the step's append is complete and its rows visible
+        if (p.step_slots && h == 0) {
+          const int len = __ldg(p.context_lens + s);
+          const long long slot = p.step_slots[s];
+          const long long want = (long long)id * kBlockTokens + (len - 1) % kBlockTokens;
+          if (slot != -1 && slot != want) atomicOr(&g_decode_error, kErrBadSlot);
+        }
+      }
+      const int st = j % kDecodeStages;
+      const uint32_t bar = bars + st * 8;
+      const uint32_t kdst = ring + st * T::kStageBytes;
+      const uint32_t vdst = kdst + T::kTileBytes;
+      mbar_arrive_expect_tx(bar, T::kStageBytes);
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+        tma_load_4d(kdst + hh * T::kHalfBytes, &tmap_k, bar, hh * 64, h, 0, id);
+        tma_load_4d(vdst + hh * T::kHalfBytes, &tmap_v, bar, hh * 64, h, 0, id);
+      }
+    }
+  };
+  for (int j = 0; j < cnt && j < kDecodeStages; ++j) issue(j);
+  int issued = cnt < kDecodeStages ? cnt : kDecodeStages;
+
+  Acc acc;
+  uint32_t qf[NH][KSTEPS][2];
+  int cur_pair = -1, cur_first = 0, cur_last = 0, cur_len = 0;
+  // the finished piece of cur_pair: the output when it is the pair's whole
+  // context, else its normalised partial at partial slot cur_pair + gw
+  auto flush = [&]() {
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 4);
+        acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 8);
+        acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 16);
+      }
+    const int s = cur_pair / Hkv, h = cur_pair - s * Hkv;
+    const bool whole = cur_first == 0 && cur_last == pre[s + 1] - pre[s] - 1;
+    const size_t row0 = size_t(s) * p.q_heads + size_t(h) * G;
+    const size_t slot = size_t(cur_pair) + size_t(gw);
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int head = 8 * nh + 2 * tig + cc;
+        if (head >= G) continue;
+        const float inv = 1.f / acc.l[nh][cc];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int dim = 16 * mt + gid;
+          const float v0 = acc.o[nh][mt][cc] * inv, v1 = acc.o[nh][mt][cc + 2] * inv;
+          if (whole) {
+            store_out(p, (row0 + head) * D + dim, v0);
+            store_out(p, (row0 + head) * D + dim + 8, v1);
+          } else {
+            float* po = p.part_o + (slot * G + head) * D;
+            po[dim] = v0;
+            po[dim + 8] = v1;
+          }
+        }
+        if (!whole && gid == 0) p.part_lse[slot * G + head] = acc.m[nh][cc] + __log2f(acc.l[nh][cc]);
+      }
+  };
+
+  bool failed = false;
+  int i = 0;
+  while (i < cnt) {
+    int id0, pair0, blk0;
+    info(i, id0, pair0, blk0);
+    bool two = false;
+    if (i + 1 < cnt) {
+      int id1, pair1, blk1;
+      info(i + 1, id1, pair1, blk1);
+      two = pair1 == pair0;
+    }
+    if (pair0 != cur_pair) {
+      if (cur_pair >= 0) flush();
+      cur_pair = pair0;
+      cur_first = blk0;
+      const int s = pair0 / Hkv, h = pair0 - s * Hkv;
+      const int n = pre[s + 1] - pre[s];
+      const int raw = __ldg(p.context_lens + s);
+      cur_len = raw < 0 ? 0 : (raw < n * kBlockTokens ? raw : n * kBlockTokens);
+      const size_t row0 = size_t(s) * p.q_heads + size_t(h) * G;
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) {
+        const int head = 8 * nh + gid;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (row0 + head) * D);
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+          const bool ok = head < G;
+          qf[nh][kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
+          qf[nh][kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          acc.o[nh][mt][0] = acc.o[nh][mt][1] = acc.o[nh][mt][2] = acc.o[nh][mt][3] = 0.f;
+        acc.m[nh][0] = acc.m[nh][1] = -INFINITY;
+        acc.l[nh][0] = acc.l[nh][1] = 0.f;
+      }
+    }
+    bool landed = mbar_wait_bounded(bars + (i % kDecodeStages) * 8, (i / kDecodeStages) & 1);
+    if (two && landed)
+      landed = mbar_wait_bounded(bars + ((i + 1) % kDecodeStages) * 8,
+                                 ((i + 1) / kDecodeStages) & 1);
+    if (!__all_sync(kFull, landed)) {
+      failed = true;
+      break;
+    }
+    if (two)
+      bf16_pages<D, G, 2, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2, lane);
+    else
+      bf16_pages<D, G, 1, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2, lane);
+    cur_last = blk0 + (two ? 1 : 0);
+    __syncwarp();  // every lane is done reading these stages
+    const int step = two ? 2 : 1;
+    for (int j = i; j < i + step; ++j)
+      if (j + kDecodeStages < cnt) {
+        issue(j + kDecodeStages);
+        ++issued;
+      }
+    i += step;
+    if ((i >> 5) != wcur && i < cnt) {
+      wcur = i >> 5;
+      c_id = n_id;
+      c_pair = n_pair;
+      c_blk = n_blk;
+      load_window(wcur + 1, n_id, n_pair, n_blk);
+    }
+  }
+  if (failed) {
+    // Record the timeout and wait (bounded) for this warp's copies still in
+    // flight, so no TMA writes into shared memory after the CTA exits.
+    if (lane == 0) {
+      atomicOr(&g_decode_error, kErrWaitTimeout);
+      for (int k = i; k < issued; ++k)
+        (void)mbar_wait_bounded(bars + (k % kDecodeStages) * 8, (k / kDecodeStages) & 1);
+    }
+    __syncwarp();
+    return;
+  }
+  if (cur_pair >= 0) flush();
+}
+
+// The merge of the flat split: row (sequence s, head hq) of pair p = s Hkv +
+// hq / G; the pair's pages [start, start + n_s) lie in the ranges of warps
+// w0 = start / c .. w1 = (start + n_s - 1) / c, and warp w's piece is at
+// partial slot p + w (pieces are ordered by pair and warp alike, so no two
+// share a slot).  A pair inside one warp's range was written by the kernel;
+// an empty sequence gets zeros.  Four dims per thread.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const DecodeParams p,
+                                                                      const DecodeFlatParams fp,
+                                                                      long long total_rows) {
+  constexpr int TPR = D / 4;
+  griddep_wait();
+  const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = gtid / TPR;
+  const int c4 = int(gtid - row * TPR);
+  if (row >= total_rows) return;
+  const int seq = int(row / p.q_heads);
+  const int hq = int(row - (long long)seq * p.q_heads);
+  const int G = p.q_heads / p.kv_heads;
+  const int h = hq / G, hg = hq - h * G;
+  const int32_t* pre = fp.pre_out;
+  const int n = __ldg(pre + seq + 1) - __ldg(pre + seq);
+  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n > 0) {
+    const long long total = (long long)p.kv_heads * __ldg(pre + fp.num_seqs);
+    const long long W = fp.total_warps;
+    const long long c = (total + W - 1) / W;
+    const long long start = (long long)p.kv_heads * __ldg(pre + seq) + (long long)h * n;
+    const long long w0 = start / c, w1 = (start + n - 1) / c;
+    if (w0 == w1) return;  // written by the kernel
+    const long long pair = (long long)seq * p.kv_heads + h;
+    float big = -INFINITY;
+    for (long long w = w0; w <= w1; ++w) big = fmaxf(big, __ldg(p.part_lse + (pair + w) * G + hg));
+    float tot = 0.f;
+    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long w = w0; w <= w1; ++w) {
+      const size_t slot = size_t(pair + w) * G + hg;
+      const float wgt = ex2(__ldg(p.part_lse + slot) - big);
+      const float4 x = __ldg(reinterpret_cast<const float4*>(p.part_o + slot * D) + c4);
+      tot += wgt;
+      val.x += wgt * x.x;
+      val.y += wgt * x.y;
+      val.z += wgt * x.z;
+      val.w += wgt * x.w;
+    }
+    res = make_float4(val.x / tot, val.y / tot, val.z / tot, val.w / tot);
+  }
+  const size_t o = size_t(row) * D + 4 * c4;
+  store_out(p, o, res.x);
+  store_out(p, o + 1, res.y);
+  store_out(p, o + 2, res.z);
+  store_out(p, o + 3, res.w);
+}
+
+template <int D, int G>
+static cudaError_t launch_flat_t(const DecodeParams& prm, const DecodeFlatParams& fp, int ctas,
+                                 const CUtensorMap* tk, const CUtensorMap* tv,
+                                 cudaStream_t stream) {
+  using F = FlatTile<D>;
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  cudaError_t e = set_smem_limit_once(paged_decode_flat_kernel<D, G>, F::kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
+  e = launch_after_previous(paged_decode_flat_kernel<D, G>, dim3(unsigned(ctas)),
+                            dim3(F::NW * 32), F::kSmemBytes, stream, *tk, *tv, prm, fp);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)fp.num_seqs * prm.q_heads;
+  const long long blocks = (rows * (D / 4) + 255) / 256;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  return launch_after_previous(paged_decode_merge_flat_kernel<D>, dim3(unsigned(blocks)),
+                               dim3(256), 0, stream, prm, fp, rows);
+}
+
+template <int D>
+static cudaError_t launch_flat_d(const DecodeParams& prm, const DecodeFlatParams& fp, int group,
+                                 int ctas, const CUtensorMap* tk, const CUtensorMap* tv,
+                                 cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_flat_t<D, 1>(prm, fp, ctas, tk, tv, st);
+    case 2: return launch_flat_t<D, 2>(prm, fp, ctas, tk, tv, st);
+    case 4: return launch_flat_t<D, 4>(prm, fp, ctas, tk, tv, st);
+    case 8: return launch_flat_t<D, 8>(prm, fp, ctas, tk, tv, st);
+    case 16: return launch_flat_t<D, 16>(prm, fp, ctas, tk, tv, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_flat_warps(int d_head) {
+  return d_head == 128 ? FlatWarps<128>::value : d_head == 64 ? FlatWarps<64>::value : 0;
+}
+int decode_flat_max_seqs() { return kFlatMaxSeqs; }
+
+cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                     const CUtensorMap* tmap_v, cudaStream_t stream) {
+  if (a.num_seqs <= 0 || a.num_seqs > kFlatMaxSeqs || a.flat_ctas <= 0 || !a.flat_pre ||
+      !a.part_o || !a.part_lse)
+    return cudaErrorInvalidValue;
+  DecodeParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.out = a.out;
+  prm.part_o = a.part_o;
+  prm.part_lse = a.part_lse;
+  prm.q_heads = a.q_heads;
+  prm.kv_heads = a.kv_heads;
+  prm.num_blocks = a.num_blocks;
+  prm.max_blocks_per_seq = a.max_blocks_per_seq;
+  prm.partition_blocks = 0;  // not used by the flat split
+  prm.num_parts = 0;
+  prm.scale_log2 = a.scale_log2;
+  prm.out_scale = 1.f;
+  prm.first_block = 0;
+  prm.force_partials = 0;
+  prm.extra_o = nullptr;
+  prm.extra_lse = nullptr;
+  prm.out_bf16 = a.out_bf16 ? 1 : 0;
+  prm.wait_late = a.wait_late ? 1 : 0;
+  prm.step_slots = a.step_slots;
+  DecodeFlatParams fp;
+  fp.pre_out = a.flat_pre;
+  fp.num_seqs = a.num_seqs;
+  fp.max_blocks = a.flat_max_blocks;
+  fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head);
+  const int group = a.q_heads / a.kv_heads;
+  if (a.d_head == 128) return launch_flat_d<128>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
+  if (a.d_head == 64) return launch_flat_d<64>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
+  return cudaErrorInvalidValue;
+}
+
+// Device address of this unit's error word on the current device.
+cudaError_t decode_flat_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_decode_error);
+}
+
+unsigned read_decode_flat_error(bool clear) {
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_decode_error, sizeof(word)) != cudaSuccess) return ~0u;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  }
+  return word;
+}
+
+}  // namespace pkv

@@ -122,6 +122,11 @@ struct Plan {
   bool list = false;
   int list_target = 0, list_items = 0, list_max_blocks = 0;
   size_t list_lse_offset = 0, list_base_offset = 0;
+  // flat split (bf16 decode only): one CTA per SM, partial slots for every
+  // pair and every warp, the page prefix sums after them
+  bool flat = false;
+  int flat_ctas = 0, flat_max_blocks = 0;
+  size_t flat_lse_offset = 0, flat_pre_offset = 0;
 };
 
 // Partition choice.  Work items are (sequence x KV head, partition).  Long
@@ -152,14 +157,19 @@ constexpr int kMixedPrefillSpanPermille = 1000;
 // serves PKV_SPLIT_BALANCED, the CTA-capped decode and the fused mixed step.
 bool list_wins(long long /*pairs*/, long long /*slots*/) { return false; }
 
+// Whether the library's own choice takes the flat split.
+bool flat_wins(long long /*pairs*/, long long /*slots*/) { return false; }
+
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
-              int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0) {
+              int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0,
+              bool allow_flat = false) {
   *plan = Plan();  // every field is this call's: a plan object may be reused
   if (num_seqs < 0 || q_heads <= 0 || kv_heads <= 0 || max_context_len < 0) return PKV_EINVAL;
   if (q_heads % kv_heads) return PKV_EUNSUPPORTED;
   if (!supported_group(q_heads / kv_heads)) return PKV_EUNSUPPORTED;
   if (d_head != 64 && d_head != 128) return PKV_EUNSUPPORTED;
-  if (partition_blocks < PKV_SPLIT_UNIFORM) return PKV_EINVAL;
+  if (partition_blocks < PKV_SPLIT_FLAT) return PKV_EINVAL;
+  if (partition_blocks == PKV_SPLIT_FLAT && !allow_flat) partition_blocks = PKV_SPLIT_UNIFORM;
   const int max_pb = pkv::decode_max_partition_blocks();
   const int nblk_max = (max_context_len + kBlockSize - 1) / kBlockSize;
   const long long pairs = (long long)num_seqs * kv_heads;
@@ -220,6 +230,27 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
     plan->ws_bytes = 0;
     plan->lse_offset = 0;
   }
+  const bool want_flat = list_ctas == 0 && (partition_blocks == PKV_SPLIT_FLAT ||
+                                             (partition_blocks == 0 && flat_wins(pairs, slots)));
+  if (allow_flat && want_flat) {
+    if (num_seqs > pkv::decode_flat_max_seqs()) {
+      if (partition_blocks == PKV_SPLIT_FLAT) return PKV_EUNSUPPORTED;
+    } else if (num_seqs > 0) {
+      // a partial slot for every pair and every warp (slot pair + warp; see
+      // the flat merge), their log2-sum-exps, then the page prefix sums
+      const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
+      const size_t slots = size_t(pairs + warps) * size_t(q_heads / kv_heads);
+      auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+      plan->flat = true;
+      plan->flat_ctas = sms;
+      plan->flat_max_blocks = nblk_max;
+      plan->flat_lse_offset = up(slots * size_t(d_head) * sizeof(float));
+      plan->flat_pre_offset = plan->flat_lse_offset + up(slots * sizeof(float));
+      plan->ws_bytes = plan->flat_pre_offset + size_t(num_seqs + 1) * sizeof(int32_t);
+      return PKV_OK;
+    }
+  }
+  if (partition_blocks == PKV_SPLIT_FLAT) partition_blocks = PKV_SPLIT_UNIFORM;
   const bool want_list = partition_blocks == PKV_SPLIT_BALANCED || list_ctas > 0 ||
                          (partition_blocks == 0 && list_wins(pairs, slots));
   if (allow_list && want_list && num_seqs > 0 && num_seqs <= pkv::decode_list_max_seqs()) {
@@ -528,7 +559,7 @@ int pkv_decode_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max
                     size_t* out_workspace_bytes) {
   Plan plan;
   const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
-                           partition_blocks, &plan, /*allow_list=*/true);
+                           partition_blocks, &plan, /*allow_list=*/true, 0, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
   if (out_partition_blocks) *out_partition_blocks = plan.partition_blocks;
   if (out_num_parts) *out_num_parts = plan.num_parts;
@@ -540,7 +571,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d
                                   int max_context_len) {
   Plan plan;
   if (make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &plan,
-                /*allow_list=*/true) != PKV_OK)
+                /*allow_list=*/true, 0, /*allow_flat=*/true) != PKV_OK)
     return 0;
   return plan.ws_bytes;
 }
@@ -549,9 +580,18 @@ int pkv_decode_plan_uses_list(int num_seqs, int q_heads, int kv_heads, int d_hea
                               int max_context_len, int partition_blocks) {
   Plan plan;
   const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
-                           partition_blocks, &plan, /*allow_list=*/true);
+                           partition_blocks, &plan, /*allow_list=*/true, 0, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
   return plan.list ? 1 : 0;
+}
+
+int pkv_decode_plan_uses_flat(int num_seqs, int q_heads, int kv_heads, int d_head,
+                              int max_context_len, int partition_blocks) {
+  Plan plan;
+  const int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                           partition_blocks, &plan, /*allow_list=*/true, 0, /*allow_flat=*/true);
+  if (st != PKV_OK) return st;
+  return plan.flat ? 1 : 0;
 }
 
 namespace {
@@ -567,7 +607,7 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
   if (st != PKV_OK) return st;
   Plan plan;
   st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
-                 partition_blocks, &plan, /*allow_list=*/true, list_ctas);
+                 partition_blocks, &plan, /*allow_list=*/true, list_ctas, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
   if (list_ctas > 0 && !plan.list) return PKV_EUNSUPPORTED;  // more than 512 sequences
   if (num_seqs == 0) return PKV_OK;
@@ -618,12 +658,23 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
     a.list_items = plan.list_items;
     a.list_max_ctas = list_ctas;
   }
-  if (step_slots) {  // the decode step: the append just launched runs beside the split kernel
+  if (plan.flat) {
+    char* ws = static_cast<char*>(workspace);
+    a.flat = true;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(ws + plan.flat_lse_offset);
+    a.flat_pre = reinterpret_cast<int32_t*>(ws + plan.flat_pre_offset);
+    a.flat_ctas = plan.flat_ctas;
+    a.flat_max_blocks = std::min(plan.flat_max_blocks, max_blocks_per_seq);
+  }
+  if (step_slots) {  // the decode step: the append just launched runs beside the decode
     if (plan.list) return PKV_EUNSUPPORTED;
     a.wait_late = true;
     a.step_slots = step_slots;
   }
-  cudaError_t e = pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
+  cudaError_t e = plan.flat
+                      ? pkv::launch_paged_decode_flat(a, &tk, &tv, static_cast<cudaStream_t>(stream))
+                      : pkv::launch_paged_decode(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -660,7 +711,8 @@ int pkv_paged_decode_step(const void* q, int num_seqs, int q_heads, const void* 
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return PKV_EINVAL;
   // ... and the decode's, before anything is launched
   Plan plan;
-  st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, 0, &plan);
+  st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len, 0, &plan,
+                 /*allow_list=*/true, 0, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
   if (!q || !block_tables || !context_lens || !out || max_blocks_per_seq <= 0 ||
       !std::isfinite(scale))
@@ -1475,7 +1527,7 @@ namespace {
 // atomic step, so a bit raised meanwhile by a kernel on another stream stays
 // for the next query instead of being lost -- and stores the OR.
 struct ErrorWordSet {
-  unsigned* word[8];
+  unsigned* word[9];
   int count;
   int clear;
 };
@@ -1493,13 +1545,13 @@ std::mutex g_collect_mutex;  // one collection in flight per process
 
 int collect_error_words(cudaStream_t stream, bool clear, unsigned* word) {
   ErrorWordSet s = {};
-  cudaError_t (*const getters[8])(unsigned**) = {
+  cudaError_t (*const getters[9])(unsigned**) = {
       pkv::append_error_word, pkv::decode_error_word, pkv::decode_fp8_error_word,
       pkv::prefill_error_word, pkv::verify_error_word, pkv::probe_error_word,
-      pkv::mixed_decode_error_word, pkv::mixed_prefill_error_word};
-  for (int i = 0; i < 8; ++i)
+      pkv::mixed_decode_error_word, pkv::mixed_prefill_error_word, pkv::decode_flat_error_word};
+  for (int i = 0; i < 9; ++i)
     if (getters[i](&s.word[i]) != cudaSuccess) return PKV_ECUDA;
-  s.count = 8;
+  s.count = 9;
   s.clear = clear ? 1 : 0;
   std::lock_guard<std::mutex> lock(g_collect_mutex);
   collect_error_words_kernel<<<1, 1, 0, stream>>>(s);
@@ -1540,9 +1592,11 @@ int pkv_get_device_error(unsigned int* word, int clear) {
   const unsigned v = pkv::read_verify_error(clear != 0);
   const unsigned w = pkv::read_probe_error(clear != 0);
   const unsigned m = pkv::read_mixed_error(clear != 0);
-  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u || w == ~0u || m == ~0u)
+  const unsigned fl = pkv::read_decode_flat_error(clear != 0);
+  if (a == ~0u || d == ~0u || f == ~0u || d8 == ~0u || v == ~0u || w == ~0u || m == ~0u ||
+      fl == ~0u)
     return PKV_ECUDA;
-  *word = a | d | f | d8 | v | w | m;
+  *word = a | d | f | d8 | v | w | m | fl;
   return PKV_OK;
 }
 

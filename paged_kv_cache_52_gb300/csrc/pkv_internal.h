@@ -20,6 +20,7 @@ cudaError_t verify_error_word(unsigned** word);
 cudaError_t probe_error_word(unsigned** word);
 cudaError_t mixed_decode_error_word(unsigned** word);
 cudaError_t mixed_prefill_error_word(unsigned** word);
+cudaError_t decode_flat_error_word(unsigned** word);
 
 // ---- kv_append.cu
 // reject (optional): a device flag set by launch_slot_duplicates; when it is
@@ -109,6 +110,14 @@ struct DecodeArgs {
   int32_t* list_base = nullptr;
   int list_target = 0, list_min_run = 0, list_max_blocks = 0, list_items = 0;
   int list_max_ctas = 0;  // > 0: at most this many CTAs, each looping over runs
+  // flat split (bf16 decode): flat_ctas CTAs (one per SM) whose warps each
+  // stream one contiguous range of the pages of all pairs laid end to end;
+  // partials at part_o / part_lse indexed by (pair + warp) * G + head, the
+  // page prefix sums at flat_pre ([num_seqs + 1] int32), at most
+  // flat_max_blocks pages per sequence
+  bool flat = false;
+  int32_t* flat_pre = nullptr;
+  int flat_ctas = 0, flat_max_blocks = 0;
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
@@ -143,6 +152,13 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                 const CUtensorMap* tmap_v, cudaStream_t stream);
 cudaError_t launch_paged_decode_merge_only(const DecodeArgs& a, cudaStream_t stream);
 unsigned read_decode_error(bool clear);
+
+// ---- paged_decode_flat.cu (the flat split of the bf16 decode, and its merge)
+int decode_flat_warps(int d_head);  // warps of a flat CTA (0: d_head not supported)
+int decode_flat_max_seqs();
+cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                     const CUtensorMap* tmap_v, cudaStream_t stream);
+unsigned read_decode_flat_error(bool clear);
 
 // ---- paged_decode_fp8.cu (e4m3 pools, d_head 128)
 cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, const CUtensorMap* tmap_k,

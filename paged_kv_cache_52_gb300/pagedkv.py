@@ -22,6 +22,7 @@ BLOCK_SIZE = 16
 # partition_blocks values that name a split rule rather than a size
 SPLIT_BALANCED = -1   # length-balanced work list (bf16 decode)
 SPLIT_UNIFORM = -2    # uniform partitions sized by the library
+SPLIT_FLAT = -3       # flat split: each warp streams one contiguous page range (bf16 decode)
 
 DEVERR_BITS = {
     0x1: "bad slot",
@@ -72,6 +73,7 @@ SIGNATURES = {
                                               ctypes.POINTER(_sz)], ctypes.c_int),
     "pkv_decode_workspace_bytes": ([ctypes.c_int] * 5, _sz),
     "pkv_decode_plan_uses_list": ([ctypes.c_int] * 6, ctypes.c_int),
+    "pkv_decode_plan_uses_flat": ([ctypes.c_int] * 6, ctypes.c_int),
     "pkv_paged_decode_step": ([_vp, ctypes.c_int, ctypes.c_int, _vp, _i64, _vp, _i64, _vp, _vp,
                                _vp, CacheDesc, _vp, ctypes.c_int, _vp, ctypes.c_int, _f32, _vp,
                                _vp, _sz, _vp], ctypes.c_int),
@@ -371,6 +373,16 @@ def decode_plan_uses_list(num_seqs: int, q_heads: int, kv_heads: int, d_head: in
                                        partition_blocks)
     if st < 0:
         _check("pkv_decode_plan_uses_list", st)
+    return st == 1
+
+
+def decode_plan_uses_flat(num_seqs: int, q_heads: int, kv_heads: int, d_head: int,
+                          max_context_len: int, partition_blocks: int = 0) -> bool:
+    """Whether the bf16 decode takes the flat split."""
+    st = lib.pkv_decode_plan_uses_flat(num_seqs, q_heads, kv_heads, d_head, max_context_len,
+                                       partition_blocks)
+    if st < 0:
+        _check("pkv_decode_plan_uses_flat", st)
     return st == 1
 
 
