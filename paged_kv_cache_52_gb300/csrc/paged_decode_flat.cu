@@ -37,12 +37,25 @@ struct FlatTile {
   static_assert(kSmemBytes <= 232448, "flat decode CTA does not fit in shared memory");
 };
 
+// Pages a warp takes at least: a shorter range would not amortise the
+// warp's start (its plan, block ids and first copies) and would only add
+// pieces to merge.
+constexpr int kFlatMinPages = 8;
+
 struct DecodeFlatParams {
   int32_t* pre_out;  // [num_seqs + 1] the page prefix sums, for the merge
   int num_seqs;      // <= kFlatMaxSeqs
   int max_blocks;    // pages attended per sequence at most
   int total_warps;   // warps of the launch
+  int min_pages;     // pages per warp at least (the last busy warp may take fewer)
 };
+
+// Pages per warp: the pages of all pairs shared out over the warps, at least
+// min_pages each (the merge must use the same value).
+__device__ __forceinline__ long long flat_chunk(long long total, long long warps, int min_pages) {
+  const long long c = total > 0 ? (total + warps - 1) / warps : 1;
+  return c > min_pages ? c : min_pages;
+}
 
 // Pages of a context of `len` tokens, clamped to `max_blocks` (bad: the
 // length was negative or had to be clamped).
@@ -145,8 +158,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // ---- this warp's range [f0, f1) of the pages laid end to end: pair
   // (s, h) = s Hkv + h holds offsets Hkv pre[s] + h n_s + b, b < n_s
   const long long total = (long long)Hkv * pre[S];
-  const long long W = (long long)gridDim.x * NW;
-  const long long c = total > 0 ? (total + W - 1) / W : 1;
+  const long long c = flat_chunk(total, (long long)gridDim.x * NW, fp.min_pages);
   const long long gw = (long long)blockIdx.x * NW + warp;
   const long long f0 = gw * c;
   const long long f1 = f0 + c < total ? f0 + c : total;
@@ -355,41 +367,64 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // w0 = start / c .. w1 = (start + n_s - 1) / c, and warp w's piece is at
 // partial slot p + w (pieces are ordered by pair and warp alike, so no two
 // share a slot).  A pair inside one warp's range was written by the kernel;
-// an empty sequence gets zeros.  Four dims per thread.
+// an empty sequence gets zeros.  The D / 4 threads of a row (a warp at
+// d_head 128, half a warp at 64) each own four dims; a small batch splits a
+// pair into many pieces, so the threads first take the pieces' log2-sum-exps
+// in turn (max and weight sum reduced over the row's threads), then each
+// accumulates its dims over every piece with eight loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const DecodeParams p,
                                                                       const DecodeFlatParams fp,
                                                                       long long total_rows) {
-  constexpr int TPR = D / 4;
+  constexpr int TPR = D / 4;  // threads per row: 32 or 16, a warp's aligned lanes
   griddep_wait();
   const long long gtid = (long long)blockIdx.x * 256 + threadIdx.x;
   const long long row = gtid / TPR;
   const int c4 = int(gtid - row * TPR);
-  if (row >= total_rows) return;
-  const int seq = int(row / p.q_heads);
-  const int hq = int(row - (long long)seq * p.q_heads);
+  // no early return before the shuffles: a warp's rows run them together
+  const bool valid = row < total_rows;
+  long long w0 = 0, w1 = -1, pair = 0;
+  int hg = 0;
+  bool merge = false;
+  if (valid) {
+    const int seq = int(row / p.q_heads);
+    const int hq = int(row - (long long)seq * p.q_heads);
+    const int G = p.q_heads / p.kv_heads;
+    const int h = hq / G;
+    hg = hq - h * G;
+    const int32_t* pre = fp.pre_out;
+    const int n = __ldg(pre + seq + 1) - __ldg(pre + seq);
+    if (n > 0) {
+      const long long total = (long long)p.kv_heads * __ldg(pre + fp.num_seqs);
+      const long long c = flat_chunk(total, fp.total_warps, fp.min_pages);
+      const long long start = (long long)p.kv_heads * __ldg(pre + seq) + (long long)h * n;
+      w0 = start / c;
+      w1 = (start + n - 1) / c;
+      pair = (long long)seq * p.kv_heads + h;
+      merge = w1 > w0;
+    }
+  }
   const int G = p.q_heads / p.kv_heads;
-  const int h = hq / G, hg = hq - h * G;
-  const int32_t* pre = fp.pre_out;
-  const int n = __ldg(pre + seq + 1) - __ldg(pre + seq);
+  auto lse_of = [&](long long w) { return __ldg(p.part_lse + size_t(pair + w) * G + hg); };
+  float big = -INFINITY;
+  if (merge)
+    for (long long w = w0 + c4; w <= w1; w += TPR) big = fmaxf(big, lse_of(w));
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) big = fmaxf(big, __shfl_xor_sync(0xffffffffu, big, o));
+  float tot = 0.f;
+  if (merge)
+    for (long long w = w0 + c4; w <= w1; w += TPR) tot += ex2(lse_of(w) - big);
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (!valid || (w1 == w0)) return;  // outside the batch, or written by the kernel
   float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (n > 0) {
-    const long long total = (long long)p.kv_heads * __ldg(pre + fp.num_seqs);
-    const long long W = fp.total_warps;
-    const long long c = (total + W - 1) / W;
-    const long long start = (long long)p.kv_heads * __ldg(pre + seq) + (long long)h * n;
-    const long long w0 = start / c, w1 = (start + n - 1) / c;
-    if (w0 == w1) return;  // written by the kernel
-    const long long pair = (long long)seq * p.kv_heads + h;
-    float big = -INFINITY;
-    for (long long w = w0; w <= w1; ++w) big = fmaxf(big, __ldg(p.part_lse + (pair + w) * G + hg));
-    float tot = 0.f;
+  if (merge) {
     float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (long long w = w0; w <= w1; ++w) {
       const size_t slot = size_t(pair + w) * G + hg;
       const float wgt = ex2(__ldg(p.part_lse + slot) - big);
       const float4 x = __ldg(reinterpret_cast<const float4*>(p.part_o + slot * D) + c4);
-      tot += wgt;
       val.x += wgt * x.x;
       val.y += wgt * x.y;
       val.z += wgt * x.z;
@@ -473,6 +508,7 @@ cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tma
   fp.num_seqs = a.num_seqs;
   fp.max_blocks = a.flat_max_blocks;
   fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head);
+  fp.min_pages = kFlatMinPages;
   const int group = a.q_heads / a.kv_heads;
   if (a.d_head == 128) return launch_flat_d<128>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
   if (a.d_head == 64) return launch_flat_d<64>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
