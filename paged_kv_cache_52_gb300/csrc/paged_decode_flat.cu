@@ -1,13 +1,16 @@
-// Flat split of the bf16 paged decode: every warp of a persistent grid (one
-// CTA per SM) streams one contiguous range of the pages of all (sequence, KV
-// head) pairs, laid end to end.  The ranges differ by at most one page, so
-// every warp finishes at about the same time whatever the lengths, and a
-// warp's ring of page copies runs on across the pair boundaries inside its
-// range, so the pipeline fills once per warp instead of once per partition.
-// A warp holding a whole pair writes its output; the pieces of a pair split
-// between warps are written as normalised partials with their log2-sum-exp
-// and combined by the flat merge (the same log-sum-exp merge as the uniform
-// split's).  The per-page arithmetic is the decode body's (bf16_pages).
+// Flat split of the bf16 paged decode.  The blocks of all sequences are laid
+// end to end and cut into equal ranges, one per group of Hkv warps of a
+// persistent grid (one CTA per SM); warp h of a group streams KV head h of
+// its group's range.  The ranges differ by at most one block, so every warp
+// finishes at about the same time whatever the lengths; a warp's ring of page
+// copies runs on across the sequence boundaries inside its range, so the
+// pipeline fills once per warp instead of once per partition; and the warps
+// of a group read the heads of the same blocks side by side, as the uniform
+// split's CTAs of one partition do.  A warp holding a whole (sequence, head)
+// pair writes its output; the pieces of a pair split between groups are
+// written as normalised partials with their log2-sum-exp and combined by the
+// flat merge (the same log-sum-exp merge as the uniform split's).  The
+// per-page arithmetic is the decode body's (bf16_pages).
 
 #include <atomic>
 #include <climits>
@@ -37,23 +40,28 @@ struct FlatTile {
   static_assert(kSmemBytes <= 232448, "flat decode CTA does not fit in shared memory");
 };
 
-// Pages a warp takes at least: a shorter range would not amortise the
-// warp's start (its plan, block ids and first copies) and would only add
+// Blocks a group takes at least: a shorter range would not amortise its
+// warps' start (the plan, block ids and first copies) and would only add
 // pieces to merge.
 constexpr int kFlatMinPages = 8;
 
 struct DecodeFlatParams {
-  int32_t* pre_out;  // [num_seqs + 1] the page prefix sums, for the merge
+  int32_t* pre_out;  // [num_seqs + 1] the block prefix sums, for the merge
   int num_seqs;      // <= kFlatMaxSeqs
-  int max_blocks;    // pages attended per sequence at most
+  int max_blocks;    // blocks attended per sequence at most
   int total_warps;   // warps of the launch
-  int min_pages;     // pages per warp at least (the last busy warp may take fewer)
+  int min_pages;     // blocks per group at least (the last busy group may take fewer)
 };
 
-// Pages per warp: the pages of all pairs shared out over the warps, at least
-// min_pages each (the merge must use the same value).
-__device__ __forceinline__ long long flat_chunk(long long total, long long warps, int min_pages) {
-  const long long c = total > 0 ? (total + warps - 1) / warps : 1;
+// Groups of a launch: its warps in groups of Hkv (the rest idle).
+__device__ __forceinline__ long long flat_groups(long long warps, int kv_heads) {
+  return warps / kv_heads;
+}
+
+// Blocks per group: the blocks of all sequences shared out over the groups,
+// at least min_pages each (the merge must use the same value).
+__device__ __forceinline__ long long flat_chunk(long long total, long long groups, int min_pages) {
+  const long long c = total > 0 ? (total + groups - 1) / groups : 1;
   return c > min_pages ? c : min_pages;
 }
 
@@ -155,67 +163,68 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (blockIdx.x == 0)
     for (int s = threadIdx.x; s <= S; s += kThreads) fp.pre_out[s] = pre[s];
 
-  // ---- this warp's range [f0, f1) of the pages laid end to end: pair
-  // (s, h) = s Hkv + h holds offsets Hkv pre[s] + h n_s + b, b < n_s
-  const long long total = (long long)Hkv * pre[S];
-  const long long c = flat_chunk(total, (long long)gridDim.x * NW, fp.min_pages);
+  // ---- this warp's range [f0, f1) of the blocks laid end to end (sequence
+  // s holds offsets pre[s] + b, b < n_s): its group's, in KV head hw
+  const long long total = pre[S];
+  const long long groups = flat_groups((long long)gridDim.x * NW, Hkv);
   const long long gw = (long long)blockIdx.x * NW + warp;
-  const long long f0 = gw * c;
-  const long long f1 = f0 + c < total ? f0 + c : total;
+  const long long g = gw / Hkv;
+  const int hw = int(gw - g * Hkv);
+  const long long c = flat_chunk(total, groups, fp.min_pages);
+  const long long f0 = g * c;
+  const long long f1 = g >= groups ? f0 : (f0 + c < total ? f0 + c : total);
   const int cnt = f0 < f1 ? int(f1 - f0) : 0;
   if (cnt == 0) return;  // no CTA-wide barrier follows
 
-  // offset f -> (sequence, KV head, block): the last sequence starting at or
-  // before f (empty sequences start where the next one does, so the search
-  // passes over them)
-  auto locate = [&](long long f, int& s, int& h, int& b) {
+  // offset f -> (sequence, block): the last sequence starting at or before f
+  // (empty sequences start where the next one does, so the search passes
+  // over them)
+  auto locate = [&](long long f, int& s, int& b) {
     int lo = 0, hi = S - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if ((long long)Hkv * pre[mid] <= f) lo = mid;
+      if (pre[mid] <= f) lo = mid;
       else hi = mid - 1;
     }
     s = lo;
-    const int n = pre[s + 1] - pre[s];
-    const long long r = f - (long long)Hkv * pre[s];
-    h = int(r / n);
-    b = int(r - (long long)h * n);
+    b = int(f - pre[s]);
   };
   // Two windows of 32 consecutive pages of the range, lane k holding page
-  // 32 w + k: its block id, pair and block.  The copies run at most
+  // 32 w + k: its block id, sequence and block.  The copies run at most
   // kDecodeStages pages ahead of the pages being computed, so they stay
   // within the current window and the next.
-  int c_id = 0, c_pair = -1, c_blk = 0, n_id = 0, n_pair = -1, n_blk = 0;
-  auto load_window = [&](int win, int& id, int& pair, int& blk) {
+  int c_id = 0, c_seq = -1, c_blk = 0, n_id = 0, n_seq = -1, n_blk = 0;
+  auto load_window = [&](int win, int& id, int& sq, int& blk) {
     const long long f = f0 + (long long)win * 32 + lane;
     id = 0;
-    pair = -1;
+    sq = -1;
     blk = 0;
     if (f < f1) {
-      int s, h, b;
-      locate(f, s, h, b);
-      id = __ldg(p.block_tables + size_t(s) * p.max_blocks_per_seq + b);
-      if (id < 0 || id >= p.num_blocks) atomicOr(&g_decode_error, kErrBadBlockId);
-      pair = s * Hkv + h;
+      int ss, b;
+      locate(f, ss, b);
+      id = __ldg(p.block_tables + size_t(ss) * p.max_blocks_per_seq + b);
+      if (hw == 0 && (id < 0 || id >= p.num_blocks)) atomicOr(&g_decode_error, kErrBadBlockId);
+      sq = ss;
       blk = b;
     }
   };
   int wcur = 0;
-  load_window(0, c_id, c_pair, c_blk);
-  load_window(1, n_id, n_pair, n_blk);
+  load_window(0, c_id, c_seq, c_blk);
+  load_window(1, n_id, n_seq, n_blk);
   // warp-wide: page j of the range (in the current window or the next)
-  auto info = [&](int j, int& id, int& pair, int& blk) {
+  auto info = [&](int j, int& id, int& sq, int& blk) {
     const bool in_cur = (j >> 5) == wcur;
     id = __shfl_sync(kFull, in_cur ? c_id : n_id, j & 31);
-    pair = __shfl_sync(kFull, in_cur ? c_pair : n_pair, j & 31);
+    sq = __shfl_sync(kFull, in_cur ? c_seq : n_seq, j & 31);
     blk = __shfl_sync(kFull, in_cur ? c_blk : n_blk, j & 31);
   };
-  // warp-wide: copy page j into ring stage j % kDecodeStages (lane 0 issues)
+  // warp-wide: copy page j (KV head hw) into ring stage j % kDecodeStages
+  // (lane 0 issues)
   auto issue = [&](int j) {
-    int id, pair, blk;
-    info(j, id, pair, blk);
+    int id, s, blk;
+    info(j, id, s, blk);
     if (lane == 0) {
-      const int s = pair / Hkv, h = pair - s * Hkv;
+      const int h = hw;
       if (p.wait_late && blk == pre[s + 1] - pre[s] - 1) {
         griddep_wait();  // the step's append is complete and its rows visible
         if (p.step_slots && h == 0) {
@@ -242,9 +251,11 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   Acc acc;
   uint32_t qf[NH][KSTEPS][2];
-  int cur_pair = -1, cur_first = 0, cur_last = 0, cur_len = 0;
-  // the finished piece of cur_pair: the output when it is the pair's whole
-  // context, else its normalised partial at partial slot cur_pair + gw
+  int cur_seq = -1, cur_first = 0, cur_last = 0, cur_len = 0;
+  // the finished piece of (cur_seq, hw): the output when it is the pair's
+  // whole context, else its normalised partial at partial slot
+  // (cur_seq + g) Hkv + hw (for one head the pieces are ordered by sequence
+  // and group alike, so no two share a slot)
   auto flush = [&]() {
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh)
@@ -254,10 +265,10 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
         acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 8);
         acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 16);
       }
-    const int s = cur_pair / Hkv, h = cur_pair - s * Hkv;
+    const int s = cur_seq, h = hw;
     const bool whole = cur_first == 0 && cur_last == pre[s + 1] - pre[s] - 1;
     const size_t row0 = size_t(s) * p.q_heads + size_t(h) * G;
-    const size_t slot = size_t(cur_pair) + size_t(gw);
+    const size_t slot = (size_t(s) + size_t(g)) * Hkv + h;
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
@@ -285,19 +296,19 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   bool failed = false;
   int i = 0;
   while (i < cnt) {
-    int id0, pair0, blk0;
-    info(i, id0, pair0, blk0);
+    int id0, seq0, blk0;
+    info(i, id0, seq0, blk0);
     bool two = false;
     if (i + 1 < cnt) {
-      int id1, pair1, blk1;
-      info(i + 1, id1, pair1, blk1);
-      two = pair1 == pair0;
+      int id1, seq1, blk1;
+      info(i + 1, id1, seq1, blk1);
+      two = seq1 == seq0;
     }
-    if (pair0 != cur_pair) {
-      if (cur_pair >= 0) flush();
-      cur_pair = pair0;
+    if (seq0 != cur_seq) {
+      if (cur_seq >= 0) flush();
+      cur_seq = seq0;
       cur_first = blk0;
-      const int s = pair0 / Hkv, h = pair0 - s * Hkv;
+      const int s = seq0, h = hw;
       const int n = pre[s + 1] - pre[s];
       const int raw = __ldg(p.context_lens + s);
       cur_len = raw < 0 ? 0 : (raw < n * kBlockTokens ? raw : n * kBlockTokens);
@@ -343,9 +354,9 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if ((i >> 5) != wcur && i < cnt) {
       wcur = i >> 5;
       c_id = n_id;
-      c_pair = n_pair;
+      c_seq = n_seq;
       c_blk = n_blk;
-      load_window(wcur + 1, n_id, n_pair, n_blk);
+      load_window(wcur + 1, n_id, n_seq, n_blk);
     }
   }
   if (failed) {
@@ -359,15 +370,14 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncwarp();
     return;
   }
-  if (cur_pair >= 0) flush();
+  if (cur_seq >= 0) flush();
 }
 
-// The merge of the flat split: row (sequence s, head hq) of pair p = s Hkv +
-// hq / G; the pair's pages [start, start + n_s) lie in the ranges of warps
-// w0 = start / c .. w1 = (start + n_s - 1) / c, and warp w's piece is at
-// partial slot p + w (pieces are ordered by pair and warp alike, so no two
-// share a slot).  A pair inside one warp's range was written by the kernel;
-// an empty sequence gets zeros.  The D / 4 threads of a row (a warp at
+// The merge of the flat split: row (sequence s, head hq) of KV head h =
+// hq / G; the sequence's blocks [pre[s], pre[s] + n_s) lie in the ranges of
+// groups w0 = pre[s] / c .. w1 = (pre[s] + n_s - 1) / c, and group w's
+// piece is at partial slot (s + w) Hkv + h.  A pair inside one group's range
+// was written by the kernel; an empty sequence gets zeros.  The D / 4 threads of a row (a warp at
 // d_head 128, half a warp at 64) each own four dims; a small batch splits a
 // pair into many pieces, so the threads first take the pieces' log2-sum-exps
 // in turn (max and weight sum reduced over the row's threads), then each
@@ -383,29 +393,30 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
   const int c4 = int(gtid - row * TPR);
   // no early return before the shuffles: a warp's rows run them together
   const bool valid = row < total_rows;
-  long long w0 = 0, w1 = -1, pair = 0;
-  int hg = 0;
+  long long w0 = 0, w1 = -1;
+  int hg = 0, h = 0, seq = 0;
   bool merge = false;
   if (valid) {
-    const int seq = int(row / p.q_heads);
+    seq = int(row / p.q_heads);
     const int hq = int(row - (long long)seq * p.q_heads);
     const int G = p.q_heads / p.kv_heads;
-    const int h = hq / G;
+    h = hq / G;
     hg = hq - h * G;
     const int32_t* pre = fp.pre_out;
     const int n = __ldg(pre + seq + 1) - __ldg(pre + seq);
     if (n > 0) {
-      const long long total = (long long)p.kv_heads * __ldg(pre + fp.num_seqs);
-      const long long c = flat_chunk(total, fp.total_warps, fp.min_pages);
-      const long long start = (long long)p.kv_heads * __ldg(pre + seq) + (long long)h * n;
+      const long long total = __ldg(pre + fp.num_seqs);
+      const long long c =
+          flat_chunk(total, flat_groups(fp.total_warps, p.kv_heads), fp.min_pages);
+      const long long start = __ldg(pre + seq);
       w0 = start / c;
       w1 = (start + n - 1) / c;
-      pair = (long long)seq * p.kv_heads + h;
       merge = w1 > w0;
     }
   }
   const int G = p.q_heads / p.kv_heads;
-  auto lse_of = [&](long long w) { return __ldg(p.part_lse + size_t(pair + w) * G + hg); };
+  auto slot_of = [&](long long w) { return (size_t(seq + w) * p.kv_heads + h) * G + hg; };
+  auto lse_of = [&](long long w) { return __ldg(p.part_lse + slot_of(w)); };
   float big = -INFINITY;
   if (merge)
     for (long long w = w0 + c4; w <= w1; w += TPR) big = fmaxf(big, lse_of(w));
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
     float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (long long w = w0; w <= w1; ++w) {
-      const size_t slot = size_t(pair + w) * G + hg;
+      const size_t slot = slot_of(w);
       const float wgt = ex2(__ldg(p.part_lse + slot) - big);
       const float4 x = __ldg(reinterpret_cast<const float4*>(p.part_o + slot * D) + c4);
       val.x += wgt * x.x;

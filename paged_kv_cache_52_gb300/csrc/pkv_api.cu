@@ -233,12 +233,13 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   const bool want_flat = list_ctas == 0 && (partition_blocks == PKV_SPLIT_FLAT ||
                                              (partition_blocks == 0 && flat_wins(pairs, slots)));
   if (allow_flat && want_flat) {
-    if (num_seqs > pkv::decode_flat_max_seqs()) {
+    const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
+    if (num_seqs > pkv::decode_flat_max_seqs() || warps < kv_heads) {
       if (partition_blocks == PKV_SPLIT_FLAT) return PKV_EUNSUPPORTED;
     } else if (num_seqs > 0) {
-      // a partial slot for every pair and every warp (slot pair + warp; see
-      // the flat merge), their log2-sum-exps, then the page prefix sums
-      const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
+      // a partial slot for every pair and every warp (at most (S + groups)
+      // Hkv pieces; see the flat merge), their log2-sum-exps, then the block
+      // prefix sums
       const size_t slots = size_t(pairs + warps) * size_t(q_heads / kv_heads);
       auto up = [](size_t x) { return (x + 255) / 256 * 256; };
       plan->flat = true;

@@ -1,10 +1,11 @@
 """The flat split of the bf16 decode (partition_blocks = SPLIT_FLAT) against
-the CPU oracle: every warp of a one-CTA-per-SM grid streams one contiguous
-range of the pages of all (sequence, KV head) pairs, so pairs are cut at
-arbitrary pages, a warp's range crosses pairs, and a pair held by one warp
-is written without the merge.  Small cases compare every element; the
-70B-GQA recipe at 8 to 256 sequences, 7B-MHA and the 128K contexts compare
-whole batches."""
+the CPU oracle: the blocks of all sequences laid end to end are cut into
+equal ranges, one per group of Hkv warps of a one-CTA-per-SM grid (warp h
+of a group takes KV head h), so sequences are cut at arbitrary blocks, a
+range crosses sequences, and a pair held by one group is written without
+the merge.  Small cases compare every element; the 70B-GQA recipe at 1 to
+64 sequences and at full size, 7B-MHA and the 128K contexts compare whole
+batches."""
 
 import numpy as np
 import pytest
@@ -47,8 +48,8 @@ def test_flat_ragged_lengths(pk, hq, hkv, d):
 
 @pytest.mark.parametrize("d", [128, 64])
 def test_flat_many_short_sequences(pk, d):
-    # 700 sequences of 1..80 tokens: most warp ranges cross several pairs,
-    # most pairs lie inside one warp's range (written without the merge)
+    # 700 sequences of 1..80 tokens: most ranges cross several sequences,
+    # most pairs lie inside one group's range (written without the merge)
     lens = [1 + (i * 37) % 80 for i in range(700)]
     spec = wl.DecodeSpec("flat short", 18, len(lens), 16, 4, d, lens=tuple(lens))
     w = wl.make_decode_workload(spec, lens_override=lens)
