@@ -807,11 +807,13 @@ def run_append_probe(dev, pagedkv, E, peak, tokens=262144, steps=20):
     return res
 
 
-def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_len=512):
+def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 16, 32, 64), steps=200,
+                    short_len=512):
     """Small-batch decode steps of the 70B-GQA layer shape: per-step time of
     eager calls vs replay of a CUDA graph captured for the batch's bucket
-    (the decode step: append + split-K decode).  Batches of 1-4 sequences have short contexts
-    (`short_len` tokens each), where launch latency dominates; 8 and 64 draw
+    (the decode step: append + decode, the library's split: uniform, or flat
+    for 16-128 sequences).  Batches of 1-4 sequences have short contexts
+    (`short_len` tokens each), where launch latency dominates; 8 to 64 draw
     their contexts from the 70B-GQA recipe."""
     from paged_kv_cache_52_gb300.graphs import DecodeGraphRunner
     res = {}
@@ -845,9 +847,10 @@ def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 64), steps=200, short_
             s1.record()
             torch.cuda.synchronize()
             times[name] = s0.elapsed_time(s1) / steps * 1e3
+        flat = pagedkv.decode_plan_uses_flat(bsz, w.q_heads, w.kv_heads, w.d_head, max_len, 0)
         res[str(bsz)] = {"eager_us": round(times["eager"], 2), "graph_us": round(times["graph"], 2),
                          "context_lens": "512 each" if lens else "U[1024, 8192]",
-                         "kv_bytes": w.kv_bytes(),
+                         "kv_bytes": w.kv_bytes(), "split": "flat" if flat else "uniform",
                          "graph_GBps": round(w.kv_bytes() / (times["graph"] / 1e6) / 1e9, 1)}
         del w, runner, b
     return res

@@ -149,10 +149,11 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
  *                        to end; the ranges differ by at most one page, and
  *                        a warp's page copies run on across the pairs of its
  *                        range, so the copy pipeline fills once per warp;
- *   0                    the library's choice between the uniform
- *                        partitions and the flat split (the balanced list
- *                        did not beat the uniform partitions at any batch
- *                        size on GB300: a small batch's time is the
+ *   0                    the library's choice: the flat split for 128 to
+ *                        1024 (sequence, KV head) pairs at d_head 128, where
+ *                        it measured faster on GB300, else the uniform
+ *                        partitions (the balanced list did not beat them at
+ *                        any batch size: a small batch's time is the
  *                        decode's fixed cost more than the balance of its
  *                        waves).
  * The FP8 decode, the verification decode and the shared-prefix decode

@@ -157,8 +157,18 @@ constexpr int kMixedPrefillSpanPermille = 1000;
 // serves PKV_SPLIT_BALANCED, the CTA-capped decode and the fused mixed step.
 bool list_wins(long long /*pairs*/, long long /*slots*/) { return false; }
 
-// Whether the library's own choice takes the flat split.
-bool flat_wins(long long /*pairs*/, long long /*slots*/) { return false; }
+// Whether the library's own choice takes the flat split: for 128 to 1024
+// (sequence, KV head) pairs at d_head 128.  Measured on GB300 (70B-GQA
+// recipe, decode call, us, uniform / flat): 8 sequences 36.2 / 39.2, 12
+// 44.9 / 44.2, 16 60.5 / 57.2, 24 82.8 / 81.9, 32 120-140 / 103.9, 48 160.0
+// / 146.4, 64 197.4 / 183.9, 96 276.9 / 261.1, 128 353.4 / 353.5, 192 535.7 /
+// 540.0, 256 694.0 / 713.1; 7B-MHA (2048 pairs) 368.6 / 377.0, 128K contexts
+// (32 pairs) 320.0 / 328.3.  Below, a warp's few pages do not amortise its
+// start and the pieces' merge; above, the uniform grid's dynamic CTA
+// scheduling evens out the tail that equal static ranges leave.
+bool flat_wins(long long pairs, int d_head) {
+  return d_head == 128 && pairs >= 128 && pairs <= 1024;
+}
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
               int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0,
@@ -231,7 +241,7 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
     plan->lse_offset = 0;
   }
   const bool want_flat = list_ctas == 0 && (partition_blocks == PKV_SPLIT_FLAT ||
-                                             (partition_blocks == 0 && flat_wins(pairs, slots)));
+                                             (partition_blocks == 0 && flat_wins(pairs, d_head)));
   if (allow_flat && want_flat) {
     const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
     if (num_seqs > pkv::decode_flat_max_seqs() || warps < kv_heads) {

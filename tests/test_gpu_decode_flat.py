@@ -139,3 +139,35 @@ def test_flat_workspace_is_required_and_sized(pk):
     assert st == -4  # PKV_ENOMEM
     # more sequences than the flat split takes: refused when forced
     assert pk.lib.pkv_decode_plan_uses_flat(1025, 8, 8, 128, 256, pk.SPLIT_FLAT) < 0
+
+
+def test_library_choice_takes_flat_for_mid_size_batches(pk):
+    # 128 to 1024 (sequence, KV head) pairs at d_head 128
+    for S, flat in ((8, False), (15, False), (16, True), (64, True), (128, True), (129, False),
+                    (256, False)):
+        assert pk.decode_plan_uses_flat(S, 64, 8, 128, 8192, 0) == flat, S
+    assert not pk.decode_plan_uses_flat(32, 64, 8, 64, 8192, 0)      # measured at d 128 only
+
+
+@pytest.mark.parametrize("num_seqs", [16, 48])
+def test_decode_step_on_the_flat_split(pk, num_seqs):
+    # the decode step with the library's choice (flat here): the append runs
+    # beside the flat kernel, whose warps wait for it only before a
+    # sequence's last page; cache rows and outputs equal append-then-decode
+    w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV,
+                                num_seqs_override=num_seqs)
+    mcl = max(w.meta["lens"])
+    assert pk.decode_plan_uses_flat(num_seqs, 64, 8, 128, mcl, 0)
+    ref = DecodeStepOracle(w, range(num_seqs)).output()
+    kc1, vc1 = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, w.slot_mapping, kc1, vc1)
+    sep = pk.paged_decode_attention(w.q, kc1, vc1, w.block_tables, w.context_lens, w.scale,
+                                    max_context_len=mcl)
+    kc2, vc2 = w.k_cache.clone(), w.v_cache.clone()
+    fused = pk.paged_decode_step(w.q, w.k_new, w.v_new, w.slot_mapping, kc2, vc2,
+                                 w.block_tables, w.context_lens, w.scale, max_context_len=mcl)
+    torch.cuda.synchronize()
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    assert torch.equal(sep, fused)
+    assert_attention_close(fused.cpu().numpy(), ref, f"decode step on the flat split, {num_seqs}")
+    assert pk.get_device_error(clear=True) == 0
