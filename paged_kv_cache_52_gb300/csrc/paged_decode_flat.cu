@@ -189,11 +189,13 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     s = lo;
     b = int(f - pre[s]);
   };
-  // Two windows of 32 consecutive pages of the range, lane k holding page
+  // Windows of 32 consecutive pages of the range, lane k holding page
   // 32 w + k: its block id, sequence and block.  The copies run at most
   // kDecodeStages pages ahead of the pages being computed, so they stay
-  // within the current window and the next.
+  // within the current window (c_) and the next (n_); the one after (p_) is
+  // loaded a window ahead, so no page waits on a block-table load.
   int c_id = 0, c_seq = -1, c_blk = 0, n_id = 0, n_seq = -1, n_blk = 0;
+  int p_id = 0, p_seq = -1, p_blk = 0;
   auto load_window = [&](int win, int& id, int& sq, int& blk) {
     const long long f = f0 + (long long)win * 32 + lane;
     id = 0;
@@ -211,6 +213,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int wcur = 0;
   load_window(0, c_id, c_seq, c_blk);
   load_window(1, n_id, n_seq, n_blk);
+  load_window(2, p_id, p_seq, p_blk);
   // warp-wide: page j of the range (in the current window or the next)
   auto info = [&](int j, int& id, int& sq, int& blk) {
     const bool in_cur = (j >> 5) == wcur;
@@ -356,7 +359,10 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
       c_id = n_id;
       c_seq = n_seq;
       c_blk = n_blk;
-      load_window(wcur + 1, n_id, n_seq, n_blk);
+      n_id = p_id;
+      n_seq = p_seq;
+      n_blk = p_blk;
+      load_window(wcur + 2, p_id, p_seq, p_blk);
     }
   }
   if (failed) {
