@@ -10,7 +10,10 @@
 // pair writes its output; the pieces of a pair split between groups are
 // written as normalised partials with their log2-sum-exp and combined by the
 // flat merge (the same log-sum-exp merge as the uniform split's).  The
-// per-page arithmetic is the decode body's (bf16_pages).
+// per-page arithmetic is the decode body's (bf16_pages).  In the
+// shared-prefix (cascade) decode a sequence's own blocks start after its
+// prefix (first_block_of), every piece of a sequence with a prefix part is
+// written as a partial, and the merge folds the prefix part in.
 
 #include <atomic>
 #include <climits>
@@ -77,6 +80,17 @@ __device__ __forceinline__ int flat_pages(int len, int max_blocks, bool& bad) {
   return n;
 }
 
+// A sequence's own pages: those after its first own block (0 without a
+// shared prefix), and that block.
+__device__ __forceinline__ int flat_own_pages(const DecodeParams& p, int seq, int max_blocks,
+                                              int& first, bool& bad) {
+  const int len = __ldg(p.context_lens + seq);
+  const int n = flat_pages(len, max_blocks, bad);
+  first = p.seq_first_block ? __ldg(p.seq_first_block + seq) : p.first_block;
+  if (first > 0 && len < first * kBlockTokens) bad = true;  // shorter than its prefix
+  return n > first ? n - first : 0;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(FlatWarps<D>::value * 32, 1)
 paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -113,7 +127,8 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int s = s_begin + k;
     if (s < S) {
       bool bad;
-      const int n = flat_pages(__ldg(p.context_lens + s), fp.max_blocks, bad);
+      int first;
+      const int n = flat_own_pages(p, s, fp.max_blocks, first, bad);
       if (bad && blockIdx.x == 0) atomicOr(&g_decode_error, kErrBadContext);
       pre[s] = n;
       local += n;
@@ -204,6 +219,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (f < f1) {
       int ss, b;
       locate(f, ss, b);
+      b += first_block_of(p, ss);  // the table's block: after the sequence's prefix
       id = __ldg(p.block_tables + size_t(ss) * p.max_blocks_per_seq + b);
       if (hw == 0 && (id < 0 || id >= p.num_blocks)) atomicOr(&g_decode_error, kErrBadBlockId);
       sq = ss;
@@ -228,6 +244,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     info(j, id, s, blk);
     if (lane == 0) {
       const int h = hw;
+      // (the decode step has no shared prefix: blocks count from 0)
       if (p.wait_late && blk == pre[s + 1] - pre[s] - 1) {
         griddep_wait();  // the step's append is complete and its rows visible
         if (p.step_slots && h == 0) {
@@ -254,7 +271,10 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   Acc acc;
   uint32_t qf[NH][KSTEPS][2];
-  int cur_seq = -1, cur_first = 0, cur_last = 0, cur_len = 0;
+  // cur_first / cur_last: the piece's first and last blocks; cur_start /
+  // cur_end: the sequence's first own block and one past its last
+  int cur_seq = -1, cur_first = 0, cur_last = 0, cur_start = 0, cur_end = 0, cur_len = 0;
+  bool cur_extra = false;  // the sequence has a prefix part, merged later
   // the finished piece of (cur_seq, hw): the output when it is the pair's
   // whole context, else its normalised partial at partial slot
   // (cur_seq + g) Hkv + hw (for one head the pieces are ordered by sequence
@@ -269,7 +289,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
         acc.l[nh][cc] += __shfl_xor_sync(kFull, acc.l[nh][cc], 16);
       }
     const int s = cur_seq, h = hw;
-    const bool whole = cur_first == 0 && cur_last == pre[s + 1] - pre[s] - 1;
+    const bool whole = !cur_extra && cur_first == cur_start && cur_last == cur_end - 1;
     const size_t row0 = size_t(s) * p.q_heads + size_t(h) * G;
     const size_t slot = (size_t(s) + size_t(g)) * Hkv + h;
 #pragma unroll
@@ -312,9 +332,11 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
       cur_seq = seq0;
       cur_first = blk0;
       const int s = seq0, h = hw;
-      const int n = pre[s + 1] - pre[s];
+      cur_start = first_block_of(p, s);
+      cur_extra = has_extra(p, s);
+      cur_end = cur_start + pre[s + 1] - pre[s];
       const int raw = __ldg(p.context_lens + s);
-      cur_len = raw < 0 ? 0 : (raw < n * kBlockTokens ? raw : n * kBlockTokens);
+      cur_len = raw < 0 ? 0 : (raw < cur_end * kBlockTokens ? raw : cur_end * kBlockTokens);
       const size_t row0 = size_t(s) * p.q_heads + size_t(h) * G;
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh) {
@@ -380,14 +402,17 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
 }
 
 // The merge of the flat split: row (sequence s, head hq) of KV head h =
-// hq / G; the sequence's blocks [pre[s], pre[s] + n_s) lie in the ranges of
-// groups w0 = pre[s] / c .. w1 = (pre[s] + n_s - 1) / c, and group w's
-// piece is at partial slot (s + w) Hkv + h.  A pair inside one group's range
-// was written by the kernel; an empty sequence gets zeros.  The D / 4 threads of a row (a warp at
-// d_head 128, half a warp at 64) each own four dims; a small batch splits a
-// pair into many pieces, so the threads first take the pieces' log2-sum-exps
-// in turn (max and weight sum reduced over the row's threads), then each
-// accumulates its dims over every piece with eight loads in flight.
+// hq / G; the sequence's own blocks [pre[s], pre[s] + n_s) in the order of
+// the launch lie in the ranges of groups w0 = pre[s] / c .. w1 = (pre[s] +
+// n_s - 1) / c, and group w's piece is at partial slot (s + w) Hkv + h.  A
+// pair inside one group's range, without a prefix part, was written by the
+// kernel; in the cascade decode the prefix part (extra_o, extra_lse) is one
+// more piece; an empty sequence without one gets zeros.  The D / 4 threads of
+// a row (a warp at d_head 128, half a warp at 64) each own four dims; a
+// small batch splits a pair into many pieces, so the threads first take the
+// pieces' log2-sum-exps in turn (max and weight sum reduced over the row's
+// threads), then each accumulates its dims over every piece with eight loads
+// in flight.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const DecodeParams p,
                                                                       const DecodeFlatParams fp,
@@ -401,13 +426,14 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
   const bool valid = row < total_rows;
   long long w0 = 0, w1 = -1;
   int hg = 0, h = 0, seq = 0;
-  bool merge = false;
+  bool extra = false;
   if (valid) {
     seq = int(row / p.q_heads);
     const int hq = int(row - (long long)seq * p.q_heads);
     const int G = p.q_heads / p.kv_heads;
     h = hq / G;
     hg = hq - h * G;
+    extra = has_extra(p, seq);
     const int32_t* pre = fp.pre_out;
     const int n = __ldg(pre + seq + 1) - __ldg(pre + seq);
     if (n > 0) {
@@ -417,26 +443,35 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
       const long long start = __ldg(pre + seq);
       w0 = start / c;
       w1 = (start + n - 1) / c;
-      merge = w1 > w0;
     }
   }
+  const bool pieces = w1 >= w0;
+  const bool merge = extra || w1 > w0;  // else written by the kernel, or zeros
   const int G = p.q_heads / p.kv_heads;
   auto slot_of = [&](long long w) { return (size_t(seq + w) * p.kv_heads + h) * G + hg; };
   auto lse_of = [&](long long w) { return __ldg(p.part_lse + slot_of(w)); };
   float big = -INFINITY;
-  if (merge)
+  if (merge && pieces)
     for (long long w = w0 + c4; w <= w1; w += TPR) big = fmaxf(big, lse_of(w));
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) big = fmaxf(big, __shfl_xor_sync(0xffffffffu, big, o));
+  const float xl = (valid && extra) ? __ldg(p.extra_lse + row) : -INFINITY;
+  big = fmaxf(big, xl);
   float tot = 0.f;
-  if (merge)
+  if (merge && pieces)
     for (long long w = w0 + c4; w <= w1; w += TPR) tot += ex2(lse_of(w) - big);
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if (!valid || (w1 == w0)) return;  // outside the batch, or written by the kernel
+  if (!valid || (!merge && pieces)) return;  // outside the batch, or written by the kernel
   float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
   if (merge) {
     float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (extra) {
+      const float wgt = ex2(xl - big);
+      const float4 x = __ldg(reinterpret_cast<const float4*>(p.extra_o + size_t(row) * D) + c4);
+      tot += wgt;
+      val = make_float4(wgt * x.x, wgt * x.y, wgt * x.z, wgt * x.w);
+    }
 #pragma unroll 8
     for (long long w = w0; w <= w1; ++w) {
       const size_t slot = slot_of(w);
@@ -456,17 +491,9 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
   store_out(p, o + 3, res.w);
 }
 
-template <int D, int G>
-static cudaError_t launch_flat_t(const DecodeParams& prm, const DecodeFlatParams& fp, int ctas,
-                                 const CUtensorMap* tk, const CUtensorMap* tv,
-                                 cudaStream_t stream) {
-  using F = FlatTile<D>;
-  static std::atomic<int> attr_done[kAttrMaxDevices];
-  cudaError_t e = set_smem_limit_once(paged_decode_flat_kernel<D, G>, F::kSmemBytes, attr_done);
-  if (e != cudaSuccess) return e;
-  e = launch_after_previous(paged_decode_flat_kernel<D, G>, dim3(unsigned(ctas)),
-                            dim3(F::NW * 32), F::kSmemBytes, stream, *tk, *tv, prm, fp);
-  if (e != cudaSuccess) return e;
+template <int D>
+static cudaError_t launch_flat_merge_t(const DecodeParams& prm, const DecodeFlatParams& fp,
+                                       cudaStream_t stream) {
   const long long rows = (long long)fp.num_seqs * prm.q_heads;
   const long long blocks = (rows * (D / 4) + 255) / 256;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
@@ -474,16 +501,30 @@ static cudaError_t launch_flat_t(const DecodeParams& prm, const DecodeFlatParams
                                dim3(256), 0, stream, prm, fp, rows);
 }
 
+template <int D, int G>
+static cudaError_t launch_flat_t(const DecodeParams& prm, const DecodeFlatParams& fp, int ctas,
+                                 const CUtensorMap* tk, const CUtensorMap* tv,
+                                 cudaStream_t stream, bool with_merge) {
+  using F = FlatTile<D>;
+  static std::atomic<int> attr_done[kAttrMaxDevices];
+  cudaError_t e = set_smem_limit_once(paged_decode_flat_kernel<D, G>, F::kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
+  e = launch_after_previous(paged_decode_flat_kernel<D, G>, dim3(unsigned(ctas)),
+                            dim3(F::NW * 32), F::kSmemBytes, stream, *tk, *tv, prm, fp);
+  if (e != cudaSuccess || !with_merge) return e;
+  return launch_flat_merge_t<D>(prm, fp, stream);
+}
+
 template <int D>
 static cudaError_t launch_flat_d(const DecodeParams& prm, const DecodeFlatParams& fp, int group,
                                  int ctas, const CUtensorMap* tk, const CUtensorMap* tv,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool with_merge) {
   switch (group) {
-    case 1: return launch_flat_t<D, 1>(prm, fp, ctas, tk, tv, st);
-    case 2: return launch_flat_t<D, 2>(prm, fp, ctas, tk, tv, st);
-    case 4: return launch_flat_t<D, 4>(prm, fp, ctas, tk, tv, st);
-    case 8: return launch_flat_t<D, 8>(prm, fp, ctas, tk, tv, st);
-    case 16: return launch_flat_t<D, 16>(prm, fp, ctas, tk, tv, st);
+    case 1: return launch_flat_t<D, 1>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 2: return launch_flat_t<D, 2>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 4: return launch_flat_t<D, 4>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 8: return launch_flat_t<D, 8>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 16: return launch_flat_t<D, 16>(prm, fp, ctas, tk, tv, st, with_merge);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -493,12 +534,11 @@ int decode_flat_warps(int d_head) {
 }
 int decode_flat_max_seqs() { return kFlatMaxSeqs; }
 
-cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
-                                     const CUtensorMap* tmap_v, cudaStream_t stream) {
+// The kernel's and the merge's parameters from the launch arguments.
+static bool flat_params(const DecodeArgs& a, DecodeParams& prm, DecodeFlatParams& fp) {
   if (a.num_seqs <= 0 || a.num_seqs > kFlatMaxSeqs || a.flat_ctas <= 0 || !a.flat_pre ||
-      !a.part_o || !a.part_lse)
-    return cudaErrorInvalidValue;
-  DecodeParams prm;
+      !a.part_o || !a.part_lse || (a.d_head != 128 && a.d_head != 64))
+    return false;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
@@ -513,23 +553,40 @@ cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tma
   prm.num_parts = 0;
   prm.scale_log2 = a.scale_log2;
   prm.out_scale = 1.f;
-  prm.first_block = 0;
+  prm.first_block = a.first_block;
   prm.force_partials = 0;
-  prm.extra_o = nullptr;
-  prm.extra_lse = nullptr;
+  prm.extra_o = a.extra_o;
+  prm.extra_lse = a.extra_lse;
   prm.out_bf16 = a.out_bf16 ? 1 : 0;
+  prm.seq_first_block = a.seq_first_block;
   prm.wait_late = a.wait_late ? 1 : 0;
   prm.step_slots = a.step_slots;
-  DecodeFlatParams fp;
   fp.pre_out = a.flat_pre;
   fp.num_seqs = a.num_seqs;
   fp.max_blocks = a.flat_max_blocks;
   fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head);
   fp.min_pages = kFlatMinPages;
+  return true;
+}
+
+cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                     const CUtensorMap* tmap_v, cudaStream_t stream) {
+  DecodeParams prm;
+  DecodeFlatParams fp;
+  if (!flat_params(a, prm, fp)) return cudaErrorInvalidValue;
   const int group = a.q_heads / a.kv_heads;
-  if (a.d_head == 128) return launch_flat_d<128>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
-  if (a.d_head == 64) return launch_flat_d<64>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream);
-  return cudaErrorInvalidValue;
+  const bool with_merge = !a.skip_merge;
+  if (a.d_head == 128)
+    return launch_flat_d<128>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream, with_merge);
+  return launch_flat_d<64>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream, with_merge);
+}
+
+cudaError_t launch_paged_decode_flat_merge(const DecodeArgs& a, cudaStream_t stream) {
+  DecodeParams prm;
+  DecodeFlatParams fp;
+  if (!flat_params(a, prm, fp)) return cudaErrorInvalidValue;
+  if (a.d_head == 128) return launch_flat_merge_t<128>(prm, fp, stream);
+  return launch_flat_merge_t<64>(prm, fp, stream);
 }
 
 // Device address of this unit's error word on the current device.

@@ -32,6 +32,39 @@ int current_device_sms() {
   return n;
 }
 
+// A library-owned stream per device, with a fork and a join event, for work
+// that runs beside a caller's kernel inside one call (the cascade decode's
+// prefix pass beside its flat suffix decode).  Created on first use; callers
+// hold g_side_mutex from the fork to the join, so the events of two calls
+// do not interleave.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mutex;
+
+SideStream* side_stream_locked() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+      if (f) cudaEventDestroy(f);
+      cudaStreamDestroy(st);
+      return nullptr;
+    }
+    ss.stream = st;
+    ss.fork = f;
+    ss.join = j;
+  }
+  return &ss;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -157,17 +190,23 @@ constexpr int kMixedPrefillSpanPermille = 1000;
 // serves PKV_SPLIT_BALANCED, the CTA-capped decode and the fused mixed step.
 bool list_wins(long long /*pairs*/, long long /*slots*/) { return false; }
 
-// Whether the library's own choice takes the flat split: for 128 to 1024
-// (sequence, KV head) pairs at d_head 128.  Measured on GB300 (70B-GQA
-// recipe, decode call, us, uniform / flat): 8 sequences 36.2 / 39.2, 12
-// 44.9 / 44.2, 16 60.5 / 57.2, 24 82.8 / 81.9, 32 120-140 / 103.9, 48 160.0
-// / 146.4, 64 197.4 / 183.9, 96 276.9 / 261.1, 128 353.4 / 353.5, 192 535.7 /
-// 540.0, 256 694.0 / 713.1; 7B-MHA (2048 pairs) 368.6 / 377.0, 128K contexts
-// (32 pairs) 320.0 / 328.3.  Below, a warp's few pages do not amortise its
-// start and the pieces' merge; above, the uniform grid's dynamic CTA
+// Whether the library's own choice takes the flat split (d_head 128): for
+// 128 to 1024 (sequence, KV head) pairs, and for more pairs when the uniform
+// split needs 3 or more partitions per pair, i.e. when the longest context
+// is several times the partition the pair count allows, as in a long-tailed
+// batch.  Measured on GB300 (decode call, us, uniform / flat): 70B-GQA
+// recipe, 8 sequences 36.2 / 39.2, 12 44.9 / 44.2, 16 60.5 / 56.2, 24 82.8 /
+// 81.9, 32 120-140 / 103.1, 48 160.0 / 146.4, 64 197.4 / 182.5, 96 276.9 /
+// 261.1, 128 353.4 / 351.4, 192 535.2 / 535.8, 256 (2 partitions) 696.1 /
+// 704.2; 7B-MHA (2048 pairs, 1 partition) 368.6 / 376.4; 128K contexts (32
+// pairs) 320.7 / 320.2; the mixed step's 248 decodes (1984 pairs, lognormal
+// contexts up to 32768 tokens, 6 partitions) 555.5 / 516.4.  With fewer
+// pairs a warp's few pages do not amortise its start and the pieces' merge;
+// with many pairs in few partitions the uniform grid's dynamic CTA
 // scheduling evens out the tail that equal static ranges leave.
-bool flat_wins(long long pairs, int d_head) {
-  return d_head == 128 && pairs >= 128 && pairs <= 1024;
+bool flat_wins(long long pairs, int d_head, long long uniform_parts) {
+  if (d_head != 128 || pairs < 128) return false;
+  return pairs <= 1024 || uniform_parts >= 3;
 }
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
@@ -241,7 +280,8 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
     plan->lse_offset = 0;
   }
   const bool want_flat = list_ctas == 0 && (partition_blocks == PKV_SPLIT_FLAT ||
-                                             (partition_blocks == 0 && flat_wins(pairs, d_head)));
+                                             (partition_blocks == 0 &&
+                                              flat_wins(pairs, d_head, parts)));
   if (allow_flat && want_flat) {
     const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
     if (num_seqs > pkv::decode_flat_max_seqs() || warps < kv_heads) {
@@ -299,19 +339,41 @@ struct CascadePlan {
   Plan suffix;
   size_t part_o_off = 0, part_lse_off = 0, pre_o_off = 0, pre_lse_off = 0;
   size_t first_off = 0, ctx_off = 0, total = 0;
+  size_t flat_pre_off = 0;  // the flat suffix's block prefix sums
 };
+
+// SMs the cascade decode leaves to its prefix pass when the suffix takes the
+// flat split (a persistent grid that otherwise holds every SM).  The prefix
+// pass of the mixed step's 248 decodes (64 tensor-core items of ~20 us)
+// takes ~80 us on 16 SMs, well inside the suffix decode, whose HBM-bound
+// warps lose nothing on 136 SMs.
+constexpr int kCascadePrefixSms = 16;
 
 int make_cascade_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
                       int num_groups, CascadePlan* cp) {
   if (num_groups < 1) return PKV_EINVAL;
-  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &cp->suffix);
+  int st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &cp->suffix,
+                     /*allow_list=*/false, 0, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
+  const int sms = current_device_sms() > 0 ? current_device_sms() : 148;
+  if (cp->suffix.flat &&
+      (long long)(sms - kCascadePrefixSms) * pkv::decode_flat_warps(d_head) < kv_heads) {
+    st = make_plan(num_seqs, q_heads, kv_heads, d_head, max_context_len, 0, &cp->suffix);
+    if (st != PKV_OK) return st;
+  }
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = size_t(num_seqs) * size_t(q_heads);
-  const size_t prow = rows * size_t(cp->suffix.num_parts);
-  cp->part_o_off = 0;
-  cp->part_lse_off = up(prow * d_head * sizeof(float));
-  cp->pre_o_off = cp->part_lse_off + up(prow * sizeof(float));
+  if (cp->suffix.flat) {
+    cp->part_o_off = 0;
+    cp->part_lse_off = cp->suffix.flat_lse_offset;
+    cp->flat_pre_off = cp->suffix.flat_pre_offset;
+    cp->pre_o_off = up(cp->suffix.ws_bytes);
+  } else {
+    const size_t prow = rows * size_t(cp->suffix.num_parts);
+    cp->part_o_off = 0;
+    cp->part_lse_off = up(prow * d_head * sizeof(float));
+    cp->pre_o_off = cp->part_lse_off + up(prow * sizeof(float));
+  }
   cp->pre_lse_off = cp->pre_o_off + up(rows * d_head * sizeof(float));
   cp->first_off = cp->pre_lse_off + up(rows * sizeof(float));
   cp->ctx_off = cp->first_off + up(size_t(num_seqs) * sizeof(int32_t));
@@ -1440,8 +1502,8 @@ int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache
       !encode_pool_map(&tk, k_cache, cache) || !encode_pool_map(&tv, v_cache, cache))
     return PKV_ECUDA;
 
-  // 1. each sequence's own blocks after its prefix, split-K, partials only.
-  //    Its CTAs let the next launch start while they run ...
+  // 1. the decode of each sequence's own blocks after its prefix, partials
+  //    only
   pkv::DecodeArgs a;
   a.q = q;
   a.block_tables = block_tables;
@@ -1465,13 +1527,10 @@ int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache
   a.extra_lse = pre_lse;
   a.early_trigger = true;
   a.skip_merge = true;
-  e = pkv::launch_paged_decode(a, &tk, &tv, s);
-  if (e != cudaSuccess) return PKV_ECUDA;
 
-  // 2. ... which is every group's queries against its prefix keys,
+  // 2. the prefix pass: every group's queries against its prefix keys,
   //    non-causal, on the tensor cores (a group is one pseudo-sequence of its
-  //    members' rows): it fills the SMs the decode's last CTAs leave, and
-  //    waits for the decode only before it finishes
+  //    members' rows)
   pkv::PrefillArgs pa;
   pa.q_start = group_start;       // null: one group of all rows
   pa.block_tables = block_tables;
@@ -1490,6 +1549,41 @@ int cascade_decode(const void* q, int num_seqs, int q_heads, const void* k_cache
   pa.causal = 0;
   pa.scale_log2 = scale_log2;
   pa.allow_empty = true;          // a group with an invalid prefix has none
+
+  if (cp.suffix.flat) {
+    // 1'-2'. the own blocks on the flat split, on all but kCascadePrefixSms
+    //    SMs, and the prefix pass beside it on the library's side stream
+    //    (forked after the setup, joined before the merge): the flat grid
+    //    holds its SMs to the end, so the prefix pass gets SMs of its own
+    a.flat = true;
+    a.flat_pre = reinterpret_cast<int32_t*>(ws + cp.flat_pre_off);
+    a.flat_ctas = current_device_sms() - kCascadePrefixSms;
+    a.flat_max_blocks = std::min(cp.suffix.flat_max_blocks, max_blocks_per_seq);
+    a.early_trigger = false;
+    if (a.flat_ctas < 1) return PKV_ECUDA;
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream* side = side_stream_locked();
+    if (!side) return PKV_ECUDA;
+    if (cudaEventRecord(side->fork, s) != cudaSuccess) return PKV_ECUDA;
+    e = pkv::launch_paged_decode_flat(a, &tk, &tv, s);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess) return PKV_ECUDA;
+    pa.defer_wait = false;
+    e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, side->stream);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+      return PKV_ECUDA;
+    // 3'. the merge folds the prefix part in as one more piece
+    e = pkv::launch_paged_decode_flat_merge(a, s);
+    return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
+
+  // 1-2. the uniform split, whose CTAs let the next launch start while they
+  //    run, then the prefix pass: it fills the SMs the decode's last CTAs
+  //    leave, and waits for the decode only before it finishes
+  e = pkv::launch_paged_decode(a, &tk, &tv, s);
+  if (e != cudaSuccess) return PKV_ECUDA;
   pa.defer_wait = true;
   e = pkv::launch_paged_prefill(pa, &tq, &tk, &tv, s);
   if (e != cudaSuccess) return PKV_ECUDA;

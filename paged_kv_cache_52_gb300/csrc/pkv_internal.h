@@ -156,8 +156,11 @@ unsigned read_decode_error(bool clear);
 // ---- paged_decode_flat.cu (the flat split of the bf16 decode, and its merge)
 int decode_flat_warps(int d_head);  // warps of a flat CTA (0: d_head not supported)
 int decode_flat_max_seqs();
+// the kernel, then (unless skip_merge) its merge; with seq_first_block /
+// first_block and extra_o / extra_lse as in the cascade decode
 cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                      const CUtensorMap* tmap_v, cudaStream_t stream);
+cudaError_t launch_paged_decode_flat_merge(const DecodeArgs& a, cudaStream_t stream);
 unsigned read_decode_flat_error(bool clear);
 
 // ---- paged_decode_fp8.cu (e4m3 pools, d_head 128)

@@ -1,6 +1,8 @@
 """Shared-prefix (cascade) decode: the prefix attended once for all
-sequences on the tensor cores, the private pages by split-K, merged by
-log-sum-exp -- equal to the plain paged decode and to the oracle."""
+sequences on the tensor cores, the private pages by split-K (or, for 128 or
+more (sequence, KV head) pairs, by the flat split beside the prefix pass on
+the library's side stream), merged by log-sum-exp -- equal to the plain
+paged decode and to the oracle."""
 
 import pytest
 import torch
@@ -184,3 +186,65 @@ def test_prefix_groups_full_mixed_step_whole_batch(pk):
     out = _run_groups(pk, w, gs, gp)
     assert_attention_close(out.cpu().numpy(), ref, "prefix group, mixed-step decodes")
     assert pk.get_device_error(clear=True) == 0
+
+
+# ---- the same with the flat split for the private pages (128 or more
+# (sequence, KV head) pairs at d_head 128), the prefix pass beside it
+
+
+def _assert_flat(pk, w):
+    S, hq, d = w.q.shape
+    assert pk.decode_plan_uses_flat(S, hq, w.k_cache.shape[2], d, max(w.meta["lens"]), 0)
+
+
+def test_prefix_groups_flat_suffix_match_oracle(pk):
+    w, gs, gp = _grouped_workload([12, 1, 9, 6], [4, 2, 8, 1], hq=64, hkv=8)
+    _assert_flat(pk, w)
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    out = _run_groups(pk, _to_dev(w), gs, gp)
+    assert_attention_close(out.cpu().numpy(), ref, "prefix groups, flat suffix")
+    assert pk.get_device_error(clear=True) == 0
+
+
+def test_prefix_group_mismatch_flat_suffix(pk):
+    w, gs, gp = _grouped_workload([8, 6, 9], [4, 3, 8], lead_free=0, tail_free=1, hq=64, hkv=8)
+    _assert_flat(pk, w)
+    used = set(w.block_tables.flatten().tolist())
+    spare = next(b for b in range(w.k_cache.shape[0]) if b not in used)
+    w.block_tables[2, 2] = spare                       # a private copy of a prefix page
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    pk.get_device_error(clear=True)
+    out = _run_groups(pk, _to_dev(w), gs, gp)
+    assert pk.get_device_error(clear=True) == PREFIX_MISMATCH
+    assert_attention_close(out.cpu().numpy(), ref, "mismatched member, flat suffix")
+
+
+@pytest.mark.parametrize("prefix", [64, 1024])
+def test_shared_prefix_flat_suffix_matches_oracle(pk, prefix):
+    # 20 decodes of 64 / 8 heads, some ending right after the prefix
+    m = wl.make_mixed_workload(num_prefill=0, num_decode=20, shared_prefix=prefix,
+                               decode_cap=prefix + 400)
+    w = _decodes(m)
+    _assert_flat(pk, w)
+    ref = DecodeStepOracle(w, range(w.num_seqs)).output()
+    casc, plain = _run(pk, _to_dev(w), prefix // 16)
+    assert_attention_close(casc.cpu().numpy(), ref, f"cascade, flat suffix, prefix {prefix}")
+    assert_attention_close(casc.cpu().numpy(), plain.cpu().numpy(), "cascade vs plain, flat")
+    assert pk.get_device_error() == 0
+
+
+def test_short_member_flat_suffix(pk):
+    m = wl.make_mixed_workload(num_prefill=0, num_decode=20, shared_prefix=64, decode_cap=300)
+    w = _to_dev(_decodes(m))
+    _assert_flat(pk, w)
+    lens = w.context_lens.clone()
+    lens[2] = 30                      # inside the 64-token prefix
+    lens[5] = 64                      # exactly the prefix: no own page
+    pk.get_device_error(clear=True)
+    out = pk.paged_decode_attention_shared_prefix(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                                  lens, w.scale, 4, int(lens.max()))
+    plain = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.scale,
+                                      max_context_len=int(lens.max()))
+    torch.cuda.synchronize()
+    assert pk.get_device_error(clear=True) == PREFIX_MISMATCH
+    assert_attention_close(out.cpu().numpy(), plain.cpu().numpy(), "short members, flat suffix")
