@@ -297,7 +297,10 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
       plan->flat_max_blocks = nblk_max;
       plan->flat_lse_offset = up(slots * size_t(d_head) * sizeof(float));
       plan->flat_pre_offset = plan->flat_lse_offset + up(slots * sizeof(float));
-      plan->ws_bytes = plan->flat_pre_offset + size_t(num_seqs + 1) * sizeof(int32_t);
+      // the workspace still covers the uniform split, which the FP8 and
+      // verification decodes take with the same sizes
+      plan->ws_bytes = std::max(plan->ws_bytes,
+                                plan->flat_pre_offset + size_t(num_seqs + 1) * sizeof(int32_t));
       return PKV_OK;
     }
   }
