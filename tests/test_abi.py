@@ -274,3 +274,22 @@ def test_wait_probe_host_validation(pk):
     assert lib.pkv_wait_timeout_probe(0, null, null) == -1
     assert lib.pkv_wait_timeout_probe(limit + 1, null, null) == -1   # never longer than a real wait
     assert lib.pkv_wait_timeout_probe(16, ctypes.c_void_p((1 << 20) + 4), null) == -1
+
+
+def test_decode_plan_flat_choice_and_workspace(pk):
+    # the library's split: flat for 128-1024 (sequence, KV head) pairs at
+    # d_head 128 and for more pairs in 3 or more uniform partitions; its
+    # workspace also covers the uniform split of the same sizes (which the
+    # FP8 and verification decodes take)
+    assert not pk.decode_plan_uses_flat(8, 64, 8, 128, 8192)
+    assert pk.decode_plan_uses_flat(32, 64, 8, 128, 8192)
+    assert not pk.decode_plan_uses_flat(256, 64, 8, 128, 8192)     # 2 partitions
+    assert pk.decode_plan_uses_flat(248, 64, 8, 128, 32768)        # 6 partitions
+    assert not pk.decode_plan_uses_flat(32, 64, 8, 64, 8192)       # d_head 64
+    for args in ((32, 64, 8, 128, 8192), (248, 64, 8, 128, 32768), (700, 16, 4, 128, 80)):
+        uni = pk.decode_plan(*args, partition_blocks=pk.SPLIT_UNIFORM)[2]
+        flat = pk.decode_plan(*args, partition_blocks=pk.SPLIT_FLAT)[2]
+        auto = pk.decode_plan(*args)[2]
+        assert flat >= uni and auto >= uni
+        assert pk.lib.pkv_decode_workspace_bytes(*args) == auto
+    assert pk.lib.pkv_decode_plan_uses_flat(2000, 8, 8, 128, 256, pk.SPLIT_FLAT) < 0
