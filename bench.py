@@ -602,14 +602,17 @@ def run_mixed(args, dev, pagedkv, E):
         "decode_shared_prefix": {
             "ms": round(t_casc, 4),
             "unique_GBps": round(dec_unique / (t_casc / 1e3) / 1e9, 1),
-            "note": "prefix attended once (tensor cores) + private pages split-K + LSE merge"},
+            "note": "prefix attended once (tensor cores, beside the private pages) + private "
+                    "pages on the library's split (flat for this batch) + LSE merge"},
         "ms_per_step_shared_prefix": round(t_app + t_pre + t_casc, 4),
         "ms_per_step_two_streams": round(t_conc[False], 4),
         "ms_per_step_two_streams_shared_prefix": round(t_conc[True], 4),
         "two_streams_sm_split": {
             "ms_per_step": round(t_split, 4), "prefill_ctas": best_ctas,
             "sweep_ms_by_prefill_ctas": split_sweep,
-            "note": "shared-prefix decode on the SMs the persistent prefill leaves free"},
+            "note": "shared-prefix decode on the SMs the persistent prefill leaves free; its "
+                    "flat split wants all but 16 SMs to itself, so beside the prefill its "
+                    "late CTAs set the time -- the fused launch is the concurrent path"},
         "unified": {
             "ms_per_step": round(t_unified_grouped, 4),
             "frac_of_roofline": round(t_roof * 1e3 / t_unified_grouped, 4),
