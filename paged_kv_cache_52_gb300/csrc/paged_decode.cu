@@ -113,7 +113,7 @@ paged_decode_list_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 // The merge of the list's runs: for the row (sequence s, head h), runs
 // r < k_s of pair (s, h / G) hold their normalised output and log2-sum-exp
-// at partial row (seq_item_base[s] + r Hkv + h / G) G + h % G; the same
+// at partial row (seq_item_base[s] + (h / G) k_s + r) G + h % G; the same
 // log-sum-exp merge as paged_decode_merge4_kernel, four dims per thread.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_merge_list_kernel(const DecodeParams p,
@@ -133,10 +133,9 @@ __global__ void __launch_bounds__(256) paged_decode_merge_list_kernel(const Deco
   const int runs = (__ldg(lp.seq_item_base + seq + 1) - b) / p.kv_heads;
   const bool extra = has_extra(p, seq);
   if (runs <= 1 && !extra) return;  // written by the decode kernel
-  const size_t r0 = size_t(b + kvh) * G + (h - kvh * G);
-  const size_t rstep = size_t(p.kv_heads) * G;  // partial rows from one run to the next
+  const size_t r0 = size_t(b + kvh * runs) * G + (h - kvh * G);
   float big = extra ? __ldg(p.extra_lse + row) : -INFINITY;
-  for (int r = 0; r < runs; ++r) big = fmaxf(big, __ldg(p.part_lse + r0 + size_t(r) * rstep));
+  for (int r = 0; r < runs; ++r) big = fmaxf(big, __ldg(p.part_lse + r0 + size_t(r) * G));
   float tot = 0.f;
   float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
   if (extra) {
@@ -147,7 +146,7 @@ __global__ void __launch_bounds__(256) paged_decode_merge_list_kernel(const Deco
   }
 #pragma unroll 4
   for (int r = 0; r < runs; ++r) {
-    const size_t pr = r0 + size_t(r) * rstep;
+    const size_t pr = r0 + size_t(r) * G;
     const float w = ex2(__ldg(p.part_lse + pr) - big);
     const float4 x = __ldg(reinterpret_cast<const float4*>(p.part_o + pr * D) + c4);
     tot += w;

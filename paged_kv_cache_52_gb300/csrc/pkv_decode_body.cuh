@@ -459,10 +459,8 @@ struct DecodeListTile {
 };
 
 // The list plan of S <= kListMaxSeqs sequences, computed by all NT threads of
-// a block: base[s] = the first run of sequence s, base[S] = the run count.
-// A sequence's runs go run-major: run r of KV head h is item base[s] + r Hkv
-// + h, so the CTAs that take neighbouring items read the heads of the same
-// blocks side by side.  The run size c is the smallest in
+// a block: base[s] = the first run of sequence s (its KV heads' runs are
+// consecutive), base[S] = the run count.  The run size c is the smallest in
 // [max(min_run, ceil(Hkv T / target)), kMaxPartitionBlocks] for which the
 // runs fit the target (binary search over the block-wide run count); when
 // none fits (more pairs than the target, or runs capped at
@@ -587,8 +585,8 @@ __device__ __forceinline__ void list_item(const CUtensorMap& tmap_k, const CUten
   const int seq = lo;
   const int runs = (base[seq + 1] - base[seq]) / p.kv_heads;
   const int local = item - base[seq];
-  const int run = local / p.kv_heads;
-  const int kvh = local - run * p.kv_heads;
+  const int kvh = local / runs;
+  const int run = local - kvh * runs;
   const int raw_len = p.context_lens[seq];
   int first = 0;
   const int ns = list_own_pages(p, lp, seq, &first);  // pages after the shared prefix
