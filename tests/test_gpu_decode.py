@@ -55,7 +55,7 @@ SHAPES = [(8, 8, 128), (8, 4, 64), (16, 4, 128), (64, 8, 128), (32, 2, 64), (16,
 EDGE_LENS = [1, 15, 16, 17, 33, 200, 0, 161]
 
 
-@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+@pytest.mark.parametrize("hq,hkv,d", SHAPES + [(128, 8, 128)])
 @pytest.mark.parametrize("pb", [0, 2])
 def test_groups_heads_and_ragged_lengths(pk, hq, hkv, d, pb):
     spec = wl.DecodeSpec("edge", 11, len(EDGE_LENS), hq, hkv, d, lens=tuple(EDGE_LENS))

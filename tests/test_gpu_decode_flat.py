@@ -28,7 +28,7 @@ def pk():
     return pagedkv
 
 
-@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+@pytest.mark.parametrize("hq,hkv,d", SHAPES + [(128, 8, 128)])
 def test_flat_ragged_lengths(pk, hq, hkv, d):
     spec = wl.DecodeSpec("flat", 17, len(FLAT_LENS), hq, hkv, d, lens=tuple(FLAT_LENS))
     w = wl.make_decode_workload(spec, lens_override=FLAT_LENS)
