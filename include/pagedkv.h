@@ -156,8 +156,11 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
  *                        any batch size: a small batch's time is the
  *                        decode's fixed cost more than the balance of its
  *                        waves).
- * The FP8 decode, the verification decode and the shared-prefix decode
- * treat every value <= 0 as PKV_SPLIT_UNIFORM.
+ * The FP8 decode takes the flat split like the bf16 decode (PKV_SPLIT_FLAT,
+ * or the library's choice with the same rule) and treats the other values
+ * <= 0 as PKV_SPLIT_UNIFORM; the verification decode treats every value
+ * <= 0 as PKV_SPLIT_UNIFORM; the shared-prefix decode takes the library's
+ * choice for the sequences' own pages.
  */
 #define PKV_SPLIT_BALANCED (-1)
 #define PKV_SPLIT_UNIFORM (-2)
@@ -635,7 +638,8 @@ PKV_API int pkv_kv_append_fp8(const void* k, int64_t k_tok_stride, const void* v
  * pools: the result is the attention of the dequantized cache
  * (K = k_scale * e4m3(k_cache), V = v_scale * e4m3(v_cache)).  d_head must
  * be 128.  Same plan and workspace as the bf16 decode (pkv_decode_plan);
- * partition_blocks <= 0 = library choice.  Query values must fit f16's range
+ * partition_blocks 0 = library choice, PKV_SPLIT_FLAT = the flat split, other
+ * values <= 0 = uniform partitions.  Query values must fit f16's range
  * (|q| < 65520), else PKV_DEVERR_FP16_RANGE is set.  P enters the P V
  * product as one f16 operand: an output element is off by at most
  * 2^-10 * max|V| of the dequantized V (measured 5.3e-5 * max|V|).

@@ -18,29 +18,35 @@
 #include <atomic>
 #include <climits>
 
+#include <type_traits>
+
 #include "pkv_decode_body.cuh"
+#include "pkv_decode_fp8_body.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
 constexpr int kFlatMaxSeqs = 1024;
 
-// Ring-owning warps of a flat CTA: 3 stages of one page each per warp, as
-// many warps as one SM's shared memory holds.
-template <int D>
-struct FlatWarps {
-  static constexpr int value = D == 128 ? 9 : 16;
-};
-
-template <int D>
-struct FlatTile {
-  static constexpr int NW = FlatWarps<D>::value;
-  using T = DecodeTile<D, NW>;  // rings and barriers (its ids area is not used)
-  static constexpr int kPreOffset = T::kIdsOffset;  // [kFlatMaxSeqs + 1] page prefix sums
+// A flat CTA by page format: bf16 pages (the decode body's 3-stage rings of
+// one 2 x 16 x D x 2-byte page per stage) or FP8 pages (4 stages of 4 KB of
+// e4m3 codes, d_head 128); as many ring-owning warps as one SM's shared
+// memory holds beside the plan.
+template <int D, bool FP8>
+struct FlatCfg {
+  static constexpr int NW = FP8 ? 12 : (D == 128 ? 9 : 16);
+  static constexpr int kStages = FP8 ? 4 : kDecodeStages;
+  static constexpr int kStageBytes = FP8 ? F8Page::kStageBytes : DecodeTile<D, NW>::kStageBytes;
+  static constexpr int kTileBytes = kStageBytes / 2;   // K, then V
+  static constexpr int kHalfBytes = kBlockTokens * 128;  // a 64-dim bf16 half of a tile
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kBarOffset = NW * kRingBytes;
+  static constexpr int kPreOffset = kBarOffset + NW * kStages * 8;  // [kFlatMaxSeqs + 1] prefix sums
   static constexpr int kScanOffset = kPreOffset + (kFlatMaxSeqs + 1) * 4;  // per-warp totals
   static constexpr int kEnd = kScanOffset + 32 * 4;
   static constexpr int kSmemBytes = kEnd + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "flat decode CTA does not fit in shared memory");
+  static_assert(!FP8 || D == kF8D, "the FP8 pages are d_head 128");
 };
 
 // Blocks a group takes at least: a shorter range would not amortise its
@@ -91,16 +97,17 @@ __device__ __forceinline__ int flat_own_pages(const DecodeParams& p, int seq, in
   return n > first ? n - first : 0;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(FlatWarps<D>::value * 32, 1)
+template <int D, int G, bool FP8>
+__global__ void __launch_bounds__(FlatCfg<D, FP8>::NW * 32, 1)
 paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p,
                          const DecodeFlatParams fp) {
-  constexpr int NW = FlatWarps<D>::value;
+  using F = FlatCfg<D, FP8>;
+  using T = F;
+  constexpr int NW = F::NW;
+  constexpr int kStages = F::kStages;
   constexpr int kThreads = NW * 32;
-  using F = FlatTile<D>;
-  using T = DecodeTile<D, NW>;
-  using Acc = DecAcc<D, G>;
+  using Acc = std::conditional_t<FP8, F8Acc<G>, DecAcc<D, G>>;
   constexpr int NH = Acc::NH;
   constexpr int MT = Acc::MT;
   constexpr int KSTEPS = D / 16;
@@ -142,9 +149,9 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   if (lane == 31) scan[warp] = incl;
   const uint32_t ring = smem_u32(smem + warp * T::kRingBytes);
-  const uint32_t bars = smem_u32(smem + T::kBarOffset) + warp * kDecodeStages * 8;
+  const uint32_t bars = smem_u32(smem + T::kBarOffset) + warp * kStages * 8;
   if (lane == 0) {
-    for (int st = 0; st < kDecodeStages; ++st) mbar_init(bars + st * 8, 1);
+    for (int st = 0; st < kStages; ++st) mbar_init(bars + st * 8, 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 0) {
@@ -206,7 +213,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   };
   // Windows of 32 consecutive pages of the range, lane k holding page
   // 32 w + k: its block id, sequence and block.  The copies run at most
-  // kDecodeStages pages ahead of the pages being computed, so they stay
+  // kStages pages ahead of the pages being computed, so they stay
   // within the current window (c_) and the next (n_); the one after (p_) is
   // loaded a window ahead, so no page waits on a block-table load.
   int c_id = 0, c_seq = -1, c_blk = 0, n_id = 0, n_seq = -1, n_blk = 0;
@@ -237,7 +244,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     sq = __shfl_sync(kFull, in_cur ? c_seq : n_seq, j & 31);
     blk = __shfl_sync(kFull, in_cur ? c_blk : n_blk, j & 31);
   };
-  // warp-wide: copy page j (KV head hw) into ring stage j % kDecodeStages
+  // warp-wide: copy page j (KV head hw) into ring stage j % kStages
   // (lane 0 issues)
   auto issue = [&](int j) {
     int id, s, blk;
@@ -254,20 +261,25 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
           if (slot != -1 && slot != want) atomicOr(&g_decode_error, kErrBadSlot);
         }
       }
-      const int st = j % kDecodeStages;
+      const int st = j % kStages;
       const uint32_t bar = bars + st * 8;
       const uint32_t kdst = ring + st * T::kStageBytes;
       const uint32_t vdst = kdst + T::kTileBytes;
       mbar_arrive_expect_tx(bar, T::kStageBytes);
+      if constexpr (FP8) {  // one 128-code box per page and tensor
+        tma_load_4d(kdst, &tmap_k, bar, 0, h, 0, id);
+        tma_load_4d(vdst, &tmap_v, bar, 0, h, 0, id);
+      } else {
 #pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        tma_load_4d(kdst + hh * T::kHalfBytes, &tmap_k, bar, hh * 64, h, 0, id);
-        tma_load_4d(vdst + hh * T::kHalfBytes, &tmap_v, bar, hh * 64, h, 0, id);
+        for (int hh = 0; hh < D / 64; ++hh) {
+          tma_load_4d(kdst + hh * T::kHalfBytes, &tmap_k, bar, hh * 64, h, 0, id);
+          tma_load_4d(vdst + hh * T::kHalfBytes, &tmap_v, bar, hh * 64, h, 0, id);
+        }
       }
     }
   };
-  for (int j = 0; j < cnt && j < kDecodeStages; ++j) issue(j);
-  int issued = cnt < kDecodeStages ? cnt : kDecodeStages;
+  for (int j = 0; j < cnt && j < kStages; ++j) issue(j);
+  int issued = cnt < kStages ? cnt : kStages;
 
   Acc acc;
   uint32_t qf[NH][KSTEPS][2];
@@ -298,18 +310,21 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
       for (int cc = 0; cc < 2; ++cc) {
         const int head = 8 * nh + 2 * tig + cc;
         if (head >= G) continue;
-        const float inv = 1.f / acc.l[nh][cc];
+        const float inv = p.out_scale / acc.l[nh][cc];  // out_scale: the V scale of FP8 pools
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const int dim = 16 * mt + gid;
+          // the accumulator rows of the m-tile: dims gid and gid + 8 (bf16
+          // body), 2 gid and 2 gid + 1 (FP8 body)
+          const int dim = FP8 ? 16 * mt + 2 * gid : 16 * mt + gid;
+          const int dim2 = FP8 ? dim + 1 : dim + 8;
           const float v0 = acc.o[nh][mt][cc] * inv, v1 = acc.o[nh][mt][cc + 2] * inv;
           if (whole) {
             store_out(p, (row0 + head) * D + dim, v0);
-            store_out(p, (row0 + head) * D + dim + 8, v1);
+            store_out(p, (row0 + head) * D + dim2, v1);
           } else {
             float* po = p.part_o + (slot * G + head) * D;
             po[dim] = v0;
-            po[dim + 8] = v1;
+            po[dim2] = v1;
           }
         }
         if (!whole && gid == 0) p.part_lse[slot * G + head] = acc.m[nh][cc] + __log2f(acc.l[nh][cc]);
@@ -342,11 +357,29 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
       for (int nh = 0; nh < NH; ++nh) {
         const int head = 8 * nh + gid;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (row0 + head) * D);
+        if constexpr (FP8) {
+          // f16 Q in the FP8 body's k-slot order: dims (4 tig .. 4 tig + 3) of
+          // each 16-dim k-step (bf16 -> f16 exact within f16's range)
+          bool range_ok = true;
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-          const bool ok = head < G;
-          qf[nh][kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
-          qf[nh][kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            if (head < G) {
+              const uint2 wq = __ldg(reinterpret_cast<const uint2*>(
+                  p.q + (row0 + head) * D + kk * 16 + 4 * tig));
+              qf[nh][kk][0] = bf16x2_to_f16x2(wq.x, &range_ok);
+              qf[nh][kk][1] = bf16x2_to_f16x2(wq.y, &range_ok);
+            } else {
+              qf[nh][kk][0] = qf[nh][kk][1] = 0u;
+            }
+          }
+          if (!range_ok) atomicOr(&g_decode_error, kErrFp16Range);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const bool ok = head < G;
+            qf[nh][kk][0] = ok ? __ldg(qrow + (kk * 16 + tig * 2) / 2) : 0u;
+            qf[nh][kk][1] = ok ? __ldg(qrow + (kk * 16 + 8 + tig * 2) / 2) : 0u;
+          }
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -355,24 +388,34 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
         acc.l[nh][0] = acc.l[nh][1] = 0.f;
       }
     }
-    bool landed = mbar_wait_bounded(bars + (i % kDecodeStages) * 8, (i / kDecodeStages) & 1);
+    bool landed = mbar_wait_bounded(bars + (i % kStages) * 8, (i / kStages) & 1);
     if (two && landed)
-      landed = mbar_wait_bounded(bars + ((i + 1) % kDecodeStages) * 8,
-                                 ((i + 1) / kDecodeStages) & 1);
+      landed = mbar_wait_bounded(bars + ((i + 1) % kStages) * 8, ((i + 1) / kStages) & 1);
     if (!__all_sync(kFull, landed)) {
       failed = true;
       break;
     }
-    if (two)
-      bf16_pages<D, G, 2, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2, lane);
-    else
-      bf16_pages<D, G, 1, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2, lane);
+    if constexpr (FP8) {
+      if (two)
+        fp8_pages<G, 2, kStages, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len,
+                                    p.scale_log2, lane);
+      else
+        fp8_pages<G, 1, kStages, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len,
+                                    p.scale_log2, lane);
+    } else {
+      if (two)
+        bf16_pages<D, G, 2, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2,
+                               lane);
+      else
+        bf16_pages<D, G, 1, 1>(acc, qf, ring, i, blk0 * kBlockTokens, cur_len, p.scale_log2,
+                               lane);
+    }
     cur_last = blk0 + (two ? 1 : 0);
     __syncwarp();  // every lane is done reading these stages
     const int step = two ? 2 : 1;
     for (int j = i; j < i + step; ++j)
-      if (j + kDecodeStages < cnt) {
-        issue(j + kDecodeStages);
+      if (j + kStages < cnt) {
+        issue(j + kStages);
         ++issued;
       }
     i += step;
@@ -393,7 +436,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (lane == 0) {
       atomicOr(&g_decode_error, kErrWaitTimeout);
       for (int k = i; k < issued; ++k)
-        (void)mbar_wait_bounded(bars + (k % kDecodeStages) * 8, (k / kDecodeStages) & 1);
+        (void)mbar_wait_bounded(bars + (k % kStages) * 8, (k / kStages) & 1);
     }
     __syncwarp();
     return;
@@ -501,43 +544,45 @@ static cudaError_t launch_flat_merge_t(const DecodeParams& prm, const DecodeFlat
                                dim3(256), 0, stream, prm, fp, rows);
 }
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 static cudaError_t launch_flat_t(const DecodeParams& prm, const DecodeFlatParams& fp, int ctas,
                                  const CUtensorMap* tk, const CUtensorMap* tv,
                                  cudaStream_t stream, bool with_merge) {
-  using F = FlatTile<D>;
+  using F = FlatCfg<D, FP8>;
   static std::atomic<int> attr_done[kAttrMaxDevices];
-  cudaError_t e = set_smem_limit_once(paged_decode_flat_kernel<D, G>, F::kSmemBytes, attr_done);
+  cudaError_t e =
+      set_smem_limit_once(paged_decode_flat_kernel<D, G, FP8>, F::kSmemBytes, attr_done);
   if (e != cudaSuccess) return e;
-  e = launch_after_previous(paged_decode_flat_kernel<D, G>, dim3(unsigned(ctas)),
+  e = launch_after_previous(paged_decode_flat_kernel<D, G, FP8>, dim3(unsigned(ctas)),
                             dim3(F::NW * 32), F::kSmemBytes, stream, *tk, *tv, prm, fp);
   if (e != cudaSuccess || !with_merge) return e;
   return launch_flat_merge_t<D>(prm, fp, stream);
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_flat_d(const DecodeParams& prm, const DecodeFlatParams& fp, int group,
                                  int ctas, const CUtensorMap* tk, const CUtensorMap* tv,
                                  cudaStream_t st, bool with_merge) {
   switch (group) {
-    case 1: return launch_flat_t<D, 1>(prm, fp, ctas, tk, tv, st, with_merge);
-    case 2: return launch_flat_t<D, 2>(prm, fp, ctas, tk, tv, st, with_merge);
-    case 4: return launch_flat_t<D, 4>(prm, fp, ctas, tk, tv, st, with_merge);
-    case 8: return launch_flat_t<D, 8>(prm, fp, ctas, tk, tv, st, with_merge);
-    case 16: return launch_flat_t<D, 16>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 1: return launch_flat_t<D, 1, FP8>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 2: return launch_flat_t<D, 2, FP8>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 4: return launch_flat_t<D, 4, FP8>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 8: return launch_flat_t<D, 8, FP8>(prm, fp, ctas, tk, tv, st, with_merge);
+    case 16: return launch_flat_t<D, 16, FP8>(prm, fp, ctas, tk, tv, st, with_merge);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int decode_flat_warps(int d_head) {
-  return d_head == 128 ? FlatWarps<128>::value : d_head == 64 ? FlatWarps<64>::value : 0;
+int decode_flat_warps(int d_head, bool fp8) {
+  if (fp8) return d_head == kF8D ? FlatCfg<kF8D, true>::NW : 0;
+  return d_head == 128 ? FlatCfg<128, false>::NW : d_head == 64 ? FlatCfg<64, false>::NW : 0;
 }
 int decode_flat_max_seqs() { return kFlatMaxSeqs; }
 
 // The kernel's and the merge's parameters from the launch arguments.
 static bool flat_params(const DecodeArgs& a, DecodeParams& prm, DecodeFlatParams& fp) {
   if (a.num_seqs <= 0 || a.num_seqs > kFlatMaxSeqs || a.flat_ctas <= 0 || !a.flat_pre ||
-      !a.part_o || !a.part_lse || (a.d_head != 128 && a.d_head != 64))
+      !a.part_o || !a.part_lse || decode_flat_warps(a.d_head, a.fp8) == 0)
     return false;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.block_tables = a.block_tables;
@@ -552,7 +597,7 @@ static bool flat_params(const DecodeArgs& a, DecodeParams& prm, DecodeFlatParams
   prm.partition_blocks = 0;  // not used by the flat split
   prm.num_parts = 0;
   prm.scale_log2 = a.scale_log2;
-  prm.out_scale = 1.f;
+  prm.out_scale = a.fp8 ? a.out_scale : 1.f;
   prm.first_block = a.first_block;
   prm.force_partials = 0;
   prm.extra_o = a.extra_o;
@@ -564,7 +609,7 @@ static bool flat_params(const DecodeArgs& a, DecodeParams& prm, DecodeFlatParams
   fp.pre_out = a.flat_pre;
   fp.num_seqs = a.num_seqs;
   fp.max_blocks = a.flat_max_blocks;
-  fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head);
+  fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head, a.fp8);
   fp.min_pages = kFlatMinPages;
   return true;
 }
@@ -576,9 +621,14 @@ cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tma
   if (!flat_params(a, prm, fp)) return cudaErrorInvalidValue;
   const int group = a.q_heads / a.kv_heads;
   const bool with_merge = !a.skip_merge;
+  if (a.fp8)
+    return launch_flat_d<kF8D, true>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream,
+                                      with_merge);
   if (a.d_head == 128)
-    return launch_flat_d<128>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream, with_merge);
-  return launch_flat_d<64>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream, with_merge);
+    return launch_flat_d<128, false>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream,
+                                     with_merge);
+  return launch_flat_d<64, false>(prm, fp, group, a.flat_ctas, tmap_k, tmap_v, stream,
+                                  with_merge);
 }
 
 cudaError_t launch_paged_decode_flat_merge(const DecodeArgs& a, cudaStream_t stream) {

@@ -283,8 +283,12 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
                                              (partition_blocks == 0 &&
                                               flat_wins(pairs, d_head, parts)));
   if (allow_flat && want_flat) {
-    const long long warps = (long long)sms * pkv::decode_flat_warps(d_head);
-    if (num_seqs > pkv::decode_flat_max_seqs() || warps < kv_heads) {
+    // partial slots for the larger of the bf16 and FP8 flat grids, so one
+    // workspace serves both decodes of these sizes
+    const long long warps = (long long)sms * std::max(pkv::decode_flat_warps(d_head, false),
+                                                      pkv::decode_flat_warps(d_head, true));
+    if (num_seqs > pkv::decode_flat_max_seqs() ||
+        (long long)sms * pkv::decode_flat_warps(d_head, false) < kv_heads) {
       if (partition_blocks == PKV_SPLIT_FLAT) return PKV_EUNSUPPORTED;
     } else if (num_seqs > 0) {
       // a partial slot for every pair and every warp (at most (S + groups)
@@ -1084,7 +1088,7 @@ int decode_fp8_pool(const void* q, int num_seqs, int q_heads, const void* k_cach
   if (cache.d_head != 128) return PKV_EUNSUPPORTED;
   Plan plan;
   st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
-                 partition_blocks, &plan);
+                 partition_blocks, &plan, /*allow_list=*/false, 0, /*allow_flat=*/true);
   if (st != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
@@ -1122,6 +1126,21 @@ int decode_fp8_pool(const void* q, int num_seqs, int q_heads, const void* k_cach
   a.num_parts = plan.num_parts;
   a.scale_log2 = scale * k_scale * 1.4426950408889634f;
   a.out_scale = v_scale;
+  if (plan.flat) {
+    if ((long long)plan.flat_ctas * pkv::decode_flat_warps(128, true) < cache.kv_heads)
+      return PKV_EUNSUPPORTED;
+    char* ws = static_cast<char*>(workspace);
+    a.flat = true;
+    a.fp8 = true;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(ws + plan.flat_lse_offset);
+    a.flat_pre = reinterpret_cast<int32_t*>(ws + plan.flat_pre_offset);
+    a.flat_ctas = plan.flat_ctas;
+    a.flat_max_blocks = std::min(plan.flat_max_blocks, max_blocks_per_seq);
+    const cudaError_t ef =
+        pkv::launch_paged_decode_flat(a, &tk, &tv, static_cast<cudaStream_t>(stream));
+    return ef == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
   cudaError_t e = pkv::launch_paged_decode_fp8(a, &tk, &tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

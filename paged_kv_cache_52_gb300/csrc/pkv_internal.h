@@ -118,6 +118,7 @@ struct DecodeArgs {
   bool flat = false;
   int32_t* flat_pre = nullptr;
   int flat_ctas = 0, flat_max_blocks = 0;
+  bool fp8 = false;  // flat split over FP8 (e4m3) pools, out_scale = v_scale
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
@@ -154,7 +155,8 @@ cudaError_t launch_paged_decode_merge_only(const DecodeArgs& a, cudaStream_t str
 unsigned read_decode_error(bool clear);
 
 // ---- paged_decode_flat.cu (the flat split of the bf16 decode, and its merge)
-int decode_flat_warps(int d_head);  // warps of a flat CTA (0: d_head not supported)
+// warps of a flat CTA over bf16 or FP8 pools (0: d_head not supported)
+int decode_flat_warps(int d_head, bool fp8 = false);
 int decode_flat_max_seqs();
 // the kernel, then (unless skip_merge) its merge; with seq_first_block /
 // first_block and extra_o / extra_lse as in the cascade decode

@@ -126,3 +126,51 @@ def test_fp8_full_size_70b_gqa_whole_batch(pk):
         assert_attention_close(out[qs].cpu().numpy(), ref, f"fp8 70B full, seqs {qs[0]}..")
     assert torch.isfinite(out).all()
     assert pk.get_device_error() == 0
+
+
+# ---- the flat split over FP8 pools (partition_blocks = SPLIT_FLAT, and the
+# library's choice for mid-size and long-tailed batches)
+
+
+@pytest.mark.parametrize("hq,hkv", SHAPES)
+def test_fp8_flat_groups_and_ragged(pk, hq, hkv):
+    lens = LENS + [16 * 1000 + 1, 2]
+    spec = wl.DecodeSpec("fp8 flat edge", 14, len(lens), hq, hkv, 128, lens=tuple(lens))
+    w = _dev(wl.make_decode_workload(spec, lens_override=lens))
+    w.slot_mapping[lens.index(0)] = -1
+    ks, vs = 0.03125, 0.03125
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    ref = _fp8_oracle(w, kc8, vc8, ks, vs, range(len(lens)))
+    out, _, _ = _step(pk, w, kc8, vc8, ks, vs, pk.SPLIT_FLAT)
+    assert_attention_close(out.cpu().numpy(), ref, f"fp8 flat {hq}/{hkv}")
+    assert np.all(out[lens.index(0)].cpu().numpy() == 0.0)
+    assert pk.get_device_error() == 0
+
+
+@pytest.mark.parametrize("num_seqs", [8, 32])
+def test_fp8_flat_batches_70b_gqa(pk, num_seqs):
+    # the 70B-GQA recipe (outlier rows included); at 32 sequences the
+    # library's own choice is the flat split
+    w = wl.make_decode_workload(wl.GQA_70B, device=DEV, gen_device=DEV,
+                                num_seqs_override=num_seqs)
+    ks, vs = wl.FP8_SCALES["gqa70b"]
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    ref = _fp8_oracle(w, kc8, vc8, ks, vs, range(num_seqs))
+    pb = pk.SPLIT_FLAT if num_seqs == 8 else 0
+    if num_seqs == 32:
+        assert pk.decode_plan_uses_flat(num_seqs, 64, 8, 128, max(w.meta["lens"]), 0)
+    out, _, _ = _step(pk, w, kc8, vc8, ks, vs, pb)
+    assert_attention_close(out.cpu().numpy(), ref, f"fp8 flat, {num_seqs} sequences")
+    assert pk.get_device_error() == 0
+
+
+def test_fp8_flat_q_range_is_flagged(pk):
+    # a query value outside f16's range is flagged by the flat split as by the
+    # uniform one
+    w = _dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[300, 40]))
+    ks, vs = 0.03125, 0.03125
+    kc8, vc8 = wl.fp8_pools(w, ks, vs)
+    w.q[1, 3, 5] = 1.0e5
+    pk.get_device_error(clear=True)
+    _step(pk, w, kc8, vc8, ks, vs, pk.SPLIT_FLAT)
+    assert pk.get_device_error(clear=True) & 0x40
