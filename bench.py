@@ -474,7 +474,13 @@ def run_mixed(args, dev, pagedkv, E):
                 w.q_prefill, w.q_start, kc8, vc8, w.prefill_tables, w.prefill_lens, True,
                 w.scale, ks8, vs8, out=pout, max_q_len=chunk, workspace=pws8, max_ctas=ctas)
         with torch.cuda.stream(s_dec):
-            parts8[2]()
+            # beside another kernel the decode takes the uniform split, whose
+            # CTAs fill whatever SMs are free (the flat split's persistent
+            # grid wants its SMs to itself)
+            pagedkv.paged_decode_attention_fp8(
+                w.q_decode, kc8, vc8, w.decode_tables, w.decode_lens, w.scale, ks8, vs8,
+                out=dout, max_context_len=max_d, workspace=ws,
+                partition_blocks=pagedkv.SPLIT_UNIFORM)
         main.wait_stream(s_pre_hi)
         main.wait_stream(s_dec)
 
