@@ -168,7 +168,7 @@ def test_fp8_flat_q_range_is_flagged(pk):
     # a query value outside f16's range is flagged by the flat split as by the
     # uniform one
     w = _dev(wl.make_decode_workload(wl.GQA_70B, lens_override=[300, 40]))
-    ks, vs = 0.03125, 0.03125
+    ks, vs = wl.FP8_SCALES["gqa70b"]
     kc8, vc8 = wl.fp8_pools(w, ks, vs)
     w.q[1, 3, 5] = 1.0e5
     pk.get_device_error(clear=True)
