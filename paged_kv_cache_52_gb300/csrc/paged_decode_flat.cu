@@ -1,5 +1,5 @@
-// Flat split of the bf16 paged decode.  The blocks of all sequences are laid
-// end to end and cut into equal ranges, one per group of Hkv warps of a
+// Flat split of the paged decode (bf16 or FP8 pools).  The blocks of all
+// sequences are laid end to end and cut into equal ranges, one per group of Hkv warps of a
 // persistent grid (one CTA per SM); warp h of a group streams KV head h of
 // its group's range.  The ranges differ by at most one block, so every warp
 // finishes at about the same time whatever the lengths; a warp's ring of page
@@ -10,14 +10,13 @@
 // pair writes its output; the pieces of a pair split between groups are
 // written as normalised partials with their log2-sum-exp and combined by the
 // flat merge (the same log-sum-exp merge as the uniform split's).  The
-// per-page arithmetic is the decode body's (bf16_pages).  In the
+// per-page arithmetic is the decode bodies' (bf16_pages, fp8_pages).  In the
 // shared-prefix (cascade) decode a sequence's own blocks start after its
 // prefix (first_block_of), every piece of a sequence with a prefix part is
 // written as a partial, and the merge folds the prefix part in.
 
 #include <atomic>
 #include <climits>
-
 #include <type_traits>
 
 #include "pkv_decode_body.cuh"
