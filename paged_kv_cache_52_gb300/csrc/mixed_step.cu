@@ -31,7 +31,6 @@
 //  * every mbarrier wait is bounded; a prefill item that times out raises the
 //    abort flag, and the CTA stops taking items.
 #include "pkv_decode_body.cuh"
-#include "pkv_decode_flat_body.cuh"
 #include "pkv_internal.h"
 #include "pkv_prefill_body.cuh"
 
@@ -54,14 +53,6 @@ struct MixedParams {
   // group's shared prefix for its members' queries (0: no groups)
   int num_prefix_items;          // groups x KV heads x prefix_tiles
   int prefix_tiles;
-  // flat decode items (instead of the list's runs): item k is ranges k R ..
-  // k R + R - 1 of the decodes' own blocks laid end to end, one per R x Hkv
-  // of the ring-owning warps, warp w taking range k R + w / Hkv in KV head
-  // w % Hkv (see flat_range); pre and info written by the plan kernel
-  int flat;                      // nonzero: flat decode items
-  int flat_ranges;               // R
-  const int32_t* flat_pre;       // [num_decode + 1] own blocks' prefix sums
-  const int32_t* flat_info;      // items, blocks per range, R, blocks in all
 };
 
 template <int D>
@@ -82,77 +73,6 @@ __global__ void __launch_bounds__(512) mixed_plan_kernel(const DecodeParams p,
   griddep_wait();
   list_plan<512>(p, lp, lp.seq_item_base);
   if (threadIdx.x == 0) *counter = 0;
-}
-
-// The flat decode plan for the mixed step (one CTA): the decodes' own blocks
-// (after any shared prefix, clamped to max_blocks) and their exclusive prefix
-// sums pre[]; ranges of c blocks, c the smallest >= kFlatMinPages that makes
-// at most `target` items of R ranges; info = {items, c, R, blocks}; and the
-// zeroed counter.  S <= kListMaxSeqs * 2 sequences (two per thread).
-__global__ void __launch_bounds__(512) mixed_flat_plan_kernel(const DecodeParams p, int S,
-                                                             int max_blocks, int ranges,
-                                                             int target, int32_t* pre,
-                                                             int32_t* info, int* counter) {
-  griddep_wait();
-  __shared__ int warp_sum[16];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int n[2];
-  int local = 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int s = threadIdx.x * 2 + j;
-    n[j] = 0;
-    if (s < S) {
-      bool bad;
-      int first;
-      n[j] = flat_own_pages(p, s, max_blocks, first, bad);
-      if (bad) atomicOr(&g_decode_error, kErrBadContext);
-    }
-    local += n[j];
-  }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sum[warp] = incl;
-  __syncthreads();
-  int before = 0, all = 0;
-  for (int w = 0; w < 16; ++w) {
-    before += w < warp ? warp_sum[w] : 0;
-    all += warp_sum[w];
-  }
-  int base = before + incl - local;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int s = threadIdx.x * 2 + j;
-    if (s < S) pre[s] = base;
-    base += n[j];
-  }
-  if (threadIdx.x == 0) {
-    pre[S] = all;
-    const long long per_item = (long long)ranges * target;
-    long long c = per_item > 0 ? ((long long)all + per_item - 1) / per_item : all;
-    if (c < kFlatMinPages) c = kFlatMinPages;
-    const long long per = c * ranges;  // blocks per item
-    info[0] = all > 0 ? int(((long long)all + per - 1) / per) : 0;
-    info[1] = int(c);
-    info[2] = ranges;
-    info[3] = all;
-    *counter = 0;
-  }
-}
-
-// A flat decode range as a call of its own: its registers are allocated
-// apart from the prefill item's and the list run's (inlined, the fused body
-// spilled), and a call per item costs nothing next to the range.
-template <int D, int G>
-__device__ __noinline__ void mixed_flat_range(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                              const DecodeParams& dp, const int32_t* pre, int S,
-                                              long long f0, long long f1, long long g, int hw,
-                                              uint32_t ring, uint32_t bars) {
-  flat_range<D, G, false>(tmap_k, tmap_v, dp, pre, S, f0, f1, g, hw, ring, bars);
 }
 
 template <int D, int G>
@@ -185,7 +105,7 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   const long long Q = mp.num_prefix_items;
   const long long P = mp.num_prefill_items;
-  const long long rest = P + (mp.flat ? mp.flat_info[0] : mp.seq_item_base[lp.num_seqs]);
+  const long long rest = P + mp.seq_item_base[lp.num_seqs];
   long long span = rest * mp.prefill_span_permille / 1000;
   if (span < P) span = P;
   if (span < 1) span = 1;
@@ -220,32 +140,6 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
         prefill_item<D, G, true>(tmap_q, tmap_k, tmap_v16, pp, smem, tmem, pair, tile);
       else if (threadIdx.x == 0)
         atomicOr(&g_prefill_error, kErrBadQueryRange);
-    } else if (mp.flat) {
-      // a flat decode item: warps below R x Hkv each stream one range of the
-      // decodes' own blocks in one KV head through their ring
-      constexpr int NWd = MixedDecodeWarps<D>::value;
-      using Tl = DecodeTile<D, NWd>;
-      const long long k = pos - before;
-      const int active = mp.flat_ranges * dp.kv_heads;
-      const uint32_t ring = smem_u32(smem + warp * Tl::kRingBytes);
-      const uint32_t bars = smem_u32(smem + Tl::kBarOffset) + warp * kDecodeStages * 8;
-      if (warp < active && lane == 0) {
-        for (int st = 0; st < kDecodeStages; ++st) mbar_init(bars + st * 8, 1);
-        fence_barrier_init();
-      }
-      __syncthreads();
-      if (warp < active) {
-        const long long c = mp.flat_info[1], total = mp.flat_info[3];
-        const long long g = k * mp.flat_ranges + warp / dp.kv_heads;
-        const long long f0 = g * c;
-        const long long f1 = f0 + c < total ? f0 + c : total;
-        mixed_flat_range<D, G>(tmap_k, tmap_v, dp, mp.flat_pre, lp.num_seqs, f0, f1, g,
-                               warp % dp.kv_heads, ring, bars);
-      }
-      __syncthreads();  // every warp's copies have landed and its pieces are written
-      // the item's barriers are retired: this memory holds prefill tiles next
-      if (warp < active && lane == 0)
-        for (int st = 0; st < kDecodeStages; ++st) mbar_inval(bars + st * 8);
     } else {
       list_item<D, G, MixedDecodeWarps<D>::value>(tmap_k, tmap_v, dp, lp, smem, mp.seq_item_base,
                                          int(pos - before));
@@ -398,20 +292,9 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
   mp.prefill_span_permille = prefill_span_permille;
   mp.num_prefix_items = int(qitems);
   mp.prefix_tiles = qtiles;
-  mp.flat = da.flat ? 1 : 0;
-  mp.flat_ranges = da.flat_ranges;
-  mp.flat_pre = da.flat_pre;
-  mp.flat_info = da.flat_info;
-  if (da.flat && (da.flat_ranges < 1 || da.flat_ranges * da.kv_heads > mixed_decode_warps(pa.d_head) ||
-                  !da.flat_pre || !da.flat_info || da.num_seqs > 2 * 512 || da.flat_target < 1))
-    return cudaErrorInvalidValue;
   // 1. the decode plan (and the zeroed counter)
-  cudaError_t e =
-      da.flat ? launch_after_previous(mixed_flat_plan_kernel, dim3(1), dim3(512), 0, stream, dp,
-                                      da.num_seqs, da.flat_max_blocks, da.flat_ranges,
-                                      da.flat_target, da.flat_pre, da.flat_info, counter)
-              : launch_after_previous(mixed_plan_kernel, dim3(1), dim3(512), 0, stream, dp, lp,
-                                      counter);
+  cudaError_t e = launch_after_previous(mixed_plan_kernel, dim3(1), dim3(512), 0, stream, dp, lp,
+                                        counter);
   if (e != cudaSuccess) return e;
   // 2. the fused launch
   MixedLaunch m{tmap_q, tmap_k, tmap_v16, tmap_v, prefix ? tmap_qd : tmap_q, &pp, &pq, &dp, &lp,
@@ -420,23 +303,8 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
   else if (pa.d_head == 64) e = launch_mixed_d<64>(m, group, stream);
   else e = cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
-  // 3. the pieces (flat items) or runs (list) of each decode pair merged
-  if (da.flat) {
-    DecodeFlatParams fp;
-    fp.pre_out = da.flat_pre;
-    fp.num_seqs = da.num_seqs;
-    fp.max_blocks = da.flat_max_blocks;
-    fp.total_warps = 0;
-    fp.min_pages = kFlatMinPages;
-    fp.chunk_dev = da.flat_info + 1;
-    return launch_decode_flat_merge(dp, fp, pa.d_head, stream);
-  }
+  // 3. the runs of each decode pair merged
   return launch_decode_list_merge(dp, lp, pa.d_head, stream);
-}
-
-int mixed_decode_warps(int d_head) {
-  return d_head == 128 ? MixedDecodeWarps<128>::value
-                       : d_head == 64 ? MixedDecodeWarps<64>::value : 0;
 }
 
 // Device addresses of this unit's error words (its copies of the decode and

@@ -180,9 +180,8 @@ __global__ void __launch_bounds__(256) paged_decode_merge_flat_kernel(const Deco
     if (n > 0) {
       const long long total = __ldg(pre + fp.num_seqs);
       const long long c =
-          fp.chunk_dev ? (long long)__ldg(fp.chunk_dev)
-          : fp.chunk > 0 ? fp.chunk
-                         : flat_chunk(total, flat_groups(fp.total_warps, p.kv_heads), fp.min_pages);
+          fp.chunk > 0 ? fp.chunk
+                       : flat_chunk(total, flat_groups(fp.total_warps, p.kv_heads), fp.min_pages);
       const long long start = __ldg(pre + seq);
       w0 = start / c;
       w1 = (start + n - 1) / c;

@@ -181,11 +181,6 @@ constexpr int kListMinRun = 8;
 // items spread over the whole list: 0.9005 ms at 1000, 0.9104 at 950,
 // 0.9134 at 900, 0.926 at 800, 0.971 at 500 (with its prefix group).
 constexpr int kMixedPrefillSpanPermille = 1000;
-// The fused mixed step's decodes as flat items (ranges of the decodes' own
-// blocks laid end to end, one per ring-owning warp and KV head), about
-// kMixedFlatItemsPerSm per SM, instead of the list's runs.
-constexpr bool kMixedFlatDecode = true;
-constexpr int kMixedFlatItemsPerSm = 4;
 
 // Whether the library's own choice (partition_blocks == 0) takes the
 // length-balanced list.  Measured on GB300 (70B-GQA recipe, 1 to 64
@@ -851,12 +846,6 @@ namespace {
 struct MixedLayout {
   Fp8PrefillLayout pre;  // offsets from its v_off
   Plan dec;
-  // flat decode items (when Hkv fits the fused CTA's ring-owning warps):
-  // ranges per item, items aimed at, and their areas from dec_off --
-  // partials, log2-sum-exps, block prefix sums, the plan's info words
-  bool flat = false;
-  int flat_ranges = 0, flat_target = 0;
-  size_t flat_lse_off = 0, flat_pre_off = 0, flat_info_off = 0, flat_bytes = 0;
   size_t pre_bytes = 0, dec_off = 0, counter_off = 0, total = 0;
   // decode prefix groups: the prefix part's output and log2-sum-exp, each
   // decode's first own block, each group's prefix length
@@ -874,24 +863,9 @@ int mixed_layout(int num_prefill, int prefill_max_blocks, int num_decode, int q_
   if (st != PKV_OK) return st;
   if (!m->dec.list) return PKV_EUNSUPPORTED;  // more than 512 decode sequences
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  // The decodes as flat items: kMixedFlatItemsPerSm items per SM aimed at,
-  // each of R = (ring-owning warps / Hkv) ranges.  Measured on GB300 (the
-  // mixed step with its prefix group): see the fused mixed step's notes.
-  const int nwd = pkv::mixed_decode_warps(d_head);
-  if (kMixedFlatDecode && nwd > 0 && kv_heads <= nwd) {
-    m->flat = true;
-    m->flat_ranges = nwd / kv_heads;
-    m->flat_target = kMixedFlatItemsPerSm * sms;
-    const size_t slots = (size_t(num_decode) + size_t(m->flat_ranges) * m->flat_target) *
-                         size_t(kv_heads) * size_t(q_heads / kv_heads);
-    m->flat_lse_off = up(slots * size_t(d_head) * sizeof(float));
-    m->flat_pre_off = m->flat_lse_off + up(slots * sizeof(float));
-    m->flat_info_off = m->flat_pre_off + up(size_t(num_decode + 1) * sizeof(int32_t));
-    m->flat_bytes = m->flat_info_off + 256;
-  }
   m->pre_bytes = m->pre.total - m->pre.v_off;
   m->dec_off = up(m->pre_bytes);
-  m->counter_off = m->dec_off + up(std::max(m->dec.ws_bytes, m->flat_bytes));
+  m->counter_off = m->dec_off + up(m->dec.ws_bytes);
   m->total = m->counter_off + 256;
   if (num_groups > 0) {
     const size_t rows = size_t(num_decode) * size_t(q_heads);
@@ -1027,16 +1001,6 @@ int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, i
   da.list_min_run = kListMinRun;
   da.list_max_blocks = std::min(m.dec.list_max_blocks, decode_max_blocks);
   da.list_items = m.dec.list_items;
-  if (m.flat) {
-    da.flat = true;
-    da.part_o = reinterpret_cast<float*>(dws);
-    da.part_lse = reinterpret_cast<float*>(dws + m.flat_lse_off);
-    da.flat_pre = reinterpret_cast<int32_t*>(dws + m.flat_pre_off);
-    da.flat_info = reinterpret_cast<int32_t*>(dws + m.flat_info_off);
-    da.flat_ranges = m.flat_ranges;
-    da.flat_target = m.flat_target;
-    da.flat_max_blocks = std::min(m.dec.list_max_blocks, decode_max_blocks);
-  }
   pkv::PrefillArgs qa;  // the prefix groups' pass over the decode queries
   CUtensorMap tqd;
   if (num_groups > 0) {

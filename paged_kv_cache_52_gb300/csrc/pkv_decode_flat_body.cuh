@@ -31,10 +31,7 @@ struct DecodeFlatParams {
   int max_blocks;    // blocks attended per sequence at most
   int total_warps;   // warps of the launch
   int min_pages;     // blocks per group at least (the last busy group may take fewer)
-  long long chunk = 0;  // > 0: the blocks per range, given
-  // non-null: the blocks per range, written on the device by the launch's
-  // plan (the fused mixed step); takes precedence over chunk
-  const int32_t* chunk_dev = nullptr;
+  long long chunk = 0;  // > 0: the blocks per range, given (the fused mixed step)
 };
 
 // Groups of a launch: its warps in groups of Hkv (the rest idle).

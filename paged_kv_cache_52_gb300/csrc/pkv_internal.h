@@ -119,12 +119,6 @@ struct DecodeArgs {
   int32_t* flat_pre = nullptr;
   int flat_ctas = 0, flat_max_blocks = 0;
   bool fp8 = false;  // flat split over FP8 (e4m3) pools, out_scale = v_scale
-  // the fused mixed step's flat decode items: flat_ranges ranges (of
-  // flat_ranges x Hkv ring-owning warps) per item, about flat_target items;
-  // flat_info ([4] int32, written by the plan kernel): items, blocks per
-  // range, ranges per item, blocks in all
-  int32_t* flat_info = nullptr;
-  int flat_ranges = 0, flat_target = 0;
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
@@ -169,8 +163,6 @@ int decode_flat_max_seqs();
 cudaError_t launch_paged_decode_flat(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                      const CUtensorMap* tmap_v, cudaStream_t stream);
 cudaError_t launch_paged_decode_flat_merge(const DecodeArgs& a, cudaStream_t stream);
-// ring-owning decode warps of a fused mixed-step CTA (mixed_step.cu)
-int mixed_decode_warps(int d_head);
 unsigned read_decode_flat_error(bool clear);
 
 // ---- paged_decode_fp8.cu (e4m3 pools, d_head 128)
