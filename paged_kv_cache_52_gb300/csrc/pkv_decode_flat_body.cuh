@@ -1,6 +1,5 @@
-// The per-warp body of the flat split of the paged decode, shared by the
-// flat decode kernel (paged_decode_flat.cu) and the fused mixed-step kernel
-// (mixed_step.cu): one warp streams the pages [f0, f1) of the blocks of all
+// The per-warp body of the flat split of the paged decode (used by the flat
+// decode kernel, paged_decode_flat.cu): one warp streams the pages [f0, f1) of the blocks of all
 // sequences laid end to end (sequence s owns offsets pre[s] + b, b < n_s, its
 // own blocks after any shared prefix) for one KV head, through its ring of
 // page copies, across the sequence boundaries inside the range; it writes a
@@ -31,7 +30,7 @@ struct DecodeFlatParams {
   int max_blocks;    // blocks attended per sequence at most
   int total_warps;   // warps of the launch
   int min_pages;     // blocks per group at least (the last busy group may take fewer)
-  long long chunk = 0;  // > 0: the blocks per range, given (the fused mixed step)
+  long long chunk = 0;  // > 0: the blocks per range, given (else from the others)
 };
 
 // Groups of a launch: its warps in groups of Hkv (the rest idle).
