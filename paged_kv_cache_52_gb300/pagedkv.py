@@ -827,7 +827,8 @@ def paged_decode_attention_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
                                          ) -> torch.Tensor:
     """Decode for sequences whose first ``prefix_blocks`` pages are shared:
     the prefix is attended once for all sequences (tensor cores), the private
-    pages by the split-K decode, and the two merged by log-sum-exp."""
+    pages by the library's split (uniform or flat), and the two merged by
+    log-sum-exp."""
     _check_cache(k_cache, v_cache)
     _need(q.is_cuda and q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(),
           "q must be a contiguous [S, Hq, d] bf16 CUDA tensor")
