@@ -244,12 +244,8 @@ PKV_API int pkv_paged_decode_attention_ex(const void* q, int num_seqs, int q_hea
  * pkv_paged_decode_step -- one decode step: pkv_kv_append of each
  * sequence's new token, then pkv_paged_decode_attention, with the same
  * results (cache rows bit for bit, outputs bit for bit) and the append's time
- * hidden: the decode's CTAs start beside the append.  On the uniform split
- * only the loads of a sequence's last page -- the one holding the appended
- * token -- wait for it; on the flat split the warp that holds that page
- * writes the appended rows (from k_new / v_new) into its copy of the page in
- * shared memory once it has landed, and the decode waits for the append
- * only before it completes.
+ * hidden: the decode's CTAs start beside the append and only the loads of a
+ * sequence's last page -- the one holding the appended token -- wait for it.
  * One new token per sequence: row s of k_new / v_new and slot_mapping[s]
  * belong to sequence s, and slot_mapping[s] must be -1 or the slot of its
  * position context_lens[s] - 1 (the usual decode step: the cache is updated,
