@@ -55,11 +55,9 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   constexpr int kStages = F::kStages;
   constexpr int kThreads = NW * 32;
   constexpr unsigned kFull = 0xffffffffu;
-  // in the decode step the grid before is the step's append, whose rows the
-  // warps take from the step's inputs instead (and wait for only at the
-  // end); otherwise every input may be the previous grid's output
-  const bool step = fp.step_k != nullptr;
-  if (!step) griddep_wait();
+  // with wait_late only the loads of a sequence's last page wait for the
+  // grid before (the step's append); otherwise every input may be its output
+  if (!p.wait_late) griddep_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,10 +139,7 @@ paged_decode_flat_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const long long f1 = g >= groups ? f0 : (f0 + c < total ? f0 + c : total);
   // (a warp with no range returns at once: no CTA-wide barrier follows)
 
-  flat_range<D, G, FP8>(tmap_k, tmap_v, p, fp, pre, S, f0, f1, g, hw, ring, bars);
-  // the step's grid completes only after the append: whatever waits for it
-  // sees the cache rows appended
-  if (step && blockIdx.x == 0 && threadIdx.x == 0) griddep_wait();
+  flat_range<D, G, FP8>(tmap_k, tmap_v, p, pre, S, f0, f1, g, hw, ring, bars);
 }
 
 // The merge of the flat split: row (sequence s, head hq) of KV head h =
@@ -322,12 +317,6 @@ static bool flat_params(const DecodeArgs& a, DecodeParams& prm, DecodeFlatParams
   fp.max_blocks = a.flat_max_blocks;
   fp.total_warps = a.flat_ctas * decode_flat_warps(a.d_head, a.fp8);
   fp.min_pages = kFlatMinPages;
-  if (a.step_slots && a.step_k && a.step_v && !a.fp8) {
-    fp.step_k = static_cast<const __nv_bfloat16*>(a.step_k);
-    fp.step_v = static_cast<const __nv_bfloat16*>(a.step_v);
-    fp.step_k_stride = a.step_k_stride;
-    fp.step_v_stride = a.step_v_stride;
-  }
   return true;
 }
 

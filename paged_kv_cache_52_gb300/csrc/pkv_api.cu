@@ -682,9 +682,7 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
                      int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                      float scale, void* out, bool out_bf16, void* workspace, size_t ws_bytes,
                      int partition_blocks, pkv_stream_t stream, int list_ctas = 0,
-                     const int64_t* step_slots = nullptr, const void* step_k = nullptr,
-                     int64_t step_k_stride = 0, const void* step_v = nullptr,
-                     int64_t step_v_stride = 0) {
+                     const int64_t* step_slots = nullptr) {
   int st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   Plan plan;
@@ -753,10 +751,6 @@ int decode_bf16_pool(const void* q, int num_seqs, int q_heads, const void* k_cac
     if (plan.list) return PKV_EUNSUPPORTED;
     a.wait_late = true;
     a.step_slots = step_slots;
-    a.step_k = step_k;
-    a.step_v = step_v;
-    a.step_k_stride = step_k_stride;
-    a.step_v_stride = step_v_stride;
   }
   cudaError_t e = plan.flat
                       ? pkv::launch_paged_decode_flat(a, &tk, &tv, static_cast<cudaStream_t>(stream))
@@ -818,8 +812,7 @@ int pkv_paged_decode_step(const void* q, int num_seqs, int q_heads, const void* 
   if (e != cudaSuccess) return PKV_ECUDA;
   return decode_bf16_pool(q, num_seqs, q_heads, k_cache, v_cache, cache, block_tables,
                           max_blocks_per_seq, context_lens, max_context_len, scale, out, false,
-                          workspace, ws_bytes, 0, stream, 0, slot_mapping, k_new, k_tok_stride,
-                          v_new, v_tok_stride);
+                          workspace, ws_bytes, 0, stream, 0, slot_mapping);
 }
 
 size_t pkv_decode_limited_workspace_bytes(int num_seqs, int q_heads, int kv_heads, int d_head,

@@ -31,21 +31,7 @@ struct DecodeFlatParams {
   int total_warps;   // warps of the launch
   int min_pages;     // blocks per group at least (the last busy group may take fewer)
   long long chunk = 0;  // > 0: the blocks per range, given (else from the others)
-  // The decode step: the appended token of sequence s (its K and V rows of
-  // every KV head, token strides in elements) is written into the tile of
-  // its last page in shared memory once the page has landed, when the
-  // step's slot for s is that position; the append's own kernel then runs
-  // beside this one with nothing to wait for (null: not a step).
-  const __nv_bfloat16* step_k = nullptr;
-  const __nv_bfloat16* step_v = nullptr;
-  long long step_k_stride = 0, step_v_stride = 0;
 };
-
-// Generic shared-memory writes before later async-proxy (TMA) writes to the
-// same memory.
-__device__ __forceinline__ void flat_fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Groups of a launch: its warps in groups of Hkv (the rest idle).
 __device__ __forceinline__ long long flat_groups(long long warps, int kv_heads) {
@@ -105,9 +91,9 @@ struct FlatPage {
 // its bounded wait ran out, with PKV_DEVERR_WAIT_TIMEOUT raised).
 template <int D, int G, bool FP8>
 __device__ __forceinline__ void flat_range(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                           const DecodeParams& p, const DecodeFlatParams& fp,
-                                           const int32_t* pre, int S, long long f0, long long f1,
-                                           long long g, int hw, uint32_t ring, uint32_t bars) {
+                                           const DecodeParams& p, const int32_t* pre, int S,
+                                           long long f0, long long f1, long long g, int hw,
+                                           uint32_t ring, uint32_t bars) {
   using Pg = FlatPage<D, FP8>;
   constexpr int kStages = Pg::kStages;
   using Acc = std::conditional_t<FP8, F8Acc<G>, DecAcc<D, G>>;
@@ -174,8 +160,16 @@ __device__ __forceinline__ void flat_range(const CUtensorMap& tmap_k, const CUte
     info(j, id, s, blk);
     if (lane == 0) {
       const int h = hw;
-      (void)s;
-      (void)blk;
+      // (the decode step has no shared prefix: blocks count from 0)
+      if (p.wait_late && blk == pre[s + 1] - pre[s] - 1) {
+        griddep_wait();  // the step's append is complete and its rows visible
+        if (p.step_slots && h == 0) {
+          const int len = __ldg(p.context_lens + s);
+          const long long slot = p.step_slots[s];
+          const long long want = (long long)id * kBlockTokens + (len - 1) % kBlockTokens;
+          if (slot != -1 && slot != want) atomicOr(&g_decode_error, kErrBadSlot);
+        }
+      }
       const int st = j % kStages;
       const uint32_t bar = bars + st * 8;
       const uint32_t kdst = ring + st * Pg::kStageBytes;
@@ -249,11 +243,11 @@ __device__ __forceinline__ void flat_range(const CUtensorMap& tmap_k, const CUte
   bool failed = false;
   int i = 0;
   while (i < cnt) {
-    int id0, seq0, blk0, id1 = 0;
+    int id0, seq0, blk0;
     info(i, id0, seq0, blk0);
     bool two = false;
     if (i + 1 < cnt) {
-      int seq1, blk1;
+      int id1, seq1, blk1;
       info(i + 1, id1, seq1, blk1);
       two = seq1 == seq0;
     }
@@ -309,40 +303,6 @@ __device__ __forceinline__ void flat_range(const CUtensorMap& tmap_k, const CUte
     if (!__all_sync(kFull, landed)) {
       failed = true;
       break;
-    }
-    if (fp.step_k) {
-      // the decode step: the sequence's last page takes the appended token's
-      // rows (head hw) from the step's inputs, in the tile's swizzled layout
-      const int last = blk0 + (two ? 1 : 0);
-      if (last == cur_end - 1) {
-        const int j = i + (two ? 1 : 0);
-        const int id = two ? id1 : id0;
-        const int len = __ldg(p.context_lens + cur_seq);
-        const int r = (len - 1) & (kBlockTokens - 1);
-        const long long slot = p.step_slots ? p.step_slots[cur_seq] : -1;
-        const long long want = (long long)id * kBlockTokens + r;
-        if (slot == want) {
-          constexpr int CH = D / 8;  // 16-byte chunks of a row
-          if (lane < 2 * CH) {
-            const bool isv = lane >= CH;
-            const int c = isv ? lane - CH : lane;
-            const __nv_bfloat16* src =
-                (isv ? fp.step_v + size_t(cur_seq) * fp.step_v_stride
-                     : fp.step_k + size_t(cur_seq) * fp.step_k_stride) +
-                size_t(hw) * D + c * 8;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-            const uint32_t tile = ring + (j % kStages) * Pg::kStageBytes + (isv ? Pg::kTileBytes : 0);
-            const uint32_t dst = tile + (c >> 3) * Pg::kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                         "r"(v.z), "r"(v.w)
-                         : "memory");
-          }
-          flat_fence_proxy_async_smem();  // before the next copy into this stage
-        } else if (slot != -1 && hw == 0 && lane == 0) {
-          atomicOr(&g_decode_error, kErrBadSlot);  // the append writes another slot
-        }
-        __syncwarp();
-      }
     }
     if constexpr (FP8) {
       if (two)

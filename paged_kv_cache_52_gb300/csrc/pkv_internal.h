@@ -119,12 +119,6 @@ struct DecodeArgs {
   int32_t* flat_pre = nullptr;
   int flat_ctas = 0, flat_max_blocks = 0;
   bool fp8 = false;  // flat split over FP8 (e4m3) pools, out_scale = v_scale
-  // the decode step on the flat split: the appended rows ([num_seqs] tokens
-  // of Hkv x d bf16, strides in elements), written into each sequence's
-  // last page as it lands (with step_slots)
-  const void* step_k = nullptr;
-  const void* step_v = nullptr;
-  long long step_k_stride = 0, step_v_stride = 0;
 };
 
 // Multi-query decode (speculative verification): q_len query tokens per
