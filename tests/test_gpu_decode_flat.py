@@ -171,3 +171,31 @@ def test_decode_step_on_the_flat_split(pk, num_seqs):
     assert torch.equal(sep, fused)
     assert_attention_close(fused.cpu().numpy(), ref, f"decode step on the flat split, {num_seqs}")
     assert pk.get_device_error(clear=True) == 0
+
+def test_decode_step_on_the_flat_split_skips_and_flags(pk):
+    # 20 sequences on the flat split: one appends nothing (slot -1: it
+    # attends the cache as is), one of length 1 (its last page is its first),
+    # one whose slot lies in a block no sequence reads (flagged; the decode
+    # attends the cache as is there too) -- equal to append-then-decode
+    lens = [1200, 3000, 1, 700, 4096] + [500 + 97 * i for i in range(15)]
+    w = _to_dev(wl.make_decode_workload(wl.GQA_70B, lens_override=lens))
+    S = len(lens)
+    assert pk.decode_plan_uses_flat(S, 64, 8, 128, max(lens), 0)
+    slots = w.slot_mapping.clone()
+    slots[1] = -1
+    used = set(w.block_tables.flatten().tolist())
+    spare = next(b for b in range(w.k_cache.shape[0]) if b not in used)
+    slots[3] = spare * 16 + 5
+    kc1, vc1 = w.k_cache.clone(), w.v_cache.clone()
+    pk.kv_append(w.k_new, w.v_new, slots, kc1, vc1)
+    sep = pk.paged_decode_attention(w.q, kc1, vc1, w.block_tables, w.context_lens, w.scale,
+                                    max_context_len=max(lens))
+    torch.cuda.synchronize()
+    pk.get_device_error(clear=True)
+    kc2, vc2 = w.k_cache.clone(), w.v_cache.clone()
+    fused = pk.paged_decode_step(w.q, w.k_new, w.v_new, slots, kc2, vc2, w.block_tables,
+                                 w.context_lens, w.scale, max_context_len=max(lens))
+    torch.cuda.synchronize()
+    assert pk.get_device_error(clear=True) == 0x1          # sequence 3's slot is elsewhere
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    assert torch.equal(sep, fused)
