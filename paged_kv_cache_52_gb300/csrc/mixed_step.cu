@@ -81,7 +81,8 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v16,
                         const __grid_constant__ CUtensorMap tmap_v,
-                        const __grid_constant__ CUtensorMap tmap_qd, const PrefillParams pp,
+                        const __grid_constant__ CUtensorMap tmap_qd,
+                        const __grid_constant__ CUtensorMap tmap_o, const PrefillParams pp,
                         const PrefillParams pq, const DecodeParams dp, const DecodeListParams lp,
                         const MixedParams mp) {
   griddep_wait();  // the plan, the f16 V pages and the appended rows are in place
@@ -124,7 +125,7 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const int r = int(at - (long long)grp * per_group);
       const int kvh = r / mp.prefix_tiles;
       const int tile = mp.prefix_tiles - 1 - (r - kvh * mp.prefix_tiles);
-      prefill_item<D, G, false>(tmap_qd, tmap_k, tmap_v, pq, smem, tmem, grp * pq.kv_heads + kvh,
+      prefill_item<D, G, false>(tmap_qd, tmap_k, tmap_v, tmap_qd, pq, smem, tmem, grp * pq.kv_heads + kvh,
                                 tile);
       fence_proxy_async_smem();
       __syncthreads();
@@ -137,7 +138,7 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (is_prefill) {
       int pair, tile;
       if (item_pair_tile(pp, before, mp.tiles_per_pair, pair, tile))
-        prefill_item<D, G, true>(tmap_q, tmap_k, tmap_v16, pp, smem, tmem, pair, tile);
+        prefill_item<D, G, true>(tmap_q, tmap_k, tmap_v16, tmap_o, pp, smem, tmem, pair, tile);
       else if (threadIdx.x == 0)
         atomicOr(&g_prefill_error, kErrBadQueryRange);
     } else {
@@ -165,7 +166,7 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
 }
 
 struct MixedLaunch {
-  const CUtensorMap *tmap_q, *tmap_k, *tmap_v16, *tmap_v, *tmap_qd;
+  const CUtensorMap *tmap_q, *tmap_k, *tmap_v16, *tmap_v, *tmap_qd, *tmap_o;
   const PrefillParams* pp;
   const PrefillParams* pq;
   const DecodeParams* dp;
@@ -182,7 +183,8 @@ static cudaError_t launch_mixed_t(const MixedLaunch& m, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   return launch_after_previous(paged_mixed_step_kernel<D, G>, dim3(unsigned(m.ctas)),
                                dim3(kPfThreads), S::kSmemBytes, stream, *m.tmap_q, *m.tmap_k,
-                               *m.tmap_v16, *m.tmap_v, *m.tmap_qd, *m.pp, *m.pq, *m.dp, *m.lp,
+                               *m.tmap_v16, *m.tmap_v, *m.tmap_qd, *m.tmap_o, *m.pp, *m.pq,
+                               *m.dp, *m.lp,
                                *m.mp);
 }
 
@@ -233,9 +235,11 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
                               int ctas, int prefill_span_permille, const CUtensorMap* tmap_q,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v16,
                               const CUtensorMap* tmap_v, cudaStream_t stream,
-                              const PrefillArgs* prefix, const CUtensorMap* tmap_qd) {
+                              const PrefillArgs* prefix, const CUtensorMap* tmap_qd,
+                              const CUtensorMap* tmap_o) {
   // prefill part: the f16 P V path over the f16 V scratch pages
   PrefillParams pp = prefill_params(pa);
+  pp.o_tma = tmap_o ? 1 : 0;
   constexpr int TPC = kPfQTiles * kPfRows;  // query rows per item
   const int group = pa.q_heads / pa.kv_heads;
   const int tokens_per_item = TPC / group;
@@ -297,8 +301,8 @@ cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* 
                                         counter);
   if (e != cudaSuccess) return e;
   // 2. the fused launch
-  MixedLaunch m{tmap_q, tmap_k, tmap_v16, tmap_v, prefix ? tmap_qd : tmap_q, &pp, &pq, &dp, &lp,
-                &mp, ctas};
+  MixedLaunch m{tmap_q, tmap_k, tmap_v16, tmap_v, prefix ? tmap_qd : tmap_q,
+                tmap_o ? tmap_o : tmap_q, &pp, &pq, &dp, &lp, &mp, ctas};
   if (pa.d_head == 128) e = launch_mixed_d<128>(m, group, stream);
   else if (pa.d_head == 64) e = launch_mixed_d<64>(m, group, stream);
   else e = cudaErrorInvalidValue;

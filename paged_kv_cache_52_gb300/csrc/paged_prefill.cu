@@ -69,7 +69,8 @@ template <int D, int G, bool F16PV, bool PERSIST>
 __global__ void __launch_bounds__(kPfThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+                     const __grid_constant__ CUtensorMap tmap_v,
+                     const __grid_constant__ CUtensorMap tmap_o, const PrefillParams p) {
   // inputs may have been written by the previous kernel in the stream; with
   // defer_wait the previous kernel wrote nothing this one reads and let it
   // start early, and the wait moves to the end
@@ -98,7 +99,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     int pair, tile;
     const long long idx = (long long)blockIdx.y * gridDim.x + blockIdx.x;
     if (item_pair_tile(p, idx, int(gridDim.y), pair, tile))
-      prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, pair, tile);
+      prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, tmap_o, p, smem, tmem, pair, tile);
     else if (threadIdx.x == 0)
       atomicOr(&g_prefill_error, kErrBadQueryRange);
   } else {
@@ -113,7 +114,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (stop) break;
       int pair, tile;
       if (item_pair_tile(p, item, p.tiles_per_pair, pair, tile))
-        prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, p, smem, tmem, pair, tile);
+        prefill_item<D, G, F16PV>(tmap_q, tmap_k, tmap_v, tmap_o, p, smem, tmem, pair, tile);
       else if (threadIdx.x == 0)
         atomicOr(&g_prefill_error, kErrBadQueryRange);
     }
@@ -131,7 +132,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
 template <int D, int G, bool F16PV>
 static cudaError_t launch_prefill_t(const PrefillParams& prm, int max_ctas,
                                     const CUtensorMap* tq, const CUtensorMap* tk,
-                                    const CUtensorMap* tv, cudaStream_t stream) {
+                                    const CUtensorMap* tv, const CUtensorMap* to,
+                                    cudaStream_t stream) {
   using L = PrefillSmem<D>;
   constexpr int TPT = kPfRows / G;
   static std::atomic<int> attr_grid[kAttrMaxDevices], attr_persist[kAttrMaxDevices];
@@ -156,25 +158,26 @@ static cudaError_t launch_prefill_t(const PrefillParams& prm, int max_ctas,
     if (e != cudaSuccess) return e;
     const int ctas = int(std::min<long long>(items, max_ctas));
     paged_prefill_kernel<D, G, F16PV, F16PV><<<ctas, kPfThreads, L::kSmemBytes, stream>>>(
-        *tq, *tk, *tv, q);
+        *tq, *tk, *tv, *to, q);
     return cudaGetLastError();
   }
   if (tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(prm.num_seqs * prm.kv_heads, tiles);
   return launch_after_previous(paged_prefill_kernel<D, G, F16PV, false>, grid, dim3(kPfThreads),
-                               L::kSmemBytes, stream, *tq, *tk, *tv, prm);
+                               L::kSmemBytes, stream, *tq, *tk, *tv, *to, prm);
 }
 
 template <int D, bool F16PV>
 static cudaError_t launch_prefill_d(const PrefillParams& prm, int max_ctas, int group,
                                     const CUtensorMap* tq, const CUtensorMap* tk,
-                                    const CUtensorMap* tv, cudaStream_t st) {
+                                    const CUtensorMap* tv, const CUtensorMap* to,
+                                    cudaStream_t st) {
   switch (group) {
-    case 1: return launch_prefill_t<D, 1, F16PV>(prm, max_ctas, tq, tk, tv, st);
-    case 2: return launch_prefill_t<D, 2, F16PV>(prm, max_ctas, tq, tk, tv, st);
-    case 4: return launch_prefill_t<D, 4, F16PV>(prm, max_ctas, tq, tk, tv, st);
-    case 8: return launch_prefill_t<D, 8, F16PV>(prm, max_ctas, tq, tk, tv, st);
-    case 16: return launch_prefill_t<D, 16, F16PV>(prm, max_ctas, tq, tk, tv, st);
+    case 1: return launch_prefill_t<D, 1, F16PV>(prm, max_ctas, tq, tk, tv, to, st);
+    case 2: return launch_prefill_t<D, 2, F16PV>(prm, max_ctas, tq, tk, tv, to, st);
+    case 4: return launch_prefill_t<D, 4, F16PV>(prm, max_ctas, tq, tk, tv, to, st);
+    case 8: return launch_prefill_t<D, 8, F16PV>(prm, max_ctas, tq, tk, tv, to, st);
+    case 16: return launch_prefill_t<D, 16, F16PV>(prm, max_ctas, tq, tk, tv, to, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -183,7 +186,7 @@ int prefill_rows_per_tile() { return kPfRows; }
 
 cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q,
                                  const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const CUtensorMap* tmap_o) {
   PrefillParams prm;
   prm.q_start = a.q_start;
   prm.block_tables = a.block_tables;
@@ -211,13 +214,16 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q
   prm.table_rows = a.table_rows;
   prm.allow_empty = a.allow_empty ? 1 : 0;
   prm.defer_wait = a.defer_wait ? 1 : 0;
+  // without an output map the kernel gets the query map as a stand-in it never uses
+  prm.o_tma = (tmap_o && !a.out_bf16) ? 1 : 0;
+  const CUtensorMap* to = tmap_o ? tmap_o : tmap_q;
   const int group = a.q_heads / a.kv_heads;
   if (a.f16_pv) {
-    if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
-    if (a.d_head == 64) return launch_prefill_d<64, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 128) return launch_prefill_d<128, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, to, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, true>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, to, stream);
   } else {
-    if (a.d_head == 128) return launch_prefill_d<128, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
-    if (a.d_head == 64) return launch_prefill_d<64, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, stream);
+    if (a.d_head == 128) return launch_prefill_d<128, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, to, stream);
+    if (a.d_head == 64) return launch_prefill_d<64, false>(prm, a.max_ctas, group, tmap_q, tmap_k, tmap_v, to, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -117,6 +117,25 @@ bool encode_query_map(CUtensorMap* map, const void* q, int total_q, int q_heads,
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view of float32 output rows [total_q][q_heads][d_head]: (d_head, q_heads,
+// total_q).  One box is 32 columns x `group` heads x 32/group tokens -- the 32
+// (token, head) rows one softmax warp of a prefill tile owns -- 128-byte
+// swizzled, written by TMA stores.
+bool encode_out_map(CUtensorMap* map, void* out, int total_q, int q_heads, int d_head,
+                    int group) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || group <= 0 || group > 32 || 32 % group) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(d_head), cuuint64_t(q_heads), cuuint64_t(total_q)};
+  const cuuint64_t row = cuuint64_t(d_head) * 4;
+  const cuuint64_t strides[2] = {row, row * cuuint64_t(q_heads)};
+  const cuuint32_t box[3] = {32, cuuint32_t(group), cuuint32_t(32 / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // FP8 pool [num_blocks][16][kv_heads][d_head] of e4m3 codes (1 byte): one box
 // is a whole 128-byte row x 16 tokens of one head, 128-byte swizzled.
 bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
@@ -453,7 +472,11 @@ int run_prefill(const void* q, const int32_t* q_start, int num_seqs, int total_q
   a.max_ctas = max_ctas;
   a.work_counter = work_counter;
   a.seq_order = seq_order;
-  cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream);
+  // float32 rows leave through TMA stores (bf16 rows through plain stores)
+  CUtensorMap to;
+  const bool tma_out =
+      !out_bf16 && encode_out_map(&to, out, total_q, q_heads, cache.d_head, group);
+  cudaError_t e = pkv::launch_paged_prefill(a, &tq, &tk, &tv, stream, tma_out ? &to : nullptr);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -1039,9 +1062,12 @@ int pkv_mixed_step_attention_ex(const void* q_prefill, const int32_t* q_start, i
     da.extra_o = pre_o;
     da.extra_lse = pre_lse;
   }
+  CUtensorMap to;  // the prefill rows leave through TMA stores
+  const bool tma_out = encode_out_map(&to, out_prefill, total_q, q_heads, cache.d_head, group);
   e = pkv::launch_mixed_step(pa, da, reinterpret_cast<int*>(ws + m.counter_off), sms,
                              prefill_span_permille, &tq, &tk, &tv16, &tv, cs,
-                             num_groups > 0 ? &qa : nullptr, num_groups > 0 ? &tqd : nullptr);
+                             num_groups > 0 ? &qa : nullptr, num_groups > 0 ? &tqd : nullptr,
+                             tma_out ? &to : nullptr);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -208,9 +208,12 @@ struct PrefillArgs {
 // Query rows (tokens x heads of a GQA group) per prefill tile.
 int prefill_rows_per_tile();
 
+// tmap_o (optional): the float32 output as d_head x q_heads x total_q, box
+// 32 columns x G heads x 32/G tokens, 128-byte swizzled (encode_out_map);
+// with it whole warps' rows are written by TMA stores
 cudaError_t launch_paged_prefill(const PrefillArgs& a, const CUtensorMap* tmap_q,
                                  const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const CUtensorMap* tmap_o = nullptr);
 unsigned read_prefill_error(bool clear);
 
 // ---- mixed_step.cu
@@ -222,13 +225,15 @@ unsigned read_prefill_error(bool clear);
 // list merge.  counter: one int of device memory.
 // prefix (optional): the decode prefix groups' pass (bf16 V from the pool,
 // queries through tmap_qd); da then carries seq_first_block and the extra
-// partial's buffers.
+// partial's buffers.  tmap_o (optional): the prefill output map of
+// launch_paged_prefill, for TMA stores of the prefill items' rows.
 cudaError_t launch_mixed_step(const PrefillArgs& pa, const DecodeArgs& da, int* counter,
                               int ctas, int prefill_span_permille, const CUtensorMap* tmap_q,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v16,
                               const CUtensorMap* tmap_v, cudaStream_t stream,
                               const PrefillArgs* prefix = nullptr,
-                              const CUtensorMap* tmap_qd = nullptr);
+                              const CUtensorMap* tmap_qd = nullptr,
+                              const CUtensorMap* tmap_o = nullptr);
 unsigned read_mixed_error(bool clear);
 
 }  // namespace pkv

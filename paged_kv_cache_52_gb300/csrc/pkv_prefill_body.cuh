@@ -74,6 +74,10 @@ struct PrefillParams {
   const int32_t* table_rows = nullptr;
   int allow_empty = 0;          // nonzero: a context of 0 is skipped without a flag
   int defer_wait = 0;           // nonzero: wait for the previous grid at the end, not the start
+  // nonzero: float32 rows of whole warps leave through the output tensor map
+  // (tmap_o: d_head x q_heads x total_q, box 32 columns x G heads x 32/G
+  // tokens, 128-byte swizzled), staged in the then idle K/V rings
+  int o_tma = 0;
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -98,9 +102,9 @@ __device__ __forceinline__ void pf_abort(volatile int* abort_flag) {
 // otherwise V is bf16 and P enters as bf16 hi + lo.
 template <int D, int G, bool F16PV>
 __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                                             const CUtensorMap& tmap_v, const PrefillParams& p,
-                                             uint8_t* smem, uint32_t tmem, int pair,
-                                             int cta_tile) {
+                                             const CUtensorMap& tmap_v, const CUtensorMap& tmap_o,
+                                             const PrefillParams& p, uint8_t* smem, uint32_t tmem,
+                                             int pair, int cta_tile) {
   using L = PrefillSmem<D>;
   constexpr int TPT = kPfRows / G;          // query tokens per Q tile
   constexpr int TPC = kPfQTiles * TPT;      // query tokens per CTA
@@ -715,6 +719,40 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
         uint4* orow_bf16 = reinterpret_cast<uint4*>(
             reinterpret_cast<__nv_bfloat16*>(p.out) + orow_idx * D);
         if (p.lse && valid_row) p.lse[orow_idx] = m_used + __log2f(lsum);
+        if (p.o_tma && !p.out_bf16 && __all_sync(0xffffffffu, valid_row)) {
+          // The warp's 32 rows (32/G tokens x the G heads) in 32-column boxes
+          // of 32 rows x 128 bytes, 128-byte swizzled, then one TMA store per
+          // box.  Tile 0 stages over K stages 0-1, free once S_1 of the last
+          // tile is done (before PV_0 of it); tile 1 over the next 128 rows'
+          // worth, free once its own last PV -- the CTA's last MMA -- is done.
+          const uint32_t stage = sbase + L::kKOff + uint32_t(wg) * (kPfRows * D * 4) +
+                                 uint32_t(warp & 3) * (32 * D * 4);
+          const uint32_t row_at = stage + uint32_t(lane) * 128;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + o_col + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              st_shared_f4(row_at + c * 4096 + ((uint32_t(i) ^ uint32_t(lane & 7)) << 4),
+                           o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                           o[4 * i + 3] * inv);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int tok0 = qs + t0 + wg * TPT + (warp & 3) * (32 / G);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tma_store_3d(&tmap_o, stage + c * 4096, c * 32, kvh * G, tok0);
+            bulk_commit_group();
+            // shared memory is read before the item ends (the next item's
+            // copies, or the next CTA, reuse it); the global writes finish
+            // on their own
+            bulk_wait_read_all();
+          }
+          __syncwarp();
+        } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -732,6 +770,7 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
               *reinterpret_cast<float4*>(orow + c * 32 + i) =
                   make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
           }
+        }
         }
       }
     }
