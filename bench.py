@@ -81,6 +81,10 @@ def parse_args():
     ap.add_argument("--append-tokens", type=int, default=262144,
                     help="tokens of the bulk append probe")
     ap.add_argument("--append-steps", type=int, default=20)
+    ap.add_argument("--only-prefill-lengths", action="store_true",
+                    help="run only the prefill over chunks of 512 tokens with 1K to 32K "
+                         "cached tokens before them (the rate against the length of a "
+                         "CTA's work; profiling runs)")
     return ap.parse_args()
 
 
@@ -636,6 +640,62 @@ def run_mixed(args, dev, pagedkv, E):
     }
 
 
+def run_prefill_lengths(dev, pagedkv, E, steps=20):
+    """The tensor-core prefill (workspace path: f16 P; plain entry point:
+    bf16 hi + lo P) of 64/8-head, d 128 causal chunks over growing cached
+    contexts: the mixed step's 8 chunks of 512 tokens, 8 chunks of 512 after
+    1K, 16K and 32K cached tokens, and 2 chunks of 4096 from an empty cache.
+    A CTA's work (two 128-row query tiles against every key they see) grows
+    with the context, so the rows separate the steady tile rate from the
+    per-CTA start and end."""
+    hq, hkv, d = 64, 8, 128
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    tflops_peak = float(peaks.get("bf16_tflops", 1900.0))
+    cases = (("mixed-step chunks", wl.mixed_prefill_priors(), [512] * 8),
+             ("8 x 512 after 1K", [1024] * 8, [512] * 8),
+             ("8 x 512 after 16K", [16384] * 8, [512] * 8),
+             ("8 x 512 after 32K", [32768] * 8, [512] * 8),
+             ("2 x 4096 from empty", [0, 0], [4096, 4096]))
+    rows = []
+    for name, priors, chunks in cases:
+        w = wl.make_chunked_workload(hq, hkv, d, priors, chunks, device=dev, gen_device=dev)
+        out = torch.empty(w.q_prefill.shape, dtype=torch.float32, device=dev)
+        ws = pagedkv.prefill_workspace(len(priors), w.prefill_tables.shape[1], hkv, d, dev)
+        flops = 4 * d * hq * prefill_flops([p + n for p, n in zip(priors, chunks)], chunks)
+        row = {"case": name, "gflop": round(flops / 1e9, 1)}
+        for path, wsp in (("workspace", ws), ("plain", None)):
+            def call():
+                pagedkv.paged_prefill_attention(w.q_prefill, w.q_start, w.k_cache, w.v_cache,
+                                                w.prefill_tables, w.prefill_lens, True, w.scale,
+                                                out=out, max_q_len=max(chunks), workspace=wsp)
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            a, b = E(enable_timing=True), E(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / steps
+            tf = flops / (ms * 1e-3) / 1e12
+            row[path] = {"ms": round(ms, 4), "TFLOPs": round(tf, 1),
+                         "frac": round(tf / tflops_peak, 3)}
+        rows.append(row)
+        del w, out, ws
+        torch.cuda.empty_cache()
+    err = pagedkv.get_device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x}: {pagedkv.describe_device_error(err)}")
+    return {"peak_tflops": tflops_peak, "peak_kind": "measured bf16 burst" if peaks else
+            "fallback", "launches_per_row": steps, "rows": rows}
+
+
 def run_fused(args, dev, pagedkv, E):
     """Only the fused continuous-batching step: append every new token, then
     pkv_mixed_step_attention_ex with the decodes' shared prefix as one
@@ -990,6 +1050,9 @@ def run_ours(args):
         return
     if args.only_fused:
         print(json.dumps({"fused_mixed_step": run_fused(args, dev, pagedkv, torch.cuda.Event)}))
+        return
+    if args.only_prefill_lengths:
+        print(json.dumps({"prefill_lengths": run_prefill_lengths(dev, pagedkv, torch.cuda.Event)}))
         return
     if args.only_append:
         peak, _ = measured_peak()

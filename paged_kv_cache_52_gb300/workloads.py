@@ -267,6 +267,25 @@ MIXED = MixedSpec("continuous-batching mixed step (8 prefill chunks x 512 + 248 
                   2048.0, 1.0, 32768, 1024, 64, 8, 128)
 
 
+def _mixed_lengths(spec: MixedSpec, P: int, D: int, lo: int, hi: int, cap: int, prefix: int):
+    """The priors of the P prefill sequences (prefix + U[lo, hi]) and the
+    lengths of the D decode sequences, drawn in that order from one seeded
+    generator."""
+    g = _cpu_gen(1000 * spec.config_id + 5)
+    priors = (prefix + torch.randint(lo, hi + 1, (P,), generator=g)).tolist()
+    priv = torch.empty(D, dtype=torch.float64).log_normal_(
+        math.log(spec.decode_median), spec.decode_sigma, generator=g)
+    priv = torch.clamp(torch.round(priv), 1, max(1, cap - prefix)).to(torch.int64)
+    return priors, (prefix + priv).tolist()
+
+
+def mixed_prefill_priors(spec: MixedSpec = MIXED) -> list:
+    """The tokens already cached for each prefill chunk of the mixed step
+    (the same draw as make_mixed_workload), without building its pools."""
+    return _mixed_lengths(spec, spec.num_prefill, spec.num_decode, *spec.prior_range,
+                          spec.max_len, spec.shared_prefix)[0]
+
+
 def make_mixed_workload(spec: MixedSpec = MIXED, device="cpu", gen_device=None,
                         num_prefill: Optional[int] = None, num_decode: Optional[int] = None,
                         chunk: Optional[int] = None, prior_range: Optional[tuple] = None,
@@ -285,12 +304,7 @@ def make_mixed_workload(spec: MixedSpec = MIXED, device="cpu", gen_device=None,
     prefix = spec.shared_prefix if shared_prefix is None else shared_prefix
     if prefix % BLOCK_SIZE:
         raise ValueError("the shared prefix must fill whole blocks")
-    g = _cpu_gen(base + 5)
-    priors = (prefix + torch.randint(lo, hi + 1, (P,), generator=g)).tolist()
-    priv = torch.empty(D, dtype=torch.float64).log_normal_(
-        math.log(spec.decode_median), spec.decode_sigma, generator=g)
-    priv = torch.clamp(torch.round(priv), 1, max(1, cap - prefix)).to(torch.int64)
-    dlens = (prefix + priv).tolist()
+    priors, dlens = _mixed_lengths(spec, P, D, lo, hi, cap, prefix)
     plens = [p + n for p in priors]
     all_lens = plens + dlens
     pblocks = prefix // BLOCK_SIZE
