@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "pkv_device.cuh"
 #include "pkv_tcgen05.cuh"
@@ -354,11 +355,29 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
         uint32_t pk[64];
         float tsum;
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-        // no max pass while the running max may stay: not on the first tile,
-        // nor where a row needs the causal mask
-        bool fast = __all_sync(0xffffffffu, j > 0 && !need_mask);
+        // No max pass while the running max may stay, on masked tiles too
+        // (the exponentials apply each row's mask).  The first tile seeds
+        // the running max from its first 32 keys and keeps it when the sum
+        // of the rounded weights allows, as any other tile does.
+        bool fast = __all_sync(0xffffffffu, j > 0);
+        bool seeded = false;
         for (;;) {
-          if (!fast) {
+          if (!fast && j == 0 && !seeded) {
+            // key 0 is visible to every row, so the seed is finite
+            float va[32];
+            tmem_ld32(lane_base + s_col, va);
+            tmem_wait_ld();
+            const bool neg = p.scale_log2 < 0.f;  // uniform over the CTA
+            float ex[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float a = neg ? -va[i] : va[i];
+              if (i <= limit) ex[i & 3] = fmaxf(ex[i & 3], a);
+            }
+            m_used = fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])) * fabsf(p.scale_log2);
+            seeded = true;
+            fast = true;
+          } else if (!fast) {
             float ex[8];
 #pragma unroll
             for (int a = 0; a < 8; ++a) ex[a] = -INFINITY;
@@ -455,15 +474,26 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
         continue;
       }
       // hi + lo P keeps fp32's exponent range, so a stale running max only
-      // has to keep the exponentials finite.  After the first tile, where no
-      // row needs the mask, the max pass is skipped: the exponentials are
-      // taken against m_used, 64 keys at a time, and a group is kept while
+      // has to keep the exponentials finite.  The max pass is skipped: the
+      // first tile seeds the running max from its first 32 keys (key 0 is
+      // visible to every row), and the exponentials are taken against m_used,
+      // 64 keys at a time with each row's causal mask, a group kept while
       // every row's sum over it stays <= 2^64 (every weight is at most that
       // sum).  A first group that fails leaves S intact for the two-pass path
       // below; a second group that fails after the first was stored raises
-      // the max from its own scores and rescales O, the row sum and the
-      // stored first group (hi + lo is exact in fp32) before recomputing.
-      if (__all_sync(0xffffffffu, j > 0 && !need_mask && p.scale_log2 > 0.f)) {
+      // the max from its own visible scores and rescales O, the row sum and
+      // the stored first group (hi + lo is exact in fp32) before recomputing.
+      if (j == 0 && p.scale_log2 > 0.f) {
+        float va[32];
+        tmem_ld32(lane_base + s_col, va);
+        tmem_wait_ld();
+        float ex[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i <= limit) ex[i & 3] = fmaxf(ex[i & 3], va[i]);
+        m_used = fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])) * p.scale_log2;
+      }
+      if (p.scale_log2 > 0.f) {  // uniform over the CTA
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
         bool two_pass = false;
         for (int g = 0; g < 2; ++g) {
@@ -475,21 +505,32 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
             uint32_t hi[32], lo[32];
             const uint64_t nm2 = f2_pack(-m_used, -m_used);
             uint64_t ls2[2] = {0ull, 0ull};
+            // arithmetic only: rows differ in need_mask
+            auto exps = [&](auto masked) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const int kk = 2 * u;
-              const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
-              const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
-              const float e0 = ex2(x0), e1 = ex2(x1);
-              const uint64_t e = f2_pack(e0, e1);
-              ls2[u & 1] = f2_add(ls2[u & 1], e);
-              hi[u] = pack_bf16x2(e0, e1);
-              float r0, r1;
-              f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0, r1);
-              lo[u] = pack_bf16x2(r0, r1);
-            }
+              for (int u = 0; u < 32; ++u) {
+                const int kk = 2 * u;
+                const float s0 = kk < 32 ? va[kk] : vb[kk - 32];
+                const float s1 = kk < 32 ? va[kk + 1] : vb[kk - 31];
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+                float e0 = ex2(x0), e1 = ex2(x1);
+                if constexpr (decltype(masked)::value) {
+                  const int key = key0 + 64 * g + kk;
+                  e0 = key <= limit ? e0 : 0.f;
+                  e1 = key + 1 <= limit ? e1 : 0.f;
+                }
+                const uint64_t e = f2_pack(e0, e1);
+                ls2[u & 1] = f2_add(ls2[u & 1], e);
+                hi[u] = pack_bf16x2(e0, e1);
+                float r0, r1;
+                f2_unpack(f2_sub(e, f2_pack(bf16_lo_to_f32(hi[u]), bf16_hi_to_f32(hi[u]))), r0,
+                          r1);
+                lo[u] = pack_bf16x2(r0, r1);
+              }
+            };
+            if (need_mask) exps(std::true_type{});
+            else exps(std::false_type{});
             float a0, a1, b0, b1;
             f2_unpack(ls2[0], a0, a1);
             f2_unpack(ls2[1], b0, b1);
@@ -505,12 +546,16 @@ __device__ __forceinline__ void prefill_item(const CUtensorMap& tmap_q, const CU
               two_pass = true;
               break;
             }
-            // the max rose within the second group: take it from its scores
+            // the max rose within the second group: take it from its visible scores
             float ex[8];
 #pragma unroll
             for (int a = 0; a < 8; ++a) ex[a] = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ex[i & 7] = max3f(ex[i & 7], va[i], vb[i]);
+            for (int i = 0; i < 32; ++i) {
+              const int key = key0 + 64 * g + i;
+              ex[i & 7] = max3f(ex[i & 7], key <= limit ? va[i] : -INFINITY,
+                                key + 32 <= limit ? vb[i] : -INFINITY);
+            }
             const float ext = fmaxf(fmaxf(fmaxf(ex[0], ex[1]), fmaxf(ex[2], ex[3])),
                                     fmaxf(fmaxf(ex[4], ex[5]), fmaxf(ex[6], ex[7])));
             const float m_new = fmaxf(m_used, ext * p.scale_log2);
