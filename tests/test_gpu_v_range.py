@@ -5,7 +5,7 @@ f16 rounds each weight p_j with a relative error of at most 2^-11, and the
 row sum adds the weights as rounded, so the output is a convex combination of
 V rows whose weights are off by at most 2^-11 relative: the error of an output
 element is at most 2^-11 * max_j |v_j - out| <= 2^-10 * max|V|.  The bound
-scales with V while the benchmark spec's 2e-3 is absolute, so these tests scale V
+scales with V while the parity tolerance's 2e-3 is absolute, so these tests scale V
 by 1, 8, 32 and 128 (exact powers of two in bf16), check the derived bound
 and the 1e-2 row-wise relative bound, and print the absolute error of each
 case (``pytest -s``) to record where it leaves 2e-3.  The plain prefill entry
