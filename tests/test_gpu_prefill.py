@@ -178,20 +178,35 @@ def test_non_causal_chunk_longer_than_context(pk):
     assert pk.get_device_error() == 0
 
 
-@pytest.mark.parametrize("key", [140, 197])
-def test_running_max_jump_inside_a_tile(pk, key):
-    # after the first 128-key tile the kernel takes the exponentials against
-    # the running max with no max pass and checks each 64-key group's sum; a
-    # key whose score jumps far above the max fails that check.  Key 140 sits
-    # in the first group of the second tile (recomputed with the max pass),
-    # key 197 in the second group, after the first group was stored (its P,
-    # O and the row sum are rescaled in place).  Both must match the oracle.
+@pytest.mark.parametrize("key", [40, 100, 140, 197])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_running_max_jump_inside_a_tile(pk, key, workspace):
+    # The kernel takes the exponentials against the running max with no max
+    # pass and checks the sums (each 64-key group's on the plain path, the
+    # tile's rounded sum on the workspace path); a key whose score jumps far
+    # above that max fails the check.  The first 128-key tile seeds the max
+    # from its first 32 keys: keys 40 and 100 lie beyond them in that tile,
+    # so its check fails and it takes the two-pass path.  Key 140 sits in the
+    # first group of the second tile (recomputed with the max pass), key 197
+    # in its second group, after the first group was stored (on the plain
+    # path its P, O and the row sum are rescaled in place).  All must match
+    # the oracle.
     w = wl.make_chunked_workload(64, 8, 128, [300], [64], config_id=21)
     rows = w.k_cache.view(-1, 8, 128)
     tables = w.prefill_tables.numpy()
     slot = int(tables[0, key // 16]) * 16 + key % 16
     rows[slot] = (rows[slot].float() * 100.0).to(torch.bfloat16)
     ref = PrefillStepOracle(w, [0]).output()
-    out, _, _ = run_prefill(pk, _to_dev(w), max_q_len=64)
+    wd = _to_dev(w)
+    if workspace:
+        kc, vc = wd.k_cache.clone(), wd.v_cache.clone()
+        pk.kv_append(wd.k_new, wd.v_new, wd.slot_mapping, kc, vc)
+        ws = pk.prefill_workspace(1, wd.prefill_tables.shape[1], 8, 128, DEV)
+        out = pk.paged_prefill_attention(wd.q_prefill, wd.q_start, kc, vc, wd.prefill_tables,
+                                         wd.prefill_lens, True, wd.scale, max_q_len=64,
+                                         workspace=ws)
+        torch.cuda.synchronize()
+    else:
+        out, _, _ = run_prefill(pk, wd, max_q_len=64)
     assert_attention_close(out.cpu().numpy(), ref, f"max jump at key {key}")
     assert pk.get_device_error(clear=True) == 0
