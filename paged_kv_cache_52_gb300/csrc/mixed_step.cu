@@ -142,8 +142,11 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
       else if (threadIdx.x == 0)
         atomicOr(&g_prefill_error, kErrBadQueryRange);
     } else {
-      list_item<D, G, MixedDecodeWarps<D>::value>(tmap_k, tmap_v, dp, lp, smem, mp.seq_item_base,
-                                         int(pos - before));
+      // one page at a time: beside the prefill items' traffic these runs are
+      // bound by the bytes each warp keeps in flight, and refilling a stage
+      // as soon as its page is done keeps more in flight than pairs
+      list_item<D, G, MixedDecodeWarps<D>::value, false>(tmap_k, tmap_v, dp, lp, smem,
+                                                          mp.seq_item_base, int(pos - before));
       __syncthreads();  // every warp has left the run's merge
       // the run's barriers are retired: this memory holds prefill tiles next
       if (warp < MixedDecodeWarps<D>::value && lane == 0)

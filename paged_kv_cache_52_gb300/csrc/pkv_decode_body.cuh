@@ -228,7 +228,10 @@ __device__ __forceinline__ void bf16_pages(DecAcc<D, G>& A,
 // the run's keys below `len`.  final_out: the run is the sequence's whole
 // context and writes the output; otherwise it writes its normalised partial
 // output and log2-sum-exp at partial row pbase + head * pstride.
-template <int D, int G, int NW>
+// PAIR: a warp takes its pages two at a time (two independent MMA and
+// exponential chains; its ring is refilled after both), else one at a time
+// (each stage refilled as soon as its page is done: more bytes in flight).
+template <int D, int G, int NW, bool PAIR = true>
 __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                            const DecodeParams& p, uint8_t* smem, int seq, int kvh,
                                            int b0, int nb_local, int len, bool final_out,
@@ -326,9 +329,9 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
   }
   bool failed = false;
   int i = 0;
-  // pages two at a time; an odd last page alone
-  for (; i < cnt; i += 2) {
-    const bool two = i + 1 < cnt;
+  // pages two at a time (PAIR) with an odd last page alone, or one at a time
+  for (; i < cnt;) {
+    const bool two = PAIR && i + 1 < cnt;
     bool landed = mbar_wait_bounded(bars + (i % kDecodeStages) * 8, (i / kDecodeStages) & 1);
     if (two && landed)
       landed = mbar_wait_bounded(bars + ((i + 1) % kDecodeStages) * 8,
@@ -350,6 +353,7 @@ __device__ __forceinline__ void decode_run(const CUtensorMap& tmap_k, const CUte
         ++issued;
       }
     }
+    i += two ? 2 : 1;
   }
 
   if (failed) {
@@ -571,7 +575,7 @@ __device__ void list_plan(const DecodeParams& p, const DecodeListParams& lp, int
 }
 
 // Run `item` of the list plan in `base` (every CTA holds the same plan).
-template <int D, int G, int NW>
+template <int D, int G, int NW, bool PAIR = true>
 __device__ __forceinline__ void list_item(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                           const DecodeParams& p, const DecodeListParams& lp,
                                           uint8_t* smem, const int32_t* base, int item) {
@@ -604,8 +608,8 @@ __device__ __forceinline__ void list_item(const CUtensorMap& tmap_k, const CUten
   const int b1 = first + int((long long)(run + 1) * ns / runs);
   // a sequence with a prefix partial always leaves its runs to the merge
   const bool final_out = runs == 1 && !has_extra(p, seq);
-  decode_run<D, G, NW>(tmap_k, tmap_v, p, smem, seq, kvh, b0, b1 - b0, len, final_out,
-                       size_t(item) * G, 1);
+  decode_run<D, G, NW, PAIR>(tmap_k, tmap_v, p, smem, seq, kvh, b0, b1 - b0, len, final_out,
+                             size_t(item) * G, 1);
 }
 
 }  // namespace pkv
