@@ -24,7 +24,9 @@
 //    V^T P^T has 16 dims per m-tile as M and the heads as N.  At G = 8 this
 //    contraction is 8 flop per KV byte, which would keep the fp32 pipe ~70%
 //    busy at HBM speed; on the tensor pipe it costs a few percent of its rate.
-//    A warp takes its pages two at a time (two independent chains).
+//    In partitions longer than 256 blocks a warp takes its pages two at a
+//    time (two independent chains); in shorter ones one at a time, each ring
+//    stage refilled as soon as its page is done.
 //  * online softmax in the log2 domain (scores pre-multiplied by
 //    scale * log2 e, MUFU ex2); a head's max and sum reduce over the 8 lanes
 //    of its column.  P^T enters the PV MMA as bf16 hi + bf16 lo (two MMAs,
@@ -46,7 +48,7 @@ namespace pkv {
 
 int decode_warps_per_cta() { return kDecodeWarps; }
 
-template <int D, int G>
+template <int D, int G, bool PAIR>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -74,8 +76,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int b0 = sp.first + part * p.partition_blocks;  // first block of this partition
   const int nb_local = min(sp.first + sp.count - b0, p.partition_blocks);
   const bool final_out = (nparts_s == 1) && !p.force_partials;
-  decode_run<D, G, kDecodeWarps>(tmap_k, tmap_v, p, smem, seq, kvh, b0, nb_local, sp.len,
-                                 final_out, row0 * p.num_parts + part, p.num_parts);
+  decode_run<D, G, kDecodeWarps, PAIR>(tmap_k, tmap_v, p, smem, seq, kvh, b0, nb_local, sp.len,
+                                       final_out, row0 * p.num_parts + part, p.num_parts);
 }
 
 // Length-balanced list decode: every CTA computes the same plan from the
@@ -249,21 +251,39 @@ __global__ void __launch_bounds__(256) paged_decode_merge4_kernel(const DecodePa
   }
 }
 
-template <int D, int G>
-static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
-                                   const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                   cudaStream_t stream, bool with_merge) {
+// Partitions longer than this take their pages in pairs (two MMA and
+// exponential chains per warp), shorter ones one at a time (each stage
+// refilled as soon as its page is done).  Same box, 70B-GQA recipe, decode
+// step, pairs / single: 8 sequences (90-block partitions) 39.7 / 38.5 us,
+// 12 (about 160) 48.0 / 44.6 us, 256 (384) within 0.4%; 128K contexts
+// (1024-block partitions) 318.5 / 328.6 us.
+constexpr int kSplitPairMinBlocks = 256;
+
+template <int D, int G, bool PAIR>
+static cudaError_t launch_split_t(const DecodeParams& prm, int num_seqs,
+                                  const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                  cudaStream_t stream) {
   using T = DecodeTile<D, kDecodeWarps>;
   static std::atomic<int> attr_done[kAttrMaxDevices];
   {
     const cudaError_t e =
-        set_smem_limit_once(paged_decode_split_kernel<D, G>, T::kSmemBytes, attr_done);
+        set_smem_limit_once(paged_decode_split_kernel<D, G, PAIR>, T::kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(num_seqs * prm.kv_heads, prm.num_parts);
-  cudaError_t e = launch_after_previous(paged_decode_split_kernel<D, G>, grid,
-                                        dim3(kDecodeWarps * 32), T::kSmemBytes, stream, *tmap_k,
-                                        *tmap_v, prm);
+  return launch_after_previous(paged_decode_split_kernel<D, G, PAIR>, grid,
+                               dim3(kDecodeWarps * 32), T::kSmemBytes, stream, *tmap_k, *tmap_v,
+                               prm);
+}
+
+template <int D, int G>
+static cudaError_t launch_decode_t(const DecodeParams& prm, int num_seqs,
+                                   const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                   cudaStream_t stream, bool with_merge) {
+  const cudaError_t e =
+      prm.partition_blocks > kSplitPairMinBlocks
+          ? launch_split_t<D, G, true>(prm, num_seqs, tmap_k, tmap_v, stream)
+          : launch_split_t<D, G, false>(prm, num_seqs, tmap_k, tmap_v, stream);
   if (e != cudaSuccess || !with_merge) return e;
   return launch_decode_merge(prm, num_seqs, D, stream);
 }
