@@ -197,8 +197,9 @@ constexpr int kListMinRun = 8;
 // The fused mixed step spreads its prefill items over this share (per mille)
 // of its work list; the rest holds decode runs only.  On GB300 the mixed
 // step (8 x 512-token chunks + 248 decodes) was fastest with the prefill
-// items spread over the whole list: 0.9005 ms at 1000, 0.9104 at 950,
-// 0.9134 at 900, 0.926 at 800, 0.971 at 500 (with its prefix group).
+// items spread over the whole list: 0.843 ms at 1000, 0.857 at 950, 0.868
+// at 900, 0.883 at 800, 0.935 at 500 (with its prefix group; the decode runs
+// taking their pages one at a time).
 constexpr int kMixedPrefillSpanPermille = 1000;
 
 // Whether the library's own choice (partition_blocks == 0) takes the
