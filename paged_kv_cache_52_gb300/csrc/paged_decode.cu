@@ -109,7 +109,11 @@ paged_decode_list_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      (warp * kDecodeStages + st) * 8);
       __syncthreads();
     }
-    list_item<D, G, kDecodeWarps>(tmap_k, tmap_v, p, lp, smem, base, item);
+    // one page at a time: the list's CTAs run at the bytes they keep in flight
+    // (capped decode of the 70B-GQA batch, GB/s at 32 / 64 / 96 / 152 / 304
+    // CTAs: 1493 / 2788 / 4161 / 5845 / 6020 against 1230 / 2271 / 3341 / 4670
+    // / 5858 with the pages in pairs)
+    list_item<D, G, kDecodeWarps, false>(tmap_k, tmap_v, p, lp, smem, base, item);
   }
 }
 
