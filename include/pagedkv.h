@@ -149,15 +149,17 @@ PKV_API int pkv_kv_append_checked(const void* k, int64_t k_tok_stride, const voi
  *                        to end; the ranges differ by at most one page, and
  *                        a warp's page copies run on across the pairs of its
  *                        range, so the copy pipeline fills once per warp;
- *   0                    the library's choice: the flat split for 128 to
- *                        1024 (sequence, KV head) pairs at d_head 128, where
- *                        it measured faster on GB300, else the uniform
+ *   0                    the library's choice: the flat split for 193 to
+ *                        1024 (sequence, KV head) pairs at d_head 128 (and
+ *                        for more pairs in 3 or more uniform partitions),
+ *                        where it measured faster on GB300, else the uniform
  *                        partitions (the balanced list did not beat them at
  *                        any batch size: a small batch's time is the
  *                        decode's fixed cost more than the balance of its
  *                        waves).
  * The FP8 decode takes the flat split like the bf16 decode (PKV_SPLIT_FLAT,
- * or the library's choice with the same rule) and treats the other values
+ * or the library's choice, from 128 pairs over FP8 pages; the workspace of
+ * the library's choice over bf16 pages covers it) and treats the other values
  * <= 0 as PKV_SPLIT_UNIFORM; the verification decode treats every value
  * <= 0 as PKV_SPLIT_UNIFORM; the shared-prefix decode takes the library's
  * choice for the sequences' own pages.

@@ -211,27 +211,35 @@ constexpr int kMixedPrefillSpanPermille = 1000;
 bool list_wins(long long /*pairs*/, long long /*slots*/) { return false; }
 
 // Whether the library's own choice takes the flat split (d_head 128): for
-// 128 to 1024 (sequence, KV head) pairs, and for more pairs when the uniform
-// split needs 3 or more partitions per pair, i.e. when the longest context
-// is several times the partition the pair count allows, as in a long-tailed
-// batch.  Measured on GB300 (decode call, us, uniform / flat): 70B-GQA
-// recipe, 8 sequences 36.2 / 39.2, 12 44.9 / 44.2, 16 60.5 / 56.2, 24 82.8 /
-// 81.9, 32 120-140 / 103.1, 48 160.0 / 146.4, 64 197.4 / 182.5, 96 276.9 /
-// 261.1, 128 353.4 / 351.4, 192 535.2 / 535.8, 256 (2 partitions) 696.1 /
-// 704.2; 7B-MHA (2048 pairs, 1 partition) 368.6 / 376.4; 128K contexts (32
-// pairs) 320.7 / 320.2; the mixed step's 248 decodes (1984 pairs, lognormal
-// contexts up to 32768 tokens, 6 partitions) 555.5 / 516.4.  With fewer
-// pairs a warp's few pages do not amortise its start and the pieces' merge;
-// with many pairs in few partitions the uniform grid's dynamic CTA
-// scheduling evens out the tail that equal static ranges leave.
-bool flat_wins(long long pairs, int d_head, long long uniform_parts) {
-  if (d_head != 128 || pairs < 128) return false;
+// 193 to 1024 (sequence, KV head) pairs over bf16 pages (128 to 1024 over
+// FP8 pages), and for more pairs when the uniform split needs 3 or more
+// partitions per pair, i.e. when the longest context is several times the
+// partition the pair count allows, as in a long-tailed batch.  Measured on
+// GB300 (decode call, us, uniform / flat): 70B-GQA recipe, 8 sequences 36.2
+// / 39.2, 12 44.9 / 44.2, 16 60.5 / 56.2, 24 82.8 / 81.9, 32 120-140 /
+// 103.1, 48 160.0 / 146.4, 64 197.4 / 182.5, 96 276.9 / 261.1, 128 353.4 /
+// 351.4, 192 535.2 / 535.8, 256 (2 partitions) 696.1 / 704.2; 7B-MHA (2048
+// pairs, 1 partition) 368.6 / 376.4; 128K contexts (32 pairs) 320.7 /
+// 320.2; the mixed step's 248 decodes (1984 pairs, lognormal contexts up to
+// 32768 tokens, 6 partitions) 555.5 / 516.4.  With the uniform split's short
+// partitions taking their pages one at a time (bf16): 12 sequences 41.6 /
+// 44.9, 16 53.4 / 57.3, 24 81.6 / 81.9, 32 113.5 / 105.1 -- so over bf16
+// pages the flat split starts above 24 sequences (192 pairs); the FP8 split
+// kernel keeps its pairs and FP8 pools keep the 128-pair start (16
+// sequences 42.5 / 39.1).  With fewer pairs a warp's few pages do not
+// amortise its start and the pieces' merge; with many pairs in few
+// partitions the uniform grid's dynamic CTA scheduling evens out the tail
+// that equal static ranges leave.
+constexpr long long kFlatMinPairsBf16 = 193;
+constexpr long long kFlatMinPairsFp8 = 128;
+bool flat_wins(long long pairs, int d_head, long long uniform_parts, bool fp8) {
+  if (d_head != 128 || pairs < (fp8 ? kFlatMinPairsFp8 : kFlatMinPairsBf16)) return false;
   return pairs <= 1024 || uniform_parts >= 3;
 }
 
 int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_context_len,
               int partition_blocks, Plan* plan, bool allow_list = false, int list_ctas = 0,
-              bool allow_flat = false) {
+              bool allow_flat = false, bool fp8 = false) {
   *plan = Plan();  // every field is this call's: a plan object may be reused
   if (num_seqs < 0 || q_heads <= 0 || kv_heads <= 0 || max_context_len < 0) return PKV_EINVAL;
   if (q_heads % kv_heads) return PKV_EUNSUPPORTED;
@@ -301,8 +309,12 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
   }
   const bool want_flat = list_ctas == 0 && (partition_blocks == PKV_SPLIT_FLAT ||
                                              (partition_blocks == 0 &&
-                                              flat_wins(pairs, d_head, parts)));
-  if (allow_flat && want_flat) {
+                                              flat_wins(pairs, d_head, parts, fp8)));
+  // the workspace of the library's choice over bf16 pages also serves the
+  // FP8 decode of the same sizes, which takes the flat split from fewer pairs
+  const bool size_flat =
+      want_flat || (list_ctas == 0 && partition_blocks == 0 && flat_wins(pairs, d_head, parts, true));
+  if (allow_flat && size_flat) {
     // partial slots for the larger of the bf16 and FP8 flat grids, so one
     // workspace serves both decodes of these sizes
     const long long warps = (long long)sms * std::max(pkv::decode_flat_warps(d_head, false),
@@ -316,16 +328,19 @@ int make_plan(int num_seqs, int q_heads, int kv_heads, int d_head, int max_conte
       // prefix sums
       const size_t slots = size_t(pairs + warps) * size_t(q_heads / kv_heads);
       auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-      plan->flat = true;
-      plan->flat_ctas = sms;
-      plan->flat_max_blocks = nblk_max;
-      plan->flat_lse_offset = up(slots * size_t(d_head) * sizeof(float));
-      plan->flat_pre_offset = plan->flat_lse_offset + up(slots * sizeof(float));
+      const size_t lse_off = up(slots * size_t(d_head) * sizeof(float));
+      const size_t pre_off = lse_off + up(slots * sizeof(float));
       // the workspace still covers the uniform split, which the FP8 and
       // verification decodes take with the same sizes
-      plan->ws_bytes = std::max(plan->ws_bytes,
-                                plan->flat_pre_offset + size_t(num_seqs + 1) * sizeof(int32_t));
-      return PKV_OK;
+      plan->ws_bytes = std::max(plan->ws_bytes, pre_off + size_t(num_seqs + 1) * sizeof(int32_t));
+      if (want_flat) {
+        plan->flat = true;
+        plan->flat_ctas = sms;
+        plan->flat_max_blocks = nblk_max;
+        plan->flat_lse_offset = lse_off;
+        plan->flat_pre_offset = pre_off;
+        return PKV_OK;
+      }
     }
   }
   if (partition_blocks == PKV_SPLIT_FLAT) partition_blocks = PKV_SPLIT_UNIFORM;
@@ -1115,7 +1130,8 @@ int decode_fp8_pool(const void* q, int num_seqs, int q_heads, const void* k_cach
   if (cache.d_head != 128) return PKV_EUNSUPPORTED;
   Plan plan;
   st = make_plan(num_seqs, q_heads, cache.kv_heads, cache.d_head, max_context_len,
-                 partition_blocks, &plan, /*allow_list=*/false, 0, /*allow_flat=*/true);
+                 partition_blocks, &plan, /*allow_list=*/false, 0, /*allow_flat=*/true,
+                 /*fp8=*/true);
   if (st != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;

@@ -277,16 +277,19 @@ def test_wait_probe_host_validation(pk):
 
 
 def test_decode_plan_flat_choice_and_workspace(pk):
-    # the library's split: flat for 128-1024 (sequence, KV head) pairs at
-    # d_head 128 and for more pairs in 3 or more uniform partitions; its
-    # workspace also covers the uniform split of the same sizes (which the
-    # FP8 and verification decodes take)
+    # the library's split over bf16 pages: flat for 193-1024 (sequence, KV
+    # head) pairs at d_head 128 and for more pairs in 3 or more uniform
+    # partitions; its workspace also covers the uniform split of the same
+    # sizes (which the FP8 and verification decodes take) and, from 128
+    # pairs, the flat split (which the FP8 decode takes from there)
     assert not pk.decode_plan_uses_flat(8, 64, 8, 128, 8192)
+    assert not pk.decode_plan_uses_flat(16, 64, 8, 128, 8192)
     assert pk.decode_plan_uses_flat(32, 64, 8, 128, 8192)
     assert not pk.decode_plan_uses_flat(256, 64, 8, 128, 8192)     # 2 partitions
     assert pk.decode_plan_uses_flat(248, 64, 8, 128, 32768)        # 6 partitions
     assert not pk.decode_plan_uses_flat(32, 64, 8, 64, 8192)       # d_head 64
-    for args in ((32, 64, 8, 128, 8192), (248, 64, 8, 128, 32768), (700, 16, 4, 128, 80)):
+    for args in ((16, 64, 8, 128, 8192), (32, 64, 8, 128, 8192), (248, 64, 8, 128, 32768),
+                 (700, 16, 4, 128, 80)):
         uni = pk.decode_plan(*args, partition_blocks=pk.SPLIT_UNIFORM)[2]
         flat = pk.decode_plan(*args, partition_blocks=pk.SPLIT_FLAT)[2]
         auto = pk.decode_plan(*args)[2]

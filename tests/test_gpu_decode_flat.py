@@ -142,14 +142,18 @@ def test_flat_workspace_is_required_and_sized(pk):
 
 
 def test_library_choice_takes_flat_for_mid_size_batches(pk):
-    # 128 to 1024 (sequence, KV head) pairs at d_head 128
-    for S, flat in ((8, False), (15, False), (16, True), (64, True), (128, True), (129, False),
-                    (256, False)):
+    # 193 to 1024 (sequence, KV head) pairs at d_head 128 over bf16 pages
+    for S, flat in ((8, False), (16, False), (24, False), (25, True), (64, True), (128, True),
+                    (129, False), (256, False)):
         assert pk.decode_plan_uses_flat(S, 64, 8, 128, 8192, 0) == flat, S
+    # the library's workspace at 16 sequences still covers the flat split,
+    # which the FP8 decode takes there
+    auto = pk.decode_plan(16, 64, 8, 128, 8192)[2]
+    assert auto >= pk.decode_plan(16, 64, 8, 128, 8192, pk.SPLIT_FLAT)[2]
     assert not pk.decode_plan_uses_flat(32, 64, 8, 64, 8192, 0)      # measured at d 128 only
 
 
-@pytest.mark.parametrize("num_seqs", [16, 48])
+@pytest.mark.parametrize("num_seqs", [32, 48])
 def test_decode_step_on_the_flat_split(pk, num_seqs):
     # the decode step with the library's choice (flat here): the append runs
     # beside the flat kernel, whose warps wait for it only before a
@@ -173,11 +177,11 @@ def test_decode_step_on_the_flat_split(pk, num_seqs):
     assert pk.get_device_error(clear=True) == 0
 
 def test_decode_step_on_the_flat_split_skips_and_flags(pk):
-    # 20 sequences on the flat split: one appends nothing (slot -1: it
+    # 30 sequences on the flat split: one appends nothing (slot -1: it
     # attends the cache as is), one of length 1 (its last page is its first),
     # one whose slot lies in a block no sequence reads (flagged; the decode
     # attends the cache as is there too) -- equal to append-then-decode
-    lens = [1200, 3000, 1, 700, 4096] + [500 + 97 * i for i in range(15)]
+    lens = [1200, 3000, 1, 700, 4096] + [500 + 97 * i for i in range(25)]
     w = _to_dev(wl.make_decode_workload(wl.GQA_70B, lens_override=lens))
     S = len(lens)
     assert pk.decode_plan_uses_flat(S, 64, 8, 128, max(lens), 0)

@@ -207,7 +207,7 @@ def test_prefix_groups_flat_suffix_match_oracle(pk):
 
 
 def test_prefix_group_mismatch_flat_suffix(pk):
-    w, gs, gp = _grouped_workload([8, 6, 9], [4, 3, 8], lead_free=0, tail_free=1, hq=64, hkv=8)
+    w, gs, gp = _grouped_workload([8, 6, 10], [4, 3, 8], lead_free=0, tail_free=1, hq=64, hkv=8)
     _assert_flat(pk, w)
     used = set(w.block_tables.flatten().tolist())
     spare = next(b for b in range(w.k_cache.shape[0]) if b not in used)
@@ -221,8 +221,8 @@ def test_prefix_group_mismatch_flat_suffix(pk):
 
 @pytest.mark.parametrize("prefix", [64, 1024])
 def test_shared_prefix_flat_suffix_matches_oracle(pk, prefix):
-    # 20 decodes of 64 / 8 heads, some ending right after the prefix
-    m = wl.make_mixed_workload(num_prefill=0, num_decode=20, shared_prefix=prefix,
+    # 28 decodes of 64 / 8 heads, some ending right after the prefix
+    m = wl.make_mixed_workload(num_prefill=0, num_decode=28, shared_prefix=prefix,
                                decode_cap=prefix + 400)
     w = _decodes(m)
     _assert_flat(pk, w)
@@ -234,7 +234,7 @@ def test_shared_prefix_flat_suffix_matches_oracle(pk, prefix):
 
 
 def test_short_member_flat_suffix(pk):
-    m = wl.make_mixed_workload(num_prefill=0, num_decode=20, shared_prefix=64, decode_cap=300)
+    m = wl.make_mixed_workload(num_prefill=0, num_decode=28, shared_prefix=64, decode_cap=300)
     w = _to_dev(_decodes(m))
     _assert_flat(pk, w)
     lens = w.context_lens.clone()
