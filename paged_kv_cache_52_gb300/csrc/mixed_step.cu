@@ -125,8 +125,10 @@ paged_mixed_step_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const int r = int(at - (long long)grp * per_group);
       const int kvh = r / mp.prefix_tiles;
       const int tile = mp.prefix_tiles - 1 - (r - kvh * mp.prefix_tiles);
-      prefill_item<D, G, false>(tmap_qd, tmap_k, tmap_v, tmap_qd, pq, smem, tmem, grp * pq.kv_heads + kvh,
-                                tile);
+      // (the prefix partials are written row by row: tmap_qd only fills the
+      // output map's place)
+      prefill_item<D, G, false>(tmap_qd, tmap_k, tmap_v, tmap_qd, pq, smem, tmem,
+                                grp * pq.kv_heads + kvh, tile);
       fence_proxy_async_smem();
       __syncthreads();
       continue;
@@ -187,8 +189,7 @@ static cudaError_t launch_mixed_t(const MixedLaunch& m, cudaStream_t stream) {
   return launch_after_previous(paged_mixed_step_kernel<D, G>, dim3(unsigned(m.ctas)),
                                dim3(kPfThreads), S::kSmemBytes, stream, *m.tmap_q, *m.tmap_k,
                                *m.tmap_v16, *m.tmap_v, *m.tmap_qd, *m.tmap_o, *m.pp, *m.pq,
-                               *m.dp, *m.lp,
-                               *m.mp);
+                               *m.dp, *m.lp, *m.mp);
 }
 
 template <int D>
