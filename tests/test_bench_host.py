@@ -33,3 +33,26 @@ def test_per_config_summary_carries_every_workload():
     # short enough to stay in the last 1500 characters of the line with the
     # CPU baseline before it
     assert len(json.dumps(out)) < 1100
+
+
+def test_prefill_flops_count_the_visible_keys():
+    # a causal chunk of n tokens after p cached ones: query i sees p + i + 1
+    # keys, so n p + n (n + 1) / 2 (query, key) pairs; brute force on small
+    # ragged cases, then the mixed step's 8 chunks x 64 heads x d 128 x 4
+    # flops per pair, the figure the bench's prefill rows divide by
+    import dataclasses
+
+    from paged_kv_cache_52_gb300 import workloads as wl
+    for priors, chunks in (([0], [1]), ([5, 0, 17], [3, 9, 1]), ([40], [64])):
+        brute = sum(p + i + 1 for p, n in zip(priors, chunks) for i in range(n))
+        assert bench.prefill_flops([p + n for p, n in zip(priors, chunks)], chunks) == brute
+    priors = wl.mixed_prefill_priors()
+    assert 4 * 128 * 64 * bench.prefill_flops([p + 512 for p in priors], [512] * 8) == \
+        518_533_414_912
+    # the priors are the mixed workload's own draw (a small spec of the same
+    # recipe, so the pools stay small)
+    spec = dataclasses.replace(wl.MIXED, num_prefill=3, num_decode=2, chunk=32,
+                               prior_range=(0, 64), shared_prefix=16, max_len=256,
+                               decode_median=64.0)
+    w = wl.make_mixed_workload(spec)
+    assert wl.mixed_prefill_priors(spec) == [L - 32 for L in w.meta["prefill_lens"]]
