@@ -881,7 +881,7 @@ def run_small_batch(dev, pagedkv, E, batches=(1, 2, 4, 8, 16, 32, 64), steps=200
     """Small-batch decode steps of the 70B-GQA layer shape: per-step time of
     eager calls vs replay of a CUDA graph captured for the batch's bucket
     (the decode step: append + decode, the library's split: uniform, or flat
-    for 16-128 sequences).  Batches of 1-4 sequences have short contexts
+    for 25-128 sequences).  Batches of 1-4 sequences have short contexts
     (`short_len` tokens each), where launch latency dominates; 8 to 64 draw
     their contexts from the 70B-GQA recipe."""
     from paged_kv_cache_52_gb300.graphs import DecodeGraphRunner
